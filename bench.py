@@ -1,0 +1,428 @@
+"""Benchmark of the GB300 sparse MoE expert layer.
+
+One step = one moe_layer_forward over one batch of synthetic tokens (router ->
+top-k -> permute -> grouped SwiGLU FFN -> combine), inputs resident in HBM.
+Default workload: the LongCat-Flash-shaped decode layer (T=64 tokens, hidden
+6144, 512 SwiGLU experts of intermediate 2048 plus 256 zero-computation
+experts, softmax top-12), weights bf16 ~N(0, 0.02).
+
+Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle
+instead, on a bounded sample of the same workload.
+
+Multi-GPU: the layer does not shard across GPUs here (no exchange step is
+built), so --gpus N under torchrun runs N independent replicas; the timing
+barrier and the max-over-ranks reduction are the only cross-rank calls.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TABLE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="longcat")
+    ap.add_argument("--gemv-max-rows", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ distributed --
+def dist_setup(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v, world, device):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [s.strip() for s in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ peaks --
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_bandwidth_gbs"):
+            if key in d:
+                return float(d[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemv.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "sparse_expert_layer_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, workload, units):
+    """DRAM bytes per launch from the committed ncu table, scaled to `units`; None
+    when absent or taken on a different kernel source."""
+    try:
+        tab = json.load(open(PROFILE_TABLE))
+    except (OSError, ValueError):
+        return None
+    rec = tab.get(f"{kernel}:{workload}")
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec["dram_bytes_per_launch"] * units / max(rec.get("units", units), 1)
+
+
+# ------------------------------------------------------------- workloads --
+def describe(spec):
+    return (f"{spec['name']}: T={spec['T']} H={spec['hidden']} E={spec['n_routed']}"
+            f"+{spec['n_zero']}zero k={spec['top_k']} I={spec['inter']}"
+            + (f" shared I={spec['shared_inter']}" if spec["shared_inter"] else ""))
+
+
+def algorithmic_bytes(spec, counts):
+    """Bytes the layer must move: unique routed experts touched + shared expert +
+    router weights + bias + x in + out."""
+    H, I, Is, E = spec["hidden"], spec["inter"], spec["shared_inter"], synth.n_experts(spec)
+    U = int((counts[:spec["n_routed"]] > 0).sum())
+    per = 6 * H * I  # gate + up + down, bf16
+    b = U * per + 6 * H * Is + 4 * E * H + 2 * 2 * spec["T"] * H
+    if spec["bias_mode"] != "none":
+        b += 4 * E
+    return b, U
+
+
+# ------------------------------------------------------------ CPU oracle --
+def oracle_sample(spec, x, w_r, bias, wts_d, n_tok, target_s):
+    """Time the fp64 oracle on the first n_tok tokens (experts copied from HBM)."""
+    import oracle
+
+    oracle.build()
+    xs = x[:n_tok]
+    b = None if bias is None else bias.numpy()
+    logits = oracle.router_logits(spec, synth.bf16_bits(xs), w_r.numpy(), b)
+    ids, _, _, _ = oracle.select(spec, logits, b)
+    need = sorted(set(int(e) for e in ids.reshape(-1) if e < spec["n_routed"]))
+    E = spec["n_routed"]
+    g, u, dn = [None] * E, [None] * E, [None] * E
+    for e in need:
+        g[e] = synth.bf16_bits(wts_d["w_gate"][e])
+        u[e] = synth.bf16_bits(wts_d["w_up"][e])
+        dn[e] = synth.bf16_bits(wts_d["w_down"][e])
+    shared = None
+    if spec["shared_inter"]:
+        shared = tuple(synth.bf16_bits(wts_d[k]) for k in ("shared_gate", "shared_up",
+                                                           "shared_down"))
+    xb = synth.bf16_bits(xs)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.layer(spec, xb, w_r.numpy(), b, g, u, dn, shared)
+        reps += 1
+        if time.perf_counter() - t0 >= target_s:
+            break
+    dt = time.perf_counter() - t0
+    threads = min(n_tok, int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
+    return reps * n_tok / dt, threads, reps, dt, len(need)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    spec = synth.spec(args.config)
+    dev = torch.device("cuda:0")
+    x, w_r, bias, _ = synth.make_inputs(spec)
+    n_tok = min(spec["T"], os.cpu_count() or 1)
+    import oracle
+
+    oracle.build()
+    b = None if bias is None else bias.numpy()
+    logits = oracle.router_logits(spec, synth.bf16_bits(x[:n_tok]), w_r.numpy(), b)
+    ids, _, _, _ = oracle.select(spec, logits, b)
+    need = sorted(set(int(e) for e in ids.reshape(-1) if e < spec["n_routed"]))
+    wts = synth.draw_weights(spec, device=dev if torch.cuda.is_available() else "cpu",
+                             experts=need)
+    times = []
+    xb = synth.bf16_bits(x[:n_tok])
+    E = spec["n_routed"]
+    g, u, dn = [None] * E, [None] * E, [None] * E
+    for e in need:
+        g[e] = synth.bf16_bits(wts["w_gate"][e])
+        u[e] = synth.bf16_bits(wts["w_up"][e])
+        dn[e] = synth.bf16_bits(wts["w_down"][e])
+    shared = None
+    if spec["shared_inter"]:
+        shared = tuple(synth.bf16_bits(wts[k]) for k in ("shared_gate", "shared_up",
+                                                         "shared_down"))
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.layer(spec, xb, w_r.numpy(), b, g, u, dn, shared)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = args.steps * n_tok / total
+    cores = min(n_tok, int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
+    sample = f"{n_tok} of {spec['T']} tokens per step (all their picks, {len(need)} experts)"
+    line = {
+        "impl": "reference", "metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(spec), "tokens_per_step": n_tok},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ ours --
+def run_ours(args, rank, world, local):
+    import sparse_expert_layer_gb300 as moe
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    spec = synth.spec(args.config)
+    T, H = spec["T"], spec["hidden"]
+    x, w_r, bias, _ = synth.make_inputs(spec)
+    wts = synth.draw_weights(spec, device=dev)
+    cfg = moe.config_from_spec(spec, out_fp32=False, gemv_max_rows=args.gemv_max_rows)
+    x_d, w_r_d = x.to(dev), w_r.to(dev)
+    bias_d = None if bias is None else bias.to(dev)
+    layer = moe.MoeLayer(cfg, T, wts, w_r_d, bias_d, dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # routing once to count the unique experts this batch touches
+    E, k = synth.n_experts(spec), spec["top_k"]
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wgt = torch.empty((T, k), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    s2e = torch.empty(T * k, dtype=torch.int32, device=dev)
+    e2s = torch.empty(T * k, dtype=torch.int32, device=dev)
+    x_perm = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+    moe.moe_route(cfg, T, x_d, w_r_d, bias_d, ids, wgt, layer.ws)
+    moe.moe_permute(cfg, T, ids, x_d, counts, offsets, s2e, e2s, x_perm, None, layer.ws)
+    counts_h = counts.cpu().numpy()
+    alg_bytes, U = algorithmic_bytes(spec, counts_h)
+    del x_perm
+
+    for _ in range(args.warmup):
+        layer.forward(x_d, out)
+    torch.cuda.synchronize()
+    if moe.moe_check_device_status(layer.ws) != moe.MOE_OK:
+        raise RuntimeError("device status set during warm-up")
+
+    # timed region: K steps, per-kernel events recorded by the library
+    moe.timing_enable(True)
+    moe.timing_collect()
+    launches0 = moe.launch_counts()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            layer.forward(x_d, out)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(stop)
+    per_kernel = moe.timing_collect()
+    moe.timing_enable(False)
+    launches1 = moe.launch_counts()
+    gpu_launches = sum(launches1.values()) - sum(launches0.values())
+    if moe.moe_check_device_status(layer.ws) != moe.MOE_OK:
+        raise RuntimeError("device status set during the timed region")
+    ms = max_over_ranks(ms, world, dev)
+    ms_step = ms / args.steps
+    value = world * T * args.steps / (ms / 1e3)
+
+    # end to end: host buffers, H2D of x and D2H of out inside the timed region
+    x_h = x.pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_e = torch.empty_like(x_d)
+    for _ in range(2):
+        x_e.copy_(x_h, non_blocking=True)
+        layer.forward(x_e, out)
+        out_h.copy_(out, non_blocking=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_e.copy_(x_h, non_blocking=True)
+        layer.forward(x_e, out)
+        out_h.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e = {"value": world * T * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": x.numel() * 2, "d2h_bytes_per_step": out.numel() * 2}
+
+    # roofline of the dominant kernel
+    peak, peak_kind = hbm_peak()
+    dom = max(per_kernel, key=lambda kname: per_kernel[kname][0])
+    dom_ms, dom_n = per_kernel[dom]
+    I, Is = spec["inter"], spec["shared_inter"]
+    R_real = int(counts_h[:spec["n_routed"]].sum())
+    kbytes = {
+        "gemv_gate_up": U * 4 * H * I + 4 * H * Is + 2 * (R_real + (T if Is else 0)) * H,
+        "gemv_down": U * 2 * H * I + 2 * H * Is + 2 * (R_real * I + (T * Is if Is else 0)),
+    }
+    dom_bytes = kbytes.get(dom)
+    roof = None
+    if dom_bytes and dom_n:
+        achieved = dom_bytes / (dom_ms / dom_n / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
+                "traffic": traffic_for(dom, spec["name"], 1),
+                "algorithmic_bytes_per_launch": dom_bytes,
+                "avg_launch_ms": dom_ms / dom_n}
+    layer_gbs = alg_bytes / (ms_step / 1e3) / 1e9
+
+    line = {
+        "metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": describe(spec), "tokens": T, "unique_experts": U,
+                   "real_picks": R_real, "l2": "inputs larger than L2: "
+                   f"{alg_bytes / 1e9:.1f} GB of weights streamed per step, 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "layer_hbm": {"achieved_gbs": layer_gbs, "algorithmic_bytes": alg_bytes,
+                      "frac": layer_gbs / peak, "peak": peak, "peak_source": peak_kind},
+        "roofline": roof,
+        "kernels_ms_per_step": {kname: v[0] / args.steps for kname, v in per_kernel.items()
+                                if v[1]},
+        "e2e": e2e,
+        "gpu_launches": gpu_launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_tok = min(T, os.cpu_count() or 1)
+        v, cores, reps, dt, n_exp = oracle_sample(spec, x, w_r, bias, wts, n_tok,
+                                                  args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n_tok} of {T} tokens, full layer, {n_exp} experts, "
+                      f"{reps} repetitions in {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,530 @@
+// C ABI of the layer: argument checks, workspace layout, launch sequencing and
+// diagnostics.  No device memory is allocated here; every buffer comes from the
+// caller (tensors) or from the caller's workspace.
+#include <math.h>
+
+#include <atomic>
+#include <climits>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kMaxExperts = 4096;
+constexpr int kMaxTopK = 32;
+constexpr int kMaxGroups = 64;
+constexpr int kRouterTargetCtas = 304;  // router split-K sized for ~2 CTAs per SM
+constexpr int kMaxDevices = 64;
+
+// ------------------------------------------------------------ bookkeeping --
+std::atomic<long long> g_launches[MOE_K_COUNT];
+std::atomic<int> g_attr_done[kAttrSlots][kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
+
+struct TimedLaunch {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::mutex g_tmu;
+std::atomic<bool> g_timing{false};
+std::vector<TimedLaunch> g_records;
+std::vector<cudaEvent_t> g_event_pool;
+thread_local cudaEvent_t t_open_event = nullptr;
+thread_local cudaError_t t_launch_error = cudaSuccess;
+
+cudaEvent_t take_event() {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+int sm_count(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  int n = g_sm_count[dev].load();
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    g_sm_count[dev].store(n);
+  }
+  return n;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------- config checks --
+moe_status check_cfg(const moe_config* c, int32_t T) {
+  if (!c || T < 0) return MOE_ERR_INVALID_ARG;
+  if (c->hidden < 8 || c->hidden % 8) return MOE_ERR_INVALID_ARG;
+  if (c->n_routed < 0 || c->n_zero < 0) return MOE_ERR_INVALID_ARG;
+  const int E = c->n_routed + c->n_zero;
+  if (E < 1) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (c->n_routed > 0 && (c->inter < 8 || c->inter % 8)) return MOE_ERR_INVALID_ARG;
+  if (c->top_k < 1 || c->top_k > E) return MOE_ERR_INVALID_ARG;
+  if (c->top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (c->n_group < 1 || E % c->n_group) return MOE_ERR_INVALID_ARG;
+  if (c->n_group > kMaxGroups) return MOE_ERR_UNSUPPORTED;
+  if (c->n_group > 1) {
+    const int G = E / c->n_group;
+    if (c->per_group_k < 0) return MOE_ERR_INVALID_ARG;
+    if (c->per_group_k > 0) {
+      if (c->per_group_k > G || c->per_group_k * c->n_group != c->top_k) return MOE_ERR_INVALID_ARG;
+    } else {
+      if (c->topk_group < 1 || c->topk_group > c->n_group) return MOE_ERR_INVALID_ARG;
+      if (c->top_k > c->topk_group * G) return MOE_ERR_INVALID_ARG;
+    }
+  }
+  if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (!isfinite(c->routed_scale)) return MOE_ERR_INVALID_ARG;
+  if (c->bias_mode < MOE_BIAS_NONE || c->bias_mode > MOE_BIAS_SELECT) return MOE_ERR_INVALID_ARG;
+  if (c->shared_inter < 0 || c->shared_inter % 8) return MOE_ERR_INVALID_ARG;
+  if (c->wdtype != MOE_W_BF16 && c->wdtype != MOE_W8A8) return MOE_ERR_INVALID_ARG;
+  if (c->wdtype == MOE_W8A8) return MOE_ERR_UNSUPPORTED;  // int8 path not in this build yet
+  if (c->out_fp32 != 0 && c->out_fp32 != 1) return MOE_ERR_INVALID_ARG;
+  if ((long long)T * c->top_k > (1LL << 30) || T > (1 << 24)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int effective_gemv_max(const moe_config& c) {
+  // The tensor-core path is not part of this build yet: every task streams.
+  (void)c;
+  return INT_MAX;
+}
+
+// --------------------------------------------------------------- workspace --
+struct Layout {
+  size_t status, partial, ids, w, bc, counts, offsets, s2e, e2s;
+  size_t wl_gemv_tasks, wl_gemv_gu, wl_gemv_dn, wl_tc_tasks, wl_tc_gu, wl_tc_dn, wl_counts;
+  size_t x_perm, x_scale, h, y, h_s, y_s;
+  size_t total;
+  int splits, nblk, wl_cap;
+};
+
+Layout make_layout(const moe_config& c, int T) {
+  Layout L{};
+  const size_t E = (size_t)c.n_routed + c.n_zero;
+  const size_t R = (size_t)T * c.top_k;
+  const size_t H = c.hidden, I = c.inter, Is = c.shared_inter;
+  L.splits = router_splits(c, T, kRouterTargetCtas / 2);
+  L.nblk = (T + kPermTokens - 1) / kPermTokens;
+  L.wl_cap = c.n_routed + 4 + (int)((R + T) / kGemvMaxRows);
+  const size_t xb = c.wdtype == MOE_W8A8 ? 1 : 2;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  L.status = take(256);
+  L.partial = take((size_t)L.splits * T * E * 4);
+  L.ids = take(R * 4);
+  L.w = take(R * 4);
+  L.bc = take((size_t)L.nblk * E * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.s2e = take(R * 4);
+  L.e2s = take(R * 4);
+  L.wl_gemv_tasks = take((size_t)L.wl_cap * sizeof(FfnTask));
+  L.wl_gemv_gu = take((size_t)L.wl_cap * 4);
+  L.wl_gemv_dn = take((size_t)L.wl_cap * 4);
+  L.wl_tc_tasks = take((size_t)L.wl_cap * sizeof(FfnTask));
+  L.wl_tc_gu = take((size_t)L.wl_cap * 4);
+  L.wl_tc_dn = take((size_t)L.wl_cap * 4);
+  L.wl_counts = take(kWlCount * 4);
+  L.x_perm = take(R * H * xb);
+  L.x_scale = take(R * 4);
+  L.h = take(R * I * 2);
+  L.y = take(R * H * 4);
+  L.h_s = take((size_t)T * Is * 2);
+  L.y_s = take(Is > 0 ? (size_t)T * H * 4 : 0);
+  L.total = off;
+  return L;
+}
+
+template <class P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+WorkList worklist_view(void* ws, const Layout& L) {
+  WorkList wl;
+  wl.gemv_tasks = at<FfnTask>(ws, L.wl_gemv_tasks);
+  wl.gemv_start_gu = at<int32_t>(ws, L.wl_gemv_gu);
+  wl.gemv_start_dn = at<int32_t>(ws, L.wl_gemv_dn);
+  wl.tc_tasks = at<FfnTask>(ws, L.wl_tc_tasks);
+  wl.tc_start_gu = at<int32_t>(ws, L.wl_tc_gu);
+  wl.tc_start_dn = at<int32_t>(ws, L.wl_tc_dn);
+  wl.counts = at<int32_t>(ws, L.wl_counts);
+  wl.capacity = L.wl_cap;
+  return wl;
+}
+
+moe_status check_ws(const moe_config& c, int T, const void* ws, size_t ws_bytes, Layout* L) {
+  *L = make_layout(c, T);
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < L->total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return MOE_OK;
+}
+
+moe_status finish() {
+  const cudaError_t e = t_launch_error;
+  t_launch_error = cudaSuccess;
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+Launch make_launch(moe_stream_t stream, void* ws, const Layout& L) {
+  Launch ln;
+  ln.stream = reinterpret_cast<cudaStream_t>(stream);
+  ln.num_sms = sm_count(current_device());
+  ln.status = at<DevStatus>(ws, L.status);
+  return ln;
+}
+
+// ---------------------------------------------------------------- stages --
+void run_route(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
+               const void* x, const float* w_router, const float* bias, int32_t* ids, float* w) {
+  float* partial = at<float>(ws, L.partial);
+  launch_router(ln, c, T, x, w_router, partial, L.splits);
+  launch_topk(ln, c, T, partial, L.splits, bias, ids, w);
+}
+
+void run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
+                 const int32_t* ids, const void* x, int32_t* counts, int32_t* offsets, int32_t* s2e,
+                 int32_t* e2s, void* x_perm, float* x_scale) {
+  const int E = c.n_routed + c.n_zero;
+  int32_t* bc = at<int32_t>(ws, L.bc);
+  launch_perm_count(ln, T, c.top_k, E, ids, bc);
+  launch_perm_scan(ln, T, E, bc, counts, offsets);
+  launch_perm_scatter(ln, T, c.top_k, E, ids, bc, s2e, e2s);
+  launch_perm_gather(ln, c, T, ids, e2s, x, x_perm, x_scale);
+}
+
+// Grouped FFN over the sorted rows plus (optionally) the shared expert.
+void run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
+             const int32_t* offsets, const void* x_perm, const void* w_gate, const void* w_up,
+             const void* w_down, float* y_perm, const void* x, const void* sg, const void* su,
+             const void* sd, float* y_shared) {
+  const WorkList wl = worklist_view(ws, L);
+  const bool shared = c.shared_inter > 0 && sg != nullptr;
+  moe_config cw = c;
+  if (!shared) cw.shared_inter = 0;
+  launch_worklist(ln, cw, T, offsets, wl, effective_gemv_max(c));
+  uint16_t* h = at<uint16_t>(ws, L.h);
+  uint16_t* h_s = at<uint16_t>(ws, L.h_s);
+
+  GemvPass gu{};
+  gu.tasks = wl.gemv_tasks;
+  gu.item_start = wl.gemv_start_gu;
+  gu.counts = wl.counts;
+  gu.task_slot = kWlGemvTasks;
+  gu.item_slot = kWlGemvItemsGU;
+  gu.w0 = static_cast<const uint16_t*>(w_gate);
+  gu.w1 = static_cast<const uint16_t*>(w_up);
+  gu.act = static_cast<const uint16_t*>(x_perm);
+  gu.out_h = h;
+  gu.sw0 = static_cast<const uint16_t*>(sg);
+  gu.sw1 = static_cast<const uint16_t*>(su);
+  gu.sact = static_cast<const uint16_t*>(x);
+  gu.sout_h = h_s;
+  gu.K = gu.Ks = c.hidden;
+  gu.N = c.inter;
+  gu.Ns = c.shared_inter;
+  launch_gemv_gate_up(ln, gu);
+
+  GemvPass dn{};
+  dn.tasks = wl.gemv_tasks;
+  dn.item_start = wl.gemv_start_dn;
+  dn.counts = wl.counts;
+  dn.task_slot = kWlGemvTasks;
+  dn.item_slot = kWlGemvItemsDN;
+  dn.w0 = static_cast<const uint16_t*>(w_down);
+  dn.act = h;
+  dn.out_y = y_perm;
+  dn.sw0 = static_cast<const uint16_t*>(sd);
+  dn.sact = h_s;
+  dn.sout_y = y_shared;
+  dn.K = c.inter;
+  dn.Ks = c.shared_inter;
+  dn.N = dn.Ns = c.hidden;
+  launch_gemv_down(ln, dn);
+}
+
+}  // namespace
+
+void set_smem_attr_once(const void* func, int bytes, int slot) {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices || slot < 0 || slot >= kAttrSlots) {
+    cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return;
+  }
+  if (g_attr_done[slot][d].load(std::memory_order_acquire)) return;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+      cudaSuccess)
+    g_attr_done[slot][d].store(1, std::memory_order_release);
+}
+
+void launch_begin(const Launch& L, int kind) {
+  g_launches[kind].fetch_add(1, std::memory_order_relaxed);
+  t_open_event = nullptr;
+  if (g_timing.load(std::memory_order_relaxed)) {
+    t_open_event = take_event();
+    if (t_open_event) cudaEventRecord(t_open_event, L.stream);
+  }
+}
+
+void launch_end(const Launch& L, int kind) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess && t_launch_error == cudaSuccess) t_launch_error = e;
+  if (t_open_event) {
+    cudaEvent_t b = take_event();
+    if (b) {
+      cudaEventRecord(b, L.stream);
+      std::lock_guard<std::mutex> lk(g_tmu);
+      g_records.push_back({kind, t_open_event, b});
+    }
+    t_open_event = nullptr;
+  }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_ALIGNMENT: return "misaligned pointer";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_CHECK: return "device-side data check failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* moe_kernel_name(int32_t kind) {
+  static const char* names[MOE_K_COUNT] = {
+      "router", "topk", "perm_count", "perm_scan", "perm_scatter", "perm_gather", "worklist",
+      "gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down", "quant_h", "combine"};
+  return (kind >= 0 && kind < MOE_K_COUNT) ? names[kind] : "unknown";
+}
+
+moe_status moe_workspace_size(const moe_config* cfg, int32_t T, size_t* bytes) {
+  const moe_status s = check_cfg(cfg, T);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(*cfg, T).total;
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_config* cfg, int32_t T, const void* x, const float* w_router,
+                     const float* bias, int32_t* topk_ids, float* topk_w, void* ws,
+                     size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_cfg(cfg, T);
+  if (s != MOE_OK) return s;
+  Layout L;
+  if ((s = check_ws(*cfg, T, ws, ws_bytes, &L)) != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (cfg->bias_mode != MOE_BIAS_NONE && !bias) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(topk_ids, 16) || !aligned(topk_w, 16))
+    return MOE_ERR_ALIGNMENT;
+  const Launch ln = make_launch(stream, ws, L);
+  run_route(ln, *cfg, T, L, ws, x, w_router, bias, topk_ids, topk_w);
+  return finish();
+}
+
+moe_status moe_permute(const moe_config* cfg, int32_t T, const int32_t* topk_ids, const void* x,
+                       int32_t* counts, int32_t* offsets, int32_t* sorted_to_expanded,
+                       int32_t* expanded_to_sorted, void* x_perm, float* x_perm_scale, void* ws,
+                       size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_cfg(cfg, T);
+  if (s != MOE_OK) return s;
+  Layout L;
+  if ((s = check_ws(*cfg, T, ws, ws_bytes, &L)) != MOE_OK) return s;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_ids || !x || !sorted_to_expanded || !expanded_to_sorted || !x_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->wdtype == MOE_W8A8 && T > 0 && !x_perm_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(x_perm, 16) || !aligned(counts, 4) || !aligned(offsets, 4))
+    return MOE_ERR_ALIGNMENT;
+  const Launch ln = make_launch(stream, ws, L);
+  if (T == 0) {
+    const int E = cfg->n_routed + cfg->n_zero;
+    if (cudaMemsetAsync(counts, 0, E * 4, ln.stream) != cudaSuccess ||
+        cudaMemsetAsync(offsets, 0, (E + 1) * 4, ln.stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  run_permute(ln, *cfg, T, L, ws, topk_ids, x, counts, offsets, sorted_to_expanded,
+              expanded_to_sorted, x_perm, x_perm_scale);
+  return finish();
+}
+
+moe_status moe_grouped_ffn(const moe_config* cfg, int32_t T, const int32_t* offsets,
+                           const void* x_perm, const float* x_perm_scale, const void* w_gate,
+                           const void* w_up, const void* w_down, const float* s_gate,
+                           const float* s_up, const float* s_down, float* y_perm, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  (void)x_perm_scale;
+  (void)s_gate;
+  (void)s_up;
+  (void)s_down;
+  moe_status s = check_cfg(cfg, T);
+  if (s != MOE_OK) return s;
+  Layout L;
+  if ((s = check_ws(*cfg, T, ws, ws_bytes, &L)) != MOE_OK) return s;
+  if (T == 0 || cfg->n_routed == 0) return MOE_OK;
+  if (!offsets || !x_perm || !w_gate || !w_up || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x_perm, 16) || !aligned(w_gate, 16) || !aligned(w_up, 16) || !aligned(w_down, 16) ||
+      !aligned(y_perm, 16))
+    return MOE_ERR_ALIGNMENT;
+  const Launch ln = make_launch(stream, ws, L);
+  moe_config c = *cfg;
+  c.shared_inter = 0;
+  run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y_perm, nullptr, nullptr,
+          nullptr, nullptr, nullptr);
+  return finish();
+}
+
+moe_status moe_combine(const moe_config* cfg, int32_t T, const float* y_perm,
+                       const int32_t* expanded_to_sorted, const int32_t* topk_ids,
+                       const float* topk_w, const void* x, const float* shared_out, void* out,
+                       moe_stream_t stream) {
+  const moe_status s = check_cfg(cfg, T);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!expanded_to_sorted || !topk_ids || !topk_w || !x || !out) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_routed > 0 && !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y_perm, 16) || !aligned(x, 16) || !aligned(shared_out, 16) || !aligned(out, 16))
+    return MOE_ERR_ALIGNMENT;
+  Launch ln;
+  ln.stream = reinterpret_cast<cudaStream_t>(stream);
+  ln.num_sms = sm_count(current_device());
+  ln.status = nullptr;
+  launch_combine(ln, *cfg, T, y_perm, expanded_to_sorted, topk_ids, topk_w, x, shared_out, out);
+  return finish();
+}
+
+moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
+                             const float* w_router, const float* bias, const void* w_gate,
+                             const void* w_up, const void* w_down, const float* s_gate,
+                             const float* s_up, const float* s_down, const void* ws_gate,
+                             const void* ws_up, const void* ws_down, void* out, void* ws,
+                             size_t ws_bytes, moe_stream_t stream) {
+  (void)s_gate;
+  (void)s_up;
+  (void)s_down;
+  moe_status s = check_cfg(cfg, T);
+  if (s != MOE_OK) return s;
+  Layout L;
+  if ((s = check_ws(*cfg, T, ws, ws_bytes, &L)) != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !out) return MOE_ERR_INVALID_ARG;
+  if (cfg->bias_mode != MOE_BIAS_NONE && !bias) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_routed > 0 && (!w_gate || !w_up || !w_down)) return MOE_ERR_INVALID_ARG;
+  if (cfg->shared_inter > 0 && (!ws_gate || !ws_up || !ws_down)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(w_gate, 16) || !aligned(w_up, 16) ||
+      !aligned(w_down, 16) || !aligned(ws_gate, 16) || !aligned(ws_up, 16) ||
+      !aligned(ws_down, 16) || !aligned(out, 16))
+    return MOE_ERR_ALIGNMENT;
+  const Launch ln = make_launch(stream, ws, L);
+  const moe_config& c = *cfg;
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* w = at<float>(ws, L.w);
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* s2e = at<int32_t>(ws, L.s2e);
+  int32_t* e2s = at<int32_t>(ws, L.e2s);
+  void* x_perm = at<void>(ws, L.x_perm);
+  float* x_scale = at<float>(ws, L.x_scale);
+  float* y = at<float>(ws, L.y);
+  float* y_s = c.shared_inter > 0 ? at<float>(ws, L.y_s) : nullptr;
+  run_route(ln, c, T, L, ws, x, w_router, bias, ids, w);
+  run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale);
+  if (c.n_routed > 0 || c.shared_inter > 0)
+    run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y, x, ws_gate, ws_up, ws_down,
+            y_s);
+  launch_combine(ln, c, T, y, e2s, ids, w, x, y_s, out);
+  return finish();
+}
+
+moe_status moe_check_device_status(void* ws, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return MOE_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DevStatus h{};
+  if (cudaMemcpyAsync(&h, ws, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h.bits == 0u) return MOE_OK;
+  if (cudaMemsetAsync(ws, 0, sizeof h, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  return (h.bits & kStTimeout) ? MOE_ERR_DEVICE_TIMEOUT : MOE_ERR_DEVICE_CHECK;
+}
+
+moe_status moe_timing_enable(int32_t enable) {
+  g_timing.store(enable != 0);
+  return MOE_OK;
+}
+
+moe_status moe_timing_collect(float* ms, int32_t* launches, int32_t n) {
+  if (!ms || !launches || n < MOE_K_COUNT) return MOE_ERR_INVALID_ARG;
+  std::vector<TimedLaunch> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_tmu);
+    recs.swap(g_records);
+  }
+  for (int i = 0; i < n; ++i) {
+    ms[i] = 0.f;
+    launches[i] = 0;
+  }
+  moe_status s = MOE_OK;
+  for (const TimedLaunch& r : recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      s = MOE_ERR_CUDA;
+    ms[r.kind] += t;
+    launches[r.kind] += 1;
+  }
+  std::lock_guard<std::mutex> lk(g_tmu);
+  for (const TimedLaunch& r : recs) {
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  return s;
+}
+
+moe_status moe_launch_counts(int64_t* launches, int32_t n) {
+  if (!launches || n < MOE_K_COUNT) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < MOE_K_COUNT; ++i) launches[i] = g_launches[i].load();
+  for (int i = MOE_K_COUNT; i < n; ++i) launches[i] = 0;
+  return MOE_OK;
+}
+
+}  // extern "C"

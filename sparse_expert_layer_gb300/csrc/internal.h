@@ -1,0 +1,115 @@
+// Host-side interface between the C ABI (abi.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+struct DevStatus;
+
+// One unit of grouped-FFN work: a contiguous run of sorted rows of one expert.
+// expert >= 0 indexes the routed weight stacks; expert == -1 is the shared
+// expert (its rows index the token matrix directly).
+struct FfnTask {
+  int32_t expert;
+  int32_t row0;
+  int32_t nrows;
+  int32_t pad;
+};
+
+// Slots of the device work-list counter array.
+enum {
+  kWlGemvTasks = 0,
+  kWlGemvItemsGU,
+  kWlGemvItemsDN,
+  kWlTcTasks,
+  kWlTcTilesGU,
+  kWlTcTilesDN,
+  kWlCount
+};
+
+struct WorkList {
+  FfnTask* gemv_tasks;
+  int32_t* gemv_start_gu;  // first item of each task, gate/up pass
+  int32_t* gemv_start_dn;  // first item of each task, down pass
+  FfnTask* tc_tasks;
+  int32_t* tc_start_gu;
+  int32_t* tc_start_dn;
+  int32_t* counts;  // kWlCount ints
+  int32_t capacity; // max tasks of each kind
+};
+
+// Geometry of the streaming (GEMV) path.
+constexpr int kGemvMaxRows = 8;    // activation rows one GEMV task carries
+constexpr int kGemvChGU = 8;       // output channels per gate/up item
+constexpr int kGemvChDN = 16;      // output channels per down item
+// Geometry of the tensor-core path (swap-AB: weights are M, tokens are N).
+constexpr int kTcM = 128;          // weight rows per tile
+constexpr int kTcMaxN = 128;       // token rows per task
+constexpr int kDefaultGemvMaxRows = 8;
+
+struct Launch {
+  cudaStream_t stream;
+  int num_sms;
+  DevStatus* status;
+};
+
+// Router + top-k (route.cu)
+int router_splits(const moe_config& c, int T, int num_sms);
+void launch_router(const Launch& L, const moe_config& c, int T, const void* x, const float* w_r,
+                   float* partial, int splits);
+void launch_topk(const Launch& L, const moe_config& c, int T, const float* partial, int splits,
+                 const float* bias, int32_t* ids, float* w);
+
+// Permutation (permute.cu)
+constexpr int kPermTokens = 256;  // tokens per permutation block
+void launch_perm_count(const Launch& L, int T, int k, int E, const int32_t* ids, int32_t* bc);
+void launch_perm_scan(const Launch& L, int T, int E, int32_t* bc, int32_t* counts,
+                      int32_t* offsets);
+void launch_perm_scatter(const Launch& L, int T, int k, int E, const int32_t* ids,
+                         const int32_t* bc, int32_t* s2e, int32_t* e2s);
+void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32_t* ids,
+                        const int32_t* e2s, const void* x, void* x_perm, float* x_perm_scale);
+void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
+                     const WorkList& wl, int gemv_max_rows);
+
+// Grouped FFN, streaming path (gemv.cu)
+struct GemvPass {
+  const FfnTask* tasks;
+  const int32_t* item_start;
+  const int32_t* counts;  // work-list counters
+  int task_slot, item_slot;
+  const uint16_t* w0;     // gate (gate/up pass) or down weights, routed stack [E, N, K]
+  const uint16_t* w1;     // up weights (gate/up pass), else nullptr
+  const uint16_t* act;    // routed activation rows [*, K]
+  uint16_t* out_h;        // gate/up pass: bf16 [*, N]
+  float* out_y;           // down pass: fp32 [*, N]
+  const uint16_t* sw0;    // shared expert counterparts (may be nullptr)
+  const uint16_t* sw1;
+  const uint16_t* sact;
+  uint16_t* sout_h;
+  float* sout_y;
+  int K, Ks;              // reduction length, routed / shared
+  int N, Ns;              // output channels, routed / shared
+};
+void launch_gemv_gate_up(const Launch& L, const GemvPass& p);
+void launch_gemv_down(const Launch& L, const GemvPass& p);
+
+// Combine (combine.cu)
+void launch_combine(const Launch& L, const moe_config& c, int T, const float* y_perm,
+                    const int32_t* e2s, const int32_t* ids, const float* w, const void* x,
+                    const float* shared_out, void* out);
+
+// Raise a kernel's dynamic shared-memory limit once per device (abi.cu).
+enum { kAttrTopk = 0, kAttrPermScatter, kAttrGemvGU, kAttrGemvDN, kAttrTcGU, kAttrTcDN, kAttrSlots };
+void set_smem_attr_once(const void* func, int bytes, int slot);
+
+// Per-launch bookkeeping (abi.cu): call before/after each kernel launch.
+void launch_begin(const Launch& L, int kind);
+void launch_end(const Launch& L, int kind);
+
+}  // namespace moe

@@ -1,0 +1,355 @@
+// Stable re-sort of the token picks by expert (InitialRouting in the DeepSeek-V3/R1
+// on Ascend article, section "2. MOE 算子优化"), the row gather, and the grouped-FFN
+// work list.
+//
+//  count   : one CTA per block of 256 tokens counts its picks per expert (smem
+//            atomics) -> block_counts[b][e].
+//  scan    : one CTA turns block counts into counts[e], offsets[e] and the first
+//            sorted position of block b within expert e.
+//  scatter : one CTA per token block; a [expert][token] bitmap in smem gives each
+//            pick its rank among the block's earlier tokens of the same expert,
+//            so the order inside an expert is by token (stable).
+//  gather  : one warp per pick copies the token row to its sorted position with
+//            128-bit loads/stores (W8A8: quantises the row on the way).
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kPermThreads = 256;
+constexpr int kWords = kPermTokens / 32;
+
+__global__ void __launch_bounds__(kPermThreads)
+    perm_count_kernel(const int32_t* ids, int32_t* bc, int T, int k, int E, DevStatus* st) {
+  extern __shared__ int32_t cnt[];
+  const int b = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += kPermThreads) cnt[e] = 0;
+  __syncthreads();
+  const int r0 = b * kPermTokens * k, r1 = min(T, (b + 1) * kPermTokens) * k;
+  for (int r = r0 + threadIdx.x; r < r1; r += kPermThreads) {
+    const int e = ids[r];
+    if ((unsigned)e >= (unsigned)E) {
+      raise_status(st, kStBadId, MOE_K_PERM_COUNT);
+      continue;
+    }
+    atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kPermThreads) bc[(size_t)b * E + e] = cnt[e];
+}
+
+__global__ void __launch_bounds__(1024)
+    perm_scan_kernel(int32_t* bc, int32_t* counts, int32_t* offsets, int nblk, int E) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t carry;
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  // per expert: exclusive prefix over blocks (in place) and the total
+  for (int e = tid; e < E; e += 1024) {
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+      const int v = bc[(size_t)b * E + e];
+      bc[(size_t)b * E + e] = run;
+      run += v;
+    }
+    counts[e] = run;
+  }
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  // exclusive scan of counts -> offsets, 1024 experts per round
+  for (int base = 0; base < E; base += 1024) {
+    const int e = base + tid;
+    const int v = e < E ? counts[e] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_tot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += n;
+      }
+      warp_tot[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - v;
+    if (e < E) offsets[e] = excl;
+    __syncthreads();
+    if (tid == 1023) carry = excl + v;
+    __syncthreads();
+  }
+  if (tid == 0) offsets[E] = carry;
+  __syncthreads();
+  for (int e = tid; e < E; e += 1024) {
+    const int off = offsets[e];
+    for (int b = 0; b < nblk; ++b) bc[(size_t)b * E + e] += off;
+  }
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+    perm_scatter_kernel(const int32_t* ids, const int32_t* base, int32_t* s2e, int32_t* e2s, int T,
+                        int k, int E) {
+  extern __shared__ uint32_t bm[];  // [E][kWords]
+  const int b = blockIdx.x;
+  for (int i = threadIdx.x; i < E * kWords; i += kPermThreads) bm[i] = 0u;
+  __syncthreads();
+  const int t0 = b * kPermTokens;
+  const int r0 = t0 * k, r1 = min(T, t0 + kPermTokens) * k;
+  for (int r = r0 + threadIdx.x; r < r1; r += kPermThreads) {
+    const int e = ids[r];
+    if ((unsigned)e >= (unsigned)E) continue;
+    const int tl = r / k - t0;
+    atomicOr(&bm[e * kWords + tl / 32], 1u << (tl % 32));
+  }
+  __syncthreads();
+  for (int r = r0 + threadIdx.x; r < r1; r += kPermThreads) {
+    const int e = ids[r];
+    if ((unsigned)e >= (unsigned)E) {
+      e2s[r] = -1;
+      continue;
+    }
+    const int tl = r / k - t0;
+    int rank = 0;
+    for (int w = 0; w < tl / 32; ++w) rank += __popc(bm[e * kWords + w]);
+    rank += __popc(bm[e * kWords + tl / 32] & ((1u << (tl % 32)) - 1u));
+    const int p = base[(size_t)b * E + e] + rank;
+    s2e[p] = r;
+    e2s[r] = p;
+  }
+}
+
+struct GatherArgs {
+  const int32_t* ids;
+  const int32_t* e2s;
+  const uint16_t* x;
+  void* x_perm;
+  float* scale;
+  int R, k, H, E_r, w8a8;
+};
+
+__global__ void __launch_bounds__(256) perm_gather_kernel(GatherArgs a) {
+  const int lane = threadIdx.x % 32;
+  const int r = blockIdx.x * 8 + threadIdx.x / 32;
+  if (r >= a.R) return;
+  const int e = a.ids[r];
+  if ((unsigned)e >= (unsigned)a.E_r) return;  // zero-computation expert or bad id
+  const int p = a.e2s[r];
+  if (p < 0) return;
+  const int t = r / a.k;
+  const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H);
+  const int nv = a.H / 8;
+  if (!a.w8a8) {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.x_perm) + (size_t)p * a.H);
+    for (int i = lane; i < nv; i += 32) dst[i] = __ldg(src + i);
+    return;
+  }
+  // W8A8: symmetric per-row int8, scale = amax / 127, round half to even.
+  float amax = 0.f;
+  for (int i = lane; i < nv; i += 32) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
+  }
+  amax = warp_max(amax);
+  const float s = amax / 127.0f;
+  if (lane == 0) a.scale[p] = s;
+  uint2* dst = reinterpret_cast<uint2*>(static_cast<int8_t*>(a.x_perm) + (size_t)p * a.H);
+  for (int i = lane; i < nv; i += 32) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t q[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float f = (j & 1) ? bf16hi(w[j / 2]) : bf16lo(w[j / 2]);
+      int qi = 0;
+      if (amax > 0.f) qi = (int)fminf(127.f, fmaxf(-127.f, rintf(f / s)));
+      q[j / 4] |= (uint32_t)(qi & 0xff) << (8 * (j % 4));
+    }
+    dst[i] = make_uint2(q[0], q[1]);
+  }
+}
+
+// Work list of the grouped FFN.  Units are the routed experts in index order,
+// then the shared expert.  A unit with n rows becomes GEMV tasks of <= 8 rows
+// when n <= gemv_max, else tensor-core tasks of <= 128 rows.
+struct WlArgs {
+  const int32_t* offsets;
+  WorkList wl;
+  int E_r, T, has_shared, gemv_max;
+  int items_gu, items_gu_shared, items_dn;        // GEMV items per task
+  int tiles_gu, tiles_gu_shared, tiles_dn;        // tensor-core tiles per task
+  DevStatus* status;
+};
+
+__device__ int block_exclusive_scan(int v, int* tot, int* sh) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (int)(blockDim.x / 32) ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    sh[lane] = w;
+  }
+  __syncthreads();
+  const int excl = (warp > 0 ? sh[warp - 1] : 0) + incl - v;
+  *tot = sh[blockDim.x / 32 - 1];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
+  __shared__ int sh[32];
+  int carry[6] = {0, 0, 0, 0, 0, 0};
+  const int units = a.E_r + (a.has_shared ? 1 : 0);
+  for (int base = 0; base < units; base += blockDim.x) {
+    const int u = base + threadIdx.x;
+    int n = 0, row0 = 0, shared = 0;
+    if (u < a.E_r) {
+      row0 = a.offsets[u];
+      n = a.offsets[u + 1] - row0;
+    } else if (u < units) {
+      n = a.T;
+      shared = 1;
+    }
+    const bool gemv = n > 0 && n <= a.gemv_max;
+    const int n_gemv = gemv ? (n + kGemvMaxRows - 1) / kGemvMaxRows : 0;
+    const int n_tc = (!gemv && n > 0) ? (n + kTcMaxN - 1) / kTcMaxN : 0;
+    const int gi_gu = shared ? a.items_gu_shared : a.items_gu;
+    const int ti_gu = shared ? a.tiles_gu_shared : a.tiles_gu;
+    int v[6] = {n_gemv, n_gemv * gi_gu, n_gemv * a.items_dn, n_tc, n_tc * ti_gu, n_tc * a.tiles_dn};
+    int pos[6];
+    for (int i = 0; i < 6; ++i) {
+      int tot;
+      pos[i] = carry[i] + block_exclusive_scan(v[i], &tot, sh);
+      carry[i] += tot;
+    }
+    for (int j = 0; j < n_gemv; ++j) {
+      const int ti = pos[0] + j;
+      if (ti >= a.wl.capacity) {
+        raise_status(a.status, kStInternal, MOE_K_WORKLIST);
+        break;
+      }
+      FfnTask tk;
+      tk.expert = shared ? -1 : u;
+      tk.row0 = row0 + j * kGemvMaxRows;
+      tk.nrows = min(kGemvMaxRows, n - j * kGemvMaxRows);
+      tk.pad = 0;
+      a.wl.gemv_tasks[ti] = tk;
+      a.wl.gemv_start_gu[ti] = pos[1] + j * gi_gu;
+      a.wl.gemv_start_dn[ti] = pos[2] + j * a.items_dn;
+    }
+    for (int j = 0; j < n_tc; ++j) {
+      const int ti = pos[3] + j;
+      if (ti >= a.wl.capacity) {
+        raise_status(a.status, kStInternal, MOE_K_WORKLIST);
+        break;
+      }
+      FfnTask tk;
+      tk.expert = shared ? -1 : u;
+      tk.row0 = row0 + j * kTcMaxN;
+      tk.nrows = min(kTcMaxN, n - j * kTcMaxN);
+      tk.pad = 0;
+      a.wl.tc_tasks[ti] = tk;
+      a.wl.tc_start_gu[ti] = pos[4] + j * ti_gu;
+      a.wl.tc_start_dn[ti] = pos[5] + j * a.tiles_dn;
+    }
+  }
+  if (threadIdx.x == 0) {
+    a.wl.counts[kWlGemvTasks] = min(carry[0], a.wl.capacity);
+    a.wl.counts[kWlGemvItemsGU] = carry[0] <= a.wl.capacity ? carry[1] : 0;
+    a.wl.counts[kWlGemvItemsDN] = carry[0] <= a.wl.capacity ? carry[2] : 0;
+    a.wl.counts[kWlTcTasks] = min(carry[3], a.wl.capacity);
+    a.wl.counts[kWlTcTilesGU] = carry[3] <= a.wl.capacity ? carry[4] : 0;
+    a.wl.counts[kWlTcTilesDN] = carry[3] <= a.wl.capacity ? carry[5] : 0;
+  }
+}
+
+}  // namespace
+
+void launch_perm_count(const Launch& L, int T, int k, int E, const int32_t* ids, int32_t* bc) {
+  const int nblk = (T + kPermTokens - 1) / kPermTokens;
+  launch_begin(L, MOE_K_PERM_COUNT);
+  perm_count_kernel<<<nblk, kPermThreads, E * sizeof(int32_t), L.stream>>>(ids, bc, T, k, E,
+                                                                          L.status);
+  launch_end(L, MOE_K_PERM_COUNT);
+}
+
+void launch_perm_scan(const Launch& L, int T, int E, int32_t* bc, int32_t* counts,
+                      int32_t* offsets) {
+  const int nblk = (T + kPermTokens - 1) / kPermTokens;
+  launch_begin(L, MOE_K_PERM_SCAN);
+  perm_scan_kernel<<<1, 1024, 0, L.stream>>>(bc, counts, offsets, nblk, E);
+  launch_end(L, MOE_K_PERM_SCAN);
+}
+
+void launch_perm_scatter(const Launch& L, int T, int k, int E, const int32_t* ids,
+                         const int32_t* bc, int32_t* s2e, int32_t* e2s) {
+  const int nblk = (T + kPermTokens - 1) / kPermTokens;
+  const size_t smem = (size_t)E * kWords * sizeof(uint32_t);
+  set_smem_attr_once(reinterpret_cast<const void*>(perm_scatter_kernel), 200 * 1024,
+                     kAttrPermScatter);
+  launch_begin(L, MOE_K_PERM_SCATTER);
+  perm_scatter_kernel<<<nblk, kPermThreads, smem, L.stream>>>(ids, bc, s2e, e2s, T, k, E);
+  launch_end(L, MOE_K_PERM_SCATTER);
+}
+
+void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32_t* ids,
+                        const int32_t* e2s, const void* x, void* x_perm, float* x_perm_scale) {
+  GatherArgs a;
+  a.ids = ids;
+  a.e2s = e2s;
+  a.x = static_cast<const uint16_t*>(x);
+  a.x_perm = x_perm;
+  a.scale = x_perm_scale;
+  a.R = T * c.top_k;
+  a.k = c.top_k;
+  a.H = c.hidden;
+  a.E_r = c.n_routed;
+  a.w8a8 = c.wdtype == MOE_W8A8;
+  launch_begin(L, MOE_K_PERM_GATHER);
+  perm_gather_kernel<<<(a.R + 7) / 8, 256, 0, L.stream>>>(a);
+  launch_end(L, MOE_K_PERM_GATHER);
+}
+
+void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
+                     const WorkList& wl, int gemv_max_rows) {
+  WlArgs a;
+  a.offsets = offsets;
+  a.wl = wl;
+  a.E_r = c.n_routed;
+  a.T = T;
+  a.has_shared = c.shared_inter > 0;
+  a.gemv_max = gemv_max_rows;
+  a.items_gu = (c.inter + kGemvChGU - 1) / kGemvChGU;
+  a.items_gu_shared = (c.shared_inter + kGemvChGU - 1) / kGemvChGU;
+  a.items_dn = (c.hidden + kGemvChDN - 1) / kGemvChDN;
+  a.tiles_gu = (c.inter + kTcM - 1) / kTcM;
+  a.tiles_gu_shared = (c.shared_inter + kTcM - 1) / kTcM;
+  a.tiles_dn = (c.hidden + kTcM - 1) / kTcM;
+  a.status = L.status;
+  launch_begin(L, MOE_K_WORKLIST);
+  worklist_kernel<<<1, 1024, 0, L.stream>>>(a);
+  launch_end(L, MOE_K_WORKLIST);
+}
+
+}  // namespace moe

@@ -1,0 +1,162 @@
+"""The C-ABI library loads, exports what include/moe.h declares, and rejects bad
+arguments on the host before touching a GPU.  No compute call is made here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from sparse_expert_layer_gb300 import build as b
+
+    b.build()
+    import sparse_expert_layer_gb300 as m
+
+    return m
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|moe_status)\s+(moe_\w+)\s*\(", src,
+                                 flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for f in ("moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_layer_forward",
+              "moe_workspace_size", "moe_check_device_status", "moe_status_string"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(moe):
+    out = subprocess.run(["nm", "-D", "--defined-only", moe._LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\w+)$", out, flags=re.M))
+    missing = [f for f in declared_functions() if f not in exported]
+    assert not missing, missing
+    for f in declared_functions():
+        getattr(moe.lib, f)  # dlsym through ctypes
+
+
+def test_binding_names_match_header(moe):
+    for f in declared_functions():
+        if f in ("moe_status_string", "moe_kernel_name", "moe_timing_enable",
+                 "moe_timing_collect", "moe_launch_counts"):
+            continue
+        assert hasattr(moe, f), f
+
+
+def test_config_struct_layout_matches_header(moe):
+    # 15 int32 + 1 float, no padding
+    assert ctypes.sizeof(moe.MoeConfig) == 16 * 4
+
+
+def _ws(moe, cfg, T):
+    return moe.moe_workspace_size(cfg, T)
+
+
+def test_workspace_size_for_the_headline_layers(moe):
+    import synth
+
+    for name in synth.HEADLINE:
+        s = synth.spec(name)
+        cfg = moe.config_from_spec(s)
+        if s["wdtype"] == "w8a8":
+            with pytest.raises(moe.MoeError) as e:
+                _ws(moe, cfg, s["T"])
+            assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+            continue
+        n1 = _ws(moe, cfg, s["T"])
+        n2 = _ws(moe, cfg, 2 * s["T"])
+        assert 0 < n1 < n2
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("hidden", 7, 1), ("hidden", 0, 1), ("top_k", 0, 1), ("top_k", 9, 1), ("n_group", 3, 1),
+    ("score", 5, 1), ("bias_mode", 3, 1), ("shared_inter", 12, 1), ("inter", 4, 1),
+    ("renormalize", 2, 1), ("n_routed", -1, 1),
+])
+def test_invalid_configs_are_rejected(moe, field, value, status):
+    import synth
+
+    cfg = moe.config_from_spec(synth.spec("tiny"))
+    setattr(cfg, field, value)
+    n = ctypes.c_size_t(0)
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 16, ctypes.byref(n)) == status
+
+
+def test_group_rules(moe):
+    import synth
+
+    cfg = moe.config_from_spec(synth.spec("dsv3"))
+    n = ctypes.c_size_t(0)
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 128, ctypes.byref(n)) == 0
+    cfg.topk_group = 9
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 128, ctypes.byref(n)) == 1
+    cfg = moe.config_from_spec(synth.spec("pangu"))
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 456, ctypes.byref(n)) == 0
+    cfg.top_k = 7  # must equal n_group * per_group_k
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 456, ctypes.byref(n)) == 1
+
+
+def test_unsupported_sizes(moe):
+    import synth
+
+    cfg = moe.config_from_spec(synth.spec("tiny"))
+    n = ctypes.c_size_t(0)
+    cfg.top_k, cfg.n_routed = 33, 64
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 16, ctypes.byref(n)) == 2
+    cfg.top_k, cfg.n_routed = 2, 5000
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 16, ctypes.byref(n)) == 2
+
+
+def test_workspace_errors_are_host_side(moe):
+    import synth
+
+    cfg = moe.config_from_spec(synth.spec("tiny"))
+    need = _ws(moe, cfg, 16)
+    fake = 1 << 40  # never dereferenced: every call below fails before any launch
+    r = moe.lib.moe_route(ctypes.byref(cfg), 16, fake, fake, None, fake, fake, None, need, None)
+    assert r == moe.MOE_ERR_INVALID_ARG
+    r = moe.lib.moe_route(ctypes.byref(cfg), 16, fake, fake, None, fake, fake, fake + 8, need, None)
+    assert r == moe.MOE_ERR_ALIGNMENT
+    r = moe.lib.moe_route(ctypes.byref(cfg), 16, fake, fake, None, fake, fake, fake, need - 1, None)
+    assert r == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    r = moe.lib.moe_route(ctypes.byref(cfg), 16, fake + 2, fake, None, fake, fake, fake, need, None)
+    assert r == moe.MOE_ERR_ALIGNMENT
+    r = moe.lib.moe_route(ctypes.byref(cfg), 16, None, fake, None, fake, fake, fake, need, None)
+    assert r == moe.MOE_ERR_INVALID_ARG
+
+
+def test_bias_is_required_when_configured(moe):
+    import synth
+
+    cfg = moe.config_from_spec(synth.spec("longcat_s"))
+    need = _ws(moe, cfg, 48)
+    fake = 1 << 40
+    r = moe.lib.moe_route(ctypes.byref(cfg), 48, fake, fake, None, fake, fake, fake, need, None)
+    assert r == moe.MOE_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(moe):
+    import synth
+
+    cfg = moe.config_from_spec(synth.spec("tiny"))
+    need = _ws(moe, cfg, 0)
+    fake = 1 << 40
+    assert moe.lib.moe_route(ctypes.byref(cfg), 0, None, None, None, None, None, fake, need,
+                             None) == 0
+    assert moe.lib.moe_layer_forward(ctypes.byref(cfg), 0, *([None] * 13), fake, need, None) == 0
+
+
+def test_status_strings(moe):
+    for s in range(8):
+        assert moe.lib.moe_status_string(s)
+    assert moe.lib.moe_kernel_name(0) == b"router"
+    assert moe.lib.moe_kernel_name(99) == b"unknown"

@@ -1,0 +1,135 @@
+"""Whole-layer parity of moe_layer_forward against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import gpu_support as gs
+from tests import support
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["tiny", "longcat_s", "dsv3_s", "pangu_s", "ragged_s"]
+
+
+@pytest.fixture(scope="module")
+def m():
+    return gs.lib()
+
+
+def oracle_out(spec, d, x=None):
+    x = d["x"] if x is None else x
+    out, ids, w = support.oracle_layer(spec, x, d["w_r"], d["bias"], d["wts"])
+    return out
+
+
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("out_fp32", [True, False])
+def test_layer_matches_oracle(m, name, out_fp32):
+    spec = synth.spec(name)
+    d = gs.inputs(spec)
+    ref = oracle_out(spec, d)
+    got = gs.run_layer(m, spec, d, out_fp32=out_fp32)
+    gs.check_out(got, ref, bf16_out=not out_fp32, what=name)
+
+
+@pytest.mark.parametrize("gemv_max_rows", [1, 3, 1000])
+def test_layer_path_choice_does_not_change_result(m, gemv_max_rows):
+    spec = synth.spec("pangu_s")
+    d = gs.inputs(spec)
+    ref = oracle_out(spec, d)
+    got = gs.run_layer(m, spec, d, gemv_max_rows=gemv_max_rows)
+    gs.check_out(got, ref, bf16_out=False, what=f"gemv_max_rows={gemv_max_rows}")
+
+
+def test_layer_is_deterministic(m):
+    spec = synth.spec("dsv3_s")
+    d = gs.inputs(spec)
+    a = gs.run_layer(m, spec, d, out_fp32=True)
+    b = gs.run_layer(m, spec, d, out_fp32=True)
+    assert torch.equal(a, b)
+
+
+def test_single_token_and_empty_batch(m):
+    spec = synth.spec("ragged_s")
+    d = gs.inputs(spec)
+    ref = oracle_out(spec, d, x=d["x"][:1])
+    got = gs.run_layer(m, spec, d, x=d["x_d"][:1].contiguous())
+    gs.check_out(got, ref, bf16_out=False, what="T=1")
+    cfg = m.config_from_spec(spec)
+    ws = m.workspace(cfg, 0)
+    out = torch.empty(0, spec["hidden"], device="cuda", dtype=torch.bfloat16)
+    w = d["wts_d"]
+    m.moe_layer_forward(cfg, 0, d["x_d"][:0], d["w_r_d"], d["bias_d"], w["w_gate"], w["w_up"],
+                        w["w_down"], None, None, None, w["shared_gate"], w["shared_up"],
+                        w["shared_down"], out, ws)
+
+
+def test_zero_experts_pass_input_through(m):
+    spec = synth.spec("longcat_s", name="allzero")
+    d = dict(gs.inputs(synth.spec("longcat_s")))
+    bias = torch.zeros(synth.n_experts(spec))
+    bias[:spec["n_routed"]] = -1e3  # every pick lands on a zero-computation expert
+    d["bias"], d["bias_d"] = bias, bias.cuda()
+    got = gs.run_layer(m, spec, d, out_fp32=True).cpu().double().numpy()
+    _, _, w = support.oracle_layer(spec, d["x"], d["w_r"], bias, d["wts"])
+    xb = support.bf16_to_f64(synth.bf16_bits(d["x"]))
+    ref = w.sum(1, keepdims=True) * xb
+    assert np.allclose(got, ref, rtol=2e-6, atol=1e-6)
+
+
+def test_single_expert_top1_is_dense_ffn(m):
+    spec = dict(synth.spec("tiny"), n_routed=1, top_k=1, renormalize=False, T=40,
+                name="dense_gpu")
+    d = gs.inputs(spec)
+    got = gs.run_layer(m, spec, d, out_fp32=True)
+    xb = support.bf16_to_f64(synth.bf16_bits(d["x"]))
+    g, u, dn = support.expert_lists(d["wts"])
+    G = support.bf16_to_f64(g[0]) @ xb.T
+    U = support.bf16_to_f64(u[0]) @ xb.T
+    ref = (support.bf16_to_f64(dn[0]) @ (G / (1 + np.exp(-G)) * U)).T
+    gs.check_out(got, ref, bf16_out=False, what="dense")
+
+
+# ------------------------------------------------------- full-size layers ---
+
+def full_size_case(m, name, n_sample=4):
+    spec = synth.spec(name)
+    x, w_r, bias, redraws = support.make_inputs(spec)
+    wts_d = synth.draw_weights(spec, device="cuda")
+    d = dict(x=x, w_r=w_r, bias=bias, x_d=x.cuda(), w_r_d=w_r.cuda(),
+             bias_d=None if bias is None else bias.cuda(), wts_d=wts_d)
+    # routing of every token, bit-exact ids
+    cfg = m.config_from_spec(spec)
+    T, k = spec["T"], spec["top_k"]
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wgt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = m.workspace(cfg, T)
+    m.moe_route(cfg, T, d["x_d"], d["w_r_d"], d["bias_d"], ids, wgt, ws)
+    torch.cuda.synchronize()
+    ids_o, w_o, _, _ = oracle.route(spec, synth.bf16_bits(x), w_r.numpy(), support.np_bias(bias))
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    assert np.allclose(wgt.cpu().numpy(), w_o, rtol=1e-5, atol=1e-7)
+    # the layer at full size, bf16 out (the benchmarked configuration)
+    out = gs.run_layer(m, spec, d, out_fp32=False)
+    # oracle on sampled tokens with only the experts they pick
+    rng = np.random.default_rng(2)
+    sample = np.sort(rng.choice(T, n_sample, replace=False))
+    need = set(int(e) for e in ids_o[sample].reshape(-1) if e < spec["n_routed"])
+    g, u, dn = gs.expert_lists_from_device(wts_d, need)
+    shared = None
+    if spec["shared_inter"] > 0:
+        shared = tuple(synth.bf16_bits(wts_d[kk]) for kk in
+                       ("shared_gate", "shared_up", "shared_down"))
+    ref, ids_s, _ = oracle.layer(spec, synth.bf16_bits(x[sample]), w_r.numpy(),
+                                 support.np_bias(bias), g, u, dn, shared)
+    assert np.array_equal(ids_s, ids_o[sample])
+    gs.check_out(out[torch.as_tensor(sample, device="cuda")], ref, bf16_out=True, what=name)
+    del wts_d, d
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["longcat", "dsv3", "pangu"])
+def test_full_size_decode_layers(m, name):
+    full_size_case(m, name)
