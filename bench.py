@@ -58,7 +58,8 @@ def dist_setup(n):
     if world > 1:
         import torch.distributed as dist
 
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        if not dist.is_initialized():
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return rank, world, local
 
 
@@ -67,6 +68,11 @@ def barrier(world):
         import torch.distributed as dist
 
         dist.barrier()
+
+
+def whole_job_rate(world, units_per_rank_step, steps, ms_max):
+    """Units processed by all ranks per second, timed by the slowest rank."""
+    return world * units_per_rank_step * steps / (ms_max / 1e3)
 
 
 def max_over_ranks(v, world, device):
@@ -336,7 +342,7 @@ def run_ours(args, rank, world, local):
         raise RuntimeError("device status set during the timed region")
     ms = max_over_ranks(ms, world, dev)
     ms_step = ms / args.steps
-    value = world * T * args.steps / (ms / 1e3)
+    value = whole_job_rate(world, T, args.steps, ms)
 
     # end to end: host buffers, H2D of x and D2H of out inside the timed region
     x_h = x.pin_memory()
@@ -357,7 +363,7 @@ def run_ours(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    e2e = {"value": world * T * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
+    e2e = {"value": whole_job_rate(world, T, args.steps, ms_e2e), "unit": "tokens/s",
            "h2d_bytes_per_step": x.numel() * 2, "d2h_bytes_per_step": out.numel() * 2}
 
     # roofline of the dominant kernel

@@ -105,10 +105,12 @@ moe_status check_cfg(const moe_config* c, int32_t T) {
   return MOE_OK;
 }
 
+// Experts (and the shared expert) with at most this many rows stream through
+// the GEMV path; the others run on tensor-core tiles.
 int effective_gemv_max(const moe_config& c) {
-  // The tensor-core path is not part of this build yet: every task streams.
-  (void)c;
-  return INT_MAX;
+  if (c.gemv_max_rows > 0) return c.gemv_max_rows;
+  if (c.gemv_max_rows < 0) return 0;
+  return kDefaultGemvMaxRows;
 }
 
 // --------------------------------------------------------------- workspace --
@@ -221,10 +223,10 @@ void run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, 
 }
 
 // Grouped FFN over the sorted rows plus (optionally) the shared expert.
-void run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
-             const int32_t* offsets, const void* x_perm, const void* w_gate, const void* w_up,
-             const void* w_down, float* y_perm, const void* x, const void* sg, const void* su,
-             const void* sd, float* y_shared) {
+moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
+                   const int32_t* offsets, const void* x_perm, const void* w_gate,
+                   const void* w_up, const void* w_down, float* y_perm, const void* x,
+                   const void* sg, const void* su, const void* sd, float* y_shared) {
   const WorkList wl = worklist_view(ws, L);
   const bool shared = c.shared_inter > 0 && sg != nullptr;
   moe_config cw = c;
@@ -252,6 +254,29 @@ void run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L, void
   gu.Ns = c.shared_inter;
   launch_gemv_gate_up(ln, gu);
 
+  const int64_t R = (int64_t)T * c.top_k;
+  TcPass tg{};
+  tg.tasks = wl.tc_tasks;
+  tg.tile_start = wl.tc_start_gu;
+  tg.counts = wl.counts;
+  tg.task_slot = kWlTcTasks;
+  tg.tile_slot = kWlTcTilesGU;
+  tg.w0 = w_gate;
+  tg.w1 = w_up;
+  tg.n_experts = c.n_routed;
+  tg.act = x_perm;
+  tg.act_rows = R;
+  tg.out_h = h;
+  tg.sw0 = shared ? sg : nullptr;
+  tg.sw1 = shared ? su : nullptr;
+  tg.sact = x;
+  tg.sact_rows = T;
+  tg.sout_h = h_s;
+  tg.K = tg.Ks = c.hidden;
+  tg.N = c.inter;
+  tg.Ns = c.shared_inter;
+  if (c.n_routed > 0 && !launch_tc_gate_up(ln, tg)) return MOE_ERR_CUDA;
+
   GemvPass dn{};
   dn.tasks = wl.gemv_tasks;
   dn.item_start = wl.gemv_start_dn;
@@ -268,6 +293,27 @@ void run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L, void
   dn.Ks = c.shared_inter;
   dn.N = dn.Ns = c.hidden;
   launch_gemv_down(ln, dn);
+
+  TcPass td{};
+  td.tasks = wl.tc_tasks;
+  td.tile_start = wl.tc_start_dn;
+  td.counts = wl.counts;
+  td.task_slot = kWlTcTasks;
+  td.tile_slot = kWlTcTilesDN;
+  td.w0 = w_down;
+  td.n_experts = c.n_routed;
+  td.act = h;
+  td.act_rows = R;
+  td.out_y = y_perm;
+  td.sw0 = shared ? sd : nullptr;
+  td.sact = h_s;
+  td.sact_rows = T;
+  td.sout_y = y_shared;
+  td.K = c.inter;
+  td.Ks = c.shared_inter;
+  td.N = td.Ns = c.hidden;
+  if (c.n_routed > 0 && !launch_tc_down(ln, td)) return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 }  // namespace
@@ -407,9 +453,10 @@ moe_status moe_grouped_ffn(const moe_config* cfg, int32_t T, const int32_t* offs
   const Launch ln = make_launch(stream, ws, L);
   moe_config c = *cfg;
   c.shared_inter = 0;
-  run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y_perm, nullptr, nullptr,
-          nullptr, nullptr, nullptr);
-  return finish();
+  s = run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y_perm, nullptr, nullptr,
+              nullptr, nullptr, nullptr);
+  const moe_status f = finish();
+  return s != MOE_OK ? s : f;
 }
 
 moe_status moe_combine(const moe_config* cfg, int32_t T, const float* y_perm,
@@ -467,11 +514,13 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
   float* y_s = c.shared_inter > 0 ? at<float>(ws, L.y_s) : nullptr;
   run_route(ln, c, T, L, ws, x, w_router, bias, ids, w);
   run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale);
+  moe_status fs = MOE_OK;
   if (c.n_routed > 0 || c.shared_inter > 0)
-    run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y, x, ws_gate, ws_up, ws_down,
-            y_s);
+    fs = run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y, x, ws_gate, ws_up,
+                 ws_down, y_s);
   launch_combine(ln, c, T, y, e2s, ids, w, x, y_s, out);
-  return finish();
+  const moe_status f = finish();
+  return fs != MOE_OK ? fs : f;
 }
 
 moe_status moe_check_device_status(void* ws, moe_stream_t stream) {

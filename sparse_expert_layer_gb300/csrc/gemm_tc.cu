@@ -1,0 +1,363 @@
+// Grouped SwiGLU FFN, tensor-core path for loaded experts (the GEMM side of the
+// GEMV/GEMM switch in the Pangu Pro MoE disclosure, section SwiftGMM).
+//
+// Swap-AB tiles: the 128 weight rows of a channel tile are the MMA's M side and
+// the task's <= 128 token rows its N side (N rounded up to 16), so a task with
+// few tokens wastes no tensor work on padding rows of M.
+//   D_gate[ch, tok] = W_gate[e][ch, :] . X[tok, :]     (and D_up likewise)
+//   h[tok, ch]      = silu(D_gate) * D_up              (epilogue, bf16)
+//   D[ch, tok]      = W_down[e][ch, :] . h[tok, :]     -> y[tok, ch] (fp32)
+//
+// Persistent CTAs, one per SM, warp-specialised:
+//   warp 0    : TMA producer -- 128x64 weight tiles (3-D map over the expert
+//               stack) and 16-row activation boxes, 128-byte swizzle, into a
+//               multi-stage shared-memory ring.
+//   warp 1    : allocates TMEM; one lane issues tcgen05.mma (kind::f16, bf16 in,
+//               fp32 accumulate) and commits stage releases / tile completion.
+//   warps 2-5 : epilogue -- tcgen05.ld of the accumulators (each warp owns one
+//               32-lane quadrant of TMEM), SwiGLU, coalesced stores.
+// Accumulators are double-buffered in TMEM so the epilogue of one tile overlaps
+// the MMAs of the next.  Every wait is bounded.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBK = 64;                          // K elements per stage: one 128-byte row
+constexpr int kATileBytes = kTcM * kBK * 2;      // 16 KB
+constexpr int kBTileBytes = kTcMaxN * kBK * 2;   // 16 KB
+constexpr int kBoxRows = 16;
+constexpr int kBoxBytes = kBoxRows * kBK * 2;    // 2 KB
+
+template <bool GU>
+struct Geom {
+  static constexpr int kNA = GU ? 2 : 1;
+  static constexpr int kStageBytes = kNA * kATileBytes + kBTileBytes;
+  static constexpr int kStages = GU ? 4 : 6;
+  static constexpr int kTmemCols = GU ? 512 : 256;
+  static constexpr int kAccStride = GU ? 256 : 128;  // TMEM columns per accumulator buffer
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+};
+
+struct TcMaps {
+  CUtensorMap a0;   // routed weights: gate (gate/up pass) or down
+  CUtensorMap a1;   // routed up weights (gate/up pass)
+  CUtensorMap sa0;  // shared expert counterparts
+  CUtensorMap sa1;
+  CUtensorMap b;    // routed activation rows
+  CUtensorMap sb;   // shared expert activation rows
+};
+
+struct TcArgs {
+  const FfnTask* tasks;
+  const int32_t* tile_start;
+  const int32_t* counts;
+  int task_slot, tile_slot;
+  uint16_t* out_h;
+  float* out_y;
+  uint16_t* sout_h;
+  float* sout_y;
+  int K, Ks, N, Ns;
+  DevStatus* status;
+};
+
+struct Tile {
+  int row0, n, ct, e, shared, K, N;
+};
+
+__device__ __forceinline__ void decode_tile(const TcArgs& a, int tile, int ntasks, Tile& t) {
+  int lo = 0, hi = ntasks - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.tile_start[mid] <= tile)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const FfnTask tk = a.tasks[lo];
+  t.ct = tile - a.tile_start[lo];
+  t.row0 = tk.row0;
+  t.n = tk.nrows;
+  t.shared = tk.expert < 0;
+  t.e = t.shared ? 0 : tk.expert;
+  t.K = t.shared ? a.Ks : a.K;
+  t.N = t.shared ? a.Ns : a.N;
+}
+
+template <bool GU>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
+  using G = Geom<GU>;
+  extern __shared__ uint8_t smem_raw[];
+  const int kind = GU ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
+  const int ntasks = a.counts[a.task_slot];
+  const int ntiles = a.counts[a.tile_slot];
+  if (ntiles <= 0 || (int)blockIdx.x >= ntiles) return;  // uniform across the CTA
+
+  // 1024-byte aligned ring (128-byte swizzle atoms), barriers after it
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kStages * G::kStageBytes);
+  uint64_t* empty = full + G::kStages;
+  uint64_t* acc_full = empty + G::kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < G::kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 4);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&maps.a0);
+    prefetch_tensormap(&maps.b);
+    if (GU) prefetch_tensormap(&maps.a1);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), G::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- producer --
+    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+    uint32_t iter = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+      Tile t;
+      decode_tile(a, tile, ntasks, t);
+      const CUtensorMap* A0 = t.shared ? &maps.sa0 : &maps.a0;
+      const CUtensorMap* A1 = t.shared ? &maps.sa1 : &maps.a1;
+      const CUtensorMap* B = t.shared ? &maps.sb : &maps.b;
+      const int nb = (t.n + kBoxRows - 1) / kBoxRows;
+      const uint32_t bytes = (uint32_t)(G::kNA * kATileBytes + nb * kBoxBytes);
+      const int nks = (t.K + kBK - 1) / kBK;
+      for (int ks = 0; ks < nks; ++ks) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const int stage = iter % G::kStages;
+        const uint32_t par = (iter / G::kStages) & 1u;
+        if (!mbar_wait(smem_u32(&empty[stage]), par ^ 1u)) {
+          raise_status(a.status, kStTimeout, kind);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const uint32_t bar = smem_u32(&full[stage]);
+        mbar_arrive_expect_tx(bar, bytes);
+        uint8_t* st = smem + (size_t)stage * G::kStageBytes;
+        tma_load_3d(smem_u32(st), A0, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
+        if (GU) tma_load_3d(smem_u32(st + kATileBytes), A1, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
+        uint8_t* sb = st + G::kNA * kATileBytes;
+        for (int j = 0; j < nb; ++j)
+          tma_load_3d(smem_u32(sb + j * kBoxBytes), B, ks * kBK, t.row0 + j * kBoxRows, 0, bar,
+                      pol_x);
+        ++iter;
+      }
+    }
+    const uint32_t first = iter > (uint32_t)G::kStages ? iter - G::kStages : 0u;
+    for (uint32_t j = first; j < iter; ++j)
+      mbar_wait(smem_u32(&full[j % G::kStages]), (j / G::kStages) & 1u);
+  } else if (warp == 1 && lane == 0) {
+    // --------------------------------------------------------- MMA issuer --
+    uint32_t iter = 0, local = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++local) {
+      Tile t;
+      decode_tile(a, tile, ntasks, t);
+      const uint32_t buf = local & 1u, use = local >> 1;
+      if (!mbar_wait(smem_u32(&acc_empty[buf]), (use & 1u) ^ 1u)) {
+        raise_status(a.status, kStTimeout, kind);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t nmma = (uint32_t)((t.n + 15) / 16 * 16);
+      const uint32_t idesc = idesc_bf16_f32(kTcM, nmma);
+      const uint32_t d0 = tmem + buf * G::kAccStride;
+      const uint32_t d1 = d0 + kTcMaxN;
+      const int nks = (t.K + kBK - 1) / kBK;
+      for (int ks = 0; ks < nks; ++ks) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const int stage = iter % G::kStages;
+        const uint32_t par = (iter / G::kStages) & 1u;
+        if (!mbar_wait(smem_u32(&full[stage]), par)) {
+          raise_status(a.status, kStTimeout, kind);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + (size_t)stage * G::kStageBytes);
+        const uint32_t sb = sa + G::kNA * kATileBytes;
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k) {
+          const uint64_t bdesc = sdesc_sw128(sb + k * 32);
+          const uint32_t acc = (ks > 0 || k > 0) ? 1u : 0u;
+          tc_mma_bf16(d0, sdesc_sw128(sa + k * 32), bdesc, idesc, acc);
+          if (GU) tc_mma_bf16(d1, sdesc_sw128(sa + kATileBytes + k * 32), bdesc, idesc, acc);
+        }
+        tc_commit(smem_u32(&empty[stage]));
+        ++iter;
+      }
+      if (!ok) break;
+      tc_commit(smem_u32(&acc_full[buf]));
+    }
+    if (*abort_flag) {  // let issued MMAs finish before TMEM is released
+      tc_commit(smem_u32(drain));
+      mbar_wait(smem_u32(drain), 0u);
+    }
+  } else if (warp >= 2) {
+    // ----------------------------------------------------------- epilogue --
+    const int q = warp % 4;  // TMEM lane quadrant this warp may access
+    uint32_t local = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+      if (*abort_flag) break;
+      Tile t;
+      decode_tile(a, tile, ntasks, t);
+      const uint32_t buf = local & 1u, use = local >> 1;
+      if (!mbar_wait(smem_u32(&acc_full[buf]), use & 1u)) {
+        if (lane == 0) raise_status(a.status, kStTimeout, kind);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int ch = t.ct * kTcM + q * 32 + lane;
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * G::kAccStride;
+      for (int j0 = 0; j0 < t.n; j0 += 16) {
+        uint32_t g[16], u[16];
+        tmem_ld16(trow + j0, g);
+        if (GU) tmem_ld16(trow + kTcMaxN + j0, u);
+        tmem_ld_wait();
+        if (ch < t.N) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int tok = j0 + i;
+            if (tok < t.n) {
+              const size_t o = (size_t)(t.row0 + tok) * t.N + ch;
+              const float gv = __uint_as_float(g[i]);
+              if (GU) {
+                const float h = gv / (1.f + expf(-gv)) * __uint_as_float(u[i]);
+                (t.shared ? a.sout_h : a.out_h)[o] = f_to_bf16(h);
+              } else {
+                (t.shared ? a.sout_y : a.out_y)[o] = gv;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[buf]));
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, G::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------ host side --
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 [outer][rows][K] tensor, box = 64 (K) x box_rows x 1, 128-byte swizzle,
+// out-of-range elements read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint64_t outer,
+              uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || !base) return false;
+  const cuuint64_t dims[3] = {K, rows, outer};
+  const cuuint64_t strides[2] = {K * 2, rows * K * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kBK, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool GU>
+bool launch_tc(const Launch& L, const TcPass& p) {
+  using G = Geom<GU>;
+  TcMaps maps;
+  memset(&maps, 0, sizeof maps);
+  const uint64_t Kr = p.K, Nr = p.N;
+  bool ok = make_map(&maps.a0, p.w0, Kr, Nr, p.n_experts, kTcM) &&
+            make_map(&maps.b, p.act, Kr, p.act_rows, 1, kBoxRows);
+  if (GU) ok = ok && make_map(&maps.a1, p.w1, Kr, Nr, p.n_experts, kTcM);
+  if (p.sw0) {
+    ok = ok && make_map(&maps.sa0, p.sw0, p.Ks, p.Ns, 1, kTcM) &&
+         make_map(&maps.sb, p.sact, p.Ks, p.sact_rows, 1, kBoxRows);
+    if (GU) ok = ok && make_map(&maps.sa1, p.sw1, p.Ks, p.Ns, 1, kTcM);
+  }
+  if (!ok) return false;
+  TcArgs a;
+  a.tasks = p.tasks;
+  a.tile_start = p.tile_start;
+  a.counts = p.counts;
+  a.task_slot = p.task_slot;
+  a.tile_slot = p.tile_slot;
+  a.out_h = p.out_h;
+  a.out_y = p.out_y;
+  a.sout_h = p.sout_h;
+  a.sout_y = p.sout_y;
+  a.K = p.K;
+  a.Ks = p.Ks;
+  a.N = p.N;
+  a.Ns = p.Ns;
+  a.status = L.status;
+  const int kind = GU ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
+  set_smem_attr_once(reinterpret_cast<const void*>(tc_kernel<GU>), G::kSmemBytes,
+                     GU ? kAttrTcGU : kAttrTcDN);
+  launch_begin(L, kind);
+  tc_kernel<GU><<<L.num_sms, kThreads, G::kSmemBytes, L.stream>>>(maps, a);
+  launch_end(L, kind);
+  return true;
+}
+
+}  // namespace
+
+bool launch_tc_gate_up(const Launch& L, const TcPass& p) { return launch_tc<true>(L, p); }
+bool launch_tc_down(const Launch& L, const TcPass& p) { return launch_tc<false>(L, p); }
+
+}  // namespace moe

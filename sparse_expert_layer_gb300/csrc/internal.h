@@ -99,6 +99,31 @@ struct GemvPass {
 void launch_gemv_gate_up(const Launch& L, const GemvPass& p);
 void launch_gemv_down(const Launch& L, const GemvPass& p);
 
+// Grouped FFN, tensor-core path (gemm_tc.cu).  Returns false if a tensor map
+// could not be encoded (nothing launched).
+struct TcPass {
+  const FfnTask* tasks;
+  const int32_t* tile_start;
+  const int32_t* counts;
+  int task_slot, tile_slot;
+  const void* w0;          // routed weights [n_experts, N, K] (gate or down)
+  const void* w1;          // routed up weights (gate/up pass)
+  int n_experts;
+  const void* act;         // routed activation rows [act_rows, K]
+  int64_t act_rows;
+  uint16_t* out_h;         // gate/up pass output, bf16 [*, N]
+  float* out_y;            // down pass output, fp32 [*, N]
+  const void* sw0;         // shared expert [Ns, Ks] (nullptr: none)
+  const void* sw1;
+  const void* sact;        // shared activation rows [sact_rows, Ks]
+  int64_t sact_rows;
+  uint16_t* sout_h;
+  float* sout_y;
+  int K, Ks, N, Ns;
+};
+bool launch_tc_gate_up(const Launch& L, const TcPass& p);
+bool launch_tc_down(const Launch& L, const TcPass& p);
+
 // Combine (combine.cu)
 void launch_combine(const Launch& L, const moe_config& c, int T, const float* y_perm,
                     const int32_t* e2s, const int32_t* ids, const float* w, const void* x,

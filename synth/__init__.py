@@ -70,10 +70,11 @@ CONFIGS = {
 HEADLINE = ["tiny", "longcat", "dsv3", "pangu", "w8a8_prefill"]
 
 
-def spec(name: str, **overrides) -> dict:
-    d = dict(CONFIGS[name])
+def spec(base: str, **overrides) -> dict:
+    """Copy of a named layer description; overrides may rename it ('name')."""
+    d = dict(CONFIGS[base])
+    d["name"] = base
     d.update(overrides)
-    d["name"] = name
     return d
 
 

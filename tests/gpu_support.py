@@ -23,9 +23,9 @@ _cache = {}
 
 
 def lib():
-    from sparse_expert_layer_gb300 import build as b
+    import __graft_entry__
 
-    b.build()
+    __graft_entry__._builder().build()
     import sparse_expert_layer_gb300 as m
 
     return m

@@ -12,9 +12,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def moe():
-    from sparse_expert_layer_gb300 import build as b
+    import __graft_entry__
 
-    b.build()
+    __graft_entry__._builder().build()
     import sparse_expert_layer_gb300 as m
 
     return m
