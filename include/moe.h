@@ -184,6 +184,26 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
                              const void* ws_up, const void* ws_down, void* out, void* ws,
                              size_t ws_bytes, moe_stream_t stream);
 
+/* Router + top-k without any caller memory besides the tensors (the pages have
+ * no counterpart; this is a library convenience).  For callers that cannot
+ * provide a workspace: a host framework that hands an operator only its input
+ * and output buffers, or a decode loop that must not call cudaMalloc (it can
+ * synchronise the device and take milliseconds).  Same arguments and results as
+ * moe_route, minus the workspace.  Nothing is allocated: the router's partial
+ * logits live in a 4 MiB array compiled into the library, present on every GPU
+ * that loads it until the process exits.
+ *  - Rejects, with MOE_ERR_WORKSPACE_TOO_SMALL, any (cfg, T) whose partial
+ *    logits need more than 4 MiB (router split-K count x T x (E_r + E_z) x 4
+ *    bytes; e.g. T = 64 with 768 experts needs 2.6 MB).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Every call on a device shares the array: calls whose work overlaps on the
+ *    GPU (other streams, other host threads) race on it and may give wrong
+ *    results.  Serialise them.  Device-side data checks are not reported. */
+moe_status moe_route_noalloc(const moe_config* cfg, int32_t T, const void* x,
+                             const float* w_router, const float* bias, int32_t* topk_ids,
+                             float* topk_w, moe_stream_t stream);
+
 /* Synchronises `stream`, reads and clears the device status word in `ws`.
  * MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_DEVICE_TIMEOUT (or MOE_ERR_CUDA). */
 moe_status moe_check_device_status(void* ws, moe_stream_t stream);

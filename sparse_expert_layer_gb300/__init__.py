@@ -77,6 +77,7 @@ _SIGS = {
     "moe_layer_forward": [_C, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                           _P],
     "moe_check_device_status": [_P, _P],
+    "moe_route_noalloc": [_C, _I, _P, _P, _P, _P, _P, _P],
     "moe_timing_enable": [_I],
     "moe_timing_collect": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_I), _I],
     "moe_launch_counts": [ctypes.POINTER(ctypes.c_int64), _I],
@@ -143,6 +144,16 @@ def moe_route(cfg, T, x, w_router, bias, topk_ids, topk_w, ws, stream=None):
     _check(lib.moe_route(ctypes.byref(cfg), T, _ptr(x), _ptr(w_router), _ptr(bias),
                          _ptr(topk_ids), _ptr(topk_w), _ptr(ws), _ws_bytes(ws), _stream(stream)),
            "moe_route")
+
+
+def moe_route_noalloc(cfg, T, x, w_router, bias, topk_ids, topk_w, stream=None):
+    """moe_route without a workspace, for callers that cannot give the library
+    any memory besides the tensors (see include/moe.h): its scratch is a fixed
+    4 MiB array inside the library, shared by every call on the device, so
+    calls that overlap on the GPU must not be issued."""
+    _check(lib.moe_route_noalloc(ctypes.byref(cfg), T, _ptr(x), _ptr(w_router), _ptr(bias),
+                                 _ptr(topk_ids), _ptr(topk_w), _stream(stream)),
+           "moe_route_noalloc")
 
 
 def moe_permute(cfg, T, topk_ids, x, counts, offsets, sorted_to_expanded, expanded_to_sorted,

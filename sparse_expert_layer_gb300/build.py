@@ -17,7 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
 
-SOURCES = ["abi.cu", "route.cu", "permute.cu", "gemv.cu", "gemm_tc.cu", "combine.cu"]
+SOURCES = ["abi.cu", "route.cu", "permute.cu", "gemv.cu", "gemm_tc.cu", "combine.cu",
+           "route_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

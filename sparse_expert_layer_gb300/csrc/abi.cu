@@ -330,6 +330,8 @@ void set_smem_attr_once(const void* func, int bytes, int slot) {
     g_attr_done[slot][d].store(1, std::memory_order_release);
 }
 
+moe_status launch_status_take() { return finish(); }
+
 void launch_begin(const Launch& L, int kind) {
   g_launches[kind].fetch_add(1, std::memory_order_relaxed);
   t_open_event = nullptr;

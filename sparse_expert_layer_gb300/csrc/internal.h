@@ -136,5 +136,7 @@ void set_smem_attr_once(const void* func, int bytes, int slot);
 // Per-launch bookkeeping (abi.cu): call before/after each kernel launch.
 void launch_begin(const Launch& L, int kind);
 void launch_end(const Launch& L, int kind);
+// Status of the launches since the last call (MOE_OK or MOE_ERR_CUDA); resets it.
+moe_status launch_status_take();
 
 }  // namespace moe
