@@ -158,24 +158,65 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def tensor_peak():
+    """Dense bf16 (= fp16) tensor peak in TFLOP/s: the sustained figure when
+    measured (kernels are timed inside a long step), else the burst one."""
+    try:
+        d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        for key in ("bf16_tflops_sustained", "bf16_tflops"):
+            if key in d:
+                return float(d[key]), "measured:" + key
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+DEFAULT_GEMV_MAX_ROWS = 0  # the library's default switch point (every unit on tensor cores)
+
+
+def kernel_work(spec, counts, gemv_max_rows):
+    """{kernel: (algorithmic bytes, flops)} per launch, from the realised loads.
+    A unit (routed expert, or the shared expert over all T rows) with n rows goes
+    to the GEMV kernels when n <= the switch point, else to the tensor-core ones;
+    bytes = its weights once + its activation rows in and results out."""
+    H, I, Is, T = spec["hidden"], spec["inter"], spec["shared_inter"], spec["T"]
+    gm = gemv_max_rows if gemv_max_rows > 0 else (0 if gemv_max_rows < 0 else DEFAULT_GEMV_MAX_ROWS)
+    wb = 1 if spec["wdtype"] == "w8a8" else 2
+    units = [(int(n), I) for n in counts[:spec["n_routed"]] if n > 0]
+    if Is:
+        units.append((T, Is))
+    out = {k: [0, 0] for k in ("gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down")}
+    for n, inter in units:
+        p = "gemv_" if n <= gm else "tc_"
+        out[p + "gate_up"][0] += 2 * inter * H * wb + 2 * n * H + 2 * n * inter
+        out[p + "gate_up"][1] += 4 * n * inter * H
+        out[p + "down"][0] += inter * H * wb + 2 * n * inter + 4 * n * H
+        out[p + "down"][1] += 2 * n * inter * H
+    return {k: tuple(v) for k, v in out.items() if v[0]}
+
+
+def kernel_source_hash(files):
     h = hashlib.sha256()
-    for f in ("gemv.cu", "common.cuh"):
+    for f in files:
         h.update(open(os.path.join(ROOT, "sparse_expert_layer_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel, workload, units):
-    """DRAM bytes per launch from the committed ncu table, scaled to `units`; None
-    when absent or taken on a different kernel source."""
+def traffic_for(kernel, algorithmic_bytes):
+    """DRAM bytes of one launch: the committed ncu capture's ratio of DRAM bytes to
+    algorithmic bytes (taken on a smaller case of the same kernel; traffic grows
+    with the weight bytes streamed) times this launch's algorithmic bytes.  None
+    when there is no capture or the kernel source changed since it was taken."""
     try:
-        tab = json.load(open(PROFILE_TABLE))
+        rec = json.load(open(PROFILE_TABLE)).get(kernel)
     except (OSError, ValueError):
         return None
-    rec = tab.get(f"{kernel}:{workload}")
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if not rec or rec.get("source_hash") != kernel_source_hash(rec["source_files"]):
         return None
-    return rec["dram_bytes_per_launch"] * units / max(rec.get("units", units), 1)
+    return rec["dram_bytes"] / rec["algorithmic_bytes"] * algorithmic_bytes
 
 
 # ------------------------------------------------------------- workloads --
@@ -190,7 +231,10 @@ def algorithmic_bytes(spec, counts):
     router weights + bias + x in + out."""
     H, I, Is, E = spec["hidden"], spec["inter"], spec["shared_inter"], synth.n_experts(spec)
     U = int((counts[:spec["n_routed"]] > 0).sum())
-    per = 6 * H * I  # gate + up + down, bf16
+    if spec["wdtype"] == "w8a8":
+        per = 3 * H * I + 4 * (2 * I + H)  # int8 gate + up + down and their scales
+    else:
+        per = 6 * H * I  # gate + up + down, bf16
     b = U * per + 6 * H * Is + 4 * E * H + 2 * 2 * spec["T"] * H
     if spec["bias_mode"] != "none":
         b += 4 * E
@@ -198,6 +242,31 @@ def algorithmic_bytes(spec, counts):
 
 
 # ------------------------------------------------------------ CPU oracle --
+def oracle_runner(spec, wts, need, w_r, b):
+    """Callable running the fp64 oracle layer on token rows (bf16 bits), with host
+    copies of just the experts in `need` (bf16 or int8 + scales)."""
+    import oracle
+
+    E = spec["n_routed"]
+    if spec["wdtype"] == "w8a8":
+        L = {k: [None] * E for k in ("w_gate", "s_gate", "w_up", "s_up", "w_down", "s_down")}
+        for e in need:
+            for k in L:
+                L[k][e] = wts[k][e].cpu().numpy()
+        return lambda xb: oracle.layer_w8a8(spec, xb, w_r.numpy(), b, L["w_gate"], L["s_gate"],
+                                            L["w_up"], L["s_up"], L["w_down"], L["s_down"])
+    g, u, dn = [None] * E, [None] * E, [None] * E
+    for e in need:
+        g[e] = synth.bf16_bits(wts["w_gate"][e])
+        u[e] = synth.bf16_bits(wts["w_up"][e])
+        dn[e] = synth.bf16_bits(wts["w_down"][e])
+    shared = None
+    if spec["shared_inter"]:
+        shared = tuple(synth.bf16_bits(wts[k]) for k in ("shared_gate", "shared_up",
+                                                         "shared_down"))
+    return lambda xb: oracle.layer(spec, xb, w_r.numpy(), b, g, u, dn, shared)
+
+
 def oracle_sample(spec, x, w_r, bias, wts_d, n_tok, target_s):
     """Time the fp64 oracle on the first n_tok tokens (experts copied from HBM)."""
     import oracle
@@ -208,20 +277,11 @@ def oracle_sample(spec, x, w_r, bias, wts_d, n_tok, target_s):
     logits = oracle.router_logits(spec, synth.bf16_bits(xs), w_r.numpy(), b)
     ids, _, _, _ = oracle.select(spec, logits, b)
     need = sorted(set(int(e) for e in ids.reshape(-1) if e < spec["n_routed"]))
-    E = spec["n_routed"]
-    g, u, dn = [None] * E, [None] * E, [None] * E
-    for e in need:
-        g[e] = synth.bf16_bits(wts_d["w_gate"][e])
-        u[e] = synth.bf16_bits(wts_d["w_up"][e])
-        dn[e] = synth.bf16_bits(wts_d["w_down"][e])
-    shared = None
-    if spec["shared_inter"]:
-        shared = tuple(synth.bf16_bits(wts_d[k]) for k in ("shared_gate", "shared_up",
-                                                           "shared_down"))
+    run = oracle_runner(spec, wts_d, need, w_r, b)
     xb = synth.bf16_bits(xs)
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.layer(spec, xb, w_r.numpy(), b, g, u, dn, shared)
+        run(xb)
         reps += 1
         if time.perf_counter() - t0 >= target_s:
             break
@@ -248,19 +308,10 @@ def run_reference(args, rank, world):
                              experts=need)
     times = []
     xb = synth.bf16_bits(x[:n_tok])
-    E = spec["n_routed"]
-    g, u, dn = [None] * E, [None] * E, [None] * E
-    for e in need:
-        g[e] = synth.bf16_bits(wts["w_gate"][e])
-        u[e] = synth.bf16_bits(wts["w_up"][e])
-        dn[e] = synth.bf16_bits(wts["w_down"][e])
-    shared = None
-    if spec["shared_inter"]:
-        shared = tuple(synth.bf16_bits(wts[k]) for k in ("shared_gate", "shared_up",
-                                                         "shared_down"))
+    run = oracle_runner(spec, wts, need, w_r, b)
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.layer(spec, xb, w_r.numpy(), b, g, u, dn, shared)
+        run(xb)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     total = sum(times)
@@ -306,9 +357,11 @@ def run_ours(args, rank, world, local):
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     s2e = torch.empty(T * k, dtype=torch.int32, device=dev)
     e2s = torch.empty(T * k, dtype=torch.int32, device=dev)
-    x_perm = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+    w8 = spec["wdtype"] == "w8a8"
+    x_perm = torch.empty((T * k, H), dtype=torch.int8 if w8 else torch.bfloat16, device=dev)
+    x_scale = torch.empty(T * k, dtype=torch.float32, device=dev) if w8 else None
     moe.moe_route(cfg, T, x_d, w_r_d, bias_d, ids, wgt, layer.ws)
-    moe.moe_permute(cfg, T, ids, x_d, counts, offsets, s2e, e2s, x_perm, None, layer.ws)
+    moe.moe_permute(cfg, T, ids, x_d, counts, offsets, s2e, e2s, x_perm, x_scale, layer.ws)
     counts_h = counts.cpu().numpy()
     alg_bytes, U = algorithmic_bytes(spec, counts_h)
     del x_perm
@@ -368,29 +421,36 @@ def run_ours(args, rank, world, local):
 
     # roofline of the dominant kernel
     peak, peak_kind = hbm_peak()
+    tpeak, tpeak_kind = tensor_peak()
     dom = max(per_kernel, key=lambda kname: per_kernel[kname][0])
     dom_ms, dom_n = per_kernel[dom]
-    I, Is = spec["inter"], spec["shared_inter"]
     R_real = int(counts_h[:spec["n_routed"]].sum())
-    kbytes = {
-        "gemv_gate_up": U * 4 * H * I + 4 * H * Is + 2 * (R_real + (T if Is else 0)) * H,
-        "gemv_down": U * 2 * H * I + 2 * H * Is + 2 * (R_real * I + (T * Is if Is else 0)),
-    }
-    dom_bytes = kbytes.get(dom)
+    work = kernel_work(spec, counts_h, args.gemv_max_rows)
+    w8 = spec["wdtype"] == "w8a8"
     roof = None
-    if dom_bytes and dom_n:
-        achieved = dom_bytes / (dom_ms / dom_n / 1e3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
-                "traffic": traffic_for(dom, spec["name"], 1),
-                "algorithmic_bytes_per_launch": dom_bytes,
-                "avg_launch_ms": dom_ms / dom_n}
+    if dom in work and dom_n:
+        kb, kf = work[dom]
+        sec = dom_ms / dom_n / 1e3
+        if w8:
+            achieved = kf / sec / 1e12
+            roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": achieved / tpeak, "peak_source": tpeak_kind,
+                    "traffic": traffic_for(dom, kb),
+                    "algorithmic_flops_per_launch": kf, "avg_launch_ms": dom_ms / dom_n}
+        else:
+            achieved = kb / sec / 1e9
+            roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
+                    "traffic": traffic_for(dom, kb),
+                    "algorithmic_bytes_per_launch": kb, "avg_launch_ms": dom_ms / dom_n}
     layer_gbs = alg_bytes / (ms_step / 1e3) / 1e9
+    layer_flops = sum(f for k_, (b_, f) in work.items() if k_.startswith(("tc_", "gemv_")))
 
     line = {
         "metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8" if w8 else "bf16",
         "data": "synthetic",
         "config": {"workload": describe(spec), "tokens": T, "unique_experts": U,
                    "real_picks": R_real, "l2": "inputs larger than L2: "
@@ -398,6 +458,9 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}"},
         "layer_hbm": {"achieved_gbs": layer_gbs, "algorithmic_bytes": alg_bytes,
                       "frac": layer_gbs / peak, "peak": peak, "peak_source": peak_kind},
+        "layer_tensor": {"achieved_tflops": layer_flops / (ms_step / 1e3) / 1e12,
+                         "expert_flops": layer_flops, "peak": tpeak, "peak_source": tpeak_kind,
+                         "frac": layer_flops / (ms_step / 1e3) / 1e12 / tpeak},
         "roofline": roof,
         "kernels_ms_per_step": {kname: v[0] / args.steps for kname, v in per_kernel.items()
                                 if v[1]},

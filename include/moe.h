@@ -111,8 +111,10 @@ typedef struct {
 const char* moe_status_string(moe_status s);
 
 /* Bytes of device workspace needed by any entry point below for (cfg, T).
- * The same workspace serves every stage; its first 256 bytes hold the device
- * status word, which the caller must zero once (cudaMemset) before first use. */
+ * The same workspace serves every stage; its first 4096 bytes hold the device
+ * status word and the router's tile counters, which the caller must zero once
+ * (cudaMemset) before first use; the library leaves the counters zero after
+ * every call. */
 moe_status moe_workspace_size(const moe_config* cfg, int32_t T, size_t* bytes);
 
 /* Router + top-k gating.  [LC-A3] 优化措施三 (Router Matmul), [PANGU] opening
@@ -192,9 +194,9 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
  * moe_route, minus the workspace.  Nothing is allocated: the router's partial
  * logits live in a 4 MiB array compiled into the library, present on every GPU
  * that loads it until the process exits.
- *  - Rejects, with MOE_ERR_WORKSPACE_TOO_SMALL, any (cfg, T) whose partial
- *    logits need more than 4 MiB (router split-K count x T x (E_r + E_z) x 4
- *    bytes; e.g. T = 64 with 768 experts needs 2.6 MB).
+ *  - Rejects, with MOE_ERR_WORKSPACE_TOO_SMALL, any (cfg, T) whose logits need
+ *    more than 4 MiB: T x (E_r + E_z) x 4 bytes, times (1 + the router's split-K
+ *    count) when it splits K; e.g. T = 64 with 768 experts needs 2.6 MB.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress); make that first call before any stream capture.
  *  - Every call on a device shares the array: calls whose work overlaps on the
@@ -225,8 +227,23 @@ typedef enum {
   MOE_K_TC_DOWN,
   MOE_K_QUANT_H,
   MOE_K_COMBINE,
+  MOE_K_W8_EXACT,
   MOE_K_COUNT
 } moe_kernel_kind;
+
+/* Grouped int8 x int8 -> int32 matmul on the W8A8 path's kernels, exposing the
+ * exact integer accumulators (QuantBatchMatmul, [LC-A3] 优化措施三):
+ *   acc[r, n] = sum_k a[r, k] * w[e, n, k]   for offsets[e] <= r < offsets[e+1].
+ *  a        int8 [R, K] rows sorted by expert; w int8 [n_experts, N, K]
+ *  offsets  int32 [n_experts + 1], device, offsets[n_experts] <= R
+ *  acc      int32 [R, N] out (rows >= offsets[n_experts] untouched)
+ * K must be a multiple of 16 (<= 131071).  Exact for every int8 input: tiles
+ * whose partial sums could reach 2^24 are recomputed with integer arithmetic. */
+moe_status moe_qgemm_s8_workspace_size(int32_t n_experts, int32_t K, int32_t N, int32_t R,
+                                       size_t* bytes);
+moe_status moe_qgemm_s8(int32_t n_experts, int32_t K, int32_t N, int32_t R, const int32_t* offsets,
+                        const void* a, const void* w, int32_t* acc, void* ws, size_t ws_bytes,
+                        moe_stream_t stream);
 
 const char* moe_kernel_name(int32_t kind);
 

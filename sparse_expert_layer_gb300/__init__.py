@@ -40,7 +40,8 @@ BIAS_NONE, BIAS_LOGIT, BIAS_SELECT = 0, 1, 2
 W_BF16, W8A8 = 0, 1
 
 KERNELS = ["router", "topk", "perm_count", "perm_scan", "perm_scatter", "perm_gather",
-           "worklist", "gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down", "quant_h", "combine"]
+           "worklist", "gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down", "quant_h", "combine",
+           "w8_exact"]
 N_KERNELS = len(KERNELS)
 
 
@@ -78,6 +79,8 @@ _SIGS = {
                           _P],
     "moe_check_device_status": [_P, _P],
     "moe_route_noalloc": [_C, _I, _P, _P, _P, _P, _P, _P],
+    "moe_qgemm_s8_workspace_size": [_I, _I, _I, _I, ctypes.POINTER(_SZ)],
+    "moe_qgemm_s8": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P],
     "moe_timing_enable": [_I],
     "moe_timing_collect": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_I), _I],
     "moe_launch_counts": [ctypes.POINTER(ctypes.c_int64), _I],
@@ -186,6 +189,19 @@ def moe_layer_forward(cfg, T, x, w_router, bias, w_gate, w_up, w_down, s_gate, s
                                  _ptr(s_up), _ptr(s_down), _ptr(ws_gate), _ptr(ws_up),
                                  _ptr(ws_down), _ptr(out), _ptr(ws), _ws_bytes(ws),
                                  _stream(stream)), "moe_layer_forward")
+
+
+def moe_qgemm_s8_workspace_size(n_experts, K, N, R) -> int:
+    n = _SZ(0)
+    _check(lib.moe_qgemm_s8_workspace_size(n_experts, K, N, R, ctypes.byref(n)),
+           "moe_qgemm_s8_workspace_size")
+    return n.value
+
+
+def moe_qgemm_s8(n_experts, K, N, R, offsets, a, w, acc, ws, stream=None):
+    """Grouped int8 x int8 -> exact int32 (see include/moe.h)."""
+    _check(lib.moe_qgemm_s8(n_experts, K, N, R, _ptr(offsets), _ptr(a), _ptr(w), _ptr(acc),
+                            _ptr(ws), _ws_bytes(ws), _stream(stream)), "moe_qgemm_s8")
 
 
 def moe_check_device_status(ws, stream=None) -> int:

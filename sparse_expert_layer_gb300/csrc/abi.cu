@@ -99,7 +99,13 @@ moe_status check_cfg(const moe_config* c, int32_t T) {
   if (c->bias_mode < MOE_BIAS_NONE || c->bias_mode > MOE_BIAS_SELECT) return MOE_ERR_INVALID_ARG;
   if (c->shared_inter < 0 || c->shared_inter % 8) return MOE_ERR_INVALID_ARG;
   if (c->wdtype != MOE_W_BF16 && c->wdtype != MOE_W8A8) return MOE_ERR_INVALID_ARG;
-  if (c->wdtype == MOE_W8A8) return MOE_ERR_UNSUPPORTED;  // int8 path not in this build yet
+  if (c->wdtype == MOE_W8A8) {
+    // int8 rows must be whole 16-byte vectors; per-row sums of squared codes must
+    // fit int32 (K <= 131071); no shared expert in this mode.
+    if (c->hidden % 16 || (c->n_routed > 0 && c->inter % 16)) return MOE_ERR_INVALID_ARG;
+    if (c->hidden > 131071 || c->inter > 131071) return MOE_ERR_UNSUPPORTED;
+    if (c->shared_inter > 0) return MOE_ERR_UNSUPPORTED;
+  }
   if (c->out_fp32 != 0 && c->out_fp32 != 1) return MOE_ERR_INVALID_ARG;
   if ((long long)T * c->top_k > (1LL << 30) || T > (1 << 24)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -112,12 +118,26 @@ int effective_gemv_max(const moe_config& c) {
   if (c.gemv_max_rows < 0) return 0;
   return kDefaultGemvMaxRows;
 }
+// The GEMV launches are skipped when no unit can take that path.
+bool gemv_possible(int gemv_max) { return gemv_max > 0; }
+
+// Rows per GEMV task: the smallest of 1, 2, 4, 8 that holds gemv_max rows (8 when
+// gemv_max is larger: such units are split into 8-row tasks).
+int gemv_chunk(int gemv_max) {
+  int c = 1;
+  while (c < gemv_max && c < kGemvMaxRows) c *= 2;
+  return c;
+}
 
 // --------------------------------------------------------------- workspace --
 struct Layout {
-  size_t status, partial, ids, w, bc, counts, offsets, s2e, e2s;
+  size_t status, partial, logits, ids, w, bc, counts, offsets, s2e, e2s;
   size_t wl_gemv_tasks, wl_gemv_gu, wl_gemv_dn, wl_tc_tasks, wl_tc_gu, wl_tc_dn, wl_counts;
   size_t x_perm, x_scale, h, y, h_s, y_s;
+  // W8A8 only: integer-valued fp16 copies of the codes, row norms, fp32 h and
+  // its codes/scales, and the guard-failure lists of the two passes
+  size_t x16, xn2, h32, hq16, hsc, hn2, redo_gu, redo_dn;
+  int redo_cap;
   size_t total;
   int splits, nblk, wl_cap;
 };
@@ -129,7 +149,7 @@ Layout make_layout(const moe_config& c, int T) {
   const size_t H = c.hidden, I = c.inter, Is = c.shared_inter;
   L.splits = router_splits(c, T, kRouterTargetCtas / 2);
   L.nblk = (T + kPermTokens - 1) / kPermTokens;
-  L.wl_cap = c.n_routed + 4 + (int)((R + T) / kGemvMaxRows);
+  L.wl_cap = c.n_routed + 4 + (int)(R + T);  // one-row tasks at worst
   const size_t xb = c.wdtype == MOE_W8A8 ? 1 : 2;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -137,8 +157,9 @@ Layout make_layout(const moe_config& c, int T) {
     off = align256(off + bytes);
     return at;
   };
-  L.status = take(256);
-  L.partial = take((size_t)L.splits * T * E * 4);
+  L.status = take(256 + kRouterCounterBytes);  // status word, then router tile counters
+  L.partial = take(L.splits > 1 ? (size_t)L.splits * T * E * 4 : 0);
+  L.logits = take((size_t)T * E * 4);
   L.ids = take(R * 4);
   L.w = take(R * 4);
   L.bc = take((size_t)L.nblk * E * 4);
@@ -159,6 +180,19 @@ Layout make_layout(const moe_config& c, int T) {
   L.y = take(R * H * 4);
   L.h_s = take((size_t)T * Is * 2);
   L.y_s = take(Is > 0 ? (size_t)T * H * 4 : 0);
+  if (c.wdtype == MOE_W8A8) {
+    const size_t tc_tasks = c.n_routed + 4 + R / kTcMaxN;
+    const size_t tiles = (std::max(I, H) + kTcM - 1) / kTcM;
+    L.redo_cap = (int)(tc_tasks * tiles);
+    L.x16 = take(R * H * 2);
+    L.xn2 = take(R * 4);
+    L.h32 = take(R * I * 4);
+    L.hq16 = take(R * I * 2);
+    L.hsc = take(R * 4);
+    L.hn2 = take(R * 4);
+    L.redo_gu = take((size_t)(1 + L.redo_cap) * 4);
+    L.redo_dn = take((size_t)(1 + L.redo_cap) * 4);
+  }
   L.total = off;
   return L;
 }
@@ -178,6 +212,8 @@ WorkList worklist_view(void* ws, const Layout& L) {
   wl.tc_start_dn = at<int32_t>(ws, L.wl_tc_dn);
   wl.counts = at<int32_t>(ws, L.wl_counts);
   wl.capacity = L.wl_cap;
+  wl.redo_gu = L.redo_cap > 0 ? at<int32_t>(ws, L.redo_gu) : nullptr;
+  wl.redo_dn = L.redo_cap > 0 ? at<int32_t>(ws, L.redo_dn) : nullptr;
   return wl;
 }
 
@@ -207,8 +243,10 @@ Launch make_launch(moe_stream_t stream, void* ws, const Layout& L) {
 void run_route(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
                const void* x, const float* w_router, const float* bias, int32_t* ids, float* w) {
   float* partial = at<float>(ws, L.partial);
-  launch_router(ln, c, T, x, w_router, partial, L.splits);
-  launch_topk(ln, c, T, partial, L.splits, bias, ids, w);
+  float* logits = at<float>(ws, L.logits);
+  int* counters = at<int>(ws, L.status + 256);
+  launch_router(ln, c, T, x, w_router, partial, L.splits, logits, counters);
+  launch_topk(ln, c, T, logits, bias, ids, w);
 }
 
 void run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
@@ -231,7 +269,9 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   const bool shared = c.shared_inter > 0 && sg != nullptr;
   moe_config cw = c;
   if (!shared) cw.shared_inter = 0;
-  launch_worklist(ln, cw, T, offsets, wl, effective_gemv_max(c));
+  const int gemv_max = effective_gemv_max(c);
+  const int chunk = gemv_chunk(gemv_max);
+  launch_worklist(ln, cw, T, offsets, wl, gemv_max, chunk);
   uint16_t* h = at<uint16_t>(ws, L.h);
   uint16_t* h_s = at<uint16_t>(ws, L.h_s);
 
@@ -252,7 +292,8 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   gu.K = gu.Ks = c.hidden;
   gu.N = c.inter;
   gu.Ns = c.shared_inter;
-  launch_gemv_gate_up(ln, gu);
+  gu.max_rows = chunk;
+  if (gemv_possible(gemv_max)) launch_gemv_gate_up(ln, gu);
 
   const int64_t R = (int64_t)T * c.top_k;
   TcPass tg{};
@@ -292,7 +333,8 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   dn.K = c.inter;
   dn.Ks = c.shared_inter;
   dn.N = dn.Ns = c.hidden;
-  launch_gemv_down(ln, dn);
+  dn.max_rows = chunk;
+  if (gemv_possible(gemv_max)) launch_gemv_down(ln, dn);
 
   TcPass td{};
   td.tasks = wl.tc_tasks;
@@ -313,6 +355,70 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   td.Ks = c.shared_inter;
   td.N = td.Ns = c.hidden;
   if (c.n_routed > 0 && !launch_tc_down(ln, td)) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// W8A8 grouped FFN over the sorted rows (int8 codes + per-row scales).
+moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
+                        const int32_t* offsets, const void* x_perm, const float* x_scale,
+                        const void* w_gate, const void* w_up, const void* w_down,
+                        const float* s_gate, const float* s_up, const float* s_down,
+                        float* y_perm) {
+  const WorkList wl = worklist_view(ws, L);
+  moe_config cw = c;
+  cw.shared_inter = 0;
+  launch_worklist(ln, cw, T, offsets, wl, 0, 1);  // every expert on tensor-core tiles
+  const int64_t R = (int64_t)T * c.top_k;
+  const int32_t* n_real = offsets + c.n_routed;   // rows that belong to FFN experts
+  uint16_t* x16 = at<uint16_t>(ws, L.x16);
+  int32_t* xn2 = at<int32_t>(ws, L.xn2);
+  float* h32 = at<float>(ws, L.h32);
+  uint16_t* hq16 = at<uint16_t>(ws, L.hq16);
+  float* hsc = at<float>(ws, L.hsc);
+  int32_t* hn2 = at<int32_t>(ws, L.hn2);
+  launch_i8_rows_to_f16(ln, static_cast<const int8_t*>(x_perm), x16, xn2, (int)R, c.hidden, n_real);
+
+  W8Pass g{};
+  g.mode = kW8GateUp;
+  g.tasks = wl.tc_tasks;
+  g.tile_start = wl.tc_start_gu;
+  g.counts = wl.counts;
+  g.task_slot = kWlTcTasks;
+  g.tile_slot = kWlTcTilesGU;
+  g.w0 = w_gate;
+  g.w1 = w_up;
+  g.n_experts = c.n_routed;
+  g.s0 = s_gate;
+  g.s1 = s_up;
+  g.act = x16;
+  g.act_rows = R;
+  g.row_norm2 = xn2;
+  g.row_scale = x_scale;
+  g.out_f32 = h32;
+  g.redo = wl.redo_gu;
+  g.redo_cap = L.redo_cap;
+  g.K = c.hidden;
+  g.N = c.inter;
+  if (!launch_w8a8(ln, g)) return MOE_ERR_CUDA;
+
+  launch_quant_rows(ln, h32, hq16, hsc, hn2, (int)R, c.inter, n_real);
+
+  W8Pass d = g;
+  d.mode = kW8Down;
+  d.tile_start = wl.tc_start_dn;
+  d.tile_slot = kWlTcTilesDN;
+  d.w0 = w_down;
+  d.w1 = nullptr;
+  d.s0 = s_down;
+  d.s1 = nullptr;
+  d.act = hq16;
+  d.row_norm2 = hn2;
+  d.row_scale = hsc;
+  d.out_f32 = y_perm;
+  d.redo = wl.redo_dn;
+  d.K = c.inter;
+  d.N = c.hidden;
+  if (!launch_w8a8(ln, d)) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
@@ -378,7 +484,7 @@ const char* moe_status_string(moe_status s) {
 const char* moe_kernel_name(int32_t kind) {
   static const char* names[MOE_K_COUNT] = {
       "router", "topk", "perm_count", "perm_scan", "perm_scatter", "perm_gather", "worklist",
-      "gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down", "quant_h", "combine"};
+      "gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down", "quant_h", "combine", "w8_exact"};
   return (kind >= 0 && kind < MOE_K_COUNT) ? names[kind] : "unknown";
 }
 
@@ -439,24 +545,27 @@ moe_status moe_grouped_ffn(const moe_config* cfg, int32_t T, const int32_t* offs
                            const void* w_up, const void* w_down, const float* s_gate,
                            const float* s_up, const float* s_down, float* y_perm, void* ws,
                            size_t ws_bytes, moe_stream_t stream) {
-  (void)x_perm_scale;
-  (void)s_gate;
-  (void)s_up;
-  (void)s_down;
   moe_status s = check_cfg(cfg, T);
   if (s != MOE_OK) return s;
   Layout L;
   if ((s = check_ws(*cfg, T, ws, ws_bytes, &L)) != MOE_OK) return s;
   if (T == 0 || cfg->n_routed == 0) return MOE_OK;
   if (!offsets || !x_perm || !w_gate || !w_up || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
+  const bool w8 = cfg->wdtype == MOE_W8A8;
+  if (w8 && (!x_perm_scale || !s_gate || !s_up || !s_down)) return MOE_ERR_INVALID_ARG;
   if (!aligned(x_perm, 16) || !aligned(w_gate, 16) || !aligned(w_up, 16) || !aligned(w_down, 16) ||
-      !aligned(y_perm, 16))
+      !aligned(y_perm, 16) || !aligned(x_perm_scale, 4) || !aligned(s_gate, 4) ||
+      !aligned(s_up, 4) || !aligned(s_down, 4))
     return MOE_ERR_ALIGNMENT;
   const Launch ln = make_launch(stream, ws, L);
   moe_config c = *cfg;
   c.shared_inter = 0;
-  s = run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y_perm, nullptr, nullptr,
-              nullptr, nullptr, nullptr);
+  if (w8)
+    s = run_ffn_w8a8(ln, c, T, L, ws, offsets, x_perm, x_perm_scale, w_gate, w_up, w_down, s_gate,
+                     s_up, s_down, y_perm);
+  else
+    s = run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y_perm, nullptr, nullptr,
+                nullptr, nullptr, nullptr);
   const moe_status f = finish();
   return s != MOE_OK ? s : f;
 }
@@ -486,9 +595,6 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
                              const float* s_up, const float* s_down, const void* ws_gate,
                              const void* ws_up, const void* ws_down, void* out, void* ws,
                              size_t ws_bytes, moe_stream_t stream) {
-  (void)s_gate;
-  (void)s_up;
-  (void)s_down;
   moe_status s = check_cfg(cfg, T);
   if (s != MOE_OK) return s;
   Layout L;
@@ -497,6 +603,9 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
   if (!x || !w_router || !out) return MOE_ERR_INVALID_ARG;
   if (cfg->bias_mode != MOE_BIAS_NONE && !bias) return MOE_ERR_INVALID_ARG;
   if (cfg->n_routed > 0 && (!w_gate || !w_up || !w_down)) return MOE_ERR_INVALID_ARG;
+  const bool w8 = cfg->wdtype == MOE_W8A8;
+  if (w8 && cfg->n_routed > 0 && (!s_gate || !s_up || !s_down)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(s_gate, 4) || !aligned(s_up, 4) || !aligned(s_down, 4)) return MOE_ERR_ALIGNMENT;
   if (cfg->shared_inter > 0 && (!ws_gate || !ws_up || !ws_down)) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(w_gate, 16) || !aligned(w_up, 16) ||
       !aligned(w_down, 16) || !aligned(ws_gate, 16) || !aligned(ws_up, 16) ||
@@ -517,12 +626,122 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
   run_route(ln, c, T, L, ws, x, w_router, bias, ids, w);
   run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale);
   moe_status fs = MOE_OK;
-  if (c.n_routed > 0 || c.shared_inter > 0)
+  if (w8 && c.n_routed > 0)
+    fs = run_ffn_w8a8(ln, c, T, L, ws, offsets, x_perm, x_scale, w_gate, w_up, w_down, s_gate,
+                      s_up, s_down, y);
+  else if (!w8 && (c.n_routed > 0 || c.shared_inter > 0))
     fs = run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y, x, ws_gate, ws_up,
                  ws_down, y_s);
   launch_combine(ln, c, T, y, e2s, ids, w, x, y_s, out);
   const moe_status f = finish();
   return fs != MOE_OK ? fs : f;
+}
+
+namespace {
+struct QLayout {
+  size_t tasks, start_gu, start_dn, tc_tasks, tc_gu, tc_dn, counts, a16, an2, redo, total;
+  int cap, redo_cap;
+};
+QLayout qgemm_layout(int E, int K, int N, int R) {
+  QLayout Q{};
+  Q.cap = E + 4 + R / kTcMaxN;
+  Q.redo_cap = Q.cap * ((N + kTcM - 1) / kTcM);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  take(256 + kRouterCounterBytes);  // status word (same head as the layer workspace)
+  Q.tasks = take((size_t)Q.cap * sizeof(FfnTask));
+  Q.start_gu = take((size_t)Q.cap * 4);
+  Q.start_dn = take((size_t)Q.cap * 4);
+  Q.tc_tasks = take((size_t)Q.cap * sizeof(FfnTask));
+  Q.tc_gu = take((size_t)Q.cap * 4);
+  Q.tc_dn = take((size_t)Q.cap * 4);
+  Q.counts = take(kWlCount * 4);
+  Q.a16 = take((size_t)R * K * 2);
+  Q.an2 = take((size_t)R * 4);
+  Q.redo = take((size_t)(1 + Q.redo_cap) * 4);
+  Q.total = off;
+  return Q;
+}
+moe_status check_qgemm(int E, int K, int N, int R) {
+  if (E < 1 || K < 16 || K % 16 || N < 1 || R < 0) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts || K > 131071 || (long long)R * (K > N ? K : N) > (1LL << 40))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+}  // namespace
+
+moe_status moe_qgemm_s8_workspace_size(int32_t n_experts, int32_t K, int32_t N, int32_t R,
+                                       size_t* bytes) {
+  const moe_status s = check_qgemm(n_experts, K, N, R);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = qgemm_layout(n_experts, K, N, R).total;
+  return MOE_OK;
+}
+
+moe_status moe_qgemm_s8(int32_t n_experts, int32_t K, int32_t N, int32_t R, const int32_t* offsets,
+                        const void* a, const void* w, int32_t* acc, void* ws, size_t ws_bytes,
+                        moe_stream_t stream) {
+  moe_status s = check_qgemm(n_experts, K, N, R);
+  if (s != MOE_OK) return s;
+  const QLayout Q = qgemm_layout(n_experts, K, N, R);
+  if (!ws || !offsets || !w || !acc || (R > 0 && !a)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < Q.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(a, 16) || !aligned(w, 16) || !aligned(acc, 4) || !aligned(offsets, 4))
+    return MOE_ERR_ALIGNMENT;
+  if (R == 0) return MOE_OK;
+  Launch ln;
+  ln.stream = reinterpret_cast<cudaStream_t>(stream);
+  ln.num_sms = sm_count(current_device());
+  ln.status = at<DevStatus>(ws, 0);
+  WorkList wl;
+  wl.gemv_tasks = at<FfnTask>(ws, Q.tasks);
+  wl.gemv_start_gu = at<int32_t>(ws, Q.start_gu);
+  wl.gemv_start_dn = at<int32_t>(ws, Q.start_dn);
+  wl.tc_tasks = at<FfnTask>(ws, Q.tc_tasks);
+  wl.tc_start_gu = at<int32_t>(ws, Q.tc_gu);
+  wl.tc_start_dn = at<int32_t>(ws, Q.tc_dn);
+  wl.counts = at<int32_t>(ws, Q.counts);
+  wl.capacity = Q.cap;
+  wl.redo_gu = nullptr;
+  wl.redo_dn = at<int32_t>(ws, Q.redo);
+  // Tasks: the experts' row ranges in <= 128-row chunks, N/128 tiles each (the
+  // work-list kernel's "down" tiling, hidden = N).
+  moe_config c{};
+  c.hidden = N;
+  c.inter = 16;
+  c.n_routed = n_experts;
+  c.top_k = 1;
+  c.n_group = 1;
+  launch_worklist(ln, c, R, offsets, wl, 0, 1);
+  uint16_t* a16 = at<uint16_t>(ws, Q.a16);
+  int32_t* an2 = at<int32_t>(ws, Q.an2);
+  launch_i8_rows_to_f16(ln, static_cast<const int8_t*>(a), a16, an2, R, K, offsets + n_experts);
+  W8Pass p{};
+  p.mode = kW8Raw;
+  p.tasks = wl.tc_tasks;
+  p.tile_start = wl.tc_start_dn;
+  p.counts = wl.counts;
+  p.task_slot = kWlTcTasks;
+  p.tile_slot = kWlTcTilesDN;
+  p.w0 = w;
+  p.n_experts = n_experts;
+  p.act = a16;
+  p.act_rows = R;
+  p.row_norm2 = an2;
+  p.out_i32 = acc;
+  p.redo = wl.redo_dn;
+  p.redo_cap = Q.redo_cap;
+  p.K = K;
+  p.N = N;
+  const bool ok = launch_w8a8(ln, p);
+  const moe_status f = finish();
+  return ok ? f : MOE_ERR_CUDA;
 }
 
 moe_status moe_check_device_status(void* ws, moe_stream_t stream) {

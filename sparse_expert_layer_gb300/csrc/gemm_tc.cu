@@ -75,16 +75,9 @@ struct Tile {
 };
 
 __device__ __forceinline__ void decode_tile(const TcArgs& a, int tile, int ntasks, Tile& t) {
-  int lo = 0, hi = ntasks - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (a.tile_start[mid] <= tile)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  const FfnTask tk = a.tasks[lo];
-  t.ct = tile - a.tile_start[lo];
+  int task;
+  tc_tile_of(a.tasks, a.tile_start, ntasks, tile, &task, &t.ct);
+  const FfnTask tk = a.tasks[task];
   t.row0 = tk.row0;
   t.n = tk.nrows;
   t.shared = tk.expert < 0;

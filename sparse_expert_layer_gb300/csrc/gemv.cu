@@ -5,10 +5,11 @@
 // This is the GEMV side: each expert's weights are read from HBM exactly once
 // and dotted with its few activation rows on CUDA cores.
 //
-// Work item = (task, block of output channels); a task is <= 8 rows of one
-// expert.  Persistent CTAs (one per SM) walk the items round-robin.
+// Work item = (task, block of output channels); a task is <= NR (1, 2, 4 or 8)
+// rows of one expert.  Persistent CTAs (one per SM) walk the items round-robin.
 //   warp 0     : producer.  Streams 1024-element slices of 16 weight rows and
-//                of the task's activation rows into a 4-stage shared-memory ring
+//                of the task's activation rows into a shared-memory ring (as many
+//                stages as fit in 200 KB: 5 to 6 at NR <= 4, 4 at NR = 8)
 //                with cp.async.bulk (weights marked evict-first in L2).
 //   warps 1..8 : consumers.  Warp w owns two weight rows -- (gate c, up c) in
 //                the gate/up pass, (c, c+1) in the down pass -- and its lanes
@@ -29,10 +30,17 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kKS = 1024;                      // elements per row slice
 constexpr int kSliceBytes = kKS * 2;           // bytes per row slice
 constexpr int kWRows = 2 * kConsumerWarps;     // weight row slices per stage
-constexpr int kStageBytes = (kWRows + kGemvMaxRows) * kSliceBytes;
-constexpr int kStages = 4;
-constexpr int kBarOffset = kStages * kStageBytes;
-constexpr int kSmemBytes = kBarOffset + 256;
+constexpr int kRingBudget = 200 * 1024;        // shared memory for the ring
+
+// A stage holds the 16 weight row slices plus room for NR activation slices, so
+// a smaller row cap leaves room for more stages (more bytes in flight).
+template <int NR>
+struct Ring {
+  static constexpr int kStageBytes = (kWRows + NR) * kSliceBytes;
+  static constexpr int kStages = kRingBudget / kStageBytes < 8 ? kRingBudget / kStageBytes : 8;
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kBarOffset + 256;
+};
 
 union F2 {
   float2 f;
@@ -96,10 +104,11 @@ __device__ __forceinline__ const uint16_t* weight_row(const Item& it, int j) {
   return it.w0 + (size_t)c * it.K;
 }
 
-template <bool GU, int NR>
+template <bool GU, int NR, int RING>
 __device__ bool consume_item(const GemvPass& p, const Item& it, uint8_t* smem, uint64_t* full,
                              uint64_t* empty, volatile int* abort_flag, uint32_t& iter, int cw,
                              int lane, DevStatus* st) {
+  using G = Ring<RING>;
   float2 acc0[NR], acc1[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) acc0[r] = acc1[r] = make_float2(0.f, 0.f);
@@ -109,14 +118,14 @@ __device__ bool consume_item(const GemvPass& p, const Item& it, uint8_t* smem, u
   const int nsl = (it.K + kKS - 1) / kKS;
   for (int s = 0; s < nsl; ++s, ++iter) {
     if (*abort_flag) return false;
-    const int stage = iter % kStages;
-    const uint32_t par = (iter / kStages) & 1u;
+    const int stage = iter % G::kStages;
+    const uint32_t par = (iter / G::kStages) & 1u;
     if (!mbar_wait(smem_u32(&full[stage]), par)) {
       if (lane == 0) raise_status(st, kStTimeout, GU ? MOE_K_GEMV_GATE_UP : MOE_K_GEMV_DOWN);
       *abort_flag = 1;
       return false;
     }
-    const uint8_t* sbase = smem + (size_t)stage * kStageBytes;
+    const uint8_t* sbase = smem + (size_t)stage * G::kStageBytes;
     const uint4* wa = reinterpret_cast<const uint4*>(sbase + sa * kSliceBytes);
     const uint4* wb = reinterpret_cast<const uint4*>(sbase + sb * kSliceBytes);
     const uint4* xs = reinterpret_cast<const uint4*>(sbase + kWRows * kSliceBytes);
@@ -167,15 +176,16 @@ __device__ bool consume_item(const GemvPass& p, const Item& it, uint8_t* smem, u
   return true;
 }
 
-template <bool GU>
+template <bool GU, int NR>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvPass p, DevStatus* st) {
+  using G = Ring<NR>;
   extern __shared__ __align__(16) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffset);
-  uint64_t* empty = full + kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kBarOffset);
+  uint64_t* empty = full + G::kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + G::kStages);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < G::kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), kConsumerWarps);
     }
@@ -203,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvPass p, DevStatus
           ok = false;
           break;
         }
-        const int stage = iter % kStages;
-        const uint32_t par = (iter / kStages) & 1u;
+        const int stage = iter % G::kStages;
+        const uint32_t par = (iter / G::kStages) & 1u;
         if (!mbar_wait(smem_u32(&empty[stage]), par ^ 1u)) {
           if (lane == 0) raise_status(st, kStTimeout, GU ? MOE_K_GEMV_GATE_UP : MOE_K_GEMV_DOWN);
           *abort_flag = 1;
@@ -216,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvPass p, DevStatus
         const uint32_t bar = smem_u32(&full[stage]);
         if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(wrows + it.n) * bytes);
         __syncwarp();
-        const uint32_t sbase = smem_u32(smem + (size_t)stage * kStageBytes);
+        const uint32_t sbase = smem_u32(smem + (size_t)stage * G::kStageBytes);
         if (lane < kWRows) {
           if (wrow) bulk_g2s(sbase + lane * kSliceBytes, wrow + (size_t)s * kKS, bytes, bar, pol_w);
         } else if (lane - kWRows < it.n) {
@@ -229,9 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvPass p, DevStatus
     }
     // Drain: every issued copy lands before the CTA may exit.
     if (lane == 0) {
-      const uint32_t first = iter > (uint32_t)kStages ? iter - kStages : 0u;
+      const uint32_t first = iter > (uint32_t)G::kStages ? iter - G::kStages : 0u;
       for (uint32_t j = first; j < iter; ++j)
-        mbar_wait(smem_u32(&full[j % kStages]), (j / kStages) & 1u);
+        mbar_wait(smem_u32(&full[j % G::kStages]), (j / G::kStages) & 1u);
     }
     return;
   }
@@ -241,26 +251,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvPass p, DevStatus
     Item it;
     decode_item<GU>(p, item, ntasks, it);
     bool ok;
-    if (it.n <= 1)
-      ok = consume_item<GU, 1>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
-    else if (it.n <= 2)
-      ok = consume_item<GU, 2>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
-    else if (it.n <= 4)
-      ok = consume_item<GU, 4>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
+    if (NR == 1 || it.n <= 1)
+      ok = consume_item<GU, 1, NR>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
+    else if (NR == 2 || it.n <= 2)
+      ok = consume_item<GU, (NR < 2 ? NR : 2), NR>(p, it, smem, full, empty, abort_flag, iter, cw,
+                                                   lane, st);
+    else if (NR == 4 || it.n <= 4)
+      ok = consume_item<GU, (NR < 4 ? NR : 4), NR>(p, it, smem, full, empty, abort_flag, iter, cw,
+                                                   lane, st);
     else
-      ok = consume_item<GU, 8>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
+      ok = consume_item<GU, NR, NR>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
     if (!ok) break;
   }
 }
 
+template <bool GU, int NR>
+void launch_nr(const Launch& L, const GemvPass& p) {
+  using G = Ring<NR>;
+  const int kind = GU ? MOE_K_GEMV_GATE_UP : MOE_K_GEMV_DOWN;
+  const int nr_slot = NR == 1 ? 0 : NR == 2 ? 1 : NR == 4 ? 2 : 3;
+  set_smem_attr_once(reinterpret_cast<const void*>(gemv_kernel<GU, NR>), G::kSmemBytes,
+                     kAttrGemvBase + (GU ? 0 : 1) + 2 * nr_slot);
+  launch_begin(L, kind);
+  gemv_kernel<GU, NR><<<L.num_sms, kThreads, G::kSmemBytes, L.stream>>>(p, L.status);
+  launch_end(L, kind);
+}
+
 template <bool GU>
 void launch_gemv(const Launch& L, const GemvPass& p) {
-  const int kind = GU ? MOE_K_GEMV_GATE_UP : MOE_K_GEMV_DOWN;
-  set_smem_attr_once(reinterpret_cast<const void*>(gemv_kernel<GU>), kSmemBytes,
-                     GU ? kAttrGemvGU : kAttrGemvDN);
-  launch_begin(L, kind);
-  gemv_kernel<GU><<<L.num_sms, kThreads, kSmemBytes, L.stream>>>(p, L.status);
-  launch_end(L, kind);
+  switch (p.max_rows) {
+    case 1: launch_nr<GU, 1>(L, p); break;
+    case 2: launch_nr<GU, 2>(L, p); break;
+    case 4: launch_nr<GU, 4>(L, p); break;
+    default: launch_nr<GU, 8>(L, p); break;
+  }
 }
 
 }  // namespace

@@ -13,13 +13,35 @@ struct DevStatus;
 
 // One unit of grouped-FFN work: a contiguous run of sorted rows of one expert.
 // expert >= 0 indexes the routed weight stacks; expert == -1 is the shared
-// expert (its rows index the token matrix directly).
+// expert (its rows index the token matrix directly).  Tensor-core tasks carry
+// (chunk index << 16 | chunks of the same expert) in `chunk`.
 struct FfnTask {
   int32_t expert;
   int32_t row0;
   int32_t nrows;
-  int32_t pad;
+  int32_t chunk;
 };
+
+// Tensor-core tile -> (task, channel tile).  The tiles of one expert's tasks
+// form one contiguous range, enumerated channel tile outer, token chunk inner,
+// so the CTAs working on an expert at the same time read the same weight tile
+// (one HBM read, the rest from L2) instead of re-streaming it per chunk.
+__device__ __forceinline__ void tc_tile_of(const FfnTask* tasks, const int32_t* start,
+                                           int ntasks, int tile, int* task, int* ct) {
+  int lo = 0, hi = ntasks - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (start[mid] <= tile)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int c = tasks[lo].chunk;
+  const int first = lo - (c >> 16), nt = c & 0xffff;
+  const int u = tile - start[first];
+  *task = first + u % nt;
+  *ct = u / nt;
+}
 
 // Slots of the device work-list counter array.
 enum {
@@ -41,16 +63,22 @@ struct WorkList {
   int32_t* tc_start_dn;
   int32_t* counts;  // kWlCount ints
   int32_t capacity; // max tasks of each kind
+  int32_t* redo_gu; // W8A8 guard-failure lists (count word zeroed here), or nullptr
+  int32_t* redo_dn;
 };
 
 // Geometry of the streaming (GEMV) path.
-constexpr int kGemvMaxRows = 8;    // activation rows one GEMV task carries
+constexpr int kGemvMaxRows = 8;    // most activation rows one GEMV task carries
 constexpr int kGemvChGU = 8;       // output channels per gate/up item
 constexpr int kGemvChDN = 16;      // output channels per down item
 // Geometry of the tensor-core path (swap-AB: weights are M, tokens are N).
 constexpr int kTcM = 128;          // weight rows per tile
 constexpr int kTcMaxN = 128;       // token rows per task
-constexpr int kDefaultGemvMaxRows = 8;
+// Measured on GB300 (LongCat/DSv3/Pangu-shaped decode layers): tensor-core
+// tiles with N = 16 stream expert weights at ~6.9 TB/s, above the CUDA-core GEMV
+// at every row count (6.4 TB/s at one row, less with more), so by default every
+// unit takes the tensor-core path; gemv_max_rows > 0 selects the GEMV path.
+constexpr int kDefaultGemvMaxRows = 0;
 
 struct Launch {
   cudaStream_t stream;
@@ -58,11 +86,15 @@ struct Launch {
   DevStatus* status;
 };
 
-// Router + top-k (route.cu)
+// Router + top-k (route.cu).  With split-K (splits > 1) the router needs the
+// partial buffer [splits, T, E] and one counter per tile (router_tiles), which
+// must be zero before the first call; the kernel leaves them zero again.
+constexpr int kRouterCounterBytes = 3840;  // counters kept right after the status word
+int router_tiles(const moe_config& c, int T);
 int router_splits(const moe_config& c, int T, int num_sms);
 void launch_router(const Launch& L, const moe_config& c, int T, const void* x, const float* w_r,
-                   float* partial, int splits);
-void launch_topk(const Launch& L, const moe_config& c, int T, const float* partial, int splits,
+                   float* partial, int splits, float* logits, int* counters);
+void launch_topk(const Launch& L, const moe_config& c, int T, const float* logits,
                  const float* bias, int32_t* ids, float* w);
 
 // Permutation (permute.cu)
@@ -75,7 +107,7 @@ void launch_perm_scatter(const Launch& L, int T, int k, int E, const int32_t* id
 void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32_t* ids,
                         const int32_t* e2s, const void* x, void* x_perm, float* x_perm_scale);
 void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
-                     const WorkList& wl, int gemv_max_rows);
+                     const WorkList& wl, int gemv_max_rows, int gemv_chunk);
 
 // Grouped FFN, streaming path (gemv.cu)
 struct GemvPass {
@@ -95,6 +127,7 @@ struct GemvPass {
   float* sout_y;
   int K, Ks;              // reduction length, routed / shared
   int N, Ns;              // output channels, routed / shared
+  int max_rows;           // rows per task (1, 2, 4 or 8); the work list chunks by it
 };
 void launch_gemv_gate_up(const Launch& L, const GemvPass& p);
 void launch_gemv_down(const Launch& L, const GemvPass& p);
@@ -124,13 +157,52 @@ struct TcPass {
 bool launch_tc_gate_up(const Launch& L, const TcPass& p);
 bool launch_tc_down(const Launch& L, const TcPass& p);
 
+// W8A8 grouped FFN (w8a8.cu): tensor-core tiles on integer-valued fp16 operands
+// with an exactness guard, then an exact CUDA-core pass over guard failures.
+enum { kW8GateUp = 0, kW8Down = 1, kW8Raw = 2 };
+struct W8Pass {
+  int mode;                 // kW8GateUp: h = silu(g)*u (fp32); kW8Down: y (fp32);
+                            // kW8Raw: int32 accumulators
+  const FfnTask* tasks;
+  const int32_t* tile_start;
+  const int32_t* counts;
+  int task_slot, tile_slot;
+  const void* w0;           // int8 weights [n_experts, N, K] (gate or down)
+  const void* w1;           // int8 up weights (gate/up mode)
+  int n_experts;
+  const float* s0;          // per-channel scales [n_experts, N]
+  const float* s1;
+  const void* act;          // integer-valued fp16 activation rows [act_rows, K]
+  int64_t act_rows;
+  const int32_t* row_norm2; // [act_rows] sum of squared codes
+  const float* row_scale;   // [act_rows]
+  float* out_f32;
+  int32_t* out_i32;
+  int32_t* redo;            // [0] count (zeroed by the work-list kernel), [1..cap]
+  int redo_cap;
+  int K, N;
+};
+bool launch_w8a8(const Launch& L, const W8Pass& p);
+void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, int32_t* norm2,
+                           int R, int K, const int32_t* nrows);
+void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, float* scale,
+                       int32_t* norm2, int R, int K, const int32_t* nrows);
+
 // Combine (combine.cu)
 void launch_combine(const Launch& L, const moe_config& c, int T, const float* y_perm,
                     const int32_t* e2s, const int32_t* ids, const float* w, const void* x,
                     const float* shared_out, void* out);
 
 // Raise a kernel's dynamic shared-memory limit once per device (abi.cu).
-enum { kAttrTopk = 0, kAttrPermScatter, kAttrGemvGU, kAttrGemvDN, kAttrTcGU, kAttrTcDN, kAttrSlots };
+enum {
+  kAttrTopk = 0,
+  kAttrPermScatter,
+  kAttrTcGU,
+  kAttrTcDN,
+  kAttrGemvBase,                 // 8 slots: (gate/up, down) x row cap 1, 2, 4, 8
+  kAttrW8Base = kAttrGemvBase + 8,  // 3 slots: W8A8 modes
+  kAttrSlots = kAttrW8Base + 3
+};
 void set_smem_attr_once(const void* func, int bytes, int slot);
 
 // Per-launch bookkeeping (abi.cu): call before/after each kernel launch.

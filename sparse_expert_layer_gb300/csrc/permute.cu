@@ -180,12 +180,12 @@ __global__ void __launch_bounds__(256) perm_gather_kernel(GatherArgs a) {
 }
 
 // Work list of the grouped FFN.  Units are the routed experts in index order,
-// then the shared expert.  A unit with n rows becomes GEMV tasks of <= 8 rows
-// when n <= gemv_max, else tensor-core tasks of <= 128 rows.
+// then the shared expert.  A unit with n rows becomes GEMV tasks of <= gemv_chunk
+// rows when n <= gemv_max, else tensor-core tasks of <= 128 rows.
 struct WlArgs {
   const int32_t* offsets;
   WorkList wl;
-  int E_r, T, has_shared, gemv_max;
+  int E_r, T, has_shared, gemv_max, gemv_chunk;
   int items_gu, items_gu_shared, items_dn;        // GEMV items per task
   int tiles_gu, tiles_gu_shared, tiles_dn;        // tensor-core tiles per task
   DevStatus* status;
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
       shared = 1;
     }
     const bool gemv = n > 0 && n <= a.gemv_max;
-    const int n_gemv = gemv ? (n + kGemvMaxRows - 1) / kGemvMaxRows : 0;
+    const int n_gemv = gemv ? (n + a.gemv_chunk - 1) / a.gemv_chunk : 0;
     const int n_tc = (!gemv && n > 0) ? (n + kTcMaxN - 1) / kTcMaxN : 0;
     const int gi_gu = shared ? a.items_gu_shared : a.items_gu;
     const int ti_gu = shared ? a.tiles_gu_shared : a.tiles_gu;
@@ -251,9 +251,9 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
       }
       FfnTask tk;
       tk.expert = shared ? -1 : u;
-      tk.row0 = row0 + j * kGemvMaxRows;
-      tk.nrows = min(kGemvMaxRows, n - j * kGemvMaxRows);
-      tk.pad = 0;
+      tk.row0 = row0 + j * a.gemv_chunk;
+      tk.nrows = min(a.gemv_chunk, n - j * a.gemv_chunk);
+      tk.chunk = 0;
       a.wl.gemv_tasks[ti] = tk;
       a.wl.gemv_start_gu[ti] = pos[1] + j * gi_gu;
       a.wl.gemv_start_dn[ti] = pos[2] + j * a.items_dn;
@@ -268,13 +268,15 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
       tk.expert = shared ? -1 : u;
       tk.row0 = row0 + j * kTcMaxN;
       tk.nrows = min(kTcMaxN, n - j * kTcMaxN);
-      tk.pad = 0;
+      tk.chunk = (j << 16) | n_tc;  // chunk index, chunks of this unit (tile interleaving)
       a.wl.tc_tasks[ti] = tk;
       a.wl.tc_start_gu[ti] = pos[4] + j * ti_gu;
       a.wl.tc_start_dn[ti] = pos[5] + j * a.tiles_dn;
     }
   }
   if (threadIdx.x == 0) {
+    if (a.wl.redo_gu) a.wl.redo_gu[0] = 0;
+    if (a.wl.redo_dn) a.wl.redo_dn[0] = 0;
     a.wl.counts[kWlGemvTasks] = min(carry[0], a.wl.capacity);
     a.wl.counts[kWlGemvItemsGU] = carry[0] <= a.wl.capacity ? carry[1] : 0;
     a.wl.counts[kWlGemvItemsDN] = carry[0] <= a.wl.capacity ? carry[2] : 0;
@@ -332,7 +334,7 @@ void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32
 }
 
 void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
-                     const WorkList& wl, int gemv_max_rows) {
+                     const WorkList& wl, int gemv_max_rows, int gemv_chunk) {
   WlArgs a;
   a.offsets = offsets;
   a.wl = wl;
@@ -340,6 +342,7 @@ void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t*
   a.T = T;
   a.has_shared = c.shared_inter > 0;
   a.gemv_max = gemv_max_rows;
+  a.gemv_chunk = gemv_chunk;
   a.items_gu = (c.inter + kGemvChGU - 1) / kGemvChGU;
   a.items_gu_shared = (c.shared_inter + kGemvChGU - 1) / kGemvChGU;
   a.items_dn = (c.hidden + kGemvChDN - 1) / kGemvChDN;

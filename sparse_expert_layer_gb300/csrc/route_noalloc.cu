@@ -9,12 +9,13 @@
 // compiled into the library instead, so the caller passes x, the router
 // weights, the bias and the two outputs, and nothing is allocated.
 //
-// The array (kNoAllocScratchBytes of partial logits plus a 256-byte status
-// word) exists on every GPU that loads the library and stays there until the
-// process exits.  All calls on a device share it: two calls whose work
-// overlaps on that GPU (different streams, or different host threads) race on
-// it and may return wrong results.  The partials are fully rewritten by every
-// call; the status word is zeroed at the start of every call.
+// The array (4 MiB of logits and split-K partials after a 4 KB head: status
+// word and router tile counters) exists on every GPU that loads the library and
+// stays there until the process exits.  All calls on a device share it: two
+// calls whose work overlaps on that GPU (different streams, or different host
+// threads) race on it and may return wrong results.  Logits and partials are
+// fully rewritten by every call, the counters start at zero and the router
+// leaves them zero, and the status word is zeroed at the start of every call.
 #include <mutex>
 
 #include "common.cuh"
@@ -25,11 +26,14 @@ namespace moe {
 namespace {
 
 constexpr size_t kNoAllocStatusBytes = 256;
-constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;  // 4 MiB of fp32 partial logits
+constexpr size_t kNoAllocHeadBytes = kNoAllocStatusBytes + kRouterCounterBytes;
+constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;  // 4 MiB of fp32 logits + partials
 constexpr int kNoAllocMaxDevices = 64;
 constexpr int kRouterCtasPerSm = 152;  // same split-K choice as moe_route
 
-static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocStatusBytes +
+// Status word, router tile counters (zero at load time; the router leaves them
+// zero after every call), then final and split-K partial logits.
+static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocHeadBytes +
                                                                kNoAllocScratchBytes];
 
 std::mutex g_setup_mu;
@@ -73,8 +77,9 @@ extern "C" moe_status moe_route_noalloc(const moe_config* cfg, int32_t T, const 
   if (mis & 15u) return MOE_ERR_ALIGNMENT;
   const int E = cfg->n_routed + cfg->n_zero;
   const int splits = router_splits(*cfg, T, kRouterCtasPerSm);
-  const size_t partial_bytes = (size_t)splits * T * E * sizeof(float);
-  if (partial_bytes > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const size_t logit_bytes = (size_t)T * E * sizeof(float);
+  const size_t partial_bytes = splits > 1 ? (size_t)splits * logit_bytes : 0;
+  if (logit_bytes + partial_bytes > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
 
   void* base = nullptr;
   if ((s = scratch_for_current_device(&base)) != MOE_OK) return s;
@@ -86,10 +91,12 @@ extern "C" moe_status moe_route_noalloc(const moe_config* cfg, int32_t T, const 
     return MOE_ERR_CUDA;
   L.num_sms = sms;
   L.status = static_cast<DevStatus*>(base);
-  float* partial = reinterpret_cast<float*>(static_cast<unsigned char*>(base) +
-                                            kNoAllocStatusBytes);
+  unsigned char* b = static_cast<unsigned char*>(base);
+  int* counters = reinterpret_cast<int*>(b + kNoAllocStatusBytes);
+  float* logits = reinterpret_cast<float*>(b + kNoAllocHeadBytes);
+  float* partial = reinterpret_cast<float*>(b + kNoAllocHeadBytes + logit_bytes);
   if (cudaMemsetAsync(base, 0, kNoAllocStatusBytes, L.stream) != cudaSuccess) return MOE_ERR_CUDA;
-  launch_router(L, *cfg, T, x, w_router, partial, splits);
-  launch_topk(L, *cfg, T, partial, splits, bias, topk_ids, topk_w);
+  launch_router(L, *cfg, T, x, w_router, partial, splits, logits, counters);
+  launch_topk(L, *cfg, T, logits, bias, topk_ids, topk_w);
   return launch_status_take();
 }

@@ -64,6 +64,10 @@ CONFIGS = {
                      bias_mode="logit", bias_kind="iid", shared_inter=136),
     "w8a8_s": dict(_BASE, T=512, hidden=1024, inter=512, n_routed=32, top_k=8, wdtype="w8a8",
                    bias_mode="logit", bias_kind="zipf", router_std_scale=1.645),
+    # Profiling-sized LongCat relative: full H and I, ~2 rows per expert like the
+    # real layer, 4.8 GB of weights (well above the 129 MB L2, a few GB on device).
+    "longcat_prof": dict(_BASE, T=16, hidden=6144, inter=2048, n_routed=64, n_zero=32,
+                         top_k=12, bias_mode="logit", bias_kind="iid"),
 }
 
 # The five headline layers, in order.

@@ -67,11 +67,6 @@ def test_workspace_size_for_the_headline_layers(moe):
     for name in synth.HEADLINE:
         s = synth.spec(name)
         cfg = moe.config_from_spec(s)
-        if s["wdtype"] == "w8a8":
-            with pytest.raises(moe.MoeError) as e:
-                _ws(moe, cfg, s["T"])
-            assert e.value.status == moe.MOE_ERR_UNSUPPORTED
-            continue
         n1 = _ws(moe, cfg, s["T"])
         n2 = _ws(moe, cfg, 2 * s["T"])
         assert 0 < n1 < n2
@@ -114,6 +109,20 @@ def test_unsupported_sizes(moe):
     assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 16, ctypes.byref(n)) == 2
     cfg.top_k, cfg.n_routed = 2, 5000
     assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 16, ctypes.byref(n)) == 2
+
+
+def test_w8a8_rules(moe):
+    import synth
+
+    n = ctypes.c_size_t(0)
+    cfg = moe.config_from_spec(synth.spec("w8a8_s"))
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 512, ctypes.byref(n)) == 0
+    cfg.hidden = 1000  # int8 rows must be whole 16-byte vectors
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 512, ctypes.byref(n)) == 1
+    cfg = moe.config_from_spec(synth.spec("w8a8_s", shared_inter=64))
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 512, ctypes.byref(n)) == 2
+    assert moe.lib.moe_qgemm_s8_workspace_size(4, 1024, 256, 100, ctypes.byref(n)) == 0
+    assert moe.lib.moe_qgemm_s8_workspace_size(4, 1000, 256, 100, ctypes.byref(n)) == 1
 
 
 def test_workspace_errors_are_host_side(moe):

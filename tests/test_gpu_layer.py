@@ -26,12 +26,13 @@ def oracle_out(spec, d, x=None):
 
 @pytest.mark.parametrize("name", SMALL)
 @pytest.mark.parametrize("out_fp32", [True, False])
-def test_layer_matches_oracle(m, name, out_fp32):
+@pytest.mark.parametrize("gemv_max_rows", [0, 8])  # library default / streaming GEMV path
+def test_layer_matches_oracle(m, name, out_fp32, gemv_max_rows):
     spec = synth.spec(name)
     d = gs.inputs(spec)
     ref = oracle_out(spec, d)
-    got = gs.run_layer(m, spec, d, out_fp32=out_fp32)
-    gs.check_out(got, ref, bf16_out=not out_fp32, what=name)
+    got = gs.run_layer(m, spec, d, out_fp32=out_fp32, gemv_max_rows=gemv_max_rows)
+    gs.check_out(got, ref, bf16_out=not out_fp32, what=f"{name} gemv<={gemv_max_rows}")
 
 
 @pytest.mark.parametrize("gemv_max_rows", [1, 3, 1000])

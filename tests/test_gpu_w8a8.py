@@ -1,0 +1,155 @@
+"""W8A8 path: exact int32 accumulators, bit-exact activation codes, and whole-layer
+parity against the oracle's W8A8 layer."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import gpu_support as gs
+from tests import support
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def m():
+    return gs.lib()
+
+
+def qgemm(m, counts, a, w):
+    E, N, K = w.shape
+    R = a.shape[0]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    ws = torch.zeros(m.moe_qgemm_s8_workspace_size(E, K, N, R), dtype=torch.uint8, device="cuda")
+    acc = torch.full((R, N), -7, dtype=torch.int32, device="cuda")
+    m.moe_qgemm_s8(E, K, N, R, torch.as_tensor(offsets, device="cuda"),
+                   torch.as_tensor(a, device="cuda"), torch.as_tensor(w, device="cuda"), acc, ws)
+    torch.cuda.synchronize()
+    assert m.moe_check_device_status(ws) == m.MOE_OK
+    return acc.cpu().numpy(), offsets
+
+
+def qgemm_ref(offsets, a, w):
+    out = np.zeros((a.shape[0], w.shape[1]), np.int64)
+    for e in range(w.shape[0]):
+        r0, r1 = offsets[e], offsets[e + 1]
+        out[r0:r1] = a[r0:r1].astype(np.int64) @ w[e].astype(np.int64).T
+    return out
+
+
+def test_qgemm_exact_on_random_codes(m):
+    rng = np.random.default_rng(21)
+    counts = [0, 1, 37, 128, 200]
+    K, N = 1024, 384
+    a = rng.integers(-127, 128, size=(sum(counts), K)).astype(np.int8)
+    w = rng.integers(-128, 128, size=(len(counts), N, K)).astype(np.int8)
+    acc, off = qgemm(m, counts, a, w)
+    assert np.array_equal(acc.astype(np.int64), qgemm_ref(off, a, w))
+
+
+def test_qgemm_exact_past_the_fp32_integer_range(m):
+    # all-+-127 codes over K = 7168: partial sums reach 1.2e8 > 2^24, so these
+    # tiles fail the tensor-core exactness guard and take the integer path
+    rng = np.random.default_rng(22)
+    counts = [40, 3, 90]
+    K, N = 7168, 256
+    a = (127 * rng.choice([-1, 1], size=(sum(counts), K))).astype(np.int8)
+    a[:10] = 127
+    w = (127 * rng.choice([-1, 1], size=(len(counts), N, K))).astype(np.int8)
+    w[0, :5] = 127
+    w[2, 7] = -128
+    acc, off = qgemm(m, counts, a, w)
+    ref = qgemm_ref(off, a, w)
+    assert ref.max() == 127 * 127 * K  # the extreme case is present
+    assert np.array_equal(acc.astype(np.int64), ref)
+
+
+def test_qgemm_ragged_k_and_n(m):
+    rng = np.random.default_rng(23)
+    counts = [17, 0, 130]
+    K, N = 1040, 200
+    a = rng.integers(-127, 128, size=(sum(counts), K)).astype(np.int8)
+    w = rng.integers(-128, 128, size=(len(counts), N, K)).astype(np.int8)
+    acc, off = qgemm(m, counts, a, w)
+    assert np.array_equal(acc.astype(np.int64), qgemm_ref(off, a, w))
+
+
+def test_activation_codes_match_oracle_bit_for_bit(m):
+    spec = synth.spec("w8a8_s")
+    d = gs.inputs(spec)
+    T, k, H = spec["T"], spec["top_k"], spec["hidden"]
+    E = synth.n_experts(spec)
+    ids_o, _, _, _ = oracle.route(spec, synth.bf16_bits(d["x"]), d["w_r"].numpy(),
+                                  support.np_bias(d["bias"]))
+    cfg = m.config_from_spec(spec)
+    ids = torch.as_tensor(ids_o, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    s2e = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    e2s = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    xq = torch.zeros((T * k, H), dtype=torch.int8, device="cuda")
+    sx = torch.zeros(T * k, dtype=torch.float32, device="cuda")
+    ws = m.workspace(cfg, T)
+    m.moe_permute(cfg, T, ids, d["x_d"], counts, offsets, s2e, e2s, xq, sx, ws)
+    torch.cuda.synchronize()
+    q_o, s_o = oracle.quantize_rows(d["x"].float().numpy())
+    s2e = s2e.cpu().numpy()
+    rows = s2e[:T * k] // k
+    assert np.array_equal(xq.cpu().numpy(), q_o[rows])
+    assert np.array_equal(sx.cpu().numpy(), s_o[rows])
+
+
+def w8_lists(wts, experts=None):
+    E = wts["w_gate"].shape[0]
+    want = set(range(E)) if experts is None else set(int(e) for e in experts)
+    out = {k: [] for k in ("qg", "sg", "qu", "su", "qd", "sd")}
+    for e in range(E):
+        ok = e in want
+        for key, name in (("qg", "w_gate"), ("qu", "w_up"), ("qd", "w_down")):
+            out[key].append(wts[name][e].cpu().numpy() if ok else None)
+        for key, name in (("sg", "s_gate"), ("su", "s_up"), ("sd", "s_down")):
+            out[key].append(wts[name][e].cpu().numpy() if ok else None)
+    return out
+
+
+@pytest.mark.parametrize("out_fp32", [True, False])
+def test_w8a8_layer_matches_oracle(m, out_fp32):
+    spec = synth.spec("w8a8_s")
+    d = gs.inputs(spec)
+    L = w8_lists(d["wts"])
+    ref, _, _, _, _ = oracle.layer_w8a8(spec, synth.bf16_bits(d["x"]), d["w_r"].numpy(),
+                                        support.np_bias(d["bias"]), L["qg"], L["sg"], L["qu"],
+                                        L["su"], L["qd"], L["sd"])
+    got = gs.run_layer(m, spec, d, out_fp32=out_fp32)
+    gs.check_out(got, ref, bf16_out=not out_fp32, what="w8a8_s")
+
+
+def test_w8a8_full_size_prefill(m):
+    spec = synth.spec("w8a8_prefill")
+    x, w_r, bias, _ = support.make_inputs(spec)
+    wts_d = synth.draw_weights(spec, device="cuda")
+    d = dict(x=x, w_r=w_r, bias=bias, x_d=x.cuda(), w_r_d=w_r.cuda(), bias_d=bias.cuda(),
+             wts_d=wts_d)
+    T, k = spec["T"], spec["top_k"]
+    cfg = m.config_from_spec(spec)
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wgt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = m.workspace(cfg, T)
+    m.moe_route(cfg, T, d["x_d"], d["w_r_d"], d["bias_d"], ids, wgt, ws)
+    torch.cuda.synchronize()
+    ids_o, w_o, _, _ = oracle.route(spec, synth.bf16_bits(x), w_r.numpy(), bias.numpy())
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    loads = np.bincount(ids_o.reshape(-1), minlength=spec["n_routed"])
+    assert loads.max() >= 10 * loads.mean()  # Zipf skew: hot experts well above the mean
+    out = gs.run_layer(m, spec, d, out_fp32=False)
+    rng = np.random.default_rng(3)
+    sample = np.sort(rng.choice(T, 3, replace=False))
+    L = w8_lists(wts_d, set(ids_o[sample].reshape(-1)))
+    ref, ids_s, _, _, _ = oracle.layer_w8a8(spec, synth.bf16_bits(x[sample]), w_r.numpy(),
+                                            bias.numpy(), L["qg"], L["sg"], L["qu"], L["su"],
+                                            L["qd"], L["sd"])
+    assert np.array_equal(ids_s, ids_o[sample])
+    gs.check_out(out[torch.as_tensor(sample, device="cuda")], ref, bf16_out=True, what="prefill")
+    del wts_d, d
+    torch.cuda.empty_cache()
