@@ -212,6 +212,14 @@ moe_status moe_check_device_status(void* ws, moe_stream_t stream);
 
 /* ---- Diagnostics ---- */
 
+/* Exercises the device-side failure path without faulting the GPU: one thread
+ * waits on a barrier that nothing completes, gives up after `limit_cycles` SM
+ * cycles (1 .. 2e9), records MOE_ERR_DEVICE_TIMEOUT in the status word of `ws`
+ * (>= 256 bytes, 256-byte aligned, first 8 bytes zero) and returns.  Every
+ * bounded wait of the library reports a timeout the same way; read it with
+ * moe_check_device_status. */
+moe_status moe_selftest_wait_timeout(void* ws, int64_t limit_cycles, moe_stream_t stream);
+
 /* Kernels of the library, for timing and launch counts. */
 typedef enum {
   MOE_K_ROUTER = 0,

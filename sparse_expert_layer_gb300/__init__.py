@@ -81,6 +81,7 @@ _SIGS = {
     "moe_route_noalloc": [_C, _I, _P, _P, _P, _P, _P, _P],
     "moe_qgemm_s8_workspace_size": [_I, _I, _I, _I, ctypes.POINTER(_SZ)],
     "moe_qgemm_s8": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P],
+    "moe_selftest_wait_timeout": [_P, ctypes.c_int64, _P],
     "moe_timing_enable": [_I],
     "moe_timing_collect": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_I), _I],
     "moe_launch_counts": [ctypes.POINTER(ctypes.c_int64), _I],
@@ -207,6 +208,12 @@ def moe_qgemm_s8(n_experts, K, N, R, offsets, a, w, acc, ws, stream=None):
 def moe_check_device_status(ws, stream=None) -> int:
     """Status code (MOE_OK / MOE_ERR_DEVICE_CHECK / MOE_ERR_DEVICE_TIMEOUT); clears it."""
     return lib.moe_check_device_status(_ptr(ws), _stream(stream))
+
+
+def moe_selftest_wait_timeout(ws, limit_cycles: int, stream=None):
+    """Launch a wait that runs out after `limit_cycles` and records a timeout in `ws`."""
+    _check(lib.moe_selftest_wait_timeout(_ptr(ws), int(limit_cycles), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def timing_enable(on: bool = True):

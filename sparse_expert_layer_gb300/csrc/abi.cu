@@ -758,6 +758,17 @@ moe_status moe_check_device_status(void* ws, moe_stream_t stream) {
   return (h.bits & kStTimeout) ? MOE_ERR_DEVICE_TIMEOUT : MOE_ERR_DEVICE_CHECK;
 }
 
+moe_status moe_selftest_wait_timeout(void* ws, int64_t limit_cycles, moe_stream_t stream) {
+  if (!ws || limit_cycles < 1 || limit_cycles > kWaitCycles) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return MOE_ERR_ALIGNMENT;
+  Launch ln;
+  ln.stream = reinterpret_cast<cudaStream_t>(stream);
+  ln.num_sms = sm_count(current_device());
+  ln.status = at<DevStatus>(ws, 0);
+  launch_wait_timeout_selftest(ln, limit_cycles);
+  return finish();
+}
+
 moe_status moe_timing_enable(int32_t enable) {
   g_timing.store(enable != 0);
   return MOE_OK;

@@ -104,4 +104,24 @@ void launch_combine(const Launch& L, const moe_config& c, int T, const float* y_
   launch_end(L, MOE_K_COMBINE);
 }
 
+namespace {
+// One thread waits on an mbarrier that nothing arrives on, with the given
+// cycle limit: the wait runs out, the status word records a timeout, and the
+// kernel returns normally (the context stays usable).
+__global__ void wait_timeout_selftest_kernel(DevStatus* st, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_barrier_init();
+  if (!mbar_wait_limit(b, 0, limit)) raise_status(st, kStTimeout, MOE_K_COMBINE);
+}
+}  // namespace
+
+void launch_wait_timeout_selftest(const Launch& L, long long limit_cycles) {
+  launch_begin(L, MOE_K_COMBINE);
+  wait_timeout_selftest_kernel<<<1, 32, 0, L.stream>>>(L.status, limit_cycles);
+  launch_end(L, MOE_K_COMBINE);
+}
+
 }  // namespace moe

@@ -193,6 +193,9 @@ void launch_combine(const Launch& L, const moe_config& c, int T, const float* y_
                     const int32_t* e2s, const int32_t* ids, const float* w, const void* x,
                     const float* shared_out, void* out);
 
+// Failure-path self-test (combine.cu): a bounded wait that is never satisfied.
+void launch_wait_timeout_selftest(const Launch& L, long long limit_cycles);
+
 // Raise a kernel's dynamic shared-memory limit once per device (abi.cu).
 enum {
   kAttrTopk = 0,

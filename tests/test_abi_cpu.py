@@ -169,3 +169,11 @@ def test_status_strings(moe):
         assert moe.lib.moe_status_string(s)
     assert moe.lib.moe_kernel_name(0) == b"router"
     assert moe.lib.moe_kernel_name(99) == b"unknown"
+
+
+def test_selftest_arguments_are_checked_on_the_host(moe):
+    fake = 1 << 40
+    assert moe.lib.moe_selftest_wait_timeout(None, 1000, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.lib.moe_selftest_wait_timeout(fake, 0, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.lib.moe_selftest_wait_timeout(fake, 3_000_000_000, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.lib.moe_selftest_wait_timeout(fake + 16, 1000, None) == moe.MOE_ERR_ALIGNMENT

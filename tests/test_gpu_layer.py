@@ -52,6 +52,42 @@ def test_layer_is_deterministic(m):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("name", ["dsv3_s", "w8a8_s"])
+def test_layer_replays_from_a_cuda_graph(m, name):
+    # The layer is stream-ordered with no host synchronisation, so one capture
+    # replays it: the replay on new inputs matches a direct call bit for bit.
+    spec = synth.spec(name)
+    d = gs.inputs(spec)
+    cfg = m.config_from_spec(spec, out_fp32=True)
+    T, H = spec["T"], spec["hidden"]
+    w = d["wts_d"]
+    x = d["x_d"].clone()
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ws = m.workspace(cfg, T)
+
+    def call(stream):
+        m.moe_layer_forward(cfg, T, x, d["w_r_d"], d["bias_d"], w.get("w_gate"), w.get("w_up"),
+                            w.get("w_down"), w.get("s_gate"), w.get("s_up"), w.get("s_down"),
+                            w.get("shared_gate"), w.get("shared_up"), w.get("shared_down"), out,
+                            ws, stream=stream)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call(s)  # first call outside capture: per-device set-up happens here
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(s)
+    x.copy_(torch.flip(d["x_d"], [0]))
+    g.replay()
+    torch.cuda.synchronize()
+    assert m.moe_check_device_status(ws) == m.MOE_OK
+    replayed = out.clone()
+    direct = gs.run_layer(m, spec, d, out_fp32=True, x=x.clone())
+    assert torch.equal(replayed, direct)
+
+
 def test_single_token_and_empty_batch(m):
     spec = synth.spec("ragged_s")
     d = gs.inputs(spec)
