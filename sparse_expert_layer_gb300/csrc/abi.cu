@@ -174,9 +174,12 @@ Layout make_layout(const moe_config& c, int T) {
   L.wl_tc_gu = take((size_t)L.wl_cap * 4);
   L.wl_tc_dn = take((size_t)L.wl_cap * 4);
   L.wl_counts = take(kWlCount * 4);
-  L.x_perm = take(R * H * xb);
+  // W8A8 layers quantise straight into x16 and keep h in fp32 (h32), so the
+  // int8 x_perm and the bf16 h are bf16-path buffers only
+  const bool w8 = c.wdtype == MOE_W8A8;
+  L.x_perm = take(w8 ? 0 : R * H * xb);
   L.x_scale = take(R * 4);
-  L.h = take(R * I * 2);
+  L.h = take(w8 ? 0 : R * I * 2);
   L.y = take(R * H * 4);
   L.h_s = take((size_t)T * Is * 2);
   L.y_s = take(Is > 0 ? (size_t)T * H * 4 : 0);
@@ -257,7 +260,7 @@ void run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, 
   launch_perm_count(ln, T, c.top_k, E, ids, bc);
   launch_perm_scan(ln, T, E, bc, counts, offsets);
   launch_perm_scatter(ln, T, c.top_k, E, ids, bc, s2e, e2s);
-  launch_perm_gather(ln, c, T, ids, e2s, x, x_perm, x_scale);
+  if (x_perm) launch_perm_gather(ln, c, T, ids, e2s, x, x_perm, x_scale);
 }
 
 // Grouped FFN over the sorted rows plus (optionally) the shared expert.
@@ -271,7 +274,7 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   if (!shared) cw.shared_inter = 0;
   const int gemv_max = effective_gemv_max(c);
   const int chunk = gemv_chunk(gemv_max);
-  launch_worklist(ln, cw, T, offsets, wl, gemv_max, chunk);
+  launch_worklist(ln, cw, T, offsets, wl, gemv_max, chunk, kTcMaxN);
   uint16_t* h = at<uint16_t>(ws, L.h);
   uint16_t* h_s = at<uint16_t>(ws, L.h_s);
 
@@ -358,7 +361,9 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   return MOE_OK;
 }
 
-// W8A8 grouped FFN over the sorted rows (int8 codes + per-row scales).
+// W8A8 grouped FFN over the sorted rows (int8 codes + per-row scales).  With
+// x_perm == nullptr the codes are already in the workspace's x16 rows (with
+// their norms and scales), as the layer path's quantising gather leaves them.
 moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
                         const int32_t* offsets, const void* x_perm, const float* x_scale,
                         const void* w_gate, const void* w_up, const void* w_down,
@@ -367,7 +372,7 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   const WorkList wl = worklist_view(ws, L);
   moe_config cw = c;
   cw.shared_inter = 0;
-  launch_worklist(ln, cw, T, offsets, wl, 0, 1);  // every expert on tensor-core tiles
+  launch_worklist(ln, cw, T, offsets, wl, 0, 1, kW8MaxN);  // every expert on tensor-core tiles
   const int64_t R = (int64_t)T * c.top_k;
   const int32_t* n_real = offsets + c.n_routed;   // rows that belong to FFN experts
   uint16_t* x16 = at<uint16_t>(ws, L.x16);
@@ -376,7 +381,9 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   uint16_t* hq16 = at<uint16_t>(ws, L.hq16);
   float* hsc = at<float>(ws, L.hsc);
   int32_t* hn2 = at<int32_t>(ws, L.hn2);
-  launch_i8_rows_to_f16(ln, static_cast<const int8_t*>(x_perm), x16, xn2, (int)R, c.hidden, n_real);
+  if (x_perm)
+    launch_i8_rows_to_f16(ln, static_cast<const int8_t*>(x_perm), x16, xn2, (int)R, c.hidden,
+                          n_real);
 
   W8Pass g{};
   g.mode = kW8GateUp;
@@ -619,12 +626,15 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* s2e = at<int32_t>(ws, L.s2e);
   int32_t* e2s = at<int32_t>(ws, L.e2s);
-  void* x_perm = at<void>(ws, L.x_perm);
+  void* x_perm = w8 ? nullptr : at<void>(ws, L.x_perm);
   float* x_scale = at<float>(ws, L.x_scale);
   float* y = at<float>(ws, L.y);
   float* y_s = c.shared_inter > 0 ? at<float>(ws, L.y_s) : nullptr;
   run_route(ln, c, T, L, ws, x, w_router, bias, ids, w);
   run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale);
+  if (w8 && c.n_routed > 0)
+    launch_quant_gather(ln, c, T, x, ids, e2s, at<uint16_t>(ws, L.x16), x_scale,
+                        at<int32_t>(ws, L.xn2));
   moe_status fs = MOE_OK;
   if (w8 && c.n_routed > 0)
     fs = run_ffn_w8a8(ln, c, T, L, ws, offsets, x_perm, x_scale, w_gate, w_up, w_down, s_gate,
@@ -718,7 +728,7 @@ moe_status moe_qgemm_s8(int32_t n_experts, int32_t K, int32_t N, int32_t R, cons
   c.n_routed = n_experts;
   c.top_k = 1;
   c.n_group = 1;
-  launch_worklist(ln, c, R, offsets, wl, 0, 1);
+  launch_worklist(ln, c, R, offsets, wl, 0, 1, kW8MaxN);
   uint16_t* a16 = at<uint16_t>(ws, Q.a16);
   int32_t* an2 = at<int32_t>(ws, Q.an2);
   launch_i8_rows_to_f16(ln, static_cast<const int8_t*>(a), a16, an2, R, K, offsets + n_experts);

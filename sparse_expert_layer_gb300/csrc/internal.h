@@ -74,6 +74,7 @@ constexpr int kGemvChDN = 16;      // output channels per down item
 // Geometry of the tensor-core path (swap-AB: weights are M, tokens are N).
 constexpr int kTcM = 128;          // weight rows per tile
 constexpr int kTcMaxN = 128;       // token rows per task
+constexpr int kW8MaxN = 256;       // token rows per W8A8 task
 // Measured on GB300 (LongCat/DSv3/Pangu-shaped decode layers): tensor-core
 // tiles with N = 16 stream expert weights at ~6.9 TB/s, above the CUDA-core GEMV
 // at every row count (6.4 TB/s at one row, less with more), so by default every
@@ -107,7 +108,7 @@ void launch_perm_scatter(const Launch& L, int T, int k, int E, const int32_t* id
 void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32_t* ids,
                         const int32_t* e2s, const void* x, void* x_perm, float* x_perm_scale);
 void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
-                     const WorkList& wl, int gemv_max_rows, int gemv_chunk);
+                     const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk);
 
 // Grouped FFN, streaming path (gemv.cu)
 struct GemvPass {
@@ -185,6 +186,11 @@ struct W8Pass {
 bool launch_w8a8(const Launch& L, const W8Pass& p);
 void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, int32_t* norm2,
                            int R, int K, const int32_t* nrows);
+// Layer path: quantise each token once and write its codes (integer-valued
+// fp16), scale and sum of squares to the sorted rows of its FFN-expert picks.
+void launch_quant_gather(const Launch& L, const moe_config& c, int T, const void* x,
+                         const int32_t* ids, const int32_t* e2s, uint16_t* x16, float* scale,
+                         int32_t* norm2);
 void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, float* scale,
                        int32_t* norm2, int R, int K, const int32_t* nrows);
 

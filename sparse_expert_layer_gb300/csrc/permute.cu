@@ -181,11 +181,11 @@ __global__ void __launch_bounds__(256) perm_gather_kernel(GatherArgs a) {
 
 // Work list of the grouped FFN.  Units are the routed experts in index order,
 // then the shared expert.  A unit with n rows becomes GEMV tasks of <= gemv_chunk
-// rows when n <= gemv_max, else tensor-core tasks of <= 128 rows.
+// rows when n <= gemv_max, else tensor-core tasks of <= tc_chunk rows.
 struct WlArgs {
   const int32_t* offsets;
   WorkList wl;
-  int E_r, T, has_shared, gemv_max, gemv_chunk;
+  int E_r, T, has_shared, gemv_max, gemv_chunk, tc_chunk;
   int items_gu, items_gu_shared, items_dn;        // GEMV items per task
   int tiles_gu, tiles_gu_shared, tiles_dn;        // tensor-core tiles per task
   DevStatus* status;
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
     }
     const bool gemv = n > 0 && n <= a.gemv_max;
     const int n_gemv = gemv ? (n + a.gemv_chunk - 1) / a.gemv_chunk : 0;
-    const int n_tc = (!gemv && n > 0) ? (n + kTcMaxN - 1) / kTcMaxN : 0;
+    const int n_tc = (!gemv && n > 0) ? (n + a.tc_chunk - 1) / a.tc_chunk : 0;
     const int gi_gu = shared ? a.items_gu_shared : a.items_gu;
     const int ti_gu = shared ? a.tiles_gu_shared : a.tiles_gu;
     int v[6] = {n_gemv, n_gemv * gi_gu, n_gemv * a.items_dn, n_tc, n_tc * ti_gu, n_tc * a.tiles_dn};
@@ -266,8 +266,8 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
       }
       FfnTask tk;
       tk.expert = shared ? -1 : u;
-      tk.row0 = row0 + j * kTcMaxN;
-      tk.nrows = min(kTcMaxN, n - j * kTcMaxN);
+      tk.row0 = row0 + j * a.tc_chunk;
+      tk.nrows = min(a.tc_chunk, n - j * a.tc_chunk);
       tk.chunk = (j << 16) | n_tc;  // chunk index, chunks of this unit (tile interleaving)
       a.wl.tc_tasks[ti] = tk;
       a.wl.tc_start_gu[ti] = pos[4] + j * ti_gu;
@@ -334,7 +334,7 @@ void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32
 }
 
 void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
-                     const WorkList& wl, int gemv_max_rows, int gemv_chunk) {
+                     const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk) {
   WlArgs a;
   a.offsets = offsets;
   a.wl = wl;
@@ -343,6 +343,7 @@ void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t*
   a.has_shared = c.shared_inter > 0;
   a.gemv_max = gemv_max_rows;
   a.gemv_chunk = gemv_chunk;
+  a.tc_chunk = tc_chunk;
   a.items_gu = (c.inter + kGemvChGU - 1) / kGemvChGU;
   a.items_gu_shared = (c.shared_inter + kGemvChGU - 1) / kGemvChGU;
   a.items_dn = (c.hidden + kGemvChDN - 1) / kGemvChDN;

@@ -16,13 +16,19 @@
 // fails it to an exact CUDA-core integer kernel, so results are exact for all
 // inputs.
 //
-// Tensor-core kernel: persistent CTAs, warp-specialised like the bf16 path, plus
-// four converter warps that turn each TMA'd int8 weight tile into the 128-byte
-// swizzled fp16 layout the MMA reads (and sum squares with dp4a).
-//   warp 0    : TMA producer (int8 weight tiles, fp16 activation boxes)
+// Tensor-core kernel: persistent CTAs, tiles of 128 output channels x up to 256
+// token rows, warp-specialised around three shared-memory rings:
+//   raw ring   int8 weight tiles, written by TMA
+//   conv ring  the same tiles as 128-byte-swizzled integer-valued fp16, written
+//              by the converter warps (which also sum squares with dp4a)
+//   act ring   fp16 activation rows, written by TMA
+// so TMA, conversion and MMA each run ahead on their own ring.
+//   warp 0    : TMA producer (raw and act rings)
 //   warp 1    : TMEM allocation, MMA issue
 //   warps 2-5 : epilogue (dequantise, SwiGLU or store, guard)
 //   warps 6-9 : int8 -> fp16 converters
+// TMEM: gate/up keeps one accumulator pair (gate columns 0-255, up 256-511);
+// down and raw modes double-buffer 256-column accumulators.
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -40,25 +46,34 @@ constexpr int kThreads = 320;
 constexpr int kBK = 64;
 constexpr int kRawTileBytes = kTcM * kBK;        // 8 KB of int8
 constexpr int kF16TileBytes = kTcM * kBK * 2;    // 16 KB of fp16
-constexpr int kBTileBytes = kTcMaxN * kBK * 2;   // 16 KB
+constexpr int kActTileBytes = kW8MaxN * kBK * 2; // 32 KB
 constexpr int kBoxRows = 16;
 constexpr int kBoxBytes = kBoxRows * kBK * 2;
 constexpr long long kGuard = 1LL << 48;          // (2^24)^2
+constexpr int kAccCols = 256;                    // TMEM columns of one accumulator
 
 template <int MODE>
 struct Geom {
-  static constexpr int kNA = MODE == kW8GateUp ? 2 : 1;
-  static constexpr int kStageBytes = kNA * (kF16TileBytes + kRawTileBytes) + kBTileBytes;
-  static constexpr int kStages = MODE == kW8GateUp ? 3 : 5;
-  static constexpr int kTmemCols = MODE == kW8GateUp ? 512 : 256;
-  static constexpr int kAccStride = MODE == kW8GateUp ? 256 : 128;
-  // stage: [fp16 A tiles][B][int8 A tiles]
-  static constexpr int kBOff = kNA * kF16TileBytes;
-  static constexpr int kRawOff = kBOff + kBTileBytes;
+  static constexpr int kNA = MODE == kW8GateUp ? 2 : 1;     // weight matrices per tile
+  static constexpr int kSRaw = MODE == kW8GateUp ? 3 : 4;   // raw ring stages
+  static constexpr int kSAct = MODE == kW8GateUp ? 3 : 4;   // act ring stages
+  static constexpr int kSConv = 2;                          // conv ring stages
+  static constexpr int kAccBufs = MODE == kW8GateUp ? 1 : 2;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kConvBytes = kNA * kF16TileBytes;
+  static constexpr int kRawBytes = kNA * kRawTileBytes;
+  // [conv stages][act stages][raw stages][barriers][weight norms]; the first two
+  // hold 128-byte-swizzled tiles and stay 1024-byte aligned
+  static constexpr int kActOff = kSConv * kConvBytes;
+  static constexpr int kRawOff = kActOff + kSAct * kActTileBytes;
+  static constexpr int kBarOff = kRawOff + kSRaw * kRawBytes;
   static constexpr int kBarBytes = 512;
-  static constexpr int kNormBytes = 2 * 2 * kTcM * 4;  // [buf][matrix][row]
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kNormBytes;
+  static constexpr int kNormOff = kBarOff + kBarBytes;
+  static constexpr int kNormBytes = 2 * 2 * kTcM * 4;  // [buffer][matrix][channel]
+  static constexpr int kSmemBytes = 1024 + kNormOff + kNormBytes;
 };
+static_assert(Geom<kW8GateUp>::kSmemBytes <= 227 * 1024, "gate/up shared memory");
+static_assert(Geom<kW8Down>::kSmemBytes <= 227 * 1024, "down shared memory");
 
 struct Maps {
   CUtensorMap a0, a1;  // int8 weights [E][N][K]
@@ -95,18 +110,19 @@ __device__ __forceinline__ void decode(const Args& a, int tile, int ntasks, Tile
   t.e = tk.expert;
 }
 
-// One output element from its exact integer accumulator(s).
+// One output element from its exact integer accumulator(s); sw0/sw1 are the
+// channel's weight scales, sr the row's activation scale.
 template <int MODE>
-__device__ __forceinline__ void emit(const Args& a, int e, int row, int ch, int acc0, int acc1) {
+__device__ __forceinline__ void emit(const Args& a, int row, int ch, int acc0, int acc1, float sr,
+                                     float sw0, float sw1) {
   const size_t o = (size_t)row * a.N + ch;
   if (MODE == kW8Raw) {
     a.out_i32[o] = acc0;
     return;
   }
-  const float sr = a.row_scale[row];
-  const float v0 = (float)acc0 * sr * a.s0[(size_t)e * a.N + ch];
+  const float v0 = (float)acc0 * sr * sw0;
   if (MODE == kW8GateUp) {
-    const float v1 = (float)acc1 * sr * a.s1[(size_t)e * a.N + ch];
+    const float v1 = (float)acc1 * sr * sw1;
     a.out_f32[o] = v0 / (1.f + expf(-v0)) * v1;
   } else {
     a.out_f32[o] = v0;
@@ -126,10 +142,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kStages * G::kStageBytes);
-  uint64_t* conv = full + G::kStages;
-  uint64_t* empty = conv + G::kStages;
-  uint64_t* acc_full = empty + G::kStages;
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + G::kBarOff);
+  uint64_t* raw_empty = raw_full + G::kSRaw;
+  uint64_t* act_full = raw_empty + G::kSRaw;
+  uint64_t* act_empty = act_full + G::kSAct;
+  uint64_t* conv_full = act_empty + G::kSAct;
+  uint64_t* conv_empty = conv_full + G::kSConv;
+  uint64_t* acc_full = conv_empty + G::kSConv;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* norm_full = acc_empty + 2;
   uint64_t* norm_empty = norm_full + 2;
@@ -138,14 +157,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* tile_bad = abort_flag + 1;   // [2], per accumulator buffer
   volatile int* tile_done = abort_flag + 3;  // [2], epilogue warps finished
-  int32_t* wnorm = reinterpret_cast<int32_t*>(smem + G::kStages * G::kStageBytes + G::kBarBytes);
+  int32_t* wnorm = reinterpret_cast<int32_t*>(smem + G::kNormOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < G::kStages; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&conv[s]), 4);
-      mbar_init(smem_u32(&empty[s]), 1);
+    for (int s = 0; s < G::kSRaw; ++s) {
+      mbar_init(smem_u32(&raw_full[s]), 1);
+      mbar_init(smem_u32(&raw_empty[s]), 4);
+    }
+    for (int s = 0; s < G::kSAct; ++s) {
+      mbar_init(smem_u32(&act_full[s]), 1);
+      mbar_init(smem_u32(&act_empty[s]), 1);
+    }
+    for (int s = 0; s < G::kSConv; ++s) {
+      mbar_init(smem_u32(&conv_full[s]), 4);
+      mbar_init(smem_u32(&conv_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
@@ -169,50 +195,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------- producer --
     const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-    uint32_t iter = 0;
+    uint32_t n_raw = 0, n_act = 0;  // copies issued into each ring
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
       Tile t;
       decode(a, tile, ntasks, t);
       const int nb = (t.n + kBoxRows - 1) / kBoxRows;
-      const uint32_t bytes = (uint32_t)(NA * kRawTileBytes + nb * kBoxBytes);
       for (int ks = 0; ks < nks; ++ks) {
         if (*abort_flag) {
           ok = false;
           break;
         }
-        const int stage = iter % G::kStages;
-        const uint32_t par = (iter / G::kStages) & 1u;
-        if (!mbar_wait(smem_u32(&empty[stage]), par ^ 1u)) {
+        const int sr = n_raw % G::kSRaw;
+        if (!mbar_wait(smem_u32(&raw_empty[sr]), ((n_raw / G::kSRaw) & 1u) ^ 1u)) {
           raise_status(a.status, kStTimeout, kind);
           *abort_flag = 1;
           ok = false;
           break;
         }
-        const uint32_t bar = smem_u32(&full[stage]);
-        mbar_arrive_expect_tx(bar, bytes);
-        uint8_t* st = smem + (size_t)stage * G::kStageBytes;
-        tma_load_3d(smem_u32(st + G::kRawOff), &maps.a0, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
-        if (NA == 2)
-          tma_load_3d(smem_u32(st + G::kRawOff + kRawTileBytes), &maps.a1, ks * kBK, t.ct * kTcM,
-                      t.e, bar, pol_w);
+        uint32_t bar = smem_u32(&raw_full[sr]);
+        mbar_arrive_expect_tx(bar, G::kRawBytes);
+        const uint32_t raw = smem_u32(smem + G::kRawOff + sr * G::kRawBytes);
+        tma_load_3d(raw, &maps.a0, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
+        if (NA == 2) tma_load_3d(raw + kRawTileBytes, &maps.a1, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
+        ++n_raw;
+        const int sa = n_act % G::kSAct;
+        if (!mbar_wait(smem_u32(&act_empty[sa]), ((n_act / G::kSAct) & 1u) ^ 1u)) {
+          raise_status(a.status, kStTimeout, kind);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        bar = smem_u32(&act_full[sa]);
+        mbar_arrive_expect_tx(bar, (uint32_t)(nb * kBoxBytes));
+        const uint32_t act = smem_u32(smem + G::kActOff + sa * kActTileBytes);
         for (int j = 0; j < nb; ++j)
-          tma_load_3d(smem_u32(st + G::kBOff + j * kBoxBytes), &maps.b, ks * kBK,
-                      t.row0 + j * kBoxRows, 0, bar, pol_x);
-        ++iter;
+          tma_load_3d(act + j * kBoxBytes, &maps.b, ks * kBK, t.row0 + j * kBoxRows, 0, bar, pol_x);
+        ++n_act;
       }
     }
-    const uint32_t first = iter > (uint32_t)G::kStages ? iter - G::kStages : 0u;
-    for (uint32_t j = first; j < iter; ++j)
-      mbar_wait(smem_u32(&full[j % G::kStages]), (j / G::kStages) & 1u);
+    // every issued copy lands before the CTA can exit
+    for (uint32_t j = n_raw > (uint32_t)G::kSRaw ? n_raw - G::kSRaw : 0u; j < n_raw; ++j)
+      mbar_wait(smem_u32(&raw_full[j % G::kSRaw]), (j / G::kSRaw) & 1u);
+    for (uint32_t j = n_act > (uint32_t)G::kSAct ? n_act - G::kSAct : 0u; j < n_act; ++j)
+      mbar_wait(smem_u32(&act_full[j % G::kSAct]), (j / G::kSAct) & 1u);
   } else if (warp == 1 && lane == 0) {
     // --------------------------------------------------------- MMA issuer --
-    uint32_t iter = 0, local = 0;
+    uint32_t it = 0, local = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++local) {
       Tile t;
       decode(a, tile, ntasks, t);
-      const uint32_t buf = local & 1u, use = local >> 1;
+      const uint32_t buf = local % G::kAccBufs, use = local / G::kAccBufs;
       if (!mbar_wait(smem_u32(&acc_empty[buf]), (use & 1u) ^ 1u)) {
         raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
@@ -220,33 +254,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t idesc = idesc_f16_f32(kTcM, (uint32_t)((t.n + 15) / 16 * 16));
-      const uint32_t d0 = tmem + buf * G::kAccStride;
-      for (int ks = 0; ks < nks; ++ks) {
+      const uint32_t d0 = tmem + buf * kAccCols;
+      for (int ks = 0; ks < nks; ++ks, ++it) {
         if (*abort_flag) {
           ok = false;
           break;
         }
-        const int stage = iter % G::kStages;
-        const uint32_t par = (iter / G::kStages) & 1u;
-        if (!mbar_wait(smem_u32(&full[stage]), par) || !mbar_wait(smem_u32(&conv[stage]), par)) {
+        const int sc = it % G::kSConv, sa = it % G::kSAct;
+        if (!mbar_wait(smem_u32(&conv_full[sc]), (it / G::kSConv) & 1u) ||
+            !mbar_wait(smem_u32(&act_full[sa]), (it / G::kSAct) & 1u)) {
           raise_status(a.status, kStTimeout, kind);
           *abort_flag = 1;
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + (size_t)stage * G::kStageBytes);
-        const uint32_t sb = sa + G::kBOff;
+        const uint32_t wa = smem_u32(smem + sc * G::kConvBytes);
+        const uint32_t xb = smem_u32(smem + G::kActOff + sa * kActTileBytes);
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k) {
-          const uint64_t bdesc = sdesc_sw128(sb + k * 32);
+          const uint64_t bdesc = sdesc_sw128(xb + k * 32);
           const uint32_t acc = (ks > 0 || k > 0) ? 1u : 0u;
-          tc_mma_bf16(d0, sdesc_sw128(sa + k * 32), bdesc, idesc, acc);
+          tc_mma_bf16(d0, sdesc_sw128(wa + k * 32), bdesc, idesc, acc);
           if (NA == 2)
-            tc_mma_bf16(d0 + kTcMaxN, sdesc_sw128(sa + kF16TileBytes + k * 32), bdesc, idesc, acc);
+            tc_mma_bf16(d0 + kAccCols, sdesc_sw128(wa + kF16TileBytes + k * 32), bdesc, idesc, acc);
         }
-        tc_commit(smem_u32(&empty[stage]));
-        ++iter;
+        tc_commit(smem_u32(&conv_empty[sc]));
+        tc_commit(smem_u32(&act_empty[sa]));
       }
       if (!ok) break;
       tc_commit(smem_u32(&acc_full[buf]));
@@ -258,8 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 6) {
     // ---------------------------------------------------------- converter --
     const int ti = threadIdx.x - 6 * 32;  // 0..127
-    const int cw = warp - 6;
-    uint32_t iter = 0, local = 0;
+    uint32_t it = 0, local = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
       if (*abort_flag) break;
       int32_t nrm[NA][4];
@@ -268,24 +301,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) nrm[m][i] = 0;
       bool ok = true;
-      for (int ks = 0; ks < nks; ++ks, ++iter) {
+      for (int ks = 0; ks < nks; ++ks, ++it) {
         if (*abort_flag) {
           ok = false;
           break;
         }
-        const int stage = iter % G::kStages;
-        const uint32_t par = (iter / G::kStages) & 1u;
-        if (!mbar_wait(smem_u32(&full[stage]), par)) {
+        const int sr = it % G::kSRaw, sc = it % G::kSConv;
+        if (!mbar_wait(smem_u32(&raw_full[sr]), (it / G::kSRaw) & 1u) ||
+            !mbar_wait(smem_u32(&conv_empty[sc]), ((it / G::kSConv) & 1u) ^ 1u)) {
           if (lane == 0) raise_status(a.status, kStTimeout, kind);
           *abort_flag = 1;
           ok = false;
           break;
         }
-        uint8_t* st = smem + (size_t)stage * G::kStageBytes;
+        const uint8_t* rawt = smem + G::kRawOff + sr * G::kRawBytes;
+        uint8_t* conv = smem + sc * G::kConvBytes;
 #pragma unroll
         for (int m = 0; m < NA; ++m) {
-          const uint8_t* raw = st + G::kRawOff + m * kRawTileBytes;
-          uint8_t* f16 = st + m * kF16TileBytes;
+          const uint8_t* raw = rawt + m * kRawTileBytes;
+          uint8_t* f16 = conv + m * kF16TileBytes;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int c = ti + 128 * i;  // 16-byte chunk of the int8 tile
@@ -307,12 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&conv[stage]));
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&conv_full[sc]));
+          mbar_arrive(smem_u32(&raw_empty[sr]));
+        }
       }
       if (!ok) break;
       // weight-row norms of this tile for the epilogue's guard
-      const uint32_t buf = local & 1u, use = local >> 1;
-      if (!mbar_wait(smem_u32(&norm_empty[buf]), (use & 1u) ^ 1u)) {
+      const uint32_t nb = local & 1u, nuse = local >> 1;
+      if (!mbar_wait(smem_u32(&norm_empty[nb]), (nuse & 1u) ^ 1u)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
@@ -324,11 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           int v = nrm[m][i];
           v += __shfl_xor_sync(0xffffffffu, v, 1);
           v += __shfl_xor_sync(0xffffffffu, v, 2);
-          if ((ti & 3) == 0) wnorm[(buf * 2 + m) * kTcM + (ti >> 2) + 32 * i] = v;
+          if ((ti & 3) == 0) wnorm[(nb * 2 + m) * kTcM + (ti >> 2) + 32 * i] = v;
         }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&norm_full[buf]));
-      (void)cw;
+      if (lane == 0) mbar_arrive(smem_u32(&norm_full[nb]));
     }
   } else if (warp >= 2) {
     // ----------------------------------------------------------- epilogue --
@@ -338,9 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) break;
       Tile t;
       decode(a, tile, ntasks, t);
-      const uint32_t buf = local & 1u, use = local >> 1;
+      const uint32_t buf = local % G::kAccBufs, use = local / G::kAccBufs;
+      const uint32_t nb = local & 1u, nuse = local >> 1;
       if (!mbar_wait(smem_u32(&acc_full[buf]), use & 1u) ||
-          !mbar_wait(smem_u32(&norm_full[buf]), use & 1u)) {
+          !mbar_wait(smem_u32(&norm_full[nb]), nuse & 1u)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
@@ -348,30 +385,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int r = q * 32 + lane;  // tile row = output channel
       const int ch = t.ct * kTcM + r;
-      const long long wn0 = wnorm[(buf * 2 + 0) * kTcM + r];
-      const long long wn1 = NA == 2 ? wnorm[(buf * 2 + 1) * kTcM + r] : 0;
-      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * G::kAccStride;
+      const bool live = ch < a.N;
+      const long long wn0 = wnorm[(nb * 2 + 0) * kTcM + r];
+      const long long wn1 = NA == 2 ? wnorm[(nb * 2 + 1) * kTcM + r] : 0;
+      float sw0 = 0.f, sw1 = 0.f;
+      if (MODE != kW8Raw && live) {
+        sw0 = a.s0[(size_t)t.e * a.N + ch];
+        if (NA == 2) sw1 = a.s1[(size_t)t.e * a.N + ch];
+      }
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
       bool bad = false;
       for (int j0 = 0; j0 < t.n; j0 += 16) {
         uint32_t g[16], u[16];
         tmem_ld16(trow + j0, g);
-        if (NA == 2) tmem_ld16(trow + kTcMaxN + j0, u);
+        if (NA == 2) tmem_ld16(trow + kAccCols + j0, u);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int tok = j0 + i;
           if (tok < t.n) {
-            const long long xn = a.row_norm2[t.row0 + tok];
+            const int row = t.row0 + tok;
+            const long long xn = a.row_norm2[row];
             bad |= xn * wn0 >= kGuard || (NA == 2 && xn * wn1 >= kGuard);
-            if (ch < a.N)
-              emit<MODE>(a, t.e, t.row0 + tok, ch, __float2int_rn(__uint_as_float(g[i])),
-                         NA == 2 ? __float2int_rn(__uint_as_float(u[i])) : 0);
+            if (live)
+              emit<MODE>(a, row, ch, __float2int_rn(__uint_as_float(g[i])),
+                         NA == 2 ? __float2int_rn(__uint_as_float(u[i])) : 0,
+                         MODE == kW8Raw ? 0.f : a.row_scale[row], sw0, sw1);
           }
         }
       }
       // The last of the four epilogue warps to finish this tile files it for
       // exact recomputation if any pair failed the guard.  This happens before
-      // the buffer is released, so the next tile on it cannot touch the flags.
+      // the accumulator is released, so the next tile on it cannot touch the flags.
       const bool any_bad = __any_sync(0xffffffffu, bad);
       if (lane == 0) {
         if (any_bad) atomicOr((int*)&tile_bad[buf], 1);
@@ -392,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_u32(&norm_empty[buf]));
+        mbar_arrive(smem_u32(&norm_empty[nb]));
         mbar_arrive(smem_u32(&acc_empty[buf]));
       }
     }
@@ -406,13 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Exact fallback: integer accumulation on CUDA cores for the tiles that failed
-// the guard (rare; adversarial inputs).  One CTA per filed tile at a time.
+// the guard (rare; adversarial inputs).  One CTA per filed tile at a time, in
+// passes of 128 token rows.
 template <int MODE>
 __global__ void __launch_bounds__(256, 1)
     w8a8_exact_kernel(const int8_t* w0, const int8_t* w1, const uint16_t* act, const Args a) {
   constexpr int NA = MODE == kW8GateUp ? 2 : 1;
+  constexpr int kPass = 128;
   __shared__ int8_t As[NA][kTcM][kBK + 4];
-  __shared__ int16_t Bs[kTcMaxN][kBK + 2];
+  __shared__ int16_t Bs[kPass][kBK + 2];
   const int ntasks = a.counts[a.task_slot];
   const int nredo = min(a.redo[0], a.redo_cap);
   const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;  // 8 channels x 8 tokens each
@@ -420,41 +467,121 @@ __global__ void __launch_bounds__(256, 1)
     Tile t;
     decode(a, a.redo[1 + idx], ntasks, t);
     const size_t mat = (size_t)a.N * a.K;
-    int acc[NA][8][8] = {};
-    for (int k0 = 0; k0 < a.K; k0 += kBK) {
-      for (int m = 0; m < NA; ++m) {
-        const int8_t* W = (m == 0 ? w0 : w1) + (size_t)t.e * mat;
-        for (int i = tid; i < kTcM * kBK; i += 256) {
-          const int r = i / kBK, k = i % kBK, ch = t.ct * kTcM + r;
-          As[m][r][k] = (ch < a.N && k0 + k < a.K) ? W[(size_t)ch * a.K + k0 + k] : (int8_t)0;
+    for (int tb = 0; tb < t.n; tb += kPass) {
+      const int tn = min(kPass, t.n - tb);
+      int acc[NA][8][8] = {};
+      for (int k0 = 0; k0 < a.K; k0 += kBK) {
+        for (int m = 0; m < NA; ++m) {
+          const int8_t* W = (m == 0 ? w0 : w1) + (size_t)t.e * mat;
+          for (int i = tid; i < kTcM * kBK; i += 256) {
+            const int r = i / kBK, k = i % kBK, ch = t.ct * kTcM + r;
+            As[m][r][k] = (ch < a.N && k0 + k < a.K) ? W[(size_t)ch * a.K + k0 + k] : (int8_t)0;
+          }
         }
+        for (int i = tid; i < kPass * kBK; i += 256) {
+          const int r = i / kBK, k = i % kBK;
+          int16_t v = 0;
+          if (r < tn && k0 + k < a.K)
+            v = (int16_t)__half2int_rn(
+                __ushort_as_half(act[(size_t)(t.row0 + tb + r) * a.K + k0 + k]));
+          Bs[r][k] = v;
+        }
+        __syncthreads();
+        for (int k = 0; k < kBK; ++k)
+#pragma unroll
+          for (int m = 0; m < NA; ++m)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                acc[m][i][j] += (int)As[m][tr * 8 + i][k] * (int)Bs[tc * 8 + j][k];
+        __syncthreads();
       }
-      for (int i = tid; i < kTcMaxN * kBK; i += 256) {
-        const int r = i / kBK, k = i % kBK;
-        int16_t v = 0;
-        if (r < t.n && k0 + k < a.K)
-          v = (int16_t)__half2int_rn(__ushort_as_half(act[(size_t)(t.row0 + r) * a.K + k0 + k]));
-        Bs[r][k] = v;
-      }
-      __syncthreads();
-      for (int k = 0; k < kBK; ++k)
 #pragma unroll
-        for (int m = 0; m < NA; ++m)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              acc[m][i][j] += (int)As[m][tr * 8 + i][k] * (int)Bs[tc * 8 + j][k];
-      __syncthreads();
+        for (int j = 0; j < 8; ++j) {
+          const int ch = t.ct * kTcM + tr * 8 + i, tok = tc * 8 + j;
+          if (ch < a.N && tok < tn) {
+            const int row = t.row0 + tb + tok;
+            float sw0 = 0.f, sw1 = 0.f, sr = 0.f;
+            if (MODE != kW8Raw) {
+              sr = a.row_scale[row];
+              sw0 = a.s0[(size_t)t.e * a.N + ch];
+              if (NA == 2) sw1 = a.s1[(size_t)t.e * a.N + ch];
+            }
+            emit<MODE>(a, row, ch, acc[0][i][j], NA == 2 ? acc[NA - 1][i][j] : 0, sr, sw0, sw1);
+          }
+        }
     }
+  }
+}
+
+// Per-token quantisation fused with the gather of the layer path: one CTA per
+// token quantises its bf16 row once (symmetric int8, scale = amax / 127, round
+// half to even, as the permutation's int8 gather does) and writes the codes as
+// integer-valued fp16, with the scale and the sum of squared codes, to the
+// sorted row of each of its picks that lands on an FFN expert.
+constexpr int kQgThreads = 256;
+constexpr int kMaxTopKQuant = 32;  // the largest top_k the layer accepts
+__global__ void __launch_bounds__(kQgThreads)
+    quant_gather_kernel(const uint16_t* x, const int32_t* ids, const int32_t* e2s, uint16_t* x16,
+                        float* scale, int32_t* norm2, int H, int k, int E_r) {
+  __shared__ float red_f[kQgThreads / 32];
+  __shared__ int red_i[kQgThreads / 32];
+  __shared__ int rows[kMaxTopKQuant];
+  __shared__ int nrows;
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  if (tid == 0) {
+    int n = 0;
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[(size_t)t * k + j];
+      const int p = e2s[(size_t)t * k + j];
+      if ((unsigned)e < (unsigned)E_r && p >= 0) rows[n++] = p;
+    }
+    nrows = n;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  const int nv = H / 8;
+  float amax = 0.f;
+  for (int i = tid; i < nv; i += kQgThreads) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
+  }
+  amax = warp_max(amax);
+  if (lane == 0) red_f[warp] = amax;
+  __syncthreads();
+  amax = red_f[0];
+  for (int w = 1; w < kQgThreads / 32; ++w) amax = fmaxf(amax, red_f[w]);
+  const int n = nrows;
+  if (n == 0) return;
+  const float s = amax / 127.0f;
+  int n2 = 0;
+  for (int i = tid; i < nv; i += kQgThreads) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int ch = t.ct * kTcM + tr * 8 + i, tok = tc * 8 + j;
-        if (ch < a.N && tok < t.n)
-          emit<MODE>(a, t.e, t.row0 + tok, ch, acc[0][i][j], NA == 2 ? acc[NA - 1][i][j] : 0);
-      }
+    for (int j = 0; j < 8; ++j) {
+      const float f = (j & 1) ? bf16hi(w[j / 2]) : bf16lo(w[j / 2]);
+      int qi = 0;
+      if (amax > 0.f) qi = (int)fminf(127.f, fmaxf(-127.f, rintf(f / s)));
+      n2 += qi * qi;
+      h[j / 2] |= (uint32_t)__half_as_ushort(__int2half_rn(qi)) << (16 * (j % 2));
+    }
+    const uint4 o = make_uint4(h[0], h[1], h[2], h[3]);
+    for (int r = 0; r < n; ++r) reinterpret_cast<uint4*>(x16 + (size_t)rows[r] * H)[i] = o;
+  }
+  for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+  if (lane == 0) red_i[warp] = n2;
+  __syncthreads();
+  if (tid < n) {
+    int tot = 0;
+    for (int w = 0; w < kQgThreads / 32; ++w) tot += red_i[w];
+    norm2[rows[tid]] = tot;
+    scale[rows[tid]] = s;
   }
 }
 
@@ -619,6 +746,16 @@ void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, in
   launch_begin(L, MOE_K_QUANT_H);
   i8_rows_to_f16_kernel<<<(R + 7) / 8, 256, 0, L.stream>>>(src, dst, norm2, R, K, nrows);
   launch_end(L, MOE_K_QUANT_H);
+}
+
+void launch_quant_gather(const Launch& L, const moe_config& c, int T, const void* x,
+                         const int32_t* ids, const int32_t* e2s, uint16_t* x16, float* scale,
+                         int32_t* norm2) {
+  launch_begin(L, MOE_K_PERM_GATHER);
+  quant_gather_kernel<<<T, kQgThreads, 0, L.stream>>>(static_cast<const uint16_t*>(x), ids, e2s,
+                                                      x16, scale, norm2, c.hidden, c.top_k,
+                                                      c.n_routed);
+  launch_end(L, MOE_K_PERM_GATHER);
 }
 
 void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, float* scale,

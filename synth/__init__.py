@@ -68,6 +68,10 @@ CONFIGS = {
     # real layer, 4.8 GB of weights (well above the 129 MB L2, a few GB on device).
     "longcat_prof": dict(_BASE, T=16, hidden=6144, inter=2048, n_routed=64, n_zero=32,
                          top_k=12, bias_mode="logit", bias_kind="iid"),
+    # Profiling-sized W8A8 prefill relative: full H and I, 64 experts, Zipf load,
+    # 2.8 GB of int8 weights and 235 MB of activation codes.
+    "w8a8_prof": dict(_BASE, T=2048, hidden=7168, inter=2048, n_routed=64, top_k=8,
+                      wdtype="w8a8", bias_mode="logit", bias_kind="zipf", router_std_scale=1.645),
 }
 
 # The five headline layers, in order.
