@@ -107,7 +107,8 @@ moe_status check_cfg(const moe_config* c, int32_t T) {
     if (c->shared_inter > 0) return MOE_ERR_UNSUPPORTED;
   }
   if (c->out_fp32 != 0 && c->out_fp32 != 1) return MOE_ERR_INVALID_ARG;
-  if ((long long)T * c->top_k > (1LL << 30) || T > (1 << 24)) return MOE_ERR_UNSUPPORTED;
+  // work-list chunk indices are 16-bit: at most 65535 chunks of 128 rows per unit
+  if ((long long)T * c->top_k > (1LL << 30) || T > 65535 * kTcMaxN) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -132,6 +133,9 @@ int gemv_chunk(int gemv_max) {
 // --------------------------------------------------------------- workspace --
 struct Layout {
   size_t status, partial, logits, ids, w, bc, counts, offsets, s2e, e2s;
+  // tensor-core router only: split weights, its work list
+  size_t rsplit, rtasks, rstart, rcounts;
+  bool tc_router;
   size_t wl_gemv_tasks, wl_gemv_gu, wl_gemv_dn, wl_tc_tasks, wl_tc_gu, wl_tc_dn, wl_counts;
   size_t x_perm, x_scale, h, y, h_s, y_s;
   // W8A8 only: integer-valued fp16 copies of the codes, row norms, fp32 h and
@@ -158,6 +162,15 @@ Layout make_layout(const moe_config& c, int T) {
     return at;
   };
   L.status = take(256 + kRouterCounterBytes);  // status word, then router tile counters
+  L.tc_router = router_on_tensor_cores(c, T);
+  if (L.tc_router) {
+    const size_t nt = ((size_t)T + kTcMaxN - 1) / kTcMaxN;
+    L.splits = 1;
+    L.rsplit = take(E * 3 * H * 2);
+    L.rtasks = take(nt * sizeof(FfnTask));
+    L.rstart = take(nt * 4);
+    L.rcounts = take(kWlCount * 4);
+  }
   L.partial = take(L.splits > 1 ? (size_t)L.splits * T * E * 4 : 0);
   L.logits = take((size_t)T * E * 4);
   L.ids = take(R * 4);
@@ -243,13 +256,23 @@ Launch make_launch(moe_stream_t stream, void* ws, const Layout& L) {
 }
 
 // ---------------------------------------------------------------- stages --
-void run_route(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
-               const void* x, const float* w_router, const float* bias, int32_t* ids, float* w) {
-  float* partial = at<float>(ws, L.partial);
+moe_status run_route(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
+                     const void* x, const float* w_router, const float* bias, int32_t* ids,
+                     float* w) {
   float* logits = at<float>(ws, L.logits);
-  int* counters = at<int>(ws, L.status + 256);
-  launch_router(ln, c, T, x, w_router, partial, L.splits, logits, counters);
+  if (L.tc_router) {
+    uint16_t* split = at<uint16_t>(ws, L.rsplit);
+    launch_router_split(ln, w_router, c.n_routed + c.n_zero, c.hidden, split);
+    if (!launch_tc_router(ln, c, T, x, split, at<FfnTask>(ws, L.rtasks), at<int32_t>(ws, L.rstart),
+                          at<int32_t>(ws, L.rcounts), logits))
+      return MOE_ERR_CUDA;
+  } else {
+    float* partial = at<float>(ws, L.partial);
+    int* counters = at<int>(ws, L.status + 256);
+    launch_router(ln, c, T, x, w_router, partial, L.splits, logits, counters);
+  }
   launch_topk(ln, c, T, logits, bias, ids, w);
+  return MOE_OK;
 }
 
 void run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
@@ -516,8 +539,9 @@ moe_status moe_route(const moe_config* cfg, int32_t T, const void* x, const floa
   if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(topk_ids, 16) || !aligned(topk_w, 16))
     return MOE_ERR_ALIGNMENT;
   const Launch ln = make_launch(stream, ws, L);
-  run_route(ln, *cfg, T, L, ws, x, w_router, bias, topk_ids, topk_w);
-  return finish();
+  const moe_status rs = run_route(ln, *cfg, T, L, ws, x, w_router, bias, topk_ids, topk_w);
+  const moe_status f = finish();
+  return rs != MOE_OK ? rs : f;
 }
 
 moe_status moe_permute(const moe_config* cfg, int32_t T, const int32_t* topk_ids, const void* x,
@@ -630,7 +654,11 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
   float* x_scale = at<float>(ws, L.x_scale);
   float* y = at<float>(ws, L.y);
   float* y_s = c.shared_inter > 0 ? at<float>(ws, L.y_s) : nullptr;
-  run_route(ln, c, T, L, ws, x, w_router, bias, ids, w);
+  const moe_status rs = run_route(ln, c, T, L, ws, x, w_router, bias, ids, w);
+  if (rs != MOE_OK) {
+    finish();
+    return rs;
+  }
   run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale);
   if (w8 && c.n_routed > 0)
     launch_quant_gather(ln, c, T, x, ids, e2s, at<uint16_t>(ws, L.x16), x_scale,

@@ -67,6 +67,7 @@ struct TcArgs {
   uint16_t* sout_h;
   float* sout_y;
   int K, Ks, N, Ns;
+  int b_kmod;  // > 0: routed activation K coordinate modulo b_kmod (router tiles)
   DevStatus* status;
 };
 
@@ -165,9 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem_u32(st), A0, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
         if (GU) tma_load_3d(smem_u32(st + kATileBytes), A1, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
         uint8_t* sb = st + G::kNA * kATileBytes;
+        const int bk = (!t.shared && a.b_kmod > 0) ? (ks * kBK) % a.b_kmod : ks * kBK;
         for (int j = 0; j < nb; ++j)
-          tma_load_3d(smem_u32(sb + j * kBoxBytes), B, ks * kBK, t.row0 + j * kBoxRows, 0, bar,
-                      pol_x);
+          tma_load_3d(smem_u32(sb + j * kBoxBytes), B, bk, t.row0 + j * kBoxRows, 0, bar, pol_x);
         ++iter;
       }
     }
@@ -309,14 +310,34 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Router work list: token chunks of <= 128 rows, all expert tiles of each.
+__global__ void router_tasks_kernel(FfnTask* tasks, int32_t* start, int32_t* counts, int T,
+                                    int ctiles) {
+  const int nt = (T + kTcMaxN - 1) / kTcMaxN;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nt; i += gridDim.x * blockDim.x) {
+    FfnTask tk;
+    tk.expert = 0;
+    tk.row0 = i * kTcMaxN;
+    tk.nrows = min(kTcMaxN, T - i * kTcMaxN);
+    tk.chunk = (i << 16) | nt;
+    tasks[i] = tk;
+    start[i] = i * ctiles;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    counts[kWlTcTasks] = nt;
+    counts[kWlTcTilesDN] = nt * ctiles;
+  }
+}
+
 template <bool GU>
-bool launch_tc(const Launch& L, const TcPass& p) {
+bool launch_tc(const Launch& L, const TcPass& p, int kind) {
   using G = Geom<GU>;
   TcMaps maps;
   memset(&maps, 0, sizeof maps);
   const uint64_t Kr = p.K, Nr = p.N;
+  const uint64_t Kb = p.b_kmod > 0 ? (uint64_t)p.b_kmod : Kr;  // activation row length
   bool ok = make_map(&maps.a0, p.w0, Kr, Nr, p.n_experts, kTcM) &&
-            make_map(&maps.b, p.act, Kr, p.act_rows, 1, kBoxRows);
+            make_map(&maps.b, p.act, Kb, p.act_rows, 1, kBoxRows);
   if (GU) ok = ok && make_map(&maps.a1, p.w1, Kr, Nr, p.n_experts, kTcM);
   if (p.sw0) {
     ok = ok && make_map(&maps.sa0, p.sw0, p.Ks, p.Ns, 1, kTcM) &&
@@ -338,8 +359,8 @@ bool launch_tc(const Launch& L, const TcPass& p) {
   a.Ks = p.Ks;
   a.N = p.N;
   a.Ns = p.Ns;
+  a.b_kmod = p.b_kmod;
   a.status = L.status;
-  const int kind = GU ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
   set_smem_attr_once(reinterpret_cast<const void*>(tc_kernel<GU>), G::kSmemBytes,
                      GU ? kAttrTcGU : kAttrTcDN);
   launch_begin(L, kind);
@@ -350,7 +371,37 @@ bool launch_tc(const Launch& L, const TcPass& p) {
 
 }  // namespace
 
-bool launch_tc_gate_up(const Launch& L, const TcPass& p) { return launch_tc<true>(L, p); }
-bool launch_tc_down(const Launch& L, const TcPass& p) { return launch_tc<false>(L, p); }
+bool launch_tc_gate_up(const Launch& L, const TcPass& p) {
+  return launch_tc<true>(L, p, MOE_K_TC_GATE_UP);
+}
+bool launch_tc_down(const Launch& L, const TcPass& p) {
+  return launch_tc<false>(L, p, MOE_K_TC_DOWN);
+}
+
+bool launch_tc_router(const Launch& L, const moe_config& c, int T, const void* x,
+                      const uint16_t* w_split, FfnTask* tasks, int32_t* start, int32_t* counts,
+                      float* logits) {
+  const int E = c.n_routed + c.n_zero;
+  const int ctiles = (E + kTcM - 1) / kTcM;
+  const int nt = (T + kTcMaxN - 1) / kTcMaxN;
+  launch_begin(L, MOE_K_ROUTER);
+  router_tasks_kernel<<<(nt + 255) / 256, 256, 0, L.stream>>>(tasks, start, counts, T, ctiles);
+  launch_end(L, MOE_K_ROUTER);
+  TcPass p{};
+  p.tasks = tasks;
+  p.tile_start = start;
+  p.counts = counts;
+  p.task_slot = kWlTcTasks;
+  p.tile_slot = kWlTcTilesDN;
+  p.w0 = w_split;
+  p.n_experts = 1;
+  p.act = x;
+  p.act_rows = T;
+  p.out_y = logits;
+  p.K = 3 * c.hidden;
+  p.N = E;
+  p.b_kmod = c.hidden;
+  return launch_tc<false>(L, p, MOE_K_ROUTER);
+}
 
 }  // namespace moe

@@ -97,6 +97,10 @@ void launch_router(const Launch& L, const moe_config& c, int T, const void* x, c
                    float* partial, int splits, float* logits, int* counters);
 void launch_topk(const Launch& L, const moe_config& c, int T, const float* logits,
                  const float* bias, int32_t* ids, float* w);
+// Large batches: the router as a tensor-core GEMM over the exact three-term
+// bf16 split of W_r ([E, 3H], written by launch_router_split).
+bool router_on_tensor_cores(const moe_config& c, int T);
+void launch_router_split(const Launch& L, const float* w_r, int E, int H, uint16_t* out);
 
 // Permutation (permute.cu)
 constexpr int kPermTokens = 256;  // tokens per permutation block
@@ -154,9 +158,15 @@ struct TcPass {
   uint16_t* sout_h;
   float* sout_y;
   int K, Ks, N, Ns;
+  int b_kmod;              // > 0: activation K coordinate taken modulo b_kmod
 };
 bool launch_tc_gate_up(const Launch& L, const TcPass& p);
 bool launch_tc_down(const Launch& L, const TcPass& p);
+// logits[T, E] = x[T, H] . [W3 | W2 | W1]^T on tensor cores (K = 3H, the token
+// rows read three times); tasks/start/counts are its own small work list.
+bool launch_tc_router(const Launch& L, const moe_config& c, int T, const void* x,
+                      const uint16_t* w_split, FfnTask* tasks, int32_t* start, int32_t* counts,
+                      float* logits);
 
 // W8A8 grouped FFN (w8a8.cu): tensor-core tiles on integer-valued fp16 operands
 // with an exactness guard, then an exact CUDA-core pass over guard failures.

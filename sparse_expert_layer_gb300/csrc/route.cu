@@ -281,7 +281,42 @@ __global__ void topk_kernel(TopkArgs a) {
   }
 }
 
+// Exact three-term bf16 split of the fp32 router weights for the tensor-core
+// router: W1 = bf16(W), W2 = bf16(W - W1), W3 = bf16(W - W1 - W2).  Each
+// remainder is exact in fp32 and W1 + W2 + W3 == W, and bf16 x bf16 products
+// are exact in fp32, so the MMA sums the same products as the fp32 router.
+// Rows hold [W3 | W2 | W1]: the small terms are accumulated first, while the
+// running sum is still small, which keeps the accumulator's rounding small.
+__global__ void router_split_kernel(const float* w, uint16_t* out, int E, int H) {
+  const size_t n = (size_t)E * H;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = i / H, h = i % H;
+    const float v = w[i];
+    const uint16_t b1 = f_to_bf16(v);
+    const float r1 = v - bf16_to_f(b1);
+    const uint16_t b2 = f_to_bf16(r1);
+    const float r2 = r1 - bf16_to_f(b2);
+    uint16_t* row = out + e * 3 * H;
+    row[h] = f_to_bf16(r2);
+    row[H + h] = b2;
+    row[2 * H + h] = b1;
+  }
+}
+
 }  // namespace
+
+bool router_on_tensor_cores(const moe_config& c, int T) {
+  const int E = c.n_routed + c.n_zero;
+  const long tiles = (long)((T + kTcMaxN - 1) / kTcMaxN) * ((E + kTcM - 1) / kTcM);
+  return c.hidden % 64 == 0 && T >= 1024 && tiles >= 64;
+}
+
+void launch_router_split(const Launch& L, const float* w_r, int E, int H, uint16_t* out) {
+  launch_begin(L, MOE_K_ROUTER);
+  router_split_kernel<<<4 * L.num_sms, 256, 0, L.stream>>>(w_r, out, E, H);
+  launch_end(L, MOE_K_ROUTER);
+}
 
 int router_tiles(const moe_config& c, int T) {
   const int E = c.n_routed + c.n_zero;

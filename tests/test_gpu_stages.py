@@ -42,6 +42,20 @@ def test_route_matches_oracle(m, name):
     assert np.allclose(w, w_o, rtol=1e-5, atol=1e-7)
 
 
+def test_route_on_tensor_cores_matches_oracle(m):
+    # 1024 tokens x 1024 experts: the router runs as the exact three-term bf16
+    # split on tensor cores (the path large prefill batches take)
+    spec = synth.spec("tiny", T=1024, hidden=1024, n_routed=1024, top_k=4, renormalize=True,
+                      name="router_tc")
+    d = gs.inputs(spec)
+    ids, w = route_gpu(m, spec, d)
+    ids_o, w_o, _, _ = oracle.route(spec, synth.bf16_bits(d["x"]), d["w_r"].numpy(),
+                                    support.np_bias(d["bias"]))
+    assert np.array_equal(ids, ids_o)
+    rel = np.abs(w - w_o) / w_o
+    assert np.allclose(w, w_o, rtol=1e-5, atol=1e-7), f"max rel {rel.max():.3e}"
+
+
 @pytest.mark.parametrize("score", ["softmax", "sigmoid"])
 def test_route_select_bias_and_groups(m, score):
     spec = synth.spec("dsv3_s", score=score, bias_mode="select", bias_kind="iid",
