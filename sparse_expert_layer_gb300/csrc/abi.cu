@@ -328,6 +328,7 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   tg.counts = wl.counts;
   tg.task_slot = kWlTcTasks;
   tg.tile_slot = kWlTcTilesGU;
+  tg.sched_slot = kWlSchedGU;
   tg.w0 = w_gate;
   tg.w1 = w_up;
   tg.n_experts = c.n_routed;
@@ -368,6 +369,7 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   td.counts = wl.counts;
   td.task_slot = kWlTcTasks;
   td.tile_slot = kWlTcTilesDN;
+  td.sched_slot = kWlSchedDN;
   td.w0 = w_down;
   td.n_experts = c.n_routed;
   td.act = h;
@@ -415,6 +417,7 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   g.counts = wl.counts;
   g.task_slot = kWlTcTasks;
   g.tile_slot = kWlTcTilesGU;
+  g.sched_slot = kWlSchedGU;
   g.w0 = w_gate;
   g.w1 = w_up;
   g.n_experts = c.n_routed;
@@ -437,6 +440,7 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   d.mode = kW8Down;
   d.tile_start = wl.tc_start_dn;
   d.tile_slot = kWlTcTilesDN;
+  d.sched_slot = kWlSchedDN;
   d.w0 = w_down;
   d.w1 = nullptr;
   d.s0 = s_down;
@@ -767,6 +771,7 @@ moe_status moe_qgemm_s8(int32_t n_experts, int32_t K, int32_t N, int32_t R, cons
   p.counts = wl.counts;
   p.task_slot = kWlTcTasks;
   p.tile_slot = kWlTcTilesDN;
+  p.sched_slot = kWlSchedDN;
   p.w0 = w;
   p.n_experts = n_experts;
   p.act = a16;

@@ -107,6 +107,42 @@ __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, l
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return mbar_wait_limit(bar, parity, kWaitCycles);
 }
+// Warp-uniform forms for roles that run as whole warps (they shuffle and
+// __syncwarp later, so every lane must take the same branch).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+__device__ __forceinline__ bool warp_flag(const volatile int* f) {
+  return __any_sync(0xffffffffu, *f != 0);
+}
+
+// -------------------------------------------------------------- tile queue --
+// Persistent tensor-core kernels schedule tiles dynamically: the producer
+// thread claims the next tile from a global counter and publishes its id (-1 =
+// no more) in a small shared-memory queue that every other role of the CTA
+// reads in the same order.  full[s]: one arrival (the producer); empty[s]: one
+// arrival per consuming thread or warp.
+constexpr int kTileQueue = 4;
+__device__ __forceinline__ bool tq_push(int* q, uint64_t* full, uint64_t* empty, uint32_t n,
+                                        int tile) {
+  const int s = n % kTileQueue;
+  if (!mbar_wait(smem_u32(&empty[s]), ((n / kTileQueue) & 1u) ^ 1u)) return false;
+  q[s] = tile;
+  mbar_arrive(smem_u32(&full[s]));
+  return true;
+}
+// Every lane of a consuming warp calls this; lane 0 (or the single consuming
+// thread, with warp_level false) releases the slot after all lanes read it.
+__device__ __forceinline__ bool tq_pop(const int* q, uint64_t* full, uint64_t* empty, uint32_t n,
+                                       int* tile, bool warp_level) {
+  const int s = n % kTileQueue;
+  bool ok = mbar_wait(smem_u32(&full[s]), (n / kTileQueue) & 1u);
+  if (warp_level) ok = __all_sync(0xffffffffu, ok);
+  *tile = ok ? reinterpret_cast<const volatile int*>(q)[s] : -1;
+  if (warp_level) __syncwarp();
+  if (ok && (!warp_level || (threadIdx.x % 32) == 0)) mbar_arrive(smem_u32(&empty[s]));
+  return ok;
+}
 
 // ------------------------------------------------------------ bulk copies ---
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -44,7 +44,7 @@ struct Geom {
   static constexpr int kStages = GU ? 4 : 6;
   static constexpr int kTmemCols = GU ? 512 : 256;
   static constexpr int kAccStride = GU ? 256 : 128;  // TMEM columns per accumulator buffer
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
 };
 
@@ -68,6 +68,7 @@ struct TcArgs {
   float* sout_y;
   int K, Ks, N, Ns;
   int b_kmod;  // > 0: routed activation K coordinate modulo b_kmod (router tiles)
+  int* sched;  // dynamic tile counter, zero at launch
   DevStatus* status;
 };
 
@@ -105,7 +106,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = empty + G::kStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* tq_full = drain + 1;
+  uint64_t* tq_empty = tq_full + kTileQueue;
+  int* tq = reinterpret_cast<int*>(tq_empty + kTileQueue);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq + kTileQueue);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -119,6 +123,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&acc_empty[b]), 4);
     }
     mbar_init(smem_u32(drain), 1);
+    for (int s = 0; s < kTileQueue; ++s) {
+      mbar_init(smem_u32(&tq_full[s]), 1);
+      mbar_init(smem_u32(&tq_empty[s]), 5);  // MMA thread + 4 epilogue warps
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -138,7 +146,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
     uint32_t iter = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+    for (uint32_t n = 0; ok; ++n) {
+      int tile = *abort_flag ? -1 : atomicAdd(a.sched, 1);
+      if (tile >= ntiles) tile = -1;
+      if (!tq_push(tq, tq_full, tq_empty, n, tile)) {
+        raise_status(a.status, kStTimeout, kind);
+        *abort_flag = 1;
+        break;
+      }
+      if (tile < 0) break;
       Tile t;
       decode_tile(a, tile, ntasks, t);
       const CUtensorMap* A0 = t.shared ? &maps.sa0 : &maps.a0;
@@ -179,7 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- MMA issuer --
     uint32_t iter = 0, local = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++local) {
+    for (uint32_t n = 0; ok; ++n, ++local) {
+      int tile;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &tile, false)) {
+        raise_status(a.status, kStTimeout, kind);
+        *abort_flag = 1;
+        break;
+      }
+      if (tile < 0) break;
       Tile t;
       decode_tile(a, tile, ntasks, t);
       const uint32_t buf = local & 1u, use = local >> 1;
@@ -231,12 +254,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------- epilogue --
     const int q = warp % 4;  // TMEM lane quadrant this warp may access
     uint32_t local = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-      if (*abort_flag) break;
+    for (uint32_t n = 0;; ++n, ++local) {
+      int tile;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &tile, true)) {
+        if (lane == 0) raise_status(a.status, kStTimeout, kind);
+        *abort_flag = 1;
+        break;
+      }
+      if (tile < 0 || warp_flag(abort_flag)) break;
       Tile t;
       decode_tile(a, tile, ntasks, t);
       const uint32_t buf = local & 1u, use = local >> 1;
-      if (!mbar_wait(smem_u32(&acc_full[buf]), use & 1u)) {
+      if (!warp_wait(smem_u32(&acc_full[buf]), use & 1u)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
@@ -326,6 +355,7 @@ __global__ void router_tasks_kernel(FfnTask* tasks, int32_t* start, int32_t* cou
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     counts[kWlTcTasks] = nt;
     counts[kWlTcTilesDN] = nt * ctiles;
+    counts[kWlSchedDN] = 0;
   }
 }
 
@@ -360,6 +390,7 @@ bool launch_tc(const Launch& L, const TcPass& p, int kind) {
   a.N = p.N;
   a.Ns = p.Ns;
   a.b_kmod = p.b_kmod;
+  a.sched = const_cast<int32_t*>(p.counts) + p.sched_slot;
   a.status = L.status;
   set_smem_attr_once(reinterpret_cast<const void*>(tc_kernel<GU>), G::kSmemBytes,
                      GU ? kAttrTcGU : kAttrTcDN);
@@ -393,6 +424,7 @@ bool launch_tc_router(const Launch& L, const moe_config& c, int T, const void* x
   p.counts = counts;
   p.task_slot = kWlTcTasks;
   p.tile_slot = kWlTcTilesDN;
+  p.sched_slot = kWlSchedDN;
   p.w0 = w_split;
   p.n_experts = 1;
   p.act = x;

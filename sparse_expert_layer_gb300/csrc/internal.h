@@ -51,6 +51,8 @@ enum {
   kWlTcTasks,
   kWlTcTilesGU,
   kWlTcTilesDN,
+  kWlSchedGU,   // dynamic tile counters of the two tensor-core passes (zeroed
+  kWlSchedDN,   // by the kernel that writes the work list)
   kWlCount
 };
 
@@ -143,7 +145,7 @@ struct TcPass {
   const FfnTask* tasks;
   const int32_t* tile_start;
   const int32_t* counts;
-  int task_slot, tile_slot;
+  int task_slot, tile_slot, sched_slot;
   const void* w0;          // routed weights [n_experts, N, K] (gate or down)
   const void* w1;          // routed up weights (gate/up pass)
   int n_experts;
@@ -177,7 +179,7 @@ struct W8Pass {
   const FfnTask* tasks;
   const int32_t* tile_start;
   const int32_t* counts;
-  int task_slot, tile_slot;
+  int task_slot, tile_slot, sched_slot;
   const void* w0;           // int8 weights [n_experts, N, K] (gate or down)
   const void* w1;           // int8 up weights (gate/up mode)
   int n_experts;

@@ -277,6 +277,8 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
   if (threadIdx.x == 0) {
     if (a.wl.redo_gu) a.wl.redo_gu[0] = 0;
     if (a.wl.redo_dn) a.wl.redo_dn[0] = 0;
+    a.wl.counts[kWlSchedGU] = 0;
+    a.wl.counts[kWlSchedDN] = 0;
     a.wl.counts[kWlGemvTasks] = min(carry[0], a.wl.capacity);
     a.wl.counts[kWlGemvItemsGU] = carry[0] <= a.wl.capacity ? carry[1] : 0;
     a.wl.counts[kWlGemvItemsDN] = carry[0] <= a.wl.capacity ? carry[2] : 0;

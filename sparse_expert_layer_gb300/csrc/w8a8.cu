@@ -93,6 +93,7 @@ struct Args {
   int32_t* out_i32;          // raw: accumulators [rows, N]
   int32_t* redo;             // [0] count, [1..] tile ids
   int redo_cap;
+  int* sched;                // dynamic tile counter, zero at launch
   int K, N;
   DevStatus* status;
 };
@@ -153,7 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* norm_full = acc_empty + 2;
   uint64_t* norm_empty = norm_full + 2;
   uint64_t* drain = norm_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* tq_full = drain + 1;
+  uint64_t* tq_empty = tq_full + kTileQueue;
+  int* tq = reinterpret_cast<int*>(tq_empty + kTileQueue);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq + kTileQueue);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* tile_bad = abort_flag + 1;   // [2], per accumulator buffer
   volatile int* tile_done = abort_flag + 3;  // [2], epilogue warps finished
@@ -182,6 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_done[b] = 0;
     }
     mbar_init(smem_u32(drain), 1);
+    for (int s = 0; s < kTileQueue; ++s) {
+      mbar_init(smem_u32(&tq_full[s]), 1);
+      mbar_init(smem_u32(&tq_empty[s]), 9);  // MMA thread + 4 converter + 4 epilogue warps
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -197,7 +205,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
     uint32_t n_raw = 0, n_act = 0;  // copies issued into each ring
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+    for (uint32_t n = 0; ok; ++n) {
+      int tile = *abort_flag ? -1 : atomicAdd(a.sched, 1);
+      if (tile >= ntiles) tile = -1;
+      if (!tq_push(tq, tq_full, tq_empty, n, tile)) {
+        raise_status(a.status, kStTimeout, kind);
+        *abort_flag = 1;
+        break;
+      }
+      if (tile < 0) break;
       Tile t;
       decode(a, tile, ntasks, t);
       const int nb = (t.n + kBoxRows - 1) / kBoxRows;
@@ -243,7 +259,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- MMA issuer --
     uint32_t it = 0, local = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++local) {
+    for (uint32_t n = 0; ok; ++n, ++local) {
+      int tile;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &tile, false)) {
+        raise_status(a.status, kStTimeout, kind);
+        *abort_flag = 1;
+        break;
+      }
+      if (tile < 0) break;
       Tile t;
       decode(a, tile, ntasks, t);
       const uint32_t buf = local % G::kAccBufs, use = local / G::kAccBufs;
@@ -293,8 +316,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- converter --
     const int ti = threadIdx.x - 6 * 32;  // 0..127
     uint32_t it = 0, local = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-      if (*abort_flag) break;
+    for (uint32_t n = 0;; ++n, ++local) {
+      int tile;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &tile, true)) {
+        if (lane == 0) raise_status(a.status, kStTimeout, kind);
+        *abort_flag = 1;
+        break;
+      }
+      if (tile < 0 || warp_flag(abort_flag)) break;
       int32_t nrm[NA][4];
 #pragma unroll
       for (int m = 0; m < NA; ++m)
@@ -302,13 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 4; ++i) nrm[m][i] = 0;
       bool ok = true;
       for (int ks = 0; ks < nks; ++ks, ++it) {
-        if (*abort_flag) {
+        if (warp_flag(abort_flag)) {
           ok = false;
           break;
         }
         const int sr = it % G::kSRaw, sc = it % G::kSConv;
-        if (!mbar_wait(smem_u32(&raw_full[sr]), (it / G::kSRaw) & 1u) ||
-            !mbar_wait(smem_u32(&conv_empty[sc]), ((it / G::kSConv) & 1u) ^ 1u)) {
+        if (!warp_wait(smem_u32(&raw_full[sr]), (it / G::kSRaw) & 1u) ||
+            !warp_wait(smem_u32(&conv_empty[sc]), ((it / G::kSConv) & 1u) ^ 1u)) {
           if (lane == 0) raise_status(a.status, kStTimeout, kind);
           *abort_flag = 1;
           ok = false;
@@ -349,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // weight-row norms of this tile for the epilogue's guard
       const uint32_t nb = local & 1u, nuse = local >> 1;
-      if (!mbar_wait(smem_u32(&norm_empty[nb]), (nuse & 1u) ^ 1u)) {
+      if (!warp_wait(smem_u32(&norm_empty[nb]), (nuse & 1u) ^ 1u)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
@@ -370,14 +399,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------- epilogue --
     const int q = warp % 4;
     uint32_t local = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-      if (*abort_flag) break;
+    for (uint32_t n = 0;; ++n, ++local) {
+      int tile;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &tile, true)) {
+        if (lane == 0) raise_status(a.status, kStTimeout, kind);
+        *abort_flag = 1;
+        break;
+      }
+      if (tile < 0 || warp_flag(abort_flag)) break;
       Tile t;
       decode(a, tile, ntasks, t);
       const uint32_t buf = local % G::kAccBufs, use = local / G::kAccBufs;
       const uint32_t nb = local & 1u, nuse = local >> 1;
-      if (!mbar_wait(smem_u32(&acc_full[buf]), use & 1u) ||
-          !mbar_wait(smem_u32(&norm_full[nb]), nuse & 1u)) {
+      if (!warp_wait(smem_u32(&acc_full[buf]), use & 1u) ||
+          !warp_wait(smem_u32(&norm_full[nb]), nuse & 1u)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
@@ -714,6 +749,7 @@ bool launch_mode(const Launch& L, const W8Pass& p) {
   a.out_i32 = p.out_i32;
   a.redo = p.redo;
   a.redo_cap = p.redo_cap;
+  a.sched = const_cast<int32_t*>(p.counts) + p.sched_slot;
   a.K = p.K;
   a.N = p.N;
   a.status = L.status;
