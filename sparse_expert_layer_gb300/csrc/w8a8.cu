@@ -47,8 +47,8 @@ constexpr int kBK = 64;
 constexpr int kRawTileBytes = kTcM * kBK;        // 8 KB of int8
 constexpr int kF16TileBytes = kTcM * kBK * 2;    // 16 KB of fp16
 constexpr int kActTileBytes = kW8MaxN * kBK * 2; // 32 KB
-constexpr int kBoxRows = 16;
-constexpr int kBoxBytes = kBoxRows * kBK * 2;
+constexpr int kBoxRows = 64;                     // activation rows per TMA box
+constexpr int kBoxBytes = kBoxRows * kBK * 2;    // 8 KB
 constexpr long long kGuard = 1LL << 48;          // (2^24)^2
 constexpr int kAccCols = 256;                    // TMEM columns of one accumulator
 
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------- producer --
-    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+    const uint64_t pol_w = policy_evict_normal(), pol_x = policy_evict_last();
     uint32_t n_raw = 0, n_act = 0;  // copies issued into each ring
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
