@@ -372,9 +372,7 @@ def run_ours(args, rank, world, local):
     if moe.moe_check_device_status(layer.ws) != moe.MOE_OK:
         raise RuntimeError("device status set during warm-up")
 
-    # timed region: K steps, per-kernel events recorded by the library
-    moe.timing_enable(True)
-    moe.timing_collect()
+    # timed region: K steps of the layer call, nothing else on the stream
     launches0 = moe.launch_counts()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -387,8 +385,6 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
     barrier(world)
     ms = start.elapsed_time(stop)
-    per_kernel = moe.timing_collect()
-    moe.timing_enable(False)
     launches1 = moe.launch_counts()
     gpu_launches = sum(launches1.values()) - sum(launches0.values())
     if moe.moe_check_device_status(layer.ws) != moe.MOE_OK:
@@ -396,6 +392,44 @@ def run_ours(args, rank, world, local):
     ms = max_over_ranks(ms, world, dev)
     ms_step = ms / args.steps
     value = whole_job_rate(world, T, args.steps, ms)
+
+    # per-kernel breakdown: the same K steps again, each launch bracketed by
+    # CUDA events on its stream (recorded by the library)
+    moe.timing_enable(True)
+    moe.timing_collect()
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        layer.forward(x_d, out)
+    torch.cuda.synchronize()
+    per_kernel = moe.timing_collect()
+    moe.timing_enable(False)
+
+    # the same step replayed from a CUDA graph (launch gaps removed)
+    graph = None
+    try:
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            layer.forward(x_d, out, stream=gs)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            layer.forward(x_d, out, stream=gs)
+        g.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        gms = max_over_ranks(g0.elapsed_time(g1), world, dev)
+        if moe.moe_check_device_status(layer.ws) != moe.MOE_OK:
+            raise RuntimeError("device status set during graph replay")
+        graph = {"value": whole_job_rate(world, T, args.steps, gms), "unit": "tokens/s",
+                 "ms_per_step": gms / args.steps}
+    except RuntimeError as exc:  # capture unavailable: report why, keep the line
+        graph = {"unavailable": str(exc)[:200]}
 
     # end to end: host buffers, H2D of x and D2H of out inside the timed region
     x_h = x.pin_memory()
@@ -465,6 +499,7 @@ def run_ours(args, rank, world, local):
         "kernels_ms_per_step": {kname: v[0] / args.steps for kname, v in per_kernel.items()
                                 if v[1]},
         "e2e": e2e,
+        "cuda_graph": graph,
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(),
     }

@@ -34,8 +34,8 @@ constexpr int kThreads = 192;
 constexpr int kBK = 64;                          // K elements per stage: one 128-byte row
 constexpr int kATileBytes = kTcM * kBK * 2;      // 16 KB
 constexpr int kBTileBytes = kTcMaxN * kBK * 2;   // 16 KB
-constexpr int kBoxRows = 16;
-constexpr int kBoxBytes = kBoxRows * kBK * 2;    // 2 KB
+constexpr int kBoxRows = 64;
+constexpr int kBoxBytes = kBoxRows * kBK * 2;    // 8 KB
 
 template <bool GU>
 struct Geom {
