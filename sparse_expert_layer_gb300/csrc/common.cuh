@@ -118,27 +118,40 @@ __device__ __forceinline__ bool warp_flag(const volatile int* f) {
 
 // -------------------------------------------------------------- tile queue --
 // Persistent tensor-core kernels schedule tiles dynamically: the producer
-// thread claims the next tile from a global counter and publishes its id (-1 =
-// no more) in a small shared-memory queue that every other role of the CTA
-// reads in the same order.  full[s]: one arrival (the producer); empty[s]: one
-// arrival per consuming thread or warp.
+// thread claims the next tile from a global counter, decodes it and publishes
+// it (tile < 0 = no more) in a small shared-memory queue that every other role
+// of the CTA reads in the same order.  full[s]: one arrival (the producer);
+// empty[s]: one arrival per consuming thread or warp.
 constexpr int kTileQueue = 4;
-__device__ __forceinline__ bool tq_push(int* q, uint64_t* full, uint64_t* empty, uint32_t n,
-                                        int tile) {
+struct QTile {
+  int tile, row0, n, ct, e, shared;
+};
+__device__ __forceinline__ bool tq_push(QTile* q, uint64_t* full, uint64_t* empty, uint32_t n,
+                                        const QTile& v) {
   const int s = n % kTileQueue;
   if (!mbar_wait(smem_u32(&empty[s]), ((n / kTileQueue) & 1u) ^ 1u)) return false;
-  q[s] = tile;
+  q[s] = v;
   mbar_arrive(smem_u32(&full[s]));
   return true;
 }
 // Every lane of a consuming warp calls this; lane 0 (or the single consuming
 // thread, with warp_level false) releases the slot after all lanes read it.
-__device__ __forceinline__ bool tq_pop(const int* q, uint64_t* full, uint64_t* empty, uint32_t n,
-                                       int* tile, bool warp_level) {
+__device__ __forceinline__ bool tq_pop(const QTile* q, uint64_t* full, uint64_t* empty,
+                                       uint32_t n, QTile* v, bool warp_level) {
   const int s = n % kTileQueue;
   bool ok = mbar_wait(smem_u32(&full[s]), (n / kTileQueue) & 1u);
   if (warp_level) ok = __all_sync(0xffffffffu, ok);
-  *tile = ok ? reinterpret_cast<const volatile int*>(q)[s] : -1;
+  if (ok) {
+    const volatile QTile* p = q + s;
+    v->tile = p->tile;
+    v->row0 = p->row0;
+    v->n = p->n;
+    v->ct = p->ct;
+    v->e = p->e;
+    v->shared = p->shared;
+  } else {
+    v->tile = -1;
+  }
   if (warp_level) __syncwarp();
   if (ok && (!warp_level || (threadIdx.x % 32) == 0)) mbar_arrive(smem_u32(&empty[s]));
   return ok;

@@ -72,20 +72,17 @@ struct TcArgs {
   DevStatus* status;
 };
 
-struct Tile {
-  int row0, n, ct, e, shared, K, N;
-};
-
-__device__ __forceinline__ void decode_tile(const TcArgs& a, int tile, int ntasks, Tile& t) {
+__device__ __forceinline__ QTile decode_tile(const TcArgs& a, int tile, int ntasks) {
+  QTile t;
   int task;
   tc_tile_of(a.tasks, a.tile_start, ntasks, tile, &task, &t.ct);
   const FfnTask tk = a.tasks[task];
+  t.tile = tile;
   t.row0 = tk.row0;
   t.n = tk.nrows;
   t.shared = tk.expert < 0;
   t.e = t.shared ? 0 : tk.expert;
-  t.K = t.shared ? a.Ks : a.K;
-  t.N = t.shared ? a.Ns : a.N;
+  return t;
 }
 
 template <bool GU>
@@ -108,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = acc_empty + 2;
   uint64_t* tq_full = drain + 1;
   uint64_t* tq_empty = tq_full + kTileQueue;
-  int* tq = reinterpret_cast<int*>(tq_empty + kTileQueue);
+  QTile* tq = reinterpret_cast<QTile*>(tq_empty + kTileQueue);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq + kTileQueue);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -147,22 +144,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t iter = 0;
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
-      int tile = *abort_flag ? -1 : atomicAdd(a.sched, 1);
-      if (tile >= ntiles) tile = -1;
-      if (!tq_push(tq, tq_full, tq_empty, n, tile)) {
+      QTile t;
+      t.tile = -1;
+      if (!*abort_flag) {
+        const int tile = atomicAdd(a.sched, 1);
+        if (tile < ntiles) t = decode_tile(a, tile, ntasks);
+      }
+      if (!tq_push(tq, tq_full, tq_empty, n, t)) {
         raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
       }
-      if (tile < 0) break;
-      Tile t;
-      decode_tile(a, tile, ntasks, t);
+      if (t.tile < 0) break;
       const CUtensorMap* A0 = t.shared ? &maps.sa0 : &maps.a0;
       const CUtensorMap* A1 = t.shared ? &maps.sa1 : &maps.a1;
       const CUtensorMap* B = t.shared ? &maps.sb : &maps.b;
       const int nb = (t.n + kBoxRows - 1) / kBoxRows;
       const uint32_t bytes = (uint32_t)(G::kNA * kATileBytes + nb * kBoxBytes);
-      const int nks = (t.K + kBK - 1) / kBK;
+      const int nks = ((t.shared ? a.Ks : a.K) + kBK - 1) / kBK;
       for (int ks = 0; ks < nks; ++ks) {
         if (*abort_flag) {
           ok = false;
@@ -196,15 +195,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t iter = 0, local = 0;
     bool ok = true;
     for (uint32_t n = 0; ok; ++n, ++local) {
-      int tile;
-      if (!tq_pop(tq, tq_full, tq_empty, n, &tile, false)) {
+      QTile t;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &t, false)) {
         raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
       }
-      if (tile < 0) break;
-      Tile t;
-      decode_tile(a, tile, ntasks, t);
+      if (t.tile < 0) break;
       const uint32_t buf = local & 1u, use = local >> 1;
       if (!mbar_wait(smem_u32(&acc_empty[buf]), (use & 1u) ^ 1u)) {
         raise_status(a.status, kStTimeout, kind);
@@ -216,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16_f32(kTcM, nmma);
       const uint32_t d0 = tmem + buf * G::kAccStride;
       const uint32_t d1 = d0 + kTcMaxN;
-      const int nks = (t.K + kBK - 1) / kBK;
+      const int nks = ((t.shared ? a.Ks : a.K) + kBK - 1) / kBK;
       for (int ks = 0; ks < nks; ++ks) {
         if (*abort_flag) {
           ok = false;
@@ -255,15 +252,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp % 4;  // TMEM lane quadrant this warp may access
     uint32_t local = 0;
     for (uint32_t n = 0;; ++n, ++local) {
-      int tile;
-      if (!tq_pop(tq, tq_full, tq_empty, n, &tile, true)) {
+      QTile t;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &t, true)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
       }
-      if (tile < 0 || warp_flag(abort_flag)) break;
-      Tile t;
-      decode_tile(a, tile, ntasks, t);
+      if (t.tile < 0 || warp_flag(abort_flag)) break;
+      const int tN = t.shared ? a.Ns : a.N;
       const uint32_t buf = local & 1u, use = local >> 1;
       if (!warp_wait(smem_u32(&acc_full[buf]), use & 1u)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
@@ -278,15 +274,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(trow + j0, g);
         if (GU) tmem_ld16(trow + kTcMaxN + j0, u);
         tmem_ld_wait();
-        if (ch < t.N) {
+        if (ch < tN) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int tok = j0 + i;
             if (tok < t.n) {
-              const size_t o = (size_t)(t.row0 + tok) * t.N + ch;
+              const size_t o = (size_t)(t.row0 + tok) * tN + ch;
               const float gv = __uint_as_float(g[i]);
               if (GU) {
-                const float h = gv / (1.f + expf(-gv)) * __uint_as_float(u[i]);
+                const float h = gv * __frcp_rn(1.f + __expf(-gv)) * __uint_as_float(u[i]);
                 (t.shared ? a.sout_h : a.out_h)[o] = f_to_bf16(h);
               } else {
                 (t.shared ? a.sout_y : a.out_y)[o] = gv;

@@ -16,19 +16,20 @@
 // fails it to an exact CUDA-core integer kernel, so results are exact for all
 // inputs.
 //
-// Tensor-core kernel: persistent CTAs, tiles of 128 output channels x up to 256
-// token rows, warp-specialised around three shared-memory rings:
+// Tensor-core kernel: persistent CTAs with dynamic tile scheduling, tiles of
+// 128 output channels x up to 256 token rows, warp-specialised around three
+// shared-memory rings:
 //   raw ring   int8 weight tiles, written by TMA
 //   conv ring  the same tiles as 128-byte-swizzled integer-valued fp16, written
 //              by the converter warps (which also sum squares with dp4a)
 //   act ring   fp16 activation rows, written by TMA
 // so TMA, conversion and MMA each run ahead on their own ring.
-//   warp 0    : TMA producer (raw and act rings)
+//   warp 0    : tile claims and decoding, TMA producer (raw and act rings)
 //   warp 1    : TMEM allocation, MMA issue
 //   warps 2-5 : epilogue (dequantise, SwiGLU or store, guard)
 //   warps 6-9 : int8 -> fp16 converters
-// TMEM: gate/up keeps one accumulator pair (gate columns 0-255, up 256-511);
-// down and raw modes double-buffer 256-column accumulators.
+// TMEM: a gate/up tile's accumulators fill all 512 columns (gate 0-255, up
+// 256-511); down and raw modes double-buffer 256-column accumulators.
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -46,26 +47,32 @@ constexpr int kThreads = 320;
 constexpr int kBK = 64;
 constexpr int kRawTileBytes = kTcM * kBK;        // 8 KB of int8
 constexpr int kF16TileBytes = kTcM * kBK * 2;    // 16 KB of fp16
-constexpr int kActTileBytes = kW8MaxN * kBK * 2; // 32 KB
 constexpr int kBoxRows = 64;                     // activation rows per TMA box
 constexpr int kBoxBytes = kBoxRows * kBK * 2;    // 8 KB
 constexpr long long kGuard = 1LL << 48;          // (2^24)^2
-constexpr int kAccCols = 256;                    // TMEM columns of one accumulator
+constexpr int kAccCols = 256;                    // TMEM columns of one accumulator buffer
 
+// Tiles take up to 256 token rows.  Down and raw tiles double-buffer their
+// 256-column accumulators so the epilogue of one tile overlaps the MMAs of the
+// next; a gate/up tile needs all 512 columns (gate 0-255, up 256-511), so its
+// epilogue runs between tiles.  (128-row gate/up tiles with two buffers were
+// measured slower: they double the weight conversion and traffic per token.)
 template <int MODE>
 struct Geom {
-  static constexpr int kNA = MODE == kW8GateUp ? 2 : 1;     // weight matrices per tile
-  static constexpr int kSRaw = MODE == kW8GateUp ? 3 : 4;   // raw ring stages
-  static constexpr int kSAct = MODE == kW8GateUp ? 3 : 4;   // act ring stages
-  static constexpr int kSConv = 2;                          // conv ring stages
-  static constexpr int kAccBufs = MODE == kW8GateUp ? 1 : 2;
+  static constexpr int kNA = MODE == kW8GateUp ? 2 : 1;      // weight matrices per tile
+  static constexpr int kTN = kW8MaxN;                        // token rows per tile
+  static constexpr int kAccBufs = MODE == kW8GateUp ? 1 : 2; // accumulator buffers
+  static constexpr int kSRaw = MODE == kW8GateUp ? 3 : 4;    // raw ring stages
+  static constexpr int kSAct = MODE == kW8GateUp ? 3 : 4;    // act ring stages
+  static constexpr int kSConv = 2;                           // conv ring stages
   static constexpr int kTmemCols = 512;
+  static constexpr int kActBytes = kTN * kBK * 2;
   static constexpr int kConvBytes = kNA * kF16TileBytes;
   static constexpr int kRawBytes = kNA * kRawTileBytes;
   // [conv stages][act stages][raw stages][barriers][weight norms]; the first two
   // hold 128-byte-swizzled tiles and stay 1024-byte aligned
   static constexpr int kActOff = kSConv * kConvBytes;
-  static constexpr int kRawOff = kActOff + kSAct * kActTileBytes;
+  static constexpr int kRawOff = kActOff + kSAct * kActBytes;
   static constexpr int kBarOff = kRawOff + kSRaw * kRawBytes;
   static constexpr int kBarBytes = 512;
   static constexpr int kNormOff = kBarOff + kBarBytes;
@@ -74,6 +81,9 @@ struct Geom {
 };
 static_assert(Geom<kW8GateUp>::kSmemBytes <= 227 * 1024, "gate/up shared memory");
 static_assert(Geom<kW8Down>::kSmemBytes <= 227 * 1024, "down shared memory");
+static_assert(Geom<kW8GateUp>::kNA * Geom<kW8GateUp>::kTN * Geom<kW8GateUp>::kAccBufs <= 512,
+              "gate/up accumulators");
+static_assert(Geom<kW8Down>::kTN * Geom<kW8Down>::kAccBufs <= 512, "down accumulators");
 
 struct Maps {
   CUtensorMap a0, a1;  // int8 weights [E][N][K]
@@ -98,17 +108,18 @@ struct Args {
   DevStatus* status;
 };
 
-struct Tile {
-  int row0, n, ct, e;
-};
-
-__device__ __forceinline__ void decode(const Args& a, int tile, int ntasks, Tile& t) {
+// Tile id -> rows, channel tile, expert.
+__device__ __forceinline__ QTile decode(const Args& a, int tile, int ntasks) {
+  QTile t;
   int task;
   tc_tile_of(a.tasks, a.tile_start, ntasks, tile, &task, &t.ct);
   const FfnTask tk = a.tasks[task];
+  t.tile = tile;
   t.row0 = tk.row0;
   t.n = tk.nrows;
   t.e = tk.expert;
+  t.shared = 0;
+  return t;
 }
 
 // One output element from its exact integer accumulator(s); sw0/sw1 are the
@@ -124,7 +135,7 @@ __device__ __forceinline__ void emit(const Args& a, int row, int ch, int acc0, i
   const float v0 = (float)acc0 * sr * sw0;
   if (MODE == kW8GateUp) {
     const float v1 = (float)acc1 * sr * sw1;
-    a.out_f32[o] = v0 / (1.f + expf(-v0)) * v1;
+    a.out_f32[o] = v0 * __frcp_rn(1.f + __expf(-v0)) * v1;
   } else {
     a.out_f32[o] = v0;
   }
@@ -135,11 +146,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     w8a8_tc_kernel(const __grid_constant__ Maps maps, const Args a) {
   using G = Geom<MODE>;
   constexpr int NA = G::kNA;
+  constexpr int TN = G::kTN;
   extern __shared__ uint8_t smem_raw[];
   const int kind = MODE == kW8GateUp ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
   const int ntasks = a.counts[a.task_slot];
   const int ntiles = a.counts[a.tile_slot];
-  if (ntiles <= 0 || (int)blockIdx.x >= ntiles) return;
+  if (ntiles <= 0) return;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -156,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = norm_empty + 2;
   uint64_t* tq_full = drain + 1;
   uint64_t* tq_empty = tq_full + kTileQueue;
-  int* tq = reinterpret_cast<int*>(tq_empty + kTileQueue);
+  QTile* tq = reinterpret_cast<QTile*>(tq_empty + kTileQueue);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq + kTileQueue);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* tile_bad = abort_flag + 1;   // [2], per accumulator buffer
@@ -206,16 +218,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n_raw = 0, n_act = 0;  // copies issued into each ring
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
-      int tile = *abort_flag ? -1 : atomicAdd(a.sched, 1);
-      if (tile >= ntiles) tile = -1;
-      if (!tq_push(tq, tq_full, tq_empty, n, tile)) {
+      QTile t;
+      t.tile = -1;
+      if (!*abort_flag) {
+        const int tile = atomicAdd(a.sched, 1);
+        if (tile < ntiles) t = decode(a, tile, ntasks);
+      }
+      if (!tq_push(tq, tq_full, tq_empty, n, t)) {
         raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
       }
-      if (tile < 0) break;
-      Tile t;
-      decode(a, tile, ntasks, t);
+      if (t.tile < 0) break;
       const int nb = (t.n + kBoxRows - 1) / kBoxRows;
       for (int ks = 0; ks < nks; ++ks) {
         if (*abort_flag) {
@@ -244,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bar = smem_u32(&act_full[sa]);
         mbar_arrive_expect_tx(bar, (uint32_t)(nb * kBoxBytes));
-        const uint32_t act = smem_u32(smem + G::kActOff + sa * kActTileBytes);
+        const uint32_t act = smem_u32(smem + G::kActOff + sa * G::kActBytes);
         for (int j = 0; j < nb; ++j)
           tma_load_3d(act + j * kBoxBytes, &maps.b, ks * kBK, t.row0 + j * kBoxRows, 0, bar, pol_x);
         ++n_act;
@@ -260,15 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, local = 0;
     bool ok = true;
     for (uint32_t n = 0; ok; ++n, ++local) {
-      int tile;
-      if (!tq_pop(tq, tq_full, tq_empty, n, &tile, false)) {
+      QTile t;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &t, false)) {
         raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
       }
-      if (tile < 0) break;
-      Tile t;
-      decode(a, tile, ntasks, t);
+      if (t.tile < 0) break;
       const uint32_t buf = local % G::kAccBufs, use = local / G::kAccBufs;
       if (!mbar_wait(smem_u32(&acc_empty[buf]), (use & 1u) ^ 1u)) {
         raise_status(a.status, kStTimeout, kind);
@@ -293,14 +305,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t wa = smem_u32(smem + sc * G::kConvBytes);
-        const uint32_t xb = smem_u32(smem + G::kActOff + sa * kActTileBytes);
+        const uint32_t xb = smem_u32(smem + G::kActOff + sa * G::kActBytes);
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k) {
           const uint64_t bdesc = sdesc_sw128(xb + k * 32);
           const uint32_t acc = (ks > 0 || k > 0) ? 1u : 0u;
           tc_mma_bf16(d0, sdesc_sw128(wa + k * 32), bdesc, idesc, acc);
           if (NA == 2)
-            tc_mma_bf16(d0 + kAccCols, sdesc_sw128(wa + kF16TileBytes + k * 32), bdesc, idesc, acc);
+            tc_mma_bf16(d0 + TN, sdesc_sw128(wa + kF16TileBytes + k * 32), bdesc, idesc, acc);
         }
         tc_commit(smem_u32(&conv_empty[sc]));
         tc_commit(smem_u32(&act_empty[sa]));
@@ -317,13 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ti = threadIdx.x - 6 * 32;  // 0..127
     uint32_t it = 0, local = 0;
     for (uint32_t n = 0;; ++n, ++local) {
-      int tile;
-      if (!tq_pop(tq, tq_full, tq_empty, n, &tile, true)) {
+      QTile t;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &t, true)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
       }
-      if (tile < 0 || warp_flag(abort_flag)) break;
+      if (t.tile < 0 || warp_flag(abort_flag)) break;
       int32_t nrm[NA][4];
 #pragma unroll
       for (int m = 0; m < NA; ++m)
@@ -400,17 +412,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp % 4;
     uint32_t local = 0;
     for (uint32_t n = 0;; ++n, ++local) {
-      int tile;
-      if (!tq_pop(tq, tq_full, tq_empty, n, &tile, true)) {
+      QTile t;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &t, true)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
       }
-      if (tile < 0 || warp_flag(abort_flag)) break;
-      Tile t;
-      decode(a, tile, ntasks, t);
+      if (t.tile < 0 || warp_flag(abort_flag)) break;
       const uint32_t buf = local % G::kAccBufs, use = local / G::kAccBufs;
-      const uint32_t nb = local & 1u, nuse = local >> 1;
+      const uint32_t nb = local & 1u, nuse = local >> 1;  // weight-norm buffers
       if (!warp_wait(smem_u32(&acc_full[buf]), use & 1u) ||
           !warp_wait(smem_u32(&norm_full[nb]), nuse & 1u)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
@@ -430,22 +440,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
       bool bad = false;
-      for (int j0 = 0; j0 < t.n; j0 += 16) {
-        uint32_t g[16], u[16];
-        tmem_ld16(trow + j0, g);
-        if (NA == 2) tmem_ld16(trow + kAccCols + j0, u);
-        tmem_ld_wait();
+      for (int c0 = 0; c0 < t.n; c0 += 32) {
+        // row data of 32 tokens: one coalesced load, then shuffles
+        const int tl = c0 + lane;
+        int xn = 0;
+        float sr_l = 0.f;
+        if (tl < t.n) {
+          xn = a.row_norm2[t.row0 + tl];
+          if (MODE != kW8Raw) sr_l = a.row_scale[t.row0 + tl];
+        }
+        // the guard for this channel over these rows: the largest row norm decides
+        int xmax = xn;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int tok = j0 + i;
-          if (tok < t.n) {
-            const int row = t.row0 + tok;
-            const long long xn = a.row_norm2[row];
-            bad |= xn * wn0 >= kGuard || (NA == 2 && xn * wn1 >= kGuard);
-            if (live)
-              emit<MODE>(a, row, ch, __float2int_rn(__uint_as_float(g[i])),
-                         NA == 2 ? __float2int_rn(__uint_as_float(u[i])) : 0,
-                         MODE == kW8Raw ? 0.f : a.row_scale[row], sw0, sw1);
+        for (int o = 16; o > 0; o >>= 1) xmax = max(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
+        bad |= (long long)xmax * wn0 >= kGuard || (NA == 2 && (long long)xmax * wn1 >= kGuard);
+        const int cn = min(32, t.n - c0);
+        for (int j0 = 0; j0 < cn; j0 += 16) {
+          uint32_t g[16], u[16];
+          tmem_ld16(trow + c0 + j0, g);
+          if (NA == 2) tmem_ld16(trow + TN + c0 + j0, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float sr = __shfl_sync(0xffffffffu, sr_l, j0 + i);
+            if (j0 + i < cn && live)
+              emit<MODE>(a, t.row0 + c0 + j0 + i, ch, __float2int_rn(__uint_as_float(g[i])),
+                         NA == 2 ? __float2int_rn(__uint_as_float(u[i])) : 0, sr, sw0, sw1);
           }
         }
       }
@@ -460,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tile_bad[buf]) {
             const int slot = atomicAdd(&a.redo[0], 1);
             if (slot < a.redo_cap)
-              a.redo[1 + slot] = tile;
+              a.redo[1 + slot] = t.tile;
             else
               raise_status(a.status, kStInternal, kind);
           }
@@ -499,8 +519,7 @@ __global__ void __launch_bounds__(256, 1)
   const int nredo = min(a.redo[0], a.redo_cap);
   const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;  // 8 channels x 8 tokens each
   for (int idx = blockIdx.x; idx < nredo; idx += gridDim.x) {
-    Tile t;
-    decode(a, a.redo[1 + idx], ntasks, t);
+    const QTile t = decode(a, a.redo[1 + idx], ntasks);
     const size_t mat = (size_t)a.N * a.K;
     for (int tb = 0; tb < t.n; tb += kPass) {
       const int tn = min(kPass, t.n - tb);
