@@ -26,7 +26,9 @@
 // so TMA, conversion and MMA each run ahead on their own ring.
 //   warp 0    : tile claims and decoding, TMA producer (raw and act rings)
 //   warp 1    : TMEM allocation, MMA issue
-//   warps 2-5 : epilogue (dequantise, SwiGLU or store, guard)
+//   warps 2-5, 10-13 : epilogue (dequantise, SwiGLU or store, guard); two warps
+//               share each 32-lane TMEM quadrant and take one half of the
+//               tile's token columns each
 //   warps 6-9 : int8 -> fp16 converters
 // TMEM: a gate/up tile's accumulators fill all 512 columns (gate 0-255, up
 // 256-511); down and raw modes double-buffer 256-column accumulators.
@@ -43,7 +45,8 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
+constexpr int kEpiWarps = 8;
 constexpr int kBK = 64;
 constexpr int kRawTileBytes = kTcM * kBK;        // 8 KB of int8
 constexpr int kF16TileBytes = kTcM * kBK * 2;    // 16 KB of fp16
@@ -191,16 +194,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
-      mbar_init(smem_u32(&acc_empty[b]), 4);
+      mbar_init(smem_u32(&acc_empty[b]), kEpiWarps);
       mbar_init(smem_u32(&norm_full[b]), 4);
-      mbar_init(smem_u32(&norm_empty[b]), 4);
+      mbar_init(smem_u32(&norm_empty[b]), kEpiWarps);
       tile_bad[b] = 0;
       tile_done[b] = 0;
     }
     mbar_init(smem_u32(drain), 1);
     for (int s = 0; s < kTileQueue; ++s) {
       mbar_init(smem_u32(&tq_full[s]), 1);
-      mbar_init(smem_u32(&tq_empty[s]), 9);  // MMA thread + 4 converter + 4 epilogue warps
+      mbar_init(smem_u32(&tq_empty[s]), 5 + kEpiWarps);  // MMA thread, converter, epilogue warps
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(smem_u32(drain));
       mbar_wait(smem_u32(drain), 0u);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < 10) {
     // ---------------------------------------------------------- converter --
     const int ti = threadIdx.x - 6 * 32;  // 0..127
     uint32_t it = 0, local = 0;
@@ -409,7 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 2) {
     // ----------------------------------------------------------- epilogue --
-    const int q = warp % 4;
+    const int q = warp % 4;              // TMEM lane quadrant
+    const int half = warp >= 10 ? 1 : 0; // token-column half of the tile
     uint32_t local = 0;
     for (uint32_t n = 0;; ++n, ++local) {
       QTile t;
@@ -440,12 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
       bool bad = false;
-      for (int c0 = 0; c0 < t.n; c0 += 32) {
+      const int cend = min(t.n, (half + 1) * (TN / 2));
+      for (int c0 = half * (TN / 2); c0 < cend; c0 += 32) {
         // row data of 32 tokens: one coalesced load, then shuffles
         const int tl = c0 + lane;
         int xn = 0;
         float sr_l = 0.f;
-        if (tl < t.n) {
+        if (tl < cend) {
           xn = a.row_norm2[t.row0 + tl];
           if (MODE != kW8Raw) sr_l = a.row_scale[t.row0 + tl];
         }
@@ -454,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) xmax = max(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
         bad |= (long long)xmax * wn0 >= kGuard || (NA == 2 && (long long)xmax * wn1 >= kGuard);
-        const int cn = min(32, t.n - c0);
+        const int cn = min(32, cend - c0);
         for (int j0 = 0; j0 < cn; j0 += 16) {
           uint32_t g[16], u[16];
           tmem_ld16(trow + c0 + j0, g);
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         if (any_bad) atomicOr((int*)&tile_bad[buf], 1);
         __threadfence_block();
-        if (atomicAdd((int*)&tile_done[buf], 1) == 3) {
+        if (atomicAdd((int*)&tile_done[buf], 1) == kEpiWarps - 1) {
           if (tile_bad[buf]) {
             const int slot = atomicAdd(&a.redo[0], 1);
             if (slot < a.redo_cap)
