@@ -40,7 +40,7 @@ PROFILE_TABLE = os.path.join(ROOT, "profiles", "traffic.json")
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="longcat")
@@ -102,12 +102,18 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # nvidia-smi takes a moment to start: wait (bounded) for its first
+            # sample so the timed region is covered from its start
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+                time.sleep(0.01)
         except (FileNotFoundError, OSError):
             self.proc = None
+        self.first = max(0, len(self.lines) - 1)  # the sample current at the start
         return self
 
     def _read(self):
@@ -127,7 +133,7 @@ class ClockSampler:
             return None
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[self.first:]:
             p = [s.strip() for s in ln.split(",")]
             if len(p) < 9:
                 continue
@@ -205,13 +211,13 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel, algorithmic_bytes):
+def traffic_for(kernel, algorithmic_bytes, wdtype):
     """DRAM bytes of one launch: the committed ncu capture's ratio of DRAM bytes to
     algorithmic bytes (taken on a smaller case of the same kernel; traffic grows
     with the weight bytes streamed) times this launch's algorithmic bytes.  None
     when there is no capture or the kernel source changed since it was taken."""
     try:
-        rec = json.load(open(PROFILE_TABLE)).get(kernel)
+        rec = json.load(open(PROFILE_TABLE)).get(f"{kernel}/{wdtype}")
     except (OSError, ValueError):
         return None
     if not rec or rec.get("source_hash") != kernel_source_hash(rec["source_files"]):
@@ -469,13 +475,13 @@ def run_ours(args, rank, world, local):
             achieved = kf / sec / 1e12
             roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tpeak,
                     "unit": "TFLOP/s", "frac": achieved / tpeak, "peak_source": tpeak_kind,
-                    "traffic": traffic_for(dom, kb),
+                    "traffic": traffic_for(dom, kb, spec["wdtype"]),
                     "algorithmic_flops_per_launch": kf, "avg_launch_ms": dom_ms / dom_n}
         else:
             achieved = kb / sec / 1e9
             roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
-                    "traffic": traffic_for(dom, kb),
+                    "traffic": traffic_for(dom, kb, spec["wdtype"]),
                     "algorithmic_bytes_per_launch": kb, "avg_launch_ms": dom_ms / dom_n}
     layer_gbs = alg_bytes / (ms_step / 1e3) / 1e9
     layer_flops = sum(f for k_, (b_, f) in work.items() if k_.startswith(("tc_", "gemv_")))
