@@ -8,9 +8,11 @@
 //   h[tok, ch]      = silu(D_gate) * D_up              (epilogue, bf16)
 //   D[ch, tok]      = W_down[e][ch, :] . h[tok, :]     -> y[tok, ch] (fp32)
 //
-// Persistent CTAs, one per SM, warp-specialised:
+// Persistent CTAs, one per SM, dynamic tile scheduling, warp-specialised:
+//   warp 6    : claims tiles from a global counter, decodes them and queues
+//               them (up to four ahead) for the other roles.
 //   warp 0    : TMA producer -- 128x64 weight tiles (3-D map over the expert
-//               stack) and 16-row activation boxes, 128-byte swizzle, into a
+//               stack) and 64-row activation boxes, 128-byte swizzle, into a
 //               multi-stage shared-memory ring.
 //   warp 1    : allocates TMEM; one lane issues tcgen05.mma (kind::f16, bf16 in,
 //               fp32 accumulate) and commits stage releases / tile completion.
@@ -30,7 +32,8 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
+constexpr int kSchedWarp = 6;
 constexpr int kBK = 64;                          // K elements per stage: one 128-byte row
 constexpr int kATileBytes = kTcM * kBK * 2;      // 16 KB
 constexpr int kBTileBytes = kTcMaxN * kBK * 2;   // 16 KB
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(drain), 1);
     for (int s = 0; s < kTileQueue; ++s) {
       mbar_init(smem_u32(&tq_full[s]), 1);
-      mbar_init(smem_u32(&tq_empty[s]), 5);  // MMA thread + 4 epilogue warps
+      mbar_init(smem_u32(&tq_empty[s]), 6);  // producer, MMA thread, 4 epilogue warps
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -138,12 +141,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------------------------------------------------- producer --
-    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-    uint32_t iter = 0;
-    bool ok = true;
-    for (uint32_t n = 0; ok; ++n) {
+  if (warp == kSchedWarp && lane == 0) {
+    // ---------------------------------------------------------- scheduler --
+    // Claims and decodes tiles up to kTileQueue ahead of the producer, so the
+    // claim's atomic and the decode's dependent loads never stall the rings.
+    for (uint32_t n = 0;; ++n) {
       QTile t;
       t.tile = -1;
       if (!*abort_flag) {
@@ -151,6 +153,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tile < ntiles) t = decode_tile(a, tile, ntasks);
       }
       if (!tq_push(tq, tq_full, tq_empty, n, t)) {
+        raise_status(a.status, kStTimeout, kind);
+        *abort_flag = 1;
+        break;
+      }
+      if (t.tile < 0) break;
+    }
+  } else if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- producer --
+    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+    uint32_t iter = 0;
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+      QTile t;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &t, false)) {
         raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
@@ -247,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(smem_u32(drain));
       mbar_wait(smem_u32(drain), 0u);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < kSchedWarp) {  // warps 2-5
     // ----------------------------------------------------------- epilogue --
     const int q = warp % 4;  // TMEM lane quadrant this warp may access
     uint32_t local = 0;

@@ -24,7 +24,8 @@
 //              by the converter warps (which also sum squares with dp4a)
 //   act ring   fp16 activation rows, written by TMA
 // so TMA, conversion and MMA each run ahead on their own ring.
-//   warp 0    : tile claims and decoding, TMA producer (raw and act rings)
+//   warp 14   : tile claims and decoding, kTileQueue tiles ahead
+//   warp 0    : TMA producer (raw and act rings)
 //   warp 1    : TMEM allocation, MMA issue
 //   warps 2-5, 10-13 : epilogue (dequantise, SwiGLU or store, guard); two warps
 //               share each 32-lane TMEM quadrant and take one half of the
@@ -45,8 +46,9 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr int kEpiWarps = 8;
+constexpr int kSchedWarp = 14;
 constexpr int kBK = 64;
 constexpr int kRawTileBytes = kTcM * kBK;        // 8 KB of int8
 constexpr int kF16TileBytes = kTcM * kBK * 2;    // 16 KB of fp16
@@ -203,7 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(drain), 1);
     for (int s = 0; s < kTileQueue; ++s) {
       mbar_init(smem_u32(&tq_full[s]), 1);
-      mbar_init(smem_u32(&tq_empty[s]), 5 + kEpiWarps);  // MMA thread, converter, epilogue warps
+      // producer and MMA threads, converter and epilogue warps
+      mbar_init(smem_u32(&tq_empty[s]), 6 + kEpiWarps);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -215,12 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int nks = (a.K + kBK - 1) / kBK;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------------------------------------------------- producer --
-    const uint64_t pol_w = policy_evict_normal(), pol_x = policy_evict_last();
-    uint32_t n_raw = 0, n_act = 0;  // copies issued into each ring
-    bool ok = true;
-    for (uint32_t n = 0; ok; ++n) {
+  if (warp == kSchedWarp && lane == 0) {
+    // ---------------------------------------------------------- scheduler --
+    // Claims and decodes tiles up to kTileQueue ahead of the producer, so the
+    // claim's atomic and the decode's dependent loads never stall the rings.
+    for (uint32_t n = 0;; ++n) {
       QTile t;
       t.tile = -1;
       if (!*abort_flag) {
@@ -228,6 +230,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tile < ntiles) t = decode(a, tile, ntasks);
       }
       if (!tq_push(tq, tq_full, tq_empty, n, t)) {
+        raise_status(a.status, kStTimeout, kind);
+        *abort_flag = 1;
+        break;
+      }
+      if (t.tile < 0) break;
+    }
+  } else if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- producer --
+    const uint64_t pol_w = policy_evict_normal(), pol_x = policy_evict_last();
+    uint32_t n_raw = 0, n_act = 0;  // copies issued into each ring
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+      QTile t;
+      if (!tq_pop(tq, tq_full, tq_empty, n, &t, false)) {
         raise_status(a.status, kStTimeout, kind);
         *abort_flag = 1;
         break;
@@ -410,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&norm_full[nb]));
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < kSchedWarp) {  // warps 2-5 and 10-13
     // ----------------------------------------------------------- epilogue --
     const int q = warp % 4;              // TMEM lane quadrant
     const int half = warp >= 10 ? 1 : 0; // token-column half of the tile
