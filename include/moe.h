@@ -103,8 +103,11 @@ typedef struct {
   int32_t wdtype;        /* moe_wdtype */
   int32_t out_fp32;      /* moe_layer_forward `out`: 1 = fp32, 0 = bf16 */
   int32_t gemv_max_rows; /* experts with <= this many rows take the streaming GEMV
-                            path, the rest tensor-core tiles.  0 = library default,
-                            < 0 = never GEMV. */
+                            path (bf16 FMA, or int8 dp4a for MOE_W8A8), the rest
+                            tensor-core tiles.  0 = library default (bf16: 0, all
+                            tensor cores; MOE_W8A8: 4), < 0 = never GEMV.  Fixed
+                            with the workspace size: W8A8 streaming needs int8 copies
+                            of the sorted activations. */
 } moe_config;
 
 /* Human-readable name of a status. Never NULL. */

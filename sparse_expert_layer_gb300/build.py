@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
 
-SOURCES = ["abi.cu", "route.cu", "permute.cu", "gemv.cu", "gemm_tc.cu", "w8a8.cu", "combine.cu",
+SOURCES = ["abi.cu", "route.cu", "permute.cu", "gemv.cu", "gemm_tc.cu", "w8a8.cu", "gemv_i8.cu", "combine.cu",
            "route_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

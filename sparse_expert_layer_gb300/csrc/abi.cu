@@ -117,7 +117,7 @@ moe_status check_cfg(const moe_config* c, int32_t T) {
 int effective_gemv_max(const moe_config& c) {
   if (c.gemv_max_rows > 0) return c.gemv_max_rows;
   if (c.gemv_max_rows < 0) return 0;
-  return kDefaultGemvMaxRows;
+  return c.wdtype == MOE_W8A8 ? kDefaultGemvMaxRowsW8 : kDefaultGemvMaxRows;
 }
 // The GEMV launches are skipped when no unit can take that path.
 bool gemv_possible(int gemv_max) { return gemv_max > 0; }
@@ -141,6 +141,7 @@ struct Layout {
   // W8A8 only: integer-valued fp16 copies of the codes, row norms, fp32 h and
   // its codes/scales, and the guard-failure lists of the two passes
   size_t x16, xn2, h32, hq16, hsc, hn2, redo_gu, redo_dn;
+  size_t x8, h8;  // int8 codes for the W8A8 streaming path (only when it may run)
   int redo_cap;
   size_t total;
   int splits, nblk, wl_cap;
@@ -208,6 +209,9 @@ Layout make_layout(const moe_config& c, int T) {
     L.hn2 = take(R * 4);
     L.redo_gu = take((size_t)(1 + L.redo_cap) * 4);
     L.redo_dn = take((size_t)(1 + L.redo_cap) * 4);
+    const bool gemv = gemv_possible(effective_gemv_max(c));
+    L.x8 = take(gemv ? R * H : 0);
+    L.h8 = take(gemv ? R * I : 0);
   }
   L.total = off;
   return L;
@@ -387,8 +391,10 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
 }
 
 // W8A8 grouped FFN over the sorted rows (int8 codes + per-row scales).  With
-// x_perm == nullptr the codes are already in the workspace's x16 rows (with
-// their norms and scales), as the layer path's quantising gather leaves them.
+// x_perm == nullptr the codes are already in the workspace's x16 rows (and x8,
+// when the streaming path may run), with their norms and scales, as the layer
+// path's quantising gather leaves them.  Experts with at most gemv_max rows
+// stream through the dp4a GEMV, the others run on tensor-core tiles.
 moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
                         const int32_t* offsets, const void* x_perm, const float* x_scale,
                         const void* w_gate, const void* w_up, const void* w_down,
@@ -397,7 +403,10 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   const WorkList wl = worklist_view(ws, L);
   moe_config cw = c;
   cw.shared_inter = 0;
-  launch_worklist(ln, cw, T, offsets, wl, 0, 1, kW8MaxN);  // every expert on tensor-core tiles
+  const int gemv_max = effective_gemv_max(c);
+  const bool gemv = gemv_possible(gemv_max);
+  const int chunk = gemv_chunk(gemv_max);
+  launch_worklist(ln, cw, T, offsets, wl, gemv_max, chunk, kW8MaxN);
   const int64_t R = (int64_t)T * c.top_k;
   const int32_t* n_real = offsets + c.n_routed;   // rows that belong to FFN experts
   uint16_t* x16 = at<uint16_t>(ws, L.x16);
@@ -409,6 +418,26 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   if (x_perm)
     launch_i8_rows_to_f16(ln, static_cast<const int8_t*>(x_perm), x16, xn2, (int)R, c.hidden,
                           n_real);
+  const int8_t* x8 = x_perm ? static_cast<const int8_t*>(x_perm) : at<int8_t>(ws, L.x8);
+  int8_t* h8 = gemv ? at<int8_t>(ws, L.h8) : nullptr;
+
+  GemvI8Pass vg{};
+  vg.tasks = wl.gemv_tasks;
+  vg.item_start = wl.gemv_start_gu;
+  vg.counts = wl.counts;
+  vg.task_slot = kWlGemvTasks;
+  vg.item_slot = kWlGemvItemsGU;
+  vg.w0 = static_cast<const int8_t*>(w_gate);
+  vg.w1 = static_cast<const int8_t*>(w_up);
+  vg.s0 = s_gate;
+  vg.s1 = s_up;
+  vg.act = x8;
+  vg.row_scale = x_scale;
+  vg.out_f32 = at<float>(ws, L.h32);
+  vg.K = c.hidden;
+  vg.N = c.inter;
+  vg.max_rows = chunk;
+  if (gemv) launch_gemv_i8_gate_up(ln, vg);
 
   W8Pass g{};
   g.mode = kW8GateUp;
@@ -434,7 +463,21 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   g.N = c.inter;
   if (!launch_w8a8(ln, g)) return MOE_ERR_CUDA;
 
-  launch_quant_rows(ln, h32, hq16, hsc, hn2, (int)R, c.inter, n_real);
+  launch_quant_rows(ln, h32, hq16, h8, hsc, hn2, (int)R, c.inter, n_real);
+
+  GemvI8Pass vd = vg;
+  vd.item_start = wl.gemv_start_dn;
+  vd.item_slot = kWlGemvItemsDN;
+  vd.w0 = static_cast<const int8_t*>(w_down);
+  vd.w1 = nullptr;
+  vd.s0 = s_down;
+  vd.s1 = nullptr;
+  vd.act = h8;
+  vd.row_scale = hsc;
+  vd.out_f32 = y_perm;
+  vd.K = c.inter;
+  vd.N = c.hidden;
+  if (gemv) launch_gemv_i8_down(ln, vd);
 
   W8Pass d = g;
   d.mode = kW8Down;
@@ -665,7 +708,9 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
   }
   run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale);
   if (w8 && c.n_routed > 0)
-    launch_quant_gather(ln, c, T, x, ids, e2s, at<uint16_t>(ws, L.x16), x_scale,
+    launch_quant_gather(ln, c, T, x, ids, e2s, at<uint16_t>(ws, L.x16),
+                        gemv_possible(effective_gemv_max(c)) ? at<int8_t>(ws, L.x8) : nullptr,
+                        x_scale,
                         at<int32_t>(ws, L.xn2));
   moe_status fs = MOE_OK;
   if (w8 && c.n_routed > 0)

@@ -31,6 +31,7 @@ constexpr int kKS = 1024;                      // elements per row slice
 constexpr int kSliceBytes = kKS * 2;           // bytes per row slice
 constexpr int kWRows = 2 * kConsumerWarps;     // weight row slices per stage
 constexpr int kRingBudget = 200 * 1024;        // shared memory for the ring
+constexpr int kStartsCache = 2048;             // item starts kept in shared memory
 
 // A stage holds the 16 weight row slices plus room for NR activation slices, so
 // a smaller row cap leaves room for more stages (more bytes in flight).
@@ -39,7 +40,8 @@ struct Ring {
   static constexpr int kStageBytes = (kWRows + NR) * kSliceBytes;
   static constexpr int kStages = kRingBudget / kStageBytes < 8 ? kRingBudget / kStageBytes : 8;
   static constexpr int kBarOffset = kStages * kStageBytes;
-  static constexpr int kSmemBytes = kBarOffset + 256;
+  static constexpr int kStartsOffset = kBarOffset + 256;  // cached item starts
+  static constexpr int kSmemBytes = kStartsOffset + kStartsCache * 4;
 };
 
 union F2 {
@@ -66,17 +68,18 @@ struct Item {
 };
 
 template <bool GU>
-__device__ __forceinline__ void decode_item(const GemvPass& p, int item, int ntasks, Item& it) {
+__device__ __forceinline__ void decode_item(const GemvPass& p, const int32_t* starts, int item,
+                                            int ntasks, Item& it) {
   int lo = 0, hi = ntasks - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.item_start[mid] <= item)
+    if (starts[mid] <= item)
       lo = mid;
     else
       hi = mid - 1;
   }
   const FfnTask tk = p.tasks[lo];
-  const int block = item - p.item_start[lo];
+  const int block = item - starts[lo];
   const bool shared = tk.expert < 0;
   it.n = tk.nrows;
   it.row0 = tk.row0;
@@ -192,17 +195,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvPass p, DevStatus
     *abort_flag = 0;
     fence_barrier_init();
   }
-  __syncthreads();
   const int ntasks = p.counts[p.task_slot];
   const int nitems = p.counts[p.item_slot];
+  // The tasks' first items, for the per-item binary search: in shared memory
+  // when they fit, so a search costs a few shared loads instead of a chain of
+  // dependent global loads.
+  int32_t* cache = reinterpret_cast<int32_t*>(smem + G::kStartsOffset);
+  const bool cached = ntasks <= kStartsCache;
+  if (cached)
+    for (int i = threadIdx.x; i < ntasks; i += blockDim.x) cache[i] = p.item_start[i];
+  const int32_t* starts = cached ? cache : p.item_start;
+  __syncthreads();
   uint32_t iter = 0;
 
   if (warp == 0) {
     const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
     bool ok = true;
+    // the next item is decoded one item ahead, so its task load is in flight
+    // while the current item's copies are issued
+    Item nit;
+    if ((int)blockIdx.x < nitems) decode_item<GU>(p, starts, blockIdx.x, ntasks, nit);
     for (int item = blockIdx.x; ok && item < nitems; item += gridDim.x) {
-      Item it;
-      decode_item<GU>(p, item, ntasks, it);
+      const Item it = nit;
+      if (item + (int)gridDim.x < nitems) decode_item<GU>(p, starts, item + gridDim.x, ntasks, nit);
       const int chans = GU ? kGemvChGU : kGemvChDN;
       const int vrows = min(chans, it.N - it.c0);
       const int wrows = GU ? 2 * vrows : vrows;
@@ -247,9 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvPass p, DevStatus
   }
 
   const int cw = warp - 1;
+  Item nit;
+  if ((int)blockIdx.x < nitems) decode_item<GU>(p, starts, blockIdx.x, ntasks, nit);
   for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
-    Item it;
-    decode_item<GU>(p, item, ntasks, it);
+    const Item it = nit;  // decoded one item ahead, like the producer's
+    if (item + (int)gridDim.x < nitems) decode_item<GU>(p, starts, item + gridDim.x, ntasks, nit);
     bool ok;
     if (NR == 1 || it.n <= 1)
       ok = consume_item<GU, 1, NR>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);

@@ -82,6 +82,12 @@ constexpr int kW8MaxN = 256;       // token rows per W8A8 task
 // at every row count (6.4 TB/s at one row, less with more), so by default every
 // unit takes the tensor-core path; gemv_max_rows > 0 selects the GEMV path.
 constexpr int kDefaultGemvMaxRows = 0;
+// W8A8: the int8 GEMV (dp4a, no conversion) beats the converting tensor-core
+// tiles on light experts.  Measured on GB300: a LongCat-shaped W8A8 decode layer
+// 3.31 ms with tensor cores only, 2.74 ms with GEMV for <= 4 rows, 2.45 ms for
+// <= 8; the Zipf-loaded prefill layer 7.74 / 7.76 / 7.87 ms.  4 keeps prefill
+// unchanged.
+constexpr int kDefaultGemvMaxRowsW8 = 4;
 
 struct Launch {
   cudaStream_t stream;
@@ -138,6 +144,25 @@ struct GemvPass {
 };
 void launch_gemv_gate_up(const Launch& L, const GemvPass& p);
 void launch_gemv_down(const Launch& L, const GemvPass& p);
+
+// W8A8 streaming path (gemv_i8.cu): int8 weights x int8 codes with dp4a.
+struct GemvI8Pass {
+  const FfnTask* tasks;
+  const int32_t* item_start;
+  const int32_t* counts;
+  int task_slot, item_slot;
+  const int8_t* w0;         // int8 weights [E, N, K] (gate or down)
+  const int8_t* w1;         // int8 up weights (gate/up pass)
+  const float* s0;          // per-channel scales [E, N]
+  const float* s1;
+  const int8_t* act;        // int8 activation codes [rows, K]
+  const float* row_scale;   // [rows]
+  float* out_f32;           // gate/up: h [rows, N]; down: y [rows, N]
+  int K, N;
+  int max_rows;             // rows per task (1, 2, 4 or 8)
+};
+void launch_gemv_i8_gate_up(const Launch& L, const GemvI8Pass& p);
+void launch_gemv_i8_down(const Launch& L, const GemvI8Pass& p);
 
 // Grouped FFN, tensor-core path (gemm_tc.cu).  Returns false if a tensor map
 // could not be encoded (nothing launched).
@@ -200,11 +225,13 @@ void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, in
                            int R, int K, const int32_t* nrows);
 // Layer path: quantise each token once and write its codes (integer-valued
 // fp16), scale and sum of squares to the sorted rows of its FFN-expert picks.
+// x8 (int8 codes, for the streaming path) may be nullptr.
 void launch_quant_gather(const Launch& L, const moe_config& c, int T, const void* x,
-                         const int32_t* ids, const int32_t* e2s, uint16_t* x16, float* scale,
-                         int32_t* norm2);
-void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, float* scale,
-                       int32_t* norm2, int R, int K, const int32_t* nrows);
+                         const int32_t* ids, const int32_t* e2s, uint16_t* x16, int8_t* x8,
+                         float* scale, int32_t* norm2);
+// dst8 (int8 codes) may be nullptr.
+void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, int8_t* dst8,
+                       float* scale, int32_t* norm2, int R, int K, const int32_t* nrows);
 
 // Combine (combine.cu)
 void launch_combine(const Launch& L, const moe_config& c, int T, const float* y_perm,
@@ -222,7 +249,8 @@ enum {
   kAttrTcDN,
   kAttrGemvBase,                 // 8 slots: (gate/up, down) x row cap 1, 2, 4, 8
   kAttrW8Base = kAttrGemvBase + 8,  // 3 slots: W8A8 modes
-  kAttrSlots = kAttrW8Base + 3
+  kAttrGemvI8Base = kAttrW8Base + 3, // 8 slots: W8A8 GEMV (gate/up, down) x row cap
+  kAttrSlots = kAttrGemvI8Base + 8
 };
 void set_smem_attr_once(const void* func, int bytes, int slot);
 

@@ -595,13 +595,14 @@ __global__ void __launch_bounds__(256, 1)
 // Per-token quantisation fused with the gather of the layer path: one CTA per
 // token quantises its bf16 row once (symmetric int8, scale = amax / 127, round
 // half to even, as the permutation's int8 gather does) and writes the codes as
-// integer-valued fp16, with the scale and the sum of squared codes, to the
-// sorted row of each of its picks that lands on an FFN expert.
+// integer-valued fp16 (and as int8 into x8, when the streaming path may run),
+// with the scale and the sum of squared codes, to the sorted row of each of its
+// picks that lands on an FFN expert.
 constexpr int kQgThreads = 256;
 constexpr int kMaxTopKQuant = 32;  // the largest top_k the layer accepts
 __global__ void __launch_bounds__(kQgThreads)
     quant_gather_kernel(const uint16_t* x, const int32_t* ids, const int32_t* e2s, uint16_t* x16,
-                        float* scale, int32_t* norm2, int H, int k, int E_r) {
+                        int8_t* x8, float* scale, int32_t* norm2, int H, int k, int E_r) {
   __shared__ float red_f[kQgThreads / 32];
   __shared__ int red_i[kQgThreads / 32];
   __shared__ int rows[kMaxTopKQuant];
@@ -637,7 +638,7 @@ __global__ void __launch_bounds__(kQgThreads)
   for (int i = tid; i < nv; i += kQgThreads) {
     const uint4 v = __ldg(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t h[4] = {0u, 0u, 0u, 0u};
+    uint32_t h[4] = {0u, 0u, 0u, 0u}, b[2] = {0u, 0u};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float f = (j & 1) ? bf16hi(w[j / 2]) : bf16lo(w[j / 2]);
@@ -645,9 +646,13 @@ __global__ void __launch_bounds__(kQgThreads)
       if (amax > 0.f) qi = (int)fminf(127.f, fmaxf(-127.f, rintf(f / s)));
       n2 += qi * qi;
       h[j / 2] |= (uint32_t)__half_as_ushort(__int2half_rn(qi)) << (16 * (j % 2));
+      b[j / 4] |= (uint32_t)(qi & 0xff) << (8 * (j % 4));
     }
     const uint4 o = make_uint4(h[0], h[1], h[2], h[3]);
     for (int r = 0; r < n; ++r) reinterpret_cast<uint4*>(x16 + (size_t)rows[r] * H)[i] = o;
+    if (x8)
+      for (int r = 0; r < n; ++r)
+        reinterpret_cast<uint2*>(x8 + (size_t)rows[r] * H)[i] = make_uint2(b[0], b[1]);
   }
   for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
   if (lane == 0) red_i[warp] = n2;
@@ -690,10 +695,11 @@ __global__ void __launch_bounds__(256)
 }
 
 // fp32 rows -> symmetric int8 codes (scale = amax/127, round half to even),
-// stored as integer-valued fp16, with the scale and the sum of squares.
+// stored as integer-valued fp16 (and as int8 into dst8, when not nullptr), with
+// the scale and the sum of squares.
 __global__ void __launch_bounds__(256)
-    quant_rows_kernel(const float* src, uint16_t* dst, float* scale, int32_t* norm2, int R, int K,
-                      const int32_t* nrows) {
+    quant_rows_kernel(const float* src, uint16_t* dst, int8_t* dst8, float* scale, int32_t* norm2,
+                      int R, int K, const int32_t* nrows) {
   const int lane = threadIdx.x % 32;
   const int r = blockIdx.x * 8 + threadIdx.x / 32;
   const int rows = nrows ? min(R, *nrows) : R;
@@ -711,7 +717,7 @@ __global__ void __launch_bounds__(256)
   for (int i = lane; i < K / 4; i += 32) {
     const float4 v = s[i];
     const float f[4] = {v.x, v.y, v.z, v.w};
-    uint32_t h[2] = {0u, 0u};
+    uint32_t h[2] = {0u, 0u}, b = 0u;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float qf = 0.f;
@@ -719,8 +725,10 @@ __global__ void __launch_bounds__(256)
       const int qi = (int)qf;
       n2 += qi * qi;
       h[j / 2] |= (uint32_t)__half_as_ushort(__int2half_rn(qi)) << (16 * (j % 2));
+      b |= (uint32_t)(qi & 0xff) << (8 * j);
     }
     d[i] = make_uint2(h[0], h[1]);
+    if (dst8) reinterpret_cast<uint32_t*>(dst8 + (size_t)r * K)[i] = b;
   }
   for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
   if (lane == 0) {
@@ -825,19 +833,19 @@ void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, in
 }
 
 void launch_quant_gather(const Launch& L, const moe_config& c, int T, const void* x,
-                         const int32_t* ids, const int32_t* e2s, uint16_t* x16, float* scale,
-                         int32_t* norm2) {
+                         const int32_t* ids, const int32_t* e2s, uint16_t* x16, int8_t* x8,
+                         float* scale, int32_t* norm2) {
   launch_begin(L, MOE_K_PERM_GATHER);
   quant_gather_kernel<<<T, kQgThreads, 0, L.stream>>>(static_cast<const uint16_t*>(x), ids, e2s,
-                                                      x16, scale, norm2, c.hidden, c.top_k,
+                                                      x16, x8, scale, norm2, c.hidden, c.top_k,
                                                       c.n_routed);
   launch_end(L, MOE_K_PERM_GATHER);
 }
 
-void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, float* scale,
-                       int32_t* norm2, int R, int K, const int32_t* nrows) {
+void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, int8_t* dst8,
+                       float* scale, int32_t* norm2, int R, int K, const int32_t* nrows) {
   launch_begin(L, MOE_K_QUANT_H);
-  quant_rows_kernel<<<(R + 7) / 8, 256, 0, L.stream>>>(src, dst, scale, norm2, R, K, nrows);
+  quant_rows_kernel<<<(R + 7) / 8, 256, 0, L.stream>>>(src, dst, dst8, scale, norm2, R, K, nrows);
   launch_end(L, MOE_K_QUANT_H);
 }
 

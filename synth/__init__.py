@@ -68,6 +68,13 @@ CONFIGS = {
     # real layer, 4.8 GB of weights (well above the 129 MB L2, a few GB on device).
     "longcat_prof": dict(_BASE, T=16, hidden=6144, inter=2048, n_routed=64, n_zero=32,
                          top_k=12, bias_mode="logit", bias_kind="iid"),
+    # LongCat-shaped decode layer with W8A8 weights (int8 halves the bytes each
+    # step must stream): the W8A8 decode workload.
+    "longcat_w8": dict(_BASE, T=64, hidden=6144, inter=2048, n_routed=512, n_zero=256, top_k=12,
+                       bias_mode="logit", bias_kind="iid", wdtype="w8a8"),
+    # Profiling-sized relative of the W8A8 decode layer (2.4 GB of int8 weights).
+    "longcat_w8_prof": dict(_BASE, T=16, hidden=6144, inter=2048, n_routed=64, n_zero=32,
+                            top_k=12, bias_mode="logit", bias_kind="iid", wdtype="w8a8"),
     # Profiling-sized W8A8 prefill relative: full H and I, 64 experts, Zipf load,
     # 2.8 GB of int8 weights and 235 MB of activation codes.
     "w8a8_prof": dict(_BASE, T=2048, hidden=7168, inter=2048, n_routed=64, top_k=8,

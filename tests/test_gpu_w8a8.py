@@ -125,6 +125,23 @@ def test_w8a8_layer_matches_oracle(m, out_fp32):
     gs.check_out(got, ref, bf16_out=not out_fp32, what="w8a8_s")
 
 
+@pytest.mark.parametrize("T,gemv", [(512, 8), (512, 1000), (40, 8), (40, 1000), (40, 2)])
+def test_w8a8_streaming_path_matches_oracle_and_tensor_cores(m, T, gemv):
+    # Experts with <= gemv rows take the dp4a GEMV; both paths accumulate the
+    # same exact integers and dequantise with the same fp32 formula, so the
+    # layer output is bit-identical to the all-tensor-core run.
+    spec = synth.spec("w8a8_s", T=T, name=f"w8a8_s_T{T}")
+    d = gs.inputs(spec)
+    L = w8_lists(d["wts"])
+    ref, _, _, _, _ = oracle.layer_w8a8(spec, synth.bf16_bits(d["x"]), d["w_r"].numpy(),
+                                        support.np_bias(d["bias"]), L["qg"], L["sg"], L["qu"],
+                                        L["su"], L["qd"], L["sd"])
+    got = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=gemv)
+    gs.check_out(got, ref, bf16_out=False, what=f"w8a8 T={T} gemv<={gemv}")
+    tc = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=-1)
+    assert torch.equal(got, tc)
+
+
 def test_w8a8_full_size_prefill(m):
     spec = synth.spec("w8a8_prefill")
     x, w_r, bias, _ = support.make_inputs(spec)
