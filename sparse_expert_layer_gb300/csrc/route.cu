@@ -116,18 +116,33 @@ __global__ void __launch_bounds__(kRtThreads) router_kernel(RouterArgs a) {
   __syncthreads();
   if (!last) return;
   __threadfence();
-  // split outer, outputs inner: eight independent loads in flight per step,
-  // each output still summed in split order
+  // four splits' partials (32 independent loads) in flight per step; each
+  // output is still summed in split order, so the result does not depend on
+  // the grouping
   float sum[2][4] = {};
-  for (int s = 0; s < a.splits; ++s) {
-    const float* ps = a.partial + (size_t)s * a.T * a.E;
+  for (int s0 = 0; s0 < a.splits; s0 += 4) {
+    float v[4][2][4];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int t = t0 + ty * 2 + i;
+    for (int u = 0; u < 4; ++u) {
+      const float* ps = a.partial + (size_t)(s0 + u) * a.T * a.E;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int e = e0 + tx * 4 + j;
-        if (t < a.T && e < a.E) sum[i][j] += __ldcg(ps + (size_t)t * a.E + e);
+      for (int i = 0; i < 2; ++i) {
+        const int t = t0 + ty * 2 + i;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e = e0 + tx * 4 + j;
+          v[u][i][j] = (s0 + u < a.splits && t < a.T && e < a.E)
+                           ? __ldcg(ps + (size_t)t * a.E + e) : 0.f;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (s0 + u < a.splits) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sum[i][j] += v[u][i][j];
       }
     }
   }
