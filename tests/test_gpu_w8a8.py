@@ -100,6 +100,53 @@ def test_activation_codes_match_oracle_bit_for_bit(m):
     assert np.array_equal(sx.cpu().numpy(), s_o[rows])
 
 
+@pytest.mark.parametrize("gemv", [-1, 1000])
+def test_w8a8_grouped_ffn_stage_matches_oracle(m, gemv):
+    # moe_grouped_ffn on the caller's int8 x_perm (from moe_permute), on tensor
+    # cores (-1) and on the streaming path (1000); the reference runs each
+    # expert through the oracle's quantiser and exact int8 matmuls
+    spec = synth.spec("w8a8_s", T=96, name="w8a8_s_T96")
+    d = gs.inputs(spec)
+    T, k, H = spec["T"], spec["top_k"], spec["hidden"]
+    E, E_r = synth.n_experts(spec), spec["n_routed"]
+    ids_o, _, _, _ = oracle.route(spec, synth.bf16_bits(d["x"]), d["w_r"].numpy(),
+                                  support.np_bias(d["bias"]))
+    cfg = m.config_from_spec(spec, gemv_max_rows=gemv)
+    ids = torch.as_tensor(ids_o, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    s2e = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    e2s = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    xq = torch.zeros((T * k, H), dtype=torch.int8, device="cuda")
+    sx = torch.zeros(T * k, dtype=torch.float32, device="cuda")
+    ws = m.workspace(cfg, T)
+    m.moe_permute(cfg, T, ids, d["x_d"], counts, offsets, s2e, e2s, xq, sx, ws)
+    y = torch.full((T * k, H), float("nan"), dtype=torch.float32, device="cuda")
+    w = d["wts_d"]
+    m.moe_grouped_ffn(cfg, T, offsets, xq, sx, w["w_gate"], w["w_up"], w["w_down"], w["s_gate"],
+                      w["s_up"], w["s_down"], y, ws)
+    torch.cuda.synchronize()
+    assert m.moe_check_device_status(ws) == m.MOE_OK
+    # reference: the oracle's permutation and codes, per expert
+    _, off, s2e_o, _ = oracle.permute(ids_o, E)
+    q_o, s_o = oracle.quantize_rows(d["x"].float().numpy())
+    L = w8_lists(d["wts"])
+    r_real = int(off[E_r])
+    ref = np.empty((r_real, H))
+    for e in range(E_r):
+        a, b = int(off[e]), int(off[e + 1])
+        if a == b:
+            continue
+        rows = s2e_o[a:b] // k
+        qa, sa = q_o[rows], s_o[rows].astype(np.float64)[:, None]
+        g = oracle.int8_matmul(qa, L["qg"][e]) * sa * L["sg"][e].astype(np.float64)[None, :]
+        u = oracle.int8_matmul(qa, L["qu"][e]) * sa * L["su"][e].astype(np.float64)[None, :]
+        qh, sh = oracle.quantize_rows((g / (1.0 + np.exp(-g)) * u).astype(np.float32))
+        ref[a:b] = (oracle.int8_matmul(qh, L["qd"][e]) * sh.astype(np.float64)[:, None]
+                    * L["sd"][e].astype(np.float64)[None, :])
+    gs.check_out(y[:r_real], ref, bf16_out=False, what=f"w8a8 grouped ffn gemv<={gemv}")
+
+
 def w8_lists(wts, experts=None):
     E = wts["w_gate"].shape[0]
     want = set(range(E)) if experts is None else set(int(e) for e in experts)
