@@ -273,6 +273,24 @@ def oracle_runner(spec, wts, need, w_r, b):
     return lambda xb: oracle.layer(spec, xb, w_r.numpy(), b, g, u, dn, shared)
 
 
+def cpu_model():
+    """The host CPU's model, from /proc/cpuinfo (x86 'model name', or Arm implementer/part)."""
+    import platform
+
+    fields = {}
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ":" in ln:
+                k, v = ln.split(":", 1)
+                fields.setdefault(k.strip().lower(), v.strip())
+    except OSError:
+        pass
+    name = fields.get("model name")
+    if not name and "cpu part" in fields:
+        name = f"implementer {fields.get('cpu implementer', '?')} part {fields['cpu part']}"
+    return f"{platform.machine()} {name or 'unknown'}"
+
+
 def oracle_sample(spec, x, w_r, bias, wts_d, n_tok, target_s):
     """Time the fp64 oracle on the first n_tok tokens (experts copied from HBM)."""
     import oracle
@@ -331,7 +349,7 @@ def run_reference(args, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": describe(spec), "tokens_per_step": n_tok},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "nproc": os.cpu_count(), "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -398,6 +416,18 @@ def run_ours(args, rank, world, local):
     ms = max_over_ranks(ms, world, dev)
     ms_step = ms / args.steps
     value = whole_job_rate(world, T, args.steps, ms)
+
+    # per-step spread: the same K steps with an event between steps
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for i in range(args.steps):
+        layer.forward(x_d, out)
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per_step = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
+    p50 = per_step[len(per_step) // 2]
+    p90 = per_step[min(len(per_step) - 1, int(0.9 * len(per_step)))]
 
     # per-kernel breakdown: the same K steps again, each launch bracketed by
     # CUDA events on its stream (recorded by the library)
@@ -489,6 +519,7 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "ms_per_step_p50": p50, "ms_per_step_p90": p90,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8" if w8 else "bf16",
         "data": "synthetic",
@@ -516,7 +547,8 @@ def run_ours(args, rank, world, local):
         line["cpu_baseline"] = {
             "value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"first {n_tok} of {T} tokens, full layer, {n_exp} experts, "
-                      f"{reps} repetitions in {dt:.1f} s"}
+                      f"{reps} repetitions in {dt:.1f} s",
+            "nproc": os.cpu_count(), "cpu_model": cpu_model()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

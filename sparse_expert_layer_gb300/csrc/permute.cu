@@ -179,8 +179,9 @@ __global__ void __launch_bounds__(256) perm_gather_kernel(GatherArgs a) {
   }
 }
 
-// Work list of the grouped FFN.  Units are the routed experts in index order,
-// then the shared expert.  A unit with n rows becomes GEMV tasks of <= gemv_chunk
+// Work list of the grouped FFN.  Units are the shared expert first (its tiles,
+// the heaviest, start early instead of running at the pass's tail), then the
+// routed experts in index order.  A unit with n rows becomes GEMV tasks of <= gemv_chunk
 // rows when n <= gemv_max, else tensor-core tasks of <= tc_chunk rows.
 struct WlArgs {
   const int32_t* offsets;
@@ -223,13 +224,16 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
   const int units = a.E_r + (a.has_shared ? 1 : 0);
   for (int base = 0; base < units; base += blockDim.x) {
     const int u = base + threadIdx.x;
+    const int e = a.has_shared ? u - 1 : u;  // routed expert of this unit; -1: shared
     int n = 0, row0 = 0, shared = 0;
-    if (u < a.E_r) {
-      row0 = a.offsets[u];
-      n = a.offsets[u + 1] - row0;
-    } else if (u < units) {
-      n = a.T;
-      shared = 1;
+    if (u < units) {
+      if (e < 0) {
+        n = a.T;
+        shared = 1;
+      } else {
+        row0 = a.offsets[e];
+        n = a.offsets[e + 1] - row0;
+      }
     }
     const bool gemv = n > 0 && n <= a.gemv_max;
     const int n_gemv = gemv ? (n + a.gemv_chunk - 1) / a.gemv_chunk : 0;
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
         break;
       }
       FfnTask tk;
-      tk.expert = shared ? -1 : u;
+      tk.expert = shared ? -1 : e;
       tk.row0 = row0 + j * a.gemv_chunk;
       tk.nrows = min(a.gemv_chunk, n - j * a.gemv_chunk);
       tk.chunk = 0;
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
         break;
       }
       FfnTask tk;
-      tk.expert = shared ? -1 : u;
+      tk.expert = shared ? -1 : e;
       tk.row0 = row0 + j * a.tc_chunk;
       tk.nrows = min(a.tc_chunk, n - j * a.tc_chunk);
       tk.chunk = (j << 16) | n_tc;  // chunk index, chunks of this unit (tile interleaving)
