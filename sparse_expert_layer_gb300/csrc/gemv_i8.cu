@@ -230,9 +230,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_i8_kernel(GemvI8Pass p, DevS
         if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(wrows + it.n) * bytes);
         __syncwarp();
         const uint32_t sbase = smem_u32(smem + (size_t)stage * G::kStageBytes);
-        if (lane < kWRows) {
+        if (p.K == kSlice) {
+          // rows are whole slices, so a block's rows are contiguous in memory and
+          // in the stage: one copy per matrix instead of one per row
+          if (lane == 0)
+            bulk_g2s(sbase, it.w0 + (size_t)it.c0 * p.K, (uint32_t)vrows * bytes, bar, pol_w);
+          if (GU && lane == 1)
+            bulk_g2s(sbase + kGemvChGU * kSlice, it.w1 + (size_t)it.c0 * p.K,
+                     (uint32_t)vrows * bytes, bar, pol_w);
+        } else if (lane < kWRows) {
           if (wrow) bulk_g2s(sbase + lane * kSlice, wrow + (size_t)s * kSlice, bytes, bar, pol_w);
-        } else if (lane - kWRows < it.n) {
+        }
+        if (lane >= kWRows && lane - kWRows < it.n) {
           const int a = lane - kWRows;
           bulk_g2s(sbase + (kWRows + a) * kSlice, it.act + (size_t)a * p.K + (size_t)s * kSlice,
                    bytes, bar, pol_x);

@@ -72,6 +72,10 @@ CONFIGS = {
     # step must stream): the W8A8 decode workload.
     "longcat_w8": dict(_BASE, T=64, hidden=6144, inter=2048, n_routed=512, n_zero=256, top_k=12,
                        bias_mode="logit", bias_kind="iid", wdtype="w8a8"),
+    # LongCat's router and gating shape (T=64, H=6144, 768 experts, k=12) with
+    # tiny experts (I=16, 0.3 GB): profiles the routing kernels alone.
+    "longcat_router": dict(_BASE, T=64, hidden=6144, inter=16, n_routed=512, n_zero=256,
+                           top_k=12, bias_mode="logit", bias_kind="iid"),
     # Profiling-sized relative of the W8A8 decode layer (2.4 GB of int8 weights).
     "longcat_w8_prof": dict(_BASE, T=16, hidden=6144, inter=2048, n_routed=64, n_zero=32,
                             top_k=12, bias_mode="logit", bias_kind="iid", wdtype="w8a8"),

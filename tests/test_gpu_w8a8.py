@@ -172,12 +172,15 @@ def test_w8a8_layer_matches_oracle(m, out_fp32):
     gs.check_out(got, ref, bf16_out=not out_fp32, what="w8a8_s")
 
 
-@pytest.mark.parametrize("T,gemv", [(512, 8), (512, 1000), (40, 8), (40, 1000), (40, 2)])
-def test_w8a8_streaming_path_matches_oracle_and_tensor_cores(m, T, gemv):
+@pytest.mark.parametrize("T,gemv,H,I", [(512, 8, 1024, 512), (512, 1000, 1024, 512),
+                                         (40, 8, 1024, 512), (40, 1000, 1024, 512),
+                                         (40, 2, 1024, 512), (40, 8, 2048, 2048)])
+def test_w8a8_streaming_path_matches_oracle_and_tensor_cores(m, T, gemv, H, I):
     # Experts with <= gemv rows take the dp4a GEMV; both paths accumulate the
     # same exact integers and dequantise with the same fp32 formula, so the
-    # layer output is bit-identical to the all-tensor-core run.
-    spec = synth.spec("w8a8_s", T=T, name=f"w8a8_s_T{T}")
+    # layer output is bit-identical to the all-tensor-core run.  K = 2048 is
+    # the case where a block's rows are fetched in one copy per matrix.
+    spec = synth.spec("w8a8_s", T=T, hidden=H, inter=I, name=f"w8a8_s_T{T}_{H}_{I}")
     d = gs.inputs(spec)
     L = w8_lists(d["wts"])
     ref, _, _, _, _ = oracle.layer_w8a8(spec, synth.bf16_bits(d["x"]), d["w_r"].numpy(),
