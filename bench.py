@@ -180,7 +180,9 @@ def tensor_peak():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-DEFAULT_GEMV_MAX_ROWS = 0  # the library's default switch point (every unit on tensor cores)
+# the library's default switch points: bf16 units all on tensor cores, W8A8 units
+# of <= 4 rows on the int8 GEMV
+DEFAULT_GEMV_MAX_ROWS = {"bf16": 0, "w8a8": 4}
 
 
 def kernel_work(spec, counts, gemv_max_rows):
@@ -189,7 +191,8 @@ def kernel_work(spec, counts, gemv_max_rows):
     to the GEMV kernels when n <= the switch point, else to the tensor-core ones;
     bytes = its weights once + its activation rows in and results out."""
     H, I, Is, T = spec["hidden"], spec["inter"], spec["shared_inter"], spec["T"]
-    gm = gemv_max_rows if gemv_max_rows > 0 else (0 if gemv_max_rows < 0 else DEFAULT_GEMV_MAX_ROWS)
+    gm = (gemv_max_rows if gemv_max_rows > 0 else
+          (0 if gemv_max_rows < 0 else DEFAULT_GEMV_MAX_ROWS[spec["wdtype"]]))
     wb = 1 if spec["wdtype"] == "w8a8" else 2
     units = [(int(n), I) for n in counts[:spec["n_routed"]] if n > 0]
     if Is:
