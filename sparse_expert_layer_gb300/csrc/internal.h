@@ -250,7 +250,8 @@ enum {
   kAttrGemvBase,                 // 8 slots: (gate/up, down) x row cap 1, 2, 4, 8
   kAttrW8Base = kAttrGemvBase + 8,  // 3 slots: W8A8 modes
   kAttrGemvI8Base = kAttrW8Base + 3, // 8 slots: W8A8 GEMV (gate/up, down) x row cap
-  kAttrSlots = kAttrGemvI8Base + 8
+  kAttrRouter = kAttrGemvI8Base + 8,
+  kAttrSlots = kAttrRouter + 1
 };
 void set_smem_attr_once(const void* func, int bytes, int slot);
 
