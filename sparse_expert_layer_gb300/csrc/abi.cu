@@ -429,15 +429,16 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   vg.item_slot = kWlGemvItemsGU;
   vg.w0 = static_cast<const int8_t*>(w_gate);
   vg.w1 = static_cast<const int8_t*>(w_up);
+  vg.n_experts = c.n_routed;
   vg.s0 = s_gate;
   vg.s1 = s_up;
   vg.act = x8;
+  vg.act_rows = R;
   vg.row_scale = x_scale;
   vg.out_f32 = at<float>(ws, L.h32);
   vg.K = c.hidden;
   vg.N = c.inter;
-  vg.max_rows = chunk;
-  if (gemv) launch_gemv_i8_gate_up(ln, vg);
+  if (gemv && !launch_gemv_i8_gate_up(ln, vg)) return MOE_ERR_CUDA;
 
   W8Pass g{};
   g.mode = kW8GateUp;
@@ -477,7 +478,7 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   vd.out_f32 = y_perm;
   vd.K = c.inter;
   vd.N = c.hidden;
-  if (gemv) launch_gemv_i8_down(ln, vd);
+  if (gemv && !launch_gemv_i8_down(ln, vd)) return MOE_ERR_CUDA;
 
   W8Pass d = g;
   d.mode = kW8Down;

@@ -7,18 +7,22 @@
 // below 2^31 for every K the layer accepts (<= 131071), so the accumulators are
 // exact without the tensor-core path's guard, and no weight is converted.
 //
-// Same shape as the bf16 GEMV: work item = (task of <= NR rows of one expert,
-// block of 8 gate/up channel pairs or 16 down channels); persistent CTAs walk
-// the items round-robin.
-//   warp 0     : producer.  Streams 2048-byte slices of 16 weight rows and of the
-//                task's activation rows into a shared-memory ring with
-//                cp.async.bulk (weights evict-first in L2).
-//   warps 1..8 : consumers.  Warp w owns two weight rows -- (gate c, up c) in
-//                the gate/up pass, (c, c+1) in the down pass -- and its lanes
-//                split the slice into 16-byte chunks; dp4a accumulates, an
-//                integer butterfly reduces at the end of the item.
+// Work item = (task of <= 8 rows of one expert, tile of 128 output channels);
+// persistent CTAs walk the items round-robin.  Each K step of 128 bytes arrives
+// as one TMA box per weight matrix (128 rows x 128 bytes, 128-byte swizzle) and
+// one 8-row box of activation codes, into a ring of 5 (gate/up) or 10 (down)
+// stages, so few large copies keep ~170 KB per SM in flight.
+//   warp 0     : producer (TMA).
+//   warps 1..8 : consumers.  Warp w owns tile rows 16w..16w+15; lane l takes
+//                row 16w + (l % 16) and half l / 16 of each K step (four
+//                16-byte chunks).  With the swizzle, the 8 lanes of a quarter
+//                warp read 8 rows at 8 distinct chunk positions: no bank
+//                conflicts.  The two halves are added by one shuffle per row.
 //   epilogue   : acc * s_row * s_channel in fp32; gate/up: h = silu(g) * u.
-#include <math.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -29,32 +33,35 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kSlice = 2048;                   // bytes (= int8 elements) per row slice
-constexpr int kWRows = 2 * kConsumerWarps;     // weight row slices per stage
-constexpr int kRingBudget = 200 * 1024;        // shared memory for the ring
-constexpr int kStartsCache = 2048;             // item starts kept in shared memory
+constexpr int kKB = 128;                   // K bytes per step: one 128-byte swizzled row
+constexpr int kWTile = kGemvI8Ch * kKB;    // 16 KB: 128 weight rows of one K step
+constexpr int kXRows = kGemvMaxRows;       // 8 activation rows per box
+constexpr int kXBox = kXRows * kKB;        // 1 KB
+constexpr int kRingBudget = 180 * 1024;
+constexpr int kStartsCache = 2048;         // item starts kept in shared memory
+static_assert(kGemvI8Ch == 16 * kConsumerWarps, "one 16-row block per consumer warp");
 
-template <int NR>
+template <bool GU>
 struct Ring {
-  static constexpr int kStageBytes = (kWRows + NR) * kSlice;
-  static constexpr int kStages = kRingBudget / kStageBytes < 8 ? kRingBudget / kStageBytes : 8;
+  static constexpr int kNA = GU ? 2 : 1;
+  static constexpr int kStageBytes = kNA * kWTile + kXBox;  // a multiple of 1024
+  static constexpr int kStages = kRingBudget / kStageBytes;
   static constexpr int kBarOffset = kStages * kStageBytes;
-  static constexpr int kStartsOffset = kBarOffset + 256;  // cached item starts
-  static constexpr int kSmemBytes = kStartsOffset + kStartsCache * 4;
+  static constexpr int kStartsOffset = kBarOffset + 256;
+  static constexpr int kSmemBytes = 1024 + kStartsOffset + kStartsCache * 4;  // + alignment
+};
+
+struct Maps {
+  CUtensorMap w0, w1;  // int8 weights [E][N][K]
+  CUtensorMap x;       // int8 activation codes [rows][K]
 };
 
 struct Item {
-  const int8_t* w0;     // first weight row of the block's matrix (gate or down)
-  const int8_t* w1;     // up rows (gate/up pass)
-  const float* s0;      // the matrix's per-channel scales
-  const float* s1;
-  const int8_t* act;    // first activation row of the task
-  int n, row0, c0;
+  int n, row0, c0, e;
 };
 
-template <bool GU>
-__device__ __forceinline__ void decode_item(const GemvI8Pass& p, const int32_t* starts, int item,
-                                            int ntasks, Item& it) {
+__device__ __forceinline__ Item decode_item(const GemvI8Pass& p, const int32_t* starts, int item,
+                                            int ntasks) {
   int lo = 0, hi = ntasks - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -64,53 +71,34 @@ __device__ __forceinline__ void decode_item(const GemvI8Pass& p, const int32_t* 
       hi = mid - 1;
   }
   const FfnTask tk = p.tasks[lo];
-  const int block = item - starts[lo];
+  Item it;
   it.n = tk.nrows;
   it.row0 = tk.row0;
-  it.c0 = block * (GU ? kGemvChGU : kGemvChDN);
-  const size_t mat = (size_t)p.N * p.K;
-  it.w0 = p.w0 + (size_t)tk.expert * mat;
-  it.w1 = GU ? p.w1 + (size_t)tk.expert * mat : nullptr;
-  it.s0 = p.s0 + (size_t)tk.expert * p.N;
-  it.s1 = GU ? p.s1 + (size_t)tk.expert * p.N : nullptr;
-  it.act = p.act + (size_t)tk.row0 * p.K;
+  it.c0 = (item - starts[lo]) * kGemvI8Ch;
+  it.e = tk.expert;
+  return it;
 }
 
-// Row of the block that weight slice j (0..15) of a stage holds; nullptr if past N.
-template <bool GU>
-__device__ __forceinline__ const int8_t* weight_row(const Item& it, int j, int N, int K) {
-  if (GU) {
-    const int c = it.c0 + (j % kGemvChGU);
-    if (c >= N) return nullptr;
-    return (j < kGemvChGU ? it.w0 : it.w1) + (size_t)c * K;
-  }
-  const int c = it.c0 + j;
-  if (c >= N) return nullptr;
-  return it.w0 + (size_t)c * K;
-}
-
-__device__ __forceinline__ int warp_sum_i(int v) { return __reduce_add_sync(0xffffffffu, v); }
-
-template <bool GU, int NR, int RING>
+template <bool GU, int NR>
 __device__ bool consume_item(const GemvI8Pass& p, const Item& it, uint8_t* smem, uint64_t* full,
                              uint64_t* empty, volatile int* abort_flag, uint32_t& iter, int cw,
                              int lane, DevStatus* st) {
-  using G = Ring<RING>;
+  using G = Ring<GU>;
   int acc0[NR], acc1[NR];
 #pragma unroll
-  for (int r = 0; r < NR; ++r) acc0[r] = acc1[r] = 0;
+  for (int a = 0; a < NR; ++a) acc0[a] = acc1[a] = 0;
   const int n = it.n;
-  const int sa = GU ? cw : 2 * cw;                 // weight slices this warp reads
-  const int sb = GU ? kGemvChGU + cw : 2 * cw + 1;
-  const int nsl = (p.K + kSlice - 1) / kSlice;
-  // the epilogue's scales, loaded now so their latency hides behind the slices:
-  // lane r < n holds row r's activation scale; every lane the warp's two
-  // channel scales
-  const int c = GU ? it.c0 + cw : it.c0 + 2 * cw;
+  const int r = 16 * cw + (lane & 15);  // tile row this lane reads
+  const int h = lane >> 4;              // half of each K step
+  const int sw = r & 7;
+  // the epilogue's scales, loaded now so their latency hides behind the stream:
+  // lane a < n holds row a's activation scale; lanes < 16 their channel's scales
+  const int ch = it.c0 + r;
   const float sr_l = lane < n ? p.row_scale[it.row0 + lane] : 0.f;
-  const float sc0 = c < p.N ? it.s0[c] : 0.f;
-  const float sc1 = GU ? (c < p.N ? it.s1[c] : 0.f) : (c + 1 < p.N ? it.s0[c + 1] : 0.f);
-  for (int s = 0; s < nsl; ++s, ++iter) {
+  const float sc0 = ch < p.N ? p.s0[(size_t)it.e * p.N + ch] : 0.f;
+  const float sc1 = GU && ch < p.N ? p.s1[(size_t)it.e * p.N + ch] : 0.f;
+  const int nks = (p.K + kKB - 1) / kKB;
+  for (int ks = 0; ks < nks; ++ks, ++iter) {
     if (*abort_flag) return false;
     const int stage = iter % G::kStages;
     const uint32_t par = (iter / G::kStages) & 1u;
@@ -119,59 +107,64 @@ __device__ bool consume_item(const GemvI8Pass& p, const Item& it, uint8_t* smem,
       *abort_flag = 1;
       return false;
     }
-    const uint8_t* sbase = smem + (size_t)stage * G::kStageBytes;
-    const uint4* wa = reinterpret_cast<const uint4*>(sbase + sa * kSlice);
-    const uint4* wb = reinterpret_cast<const uint4*>(sbase + sb * kSlice);
-    const uint4* xs = reinterpret_cast<const uint4*>(sbase + kWRows * kSlice);
-    const int nchunks = min(kSlice, p.K - s * kSlice) / 16;
-    for (int q = lane; q < nchunks; q += 32) {
-      const uint4 A = wa[q], B = wb[q];
+    const uint8_t* wt = smem + (size_t)stage * G::kStageBytes;
+    const uint8_t* xt = wt + G::kNA * kWTile;
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        if (r < n) {
-          const uint4 X = xs[r * (kSlice / 16) + q];
-          acc0[r] = __dp4a((int)A.x, (int)X.x, acc0[r]);
-          acc1[r] = __dp4a((int)B.x, (int)X.x, acc1[r]);
-          acc0[r] = __dp4a((int)A.y, (int)X.y, acc0[r]);
-          acc1[r] = __dp4a((int)B.y, (int)X.y, acc1[r]);
-          acc0[r] = __dp4a((int)A.z, (int)X.z, acc0[r]);
-          acc1[r] = __dp4a((int)B.z, (int)X.z, acc1[r]);
-          acc0[r] = __dp4a((int)A.w, (int)X.w, acc0[r]);
-          acc1[r] = __dp4a((int)B.w, (int)X.w, acc1[r]);
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const int c = 4 * h + c4;  // logical 16-byte chunk of the 128-byte row
+      const uint4 W = *reinterpret_cast<const uint4*>(wt + r * kKB + ((c ^ sw) << 4));
+      uint4 U = make_uint4(0u, 0u, 0u, 0u);
+      if (GU) U = *reinterpret_cast<const uint4*>(wt + kWTile + r * kKB + ((c ^ sw) << 4));
+#pragma unroll
+      for (int a = 0; a < NR; ++a) {
+        if (a < n) {
+          const uint4 X = *reinterpret_cast<const uint4*>(xt + a * kKB + ((c ^ (a & 7)) << 4));
+          acc0[a] = __dp4a((int)W.x, (int)X.x, acc0[a]);
+          acc0[a] = __dp4a((int)W.y, (int)X.y, acc0[a]);
+          acc0[a] = __dp4a((int)W.z, (int)X.z, acc0[a]);
+          acc0[a] = __dp4a((int)W.w, (int)X.w, acc0[a]);
+          if (GU) {
+            acc1[a] = __dp4a((int)U.x, (int)X.x, acc1[a]);
+            acc1[a] = __dp4a((int)U.y, (int)X.y, acc1[a]);
+            acc1[a] = __dp4a((int)U.z, (int)X.z, acc1[a]);
+            acc1[a] = __dp4a((int)U.w, (int)X.w, acc1[a]);
+          }
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
   }
-  // epilogue: exact integer sums, then dequantisation in fp32
+  // the two halves of each row, then the epilogue on lanes 0..15
 #pragma unroll
-  for (int r = 0; r < NR; ++r) {
-    if (r < n) {
-      const int g = warp_sum_i(acc0[r]);
-      const int u = warp_sum_i(acc1[r]);
-      if (lane == r) {
-        const size_t o = (size_t)(it.row0 + r) * p.N;
-        if (GU) {
-          if (c < p.N) {
-            const float gv = (float)g * sr_l * sc0;
-            const float uv = (float)u * sr_l * sc1;
-            p.out_f32[o + c] = gv * __frcp_rn(1.f + __expf(-gv)) * uv;
-          }
-        } else {
-          if (c < p.N) p.out_f32[o + c] = (float)g * sr_l * sc0;
-          if (c + 1 < p.N) p.out_f32[o + c + 1] = (float)u * sr_l * sc1;
-        }
+  for (int a = 0; a < NR; ++a) {
+    acc0[a] += __shfl_xor_sync(0xffffffffu, acc0[a], 16);
+    if (GU) acc1[a] += __shfl_xor_sync(0xffffffffu, acc1[a], 16);
+  }
+#pragma unroll
+  for (int a = 0; a < NR; ++a) {
+    const float sr = __shfl_sync(0xffffffffu, sr_l, a);
+    if (a < n && lane < 16 && ch < p.N) {
+      const size_t o = (size_t)(it.row0 + a) * p.N + ch;
+      const float g = (float)acc0[a] * sr * sc0;
+      if (GU) {
+        const float u = (float)acc1[a] * sr * sc1;
+        p.out_f32[o] = g * __frcp_rn(1.f + __expf(-g)) * u;
+      } else {
+        p.out_f32[o] = g;
       }
     }
   }
   return true;
 }
 
-template <bool GU, int NR>
-__global__ void __launch_bounds__(kThreads, 1) gemv_i8_kernel(GemvI8Pass p, DevStatus* st) {
-  using G = Ring<NR>;
-  extern __shared__ __align__(16) uint8_t smem[];
+template <bool GU>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_i8_kernel(const __grid_constant__ Maps maps, const GemvI8Pass p, DevStatus* st) {
+  using G = Ring<GU>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kBarOffset);
   uint64_t* empty = full + G::kStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + G::kStages);
@@ -196,61 +189,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_i8_kernel(GemvI8Pass p, DevS
   const int32_t* starts = cached ? cache : p.item_start;
   __syncthreads();
   uint32_t iter = 0;
+  const int nks = (p.K + kKB - 1) / kKB;
 
   if (warp == 0) {
-    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-    bool ok = true;
-    // the next item is decoded one item ahead, so its task load is in flight
-    // while the current item's copies are issued
-    Item nit;
-    if ((int)blockIdx.x < nitems) decode_item<GU>(p, starts, blockIdx.x, ntasks, nit);
-    for (int item = blockIdx.x; ok && item < nitems; item += gridDim.x) {
-      const Item it = nit;
-      if (item + (int)gridDim.x < nitems) decode_item<GU>(p, starts, item + gridDim.x, ntasks, nit);
-      const int chans = GU ? kGemvChGU : kGemvChDN;
-      const int vrows = min(chans, p.N - it.c0);
-      const int wrows = GU ? 2 * vrows : vrows;
-      const int8_t* wrow = weight_row<GU>(it, lane % kWRows, p.N, p.K);
-      const int nsl = (p.K + kSlice - 1) / kSlice;
-      for (int s = 0; s < nsl; ++s) {
-        if (*abort_flag) {
-          ok = false;
-          break;
-        }
-        const int stage = iter % G::kStages;
-        const uint32_t par = (iter / G::kStages) & 1u;
-        if (!mbar_wait(smem_u32(&empty[stage]), par ^ 1u)) {
-          if (lane == 0) raise_status(st, kStTimeout, GU ? MOE_K_GEMV_GATE_UP : MOE_K_GEMV_DOWN);
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        const uint32_t bytes = (uint32_t)min(kSlice, p.K - s * kSlice);  // K % 16 == 0
-        const uint32_t bar = smem_u32(&full[stage]);
-        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(wrows + it.n) * bytes);
-        __syncwarp();
-        const uint32_t sbase = smem_u32(smem + (size_t)stage * G::kStageBytes);
-        if (p.K == kSlice) {
-          // rows are whole slices, so a block's rows are contiguous in memory and
-          // in the stage: one copy per matrix instead of one per row
-          if (lane == 0)
-            bulk_g2s(sbase, it.w0 + (size_t)it.c0 * p.K, (uint32_t)vrows * bytes, bar, pol_w);
-          if (GU && lane == 1)
-            bulk_g2s(sbase + kGemvChGU * kSlice, it.w1 + (size_t)it.c0 * p.K,
-                     (uint32_t)vrows * bytes, bar, pol_w);
-        } else if (lane < kWRows) {
-          if (wrow) bulk_g2s(sbase + lane * kSlice, wrow + (size_t)s * kSlice, bytes, bar, pol_w);
-        }
-        if (lane >= kWRows && lane - kWRows < it.n) {
-          const int a = lane - kWRows;
-          bulk_g2s(sbase + (kWRows + a) * kSlice, it.act + (size_t)a * p.K + (size_t)s * kSlice,
-                   bytes, bar, pol_x);
-        }
-        ++iter;
-      }
-    }
-    // Drain: every issued copy lands before the CTA may exit.
     if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      const uint32_t bytes = (uint32_t)(G::kNA * kWTile + kXBox);
+      bool ok = true;
+      // the next item is decoded one item ahead, so its task load is in flight
+      // while the current item's copies are issued
+      Item nit = (int)blockIdx.x < nitems ? decode_item(p, starts, blockIdx.x, ntasks) : Item{};
+      for (int item = blockIdx.x; ok && item < nitems; item += gridDim.x) {
+        const Item it = nit;
+        if (item + (int)gridDim.x < nitems) nit = decode_item(p, starts, item + gridDim.x, ntasks);
+        for (int ks = 0; ks < nks; ++ks) {
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          const int stage = iter % G::kStages;
+          if (!mbar_wait(smem_u32(&empty[stage]), ((iter / G::kStages) & 1u) ^ 1u)) {
+            raise_status(st, kStTimeout, GU ? MOE_K_GEMV_GATE_UP : MOE_K_GEMV_DOWN);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(bar, bytes);
+          const uint32_t base = smem_u32(smem + (size_t)stage * G::kStageBytes);
+          tma_load_3d(base, &maps.w0, ks * kKB, it.c0, it.e, bar, pol_w);
+          if (GU) tma_load_3d(base + kWTile, &maps.w1, ks * kKB, it.c0, it.e, bar, pol_w);
+          tma_load_3d(base + G::kNA * kWTile, &maps.x, ks * kKB, it.row0, 0, bar, pol_x);
+          ++iter;
+        }
+      }
+      // every issued copy lands before the CTA may exit
       const uint32_t first = iter > (uint32_t)G::kStages ? iter - G::kStages : 0u;
       for (uint32_t j = first; j < iter; ++j)
         mbar_wait(smem_u32(&full[j % G::kStages]), (j / G::kStages) & 1u);
@@ -259,51 +232,78 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_i8_kernel(GemvI8Pass p, DevS
   }
 
   const int cw = warp - 1;
-  Item nit;
-  if ((int)blockIdx.x < nitems) decode_item<GU>(p, starts, blockIdx.x, ntasks, nit);
+  Item nit = (int)blockIdx.x < nitems ? decode_item(p, starts, blockIdx.x, ntasks) : Item{};
   for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
     const Item it = nit;  // decoded one item ahead, like the producer's
-    if (item + (int)gridDim.x < nitems) decode_item<GU>(p, starts, item + gridDim.x, ntasks, nit);
+    if (item + (int)gridDim.x < nitems) nit = decode_item(p, starts, item + gridDim.x, ntasks);
     bool ok;
-    if (NR == 1 || it.n <= 1)
-      ok = consume_item<GU, 1, NR>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
-    else if (NR == 2 || it.n <= 2)
-      ok = consume_item<GU, (NR < 2 ? NR : 2), NR>(p, it, smem, full, empty, abort_flag, iter, cw,
-                                                   lane, st);
-    else if (NR == 4 || it.n <= 4)
-      ok = consume_item<GU, (NR < 4 ? NR : 4), NR>(p, it, smem, full, empty, abort_flag, iter, cw,
-                                                   lane, st);
+    if (it.n <= 1)
+      ok = consume_item<GU, 1>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
+    else if (it.n <= 2)
+      ok = consume_item<GU, 2>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
+    else if (it.n <= 4)
+      ok = consume_item<GU, 4>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
     else
-      ok = consume_item<GU, NR, NR>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
+      ok = consume_item<GU, 8>(p, it, smem, full, empty, abort_flag, iter, cw, lane, st);
     if (!ok) break;
   }
 }
 
-template <bool GU, int NR>
-void launch_nr(const Launch& L, const GemvI8Pass& p) {
-  using G = Ring<NR>;
-  const int kind = GU ? MOE_K_GEMV_GATE_UP : MOE_K_GEMV_DOWN;
-  const int nr_slot = NR == 1 ? 0 : NR == 2 ? 1 : NR == 4 ? 2 : 3;
-  set_smem_attr_once(reinterpret_cast<const void*>(gemv_i8_kernel<GU, NR>), G::kSmemBytes,
-                     kAttrGemvI8Base + (GU ? 0 : 1) + 2 * nr_slot);
-  launch_begin(L, kind);
-  gemv_i8_kernel<GU, NR><<<L.num_sms, kThreads, G::kSmemBytes, L.stream>>>(p, L.status);
-  launch_end(L, kind);
+// ------------------------------------------------------------ host side --
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// int8 [outer][rows][K] tensor, box = 128 bytes x box_rows x 1, 128-byte swizzle;
+// out-of-range elements read as zero.
+bool map_i8_sw128(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint64_t outer,
+                  uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || !base) return false;
+  const cuuint64_t dims[3] = {K, rows, outer};
+  const cuuint64_t strides[2] = {K, rows * K};
+  const cuuint32_t box[3] = {(cuuint32_t)kKB, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool GU>
-void launch_gemv_i8(const Launch& L, const GemvI8Pass& p) {
-  switch (p.max_rows) {
-    case 1: launch_nr<GU, 1>(L, p); break;
-    case 2: launch_nr<GU, 2>(L, p); break;
-    case 4: launch_nr<GU, 4>(L, p); break;
-    default: launch_nr<GU, 8>(L, p); break;
-  }
+bool launch_gemv_i8(const Launch& L, const GemvI8Pass& p) {
+  using G = Ring<GU>;
+  Maps maps;
+  memset(&maps, 0, sizeof maps);
+  bool ok = map_i8_sw128(&maps.w0, p.w0, p.K, p.N, p.n_experts, kGemvI8Ch) &&
+            map_i8_sw128(&maps.x, p.act, p.K, p.act_rows, 1, kXRows);
+  if (GU) ok = ok && map_i8_sw128(&maps.w1, p.w1, p.K, p.N, p.n_experts, kGemvI8Ch);
+  if (!ok) return false;
+  const int kind = GU ? MOE_K_GEMV_GATE_UP : MOE_K_GEMV_DOWN;
+  set_smem_attr_once(reinterpret_cast<const void*>(gemv_i8_kernel<GU>), G::kSmemBytes,
+                     kAttrGemvI8Base + (GU ? 0 : 1));
+  launch_begin(L, kind);
+  gemv_i8_kernel<GU><<<L.num_sms, kThreads, G::kSmemBytes, L.stream>>>(maps, p, L.status);
+  launch_end(L, kind);
+  return true;
 }
 
 }  // namespace
 
-void launch_gemv_i8_gate_up(const Launch& L, const GemvI8Pass& p) { launch_gemv_i8<true>(L, p); }
-void launch_gemv_i8_down(const Launch& L, const GemvI8Pass& p) { launch_gemv_i8<false>(L, p); }
+bool launch_gemv_i8_gate_up(const Launch& L, const GemvI8Pass& p) {
+  return launch_gemv_i8<true>(L, p);
+}
+bool launch_gemv_i8_down(const Launch& L, const GemvI8Pass& p) {
+  return launch_gemv_i8<false>(L, p);
+}
 
 }  // namespace moe

@@ -73,6 +73,7 @@ struct WorkList {
 constexpr int kGemvMaxRows = 8;    // most activation rows one GEMV task carries
 constexpr int kGemvChGU = 8;       // output channels per gate/up item
 constexpr int kGemvChDN = 16;      // output channels per down item
+constexpr int kGemvI8Ch = 128;     // output channels per W8A8 streaming item (both passes)
 // Geometry of the tensor-core path (swap-AB: weights are M, tokens are N).
 constexpr int kTcM = 128;          // weight rows per tile
 constexpr int kTcMaxN = 128;       // token rows per task
@@ -145,7 +146,9 @@ struct GemvPass {
 void launch_gemv_gate_up(const Launch& L, const GemvPass& p);
 void launch_gemv_down(const Launch& L, const GemvPass& p);
 
-// W8A8 streaming path (gemv_i8.cu): int8 weights x int8 codes with dp4a.
+// W8A8 streaming path (gemv_i8.cu): int8 weights x int8 codes with dp4a, items
+// of <= 8 rows x 128 channels.  Returns false if a tensor map could not be
+// encoded (nothing launched).
 struct GemvI8Pass {
   const FfnTask* tasks;
   const int32_t* item_start;
@@ -153,16 +156,17 @@ struct GemvI8Pass {
   int task_slot, item_slot;
   const int8_t* w0;         // int8 weights [E, N, K] (gate or down)
   const int8_t* w1;         // int8 up weights (gate/up pass)
+  int n_experts;
   const float* s0;          // per-channel scales [E, N]
   const float* s1;
-  const int8_t* act;        // int8 activation codes [rows, K]
+  const int8_t* act;        // int8 activation codes [act_rows, K]
+  int64_t act_rows;
   const float* row_scale;   // [rows]
   float* out_f32;           // gate/up: h [rows, N]; down: y [rows, N]
   int K, N;
-  int max_rows;             // rows per task (1, 2, 4 or 8)
 };
-void launch_gemv_i8_gate_up(const Launch& L, const GemvI8Pass& p);
-void launch_gemv_i8_down(const Launch& L, const GemvI8Pass& p);
+bool launch_gemv_i8_gate_up(const Launch& L, const GemvI8Pass& p);
+bool launch_gemv_i8_down(const Launch& L, const GemvI8Pass& p);
 
 // Grouped FFN, tensor-core path (gemm_tc.cu).  Returns false if a tensor map
 // could not be encoded (nothing launched).

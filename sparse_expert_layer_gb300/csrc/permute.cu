@@ -350,9 +350,13 @@ void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t*
   a.gemv_max = gemv_max_rows;
   a.gemv_chunk = gemv_chunk;
   a.tc_chunk = tc_chunk;
-  a.items_gu = (c.inter + kGemvChGU - 1) / kGemvChGU;
-  a.items_gu_shared = (c.shared_inter + kGemvChGU - 1) / kGemvChGU;
-  a.items_dn = (c.hidden + kGemvChDN - 1) / kGemvChDN;
+  // W8A8 streaming items are 128-channel tiles; bf16 ones 8 gate/up pairs or 16
+  // down channels
+  const int ch_gu = c.wdtype == MOE_W8A8 ? kGemvI8Ch : kGemvChGU;
+  const int ch_dn = c.wdtype == MOE_W8A8 ? kGemvI8Ch : kGemvChDN;
+  a.items_gu = (c.inter + ch_gu - 1) / ch_gu;
+  a.items_gu_shared = (c.shared_inter + ch_gu - 1) / ch_gu;
+  a.items_dn = (c.hidden + ch_dn - 1) / ch_dn;
   a.tiles_gu = (c.inter + kTcM - 1) / kTcM;
   a.tiles_gu_shared = (c.shared_inter + kTcM - 1) / kTcM;
   a.tiles_dn = (c.hidden + kTcM - 1) / kTcM;
