@@ -181,8 +181,8 @@ def tensor_peak():
 
 
 # the library's default switch points: bf16 units all on tensor cores, W8A8 units
-# of <= 4 rows on the int8 GEMV
-DEFAULT_GEMV_MAX_ROWS = {"bf16": 0, "w8a8": 4}
+# of <= 8 rows on the int8 GEMV
+DEFAULT_GEMV_MAX_ROWS = {"bf16": 0, "w8a8": 8}
 
 
 def kernel_work(spec, counts, gemv_max_rows):

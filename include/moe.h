@@ -105,7 +105,7 @@ typedef struct {
   int32_t gemv_max_rows; /* experts with <= this many rows take the streaming GEMV
                             path (bf16 FMA, or int8 dp4a for MOE_W8A8), the rest
                             tensor-core tiles.  0 = library default (bf16: 0, all
-                            tensor cores; MOE_W8A8: 4), < 0 = never GEMV.  Fixed
+                            tensor cores; MOE_W8A8: 8), < 0 = never GEMV.  Fixed
                             with the workspace size: W8A8 streaming needs int8 copies
                             of the sorted activations. */
 } moe_config;

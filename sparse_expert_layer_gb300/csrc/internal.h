@@ -84,11 +84,10 @@ constexpr int kW8MaxN = 256;       // token rows per W8A8 task
 // unit takes the tensor-core path; gemv_max_rows > 0 selects the GEMV path.
 constexpr int kDefaultGemvMaxRows = 0;
 // W8A8: the int8 GEMV (dp4a, no conversion) beats the converting tensor-core
-// tiles on light experts.  Measured on GB300: a LongCat-shaped W8A8 decode layer
-// 3.31 ms with tensor cores only, 2.74 ms with GEMV for <= 4 rows, 2.45 ms for
-// <= 8; the Zipf-loaded prefill layer 7.74 / 7.76 / 7.87 ms.  4 keeps prefill
-// unchanged.
-constexpr int kDefaultGemvMaxRowsW8 = 4;
+// tiles on light experts.  Measured on GB300 (tensor cores only / GEMV for <= 2,
+// 4, 8, 16 rows): a LongCat-shaped W8A8 decode layer 3.31 / 2.03 / 1.77 / 1.71 /
+// 1.75 ms; the Zipf-loaded prefill layer 7.74 / - / 7.57 / 7.47 / 7.76 ms.
+constexpr int kDefaultGemvMaxRowsW8 = 8;
 
 struct Launch {
   cudaStream_t stream;
