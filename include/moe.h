@@ -239,6 +239,7 @@ typedef enum {
   MOE_K_QUANT_H,
   MOE_K_COMBINE,
   MOE_K_W8_EXACT,
+  MOE_K_SORT,  /* small batches: count, scan, scatter and work list in one launch */
   MOE_K_COUNT
 } moe_kernel_kind;
 

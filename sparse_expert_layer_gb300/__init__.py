@@ -41,7 +41,7 @@ W_BF16, W8A8 = 0, 1
 
 KERNELS = ["router", "topk", "perm_count", "perm_scan", "perm_scatter", "perm_gather",
            "worklist", "gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down", "quant_h", "combine",
-           "w8_exact"]
+           "w8_exact", "sort"]
 N_KERNELS = len(KERNELS)
 
 

@@ -279,29 +279,58 @@ moe_status run_route(const Launch& ln, const moe_config& c, int T, const Layout&
   return MOE_OK;
 }
 
-void run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
-                 const int32_t* ids, const void* x, int32_t* counts, int32_t* offsets, int32_t* s2e,
-                 int32_t* e2s, void* x_perm, float* x_scale) {
+// How the grouped FFN's work list is cut: the config it sees (shared expert
+// dropped when its weights are absent or in W8A8), the GEMV switch point and
+// chunk, and the tensor-core chunk.
+struct WlPlan {
+  moe_config cw;
+  int gemv_max, chunk, tc_chunk;
+};
+WlPlan wl_plan(const moe_config& c, bool shared_weights) {
+  WlPlan p;
+  p.cw = c;
+  if (!shared_weights || c.wdtype == MOE_W8A8) p.cw.shared_inter = 0;
+  p.gemv_max = effective_gemv_max(c);
+  p.chunk = gemv_chunk(p.gemv_max);
+  p.tc_chunk = c.wdtype == MOE_W8A8 ? kW8MaxN : kTcMaxN;
+  return p;
+}
+
+// Re-sort (and, for a plan, the work list).  Small batches take the one-CTA
+// sort; returns whether the work list was built.
+bool run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
+                 const int32_t* ids, const void* x, int32_t* counts, int32_t* offsets,
+                 int32_t* s2e, int32_t* e2s, void* x_perm, float* x_scale, const WlPlan* plan) {
   const int E = c.n_routed + c.n_zero;
-  int32_t* bc = at<int32_t>(ws, L.bc);
-  launch_perm_count(ln, T, c.top_k, E, ids, bc);
-  launch_perm_scan(ln, T, E, bc, counts, offsets);
-  launch_perm_scatter(ln, T, c.top_k, E, ids, bc, s2e, e2s);
+  bool built = false;
+  if (sort_small_fits(T, E)) {
+    const WorkList wl = worklist_view(ws, L);
+    launch_sort_small(ln, plan ? plan->cw : c, T, ids, counts, offsets, s2e, e2s,
+                      plan ? &wl : nullptr, plan ? plan->gemv_max : 0, plan ? plan->chunk : 1,
+                      plan ? plan->tc_chunk : kTcMaxN);
+    built = plan != nullptr;
+  } else {
+    int32_t* bc = at<int32_t>(ws, L.bc);
+    launch_perm_count(ln, T, c.top_k, E, ids, bc);
+    launch_perm_scan(ln, T, E, bc, counts, offsets);
+    launch_perm_scatter(ln, T, c.top_k, E, ids, bc, s2e, e2s);
+  }
   if (x_perm) launch_perm_gather(ln, c, T, ids, e2s, x, x_perm, x_scale);
+  return built;
 }
 
 // Grouped FFN over the sorted rows plus (optionally) the shared expert.
 moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
                    const int32_t* offsets, const void* x_perm, const void* w_gate,
                    const void* w_up, const void* w_down, float* y_perm, const void* x,
-                   const void* sg, const void* su, const void* sd, float* y_shared) {
+                   const void* sg, const void* su, const void* sd, float* y_shared,
+                   bool wl_built) {
   const WorkList wl = worklist_view(ws, L);
   const bool shared = c.shared_inter > 0 && sg != nullptr;
-  moe_config cw = c;
-  if (!shared) cw.shared_inter = 0;
-  const int gemv_max = effective_gemv_max(c);
-  const int chunk = gemv_chunk(gemv_max);
-  launch_worklist(ln, cw, T, offsets, wl, gemv_max, chunk, kTcMaxN);
+  const WlPlan plan = wl_plan(c, shared);
+  const int gemv_max = plan.gemv_max;
+  const int chunk = plan.chunk;
+  if (!wl_built) launch_worklist(ln, plan.cw, T, offsets, wl, gemv_max, chunk, plan.tc_chunk);
   uint16_t* h = at<uint16_t>(ws, L.h);
   uint16_t* h_s = at<uint16_t>(ws, L.h_s);
 
@@ -399,14 +428,13 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
                         const int32_t* offsets, const void* x_perm, const float* x_scale,
                         const void* w_gate, const void* w_up, const void* w_down,
                         const float* s_gate, const float* s_up, const float* s_down,
-                        float* y_perm) {
+                        float* y_perm, bool wl_built) {
   const WorkList wl = worklist_view(ws, L);
-  moe_config cw = c;
-  cw.shared_inter = 0;
-  const int gemv_max = effective_gemv_max(c);
+  const WlPlan plan = wl_plan(c, false);
+  const int gemv_max = plan.gemv_max;
   const bool gemv = gemv_possible(gemv_max);
-  const int chunk = gemv_chunk(gemv_max);
-  launch_worklist(ln, cw, T, offsets, wl, gemv_max, chunk, kW8MaxN);
+  if (!wl_built)
+    launch_worklist(ln, plan.cw, T, offsets, wl, gemv_max, plan.chunk, plan.tc_chunk);
   const int64_t R = (int64_t)T * c.top_k;
   const int32_t* n_real = offsets + c.n_routed;   // rows that belong to FFN experts
   uint16_t* x16 = at<uint16_t>(ws, L.x16);
@@ -562,7 +590,8 @@ const char* moe_status_string(moe_status s) {
 const char* moe_kernel_name(int32_t kind) {
   static const char* names[MOE_K_COUNT] = {
       "router", "topk", "perm_count", "perm_scan", "perm_scatter", "perm_gather", "worklist",
-      "gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down", "quant_h", "combine", "w8_exact"};
+      "gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down", "quant_h", "combine", "w8_exact",
+      "sort"};
   return (kind >= 0 && kind < MOE_K_COUNT) ? names[kind] : "unknown";
 }
 
@@ -615,7 +644,7 @@ moe_status moe_permute(const moe_config* cfg, int32_t T, const int32_t* topk_ids
     return MOE_OK;
   }
   run_permute(ln, *cfg, T, L, ws, topk_ids, x, counts, offsets, sorted_to_expanded,
-              expanded_to_sorted, x_perm, x_perm_scale);
+              expanded_to_sorted, x_perm, x_perm_scale, nullptr);
   return finish();
 }
 
@@ -641,10 +670,10 @@ moe_status moe_grouped_ffn(const moe_config* cfg, int32_t T, const int32_t* offs
   c.shared_inter = 0;
   if (w8)
     s = run_ffn_w8a8(ln, c, T, L, ws, offsets, x_perm, x_perm_scale, w_gate, w_up, w_down, s_gate,
-                     s_up, s_down, y_perm);
+                     s_up, s_down, y_perm, false);
   else
     s = run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y_perm, nullptr, nullptr,
-                nullptr, nullptr, nullptr);
+                nullptr, nullptr, nullptr, false);
   const moe_status f = finish();
   return s != MOE_OK ? s : f;
 }
@@ -707,7 +736,12 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
     finish();
     return rs;
   }
-  run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale);
+  // the FFN's work list is built with the re-sort when that runs as one CTA
+  const bool ffn = w8 ? c.n_routed > 0 : (c.n_routed > 0 || c.shared_inter > 0);
+  const WlPlan plan = wl_plan(c, !w8 && c.shared_inter > 0);
+  const bool wl_built =
+      run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale,
+                  ffn ? &plan : nullptr);
   if (w8 && c.n_routed > 0)
     launch_quant_gather(ln, c, T, x, ids, e2s, at<uint16_t>(ws, L.x16),
                         gemv_possible(effective_gemv_max(c)) ? at<int8_t>(ws, L.x8) : nullptr,
@@ -716,10 +750,10 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
   moe_status fs = MOE_OK;
   if (w8 && c.n_routed > 0)
     fs = run_ffn_w8a8(ln, c, T, L, ws, offsets, x_perm, x_scale, w_gate, w_up, w_down, s_gate,
-                      s_up, s_down, y);
+                      s_up, s_down, y, wl_built);
   else if (!w8 && (c.n_routed > 0 || c.shared_inter > 0))
     fs = run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y, x, ws_gate, ws_up,
-                 ws_down, y_s);
+                 ws_down, y_s, wl_built);
   launch_combine(ln, c, T, y, e2s, ids, w, x, y_s, out);
   const moe_status f = finish();
   return fs != MOE_OK ? fs : f;

@@ -121,6 +121,15 @@ void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32
                         const int32_t* e2s, const void* x, void* x_perm, float* x_perm_scale);
 void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
                      const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk);
+// Small batches (one CTA holds the [expert][token] pick bitmap): count, scan and
+// stable scatter in one launch, plus the work list when wl is not nullptr.
+// Outputs equal those of the count / scan / scatter / work-list launches.
+constexpr int kSortSmallMaxT = 1024;
+constexpr int kSortSmallSmem = 96 * 1024;
+bool sort_small_fits(int T, int E);
+void launch_sort_small(const Launch& L, const moe_config& c, int T, const int32_t* ids,
+                       int32_t* counts, int32_t* offsets, int32_t* s2e, int32_t* e2s,
+                       const WorkList* wl, int gemv_max_rows, int gemv_chunk, int tc_chunk);
 
 // Grouped FFN, streaming path (gemv.cu)
 struct GemvPass {
@@ -254,7 +263,8 @@ enum {
   kAttrW8Base = kAttrGemvBase + 8,  // 3 slots: W8A8 modes
   kAttrGemvI8Base = kAttrW8Base + 3, // 8 slots: W8A8 GEMV (gate/up, down) x row cap
   kAttrRouter = kAttrGemvI8Base + 8,
-  kAttrSlots = kAttrRouter + 1
+  kAttrSortSmall,
+  kAttrSlots
 };
 void set_smem_attr_once(const void* func, int bytes, int slot);
 

@@ -218,8 +218,9 @@ __device__ int block_exclusive_scan(int v, int* tot, int* sh) {
   return excl;
 }
 
-__global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
-  __shared__ int sh[32];
+// Builds the work list from the experts' offsets; called by all threads of a
+// 1024-thread CTA (block-wide scans inside).
+__device__ void build_worklist(const WlArgs& a, const int32_t* offsets, int* sh) {
   int carry[6] = {0, 0, 0, 0, 0, 0};
   const int units = a.E_r + (a.has_shared ? 1 : 0);
   for (int base = 0; base < units; base += blockDim.x) {
@@ -231,8 +232,8 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
         n = a.T;
         shared = 1;
       } else {
-        row0 = a.offsets[e];
-        n = a.offsets[e + 1] - row0;
+        row0 = offsets[e];
+        n = offsets[e + 1] - row0;
       }
     }
     const bool gemv = n > 0 && n <= a.gemv_max;
@@ -292,7 +293,123 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
   }
 }
 
+__global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
+  __shared__ int sh[32];
+  build_worklist(a, a.offsets, sh);
+}
+
+// Small batches: the whole re-sort in one CTA, and (with build_wl) the work list
+// after it, in place of the count / scan / scatter / work-list launches.  An
+// [expert][token] bitmap of all T tokens sits in shared memory: popcounts give
+// each expert's count and each pick's rank among the earlier tokens of its
+// expert, so the order inside an expert is by token, as in the multi-CTA path.
+__global__ void __launch_bounds__(1024)
+    sort_small_kernel(const int32_t* ids, int32_t* counts, int32_t* offsets, int32_t* s2e,
+                      int32_t* e2s, int T, int k, int E, WlArgs wla, int build_wl,
+                      DevStatus* st) {
+  extern __shared__ uint32_t sm[];  // bitmap [E][W], then offsets [E + 1]
+  __shared__ int sh[32];
+  const int tid = threadIdx.x;
+  const int W = (T + 31) / 32, R = T * k;
+  uint32_t* bm = sm;
+  int32_t* off = reinterpret_cast<int32_t*>(sm + (size_t)E * W);
+  for (int i = tid; i < E * W; i += blockDim.x) bm[i] = 0u;
+  __syncthreads();
+  for (int r = tid; r < R; r += blockDim.x) {
+    const int e = ids[r];
+    if ((unsigned)e >= (unsigned)E) {
+      raise_status(st, kStBadId, MOE_K_SORT);
+      continue;
+    }
+    const int t = r / k;
+    atomicOr(&bm[e * W + t / 32], 1u << (t % 32));
+  }
+  __syncthreads();
+  // counts, and their exclusive scan, 1024 experts per round
+  int carry = 0;
+  for (int base = 0; base < E; base += blockDim.x) {
+    const int e = base + tid;
+    int c = 0;
+    if (e < E) {
+      for (int w = 0; w < W; ++w) c += __popc(bm[e * W + w]);
+      counts[e] = c;
+    }
+    int tot;
+    const int excl = block_exclusive_scan(c, &tot, sh);
+    if (e < E) off[e] = carry + excl;
+    carry += tot;
+  }
+  if (tid == 0) off[E] = carry;
+  __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) offsets[e] = off[e];
+  for (int r = tid; r < R; r += blockDim.x) {
+    const int e = ids[r];
+    if ((unsigned)e >= (unsigned)E) {
+      e2s[r] = -1;
+      continue;
+    }
+    const int t = r / k;
+    int rank = 0;
+    for (int w = 0; w < t / 32; ++w) rank += __popc(bm[e * W + w]);
+    rank += __popc(bm[e * W + t / 32] & ((1u << (t % 32)) - 1u));
+    const int p = off[e] + rank;
+    s2e[p] = r;
+    e2s[r] = p;
+  }
+  if (build_wl) {
+    __syncthreads();
+    build_worklist(wla, off, sh);
+  }
+}
+
+WlArgs make_wl_args(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
+                    const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk) {
+  WlArgs a;
+  a.offsets = offsets;
+  a.wl = wl;
+  a.E_r = c.n_routed;
+  a.T = T;
+  a.has_shared = c.shared_inter > 0;
+  a.gemv_max = gemv_max_rows;
+  a.gemv_chunk = gemv_chunk;
+  a.tc_chunk = tc_chunk;
+  // W8A8 streaming items are 128-channel tiles; bf16 ones 8 gate/up pairs or 16
+  // down channels
+  const int ch_gu = c.wdtype == MOE_W8A8 ? kGemvI8Ch : kGemvChGU;
+  const int ch_dn = c.wdtype == MOE_W8A8 ? kGemvI8Ch : kGemvChDN;
+  a.items_gu = (c.inter + ch_gu - 1) / ch_gu;
+  a.items_gu_shared = (c.shared_inter + ch_gu - 1) / ch_gu;
+  a.items_dn = (c.hidden + ch_dn - 1) / ch_dn;
+  a.tiles_gu = (c.inter + kTcM - 1) / kTcM;
+  a.tiles_gu_shared = (c.shared_inter + kTcM - 1) / kTcM;
+  a.tiles_dn = (c.hidden + kTcM - 1) / kTcM;
+  a.status = L.status;
+  return a;
+}
+
+size_t sort_small_smem(int T, int E) {
+  return ((size_t)E * ((T + 31) / 32) + E + 1) * 4;
+}
+
 }  // namespace
+
+bool sort_small_fits(int T, int E) {
+  return T <= kSortSmallMaxT && sort_small_smem(T, E) <= (size_t)kSortSmallSmem;
+}
+
+void launch_sort_small(const Launch& L, const moe_config& c, int T, const int32_t* ids,
+                       int32_t* counts, int32_t* offsets, int32_t* s2e, int32_t* e2s,
+                       const WorkList* wl, int gemv_max_rows, int gemv_chunk, int tc_chunk) {
+  const int E = c.n_routed + c.n_zero;
+  WlArgs a{};
+  if (wl) a = make_wl_args(L, c, T, offsets, *wl, gemv_max_rows, gemv_chunk, tc_chunk);
+  set_smem_attr_once(reinterpret_cast<const void*>(sort_small_kernel), kSortSmallSmem,
+                     kAttrSortSmall);
+  launch_begin(L, MOE_K_SORT);
+  sort_small_kernel<<<1, 1024, sort_small_smem(T, E), L.stream>>>(
+      ids, counts, offsets, s2e, e2s, T, c.top_k, E, a, wl ? 1 : 0, L.status);
+  launch_end(L, MOE_K_SORT);
+}
 
 void launch_perm_count(const Launch& L, int T, int k, int E, const int32_t* ids, int32_t* bc) {
   const int nblk = (T + kPermTokens - 1) / kPermTokens;
@@ -341,26 +458,7 @@ void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32
 
 void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
                      const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk) {
-  WlArgs a;
-  a.offsets = offsets;
-  a.wl = wl;
-  a.E_r = c.n_routed;
-  a.T = T;
-  a.has_shared = c.shared_inter > 0;
-  a.gemv_max = gemv_max_rows;
-  a.gemv_chunk = gemv_chunk;
-  a.tc_chunk = tc_chunk;
-  // W8A8 streaming items are 128-channel tiles; bf16 ones 8 gate/up pairs or 16
-  // down channels
-  const int ch_gu = c.wdtype == MOE_W8A8 ? kGemvI8Ch : kGemvChGU;
-  const int ch_dn = c.wdtype == MOE_W8A8 ? kGemvI8Ch : kGemvChDN;
-  a.items_gu = (c.inter + ch_gu - 1) / ch_gu;
-  a.items_gu_shared = (c.shared_inter + ch_gu - 1) / ch_gu;
-  a.items_dn = (c.hidden + ch_dn - 1) / ch_dn;
-  a.tiles_gu = (c.inter + kTcM - 1) / kTcM;
-  a.tiles_gu_shared = (c.shared_inter + kTcM - 1) / kTcM;
-  a.tiles_dn = (c.hidden + kTcM - 1) / kTcM;
-  a.status = L.status;
+  const WlArgs a = make_wl_args(L, c, T, offsets, wl, gemv_max_rows, gemv_chunk, tc_chunk);
   launch_begin(L, MOE_K_WORKLIST);
   worklist_kernel<<<1, 1024, 0, L.stream>>>(a);
   launch_end(L, MOE_K_WORKLIST);

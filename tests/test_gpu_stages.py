@@ -105,14 +105,17 @@ def test_permute_matches_oracle(m, name):
     assert torch.equal(x_perm[:r_real].cpu(), want)
 
 
-def test_permute_many_blocks_and_skew(m):
-    # 1300 tokens span six 256-token blocks; one expert takes most picks.
-    spec = synth.spec("tiny", T=1300, n_routed=40, top_k=4, name="perm_skew")
+@pytest.mark.parametrize("T", [1000, 1300])
+def test_permute_many_blocks_and_skew(m, T):
+    # One expert takes most picks.  1000 tokens: the one-CTA sort (all tokens'
+    # bitmap in shared memory); 1300 tokens: six 256-token blocks of the
+    # multi-CTA count / scan / scatter.
+    spec = synth.spec("tiny", T=T, n_routed=40, top_k=4, name=f"perm_skew_{T}")
     rng = np.random.default_rng(11)
     ids = np.stack([np.concatenate([[0], rng.choice(np.arange(1, 40), 3, replace=False)])
                     if rng.random() < 0.8 else rng.choice(40, 4, replace=False)
-                    for _ in range(1300)]).astype(np.int32)
-    x = torch.randn(1300, spec["hidden"]).to(torch.bfloat16)
+                    for _ in range(T)]).astype(np.int32)
+    x = torch.randn(T, spec["hidden"]).to(torch.bfloat16)
     d = dict(x_d=x.cuda())
     ws, counts, offsets, s2e, e2s, x_perm = permute_gpu(m, spec, d, ids)
     c_o, o_o, s_o, e_o = oracle.permute(ids, 40)
