@@ -146,6 +146,27 @@ __device__ __forceinline__ void emit(const Args& a, int row, int ch, int acc0, i
   }
 }
 
+// The same from fp32 accumulators (tensor-core tiles): they hold the exact
+// integers whenever the tile passes the guard, so they are dequantised as they
+// are (no round trip through int); a tile that fails is recomputed and
+// overwritten by the exact kernel.
+template <int MODE>
+__device__ __forceinline__ void emit_f(const Args& a, int row, int ch, float acc0, float acc1,
+                                       float sr, float sw0, float sw1) {
+  const size_t o = (size_t)row * a.N + ch;
+  if (MODE == kW8Raw) {
+    a.out_i32[o] = __float2int_rn(acc0);
+    return;
+  }
+  const float v0 = acc0 * sr * sw0;
+  if (MODE == kW8GateUp) {
+    const float v1 = acc1 * sr * sw1;
+    a.out_f32[o] = v0 * __frcp_rn(1.f + __expf(-v0)) * v1;
+  } else {
+    a.out_f32[o] = v0;
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_tc_kernel(const __grid_constant__ Maps maps, const Args a) {
@@ -485,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i) {
             const float sr = __shfl_sync(0xffffffffu, sr_l, j0 + i);
             if (j0 + i < cn && live)
-              emit<MODE>(a, t.row0 + c0 + j0 + i, ch, __float2int_rn(__uint_as_float(g[i])),
-                         NA == 2 ? __float2int_rn(__uint_as_float(u[i])) : 0, sr, sw0, sw1);
+              emit_f<MODE>(a, t.row0 + c0 + j0 + i, ch, __uint_as_float(g[i]),
+                           NA == 2 ? __uint_as_float(u[i]) : 0.f, sr, sw0, sw1);
           }
         }
       }
