@@ -57,7 +57,7 @@ typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,         /* NULL pointer, bad size or inconsistent config */
-  MOE_ERR_UNSUPPORTED = 2,         /* valid request outside what this build implements */
+  MOE_ERR_UNSUPPORTED = 2,         /* valid request outside what the library implements */
   MOE_ERR_ALIGNMENT = 3,           /* a pointer is not 16-byte aligned (workspace: 256) */
   MOE_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes < moe_workspace_size() */
   MOE_ERR_CUDA = 5,                /* a CUDA runtime call or launch failed */
