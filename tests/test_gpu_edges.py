@@ -73,9 +73,10 @@ def test_every_expert_picked(m):
                      what=f"k=E gemv<={g}")
 
 
-@pytest.mark.parametrize("hidden,inter", [(16, 16), (64, 8)])
+@pytest.mark.parametrize("hidden,inter", [(16, 16), (64, 8), (1032, 264)])
 def test_smallest_shapes(m, hidden, inter):
-    # one K step and one partial tile on either path
+    # one K step and one partial tile on either path; 1032 x 264 ends every
+    # pass with an 8-element K step and an 8-channel tile
     spec = synth.spec("tiny", T=9, hidden=hidden, inter=inter, name=f"small_{hidden}_{inter}")
     d = gs.inputs(spec)
     ref, _, _ = support.oracle_layer(spec, d["x"], d["w_r"], d["bias"], d["wts"])

@@ -174,12 +174,14 @@ def test_w8a8_layer_matches_oracle(m, out_fp32):
 
 @pytest.mark.parametrize("T,gemv,H,I", [(512, 8, 1024, 512), (512, 1000, 1024, 512),
                                          (40, 8, 1024, 512), (40, 1000, 1024, 512),
-                                         (40, 2, 1024, 512), (40, 8, 2048, 2048)])
+                                         (40, 2, 1024, 512), (40, 8, 2048, 2048),
+                                         (40, 1000, 1040, 272), (200, 8, 1040, 272)])
 def test_w8a8_streaming_path_matches_oracle_and_tensor_cores(m, T, gemv, H, I):
     # Experts with <= gemv rows take the dp4a GEMV; both paths accumulate the
     # same exact integers and dequantise with the same fp32 formula, so the
-    # layer output is bit-identical to the all-tensor-core run.  K = 2048 is
-    # the case where a block's rows are fetched in one copy per matrix.
+    # layer output is bit-identical to the all-tensor-core run.  H = 1040 and
+    # I = 272 leave the last 128-channel tile and the last 128-byte K step of
+    # each pass partly outside the matrices (filled with zeros by TMA).
     spec = synth.spec("w8a8_s", T=T, hidden=H, inter=I, name=f"w8a8_s_T{T}_{H}_{I}")
     d = gs.inputs(spec)
     L = w8_lists(d["wts"])
