@@ -492,7 +492,7 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   g.N = c.inter;
   if (!launch_w8a8(ln, g)) return MOE_ERR_CUDA;
 
-  launch_quant_rows(ln, h32, hq16, h8, hsc, hn2, (int)R, c.inter, n_real);
+  launch_quant_rows(ln, h32, hq16, h8, hsc, hn2, (int)R, c.inter, offsets, c.n_routed, gemv_max);
 
   GemvI8Pass vd = vg;
   vd.item_start = wl.gemv_start_dn;
@@ -743,9 +743,8 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
       run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale,
                   ffn ? &plan : nullptr);
   if (w8 && c.n_routed > 0)
-    launch_quant_gather(ln, c, T, x, ids, e2s, at<uint16_t>(ws, L.x16),
-                        gemv_possible(effective_gemv_max(c)) ? at<int8_t>(ws, L.x8) : nullptr,
-                        x_scale,
+    launch_quant_gather(ln, c, T, x, ids, e2s, offsets, plan.gemv_max, at<uint16_t>(ws, L.x16),
+                        gemv_possible(plan.gemv_max) ? at<int8_t>(ws, L.x8) : nullptr, x_scale,
                         at<int32_t>(ws, L.xn2));
   moe_status fs = MOE_OK;
   if (w8 && c.n_routed > 0)

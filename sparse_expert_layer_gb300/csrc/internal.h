@@ -235,15 +235,19 @@ struct W8Pass {
 bool launch_w8a8(const Launch& L, const W8Pass& p);
 void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, int32_t* norm2,
                            int R, int K, const int32_t* nrows);
-// Layer path: quantise each token once and write its codes (integer-valued
-// fp16), scale and sum of squares to the sorted rows of its FFN-expert picks.
-// x8 (int8 codes, for the streaming path) may be nullptr.
+// Layer path: quantise each token once and write its codes, scale and sum of
+// squares to the sorted rows of its FFN-expert picks.  A row of an expert of at
+// most gemv_max rows (offsets give the loads) gets int8 codes in x8, any other
+// row integer-valued fp16 codes in x16; x8 nullptr sends every row to x16.
 void launch_quant_gather(const Launch& L, const moe_config& c, int T, const void* x,
-                         const int32_t* ids, const int32_t* e2s, uint16_t* x16, int8_t* x8,
-                         float* scale, int32_t* norm2);
-// dst8 (int8 codes) may be nullptr.
+                         const int32_t* ids, const int32_t* e2s, const int32_t* offsets,
+                         int gemv_max, uint16_t* x16, int8_t* x8, float* scale, int32_t* norm2);
+// The first offsets[n_experts] of R fp32 rows -> codes, by the same rule: int8
+// into dst8 for rows of experts of at most gemv_max rows, else fp16 into dst;
+// dst8 nullptr sends every row to dst.
 void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, int8_t* dst8,
-                       float* scale, int32_t* norm2, int R, int K, const int32_t* nrows);
+                       float* scale, int32_t* norm2, int R, int K, const int32_t* offsets,
+                       int n_experts, int gemv_max);
 
 // Combine (combine.cu)
 void launch_combine(const Launch& L, const moe_config& c, int T, const float* y_perm,

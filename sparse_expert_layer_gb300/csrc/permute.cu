@@ -382,7 +382,9 @@ WlArgs make_wl_args(const Launch& L, const moe_config& c, int T, const int32_t* 
   a.items_dn = (c.hidden + ch_dn - 1) / ch_dn;
   a.tiles_gu = (c.inter + kTcM - 1) / kTcM;
   a.tiles_gu_shared = (c.shared_inter + kTcM - 1) / kTcM;
-  a.tiles_dn = (c.hidden + kTcM - 1) / kTcM;
+  // W8A8 down tiles take 256 channels (two 128-row weight boxes)
+  const int dn_ch = c.wdtype == MOE_W8A8 ? 2 * kTcM : kTcM;
+  a.tiles_dn = (c.hidden + dn_ch - 1) / dn_ch;
   a.status = L.status;
   return a;
 }

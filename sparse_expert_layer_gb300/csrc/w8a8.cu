@@ -57,18 +57,22 @@ constexpr int kBoxBytes = kBoxRows * kBK * 2;    // 8 KB
 constexpr long long kGuard = 1LL << 48;          // (2^24)^2
 constexpr int kAccCols = 256;                    // TMEM columns of one accumulator buffer
 
-// Tiles take up to 256 token rows.  Down and raw tiles double-buffer their
-// 256-column accumulators so the epilogue of one tile overlaps the MMAs of the
-// next; a gate/up tile needs all 512 columns (gate 0-255, up 256-511), so its
-// epilogue runs between tiles.  (128-row gate/up tiles with two buffers were
-// measured slower: they double the weight conversion and traffic per token.)
+// Tiles take up to 256 token rows.  A gate/up tile holds 128 channels of both
+// matrices and a down tile 256 channels (two 128-row boxes of the down matrix):
+// two 256-column accumulators share each activation K-step, which halves the
+// activation bytes a down tile streams per multiply against 128-channel tiles.
+// They fill TMEM, so the epilogue runs between tiles.  Raw tiles
+// (int32 output) take 128 channels and double-buffer their accumulators.
+// (128-row gate/up tiles with two buffers were measured slower: they double the
+// weight conversion and traffic per token.)
 template <int MODE>
 struct Geom {
-  static constexpr int kNA = MODE == kW8GateUp ? 2 : 1;      // weight matrices per tile
+  static constexpr bool kTwo = MODE != kW8Raw;
+  static constexpr int kNA = kTwo ? 2 : 1;                   // weight boxes per tile
   static constexpr int kTN = kW8MaxN;                        // token rows per tile
-  static constexpr int kAccBufs = MODE == kW8GateUp ? 1 : 2; // accumulator buffers
-  static constexpr int kSRaw = MODE == kW8GateUp ? 3 : 4;    // raw ring stages
-  static constexpr int kSAct = MODE == kW8GateUp ? 3 : 4;    // act ring stages
+  static constexpr int kAccBufs = kTwo ? 1 : 2;              // accumulator buffers
+  static constexpr int kSRaw = kTwo ? 3 : 4;                 // raw ring stages
+  static constexpr int kSAct = kTwo ? 3 : 4;                 // act ring stages
   static constexpr int kSConv = 2;                           // conv ring stages
   static constexpr int kTmemCols = 512;
   static constexpr int kActBytes = kTN * kBK * 2;
@@ -88,7 +92,10 @@ static_assert(Geom<kW8GateUp>::kSmemBytes <= 227 * 1024, "gate/up shared memory"
 static_assert(Geom<kW8Down>::kSmemBytes <= 227 * 1024, "down shared memory");
 static_assert(Geom<kW8GateUp>::kNA * Geom<kW8GateUp>::kTN * Geom<kW8GateUp>::kAccBufs <= 512,
               "gate/up accumulators");
-static_assert(Geom<kW8Down>::kTN * Geom<kW8Down>::kAccBufs <= 512, "down accumulators");
+static_assert(Geom<kW8Down>::kNA * Geom<kW8Down>::kTN * Geom<kW8Down>::kAccBufs <= 512,
+              "down accumulators");
+static_assert(Geom<kW8Raw>::kNA * Geom<kW8Raw>::kTN * Geom<kW8Raw>::kAccBufs <= 512,
+              "raw accumulators");
 
 struct Maps {
   CUtensorMap a0, a1;  // int8 weights [E][N][K]
@@ -112,6 +119,14 @@ struct Args {
   int K, N;
   DevStatus* status;
 };
+
+// First output channel of weight box m (0 or 1) of channel tile ct: gate/up
+// boxes cover the same 128 channels of two matrices, down boxes the two halves
+// of 256 channels of one matrix.
+template <int MODE>
+__device__ __forceinline__ int box_channel(int ct, int m) {
+  return MODE == kW8Down ? ct * 2 * kTcM + m * kTcM : ct * kTcM;
+}
 
 // Tile id -> rows, channel tile, expert.
 __device__ __forceinline__ QTile decode(const Args& a, int tile, int ntasks) {
@@ -150,9 +165,11 @@ __device__ __forceinline__ void emit(const Args& a, int row, int ch, int acc0, i
 // integers whenever the tile passes the guard, so they are dequantised as they
 // are (no round trip through int); a tile that fails is recomputed and
 // overwritten by the exact kernel.
+// A down tile's second accumulator is the channel kTcM further on (written
+// when live1).
 template <int MODE>
 __device__ __forceinline__ void emit_f(const Args& a, int row, int ch, float acc0, float acc1,
-                                       float sr, float sw0, float sw1) {
+                                       float sr, float sw0, float sw1, bool live1) {
   const size_t o = (size_t)row * a.N + ch;
   if (MODE == kW8Raw) {
     a.out_i32[o] = __float2int_rn(acc0);
@@ -164,6 +181,7 @@ __device__ __forceinline__ void emit_f(const Args& a, int row, int ch, float acc
     a.out_f32[o] = v0 * __frcp_rn(1.f + __expf(-v0)) * v1;
   } else {
     a.out_f32[o] = v0;
+    if (live1) a.out_f32[o + kTcM] = acc1 * sr * sw1;
   }
 }
 
@@ -286,8 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t bar = smem_u32(&raw_full[sr]);
         mbar_arrive_expect_tx(bar, G::kRawBytes);
         const uint32_t raw = smem_u32(smem + G::kRawOff + sr * G::kRawBytes);
-        tma_load_3d(raw, &maps.a0, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
-        if (NA == 2) tma_load_3d(raw + kRawTileBytes, &maps.a1, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
+        tma_load_3d(raw, &maps.a0, ks * kBK, box_channel<MODE>(t.ct, 0), t.e, bar, pol_w);
+        if (NA == 2)
+          tma_load_3d(raw + kRawTileBytes, MODE == kW8Down ? &maps.a0 : &maps.a1, ks * kBK,
+                      box_channel<MODE>(t.ct, 1), t.e, bar, pol_w);
         ++n_raw;
         const int sa = n_act % G::kSAct;
         if (!mbar_wait(smem_u32(&act_empty[sa]), ((n_act / G::kSAct) & 1u) ^ 1u)) {
@@ -462,6 +482,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t.tile < 0 || warp_flag(abort_flag)) break;
       const uint32_t buf = local % G::kAccBufs, use = local / G::kAccBufs;
       const uint32_t nb = local & 1u, nuse = local >> 1;  // weight-norm buffers
+      // Everything the epilogue reads from global memory is loaded before the
+      // accumulator is ready (during the tile's MMAs): the channel scales and
+      // the row norms and scales of this warp's tokens, 32 per chunk.
+      constexpr int kChunks = TN / 2 / 32;
+      const int r = q * 32 + lane;  // tile row
+      const int ch = box_channel<MODE>(t.ct, 0) + r;
+      const int ch1 = box_channel<MODE>(t.ct, 1) + r;
+      const bool live = ch < a.N, live1 = NA == 2 && ch1 < a.N;
+      float sw0 = 0.f, sw1 = 0.f;
+      if (MODE != kW8Raw && live) {
+        sw0 = a.s0[(size_t)t.e * a.N + ch];
+        if (live1) sw1 = (MODE == kW8Down ? a.s0 : a.s1)[(size_t)t.e * a.N + ch1];
+      }
+      const int cbeg = half * (TN / 2), cend = min(t.n, (half + 1) * (TN / 2));
+      int xn[kChunks];
+      float sr_l[kChunks];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int tl = cbeg + 32 * c + lane;
+        xn[c] = 0;
+        sr_l[c] = 0.f;
+        if (tl < cend) {
+          xn[c] = a.row_norm2[t.row0 + tl];
+          if (MODE != kW8Raw) sr_l[c] = a.row_scale[t.row0 + tl];
+        }
+      }
       if (!warp_wait(smem_u32(&acc_full[buf]), use & 1u) ||
           !warp_wait(smem_u32(&norm_full[nb]), nuse & 1u)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
@@ -469,30 +515,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int r = q * 32 + lane;  // tile row = output channel
-      const int ch = t.ct * kTcM + r;
-      const bool live = ch < a.N;
       const long long wn0 = wnorm[(nb * 2 + 0) * kTcM + r];
       const long long wn1 = NA == 2 ? wnorm[(nb * 2 + 1) * kTcM + r] : 0;
-      float sw0 = 0.f, sw1 = 0.f;
-      if (MODE != kW8Raw && live) {
-        sw0 = a.s0[(size_t)t.e * a.N + ch];
-        if (NA == 2) sw1 = a.s1[(size_t)t.e * a.N + ch];
-      }
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
       bool bad = false;
-      const int cend = min(t.n, (half + 1) * (TN / 2));
-      for (int c0 = half * (TN / 2); c0 < cend; c0 += 32) {
-        // row data of 32 tokens: one coalesced load, then shuffles
-        const int tl = c0 + lane;
-        int xn = 0;
-        float sr_l = 0.f;
-        if (tl < cend) {
-          xn = a.row_norm2[t.row0 + tl];
-          if (MODE != kW8Raw) sr_l = a.row_scale[t.row0 + tl];
-        }
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int c0 = cbeg + 32 * c;
+        if (c0 >= cend) break;
         // the guard for this channel over these rows: the largest row norm decides
-        int xmax = xn;
+        int xmax = xn[c];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) xmax = max(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
         bad |= (long long)xmax * wn0 >= kGuard || (NA == 2 && (long long)xmax * wn1 >= kGuard);
@@ -504,10 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float sr = __shfl_sync(0xffffffffu, sr_l, j0 + i);
+            const float sr = __shfl_sync(0xffffffffu, sr_l[c], j0 + i);
             if (j0 + i < cn && live)
               emit_f<MODE>(a, t.row0 + c0 + j0 + i, ch, __uint_as_float(g[i]),
-                           NA == 2 ? __uint_as_float(u[i]) : 0.f, sr, sw0, sw1);
+                           NA == 2 ? __uint_as_float(u[i]) : 0.f, sr, sw0, sw1, live1);
           }
         }
       }
@@ -553,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int MODE>
 __global__ void __launch_bounds__(256, 1)
     w8a8_exact_kernel(const int8_t* w0, const int8_t* w1, const uint16_t* act, const Args a) {
-  constexpr int NA = MODE == kW8GateUp ? 2 : 1;
+  constexpr int NA = Geom<MODE>::kNA;
   constexpr int kPass = 128;
   __shared__ int8_t As[NA][kTcM][kBK + 4];
   __shared__ int16_t Bs[kPass][kBK + 2];
@@ -568,9 +600,9 @@ __global__ void __launch_bounds__(256, 1)
       int acc[NA][8][8] = {};
       for (int k0 = 0; k0 < a.K; k0 += kBK) {
         for (int m = 0; m < NA; ++m) {
-          const int8_t* W = (m == 0 ? w0 : w1) + (size_t)t.e * mat;
+          const int8_t* W = (m == 0 || MODE == kW8Down ? w0 : w1) + (size_t)t.e * mat;
           for (int i = tid; i < kTcM * kBK; i += 256) {
-            const int r = i / kBK, k = i % kBK, ch = t.ct * kTcM + r;
+            const int r = i / kBK, k = i % kBK, ch = box_channel<MODE>(t.ct, m) + r;
             As[m][r][k] = (ch < a.N && k0 + k < a.K) ? W[(size_t)ch * a.K + k0 + k] : (int8_t)0;
           }
         }
@@ -593,50 +625,65 @@ __global__ void __launch_bounds__(256, 1)
                 acc[m][i][j] += (int)As[m][tr * 8 + i][k] * (int)Bs[tc * 8 + j][k];
         __syncthreads();
       }
+      // gate/up: one output per (gate, up) pair; down: one per box
+      constexpr int kOut = MODE == kW8Down ? NA : 1;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int m = 0; m < kOut; ++m)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int ch = t.ct * kTcM + tr * 8 + i, tok = tc * 8 + j;
-          if (ch < a.N && tok < tn) {
-            const int row = t.row0 + tb + tok;
-            float sw0 = 0.f, sw1 = 0.f, sr = 0.f;
-            if (MODE != kW8Raw) {
-              sr = a.row_scale[row];
-              sw0 = a.s0[(size_t)t.e * a.N + ch];
-              if (NA == 2) sw1 = a.s1[(size_t)t.e * a.N + ch];
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int ch = box_channel<MODE>(t.ct, m) + tr * 8 + i, tok = tc * 8 + j;
+            if (ch < a.N && tok < tn) {
+              const int row = t.row0 + tb + tok;
+              float sw0 = 0.f, sw1 = 0.f, sr = 0.f;
+              if (MODE != kW8Raw) {
+                sr = a.row_scale[row];
+                sw0 = a.s0[(size_t)t.e * a.N + ch];
+                if (MODE == kW8GateUp) sw1 = a.s1[(size_t)t.e * a.N + ch];
+              }
+              emit<MODE>(a, row, ch, acc[m][i][j], MODE == kW8GateUp ? acc[1][i][j] : 0, sr, sw0,
+                         sw1);
             }
-            emit<MODE>(a, row, ch, acc[0][i][j], NA == 2 ? acc[NA - 1][i][j] : 0, sr, sw0, sw1);
           }
-        }
     }
   }
 }
 
 // Per-token quantisation fused with the gather of the layer path: one CTA per
 // token quantises its bf16 row once (symmetric int8, scale = amax / 127, round
-// half to even, as the permutation's int8 gather does) and writes the codes as
-// integer-valued fp16 (and as int8 into x8, when the streaming path may run),
-// with the scale and the sum of squared codes, to the sorted row of each of its
-// picks that lands on an FFN expert.
+// half to even, as the permutation's int8 gather does) and writes, with the
+// scale and the sum of squared codes, to the sorted row of each of its picks
+// that lands on an FFN expert.  The codes go out once per row, in the form
+// that row's pass reads: int8 into x8 for an expert of at most gemv_max rows
+// (the streaming path, when x8 is given), else integer-valued fp16 into x16.
 constexpr int kQgThreads = 256;
 constexpr int kMaxTopKQuant = 32;  // the largest top_k the layer accepts
 __global__ void __launch_bounds__(kQgThreads)
-    quant_gather_kernel(const uint16_t* x, const int32_t* ids, const int32_t* e2s, uint16_t* x16,
-                        int8_t* x8, float* scale, int32_t* norm2, int H, int k, int E_r) {
+    quant_gather_kernel(const uint16_t* x, const int32_t* ids, const int32_t* e2s,
+                        const int32_t* offsets, int gemv_max, uint16_t* x16, int8_t* x8,
+                        float* scale, int32_t* norm2, int H, int k, int E_r) {
   __shared__ float red_f[kQgThreads / 32];
   __shared__ int red_i[kQgThreads / 32];
-  __shared__ int rows[kMaxTopKQuant];
-  __shared__ int nrows;
+  __shared__ int rows[kMaxTopKQuant];   // all FFN rows: the fp16 ones, then the int8 ones
+  __shared__ int rows8[kMaxTopKQuant];
+  __shared__ int nrows, n16;
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   if (tid == 0) {
-    int n = 0;
+    int a = 0, b = 0;
     for (int j = 0; j < k; ++j) {
       const int e = ids[(size_t)t * k + j];
       const int p = e2s[(size_t)t * k + j];
-      if ((unsigned)e < (unsigned)E_r && p >= 0) rows[n++] = p;
+      if ((unsigned)e >= (unsigned)E_r || p < 0) continue;
+      const int ne = offsets[e + 1] - offsets[e];
+      if (x8 && ne <= gemv_max)
+        rows8[b++] = p;
+      else
+        rows[a++] = p;
     }
-    nrows = n;
+    for (int i = 0; i < b; ++i) rows[a + i] = rows8[i];
+    nrows = a + b;
+    n16 = a;
   }
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   const int nv = H / 8;
@@ -652,7 +699,7 @@ __global__ void __launch_bounds__(kQgThreads)
   __syncthreads();
   amax = red_f[0];
   for (int w = 1; w < kQgThreads / 32; ++w) amax = fmaxf(amax, red_f[w]);
-  const int n = nrows;
+  const int n = nrows, na = n16;
   if (n == 0) return;
   const float s = amax / 127.0f;
   int n2 = 0;
@@ -670,10 +717,9 @@ __global__ void __launch_bounds__(kQgThreads)
       b[j / 4] |= (uint32_t)(qi & 0xff) << (8 * (j % 4));
     }
     const uint4 o = make_uint4(h[0], h[1], h[2], h[3]);
-    for (int r = 0; r < n; ++r) reinterpret_cast<uint4*>(x16 + (size_t)rows[r] * H)[i] = o;
-    if (x8)
-      for (int r = 0; r < n; ++r)
-        reinterpret_cast<uint2*>(x8 + (size_t)rows[r] * H)[i] = make_uint2(b[0], b[1]);
+    for (int r = 0; r < na; ++r) reinterpret_cast<uint4*>(x16 + (size_t)rows[r] * H)[i] = o;
+    for (int r = na; r < n; ++r)
+      reinterpret_cast<uint2*>(x8 + (size_t)rows[r] * H)[i] = make_uint2(b[0], b[1]);
   }
   for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
   if (lane == 0) red_i[warp] = n2;
@@ -716,15 +762,26 @@ __global__ void __launch_bounds__(256)
 }
 
 // fp32 rows -> symmetric int8 codes (scale = amax/127, round half to even),
-// stored as integer-valued fp16 (and as int8 into dst8, when not nullptr), with
-// the scale and the sum of squares.
+// with the scale and the sum of squares.  The codes are stored once, in the
+// form the row's pass reads: as int8 into dst8 for a row of an expert of at
+// most gemv_max rows (when dst8 is given), else as integer-valued fp16.
 __global__ void __launch_bounds__(256)
     quant_rows_kernel(const float* src, uint16_t* dst, int8_t* dst8, float* scale, int32_t* norm2,
-                      int R, int K, const int32_t* nrows) {
+                      int R, int K, const int32_t* offsets, int n_experts, int gemv_max) {
   const int lane = threadIdx.x % 32;
   const int r = blockIdx.x * 8 + threadIdx.x / 32;
-  const int rows = nrows ? min(R, *nrows) : R;
+  const int rows = min(R, offsets[n_experts]);
   if (r >= rows) return;
+  bool streamed = false;
+  if (dst8) {
+    // the expert holding row r: the last e with offsets[e] <= r
+    int lo = 0, hi = n_experts - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    streamed = offsets[lo + 1] - offsets[lo] <= gemv_max;
+  }
   const float4* s = reinterpret_cast<const float4*>(src + (size_t)r * K);
   float amax = 0.f;
   for (int i = lane; i < K / 4; i += 32) {
@@ -748,8 +805,10 @@ __global__ void __launch_bounds__(256)
       h[j / 2] |= (uint32_t)__half_as_ushort(__int2half_rn(qi)) << (16 * (j % 2));
       b |= (uint32_t)(qi & 0xff) << (8 * j);
     }
-    d[i] = make_uint2(h[0], h[1]);
-    if (dst8) reinterpret_cast<uint32_t*>(dst8 + (size_t)r * K)[i] = b;
+    if (streamed)
+      reinterpret_cast<uint32_t*>(dst8 + (size_t)r * K)[i] = b;
+    else
+      d[i] = make_uint2(h[0], h[1]);
   }
   for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
   if (lane == 0) {
@@ -854,19 +913,21 @@ void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, in
 }
 
 void launch_quant_gather(const Launch& L, const moe_config& c, int T, const void* x,
-                         const int32_t* ids, const int32_t* e2s, uint16_t* x16, int8_t* x8,
-                         float* scale, int32_t* norm2) {
+                         const int32_t* ids, const int32_t* e2s, const int32_t* offsets,
+                         int gemv_max, uint16_t* x16, int8_t* x8, float* scale, int32_t* norm2) {
   launch_begin(L, MOE_K_PERM_GATHER);
   quant_gather_kernel<<<T, kQgThreads, 0, L.stream>>>(static_cast<const uint16_t*>(x), ids, e2s,
-                                                      x16, x8, scale, norm2, c.hidden, c.top_k,
-                                                      c.n_routed);
+                                                      offsets, gemv_max, x16, x8, scale, norm2,
+                                                      c.hidden, c.top_k, c.n_routed);
   launch_end(L, MOE_K_PERM_GATHER);
 }
 
 void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, int8_t* dst8,
-                       float* scale, int32_t* norm2, int R, int K, const int32_t* nrows) {
+                       float* scale, int32_t* norm2, int R, int K, const int32_t* offsets,
+                       int n_experts, int gemv_max) {
   launch_begin(L, MOE_K_QUANT_H);
-  quant_rows_kernel<<<(R + 7) / 8, 256, 0, L.stream>>>(src, dst, dst8, scale, norm2, R, K, nrows);
+  quant_rows_kernel<<<(R + 7) / 8, 256, 0, L.stream>>>(src, dst, dst8, scale, norm2, R, K,
+                                                       offsets, n_experts, gemv_max);
   launch_end(L, MOE_K_QUANT_H);
 }
 
