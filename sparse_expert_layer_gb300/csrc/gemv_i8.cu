@@ -149,7 +149,7 @@ __device__ bool consume_item(const GemvI8Pass& p, const Item& it, uint8_t* smem,
       const float g = (float)acc0[a] * sr * sc0;
       if (GU) {
         const float u = (float)acc1[a] * sr * sc1;
-        p.out_f32[o] = g * __frcp_rn(1.f + __expf(-g)) * u;
+        p.out_f32[o] = __fdividef(g, 1.f + __expf(-g)) * u;
       } else {
         p.out_f32[o] = g;
       }

@@ -155,7 +155,7 @@ __device__ __forceinline__ void emit(const Args& a, int row, int ch, int acc0, i
   const float v0 = (float)acc0 * sr * sw0;
   if (MODE == kW8GateUp) {
     const float v1 = (float)acc1 * sr * sw1;
-    a.out_f32[o] = v0 * __frcp_rn(1.f + __expf(-v0)) * v1;
+    a.out_f32[o] = __fdividef(v0, 1.f + __expf(-v0)) * v1;
   } else {
     a.out_f32[o] = v0;
   }
@@ -178,7 +178,7 @@ __device__ __forceinline__ void emit_f(const Args& a, int row, int ch, float acc
   const float v0 = acc0 * sr * sw0;
   if (MODE == kW8GateUp) {
     const float v1 = acc1 * sr * sw1;
-    a.out_f32[o] = v0 * __frcp_rn(1.f + __expf(-v0)) * v1;
+    a.out_f32[o] = __fdividef(v0, 1.f + __expf(-v0)) * v1;
   } else {
     a.out_f32[o] = v0;
     if (live1) a.out_f32[o + kTcM] = acc1 * sr * sw1;
@@ -529,18 +529,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int o = 16; o > 0; o >>= 1) xmax = max(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
         bad |= (long long)xmax * wn0 >= kGuard || (NA == 2 && (long long)xmax * wn1 >= kGuard);
         const int cn = min(32, cend - c0);
-        for (int j0 = 0; j0 < cn; j0 += 16) {
-          uint32_t g[16], u[16];
-          tmem_ld16(trow + c0 + j0, g);
-          if (NA == 2) tmem_ld16(trow + TN + c0 + j0, u);
-          tmem_ld_wait();
+        // 32 token columns of each accumulator per wait
+        uint32_t g[32], u[32];
+        tmem_ld32(trow + c0, g);
+        if (NA == 2) tmem_ld32(trow + TN + c0, u);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float sr = __shfl_sync(0xffffffffu, sr_l[c], j0 + i);
-            if (j0 + i < cn && live)
-              emit_f<MODE>(a, t.row0 + c0 + j0 + i, ch, __uint_as_float(g[i]),
-                           NA == 2 ? __uint_as_float(u[i]) : 0.f, sr, sw0, sw1, live1);
-          }
+        for (int i = 0; i < 32; ++i) {
+          const float sr = __shfl_sync(0xffffffffu, sr_l[c], i);
+          if (i < cn && live)
+            emit_f<MODE>(a, t.row0 + c0 + i, ch, __uint_as_float(g[i]),
+                         NA == 2 ? __uint_as_float(u[i]) : 0.f, sr, sw0, sw1, live1);
         }
       }
       // The last of the four epilogue warps to finish this tile files it for
