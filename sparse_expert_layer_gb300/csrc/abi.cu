@@ -199,7 +199,8 @@ Layout make_layout(const moe_config& c, int T) {
   L.y_s = take(Is > 0 ? (size_t)T * H * 4 : 0);
   if (c.wdtype == MOE_W8A8) {
     const size_t tc_tasks = c.n_routed + 4 + R / kTcMaxN;
-    const size_t tiles = (std::max(I, H) + kTcM - 1) / kTcM;
+    // one entry per CTA half of each two-SM tile of 256 channels
+    const size_t tiles = 2 * ((std::max(I, H) + 2 * kTcM - 1) / (2 * kTcM));
     L.redo_cap = (int)(tc_tasks * tiles);
     L.x16 = take(R * H * 2);
     L.xn2 = take(R * 4);

@@ -380,11 +380,11 @@ WlArgs make_wl_args(const Launch& L, const moe_config& c, int T, const int32_t* 
   a.items_gu = (c.inter + ch_gu - 1) / ch_gu;
   a.items_gu_shared = (c.shared_inter + ch_gu - 1) / ch_gu;
   a.items_dn = (c.hidden + ch_dn - 1) / ch_dn;
-  a.tiles_gu = (c.inter + kTcM - 1) / kTcM;
+  // W8A8 tensor-core tiles span 256 channels (two-SM tiles), bf16 ones 128
+  const int tch = c.wdtype == MOE_W8A8 ? 2 * kTcM : kTcM;
+  a.tiles_gu = (c.inter + tch - 1) / tch;
   a.tiles_gu_shared = (c.shared_inter + kTcM - 1) / kTcM;
-  // W8A8 down tiles take 256 channels (two 128-row weight boxes)
-  const int dn_ch = c.wdtype == MOE_W8A8 ? 2 * kTcM : kTcM;
-  a.tiles_dn = (c.hidden + dn_ch - 1) / dn_ch;
+  a.tiles_dn = (c.hidden + tch - 1) / tch;
   a.status = L.status;
   return a;
 }

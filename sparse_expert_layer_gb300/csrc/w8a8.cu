@@ -37,6 +37,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -578,13 +579,551 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ----------------------------------------------------------------------------
+// Two-SM tiles for the layer's gate/up and down passes.
+//
+// A cluster of two CTAs (one per SM) computes a tile of 256 channels and up to
+// 256 token rows with tcgen05 .cta_group::2 MMAs (M = 256): each CTA converts
+// its own 128 weight rows and loads half of the tile's activation rows, and
+// every MMA multiplies both halves by both.  Per SM that halves the activation
+// bytes a tile streams, and the smaller activation stages leave room for
+// deeper rings.  The first CTA (rank 0) claims the tiles for both, issues the
+// MMAs and owns the barriers that gather both halves (its activation stages
+// also count the other CTA's copies); each CTA keeps its 128 accumulator rows
+// in its own TMEM and runs its own epilogue.  A gate/up CTA holds 128 channels
+// of both matrices (gate 0-255, up 256-511 in TMEM); a down CTA holds 128
+// channels and double-buffers its accumulator.
+template <int MODE>
+struct PGeom {
+  static constexpr int kNA = MODE == kW8GateUp ? 2 : 1;      // weight matrices per CTA
+  static constexpr int kTN = kW8MaxN;                        // token rows per tile
+  static constexpr int kHalfRows = kTN / 2;                  // activation rows per CTA
+  static constexpr int kAccBufs = MODE == kW8GateUp ? 1 : 2;
+  // 64-wide K sub-steps per ring stage: a down stage carries two, so each
+  // handshake of the pipeline feeds as many MMAs as a gate/up stage
+  static constexpr int kSub = MODE == kW8GateUp ? 1 : 2;
+  static constexpr int kSRaw = 3;                            // raw ring stages
+  static constexpr int kSAct = MODE == kW8GateUp ? 6 : 3;    // act ring stages
+  static constexpr int kSConv = 2;                           // conv ring stages
+  static constexpr int kTmemCols = 512;
+  static constexpr int kActSub = kHalfRows * kBK * 2;        // one sub-step of activations
+  static constexpr int kActBytes = kSub * kActSub;
+  static constexpr int kConvBytes = kSub * kNA * kF16TileBytes;
+  static constexpr int kRawBytes = kSub * kNA * kRawTileBytes;
+  static constexpr int kActOff = kSConv * kConvBytes;
+  static constexpr int kRawOff = kActOff + kSAct * kActBytes;
+  static constexpr int kBarOff = kRawOff + kSRaw * kRawBytes;
+  static constexpr int kBarCount = 2 * kSRaw + 2 * kSAct + 2 * kSConv + 8 + 1 + 2 * kTileQueue;
+  static constexpr int kBarBytes = 1024;
+  static constexpr int kNormOff = kBarOff + kBarBytes;
+  static constexpr int kNormBytes = 2 * 2 * kTcM * 4;
+  static constexpr int kSmemBytes = 1024 + kNormOff + kNormBytes;
+};
+static_assert(PGeom<kW8GateUp>::kSmemBytes <= 227 * 1024, "pair gate/up shared memory");
+static_assert(PGeom<kW8Down>::kSmemBytes <= 227 * 1024, "pair down shared memory");
+static_assert(PGeom<kW8GateUp>::kBarCount * 8 + kTileQueue * (int)sizeof(QTile) + 32 <=
+                  PGeom<kW8GateUp>::kBarBytes, "pair gate/up barriers");
+static_assert(PGeom<kW8Down>::kBarCount * 8 + kTileQueue * (int)sizeof(QTile) + 32 <=
+                  PGeom<kW8Down>::kBarBytes, "pair down barriers");
+static_assert(PGeom<kW8GateUp>::kNA * kAccCols * PGeom<kW8GateUp>::kAccBufs <= 512,
+              "pair gate/up accumulators");
+static_assert(PGeom<kW8Down>::kNA * kAccCols * PGeom<kW8Down>::kAccBufs <= 512,
+              "pair down accumulators");
+
+// Queue consumers that release a slot: in the first CTA the producer and MMA
+// threads, the converter and epilogue warps; in the second the same without
+// the MMA thread.
+constexpr int kPairQueueReaders = (2 + 4 + kEpiWarps) + (1 + 4 + kEpiWarps);
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    w8a8_pair_kernel(const __grid_constant__ Maps maps, const Args a) {
+  using G = PGeom<MODE>;
+  constexpr int NA = G::kNA;
+  constexpr int TN = G::kTN;
+  extern __shared__ uint8_t smem_raw[];
+  const int kind = MODE == kW8GateUp ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
+  const int ntasks = a.counts[a.task_slot];
+  const int ntiles = a.counts[a.tile_slot];
+  if (ntiles <= 0) return;  // both CTAs of the pair read the same count
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + G::kBarOff);
+  uint64_t* raw_empty = raw_full + G::kSRaw;
+  uint64_t* act_full = raw_empty + G::kSRaw;
+  uint64_t* act_empty = act_full + G::kSAct;
+  uint64_t* conv_full = act_empty + G::kSAct;
+  uint64_t* conv_empty = conv_full + G::kSConv;
+  uint64_t* acc_full = conv_empty + G::kSConv;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* norm_full = acc_empty + 2;
+  uint64_t* norm_empty = norm_full + 2;
+  uint64_t* drain = norm_empty + 2;
+  uint64_t* tq_full = drain + 1;
+  uint64_t* tq_empty = tq_full + kTileQueue;
+  QTile* tq = reinterpret_cast<QTile*>(tq_empty + kTileQueue);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq + kTileQueue);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* tile_bad = abort_flag + 1;   // [2], per accumulator buffer
+  volatile int* tile_done = abort_flag + 3;  // [2], epilogue warps finished
+  int32_t* wnorm = reinterpret_cast<int32_t*>(smem + G::kNormOff);
+
+  const uint32_t rank = cluster_rank();
+  const bool lead = rank == 0;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < G::kSRaw; ++s) {
+      mbar_init(smem_u32(&raw_full[s]), 1);
+      mbar_init(smem_u32(&raw_empty[s]), 4);
+    }
+    for (int s = 0; s < G::kSAct; ++s) {
+      mbar_init(smem_u32(&act_full[s]), 1);   // first CTA: its producer's expect_tx
+      mbar_init(smem_u32(&act_empty[s]), 1);  // the MMA commit, in both CTAs
+    }
+    for (int s = 0; s < G::kSConv; ++s) {
+      mbar_init(smem_u32(&conv_full[s]), 8);  // first CTA: both CTAs' converter warps
+      mbar_init(smem_u32(&conv_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 2 * kEpiWarps);  // first CTA: both epilogues
+      mbar_init(smem_u32(&norm_full[b]), 4);
+      mbar_init(smem_u32(&norm_empty[b]), kEpiWarps);
+      tile_bad[b] = 0;
+      tile_done[b] = 0;
+    }
+    mbar_init(smem_u32(drain), 1);
+    for (int s = 0; s < kTileQueue; ++s) {
+      mbar_init(smem_u32(&tq_full[s]), 1);
+      mbar_init(smem_u32(&tq_empty[s]), kPairQueueReaders);  // first CTA
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), G::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before either signals the other
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nks = (a.K + kBK * G::kSub - 1) / (kBK * G::kSub);  // ring stages per tile
+  // cluster addresses: the first CTA's gathering barriers, the other CTA's flag
+  const uint32_t lead_tq_empty = mapa_shared(smem_u32(tq_empty), 0);
+  const uint32_t lead_act_full = mapa_shared(smem_u32(act_full), 0);
+  const uint32_t lead_conv_full = mapa_shared(smem_u32(conv_full), 0);
+  const uint32_t lead_acc_empty = mapa_shared(smem_u32(acc_empty), 0);
+  const uint32_t other_abort = mapa_shared(smem_u32((const void*)abort_flag), rank ^ 1u);
+  auto fail = [&]() {
+    *abort_flag = 1;
+    st_cluster_u32(other_abort, 1u);
+  };
+  // Reads queue slot n (whole warp when warp_level) and releases it to the
+  // first CTA's scheduler.
+  auto pop = [&](uint32_t n, QTile* v, bool warp_level) -> bool {
+    const int s = n % kTileQueue;
+    bool ok = mbar_wait_cluster(smem_u32(&tq_full[s]), (n / kTileQueue) & 1u);
+    if (warp_level) ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      const volatile QTile* p = tq + s;
+      v->tile = p->tile;
+      v->row0 = p->row0;
+      v->n = p->n;
+      v->ct = p->ct;
+      v->e = p->e;
+      v->shared = p->shared;
+    } else {
+      v->tile = -1;
+    }
+    if (warp_level) __syncwarp();
+    if (ok && (!warp_level || lane == 0)) mbar_arrive_cluster(lead_tq_empty + 8u * s);
+    return ok;
+  };
+
+  if (warp == kSchedWarp && lane == 0 && lead) {
+    // ---------------------------------------------------------- scheduler --
+    // Claims and decodes tiles ahead of both CTAs and writes each into both
+    // queues.
+    const uint32_t other_tq = mapa_shared(smem_u32(tq), 1);
+    const uint32_t other_full = mapa_shared(smem_u32(tq_full), 1);
+    for (uint32_t n = 0;; ++n) {
+      QTile t;
+      t.tile = -1;
+      t.row0 = t.n = t.ct = t.e = t.shared = 0;
+      if (!*abort_flag) {
+        const int tile = atomicAdd(a.sched, 1);
+        if (tile < ntiles) t = decode(a, tile, ntasks);
+      }
+      const int s = n % kTileQueue;
+      if (!mbar_wait_cluster(smem_u32(&tq_empty[s]), ((n / kTileQueue) & 1u) ^ 1u)) {
+        raise_status(a.status, kStTimeout, kind);
+        fail();
+        break;
+      }
+      tq[s] = t;
+      const uint32_t d = other_tq + (uint32_t)(s * sizeof(QTile));
+      st_cluster_u32(d + 0, (uint32_t)t.tile);
+      st_cluster_u32(d + 4, (uint32_t)t.row0);
+      st_cluster_u32(d + 8, (uint32_t)t.n);
+      st_cluster_u32(d + 12, (uint32_t)t.ct);
+      st_cluster_u32(d + 16, (uint32_t)t.e);
+      st_cluster_u32(d + 20, (uint32_t)t.shared);
+      mbar_arrive(smem_u32(&tq_full[s]));
+      mbar_arrive_cluster(other_full + 8u * s);
+      if (t.tile < 0) break;
+    }
+  } else if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- producer --
+    const uint64_t pol_w = policy_evict_normal(), pol_x = policy_evict_last();
+    uint32_t n_raw = 0, n_act = 0;  // copies issued into each ring
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+      QTile t;
+      if (!pop(n, &t, false)) {
+        raise_status(a.status, kStTimeout, kind);
+        fail();
+        break;
+      }
+      if (t.tile < 0) break;
+      const int np = (t.n + 15) / 16 * 16;  // the pair's MMA N
+      const int hrows = np / 2;             // this CTA's activation rows
+      const int nb = (hrows + kBoxRows - 1) / kBoxRows;
+      const int arow = t.row0 + (int)rank * hrows;
+      const int wrow = (t.ct * 2 + (int)rank) * kTcM;
+      for (int ks = 0; ks < nks; ++ks) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const int sr = n_raw % G::kSRaw;
+        if (!mbar_wait(smem_u32(&raw_empty[sr]), ((n_raw / G::kSRaw) & 1u) ^ 1u)) {
+          raise_status(a.status, kStTimeout, kind);
+          fail();
+          ok = false;
+          break;
+        }
+        // a sub-step past K is a box outside the matrix: TMA fills it with zeros
+        uint32_t bar = smem_u32(&raw_full[sr]);
+        mbar_arrive_expect_tx(bar, G::kRawBytes);
+        const uint32_t raw = smem_u32(smem + G::kRawOff + sr * G::kRawBytes);
+#pragma unroll
+        for (int u = 0; u < G::kSub; ++u) {
+          const int kx = (ks * G::kSub + u) * kBK;
+          tma_load_3d(raw + (u * NA) * kRawTileBytes, &maps.a0, kx, wrow, t.e, bar, pol_w);
+          if (NA == 2)
+            tma_load_3d(raw + (u * NA + 1) * kRawTileBytes, &maps.a1, kx, wrow, t.e, bar, pol_w);
+        }
+        ++n_raw;
+        const int sa = n_act % G::kSAct;
+        if (!mbar_wait_cluster(smem_u32(&act_empty[sa]), ((n_act / G::kSAct) & 1u) ^ 1u)) {
+          raise_status(a.status, kStTimeout, kind);
+          fail();
+          ok = false;
+          break;
+        }
+        // both CTAs' copies complete on the first CTA's barrier
+        if (lead)
+          mbar_arrive_expect_tx(smem_u32(&act_full[sa]), (uint32_t)(2 * G::kSub * nb * kBoxBytes));
+        const uint32_t act = smem_u32(smem + G::kActOff + sa * G::kActBytes);
+#pragma unroll
+        for (int u = 0; u < G::kSub; ++u)
+          for (int j = 0; j < nb; ++j)
+            tma_load_3d_pair(act + u * G::kActSub + j * kBoxBytes, &maps.b,
+                             (ks * G::kSub + u) * kBK, arow + j * kBoxRows, 0,
+                             lead_act_full + 8u * sa, pol_x);
+        ++n_act;
+      }
+    }
+    // every issued copy lands before the CTA can exit (the first CTA's
+    // activation barriers also count the second CTA's copies)
+    for (uint32_t j = n_raw > (uint32_t)G::kSRaw ? n_raw - G::kSRaw : 0u; j < n_raw; ++j)
+      mbar_wait(smem_u32(&raw_full[j % G::kSRaw]), (j / G::kSRaw) & 1u);
+    if (lead)
+      for (uint32_t j = n_act > (uint32_t)G::kSAct ? n_act - G::kSAct : 0u; j < n_act; ++j)
+        mbar_wait_cluster(smem_u32(&act_full[j % G::kSAct]), (j / G::kSAct) & 1u);
+  } else if (warp == 1 && lane == 0 && lead) {
+    // --------------------------------------------------------- MMA issuer --
+    uint32_t it = 0, local = 0;
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n, ++local) {
+      QTile t;
+      if (!pop(n, &t, false)) {
+        raise_status(a.status, kStTimeout, kind);
+        fail();
+        break;
+      }
+      if (t.tile < 0) break;
+      const uint32_t buf = local % G::kAccBufs, use = local / G::kAccBufs;
+      if (!mbar_wait_cluster(smem_u32(&acc_empty[buf]), (use & 1u) ^ 1u)) {
+        raise_status(a.status, kStTimeout, kind);
+        fail();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t idesc = idesc_f16_f32(2 * kTcM, (uint32_t)((t.n + 15) / 16 * 16));
+      const uint32_t d0 = tmem + buf * kAccCols;
+      for (int ks = 0; ks < nks; ++ks, ++it) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const int sc = it % G::kSConv, sa = it % G::kSAct;
+        if (!mbar_wait_cluster(smem_u32(&conv_full[sc]), (it / G::kSConv) & 1u) ||
+            !mbar_wait_cluster(smem_u32(&act_full[sa]), (it / G::kSAct) & 1u)) {
+          raise_status(a.status, kStTimeout, kind);
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int u = 0; u < G::kSub; ++u) {
+          const uint32_t wa = smem_u32(smem + sc * G::kConvBytes + u * NA * kF16TileBytes);
+          const uint32_t xb = smem_u32(smem + G::kActOff + sa * G::kActBytes + u * G::kActSub);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t bdesc = sdesc_sw128(xb + k * 32);
+            const uint32_t acc = (ks > 0 || u > 0 || k > 0) ? 1u : 0u;
+            tc_mma_pair(d0, sdesc_sw128(wa + k * 32), bdesc, idesc, acc);
+            if (NA == 2)
+              tc_mma_pair(d0 + TN, sdesc_sw128(wa + kF16TileBytes + k * 32), bdesc, idesc, acc);
+          }
+        }
+        tc_commit_pair(smem_u32(&conv_empty[sc]));
+        tc_commit_pair(smem_u32(&act_empty[sa]));
+      }
+      if (!ok) break;
+      tc_commit_pair(smem_u32(&acc_full[buf]));
+    }
+    // the MMAs in flight finish before TMEM can be released
+    tc_commit_pair(smem_u32(drain));
+    mbar_wait_cluster(smem_u32(drain), 0u);
+  } else if (warp >= 6 && warp < 10) {
+    // ---------------------------------------------------------- converter --
+    const int ti = threadIdx.x - 6 * 32;  // 0..127
+    uint32_t it = 0, local = 0;
+    for (uint32_t n = 0;; ++n, ++local) {
+      QTile t;
+      if (!pop(n, &t, true)) {
+        if (lane == 0) {
+          raise_status(a.status, kStTimeout, kind);
+          fail();
+        }
+        break;
+      }
+      if (t.tile < 0 || warp_flag(abort_flag)) break;
+      int32_t nrm[NA][4];
+#pragma unroll
+      for (int m = 0; m < NA; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) nrm[m][i] = 0;
+      bool ok = true;
+      for (int ks = 0; ks < nks; ++ks, ++it) {
+        const int sr = it % G::kSRaw, sc = it % G::kSConv;
+        if (!warp_wait(smem_u32(&raw_full[sr]), (it / G::kSRaw) & 1u) ||
+            !warp_wait_cluster(smem_u32(&conv_empty[sc]), ((it / G::kSConv) & 1u) ^ 1u)) {
+          if (lane == 0) {
+            raise_status(a.status, kStTimeout, kind);
+            fail();
+          }
+          ok = false;
+          break;
+        }
+        const uint8_t* rawt = smem + G::kRawOff + sr * G::kRawBytes;
+        uint8_t* conv = smem + sc * G::kConvBytes;
+        // all of this thread's 16-byte chunks are loaded before any store, so
+        // their latencies overlap (a store could alias a later load otherwise)
+        // (int8 tiles [sub-step][matrix], 64 bytes a row; fp16 tiles in the same
+        // order, 128-byte rows, 128-byte swizzle)
+        uint4 v[G::kSub * NA][4];
+#pragma unroll
+        for (int b = 0; b < G::kSub * NA; ++b)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = ti + 128 * i;  // 16-byte chunk of the int8 tile
+            v[b][i] = *reinterpret_cast<const uint4*>(rawt + b * kRawTileBytes + (c >> 2) * kBK +
+                                                      (c & 3) * 16);
+          }
+#pragma unroll
+        for (int b = 0; b < G::kSub * NA; ++b) {
+          const int m = b % NA;
+          uint8_t* f16 = conv + b * kF16TileBytes;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = ti + 128 * i;
+            const int row = c >> 2, j = c & 3;
+            const uint4 w = v[b][i];
+            nrm[m][i] = __dp4a((int)w.x, (int)w.x, nrm[m][i]);
+            nrm[m][i] = __dp4a((int)w.y, (int)w.y, nrm[m][i]);
+            nrm[m][i] = __dp4a((int)w.z, (int)w.z, nrm[m][i]);
+            nrm[m][i] = __dp4a((int)w.w, (int)w.w, nrm[m][i]);
+            uint4 o0, o1;
+            i8x4_to_f16x4(w.x, o0.x, o0.y);
+            i8x4_to_f16x4(w.y, o0.z, o0.w);
+            i8x4_to_f16x4(w.z, o1.x, o1.y);
+            i8x4_to_f16x4(w.w, o1.z, o1.w);
+            const int sw = row & 7;
+            *reinterpret_cast<uint4*>(f16 + row * 128 + (((2 * j) ^ sw) << 4)) = o0;
+            *reinterpret_cast<uint4*>(f16 + row * 128 + (((2 * j + 1) ^ sw) << 4)) = o1;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          // the first CTA's MMA thread waits on this; the converted tile is
+          // read by this CTA's own tensor core
+          mbar_arrive_remote(lead_conv_full + 8u * sc);
+          mbar_arrive(smem_u32(&raw_empty[sr]));
+        }
+      }
+      if (!ok) break;
+      // weight-row norms of this tile for the epilogue's guard
+      const uint32_t nb = local & 1u, nuse = local >> 1;
+      if (!warp_wait(smem_u32(&norm_empty[nb]), (nuse & 1u) ^ 1u)) {
+        if (lane == 0) {
+          raise_status(a.status, kStTimeout, kind);
+          fail();
+        }
+        break;
+      }
+#pragma unroll
+      for (int m = 0; m < NA; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          int v = nrm[m][i];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          if ((ti & 3) == 0) wnorm[(nb * 2 + m) * kTcM + (ti >> 2) + 32 * i] = v;
+        }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&norm_full[nb]));
+    }
+  } else if (warp >= 2 && warp < kSchedWarp) {  // warps 2-5 and 10-13
+    // ----------------------------------------------------------- epilogue --
+    const int q = warp % 4;              // TMEM lane quadrant
+    const int half = warp >= 10 ? 1 : 0; // token-column half of the tile
+    uint32_t local = 0;
+    for (uint32_t n = 0;; ++n, ++local) {
+      QTile t;
+      if (!pop(n, &t, true)) {
+        if (lane == 0) {
+          raise_status(a.status, kStTimeout, kind);
+          fail();
+        }
+        break;
+      }
+      if (t.tile < 0 || warp_flag(abort_flag)) break;
+      const uint32_t buf = local % G::kAccBufs, use = local / G::kAccBufs;
+      const uint32_t nb = local & 1u, nuse = local >> 1;  // weight-norm buffers
+      // Global loads ahead of the accumulator: channel scales, and the row
+      // norms and scales of this warp's tokens (32 per chunk).
+      constexpr int kChunks = TN / 2 / 32;
+      const int r = q * 32 + lane;                              // TMEM lane = channel row
+      const int ch = (t.ct * 2 + (int)rank) * kTcM + r;
+      const bool live = ch < a.N;
+      float sw0 = 0.f, sw1 = 0.f;
+      if (live) {
+        sw0 = a.s0[(size_t)t.e * a.N + ch];
+        if (NA == 2) sw1 = a.s1[(size_t)t.e * a.N + ch];
+      }
+      const int cbeg = half * (TN / 2), cend = min(t.n, (half + 1) * (TN / 2));
+      int xn[kChunks];
+      float sr_l[kChunks];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int tl = cbeg + 32 * c + lane;
+        xn[c] = 0;
+        sr_l[c] = 0.f;
+        if (tl < cend) {
+          xn[c] = a.row_norm2[t.row0 + tl];
+          sr_l[c] = a.row_scale[t.row0 + tl];
+        }
+      }
+      if (!warp_wait_cluster(smem_u32(&acc_full[buf]), use & 1u) ||
+          !warp_wait(smem_u32(&norm_full[nb]), nuse & 1u)) {
+        if (lane == 0) {
+          raise_status(a.status, kStTimeout, kind);
+          fail();
+        }
+        break;
+      }
+      tc_fence_after();
+      const long long wn0 = wnorm[(nb * 2 + 0) * kTcM + r];
+      const long long wn1 = NA == 2 ? wnorm[(nb * 2 + 1) * kTcM + r] : 0;
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
+      bool bad = false;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int c0 = cbeg + 32 * c;
+        if (c0 >= cend) break;
+        // the guard for this channel over these rows: the largest row norm decides
+        int xmax = xn[c];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) xmax = max(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
+        bad |= (long long)xmax * wn0 >= kGuard || (NA == 2 && (long long)xmax * wn1 >= kGuard);
+        const int cn = min(32, cend - c0);
+        uint32_t g[32], u[32];
+        tmem_ld32(trow + c0, g);
+        if (NA == 2) tmem_ld32(trow + TN + c0, u);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float sr = __shfl_sync(0xffffffffu, sr_l[c], i);
+          if (i < cn && live)
+            emit_f<MODE>(a, t.row0 + c0 + i, ch, __uint_as_float(g[i]),
+                         NA == 2 ? __uint_as_float(u[i]) : 0.f, sr, sw0, sw1, false);
+        }
+      }
+      // The last of this CTA's epilogue warps to finish the tile files its
+      // half (tile * 2 + rank) for exact recomputation if any pair failed the
+      // guard, before the accumulator is released.
+      const bool any_bad = __any_sync(0xffffffffu, bad);
+      if (lane == 0) {
+        if (any_bad) atomicOr((int*)&tile_bad[buf], 1);
+        __threadfence_block();
+        if (atomicAdd((int*)&tile_done[buf], 1) == kEpiWarps - 1) {
+          if (tile_bad[buf]) {
+            const int slot = atomicAdd(&a.redo[0], 1);
+            if (slot < a.redo_cap)
+              a.redo[1 + slot] = t.tile * 2 + (int)rank;
+            else
+              raise_status(a.status, kStInternal, kind);
+          }
+          tile_bad[buf] = 0;
+          tile_done[buf] = 0;
+          __threadfence_block();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&norm_empty[nb]));
+        mbar_arrive_remote(lead_acc_empty + 8u * buf);
+      }
+    }
+  }
+
+  // After a failure, copies of the other CTA may still be in flight into this
+  // CTA's shared memory or barriers: give them time to land before the pair
+  // tears down (normal termination has consumed every copy).
+  if (threadIdx.x == 0 && *abort_flag)
+    for (int i = 0; i < 400; ++i) __nanosleep(100);
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, G::kTmemCols);
+  }
+}
+
 // Exact fallback: integer accumulation on CUDA cores for the tiles that failed
-// the guard (rare; adversarial inputs).  One CTA per filed tile at a time, in
-// passes of 128 token rows.
+// the guard (rare; adversarial inputs).  One CTA per filed entry at a time, in
+// passes of 128 token rows.  A raw entry is a 128-channel tile; a gate/up or
+// down entry is one CTA's half of a two-SM tile (tile * 2 + half).
 template <int MODE>
 __global__ void __launch_bounds__(256, 1)
     w8a8_exact_kernel(const int8_t* w0, const int8_t* w1, const uint16_t* act, const Args a) {
-  constexpr int NA = Geom<MODE>::kNA;
+  constexpr int NA = MODE == kW8GateUp ? 2 : 1;
   constexpr int kPass = 128;
   __shared__ int8_t As[NA][kTcM][kBK + 4];
   __shared__ int16_t Bs[kPass][kBK + 2];
@@ -592,16 +1131,19 @@ __global__ void __launch_bounds__(256, 1)
   const int nredo = min(a.redo[0], a.redo_cap);
   const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;  // 8 channels x 8 tokens each
   for (int idx = blockIdx.x; idx < nredo; idx += gridDim.x) {
-    const QTile t = decode(a, a.redo[1 + idx], ntasks);
+    const int entry = a.redo[1 + idx];
+    const int tile = MODE == kW8Raw ? entry : entry >> 1;
+    const QTile t = decode(a, tile, ntasks);
+    const int cbase = MODE == kW8Raw ? t.ct * kTcM : (t.ct * 2 + (entry & 1)) * kTcM;
     const size_t mat = (size_t)a.N * a.K;
     for (int tb = 0; tb < t.n; tb += kPass) {
       const int tn = min(kPass, t.n - tb);
       int acc[NA][8][8] = {};
       for (int k0 = 0; k0 < a.K; k0 += kBK) {
         for (int m = 0; m < NA; ++m) {
-          const int8_t* W = (m == 0 || MODE == kW8Down ? w0 : w1) + (size_t)t.e * mat;
+          const int8_t* W = (m == 0 ? w0 : w1) + (size_t)t.e * mat;
           for (int i = tid; i < kTcM * kBK; i += 256) {
-            const int r = i / kBK, k = i % kBK, ch = box_channel<MODE>(t.ct, m) + r;
+            const int r = i / kBK, k = i % kBK, ch = cbase + r;
             As[m][r][k] = (ch < a.N && k0 + k < a.K) ? W[(size_t)ch * a.K + k0 + k] : (int8_t)0;
           }
         }
@@ -624,27 +1166,22 @@ __global__ void __launch_bounds__(256, 1)
                 acc[m][i][j] += (int)As[m][tr * 8 + i][k] * (int)Bs[tc * 8 + j][k];
         __syncthreads();
       }
-      // gate/up: one output per (gate, up) pair; down: one per box
-      constexpr int kOut = MODE == kW8Down ? NA : 1;
 #pragma unroll
-      for (int m = 0; m < kOut; ++m)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int ch = box_channel<MODE>(t.ct, m) + tr * 8 + i, tok = tc * 8 + j;
-            if (ch < a.N && tok < tn) {
-              const int row = t.row0 + tb + tok;
-              float sw0 = 0.f, sw1 = 0.f, sr = 0.f;
-              if (MODE != kW8Raw) {
-                sr = a.row_scale[row];
-                sw0 = a.s0[(size_t)t.e * a.N + ch];
-                if (MODE == kW8GateUp) sw1 = a.s1[(size_t)t.e * a.N + ch];
-              }
-              emit<MODE>(a, row, ch, acc[m][i][j], MODE == kW8GateUp ? acc[1][i][j] : 0, sr, sw0,
-                         sw1);
+        for (int j = 0; j < 8; ++j) {
+          const int ch = cbase + tr * 8 + i, tok = tc * 8 + j;
+          if (ch < a.N && tok < tn) {
+            const int row = t.row0 + tb + tok;
+            float sw0 = 0.f, sw1 = 0.f, sr = 0.f;
+            if (MODE != kW8Raw) {
+              sr = a.row_scale[row];
+              sw0 = a.s0[(size_t)t.e * a.N + ch];
+              if (NA == 2) sw1 = a.s1[(size_t)t.e * a.N + ch];
             }
+            emit<MODE>(a, row, ch, acc[0][i][j], NA == 2 ? acc[NA - 1][i][j] : 0, sr, sw0, sw1);
           }
+        }
     }
   }
 }
@@ -854,14 +1391,7 @@ bool map_f16(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
-bool launch_mode(const Launch& L, const W8Pass& p) {
-  using G = Geom<MODE>;
-  Maps maps;
-  memset(&maps, 0, sizeof maps);
-  bool ok = map_i8(&maps.a0, p.w0, p.K, p.N, p.n_experts) && map_f16(&maps.b, p.act, p.K, p.act_rows);
-  if (MODE == kW8GateUp) ok = ok && map_i8(&maps.a1, p.w1, p.K, p.N, p.n_experts);
-  if (!ok) return false;
+Args make_args(const Launch& L, const W8Pass& p) {
   Args a;
   a.tasks = p.tasks;
   a.tile_start = p.tile_start;
@@ -880,6 +1410,19 @@ bool launch_mode(const Launch& L, const W8Pass& p) {
   a.K = p.K;
   a.N = p.N;
   a.status = L.status;
+  return a;
+}
+
+// Raw int32 accumulators (the exact int8 matmul): one-CTA tiles.
+template <int MODE>
+bool launch_mode(const Launch& L, const W8Pass& p) {
+  using G = Geom<MODE>;
+  Maps maps;
+  memset(&maps, 0, sizeof maps);
+  bool ok = map_i8(&maps.a0, p.w0, p.K, p.N, p.n_experts) && map_f16(&maps.b, p.act, p.K, p.act_rows);
+  if (MODE == kW8GateUp) ok = ok && map_i8(&maps.a1, p.w1, p.K, p.N, p.n_experts);
+  if (!ok) return false;
+  const Args a = make_args(L, p);
   const int kind = MODE == kW8GateUp ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
   set_smem_attr_once(reinterpret_cast<const void*>(w8a8_tc_kernel<MODE>), G::kSmemBytes,
                      kAttrW8Base + MODE);
@@ -896,10 +1439,35 @@ bool launch_mode(const Launch& L, const W8Pass& p) {
 
 }  // namespace
 
+// Gate/up and down passes: two-SM tiles (clusters of two CTAs).
+template <int MODE>
+bool launch_pair(const Launch& L, const W8Pass& p) {
+  using G = PGeom<MODE>;
+  Maps maps;
+  memset(&maps, 0, sizeof maps);
+  bool ok = map_i8(&maps.a0, p.w0, p.K, p.N, p.n_experts) && map_f16(&maps.b, p.act, p.K, p.act_rows);
+  if (MODE == kW8GateUp) ok = ok && map_i8(&maps.a1, p.w1, p.K, p.N, p.n_experts);
+  if (!ok) return false;
+  const Args a = make_args(L, p);
+  const int kind = MODE == kW8GateUp ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
+  set_smem_attr_once(reinterpret_cast<const void*>(w8a8_pair_kernel<MODE>), G::kSmemBytes,
+                     kAttrW8PairBase + MODE);
+  const int grid = std::max(2, L.num_sms & ~1);  // whole clusters of two
+  launch_begin(L, kind);
+  w8a8_pair_kernel<MODE><<<grid, kThreads, G::kSmemBytes, L.stream>>>(maps, a);
+  launch_end(L, kind);
+  launch_begin(L, MOE_K_W8_EXACT);
+  w8a8_exact_kernel<MODE><<<L.num_sms, 256, 0, L.stream>>>(
+      static_cast<const int8_t*>(p.w0), static_cast<const int8_t*>(p.w1),
+      static_cast<const uint16_t*>(p.act), a);
+  launch_end(L, MOE_K_W8_EXACT);
+  return true;
+}
+
 bool launch_w8a8(const Launch& L, const W8Pass& p) {
   switch (p.mode) {
-    case kW8GateUp: return launch_mode<kW8GateUp>(L, p);
-    case kW8Down: return launch_mode<kW8Down>(L, p);
+    case kW8GateUp: return launch_pair<kW8GateUp>(L, p);
+    case kW8Down: return launch_pair<kW8Down>(L, p);
     default: return launch_mode<kW8Raw>(L, p);
   }
 }
