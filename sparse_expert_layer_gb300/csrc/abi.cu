@@ -767,7 +767,8 @@ struct QLayout {
 QLayout qgemm_layout(int E, int K, int N, int R) {
   QLayout Q{};
   Q.cap = E + 4 + R / kTcMaxN;
-  Q.redo_cap = Q.cap * ((N + kTcM - 1) / kTcM);
+  // one exact-fallback entry per CTA half of each two-SM tile of 256 channels
+  Q.redo_cap = Q.cap * 2 * ((N + 2 * kTcM - 1) / (2 * kTcM));
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -832,14 +833,15 @@ moe_status moe_qgemm_s8(int32_t n_experts, int32_t K, int32_t N, int32_t R, cons
   wl.capacity = Q.cap;
   wl.redo_gu = nullptr;
   wl.redo_dn = at<int32_t>(ws, Q.redo);
-  // Tasks: the experts' row ranges in <= 128-row chunks, N/128 tiles each (the
-  // work-list kernel's "down" tiling, hidden = N).
+  // Tasks: the experts' row ranges in <= 256-row chunks, N/256 two-SM tiles
+  // each (the work-list kernel's W8A8 "down" tiling, hidden = N).
   moe_config c{};
   c.hidden = N;
   c.inter = 16;
   c.n_routed = n_experts;
   c.top_k = 1;
   c.n_group = 1;
+  c.wdtype = MOE_W8A8;
   launch_worklist(ln, c, R, offsets, wl, 0, 1, kW8MaxN);
   uint16_t* a16 = at<uint16_t>(ws, Q.a16);
   int32_t* an2 = at<int32_t>(ws, Q.an2);

@@ -265,8 +265,7 @@ enum {
   kAttrTcDN,
   kAttrGemvBase,                 // 8 slots: (gate/up, down) x row cap 1, 2, 4, 8
   kAttrW8Base = kAttrGemvBase + 8,  // 3 slots: W8A8 modes
-  kAttrW8PairBase = kAttrW8Base + 3, // 2 slots: W8A8 two-SM gate/up and down
-  kAttrGemvI8Base = kAttrW8PairBase + 2, // 8 slots: W8A8 GEMV (gate/up, down) x row cap
+  kAttrGemvI8Base = kAttrW8Base + 3, // 8 slots: W8A8 GEMV (gate/up, down) x row cap
   kAttrRouter = kAttrGemvI8Base + 8,
   kAttrSortSmall,
   kAttrSlots

@@ -16,23 +16,26 @@
 // fails it to an exact CUDA-core integer kernel, so results are exact for all
 // inputs.
 //
-// Tensor-core kernel: persistent CTAs with dynamic tile scheduling, tiles of
-// 128 output channels x up to 256 token rows, warp-specialised around three
+// Tensor-core kernel: persistent clusters of two CTAs (one per SM) with
+// dynamic tile scheduling; a tile is 256 output channels x up to 256 token
+// rows, computed with two-SM MMAs (tcgen05 .cta_group::2, M = 256) of which
+// each CTA holds 128 channel rows.  Each CTA is warp-specialised around three
 // shared-memory rings:
-//   raw ring   int8 weight tiles, written by TMA
+//   raw ring   int8 weight tiles of its 128 channels, written by TMA
 //   conv ring  the same tiles as 128-byte-swizzled integer-valued fp16, written
 //              by the converter warps (which also sum squares with dp4a)
-//   act ring   fp16 activation rows, written by TMA
+//   act ring   its half of the tile's fp16 activation rows, written by TMA
 // so TMA, conversion and MMA each run ahead on their own ring.
-//   warp 14   : tile claims and decoding, kTileQueue tiles ahead
+//   warp 14   : tile claims and decoding for both CTAs (first CTA)
 //   warp 0    : TMA producer (raw and act rings)
-//   warp 1    : TMEM allocation, MMA issue
+//   warp 1    : TMEM allocation; MMA issue (first CTA)
 //   warps 2-5, 10-13 : epilogue (dequantise, SwiGLU or store, guard); two warps
 //               share each 32-lane TMEM quadrant and take one half of the
 //               tile's token columns each
 //   warps 6-9 : int8 -> fp16 converters
-// TMEM: a gate/up tile's accumulators fill all 512 columns (gate 0-255, up
+// TMEM: a gate/up CTA's accumulators fill all 512 columns (gate 0-255, up
 // 256-511); down and raw modes double-buffer 256-column accumulators.
+
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -58,46 +61,6 @@ constexpr int kBoxBytes = kBoxRows * kBK * 2;    // 8 KB
 constexpr long long kGuard = 1LL << 48;          // (2^24)^2
 constexpr int kAccCols = 256;                    // TMEM columns of one accumulator buffer
 
-// Tiles take up to 256 token rows.  A gate/up tile holds 128 channels of both
-// matrices and a down tile 256 channels (two 128-row boxes of the down matrix):
-// two 256-column accumulators share each activation K-step, which halves the
-// activation bytes a down tile streams per multiply against 128-channel tiles.
-// They fill TMEM, so the epilogue runs between tiles.  Raw tiles
-// (int32 output) take 128 channels and double-buffer their accumulators.
-// (128-row gate/up tiles with two buffers were measured slower: they double the
-// weight conversion and traffic per token.)
-template <int MODE>
-struct Geom {
-  static constexpr bool kTwo = MODE != kW8Raw;
-  static constexpr int kNA = kTwo ? 2 : 1;                   // weight boxes per tile
-  static constexpr int kTN = kW8MaxN;                        // token rows per tile
-  static constexpr int kAccBufs = kTwo ? 1 : 2;              // accumulator buffers
-  static constexpr int kSRaw = kTwo ? 3 : 4;                 // raw ring stages
-  static constexpr int kSAct = kTwo ? 3 : 4;                 // act ring stages
-  static constexpr int kSConv = 2;                           // conv ring stages
-  static constexpr int kTmemCols = 512;
-  static constexpr int kActBytes = kTN * kBK * 2;
-  static constexpr int kConvBytes = kNA * kF16TileBytes;
-  static constexpr int kRawBytes = kNA * kRawTileBytes;
-  // [conv stages][act stages][raw stages][barriers][weight norms]; the first two
-  // hold 128-byte-swizzled tiles and stay 1024-byte aligned
-  static constexpr int kActOff = kSConv * kConvBytes;
-  static constexpr int kRawOff = kActOff + kSAct * kActBytes;
-  static constexpr int kBarOff = kRawOff + kSRaw * kRawBytes;
-  static constexpr int kBarBytes = 512;
-  static constexpr int kNormOff = kBarOff + kBarBytes;
-  static constexpr int kNormBytes = 2 * 2 * kTcM * 4;  // [buffer][matrix][channel]
-  static constexpr int kSmemBytes = 1024 + kNormOff + kNormBytes;
-};
-static_assert(Geom<kW8GateUp>::kSmemBytes <= 227 * 1024, "gate/up shared memory");
-static_assert(Geom<kW8Down>::kSmemBytes <= 227 * 1024, "down shared memory");
-static_assert(Geom<kW8GateUp>::kNA * Geom<kW8GateUp>::kTN * Geom<kW8GateUp>::kAccBufs <= 512,
-              "gate/up accumulators");
-static_assert(Geom<kW8Down>::kNA * Geom<kW8Down>::kTN * Geom<kW8Down>::kAccBufs <= 512,
-              "down accumulators");
-static_assert(Geom<kW8Raw>::kNA * Geom<kW8Raw>::kTN * Geom<kW8Raw>::kAccBufs <= 512,
-              "raw accumulators");
-
 struct Maps {
   CUtensorMap a0, a1;  // int8 weights [E][N][K]
   CUtensorMap b;       // fp16 activation rows [rows][K]
@@ -120,14 +83,6 @@ struct Args {
   int K, N;
   DevStatus* status;
 };
-
-// First output channel of weight box m (0 or 1) of channel tile ct: gate/up
-// boxes cover the same 128 channels of two matrices, down boxes the two halves
-// of 256 channels of one matrix.
-template <int MODE>
-__device__ __forceinline__ int box_channel(int ct, int m) {
-  return MODE == kW8Down ? ct * 2 * kTcM + m * kTcM : ct * kTcM;
-}
 
 // Tile id -> rows, channel tile, expert.
 __device__ __forceinline__ QTile decode(const Args& a, int tile, int ntasks) {
@@ -166,11 +121,9 @@ __device__ __forceinline__ void emit(const Args& a, int row, int ch, int acc0, i
 // integers whenever the tile passes the guard, so they are dequantised as they
 // are (no round trip through int); a tile that fails is recomputed and
 // overwritten by the exact kernel.
-// A down tile's second accumulator is the channel kTcM further on (written
-// when live1).
 template <int MODE>
 __device__ __forceinline__ void emit_f(const Args& a, int row, int ch, float acc0, float acc1,
-                                       float sr, float sw0, float sw1, bool live1) {
+                                       float sr, float sw0, float sw1) {
   const size_t o = (size_t)row * a.N + ch;
   if (MODE == kW8Raw) {
     a.out_i32[o] = __float2int_rn(acc0);
@@ -182,405 +135,11 @@ __device__ __forceinline__ void emit_f(const Args& a, int row, int ch, float acc
     a.out_f32[o] = __fdividef(v0, 1.f + __expf(-v0)) * v1;
   } else {
     a.out_f32[o] = v0;
-    if (live1) a.out_f32[o + kTcM] = acc1 * sr * sw1;
-  }
-}
-
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-    w8a8_tc_kernel(const __grid_constant__ Maps maps, const Args a) {
-  using G = Geom<MODE>;
-  constexpr int NA = G::kNA;
-  constexpr int TN = G::kTN;
-  extern __shared__ uint8_t smem_raw[];
-  const int kind = MODE == kW8GateUp ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
-  const int ntasks = a.counts[a.task_slot];
-  const int ntiles = a.counts[a.tile_slot];
-  if (ntiles <= 0) return;
-
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + G::kBarOff);
-  uint64_t* raw_empty = raw_full + G::kSRaw;
-  uint64_t* act_full = raw_empty + G::kSRaw;
-  uint64_t* act_empty = act_full + G::kSAct;
-  uint64_t* conv_full = act_empty + G::kSAct;
-  uint64_t* conv_empty = conv_full + G::kSConv;
-  uint64_t* acc_full = conv_empty + G::kSConv;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* norm_full = acc_empty + 2;
-  uint64_t* norm_empty = norm_full + 2;
-  uint64_t* drain = norm_empty + 2;
-  uint64_t* tq_full = drain + 1;
-  uint64_t* tq_empty = tq_full + kTileQueue;
-  QTile* tq = reinterpret_cast<QTile*>(tq_empty + kTileQueue);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq + kTileQueue);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* tile_bad = abort_flag + 1;   // [2], per accumulator buffer
-  volatile int* tile_done = abort_flag + 3;  // [2], epilogue warps finished
-  int32_t* wnorm = reinterpret_cast<int32_t*>(smem + G::kNormOff);
-
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < G::kSRaw; ++s) {
-      mbar_init(smem_u32(&raw_full[s]), 1);
-      mbar_init(smem_u32(&raw_empty[s]), 4);
-    }
-    for (int s = 0; s < G::kSAct; ++s) {
-      mbar_init(smem_u32(&act_full[s]), 1);
-      mbar_init(smem_u32(&act_empty[s]), 1);
-    }
-    for (int s = 0; s < G::kSConv; ++s) {
-      mbar_init(smem_u32(&conv_full[s]), 4);
-      mbar_init(smem_u32(&conv_empty[s]), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&acc_full[b]), 1);
-      mbar_init(smem_u32(&acc_empty[b]), kEpiWarps);
-      mbar_init(smem_u32(&norm_full[b]), 4);
-      mbar_init(smem_u32(&norm_empty[b]), kEpiWarps);
-      tile_bad[b] = 0;
-      tile_done[b] = 0;
-    }
-    mbar_init(smem_u32(drain), 1);
-    for (int s = 0; s < kTileQueue; ++s) {
-      mbar_init(smem_u32(&tq_full[s]), 1);
-      // producer and MMA threads, converter and epilogue warps
-      mbar_init(smem_u32(&tq_empty[s]), 6 + kEpiWarps);
-    }
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), G::kTmemCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const int nks = (a.K + kBK - 1) / kBK;
-
-  if (warp == kSchedWarp && lane == 0) {
-    // ---------------------------------------------------------- scheduler --
-    // Claims and decodes tiles up to kTileQueue ahead of the producer, so the
-    // claim's atomic and the decode's dependent loads never stall the rings.
-    for (uint32_t n = 0;; ++n) {
-      QTile t;
-      t.tile = -1;
-      if (!*abort_flag) {
-        const int tile = atomicAdd(a.sched, 1);
-        if (tile < ntiles) t = decode(a, tile, ntasks);
-      }
-      if (!tq_push(tq, tq_full, tq_empty, n, t)) {
-        raise_status(a.status, kStTimeout, kind);
-        *abort_flag = 1;
-        break;
-      }
-      if (t.tile < 0) break;
-    }
-  } else if (warp == 0 && lane == 0) {
-    // ---------------------------------------------------------- producer --
-    const uint64_t pol_w = policy_evict_normal(), pol_x = policy_evict_last();
-    uint32_t n_raw = 0, n_act = 0;  // copies issued into each ring
-    bool ok = true;
-    for (uint32_t n = 0; ok; ++n) {
-      QTile t;
-      if (!tq_pop(tq, tq_full, tq_empty, n, &t, false)) {
-        raise_status(a.status, kStTimeout, kind);
-        *abort_flag = 1;
-        break;
-      }
-      if (t.tile < 0) break;
-      const int nb = (t.n + kBoxRows - 1) / kBoxRows;
-      for (int ks = 0; ks < nks; ++ks) {
-        if (*abort_flag) {
-          ok = false;
-          break;
-        }
-        const int sr = n_raw % G::kSRaw;
-        if (!mbar_wait(smem_u32(&raw_empty[sr]), ((n_raw / G::kSRaw) & 1u) ^ 1u)) {
-          raise_status(a.status, kStTimeout, kind);
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        uint32_t bar = smem_u32(&raw_full[sr]);
-        mbar_arrive_expect_tx(bar, G::kRawBytes);
-        const uint32_t raw = smem_u32(smem + G::kRawOff + sr * G::kRawBytes);
-        tma_load_3d(raw, &maps.a0, ks * kBK, box_channel<MODE>(t.ct, 0), t.e, bar, pol_w);
-        if (NA == 2)
-          tma_load_3d(raw + kRawTileBytes, MODE == kW8Down ? &maps.a0 : &maps.a1, ks * kBK,
-                      box_channel<MODE>(t.ct, 1), t.e, bar, pol_w);
-        ++n_raw;
-        const int sa = n_act % G::kSAct;
-        if (!mbar_wait(smem_u32(&act_empty[sa]), ((n_act / G::kSAct) & 1u) ^ 1u)) {
-          raise_status(a.status, kStTimeout, kind);
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        bar = smem_u32(&act_full[sa]);
-        mbar_arrive_expect_tx(bar, (uint32_t)(nb * kBoxBytes));
-        const uint32_t act = smem_u32(smem + G::kActOff + sa * G::kActBytes);
-        for (int j = 0; j < nb; ++j)
-          tma_load_3d(act + j * kBoxBytes, &maps.b, ks * kBK, t.row0 + j * kBoxRows, 0, bar, pol_x);
-        ++n_act;
-      }
-    }
-    // every issued copy lands before the CTA can exit
-    for (uint32_t j = n_raw > (uint32_t)G::kSRaw ? n_raw - G::kSRaw : 0u; j < n_raw; ++j)
-      mbar_wait(smem_u32(&raw_full[j % G::kSRaw]), (j / G::kSRaw) & 1u);
-    for (uint32_t j = n_act > (uint32_t)G::kSAct ? n_act - G::kSAct : 0u; j < n_act; ++j)
-      mbar_wait(smem_u32(&act_full[j % G::kSAct]), (j / G::kSAct) & 1u);
-  } else if (warp == 1 && lane == 0) {
-    // --------------------------------------------------------- MMA issuer --
-    uint32_t it = 0, local = 0;
-    bool ok = true;
-    for (uint32_t n = 0; ok; ++n, ++local) {
-      QTile t;
-      if (!tq_pop(tq, tq_full, tq_empty, n, &t, false)) {
-        raise_status(a.status, kStTimeout, kind);
-        *abort_flag = 1;
-        break;
-      }
-      if (t.tile < 0) break;
-      const uint32_t buf = local % G::kAccBufs, use = local / G::kAccBufs;
-      if (!mbar_wait(smem_u32(&acc_empty[buf]), (use & 1u) ^ 1u)) {
-        raise_status(a.status, kStTimeout, kind);
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t idesc = idesc_f16_f32(kTcM, (uint32_t)((t.n + 15) / 16 * 16));
-      const uint32_t d0 = tmem + buf * kAccCols;
-      for (int ks = 0; ks < nks; ++ks, ++it) {
-        if (*abort_flag) {
-          ok = false;
-          break;
-        }
-        const int sc = it % G::kSConv, sa = it % G::kSAct;
-        if (!mbar_wait(smem_u32(&conv_full[sc]), (it / G::kSConv) & 1u) ||
-            !mbar_wait(smem_u32(&act_full[sa]), (it / G::kSAct) & 1u)) {
-          raise_status(a.status, kStTimeout, kind);
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t wa = smem_u32(smem + sc * G::kConvBytes);
-        const uint32_t xb = smem_u32(smem + G::kActOff + sa * G::kActBytes);
-#pragma unroll
-        for (int k = 0; k < kBK / 16; ++k) {
-          const uint64_t bdesc = sdesc_sw128(xb + k * 32);
-          const uint32_t acc = (ks > 0 || k > 0) ? 1u : 0u;
-          tc_mma_bf16(d0, sdesc_sw128(wa + k * 32), bdesc, idesc, acc);
-          if (NA == 2)
-            tc_mma_bf16(d0 + TN, sdesc_sw128(wa + kF16TileBytes + k * 32), bdesc, idesc, acc);
-        }
-        tc_commit(smem_u32(&conv_empty[sc]));
-        tc_commit(smem_u32(&act_empty[sa]));
-      }
-      if (!ok) break;
-      tc_commit(smem_u32(&acc_full[buf]));
-    }
-    if (*abort_flag) {
-      tc_commit(smem_u32(drain));
-      mbar_wait(smem_u32(drain), 0u);
-    }
-  } else if (warp >= 6 && warp < 10) {
-    // ---------------------------------------------------------- converter --
-    const int ti = threadIdx.x - 6 * 32;  // 0..127
-    uint32_t it = 0, local = 0;
-    for (uint32_t n = 0;; ++n, ++local) {
-      QTile t;
-      if (!tq_pop(tq, tq_full, tq_empty, n, &t, true)) {
-        if (lane == 0) raise_status(a.status, kStTimeout, kind);
-        *abort_flag = 1;
-        break;
-      }
-      if (t.tile < 0 || warp_flag(abort_flag)) break;
-      int32_t nrm[NA][4];
-#pragma unroll
-      for (int m = 0; m < NA; ++m)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) nrm[m][i] = 0;
-      bool ok = true;
-      for (int ks = 0; ks < nks; ++ks, ++it) {
-        if (warp_flag(abort_flag)) {
-          ok = false;
-          break;
-        }
-        const int sr = it % G::kSRaw, sc = it % G::kSConv;
-        if (!warp_wait(smem_u32(&raw_full[sr]), (it / G::kSRaw) & 1u) ||
-            !warp_wait(smem_u32(&conv_empty[sc]), ((it / G::kSConv) & 1u) ^ 1u)) {
-          if (lane == 0) raise_status(a.status, kStTimeout, kind);
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        const uint8_t* rawt = smem + G::kRawOff + sr * G::kRawBytes;
-        uint8_t* conv = smem + sc * G::kConvBytes;
-#pragma unroll
-        for (int m = 0; m < NA; ++m) {
-          const uint8_t* raw = rawt + m * kRawTileBytes;
-          uint8_t* f16 = conv + m * kF16TileBytes;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = ti + 128 * i;  // 16-byte chunk of the int8 tile
-            const int row = c >> 2, j = c & 3;
-            const uint4 v = *reinterpret_cast<const uint4*>(raw + row * kBK + j * 16);
-            nrm[m][i] = __dp4a((int)v.x, (int)v.x, nrm[m][i]);
-            nrm[m][i] = __dp4a((int)v.y, (int)v.y, nrm[m][i]);
-            nrm[m][i] = __dp4a((int)v.z, (int)v.z, nrm[m][i]);
-            nrm[m][i] = __dp4a((int)v.w, (int)v.w, nrm[m][i]);
-            uint4 o0, o1;
-            i8x4_to_f16x4(v.x, o0.x, o0.y);
-            i8x4_to_f16x4(v.y, o0.z, o0.w);
-            i8x4_to_f16x4(v.z, o1.x, o1.y);
-            i8x4_to_f16x4(v.w, o1.z, o1.w);
-            const int sw = row & 7;
-            *reinterpret_cast<uint4*>(f16 + row * 128 + (((2 * j) ^ sw) << 4)) = o0;
-            *reinterpret_cast<uint4*>(f16 + row * 128 + (((2 * j + 1) ^ sw) << 4)) = o1;
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&conv_full[sc]));
-          mbar_arrive(smem_u32(&raw_empty[sr]));
-        }
-      }
-      if (!ok) break;
-      // weight-row norms of this tile for the epilogue's guard
-      const uint32_t nb = local & 1u, nuse = local >> 1;
-      if (!warp_wait(smem_u32(&norm_empty[nb]), (nuse & 1u) ^ 1u)) {
-        if (lane == 0) raise_status(a.status, kStTimeout, kind);
-        *abort_flag = 1;
-        break;
-      }
-#pragma unroll
-      for (int m = 0; m < NA; ++m)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          int v = nrm[m][i];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          if ((ti & 3) == 0) wnorm[(nb * 2 + m) * kTcM + (ti >> 2) + 32 * i] = v;
-        }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&norm_full[nb]));
-    }
-  } else if (warp >= 2 && warp < kSchedWarp) {  // warps 2-5 and 10-13
-    // ----------------------------------------------------------- epilogue --
-    const int q = warp % 4;              // TMEM lane quadrant
-    const int half = warp >= 10 ? 1 : 0; // token-column half of the tile
-    uint32_t local = 0;
-    for (uint32_t n = 0;; ++n, ++local) {
-      QTile t;
-      if (!tq_pop(tq, tq_full, tq_empty, n, &t, true)) {
-        if (lane == 0) raise_status(a.status, kStTimeout, kind);
-        *abort_flag = 1;
-        break;
-      }
-      if (t.tile < 0 || warp_flag(abort_flag)) break;
-      const uint32_t buf = local % G::kAccBufs, use = local / G::kAccBufs;
-      const uint32_t nb = local & 1u, nuse = local >> 1;  // weight-norm buffers
-      // Everything the epilogue reads from global memory is loaded before the
-      // accumulator is ready (during the tile's MMAs): the channel scales and
-      // the row norms and scales of this warp's tokens, 32 per chunk.
-      constexpr int kChunks = TN / 2 / 32;
-      const int r = q * 32 + lane;  // tile row
-      const int ch = box_channel<MODE>(t.ct, 0) + r;
-      const int ch1 = box_channel<MODE>(t.ct, 1) + r;
-      const bool live = ch < a.N, live1 = NA == 2 && ch1 < a.N;
-      float sw0 = 0.f, sw1 = 0.f;
-      if (MODE != kW8Raw && live) {
-        sw0 = a.s0[(size_t)t.e * a.N + ch];
-        if (live1) sw1 = (MODE == kW8Down ? a.s0 : a.s1)[(size_t)t.e * a.N + ch1];
-      }
-      const int cbeg = half * (TN / 2), cend = min(t.n, (half + 1) * (TN / 2));
-      int xn[kChunks];
-      float sr_l[kChunks];
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const int tl = cbeg + 32 * c + lane;
-        xn[c] = 0;
-        sr_l[c] = 0.f;
-        if (tl < cend) {
-          xn[c] = a.row_norm2[t.row0 + tl];
-          if (MODE != kW8Raw) sr_l[c] = a.row_scale[t.row0 + tl];
-        }
-      }
-      if (!warp_wait(smem_u32(&acc_full[buf]), use & 1u) ||
-          !warp_wait(smem_u32(&norm_full[nb]), nuse & 1u)) {
-        if (lane == 0) raise_status(a.status, kStTimeout, kind);
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
-      const long long wn0 = wnorm[(nb * 2 + 0) * kTcM + r];
-      const long long wn1 = NA == 2 ? wnorm[(nb * 2 + 1) * kTcM + r] : 0;
-      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
-      bool bad = false;
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const int c0 = cbeg + 32 * c;
-        if (c0 >= cend) break;
-        // the guard for this channel over these rows: the largest row norm decides
-        int xmax = xn[c];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) xmax = max(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
-        bad |= (long long)xmax * wn0 >= kGuard || (NA == 2 && (long long)xmax * wn1 >= kGuard);
-        const int cn = min(32, cend - c0);
-        // 32 token columns of each accumulator per wait
-        uint32_t g[32], u[32];
-        tmem_ld32(trow + c0, g);
-        if (NA == 2) tmem_ld32(trow + TN + c0, u);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float sr = __shfl_sync(0xffffffffu, sr_l[c], i);
-          if (i < cn && live)
-            emit_f<MODE>(a, t.row0 + c0 + i, ch, __uint_as_float(g[i]),
-                         NA == 2 ? __uint_as_float(u[i]) : 0.f, sr, sw0, sw1, live1);
-        }
-      }
-      // The last of the four epilogue warps to finish this tile files it for
-      // exact recomputation if any pair failed the guard.  This happens before
-      // the accumulator is released, so the next tile on it cannot touch the flags.
-      const bool any_bad = __any_sync(0xffffffffu, bad);
-      if (lane == 0) {
-        if (any_bad) atomicOr((int*)&tile_bad[buf], 1);
-        __threadfence_block();
-        if (atomicAdd((int*)&tile_done[buf], 1) == kEpiWarps - 1) {
-          if (tile_bad[buf]) {
-            const int slot = atomicAdd(&a.redo[0], 1);
-            if (slot < a.redo_cap)
-              a.redo[1 + slot] = t.tile;
-            else
-              raise_status(a.status, kStInternal, kind);
-          }
-          tile_bad[buf] = 0;
-          tile_done[buf] = 0;
-          __threadfence_block();
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&norm_empty[nb]));
-        mbar_arrive(smem_u32(&acc_empty[buf]));
-      }
-    }
-  }
-
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, G::kTmemCols);
   }
 }
 
 // ----------------------------------------------------------------------------
-// Two-SM tiles for the layer's gate/up and down passes.
+// Two-SM tiles: the layer's gate/up and down passes and the raw int32 matmul.
 //
 // A cluster of two CTAs (one per SM) computes a tile of 256 channels and up to
 // 256 token rows with tcgen05 .cta_group::2 MMAs (M = 256): each CTA converts
@@ -591,16 +150,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // MMAs and owns the barriers that gather both halves (its activation stages
 // also count the other CTA's copies); each CTA keeps its 128 accumulator rows
 // in its own TMEM and runs its own epilogue.  A gate/up CTA holds 128 channels
-// of both matrices (gate 0-255, up 256-511 in TMEM); a down CTA holds 128
-// channels and double-buffers its accumulator.
+// of both matrices (gate 0-255, up 256-511 in TMEM); a down or raw CTA holds
+// 128 channels and double-buffers its accumulator.
 template <int MODE>
 struct PGeom {
   static constexpr int kNA = MODE == kW8GateUp ? 2 : 1;      // weight matrices per CTA
   static constexpr int kTN = kW8MaxN;                        // token rows per tile
   static constexpr int kHalfRows = kTN / 2;                  // activation rows per CTA
   static constexpr int kAccBufs = MODE == kW8GateUp ? 1 : 2;
-  // 64-wide K sub-steps per ring stage: a down stage carries two, so each
-  // handshake of the pipeline feeds as many MMAs as a gate/up stage
+  // 64-wide K sub-steps per ring stage: a down or raw stage carries two, so
+  // each handshake of the pipeline feeds as many MMAs as a gate/up stage
   static constexpr int kSub = MODE == kW8GateUp ? 1 : 2;
   static constexpr int kSRaw = 3;                            // raw ring stages
   static constexpr int kSAct = MODE == kW8GateUp ? 6 : 3;    // act ring stages
@@ -629,6 +188,9 @@ static_assert(PGeom<kW8GateUp>::kNA * kAccCols * PGeom<kW8GateUp>::kAccBufs <= 5
               "pair gate/up accumulators");
 static_assert(PGeom<kW8Down>::kNA * kAccCols * PGeom<kW8Down>::kAccBufs <= 512,
               "pair down accumulators");
+static_assert(PGeom<kW8Raw>::kSmemBytes == PGeom<kW8Down>::kSmemBytes &&
+                  PGeom<kW8Raw>::kBarCount == PGeom<kW8Down>::kBarCount,
+              "raw tiles take the down geometry");
 
 // Queue consumers that release a slot: in the first CTA the producer and MMA
 // threads, the converter and epilogue warps; in the second the same without
@@ -1022,7 +584,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int ch = (t.ct * 2 + (int)rank) * kTcM + r;
       const bool live = ch < a.N;
       float sw0 = 0.f, sw1 = 0.f;
-      if (live) {
+      if (MODE != kW8Raw && live) {
         sw0 = a.s0[(size_t)t.e * a.N + ch];
         if (NA == 2) sw1 = a.s1[(size_t)t.e * a.N + ch];
       }
@@ -1036,7 +598,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         sr_l[c] = 0.f;
         if (tl < cend) {
           xn[c] = a.row_norm2[t.row0 + tl];
-          sr_l[c] = a.row_scale[t.row0 + tl];
+          if (MODE != kW8Raw) sr_l[c] = a.row_scale[t.row0 + tl];
         }
       }
       if (!warp_wait_cluster(smem_u32(&acc_full[buf]), use & 1u) ||
@@ -1071,7 +633,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float sr = __shfl_sync(0xffffffffu, sr_l[c], i);
           if (i < cn && live)
             emit_f<MODE>(a, t.row0 + c0 + i, ch, __uint_as_float(g[i]),
-                         NA == 2 ? __uint_as_float(u[i]) : 0.f, sr, sw0, sw1, false);
+                         NA == 2 ? __uint_as_float(u[i]) : 0.f, sr, sw0, sw1);
         }
       }
       // The last of this CTA's epilogue warps to finish the tile files its
@@ -1118,8 +680,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // Exact fallback: integer accumulation on CUDA cores for the tiles that failed
 // the guard (rare; adversarial inputs).  One CTA per filed entry at a time, in
-// passes of 128 token rows.  A raw entry is a 128-channel tile; a gate/up or
-// down entry is one CTA's half of a two-SM tile (tile * 2 + half).
+// passes of 128 token rows.  An entry is one CTA's half of a two-SM tile
+// (tile * 2 + half): 128 channels.
 template <int MODE>
 __global__ void __launch_bounds__(256, 1)
     w8a8_exact_kernel(const int8_t* w0, const int8_t* w1, const uint16_t* act, const Args a) {
@@ -1132,9 +694,8 @@ __global__ void __launch_bounds__(256, 1)
   const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;  // 8 channels x 8 tokens each
   for (int idx = blockIdx.x; idx < nredo; idx += gridDim.x) {
     const int entry = a.redo[1 + idx];
-    const int tile = MODE == kW8Raw ? entry : entry >> 1;
-    const QTile t = decode(a, tile, ntasks);
-    const int cbase = MODE == kW8Raw ? t.ct * kTcM : (t.ct * 2 + (entry & 1)) * kTcM;
+    const QTile t = decode(a, entry >> 1, ntasks);
+    const int cbase = (t.ct * 2 + (entry & 1)) * kTcM;
     const size_t mat = (size_t)a.N * a.K;
     for (int tb = 0; tb < t.n; tb += kPass) {
       const int tn = min(kPass, t.n - tb);
@@ -1413,33 +974,8 @@ Args make_args(const Launch& L, const W8Pass& p) {
   return a;
 }
 
-// Raw int32 accumulators (the exact int8 matmul): one-CTA tiles.
-template <int MODE>
-bool launch_mode(const Launch& L, const W8Pass& p) {
-  using G = Geom<MODE>;
-  Maps maps;
-  memset(&maps, 0, sizeof maps);
-  bool ok = map_i8(&maps.a0, p.w0, p.K, p.N, p.n_experts) && map_f16(&maps.b, p.act, p.K, p.act_rows);
-  if (MODE == kW8GateUp) ok = ok && map_i8(&maps.a1, p.w1, p.K, p.N, p.n_experts);
-  if (!ok) return false;
-  const Args a = make_args(L, p);
-  const int kind = MODE == kW8GateUp ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
-  set_smem_attr_once(reinterpret_cast<const void*>(w8a8_tc_kernel<MODE>), G::kSmemBytes,
-                     kAttrW8Base + MODE);
-  launch_begin(L, kind);
-  w8a8_tc_kernel<MODE><<<L.num_sms, kThreads, G::kSmemBytes, L.stream>>>(maps, a);
-  launch_end(L, kind);
-  launch_begin(L, MOE_K_W8_EXACT);
-  w8a8_exact_kernel<MODE><<<L.num_sms, 256, 0, L.stream>>>(
-      static_cast<const int8_t*>(p.w0), static_cast<const int8_t*>(p.w1),
-      static_cast<const uint16_t*>(p.act), a);
-  launch_end(L, MOE_K_W8_EXACT);
-  return true;
-}
-
-}  // namespace
-
-// Gate/up and down passes: two-SM tiles (clusters of two CTAs).
+// Two-SM tiles (clusters of two CTAs), then the exact fallback for entries
+// that failed the guard.
 template <int MODE>
 bool launch_pair(const Launch& L, const W8Pass& p) {
   using G = PGeom<MODE>;
@@ -1451,7 +987,7 @@ bool launch_pair(const Launch& L, const W8Pass& p) {
   const Args a = make_args(L, p);
   const int kind = MODE == kW8GateUp ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
   set_smem_attr_once(reinterpret_cast<const void*>(w8a8_pair_kernel<MODE>), G::kSmemBytes,
-                     kAttrW8PairBase + MODE);
+                     kAttrW8Base + MODE);
   const int grid = std::max(2, L.num_sms & ~1);  // whole clusters of two
   launch_begin(L, kind);
   w8a8_pair_kernel<MODE><<<grid, kThreads, G::kSmemBytes, L.stream>>>(maps, a);
@@ -1464,11 +1000,13 @@ bool launch_pair(const Launch& L, const W8Pass& p) {
   return true;
 }
 
+}  // namespace
+
 bool launch_w8a8(const Launch& L, const W8Pass& p) {
   switch (p.mode) {
     case kW8GateUp: return launch_pair<kW8GateUp>(L, p);
     case kW8Down: return launch_pair<kW8Down>(L, p);
-    default: return launch_mode<kW8Raw>(L, p);
+    default: return launch_pair<kW8Raw>(L, p);
   }
 }
 
