@@ -430,8 +430,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         const int sc = it % G::kSConv, sa = it % G::kSAct;
-        if (!mbar_wait_cluster(smem_u32(&conv_full[sc]), (it / G::kSConv) & 1u) ||
-            !mbar_wait_cluster(smem_u32(&act_full[sa]), (it / G::kSAct) & 1u)) {
+        // conv_full completes once both CTAs converted the stage and the first
+        // CTA's converters saw its activations land (both CTAs' copies)
+        if (!mbar_wait_cluster(smem_u32(&conv_full[sc]), (it / G::kSConv) & 1u)) {
           raise_status(a.status, kStTimeout, kind);
           fail();
           ok = false;
@@ -530,6 +531,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         fence_proxy_async_smem();
+        // The first CTA's converters also wait for the stage's activations
+        // (their barrier counts both CTAs' copies), so conv_full alone tells the
+        // MMA thread that the whole stage is in place: one wait fewer on its path.
+        const int sa = it % G::kSAct;
+        if (lead && !warp_wait_cluster(smem_u32(&act_full[sa]), (it / G::kSAct) & 1u)) {
+          if (lane == 0) {
+            raise_status(a.status, kStTimeout, kind);
+            fail();
+          }
+          ok = false;
+          break;
+        }
         __syncwarp();
         if (lane == 0) {
           // the first CTA's MMA thread waits on this; the converted tile is

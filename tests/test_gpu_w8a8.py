@@ -222,3 +222,31 @@ def test_w8a8_full_size_prefill(m):
     gs.check_out(out[torch.as_tensor(sample, device="cuda")], ref, bf16_out=True, what="prefill")
     del wts_d, d
     torch.cuda.empty_cache()
+
+
+def test_w8a8_layer_exact_fallback_on_guard_failures(m):
+    # Activations of +-1 and weight codes of +-127: every row norm is 127^2 H and
+    # every gate/up channel norm 127^2 H, so at H = 2048 each gate/up pair breaks
+    # the tensor-core guard (127^4 H^2 > 2^48) and both halves of every two-SM
+    # gate/up tile are recomputed by the exact integer kernel.  The dp4a
+    # streaming path sums the same integers exactly and dequantises with the same
+    # fp32 formula, so the two runs agree bit for bit.
+    H, I, E = 2048, 256, 8
+    assert (127 ** 4) * H * H >= 2 ** 48
+    spec = synth.spec("w8a8_s", T=64, hidden=H, inter=I, n_routed=E, top_k=2, name="w8_guard")
+    base = gs.inputs(spec)
+    rng = np.random.default_rng(31)
+    x = torch.as_tensor(rng.choice([-1.0, 1.0], size=(spec["T"], H)), dtype=torch.bfloat16)
+    codes = lambda *shape: torch.as_tensor(127 * rng.choice([-1, 1], size=shape), dtype=torch.int8)
+    wts = {"w_gate": codes(E, I, H), "w_up": codes(E, I, H), "w_down": codes(E, H, I),
+           "s_gate": torch.full((E, I), 1e-4), "s_up": torch.full((E, I), 1e-4),
+           "s_down": torch.full((E, H), 1e-3)}
+    d = dict(base, x=x, x_d=x.cuda(), wts=wts, wts_d={k: v.cuda() for k, v in wts.items()})
+    L = w8_lists(wts)
+    ref, _, _, _, _ = oracle.layer_w8a8(spec, synth.bf16_bits(x), d["w_r"].numpy(),
+                                        support.np_bias(d["bias"]), L["qg"], L["sg"], L["qu"],
+                                        L["su"], L["qd"], L["sd"])
+    tc = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=-1)
+    gs.check_out(tc, ref, bf16_out=False, what="w8a8 guard fallback")
+    stream = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=100000)
+    assert torch.equal(tc, stream)
