@@ -21,36 +21,61 @@ struct CombineArgs {
   int T, H, k, E_r, E, out_fp32;
 };
 
+constexpr int kCombineMaxK = 32;  // the largest top_k the layer accepts
+constexpr int kCombineBatch = 4;  // picks whose rows are loaded together
+
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+  // The token's picks, read once per CTA: the sorted row of an FFN-expert pick,
+  // -1 for a zero-computation expert (the token itself), -2 to skip.
+  __shared__ int rows[kCombineMaxK];
+  __shared__ float wts[kCombineMaxK];
   const int t = blockIdx.x;
+  if (threadIdx.x < a.k) {
+    const int r = t * a.k + threadIdx.x;
+    const int e = a.ids[r];
+    int p = -2;
+    if ((unsigned)e < (unsigned)a.E_r)
+      p = a.e2s[r] >= 0 ? a.e2s[r] : -2;
+    else if ((unsigned)e < (unsigned)a.E)
+      p = -1;
+    rows[threadIdx.x] = p;
+    wts[threadIdx.x] = a.w[r];
+  }
+  __syncthreads();
   const int h0 = (blockIdx.y * 256 + threadIdx.x) * 8;
   if (h0 >= a.H) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < a.k; ++j) {
-    const int r = t * a.k + j;
-    const int e = a.ids[r];
-    const float wj = a.w[r];
-    if ((unsigned)e < (unsigned)a.E_r) {
-      const int p = a.e2s[r];
-      if (p < 0) continue;
-      const float4* y = reinterpret_cast<const float4*>(a.y_perm + (size_t)p * a.H + h0);
-      const float4 y0 = y[0], y1 = y[1];
-      acc[0] += wj * y0.x;
-      acc[1] += wj * y0.y;
-      acc[2] += wj * y0.z;
-      acc[3] += wj * y0.w;
-      acc[4] += wj * y1.x;
-      acc[5] += wj * y1.y;
-      acc[6] += wj * y1.z;
-      acc[7] += wj * y1.w;
-    } else if ((unsigned)e < (unsigned)a.E) {
-      const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H + h0);
-      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+  // Rows of kCombineBatch picks are loaded before any is added, so their
+  // latencies overlap; the sum still runs over the picks in slot order.
+  for (int j0 = 0; j0 < a.k; j0 += kCombineBatch) {
+    float4 y[kCombineBatch][2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] += wj * bf16lo(q[i]);
-        acc[2 * i + 1] += wj * bf16hi(q[i]);
+    for (int b = 0; b < kCombineBatch; ++b) {
+      const int j = j0 + b;
+      const int p = j < a.k ? rows[j] : -2;
+      if (p >= 0) {
+        const float4* src = reinterpret_cast<const float4*>(a.y_perm + (size_t)p * a.H + h0);
+        y[b][0] = src[0];
+        y[b][1] = src[1];
+      } else if (p == -1) {
+        const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H + h0);
+        y[b][0] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+        y[b][1] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
       }
+    }
+#pragma unroll
+    for (int b = 0; b < kCombineBatch; ++b) {
+      const int j = j0 + b;
+      if (j >= a.k || rows[j] == -2) continue;
+      const float wj = wts[j];
+      acc[0] += wj * y[b][0].x;
+      acc[1] += wj * y[b][0].y;
+      acc[2] += wj * y[b][0].z;
+      acc[3] += wj * y[b][0].w;
+      acc[4] += wj * y[b][1].x;
+      acc[5] += wj * y[b][1].y;
+      acc[6] += wj * y[b][1].z;
+      acc[7] += wj * y[b][1].w;
     }
   }
   if (a.shared_out) {
