@@ -13,15 +13,14 @@
 // one 8-row box of activation codes, into a ring of 5 (gate/up) or 10 (down)
 // stages, so few large copies keep ~170 KB per SM in flight.
 //   warp 0     : producer (TMA).
-//   warps 1..8 : consumers.  Warp w owns tile rows 16w..16w+15.  Gate/up: lane
-//                l takes row 16w + (l % 16) of both matrices and half l / 16 of
-//                each K step (four 16-byte chunks).  Down: lane l takes rows
-//                16w + (l % 8) and 16w + (l % 8) + 8 and quarter l / 8 (two
-//                chunks).  Either way each activation chunk a lane loads meets
-//                two weight chunks.  With the swizzle, the 8 lanes of a quarter
-//                warp read 8 rows at 8 distinct chunk positions (no bank
-//                conflicts) and one activation chunk (a broadcast).  Shuffles
-//                add the parts of each row.
+//   warps 1..8 : consumers.  Warp w owns tile rows 16w..16w+15; lane l takes
+//                rows 16w + (l % 8) and 16w + (l % 8) + 8 (of both matrices in
+//                the gate/up pass) and quarter l / 8 of each K step (two 16-byte
+//                chunks), so each activation chunk it loads meets two (down) or
+//                four (gate/up) weight chunks.  With the swizzle, the 8 lanes of
+//                a quarter warp read 8 rows at 8 distinct chunk positions (no
+//                bank conflicts) and one activation chunk (a broadcast).
+//                Shuffles add the quarters of each row.
 //   epilogue   : acc * s_row * s_channel in fp32; gate/up: h = silu(g) * u.
 #include <cudaTypedefs.h>
 
@@ -88,25 +87,32 @@ __device__ bool consume_item(const GemvI8Pass& p, const Item& it, uint8_t* smem,
                              uint64_t* empty, volatile int* abort_flag, uint32_t& iter, int cw,
                              int lane, DevStatus* st) {
   using G = Ring<GU>;
-  // acc0/acc1: gate and up of one row (gate/up pass), or rows r0 and r1 (down
-  // pass).  Each lane meets every activation chunk it loads with two weight
-  // chunks: gate/up lanes take one row of both matrices and half of each K step,
-  // down lanes rows r0 and r0 + 8 and a quarter of each K step.
-  int acc0[NR], acc1[NR];
+  constexpr int NA = G::kNA;
+  // Lane l takes rows r0 = 16w + l % 8 and r1 = r0 + 8 (of both matrices in
+  // the gate/up pass) and quarter l / 8 of each K step (two 16-byte chunks),
+  // so each activation chunk it loads meets 2 * NA weight chunks.
+  // acc[m][i][a]: matrix m (gate or down; up), row r_i, activation row a.
+  int acc[NA][2][NR];
 #pragma unroll
-  for (int a = 0; a < NR; ++a) acc0[a] = acc1[a] = 0;
+  for (int m = 0; m < NA; ++m)
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int a = 0; a < NR; ++a) acc[m][i][a] = 0;
   const int n = it.n;
-  const int r0 = GU ? 16 * cw + (lane & 15) : 16 * cw + (lane & 7);
-  const int r1 = GU ? r0 : r0 + 8;
-  const int part = GU ? lane >> 4 : lane >> 3;  // half (gate/up) or quarter (down) of a K step
-  constexpr int kChunks = GU ? 4 : 2;           // 16-byte chunks per lane and K step
-  const int sw = r0 & 7;                        // = r1 & 7
+  const int r0 = 16 * cw + (lane & 7);
+  const int part = lane >> 3;
+  const int sw = r0 & 7;  // = (r0 + 8) & 7
   // the epilogue's scales, loaded now so their latency hides behind the stream:
   // lane a < n holds row a's activation scale
-  const int ch0 = it.c0 + r0, ch1 = it.c0 + r1;
+  const int ch[2] = {it.c0 + r0, it.c0 + r0 + 8};
   const float sr_l = lane < n ? p.row_scale[it.row0 + lane] : 0.f;
-  const float sc0 = ch0 < p.N ? p.s0[(size_t)it.e * p.N + ch0] : 0.f;
-  const float sc1 = ch1 < p.N ? (GU ? p.s1 : p.s0)[(size_t)it.e * p.N + ch1] : 0.f;
+  float sc[NA][2];
+#pragma unroll
+  for (int m = 0; m < NA; ++m)
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      sc[m][i] = ch[i] < p.N ? (m == 0 ? p.s0 : p.s1)[(size_t)it.e * p.N + ch[i]] : 0.f;
   const int nks = (p.K + kKB - 1) / kKB;
   for (int ks = 0; ks < nks; ++ks, ++iter) {
     if (*abort_flag) return false;
@@ -118,56 +124,64 @@ __device__ bool consume_item(const GemvI8Pass& p, const Item& it, uint8_t* smem,
       return false;
     }
     const uint8_t* wt = smem + (size_t)stage * G::kStageBytes;
-    const uint8_t* xt = wt + G::kNA * kWTile;
+    const uint8_t* xt = wt + NA * kWTile;
 #pragma unroll
-    for (int c4 = 0; c4 < kChunks; ++c4) {
-      const int c = kChunks * part + c4;  // logical 16-byte chunk of the 128-byte row
-      const uint4 W = *reinterpret_cast<const uint4*>(wt + r0 * kKB + ((c ^ sw) << 4));
-      const uint4 U = *reinterpret_cast<const uint4*>(wt + (GU ? kWTile : 0) + r1 * kKB +
-                                                      ((c ^ sw) << 4));
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const int c = 2 * part + c2;  // logical 16-byte chunk of the 128-byte row
+      uint4 W[NA][2];
+#pragma unroll
+      for (int m = 0; m < NA; ++m)
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          W[m][i] = *reinterpret_cast<const uint4*>(wt + m * kWTile + (r0 + 8 * i) * kKB +
+                                                    ((c ^ sw) << 4));
 #pragma unroll
       for (int a = 0; a < NR; ++a) {
         if (a < n) {
           const uint4 X = *reinterpret_cast<const uint4*>(xt + a * kKB + ((c ^ (a & 7)) << 4));
-          acc0[a] = __dp4a((int)W.x, (int)X.x, acc0[a]);
-          acc0[a] = __dp4a((int)W.y, (int)X.y, acc0[a]);
-          acc0[a] = __dp4a((int)W.z, (int)X.z, acc0[a]);
-          acc0[a] = __dp4a((int)W.w, (int)X.w, acc0[a]);
-          acc1[a] = __dp4a((int)U.x, (int)X.x, acc1[a]);
-          acc1[a] = __dp4a((int)U.y, (int)X.y, acc1[a]);
-          acc1[a] = __dp4a((int)U.z, (int)X.z, acc1[a]);
-          acc1[a] = __dp4a((int)U.w, (int)X.w, acc1[a]);
+#pragma unroll
+          for (int m = 0; m < NA; ++m)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              int v = acc[m][i][a];
+              v = __dp4a((int)W[m][i].x, (int)X.x, v);
+              v = __dp4a((int)W[m][i].y, (int)X.y, v);
+              v = __dp4a((int)W[m][i].z, (int)X.z, v);
+              v = __dp4a((int)W[m][i].w, (int)X.w, v);
+              acc[m][i][a] = v;
+            }
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
   }
-  // the parts of each row (lanes 16 apart, or 8, 16 and 24 apart), then the
-  // epilogue on the lanes of part 0
+  // the four quarters of each row (lanes 8, 16 and 24 apart), then the
+  // epilogue on the lanes of quarter 0
 #pragma unroll
-  for (int a = 0; a < NR; ++a) {
-    if (!GU) {
-      acc0[a] += __shfl_xor_sync(0xffffffffu, acc0[a], 8);
-      acc1[a] += __shfl_xor_sync(0xffffffffu, acc1[a], 8);
-    }
-    acc0[a] += __shfl_xor_sync(0xffffffffu, acc0[a], 16);
-    acc1[a] += __shfl_xor_sync(0xffffffffu, acc1[a], 16);
-  }
+  for (int m = 0; m < NA; ++m)
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int a = 0; a < NR; ++a) {
+        acc[m][i][a] += __shfl_xor_sync(0xffffffffu, acc[m][i][a], 8);
+        acc[m][i][a] += __shfl_xor_sync(0xffffffffu, acc[m][i][a], 16);
+      }
 #pragma unroll
   for (int a = 0; a < NR; ++a) {
     const float sr = __shfl_sync(0xffffffffu, sr_l, a);
     if (a < n && part == 0) {
       const size_t o = (size_t)(it.row0 + a) * p.N;
-      if (GU) {
-        if (ch0 < p.N) {
-          const float g = (float)acc0[a] * sr * sc0;
-          const float u = (float)acc1[a] * sr * sc1;
-          p.out_f32[o + ch0] = __fdividef(g, 1.f + __expf(-g)) * u;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (ch[i] >= p.N) continue;
+        const float g = (float)acc[0][i][a] * sr * sc[0][i];
+        if (GU) {
+          const float u = (float)acc[NA - 1][i][a] * sr * sc[NA - 1][i];
+          p.out_f32[o + ch[i]] = __fdividef(g, 1.f + __expf(-g)) * u;
+        } else {
+          p.out_f32[o + ch[i]] = g;
         }
-      } else {
-        if (ch0 < p.N) p.out_f32[o + ch0] = (float)acc0[a] * sr * sc0;
-        if (ch1 < p.N) p.out_f32[o + ch1] = (float)acc1[a] * sr * sc1;
       }
     }
   }
