@@ -874,7 +874,28 @@ __global__ void __launch_bounds__(256)
 // fp32 rows -> symmetric int8 codes (scale = amax/127, round half to even),
 // with the scale and the sum of squares.  The codes are stored once, in the
 // form the row's pass reads: as int8 into dst8 for a row of an expert of at
-// most gemv_max rows (when dst8 is given), else as integer-valued fp16.
+// most gemv_max rows (when dst8 is given), else as integer-valued fp16.  One
+// warp per row, two passes over it (amax, then codes; the second mostly hits
+// L1).  (Holding the row in registers between the passes was measured slower
+// on the prefill layer: fewer warps per SM.)
+
+__device__ __forceinline__ void quant4(float4 v, float sc, bool zero, int& n2, uint2& h16,
+                                       uint32_t& b8) {
+  const float f[4] = {v.x, v.y, v.z, v.w};
+  uint32_t h[2] = {0u, 0u}, b = 0u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float qf = 0.f;
+    if (!zero) qf = fminf(127.f, fmaxf(-127.f, rintf(f[j] / sc)));
+    const int qi = (int)qf;
+    n2 += qi * qi;
+    h[j / 2] |= (uint32_t)__half_as_ushort(__int2half_rn(qi)) << (16 * (j % 2));
+    b |= (uint32_t)(qi & 0xff) << (8 * j);
+  }
+  h16 = make_uint2(h[0], h[1]);
+  b8 = b;
+}
+
 __global__ void __launch_bounds__(256)
     quant_rows_kernel(const float* src, uint16_t* dst, int8_t* dst8, float* scale, int32_t* norm2,
                       int R, int K, const int32_t* offsets, int n_experts, int gemv_max) {
@@ -884,41 +905,43 @@ __global__ void __launch_bounds__(256)
   if (r >= rows) return;
   bool streamed = false;
   if (dst8) {
-    // the expert holding row r: the last e with offsets[e] <= r
-    int lo = 0, hi = n_experts - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+    // the expert holding row r, the last e with offsets[e] <= r: a 32-way
+    // search probing 32 evenly spaced offsets per round (offsets[lo] <= r holds
+    // throughout, so lane 0's probe is always true)
+    int lo = 0, span = n_experts;  // e in [lo, lo + span)
+    while (span > 1) {
+      const int step = (span + 31) / 32;
+      const int idx = lo + lane * step;
+      const bool le = lane * step < span && offsets[idx] <= r;
+      const int last = 31 - __clz((int)__ballot_sync(0xffffffffu, le));
+      lo += last * step;
+      span = min(step, span - last * step);
     }
     streamed = offsets[lo + 1] - offsets[lo] <= gemv_max;
   }
   const float4* s = reinterpret_cast<const float4*>(src + (size_t)r * K);
-  float amax = 0.f;
-  for (int i = lane; i < K / 4; i += 32) {
-    const float4 v = s[i];
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-  }
-  amax = warp_max(amax);
-  const float sc = amax / 127.0f;
+  uint2* d16 = reinterpret_cast<uint2*>(dst + (size_t)r * K);
+  uint32_t* d8 = streamed ? reinterpret_cast<uint32_t*>(dst8 + (size_t)r * K) : nullptr;
+  const int nv = K / 4;
   int n2 = 0;
-  uint2* d = reinterpret_cast<uint2*>(dst + (size_t)r * K);
-  for (int i = lane; i < K / 4; i += 32) {
-    const float4 v = s[i];
-    const float f[4] = {v.x, v.y, v.z, v.w};
-    uint32_t h[2] = {0u, 0u}, b = 0u;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float qf = 0.f;
-      if (amax > 0.f) qf = fminf(127.f, fmaxf(-127.f, rintf(f[j] / sc)));
-      const int qi = (int)qf;
-      n2 += qi * qi;
-      h[j / 2] |= (uint32_t)__half_as_ushort(__int2half_rn(qi)) << (16 * (j % 2));
-      b |= (uint32_t)(qi & 0xff) << (8 * j);
+  float sc;
+  {
+    float amax = 0.f;
+    for (int i = lane; i < nv; i += 32) {
+      const float4 v = s[i];
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
-    if (streamed)
-      reinterpret_cast<uint32_t*>(dst8 + (size_t)r * K)[i] = b;
-    else
-      d[i] = make_uint2(h[0], h[1]);
+    amax = warp_max(amax);
+    sc = amax / 127.0f;
+    for (int i = lane; i < nv; i += 32) {
+      uint2 h;
+      uint32_t b;
+      quant4(s[i], sc, !(amax > 0.f), n2, h, b);
+      if (d8)
+        d8[i] = b;
+      else
+        d16[i] = h;
+    }
   }
   for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
   if (lane == 0) {
