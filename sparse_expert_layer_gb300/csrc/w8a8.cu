@@ -877,7 +877,8 @@ __global__ void __launch_bounds__(256)
 // most gemv_max rows (when dst8 is given), else as integer-valued fp16.  One
 // warp per row, two passes over it (amax, then codes; the second mostly hits
 // L1).  (Holding the row in registers between the passes was measured slower
-// on the prefill layer: fewer warps per SM.)
+// on the prefill layer: fewer warps per SM.)  Each pass loads four 16-byte
+// segments per lane before using any of them.
 
 __device__ __forceinline__ void quant4(float4 v, float sc, bool zero, int& n2, uint2& h16,
                                        uint32_t& b8) {
@@ -895,6 +896,8 @@ __device__ __forceinline__ void quant4(float4 v, float sc, bool zero, int& n2, u
   h16 = make_uint2(h[0], h[1]);
   b8 = b;
 }
+
+constexpr int kQrBatch = 4;  // row segments (float4) a lane loads at once
 
 __global__ void __launch_bounds__(256)
     quant_rows_kernel(const float* src, uint16_t* dst, int8_t* dst8, float* scale, int32_t* norm2,
@@ -926,21 +929,39 @@ __global__ void __launch_bounds__(256)
   int n2 = 0;
   float sc;
   {
+    // both passes load kQrBatch float4 per lane before using any, so a warp has
+    // that many row segments in flight
     float amax = 0.f;
-    for (int i = lane; i < nv; i += 32) {
-      const float4 v = s[i];
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    for (int i0 = lane; i0 < nv; i0 += 32 * kQrBatch) {
+      float4 v[kQrBatch];
+#pragma unroll
+      for (int b = 0; b < kQrBatch; ++b)
+        v[b] = i0 + 32 * b < nv ? s[i0 + 32 * b] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int b = 0; b < kQrBatch; ++b)
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[b].x), fabsf(v[b].y)),
+                                 fmaxf(fabsf(v[b].z), fabsf(v[b].w))));
     }
     amax = warp_max(amax);
     sc = amax / 127.0f;
-    for (int i = lane; i < nv; i += 32) {
-      uint2 h;
-      uint32_t b;
-      quant4(s[i], sc, !(amax > 0.f), n2, h, b);
-      if (d8)
-        d8[i] = b;
-      else
-        d16[i] = h;
+    const bool zero = !(amax > 0.f);
+    for (int i0 = lane; i0 < nv; i0 += 32 * kQrBatch) {
+      float4 v[kQrBatch];
+#pragma unroll
+      for (int b = 0; b < kQrBatch; ++b)
+        if (i0 + 32 * b < nv) v[b] = s[i0 + 32 * b];
+#pragma unroll
+      for (int b = 0; b < kQrBatch; ++b) {
+        const int i = i0 + 32 * b;
+        if (i >= nv) break;
+        uint2 h;
+        uint32_t q8;
+        quant4(v[b], sc, zero, n2, h, q8);
+        if (d8)
+          d8[i] = q8;
+        else
+          d16[i] = h;
+      }
     }
   }
   for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
