@@ -32,6 +32,7 @@ constexpr int kXStride = kRtK + 8;  // bf16 per x row in shared memory (16-byte 
 constexpr int kWStride = kRtK + 4;  // fp32 per W row (16-byte pad)
 constexpr int kRtStageBytes = kRtTok * kXStride * 2 + kRtExp * kWStride * 4;
 constexpr int kRtSmemBytes = kRtStages * kRtStageBytes;
+constexpr int kRtRedSplits = 4;  // split partials in flight per thread in the reduction
 
 struct RouterArgs {
   const uint16_t* x;
@@ -157,42 +158,81 @@ __global__ void __launch_bounds__(kRtThreads) router_kernel(RouterArgs a) {
   __syncthreads();
   if (!last) return;
   __threadfence();
-  // two splits' partials (32 independent loads) in flight per step; each output
-  // is still summed in split order, so the result does not depend on the grouping
-  float sum[4][4] = {};
-  for (int s0 = 0; s0 < a.splits; s0 += 2) {
-    float v[2][4][4];
+  // Each output is summed in split order, so the result does not depend on how
+  // the loads are grouped.
+  if (a.E % 4 == 0) {
+    // thread: four 4-expert groups (float4), kRtRedSplits splits' loads in flight
+    float4 sum[4];
+    int off[4];
+    bool in[4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const float* ps = a.partial + (size_t)(s0 + u) * a.T * a.E;
+    for (int u = 0; u < 4; ++u) {
+      const int q = tid + u * kRtThreads, t = t0 + q / 16, e = e0 + (q % 16) * 4;
+      in[u] = t < a.T && e < a.E;
+      off[u] = in[u] ? t * a.E + e : 0;
+      sum[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int s0 = 0; s0 < a.splits; s0 += kRtRedSplits) {
+      float4 v[kRtRedSplits][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int t = t0 + ty + 16 * i;
+      for (int r = 0; r < kRtRedSplits; ++r) {
+        const float* ps = a.partial + (size_t)min(s0 + r, a.splits - 1) * a.T * a.E;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = e0 + tx + 16 * j;
-          v[u][i][j] = (s0 + u < a.splits && t < a.T && e < a.E)
-                           ? __ldcg(ps + (size_t)t * a.E + e) : 0.f;
+        for (int u = 0; u < 4; ++u)
+          v[r][u] = in[u] ? __ldcg(reinterpret_cast<const float4*>(ps + off[u]))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int r = 0; r < kRtRedSplits; ++r)
+        if (s0 + r < a.splits)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            sum[u].x += v[r][u].x;
+            sum[u].y += v[r][u].y;
+            sum[u].z += v[r][u].z;
+            sum[u].w += v[r][u].w;
+          }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (in[u]) *reinterpret_cast<float4*>(a.logits + off[u]) = sum[u];
+  } else {
+    // two splits' partials (32 independent loads) in flight per step
+    float sum[4][4] = {};
+    for (int s0 = 0; s0 < a.splits; s0 += 2) {
+      float v[2][4][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float* ps = a.partial + (size_t)(s0 + u) * a.T * a.E;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = t0 + ty + 16 * i;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int e = e0 + tx + 16 * j;
+            v[u][i][j] = (s0 + u < a.splits && t < a.T && e < a.E)
+                             ? __ldcg(ps + (size_t)t * a.E + e) : 0.f;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (s0 + u < a.splits) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sum[i][j] += v[u][i][j];
         }
       }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      if (s0 + u < a.splits) {
+    for (int i = 0; i < 4; ++i) {
+      const int t = t0 + ty + 16 * i;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) sum[i][j] += v[u][i][j];
+      for (int j = 0; j < 4; ++j) {
+        const int e = e0 + tx + 16 * j;
+        if (t < a.T && e < a.E) a.logits[(size_t)t * a.E + e] = sum[i][j];
       }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty + 16 * i;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx + 16 * j;
-      if (t < a.T && e < a.E) a.logits[(size_t)t * a.E + e] = sum[i][j];
     }
   }
   if (tid == 0) a.counters[tile] = 0;  // ready for the next call
@@ -210,6 +250,8 @@ struct TopkArgs {
   float scale;
 };
 
+constexpr int kTkBatch = 8;  // experts per lane whose logits are loaded together
+
 __global__ void topk_kernel(TopkArgs a) {
   extern __shared__ float sm[];
   const int warps = blockDim.x / 32;
@@ -221,13 +263,30 @@ __global__ void topk_kernel(TopkArgs a) {
   float* sel = sc + E;                    // selection keys, -inf = not eligible
   float* tmp = sel + E;
 
-  // logits and scores
+  // logits and scores.  The global loads of kTkBatch experts per lane are
+  // issued together (the select bias is parked in sel until the scores exist).
   float m = -INFINITY;
-  for (int e = lane; e < E; e += 32) {
-    float l = a.logits[(size_t)t * E + e];
-    if (a.bias_mode == MOE_BIAS_LOGIT) l += a.bias[e];
-    sc[e] = l;
-    m = fmaxf(m, l);
+  const bool logit_bias = a.bias_mode == MOE_BIAS_LOGIT;
+  const bool select_bias = a.bias_mode == MOE_BIAS_SELECT;
+  for (int e0 = lane; e0 < E; e0 += 32 * kTkBatch) {
+    float l[kTkBatch], bv[kTkBatch];
+#pragma unroll
+    for (int b = 0; b < kTkBatch; ++b) {
+      const int e = e0 + 32 * b;
+      l[b] = e < E ? a.logits[(size_t)t * E + e] : 0.f;
+      bv[b] = e < E && a.bias_mode != MOE_BIAS_NONE ? a.bias[e] : 0.f;
+    }
+#pragma unroll
+    for (int b = 0; b < kTkBatch; ++b) {
+      const int e = e0 + 32 * b;
+      if (e < E) {
+        float v = l[b];
+        if (logit_bias) v += bv[b];
+        sc[e] = v;
+        sel[e] = select_bias ? bv[b] : 0.f;
+        m = fmaxf(m, v);
+      }
+    }
   }
   if (a.score == MOE_SCORE_SOFTMAX) {
     m = warp_max(m);
@@ -242,8 +301,7 @@ __global__ void topk_kernel(TopkArgs a) {
   } else {
     for (int e = lane; e < E; e += 32) sc[e] = 1.f / (1.f + expf(-sc[e]));
   }
-  for (int e = lane; e < E; e += 32)
-    sel[e] = sc[e] + (a.bias_mode == MOE_BIAS_SELECT ? a.bias[e] : 0.f);
+  for (int e = lane; e < E; e += 32) sel[e] = sc[e] + sel[e];
   __syncwarp();
 
   // group stage
