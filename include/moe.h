@@ -33,6 +33,11 @@
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  Calls keep no state between them; concurrent calls on
  *    different streams need different workspaces.
+ *  - The library's kernels are launched with programmatic dependent launch: each
+ *    may be scheduled while the kernel before it on the stream is finishing, and
+ *    waits for that kernel to complete before it reads or writes device memory,
+ *    so results and stream order are those of plain launches.  The environment
+ *    variable MOE_PDL=0, read once per process, turns this off.
  *  - bf16 tensors are passed as `const void*` holding IEEE bfloat16 values.
  *  - Expert indices 0 .. n_routed-1 are FFN experts; n_routed .. n_routed+n_zero-1
  *    are zero-computation experts (no weights; their pick contributes w * x_t).

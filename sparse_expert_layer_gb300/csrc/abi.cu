@@ -5,6 +5,7 @@
 
 #include <atomic>
 #include <climits>
+#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -544,6 +545,18 @@ void set_smem_attr_once(const void* func, int bytes, int slot) {
 }
 
 moe_status launch_status_take() { return finish(); }
+
+void launch_note(cudaError_t e) {
+  if (e != cudaSuccess && t_launch_error == cudaSuccess) t_launch_error = e;
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_PDL");
+    return !(v && v[0] == '0' && v[1] == 0);
+  }();
+  return on;
+}
 
 void launch_begin(const Launch& L, int kind) {
   g_launches[kind].fetch_add(1, std::memory_order_relaxed);

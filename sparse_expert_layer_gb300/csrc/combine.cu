@@ -25,6 +25,7 @@ constexpr int kCombineMaxK = 32;  // the largest top_k the layer accepts
 constexpr int kCombineBatch = 4;  // picks whose rows are loaded together
 
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+  pdl_enter();
   // The token's picks, read once per CTA: the sorted row of an FFN-expert pick,
   // -1 for a zero-computation expert (the token itself), -2 to skip.
   __shared__ int rows[kCombineMaxK];
@@ -125,7 +126,7 @@ void launch_combine(const Launch& L, const moe_config& c, int T, const float* y_
   a.out_fp32 = c.out_fp32;
   dim3 grid(T, (c.hidden / 8 + 255) / 256);
   launch_begin(L, MOE_K_COMBINE);
-  combine_kernel<<<grid, 256, 0, L.stream>>>(a);
+  launch_kernel(combine_kernel, grid, 256, 0, L.stream, a);
   launch_end(L, MOE_K_COMBINE);
 }
 

@@ -41,6 +41,27 @@ __device__ __forceinline__ uint16_t f_to_bf16(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// ------------------------------------------------- programmatic launch ----
+// Every kernel of the library is launched allowed to start before the previous
+// kernel of its stream has finished (launch_kernel).  Before it touches global
+// memory it waits until that predecessor, and so everything before it, has
+// completed and its writes are visible (pdl_wait).  Letting the next kernel
+// launch (pdl_trigger) is what overlaps that kernel's launch and set-up with
+// the rest of this one: short kernels do it right after the wait (pdl_enter);
+// the persistent tensor-core kernels when their tile queue runs dry, at the
+// start of their tail; the streaming GEMV and exact-fallback kernels not at
+// all (their successor launches when they finish).
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_trigger();
+}
+
 // ------------------------------------------------------------ warp utils ----
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

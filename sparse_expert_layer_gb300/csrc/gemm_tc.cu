@@ -91,6 +91,7 @@ __device__ __forceinline__ QTile decode_tile(const TcArgs& a, int tile, int ntas
 template <bool GU>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
+  pdl_wait();
   using G = Geom<GU>;
   extern __shared__ uint8_t smem_raw[];
   const int kind = GU ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
@@ -157,7 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
         break;
       }
-      if (t.tile < 0) break;
+      if (t.tile < 0) {
+        pdl_trigger();  // no tiles left: the next kernel may launch
+        break;
+      }
     }
   } else if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------- producer --
@@ -354,6 +358,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint6
 // Router work list: token chunks of <= 128 rows, all expert tiles of each.
 __global__ void router_tasks_kernel(FfnTask* tasks, int32_t* start, int32_t* counts, int T,
                                     int ctiles) {
+  pdl_enter();
   const int nt = (T + kTcMaxN - 1) / kTcMaxN;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nt; i += gridDim.x * blockDim.x) {
     FfnTask tk;
@@ -407,7 +412,7 @@ bool launch_tc(const Launch& L, const TcPass& p, int kind) {
   set_smem_attr_once(reinterpret_cast<const void*>(tc_kernel<GU>), G::kSmemBytes,
                      GU ? kAttrTcGU : kAttrTcDN);
   launch_begin(L, kind);
-  tc_kernel<GU><<<L.num_sms, kThreads, G::kSmemBytes, L.stream>>>(maps, a);
+  launch_kernel(tc_kernel<GU>, L.num_sms, kThreads, G::kSmemBytes, L.stream, maps, a);
   launch_end(L, kind);
   return true;
 }
@@ -428,7 +433,8 @@ bool launch_tc_router(const Launch& L, const moe_config& c, int T, const void* x
   const int ctiles = (E + kTcM - 1) / kTcM;
   const int nt = (T + kTcMaxN - 1) / kTcMaxN;
   launch_begin(L, MOE_K_ROUTER);
-  router_tasks_kernel<<<(nt + 255) / 256, 256, 0, L.stream>>>(tasks, start, counts, T, ctiles);
+  launch_kernel(router_tasks_kernel, (nt + 255) / 256, 256, 0, L.stream, tasks, start, counts, T,
+                ctiles);
   launch_end(L, MOE_K_ROUTER);
   TcPass p{};
   p.tasks = tasks;

@@ -181,6 +181,7 @@ __device__ bool consume_item(const GemvPass& p, const Item& it, uint8_t* smem, u
 
 template <bool GU, int NR>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvPass p, DevStatus* st) {
+  pdl_wait();
   using G = Ring<NR>;
   extern __shared__ __align__(16) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kBarOffset);
@@ -290,7 +291,7 @@ void launch_nr(const Launch& L, const GemvPass& p) {
   set_smem_attr_once(reinterpret_cast<const void*>(gemv_kernel<GU, NR>), G::kSmemBytes,
                      kAttrGemvBase + (GU ? 0 : 1) + 2 * nr_slot);
   launch_begin(L, kind);
-  gemv_kernel<GU, NR><<<L.num_sms, kThreads, G::kSmemBytes, L.stream>>>(p, L.status);
+  launch_kernel(gemv_kernel<GU, NR>, L.num_sms, kThreads, G::kSmemBytes, L.stream, p, L.status);
   launch_end(L, kind);
 }
 

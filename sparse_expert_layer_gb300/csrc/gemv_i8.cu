@@ -191,6 +191,7 @@ __device__ bool consume_item(const GemvI8Pass& p, const Item& it, uint8_t* smem,
 template <bool GU>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_i8_kernel(const __grid_constant__ Maps maps, const GemvI8Pass p, DevStatus* st) {
+  pdl_wait();
   using G = Ring<GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -322,7 +323,8 @@ bool launch_gemv_i8(const Launch& L, const GemvI8Pass& p) {
   set_smem_attr_once(reinterpret_cast<const void*>(gemv_i8_kernel<GU>), G::kSmemBytes,
                      kAttrGemvI8Base + (GU ? 0 : 1));
   launch_begin(L, kind);
-  gemv_i8_kernel<GU><<<L.num_sms, kThreads, G::kSmemBytes, L.stream>>>(maps, p, L.status);
+  launch_kernel(gemv_i8_kernel<GU>, L.num_sms, kThreads, G::kSmemBytes, L.stream, maps, p,
+                L.status);
   launch_end(L, kind);
   return true;
 }

@@ -275,6 +275,30 @@ void set_smem_attr_once(const void* func, int bytes, int slot);
 // Per-launch bookkeeping (abi.cu): call before/after each kernel launch.
 void launch_begin(const Launch& L, int kind);
 void launch_end(const Launch& L, int kind);
+// Records a launch's error for launch_status_take (the first one wins).
+void launch_note(cudaError_t e);
+// Programmatic dependent launch of the library's kernels: on unless the
+// environment sets MOE_PDL=0 (read once).
+bool pdl_enabled();
+
+// Launches a library kernel so that it may start while the previous kernel of
+// the stream is still running (the kernel waits, pdl_wait, before it touches
+// global memory).
+template <typename... P, typename... A>
+void launch_kernel(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                   A&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  launch_note(cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...));
+}
 // Status of the launches since the last call (MOE_OK or MOE_ERR_CUDA); resets it.
 moe_status launch_status_take();
 

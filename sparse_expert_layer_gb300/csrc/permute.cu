@@ -25,6 +25,7 @@ constexpr int kWords = kPermTokens / 32;
 
 __global__ void __launch_bounds__(kPermThreads)
     perm_count_kernel(const int32_t* ids, int32_t* bc, int T, int k, int E, DevStatus* st) {
+  pdl_enter();
   extern __shared__ int32_t cnt[];
   const int b = blockIdx.x;
   for (int e = threadIdx.x; e < E; e += kPermThreads) cnt[e] = 0;
@@ -44,6 +45,7 @@ __global__ void __launch_bounds__(kPermThreads)
 
 __global__ void __launch_bounds__(1024)
     perm_scan_kernel(int32_t* bc, int32_t* counts, int32_t* offsets, int nblk, int E) {
+  pdl_enter();
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t carry;
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
@@ -98,6 +100,7 @@ __global__ void __launch_bounds__(1024)
 __global__ void __launch_bounds__(kPermThreads)
     perm_scatter_kernel(const int32_t* ids, const int32_t* base, int32_t* s2e, int32_t* e2s, int T,
                         int k, int E) {
+  pdl_enter();
   extern __shared__ uint32_t bm[];  // [E][kWords]
   const int b = blockIdx.x;
   for (int i = threadIdx.x; i < E * kWords; i += kPermThreads) bm[i] = 0u;
@@ -137,6 +140,7 @@ struct GatherArgs {
 };
 
 __global__ void __launch_bounds__(256) perm_gather_kernel(GatherArgs a) {
+  pdl_enter();
   const int lane = threadIdx.x % 32;
   const int r = blockIdx.x * 8 + threadIdx.x / 32;
   if (r >= a.R) return;
@@ -294,6 +298,7 @@ __device__ void build_worklist(const WlArgs& a, const int32_t* offsets, int* sh)
 }
 
 __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
+  pdl_enter();
   __shared__ int sh[32];
   build_worklist(a, a.offsets, sh);
 }
@@ -307,6 +312,7 @@ __global__ void __launch_bounds__(1024)
     sort_small_kernel(const int32_t* ids, int32_t* counts, int32_t* offsets, int32_t* s2e,
                       int32_t* e2s, int T, int k, int E, WlArgs wla, int build_wl,
                       DevStatus* st) {
+  pdl_enter();
   extern __shared__ uint32_t sm[];  // bitmap [E][W], then offsets [E + 1]
   __shared__ int sh[32];
   const int tid = threadIdx.x;
@@ -408,16 +414,16 @@ void launch_sort_small(const Launch& L, const moe_config& c, int T, const int32_
   set_smem_attr_once(reinterpret_cast<const void*>(sort_small_kernel), kSortSmallSmem,
                      kAttrSortSmall);
   launch_begin(L, MOE_K_SORT);
-  sort_small_kernel<<<1, 1024, sort_small_smem(T, E), L.stream>>>(
-      ids, counts, offsets, s2e, e2s, T, c.top_k, E, a, wl ? 1 : 0, L.status);
+  launch_kernel(sort_small_kernel, 1, 1024, sort_small_smem(T, E), L.stream, ids, counts, offsets,
+                s2e, e2s, T, c.top_k, E, a, wl ? 1 : 0, L.status);
   launch_end(L, MOE_K_SORT);
 }
 
 void launch_perm_count(const Launch& L, int T, int k, int E, const int32_t* ids, int32_t* bc) {
   const int nblk = (T + kPermTokens - 1) / kPermTokens;
   launch_begin(L, MOE_K_PERM_COUNT);
-  perm_count_kernel<<<nblk, kPermThreads, E * sizeof(int32_t), L.stream>>>(ids, bc, T, k, E,
-                                                                          L.status);
+  launch_kernel(perm_count_kernel, nblk, kPermThreads, E * sizeof(int32_t), L.stream, ids, bc, T,
+                k, E, L.status);
   launch_end(L, MOE_K_PERM_COUNT);
 }
 
@@ -425,7 +431,7 @@ void launch_perm_scan(const Launch& L, int T, int E, int32_t* bc, int32_t* count
                       int32_t* offsets) {
   const int nblk = (T + kPermTokens - 1) / kPermTokens;
   launch_begin(L, MOE_K_PERM_SCAN);
-  perm_scan_kernel<<<1, 1024, 0, L.stream>>>(bc, counts, offsets, nblk, E);
+  launch_kernel(perm_scan_kernel, 1, 1024, 0, L.stream, bc, counts, offsets, nblk, E);
   launch_end(L, MOE_K_PERM_SCAN);
 }
 
@@ -436,7 +442,8 @@ void launch_perm_scatter(const Launch& L, int T, int k, int E, const int32_t* id
   set_smem_attr_once(reinterpret_cast<const void*>(perm_scatter_kernel), 200 * 1024,
                      kAttrPermScatter);
   launch_begin(L, MOE_K_PERM_SCATTER);
-  perm_scatter_kernel<<<nblk, kPermThreads, smem, L.stream>>>(ids, bc, s2e, e2s, T, k, E);
+  launch_kernel(perm_scatter_kernel, nblk, kPermThreads, smem, L.stream, ids, bc, s2e, e2s, T, k,
+                E);
   launch_end(L, MOE_K_PERM_SCATTER);
 }
 
@@ -454,7 +461,7 @@ void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32
   a.E_r = c.n_routed;
   a.w8a8 = c.wdtype == MOE_W8A8;
   launch_begin(L, MOE_K_PERM_GATHER);
-  perm_gather_kernel<<<(a.R + 7) / 8, 256, 0, L.stream>>>(a);
+  launch_kernel(perm_gather_kernel, (a.R + 7) / 8, 256, 0, L.stream, a);
   launch_end(L, MOE_K_PERM_GATHER);
 }
 
@@ -462,7 +469,7 @@ void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t*
                      const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk) {
   const WlArgs a = make_wl_args(L, c, T, offsets, wl, gemv_max_rows, gemv_chunk, tc_chunk);
   launch_begin(L, MOE_K_WORKLIST);
-  worklist_kernel<<<1, 1024, 0, L.stream>>>(a);
+  launch_kernel(worklist_kernel, 1, 1024, 0, L.stream, a);
   launch_end(L, MOE_K_WORKLIST);
 }
 

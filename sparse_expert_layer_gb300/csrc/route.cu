@@ -62,6 +62,7 @@ __device__ __forceinline__ void cp_async_wait() {
 // both operands keep their natural row-major layout (K contiguous), so the
 // tiles arrive by 16-byte asynchronous copies without any transposition.
 __global__ void __launch_bounds__(kRtThreads) router_kernel(RouterArgs a) {
+  pdl_enter();
   extern __shared__ __align__(16) uint8_t rt_smem[];
   __shared__ int last;
   const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
@@ -253,6 +254,7 @@ struct TopkArgs {
 constexpr int kTkBatch = 8;  // experts per lane whose logits are loaded together
 
 __global__ void topk_kernel(TopkArgs a) {
+  pdl_enter();
   extern __shared__ float sm[];
   const int warps = blockDim.x / 32;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -401,6 +403,7 @@ __global__ void topk_kernel(TopkArgs a) {
 // Rows hold [W3 | W2 | W1]: the small terms are accumulated first, while the
 // running sum is still small, which keeps the accumulator's rounding small.
 __global__ void router_split_kernel(const float* w, uint16_t* out, int E, int H) {
+  pdl_enter();
   const size_t n = (size_t)E * H;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -427,7 +430,7 @@ bool router_on_tensor_cores(const moe_config& c, int T) {
 
 void launch_router_split(const Launch& L, const float* w_r, int E, int H, uint16_t* out) {
   launch_begin(L, MOE_K_ROUTER);
-  router_split_kernel<<<4 * L.num_sms, 256, 0, L.stream>>>(w_r, out, E, H);
+  launch_kernel(router_split_kernel, 4 * L.num_sms, 256, 0, L.stream, w_r, out, E, H);
   launch_end(L, MOE_K_ROUTER);
 }
 
@@ -465,7 +468,7 @@ void launch_router(const Launch& L, const moe_config& c, int T, const void* x, c
   dim3 grid((a.E + kRtExp - 1) / kRtExp, (T + kRtTok - 1) / kRtTok, splits);
   set_smem_attr_once(reinterpret_cast<const void*>(router_kernel), kRtSmemBytes, kAttrRouter);
   launch_begin(L, MOE_K_ROUTER);
-  router_kernel<<<grid, kRtThreads, kRtSmemBytes, L.stream>>>(a);
+  launch_kernel(router_kernel, grid, kRtThreads, kRtSmemBytes, L.stream, a);
   launch_end(L, MOE_K_ROUTER);
 }
 
@@ -494,7 +497,7 @@ void launch_topk(const Launch& L, const moe_config& c, int T, const float* logit
   const size_t smem = per_warp * warps;
   set_smem_attr_once(reinterpret_cast<const void*>(topk_kernel), 100 * 1024, kAttrTopk);
   launch_begin(L, MOE_K_TOPK);
-  topk_kernel<<<(T + warps - 1) / warps, warps * 32, smem, L.stream>>>(a);
+  launch_kernel(topk_kernel, (T + warps - 1) / warps, warps * 32, smem, L.stream, a);
   launch_end(L, MOE_K_TOPK);
 }
 

@@ -200,6 +200,7 @@ constexpr int kPairQueueReaders = (2 + 4 + kEpiWarps) + (1 + 4 + kEpiWarps);
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     w8a8_pair_kernel(const __grid_constant__ Maps maps, const Args a) {
+  pdl_wait();
   using G = PGeom<MODE>;
   constexpr int NA = G::kNA;
   constexpr int TN = G::kTN;
@@ -346,7 +347,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fail();
         break;
       }
-      if (t.tile < 0) break;
+      if (t.tile < 0) {
+        pdl_trigger();  // no tiles left: the next kernel may launch
+        break;
+      }
       const int np = (t.n + 15) / 16 * 16;  // the pair's MMA N
       const int hrows = np / 2;             // this CTA's activation rows
       const int nb = (hrows + kBoxRows - 1) / kBoxRows;
@@ -698,6 +702,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 template <int MODE>
 __global__ void __launch_bounds__(256, 1)
     w8a8_exact_kernel(const int8_t* w0, const int8_t* w1, const uint16_t* act, const Args a) {
+  pdl_wait();
   constexpr int NA = MODE == kW8GateUp ? 2 : 1;
   constexpr int kPass = 128;
   __shared__ int8_t As[NA][kTcM][kBK + 4];
@@ -773,6 +778,7 @@ __global__ void __launch_bounds__(kQgThreads)
     quant_gather_kernel(const uint16_t* x, const int32_t* ids, const int32_t* e2s,
                         const int32_t* offsets, int gemv_max, uint16_t* x16, int8_t* x8,
                         float* scale, int32_t* norm2, int H, int k, int E_r) {
+  pdl_enter();
   __shared__ float red_f[kQgThreads / 32];
   __shared__ int red_i[kQgThreads / 32];
   __shared__ int rows[kMaxTopKQuant];   // all FFN rows: the fp16 ones, then the int8 ones
@@ -846,6 +852,7 @@ __global__ void __launch_bounds__(kQgThreads)
 __global__ void __launch_bounds__(256)
     i8_rows_to_f16_kernel(const int8_t* src, uint16_t* dst, int32_t* norm2, int R, int K,
                           const int32_t* nrows) {
+  pdl_enter();
   const int lane = threadIdx.x % 32;
   const int r = blockIdx.x * 8 + threadIdx.x / 32;
   const int rows = nrows ? min(R, *nrows) : R;
@@ -902,6 +909,7 @@ constexpr int kQrBatch = 4;  // row segments (float4) a lane loads at once
 __global__ void __launch_bounds__(256)
     quant_rows_kernel(const float* src, uint16_t* dst, int8_t* dst8, float* scale, int32_t* norm2,
                       int R, int K, const int32_t* offsets, int n_experts, int gemv_max) {
+  pdl_enter();
   const int lane = threadIdx.x % 32;
   const int r = blockIdx.x * 8 + threadIdx.x / 32;
   const int rows = min(R, offsets[n_experts]);
@@ -1047,12 +1055,12 @@ bool launch_pair(const Launch& L, const W8Pass& p) {
                      kAttrW8Base + MODE);
   const int grid = std::max(2, L.num_sms & ~1);  // whole clusters of two
   launch_begin(L, kind);
-  w8a8_pair_kernel<MODE><<<grid, kThreads, G::kSmemBytes, L.stream>>>(maps, a);
+  launch_kernel(w8a8_pair_kernel<MODE>, grid, kThreads, G::kSmemBytes, L.stream, maps, a);
   launch_end(L, kind);
   launch_begin(L, MOE_K_W8_EXACT);
-  w8a8_exact_kernel<MODE><<<L.num_sms, 256, 0, L.stream>>>(
-      static_cast<const int8_t*>(p.w0), static_cast<const int8_t*>(p.w1),
-      static_cast<const uint16_t*>(p.act), a);
+  launch_kernel(w8a8_exact_kernel<MODE>, L.num_sms, 256, 0, L.stream,
+                static_cast<const int8_t*>(p.w0), static_cast<const int8_t*>(p.w1),
+                static_cast<const uint16_t*>(p.act), a);
   launch_end(L, MOE_K_W8_EXACT);
   return true;
 }
@@ -1070,7 +1078,8 @@ bool launch_w8a8(const Launch& L, const W8Pass& p) {
 void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, int32_t* norm2,
                            int R, int K, const int32_t* nrows) {
   launch_begin(L, MOE_K_QUANT_H);
-  i8_rows_to_f16_kernel<<<(R + 7) / 8, 256, 0, L.stream>>>(src, dst, norm2, R, K, nrows);
+  launch_kernel(i8_rows_to_f16_kernel, (R + 7) / 8, 256, 0, L.stream, src, dst, norm2, R, K,
+                nrows);
   launch_end(L, MOE_K_QUANT_H);
 }
 
@@ -1078,9 +1087,9 @@ void launch_quant_gather(const Launch& L, const moe_config& c, int T, const void
                          const int32_t* ids, const int32_t* e2s, const int32_t* offsets,
                          int gemv_max, uint16_t* x16, int8_t* x8, float* scale, int32_t* norm2) {
   launch_begin(L, MOE_K_PERM_GATHER);
-  quant_gather_kernel<<<T, kQgThreads, 0, L.stream>>>(static_cast<const uint16_t*>(x), ids, e2s,
-                                                      offsets, gemv_max, x16, x8, scale, norm2,
-                                                      c.hidden, c.top_k, c.n_routed);
+  launch_kernel(quant_gather_kernel, T, kQgThreads, 0, L.stream, static_cast<const uint16_t*>(x),
+                ids, e2s, offsets, gemv_max, x16, x8, scale, norm2, c.hidden, c.top_k,
+                c.n_routed);
   launch_end(L, MOE_K_PERM_GATHER);
 }
 
@@ -1088,8 +1097,8 @@ void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, int8_t*
                        float* scale, int32_t* norm2, int R, int K, const int32_t* offsets,
                        int n_experts, int gemv_max) {
   launch_begin(L, MOE_K_QUANT_H);
-  quant_rows_kernel<<<(R + 7) / 8, 256, 0, L.stream>>>(src, dst, dst8, scale, norm2, R, K,
-                                                       offsets, n_experts, gemv_max);
+  launch_kernel(quant_rows_kernel, (R + 7) / 8, 256, 0, L.stream, src, dst, dst8, scale, norm2, R,
+                K, offsets, n_experts, gemv_max);
   launch_end(L, MOE_K_QUANT_H);
 }
 
