@@ -1,0 +1,89 @@
+"""Launch-order checks of moe_layer_forward.
+
+The library's kernels are launched with programmatic dependent launch: each may
+be scheduled while its predecessor on the stream is finishing and waits for it
+before touching device memory.  A kernel that read or wrote memory too early
+would race with the kernel before it, or with the previous call on the same
+workspace.  These tests look for such races and compare against plain launches.
+"""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests import gpu_support as gs
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def m():
+    return gs.lib()
+
+
+def _forward(m, spec, d, cfg, x, out, ws):
+    w = d["wts_d"]
+    m.moe_layer_forward(cfg, x.shape[0], x, d["w_r_d"], d["bias_d"], w.get("w_gate"),
+                        w.get("w_up"), w.get("w_down"), w.get("s_gate"), w.get("s_up"),
+                        w.get("s_down"), w.get("shared_gate"), w.get("shared_up"),
+                        w.get("shared_down"), out, ws)
+
+
+@pytest.mark.parametrize("name", ["longcat_s", "dsv3_s", "ragged_s", "w8a8_s"])
+def test_back_to_back_calls_on_one_workspace(m, name):
+    # Calls alternate between two inputs on one stream and one workspace with
+    # no synchronisation in between; each must equal its input's result from a
+    # synchronised call.  A kernel that ran ahead of its predecessor would mix
+    # the two inputs' intermediate buffers.
+    spec = synth.spec(name)
+    d = gs.inputs(spec)
+    xa = d["x_d"]
+    xb = torch.flip(xa, dims=[0]).contiguous()
+    ref_a = gs.run_layer(m, spec, d, out_fp32=True, x=xa)
+    ref_b = gs.run_layer(m, spec, d, out_fp32=True, x=xb)
+    cfg = m.config_from_spec(spec, out_fp32=True)
+    T = xa.shape[0]
+    ws = m.workspace(cfg, T, xa.device)
+    outs = [torch.empty((T, spec["hidden"]), dtype=torch.float32, device=xa.device)
+            for _ in range(12)]
+    for i, out in enumerate(outs):
+        _forward(m, spec, d, cfg, xa if i % 2 == 0 else xb, out, ws)
+    torch.cuda.synchronize()
+    assert m.moe_check_device_status(ws) == m.MOE_OK
+    for i, out in enumerate(outs):
+        assert torch.equal(out, ref_a if i % 2 == 0 else ref_b), f"call {i}"
+
+
+_PLAIN = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import synth
+from tests import gpu_support as gs
+m = gs.lib()
+spec = synth.spec(sys.argv[2])
+d = gs.inputs(spec)
+out = gs.run_layer(m, spec, d, out_fp32=True)
+np.save(sys.argv[3], out.cpu().numpy())
+"""
+
+
+@pytest.mark.parametrize("name", ["dsv3_s", "w8a8_s"])
+def test_plain_launches_give_the_same_bits(m, name, tmp_path):
+    # MOE_PDL=0 (read once per process) launches every kernel in plain stream
+    # order; the outputs must be identical.
+    spec = synth.spec(name)
+    d = gs.inputs(spec)
+    got = gs.run_layer(m, spec, d, out_fp32=True).cpu().numpy()
+    path = str(tmp_path / "plain.npy")
+    env = dict(os.environ, MOE_PDL="0", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-c", _PLAIN, ROOT, name, path], env=env, cwd=ROOT,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    plain = np.load(path)
+    assert np.array_equal(got, plain)
