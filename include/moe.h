@@ -38,6 +38,10 @@
  *    waits for that kernel to complete before it reads or writes device memory,
  *    so results and stream order are those of plain launches.  The environment
  *    variable MOE_PDL=0, read once per process, turns this off.
+ *  - Small-batch routing runs its matmul on tensor cores where the batch gives
+ *    enough parallel work; MOE_ROUTER_TC=0 (read once) keeps it on CUDA cores.
+ *    Both compute fp32-class logits (routing ids do not depend on the choice
+ *    beyond ties closer than the logits' rounding).
  *  - bf16 tensors are passed as `const void*` holding IEEE bfloat16 values.
  *  - Expert indices 0 .. n_routed-1 are FFN experts; n_routed .. n_routed+n_zero-1
  *    are zero-computation experts (no weights; their pick contributes w * x_t).

@@ -376,7 +376,13 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
 __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity));
 }
-// Every thread of both CTAs.
+// A 32-bit load from the shared memory of a CTA of the cluster (cluster address).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr));
+  return v;
+}
+// Every thread of every CTA of the cluster.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");

@@ -267,6 +267,7 @@ enum {
   kAttrW8Base = kAttrGemvBase + 8,  // 3 slots: W8A8 modes
   kAttrGemvI8Base = kAttrW8Base + 3, // 8 slots: W8A8 GEMV (gate/up, down) x row cap
   kAttrRouter = kAttrGemvI8Base + 8,
+  kAttrRouterTc,
   kAttrSortSmall,
   kAttrSlots
 };

@@ -14,7 +14,12 @@
 // sigmoid; the group stage follows the grouped-expert designs of the Pangu Pro
 // MoE disclosure (opening section and section H2P); picks are taken in
 // descending key order, ties to the lower expert index.
+#include <cudaTypedefs.h>
 #include <math.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -420,7 +425,274 @@ __global__ void router_split_kernel(const float* w, uint16_t* out, int E, int H)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Decode router on tensor cores.
+//
+// The same logits, x . W_r^T, with W_r split inside the kernel into three bf16
+// terms as above (W1 + W2 + W3 == W, every product exact in fp32), multiplied
+// by tcgen05 MMAs (kind::f16, fp32 accumulate).  A CTA owns 128 experts (the
+// MMA's M side) x 128 tokens (N) x one eighth of H:
+//   - W_r arrives by TMA, one 128 x 64 fp32 box per K chunk, into a three-stage
+//     ring; x by TMA, 128 x 64 bf16 boxes, two stages;
+//   - all threads split a chunk's weights into three bf16 planes (128-byte
+//     swizzle, the MMA's K-major layout; the planes are double-buffered, so the
+//     split of one chunk overlaps the MMAs of the one before), then the first
+//     thread issues the chunk's MMAs: the W3 and W2 products accumulate in one
+//     TMEM accumulator, the W1 products in another, so the small terms are never
+//     rounded against the large ones; the CTA's slice of the logits is the sum.
+// The eight CTAs of an (expert, token) tile form a cluster and add their slices
+// in rank order through distributed shared memory: the result does not depend
+// on scheduling, and no scratch memory is needed.
+constexpr int kRcM = 128;                     // experts per tile (MMA M)
+constexpr int kRcN = 128;                     // tokens per tile (MMA N, rounded up to 16)
+constexpr int kRcK = 64;                      // K chunk: one 128-byte bf16 row
+constexpr int kRcSplits = 8;                  // CTAs per cluster, one H slice each
+constexpr int kRcThreads = 256;
+constexpr int kRcWStages = 3;
+constexpr int kRcWStage = kRcM * kRcK * 4;    // one fp32 W chunk (TMA box, 256-byte rows)
+constexpr int kRcPlane = kRcM * kRcK * 2;     // one bf16 term of a W chunk
+constexpr int kRcPlanes = 3 * kRcPlane;       // W3, W2, W1 of a chunk
+constexpr int kRcX = kRcN * kRcK * 2;         // one x chunk
+constexpr int kRcXOff = 2 * kRcPlanes;        // two plane buffers first
+constexpr int kRcWOff = kRcXOff + 2 * kRcX;
+constexpr int kRcBarOff = kRcWOff + kRcWStages * kRcWStage;
+constexpr int kRcSmem = 1024 + kRcBarOff + 128;
+static_assert(kRcSmem <= 227 * 1024, "decode router shared memory");
+static_assert(kRcWStages * kRcWStage >= kRcN * kRcM * 4, "a logits slice fits in the W ring");
+
+__device__ __forceinline__ uint32_t bf162_as_u32(__nv_bfloat162 v) {
+  uint32_t u;
+  memcpy(&u, &v, sizeof u);
+  return u;
+}
+
+// Two weights to their three bf16 terms, packed in pairs (low half: a).
+__device__ __forceinline__ void split3x2(float a, float b, uint32_t& p1, uint32_t& p2,
+                                         uint32_t& p3) {
+  p1 = bf162_as_u32(__floats2bfloat162_rn(a, b));
+  const float ra = a - bf16lo(p1), rb = b - bf16hi(p1);
+  p2 = bf162_as_u32(__floats2bfloat162_rn(ra, rb));
+  const float sa = ra - bf16lo(p2), sb = rb - bf16hi(p2);
+  p3 = bf162_as_u32(__floats2bfloat162_rn(sa, sb));
+}
+
+__global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap xmap,
+                     const __grid_constant__ CUtensorMap wmap, float* logits, int T, int E, int H,
+                     DevStatus* st) {
+  pdl_enter();
+  extern __shared__ uint8_t rc_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(rc_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* x_full = reinterpret_cast<uint64_t*>(smem + kRcBarOff);  // [2]
+  uint64_t* w_full = x_full + 2;                                      // [kRcWStages]
+  uint64_t* mma_done = w_full + kRcWStages;                           // [2], per plane buffer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int e0 = blockIdx.x * kRcM, t0 = blockIdx.y * kRcN;
+  const int rank = (int)cluster_rank();  // this CTA's H slice
+  const int nch_all = H / kRcK;
+  const int per = (nch_all + kRcSplits - 1) / kRcSplits;
+  const int c0 = min(nch_all, rank * per);
+  const int nch = min(nch_all, c0 + per) - c0;
+  const int rows = min(kRcN, T - t0);
+  const uint32_t N = (uint32_t)((rows + 15) / 16 * 16);
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&x_full[b]), 1);
+      mbar_init(smem_u32(&mma_done[b]), 1);
+    }
+    for (int s = 0; s < kRcWStages; ++s) mbar_init(smem_u32(&w_full[s]), 1);
+    fence_barrier_init();
+    prefetch_tensormap(&xmap);
+    prefetch_tensormap(&wmap);
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 2 * kRcN);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint64_t pol_x = policy_evict_last(), pol_w = policy_evict_first();
+  // chunk i of this CTA's slice (issued by thread 0); rows past E or T read as zero
+  auto w_copy = [&](int i) {
+    const uint32_t bar = smem_u32(&w_full[i % kRcWStages]);
+    mbar_arrive_expect_tx(bar, (uint32_t)kRcWStage);
+    tma_load_2d(smem_u32(smem + kRcWOff + (i % kRcWStages) * kRcWStage), &wmap, (c0 + i) * kRcK,
+                e0, bar, pol_w);
+  };
+  auto x_copy = [&](int i) {
+    const uint32_t bar = smem_u32(&x_full[i & 1]);
+    mbar_arrive_expect_tx(bar, (uint32_t)kRcX);
+    tma_load_3d(smem_u32(smem + kRcXOff + (i & 1) * kRcX), &xmap, (c0 + i) * kRcK, t0, 0, bar,
+                pol_x);
+  };
+  if (tid == 0)
+    for (int i = 0; i < kRcWStages - 1 && i < nch; ++i) w_copy(i);
+  const uint32_t idesc = idesc_bf16_f32(kRcM, N);
+  for (int i = 0; i < nch; ++i) {
+    const int pbuf = i & 1;
+    // (a wait that runs out is reported; the pipeline keeps its order so that
+    // every thread reaches the same barriers)
+    // plane buffer pbuf and x stage pbuf are free once chunk i - 2's MMAs are done
+    if (i >= 2 && !mbar_wait(smem_u32(&mma_done[pbuf]), (uint32_t)((i - 2) >> 1) & 1u) &&
+        lane == 0)
+      raise_status(st, kStTimeout, MOE_K_ROUTER);
+    if (tid == 0) {
+      x_copy(i);
+      // the W stage of chunk i - 1 was read before the last block barrier
+      if (i + kRcWStages - 1 < nch) w_copy(i + kRcWStages - 1);
+    }
+    if (!mbar_wait(smem_u32(&w_full[i % kRcWStages]), (uint32_t)(i / kRcWStages) & 1u) &&
+        lane == 0)
+      raise_status(st, kStTimeout, MOE_K_ROUTER);
+    // split: a quarter warp takes one W row, eight 16-byte plane chunks of it
+    const uint8_t* wst = smem + kRcWOff + (i % kRcWStages) * kRcWStage;
+    uint8_t* planes = smem + pbuf * kRcPlanes;
+#pragma unroll
+    for (int m = 0; m < kRcM * 8 / kRcThreads; ++m) {
+      const int u = tid + m * kRcThreads;
+      const int r = u >> 3, j = u & 7;
+      const float4 va = *reinterpret_cast<const float4*>(wst + r * kRcK * 4 + j * 32);
+      const float4 vb = *reinterpret_cast<const float4*>(wst + r * kRcK * 4 + j * 32 + 16);
+      uint4 q1, q2, q3;
+      split3x2(va.x, va.y, q1.x, q2.x, q3.x);
+      split3x2(va.z, va.w, q1.y, q2.y, q3.y);
+      split3x2(vb.x, vb.y, q1.z, q2.z, q3.z);
+      split3x2(vb.z, vb.w, q1.w, q2.w, q3.w);
+      const int off = r * 128 + ((j ^ (r & 7)) * 16);
+      *reinterpret_cast<uint4*>(planes + 0 * kRcPlane + off) = q3;
+      *reinterpret_cast<uint4*>(planes + 1 * kRcPlane + off) = q2;
+      *reinterpret_cast<uint4*>(planes + 2 * kRcPlane + off) = q1;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      if (!mbar_wait(smem_u32(&x_full[pbuf]), (uint32_t)(i >> 1) & 1u))
+        raise_status(st, kStTimeout, MOE_K_ROUTER);
+      tc_fence_after();
+      const uint32_t xb = smem_u32(smem + kRcXOff + pbuf * kRcX);
+      const uint32_t pb = smem_u32(planes);
+#pragma unroll
+      for (int kk = 0; kk < kRcK / 16; ++kk) {
+        const uint64_t bd = sdesc_sw128(xb + kk * 32);
+        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+        tc_mma_bf16(tmem, sdesc_sw128(pb + 0 * kRcPlane + kk * 32), bd, idesc, acc);  // W3
+        tc_mma_bf16(tmem, sdesc_sw128(pb + 1 * kRcPlane + kk * 32), bd, idesc, 1u);   // W2
+        tc_mma_bf16(tmem + kRcN, sdesc_sw128(pb + 2 * kRcPlane + kk * 32), bd, idesc, acc);  // W1
+      }
+      tc_commit(smem_u32(&mma_done[pbuf]));
+    }
+  }
+  // the last commit covers every MMA of the CTA
+  if (nch > 0 && !mbar_wait(smem_u32(&mma_done[(nch - 1) & 1]), (uint32_t)((nch - 1) >> 1) & 1u) &&
+      lane == 0)
+    raise_status(st, kStTimeout, MOE_K_ROUTER);
+  tc_fence_after();
+  __syncthreads();  // the W ring is free for the slice
+
+  // this CTA's slice, [token][expert]: small-term sum + W1 sum
+  float* slice = reinterpret_cast<float*>(smem + kRcWOff);
+  {
+    const int quad = warp % 4, half = warp / 4;  // TMEM lane quadrant, token half
+    const int el = quad * 32 + lane;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int tc = half * 64 + cc * 32;
+      uint32_t sm[32], bg[32];
+      if (nch > 0 && tc < (int)N) {
+        const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + tc;
+        tmem_ld32(ta, sm);
+        tmem_ld32(ta + kRcN, bg);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) sm[u] = bg[u] = 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        slice[(tc + u) * kRcM + el] = __uint_as_float(sm[u]) + __uint_as_float(bg[u]);
+    }
+  }
+  cluster_sync_all();  // every CTA's slice is in place
+  {
+    // this CTA adds the eight slices, in rank order, for 16 of the tile's tokens
+    const int el = tid % kRcM;
+    const int tb = rank * (kRcN / kRcSplits) + (tid / kRcM) * (kRcN / kRcSplits / 2);
+    const uint32_t base = smem_u32(slice);
+#pragma unroll 1
+    for (int u = 0; u < kRcN / kRcSplits / 2; ++u) {
+      const int t = tb + u;
+      if (t < rows) {
+        const uint32_t a = base + (uint32_t)((t * kRcM + el) * 4);
+        float v[kRcSplits];
+#pragma unroll
+        for (int q = 0; q < kRcSplits; ++q) v[q] = ld_cluster_f32(mapa_shared(a, (uint32_t)q));
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < kRcSplits; ++q) sum += v[q];
+        if (e0 + el < E) logits[(size_t)(t0 + t) * E + e0 + el] = sum;
+      }
+    }
+  }
+  cluster_sync_all();  // no CTA leaves while another reads its slice
+  tc_fence_before();
+  if (warp == 0) tmem_dealloc(tmem, 2 * kRcN);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 rc_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// W_r [E][H] fp32 as 128-expert x 64-column boxes (256-byte rows, no swizzle),
+// rows past E read as zero.
+bool rc_w_map(CUtensorMap* m, const float* w, int E, int H) {
+  auto fn = rc_encode_fn();
+  if (!fn || !w) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)E};
+  const cuuint64_t strides[1] = {(cuuint64_t)H * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)kRcK, (cuuint32_t)kRcM};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(w), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// x [T][H] bf16 as 128-token x 64-column boxes, 128-byte swizzle, rows past T
+// read as zero.
+bool rc_x_map(CUtensorMap* m, const void* x, int T, int H) {
+  auto fn = rc_encode_fn();
+  if (!fn || !x) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)T, 1};
+  const cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)T * H * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kRcK, (cuuint32_t)kRcN, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
+
+// The decode router on tensor cores, unless the environment sets
+// MOE_ROUTER_TC=0 (read once; the CUDA-core router then runs).
+bool router_tc_decode_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_ROUTER_TC");
+    return !(v && v[0] == '0' && v[1] == 0);
+  }();
+  return on;
+}
 
 bool router_on_tensor_cores(const moe_config& c, int T) {
   const int E = c.n_routed + c.n_zero;
@@ -465,6 +737,27 @@ void launch_router(const Launch& L, const moe_config& c, int T, const void* x, c
   a.H = c.hidden;
   a.splits = splits;
   a.kper = ((c.hidden + splits - 1) / splits + kRtK - 1) / kRtK * kRtK;
+  const int E = c.n_routed + c.n_zero;
+  CUtensorMap xmap, wmap;
+  memset(&xmap, 0, sizeof xmap);
+  memset(&wmap, 0, sizeof wmap);
+  // The tensor-core router runs where it has enough parallel work: at least 32
+  // CTAs, or at most four K chunks per CTA (a few-tile layer with a long H, such
+  // as 256 experts x 128 tokens x 7168, keeps the CUDA-core router's wider grid).
+  const int rc_tiles = ((E + kRcM - 1) / kRcM) * ((T + kRcN - 1) / kRcN);
+  const int rc_chunks = (c.hidden / kRcK + kRcSplits - 1) / kRcSplits;
+  const bool rc_fits = rc_tiles * kRcSplits >= 32 || rc_chunks <= 4;
+  if (router_tc_decode_enabled() && c.hidden % kRcK == 0 && rc_fits &&
+      rc_x_map(&xmap, x, T, c.hidden) && rc_w_map(&wmap, w_r, E, c.hidden)) {
+    // decode router on tensor cores: clusters of kRcSplits CTAs, one per H slice
+    const dim3 g((E + kRcM - 1) / kRcM, (T + kRcN - 1) / kRcN, kRcSplits);
+    set_smem_attr_once(reinterpret_cast<const void*>(router_tc_kernel), kRcSmem, kAttrRouterTc);
+    launch_begin(L, MOE_K_ROUTER);
+    launch_kernel(router_tc_kernel, g, kRcThreads, kRcSmem, L.stream, xmap, wmap, logits, T, E,
+                  c.hidden, L.status);
+    launch_end(L, MOE_K_ROUTER);
+    return;
+  }
   dim3 grid((a.E + kRtExp - 1) / kRtExp, (T + kRtTok - 1) / kRtTok, splits);
   set_smem_attr_once(reinterpret_cast<const void*>(router_kernel), kRtSmemBytes, kAttrRouter);
   launch_begin(L, MOE_K_ROUTER);
