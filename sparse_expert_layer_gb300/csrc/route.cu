@@ -7,7 +7,9 @@
 // K steps in flight while the current one is multiplied out of shared memory,
 // 4 x 4 outputs per thread.  Each output is summed over K in order; with
 // split-K, the last CTA of a tile to finish adds the slices in a fixed order,
-// so logits do not depend on scheduling.
+// so logits do not depend on scheduling.  Where H is a multiple of 64 and the
+// batch gives the tensor cores enough parallel work, the tensor-core router
+// below takes its place (it needs neither the partials nor the tile counters).
 //
 // Top-k: one warp per token.  Scores are a softmax over every expert (zero-
 // computation ones included, as in LongCat-Flash's 768-way choice) or a
