@@ -6,8 +6,13 @@ Default workload: the LongCat-Flash-shaped decode layer (T=64 tokens, hidden
 6144, 512 SwiGLU experts of intermediate 2048 plus 256 zero-computation
 experts, softmax top-12), weights bf16 ~N(0, 0.02).
 
-Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle
-instead, on a bounded sample of the same workload.
+Prints one JSON line (rank 0).  Its headline is the main workload; its
+"configs" object holds the same measurements (ms per step with p50/p90,
+tokens/s, the layer's fraction of its roofline, the dominant kernel's roofline,
+the oracle timed on a sample) for the other headline layers: the tiny layer, the
+DSv3- and Pangu-shaped decode layers and the skewed W8A8 prefill layer, each
+generated, measured and freed in turn.  --impl reference times the fp64 CPU
+oracle instead, on a bounded sample of the main workload.
 
 Multi-GPU: the layer does not shard across GPUs here (no exchange step is
 built), so --gpus N under torchrun runs N independent replicas; the timing
@@ -45,8 +50,13 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="longcat")
     ap.add_argument("--gemv-max-rows", type=int, default=0)
+    ap.add_argument("--combine", default="default", choices=["default", "ordered", "fused"],
+                    help="how the expert outputs return to their tokens (library default: fused)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds-extra", type=float, default=5.0)
+    ap.add_argument("--extra-configs", default=",".join(EXTRA_CONFIGS),
+                    help="comma-separated layers measured after the main one ('none': skip)")
     return ap.parse_args()
 
 
@@ -360,16 +370,28 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ ours --
-def run_ours(args, rank, world, local):
+# The other headline layers, measured after the main one in the same run (one
+# layer's weights on the device at a time): the tiny layer, the DSv3- and
+# Pangu-shaped decode layers and the skewed W8A8 prefill layer.
+EXTRA_CONFIGS = ["tiny", "dsv3", "pangu", "w8a8_prefill"]
+COMBINE_MODES = {"default": 0, "ordered": 1, "fused": 2}
+
+
+def zero_pick_share(spec, counts_h):
+    """Share of the T*k picks that land on zero-computation experts."""
+    return float(counts_h[spec["n_routed"]:].sum()) / (spec["T"] * spec["top_k"])
+
+
+def measure(args, spec, dev, world, full):
+    """Times the layer on one workload.  full: also the launch count, CUDA-graph
+    replay and the end-to-end run with host buffers (the main workload)."""
     import sparse_expert_layer_gb300 as moe
 
-    dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
-    spec = synth.spec(args.config)
     T, H = spec["T"], spec["hidden"]
     x, w_r, bias, _ = synth.make_inputs(spec)
     wts = synth.draw_weights(spec, device=dev)
-    cfg = moe.config_from_spec(spec, out_fp32=False, gemv_max_rows=args.gemv_max_rows)
+    cfg = moe.config_from_spec(spec, out_fp32=False, gemv_max_rows=args.gemv_max_rows,
+                               combine=COMBINE_MODES[args.combine])
     x_d, w_r_d = x.to(dev), w_r.to(dev)
     bias_d = None if bias is None else bias.to(dev)
     layer = moe.MoeLayer(cfg, T, wts, w_r_d, bias_d, dev)
@@ -392,6 +414,13 @@ def run_ours(args, rank, world, local):
     counts_h = counts.cpu().numpy()
     alg_bytes, U = algorithmic_bytes(spec, counts_h)
     del x_perm
+    if spec["n_zero"] > 0 and spec["bias_kind"] == "iid":
+        # the LongCat-shaped router is drawn so that about a third of the picks
+        # land on zero-computation experts
+        share = zero_pick_share(spec, counts_h)
+        if not 0.30 <= share <= 0.37:
+            raise RuntimeError(f"{spec['name']}: zero-expert pick share {share:.3f} "
+                               "outside [0.30, 0.37]")
 
     for _ in range(args.warmup):
         layer.forward(x_d, out)
@@ -404,7 +433,7 @@ def run_ours(args, rank, world, local):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev.index or 0) as clk:
         start.record(stream)
         for _ in range(args.steps):
             layer.forward(x_d, out)
@@ -443,8 +472,34 @@ def run_ours(args, rank, world, local):
     per_kernel = moe.timing_collect()
     moe.timing_enable(False)
 
-    # the same step replayed from a CUDA graph (launch gaps removed)
-    graph = None
+    res = {"spec": spec, "combine": args.combine, "value": value, "ms_step": ms_step,
+           "p50": p50, "p90": p90,
+           "gpu_launches": gpu_launches, "clocks": clk.summary(), "per_kernel": per_kernel,
+           "counts": counts_h, "alg_bytes": alg_bytes, "U": U}
+    if full:
+        res["graph"] = graph_replay(args, layer, x_d, out, dev, world, T)
+        res["e2e"] = end_to_end(args, layer, x, x_d, out, dev, world, T, H)
+    res["cpu"] = None
+    if world == 1 and not args.no_cpu_baseline:
+        n_tok = min(T, os.cpu_count() or 1)
+        secs = args.cpu_seconds if full else args.cpu_seconds_extra
+        v, cores, reps, dt, n_exp = oracle_sample(spec, x, w_r, bias, wts, n_tok, secs)
+        res["cpu"] = {
+            "value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n_tok} of {T} tokens, full layer, {n_exp} experts, "
+                      f"{reps} repetitions in {dt:.1f} s",
+            "nproc": os.cpu_count(), "cpu_model": cpu_model()}
+    del layer, wts
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def graph_replay(args, layer, x_d, out, dev, world, T):
+    """The same step replayed from a CUDA graph (launch gaps removed)."""
+    import sparse_expert_layer_gb300 as moe
+
+    stream = torch.cuda.current_stream(dev)
     try:
         gs = torch.cuda.Stream(dev)
         gs.wait_stream(stream)
@@ -465,12 +520,15 @@ def run_ours(args, rank, world, local):
         gms = max_over_ranks(g0.elapsed_time(g1), world, dev)
         if moe.moe_check_device_status(layer.ws) != moe.MOE_OK:
             raise RuntimeError("device status set during graph replay")
-        graph = {"value": whole_job_rate(world, T, args.steps, gms), "unit": "tokens/s",
-                 "ms_per_step": gms / args.steps}
+        return {"value": whole_job_rate(world, T, args.steps, gms), "unit": "tokens/s",
+                "ms_per_step": gms / args.steps}
     except RuntimeError as exc:  # capture unavailable: report why, keep the line
-        graph = {"unavailable": str(exc)[:200]}
+        return {"unavailable": str(exc)[:200]}
 
-    # end to end: host buffers, H2D of x and D2H of out inside the timed region
+
+def end_to_end(args, layer, x, x_d, out, dev, world, T, H):
+    """Host buffers: the H2D copy of x and the D2H copy of out inside the timed region."""
+    stream = torch.cuda.current_stream(dev)
     x_h = x.pin_memory()
     out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     x_e = torch.empty_like(x_d)
@@ -489,17 +547,18 @@ def run_ours(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    e2e = {"value": whole_job_rate(world, T, args.steps, ms_e2e), "unit": "tokens/s",
-           "h2d_bytes_per_step": x.numel() * 2, "d2h_bytes_per_step": out.numel() * 2}
+    return {"value": whole_job_rate(world, T, args.steps, ms_e2e), "unit": "tokens/s",
+            "h2d_bytes_per_step": x.numel() * 2, "d2h_bytes_per_step": out.numel() * 2}
 
-    # roofline of the dominant kernel
+
+def roofline_of(args, res):
+    """Roofline of the dominant kernel, the layer's HBM and tensor fractions."""
+    spec, per_kernel, counts_h = res["spec"], res["per_kernel"], res["counts"]
     peak, peak_kind = hbm_peak()
     tpeak, tpeak_kind = tensor_peak()
     dom = max(per_kernel, key=lambda kname: per_kernel[kname][0])
     dom_ms, dom_n = per_kernel[dom]
-    R_real = int(counts_h[:spec["n_routed"]].sum())
     work = kernel_work(spec, counts_h, args.gemv_max_rows)
-    w8 = spec["wdtype"] == "w8a8"
     roof = None
     if dom in work and dom_n:
         kb, kf = work[dom]
@@ -518,42 +577,85 @@ def run_ours(args, rank, world, local):
                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
                     "traffic": traffic_for(dom, kb, spec["wdtype"]),
                     "algorithmic_bytes_per_launch": kb, "avg_launch_ms": dom_ms / dom_n}
-    layer_gbs = alg_bytes / (ms_step / 1e3) / 1e9
+    ms_step = res["ms_step"]
+    layer_gbs = res["alg_bytes"] / (ms_step / 1e3) / 1e9
     layer_flops = sum(f for k_, (b_, f) in work.items() if k_.startswith(("tc_", "gemv_")))
+    layer_hbm = {"achieved_gbs": layer_gbs, "algorithmic_bytes": res["alg_bytes"],
+                 "frac": layer_gbs / peak, "peak": peak, "peak_source": peak_kind}
+    layer_tensor = {"achieved_tflops": layer_flops / (ms_step / 1e3) / 1e12,
+                    "expert_flops": layer_flops, "peak": tpeak, "peak_source": tpeak_kind,
+                    "frac": layer_flops / (ms_step / 1e3) / 1e12 / tpeak}
+    return roof, layer_hbm, layer_tensor
 
+
+def config_block(spec, res):
+    counts_h = res["counts"]
+    gb = res["alg_bytes"] / 1e9
+    l2 = (f"inputs larger than L2: {gb:.1f} GB of weights streamed per step, 129 MB L2"
+          if gb > 0.5 else f"L2-resident: {gb * 1e3:.1f} MB per step, not flushed "
+          "(latency-bound layer)")
+    return {"workload": describe(spec), "tokens": spec["T"], "unique_experts": res["U"],
+            "real_picks": int(counts_h[:spec["n_routed"]].sum()),
+            "zero_pick_share": zero_pick_share(spec, counts_h) if spec["n_zero"] else 0.0,
+            "l2": l2, "combine": res["combine"]}
+
+
+def summary_of(args, res):
+    """One entry of the per-layer table: every headline layer but the main one."""
+    spec = res["spec"]
+    roof, layer_hbm, layer_tensor = roofline_of(args, res)
+    w8 = spec["wdtype"] == "w8a8"
+    bound = "tensor" if w8 else ("latency" if spec["name"] == "tiny" else "hbm")
+    return {
+        "config": config_block(spec, res), "dtype": "int8" if w8 else "bf16",
+        "steps": args.steps, "warmup": args.warmup,
+        "value": res["value"], "unit": "tokens/s", "ms_per_step": res["ms_step"],
+        "ms_per_step_p50": res["p50"], "ms_per_step_p90": res["p90"],
+        "layer_bound": bound,
+        "layer_frac": layer_tensor["frac"] if w8 else layer_hbm["frac"],
+        "layer_hbm": layer_hbm, "layer_tensor": layer_tensor, "roofline": roof,
+        "kernels_ms_per_step": {k: v[0] / args.steps for k, v in res["per_kernel"].items()
+                                if v[1]},
+        "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
+        "cpu_baseline": res["cpu"],
+    }
+
+
+def run_ours(args, rank, world, local):
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    spec = synth.spec(args.config)
+    res = measure(args, spec, dev, world, full=True)
+    T = spec["T"]
+    roof, layer_hbm, layer_tensor = roofline_of(args, res)
+    w8 = spec["wdtype"] == "w8a8"
     line = {
-        "metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "ms_per_step_p50": p50, "ms_per_step_p90": p90,
+        "metric": "MoE-layer tokens/s", "value": res["value"], "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": res["ms_step"], "ms_per_step_p50": res["p50"],
+        "ms_per_step_p90": res["p90"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8" if w8 else "bf16",
         "data": "synthetic",
-        "config": {"workload": describe(spec), "tokens": T, "unique_experts": U,
-                   "real_picks": R_real, "l2": "inputs larger than L2: "
-                   f"{alg_bytes / 1e9:.1f} GB of weights streamed per step, 129 MB L2",
-                   "parallelism": f"replicas x{world}"},
-        "layer_hbm": {"achieved_gbs": layer_gbs, "algorithmic_bytes": alg_bytes,
-                      "frac": layer_gbs / peak, "peak": peak, "peak_source": peak_kind},
-        "layer_tensor": {"achieved_tflops": layer_flops / (ms_step / 1e3) / 1e12,
-                         "expert_flops": layer_flops, "peak": tpeak, "peak_source": tpeak_kind,
-                         "frac": layer_flops / (ms_step / 1e3) / 1e12 / tpeak},
+        "config": dict(config_block(spec, res), parallelism=f"replicas x{world}"),
+        "layer_hbm": layer_hbm, "layer_tensor": layer_tensor,
         "roofline": roof,
-        "kernels_ms_per_step": {kname: v[0] / args.steps for kname, v in per_kernel.items()
+        "kernels_ms_per_step": {kname: v[0] / args.steps for kname, v in res["per_kernel"].items()
                                 if v[1]},
-        "e2e": e2e,
-        "cuda_graph": graph,
-        "gpu_launches": gpu_launches,
-        "clocks": clk.summary(),
+        "e2e": res["e2e"],
+        "cuda_graph": res["graph"],
+        "gpu_launches": res["gpu_launches"],
+        "clocks": res["clocks"],
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_tok = min(T, os.cpu_count() or 1)
-        v, cores, reps, dt, n_exp = oracle_sample(spec, x, w_r, bias, wts, n_tok,
-                                                  args.cpu_seconds)
-        line["cpu_baseline"] = {
-            "value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {n_tok} of {T} tokens, full layer, {n_exp} experts, "
-                      f"{reps} repetitions in {dt:.1f} s",
-            "nproc": os.cpu_count(), "cpu_model": cpu_model()}
+    if res["cpu"] is not None and rank == 0:
+        line["cpu_baseline"] = res["cpu"]
+    extras = [c for c in (args.extra_configs.split(",") if args.extra_configs else [])
+              if c and c != "none" and c != args.config]
+    if extras:
+        line["configs"] = {}
+        for name in extras:
+            line["configs"][name] = summary_of(args, measure(args, synth.spec(name), dev, world,
+                                                             full=False))
     if rank == 0:
         print(json.dumps(line), flush=True)
 

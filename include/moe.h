@@ -82,6 +82,18 @@ typedef enum {
   MOE_BIAS_SELECT = 2 /* bias[e] added to the score for selection only */
 } moe_bias_mode;
 
+/* How moe_layer_forward returns the expert outputs to their tokens. */
+typedef enum {
+  MOE_COMBINE_DEFAULT = 0, /* the library's choice (MOE_COMBINE_FUSED) */
+  MOE_COMBINE_ORDERED = 1, /* the down projection writes one fp32 row per pick; a
+                              combine kernel adds each token's picks in slot order
+                              (deterministic: the same bits on every call) */
+  MOE_COMBINE_FUSED = 2    /* the down projection's epilogue adds w * y into the
+                              token's fp32 accumulator (atomic adds; the order of
+                              a token's picks, and so the last bits, can change
+                              from call to call) */
+} moe_combine_mode;
+
 typedef enum {
   MOE_W_BF16 = 0, /* bf16 weights and activations, fp32 accumulation */
   MOE_W8A8 = 1    /* int8 weights + per-output-channel fp32 scales; per-row int8 activations */
@@ -117,6 +129,7 @@ typedef struct {
                             tensor cores; MOE_W8A8: 8), < 0 = never GEMV.  Fixed
                             with the workspace size: W8A8 streaming needs int8 copies
                             of the sorted activations. */
+  int32_t combine;       /* moe_combine_mode; fixed with the workspace size */
 } moe_config;
 
 /* Human-readable name of a status. Never NULL. */
@@ -202,13 +215,19 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
  * no counterpart; this is a library convenience).  For callers that cannot
  * provide a workspace: a host framework that hands an operator only its input
  * and output buffers, or a decode loop that must not call cudaMalloc (it can
- * synchronise the device and take milliseconds).  Same arguments and results as
- * moe_route, minus the workspace.  Nothing is allocated: the router's partial
- * logits live in a 4 MiB array compiled into the library, present on every GPU
- * that loads it until the process exits.
+ * synchronise the device and take milliseconds).  Same arguments as moe_route,
+ * minus the workspace, and the same results for batches below 1024 tokens.
+ * Nothing is allocated: the router's logits live in a 4 MiB array compiled
+ * into the library, present on every GPU that loads it until the process exits.
+ *  - It always takes moe_route's small-batch router.  For T >= 1024 with H a
+ *    multiple of 64, where moe_route may switch to its large-batch router, the
+ *    two sum the same products in a different order: ids are equal unless two
+ *    keys are closer than the logits' rounding, weights agree to ~1e-5 relative.
  *  - Rejects, with MOE_ERR_WORKSPACE_TOO_SMALL, any (cfg, T) whose logits need
  *    more than 4 MiB: T x (E_r + E_z) x 4 bytes, times (1 + the router's split-K
- *    count) when it splits K; e.g. T = 64 with 768 experts needs 2.6 MB.
+ *    count) when the CUDA-core router runs and splits K (the tensor-core router,
+ *    taken where H is a multiple of 64 and the batch has enough tiles, needs no
+ *    partials); e.g. T = 64 with 768 experts needs 196 KB, T = E = 1024 4 MiB.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress); make that first call before any stream capture.
  *  - Every call on a device shares the array: calls whose work overlaps on the

@@ -38,6 +38,7 @@ MOE_ERR_DEVICE_TIMEOUT = 7
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 BIAS_NONE, BIAS_LOGIT, BIAS_SELECT = 0, 1, 2
 W_BF16, W8A8 = 0, 1
+COMBINE_DEFAULT, COMBINE_ORDERED, COMBINE_FUSED = 0, 1, 2
 
 KERNELS = ["router", "topk", "perm_count", "perm_scan", "perm_scatter", "perm_gather",
            "worklist", "gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down", "quant_h", "combine",
@@ -51,7 +52,7 @@ class MoeConfig(ctypes.Structure):
         "hidden", "inter", "n_routed", "n_zero", "top_k", "n_group", "topk_group", "per_group_k",
         "score", "renormalize")] + [("routed_scale", ctypes.c_float)] + [
         (n, ctypes.c_int32) for n in (
-            "bias_mode", "shared_inter", "wdtype", "out_fp32", "gemv_max_rows")]
+            "bias_mode", "shared_inter", "wdtype", "out_fp32", "gemv_max_rows", "combine")]
 
 
 class MoeError(RuntimeError):
@@ -116,7 +117,8 @@ def _check(status, what):
         raise MoeError(status, what)
 
 
-def config_from_spec(spec: dict, out_fp32: bool = False, gemv_max_rows: int = 0) -> MoeConfig:
+def config_from_spec(spec: dict, out_fp32: bool = False, gemv_max_rows: int = 0,
+                     combine: int = COMBINE_DEFAULT) -> MoeConfig:
     """MoeConfig from a layer description dict (the keys used by the input generator)."""
     return MoeConfig(
         hidden=spec["hidden"], inter=spec["inter"], n_routed=spec["n_routed"],
@@ -129,7 +131,7 @@ def config_from_spec(spec: dict, out_fp32: bool = False, gemv_max_rows: int = 0)
             spec.get("bias_mode", "none")],
         shared_inter=spec.get("shared_inter", 0),
         wdtype=W8A8 if spec.get("wdtype", "bf16") == "w8a8" else W_BF16,
-        out_fp32=int(bool(out_fp32)), gemv_max_rows=int(gemv_max_rows))
+        out_fp32=int(bool(out_fp32)), gemv_max_rows=int(gemv_max_rows), combine=int(combine))
 
 
 def moe_workspace_size(cfg: MoeConfig, T: int) -> int:

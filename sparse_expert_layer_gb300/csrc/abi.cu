@@ -19,7 +19,6 @@ namespace {
 constexpr int kMaxExperts = 4096;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxGroups = 64;
-constexpr int kRouterTargetCtas = 304;  // router split-K sized for ~2 CTAs per SM
 constexpr int kMaxDevices = 64;
 
 // ------------------------------------------------------------ bookkeeping --
@@ -108,6 +107,8 @@ moe_status check_cfg(const moe_config* c, int32_t T) {
     if (c->shared_inter > 0) return MOE_ERR_UNSUPPORTED;
   }
   if (c->out_fp32 != 0 && c->out_fp32 != 1) return MOE_ERR_INVALID_ARG;
+  if (c->combine < MOE_COMBINE_DEFAULT || c->combine > MOE_COMBINE_FUSED)
+    return MOE_ERR_INVALID_ARG;
   // work-list chunk indices are 16-bit: at most 65535 chunks of 128 rows per unit
   if ((long long)T * c->top_k > (1LL << 30) || T > 65535 * kTcMaxN) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -120,6 +121,34 @@ int effective_gemv_max(const moe_config& c) {
   if (c.gemv_max_rows < 0) return 0;
   return c.wdtype == MOE_W8A8 ? kDefaultGemvMaxRowsW8 : kDefaultGemvMaxRows;
 }
+// Whether moe_layer_forward adds the expert outputs into the tokens' fp32
+// accumulators in the down projection's epilogue (the library default) instead
+// of writing per-pick rows for the ordered combine kernel.  A W8A8 layer without
+// FFN experts has no quantising gather to start the accumulators, so it takes
+// the ordered combine.
+bool fused_combine(const moe_config& c) {
+  if (c.combine == MOE_COMBINE_ORDERED) return false;
+  if (c.wdtype == MOE_W8A8 && c.n_routed == 0) return false;
+  return true;
+}
+
+// Whether the bf16 grouped FFN runs its tensor-core gate/up and down passes as
+// one persistent launch (down tiles wait for their task's gate/up tiles, which
+// fills the gate/up pass's last partial wave) instead of two.  MOE_FFN_ONE_LAUNCH
+// =0 or =1 in the environment (read once) overrides the choice.
+bool ffn_one_launch(const moe_config& c, int T) {
+  static const int env = [] {
+    const char* v = getenv("MOE_FFN_ONE_LAUNCH");
+    if (v && v[0] == '0' && v[1] == 0) return 0;
+    if (v && v[0] == '1' && v[1] == 0) return 1;
+    return -1;
+  }();
+  (void)T;
+  (void)c;
+  if (env >= 0) return env == 1;
+  return false;
+}
+
 // The GEMV launches are skipped when no unit can take that path.
 bool gemv_possible(int gemv_max) { return gemv_max > 0; }
 
@@ -138,7 +167,9 @@ struct Layout {
   size_t rsplit, rtasks, rstart, rcounts;
   bool tc_router;
   size_t wl_gemv_tasks, wl_gemv_gu, wl_gemv_dn, wl_tc_tasks, wl_tc_gu, wl_tc_dn, wl_counts;
+  size_t wl_gu_done;  // single-launch FFN: per task count of stored gate/up tiles
   size_t x_perm, x_scale, h, y, h_s, y_s;
+  size_t acc;  // fused combine with bf16 output: the tokens' fp32 accumulators
   // W8A8 only: integer-valued fp16 copies of the codes, row norms, fp32 h and
   // its codes/scales, and the guard-failure lists of the two passes
   size_t x16, xn2, h32, hq16, hsc, hn2, redo_gu, redo_dn;
@@ -153,7 +184,7 @@ Layout make_layout(const moe_config& c, int T) {
   const size_t E = (size_t)c.n_routed + c.n_zero;
   const size_t R = (size_t)T * c.top_k;
   const size_t H = c.hidden, I = c.inter, Is = c.shared_inter;
-  L.splits = router_splits(c, T, kRouterTargetCtas / 2);
+  L.splits = router_splits_default(c, T);
   L.nblk = (T + kPermTokens - 1) / kPermTokens;
   L.wl_cap = c.n_routed + 4 + (int)(R + T);  // one-row tasks at worst
   const size_t xb = c.wdtype == MOE_W8A8 ? 1 : 2;
@@ -189,15 +220,21 @@ Layout make_layout(const moe_config& c, int T) {
   L.wl_tc_gu = take((size_t)L.wl_cap * 4);
   L.wl_tc_dn = take((size_t)L.wl_cap * 4);
   L.wl_counts = take(kWlCount * 4);
+  L.wl_gu_done = take((size_t)L.wl_cap * 4);
   // W8A8 layers quantise straight into x16 and keep h in fp32 (h32), so the
   // int8 x_perm and the bf16 h are bf16-path buffers only
   const bool w8 = c.wdtype == MOE_W8A8;
   L.x_perm = take(w8 ? 0 : R * H * xb);
   L.x_scale = take(R * 4);
   L.h = take(w8 ? 0 : R * I * 2);
-  L.y = take(R * H * 4);
+  // the ordered combine reads per-pick rows (and the shared expert's output);
+  // the fused one adds into per-token accumulators (the caller's fp32 output, or
+  // this buffer ahead of the bf16 rounding)
+  const bool fused = fused_combine(c);
+  L.y = take(fused ? 0 : R * H * 4);
   L.h_s = take((size_t)T * Is * 2);
-  L.y_s = take(Is > 0 ? (size_t)T * H * 4 : 0);
+  L.y_s = take(Is > 0 && !fused ? (size_t)T * H * 4 : 0);
+  L.acc = take(fused && !c.out_fp32 ? (size_t)T * H * 4 : 0);
   if (c.wdtype == MOE_W8A8) {
     const size_t tc_tasks = c.n_routed + 4 + R / kTcMaxN;
     // one entry per CTA half of each two-SM tile of 256 channels
@@ -236,6 +273,7 @@ WorkList worklist_view(void* ws, const Layout& L) {
   wl.capacity = L.wl_cap;
   wl.redo_gu = L.redo_cap > 0 ? at<int32_t>(ws, L.redo_gu) : nullptr;
   wl.redo_dn = L.redo_cap > 0 ? at<int32_t>(ws, L.redo_dn) : nullptr;
+  wl.gu_done = at<int32_t>(ws, L.wl_gu_done);
   return wl;
 }
 
@@ -302,7 +340,8 @@ WlPlan wl_plan(const moe_config& c, bool shared_weights) {
 // sort; returns whether the work list was built.
 bool run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
                  const int32_t* ids, const void* x, int32_t* counts, int32_t* offsets,
-                 int32_t* s2e, int32_t* e2s, void* x_perm, float* x_scale, const WlPlan* plan) {
+                 int32_t* s2e, int32_t* e2s, void* x_perm, float* x_scale, const WlPlan* plan,
+                 const float* w = nullptr, float* acc = nullptr) {
   const int E = c.n_routed + c.n_zero;
   bool built = false;
   if (sort_small_fits(T, E)) {
@@ -317,7 +356,7 @@ bool run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, 
     launch_perm_scan(ln, T, E, bc, counts, offsets);
     launch_perm_scatter(ln, T, c.top_k, E, ids, bc, s2e, e2s);
   }
-  if (x_perm) launch_perm_gather(ln, c, T, ids, e2s, x, x_perm, x_scale);
+  if (x_perm) launch_perm_gather(ln, c, T, ids, e2s, x, x_perm, x_scale, w, acc);
   return built;
 }
 
@@ -326,7 +365,7 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
                    const int32_t* offsets, const void* x_perm, const void* w_gate,
                    const void* w_up, const void* w_down, float* y_perm, const void* x,
                    const void* sg, const void* su, const void* sd, float* y_shared,
-                   bool wl_built) {
+                   bool wl_built, const ScatterAdd& sc = ScatterAdd{}) {
   const WorkList wl = worklist_view(ws, L);
   const bool shared = c.shared_inter > 0 && sg != nullptr;
   const WlPlan plan = wl_plan(c, shared);
@@ -378,7 +417,8 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   tg.K = tg.Ks = c.hidden;
   tg.N = c.inter;
   tg.Ns = c.shared_inter;
-  if (c.n_routed > 0 && !launch_tc_gate_up(ln, tg)) return MOE_ERR_CUDA;
+  const bool one_launch = ffn_one_launch(c, T);
+  if (c.n_routed > 0 && !one_launch && !launch_tc_gate_up(ln, tg)) return MOE_ERR_CUDA;
 
   GemvPass dn{};
   dn.tasks = wl.gemv_tasks;
@@ -396,6 +436,7 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   dn.Ks = c.shared_inter;
   dn.N = dn.Ns = c.hidden;
   dn.max_rows = chunk;
+  dn.sc = sc;
   if (gemv_possible(gemv_max)) launch_gemv_down(ln, dn);
 
   TcPass td{};
@@ -417,7 +458,11 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   td.K = c.inter;
   td.Ks = c.shared_inter;
   td.N = td.Ns = c.hidden;
-  if (c.n_routed > 0 && !launch_tc_down(ln, td)) return MOE_ERR_CUDA;
+  td.sc = sc;
+  if (c.n_routed > 0) {
+    const bool ok = one_launch ? launch_tc_ffn(ln, tg, td, wl.gu_done) : launch_tc_down(ln, td);
+    if (!ok) return MOE_ERR_CUDA;
+  }
   return MOE_OK;
 }
 
@@ -430,7 +475,7 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
                         const int32_t* offsets, const void* x_perm, const float* x_scale,
                         const void* w_gate, const void* w_up, const void* w_down,
                         const float* s_gate, const float* s_up, const float* s_down,
-                        float* y_perm, bool wl_built) {
+                        float* y_perm, bool wl_built, const ScatterAdd& sc = ScatterAdd{}) {
   const WorkList wl = worklist_view(ws, L);
   const WlPlan plan = wl_plan(c, false);
   const int gemv_max = plan.gemv_max;
@@ -508,6 +553,7 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   vd.out_f32 = y_perm;
   vd.K = c.inter;
   vd.N = c.hidden;
+  vd.sc = sc;
   if (gemv && !launch_gemv_i8_down(ln, vd)) return MOE_ERR_CUDA;
 
   W8Pass d = g;
@@ -526,6 +572,7 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   d.redo = wl.redo_dn;
   d.K = c.inter;
   d.N = c.hidden;
+  d.sc = sc;
   if (!launch_w8a8(ln, d)) return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -743,8 +790,18 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
   int32_t* e2s = at<int32_t>(ws, L.e2s);
   void* x_perm = w8 ? nullptr : at<void>(ws, L.x_perm);
   float* x_scale = at<float>(ws, L.x_scale);
-  float* y = at<float>(ws, L.y);
-  float* y_s = c.shared_inter > 0 ? at<float>(ws, L.y_s) : nullptr;
+  const bool fused = fused_combine(c);
+  float* y = fused ? nullptr : at<float>(ws, L.y);
+  float* y_s = c.shared_inter > 0 && !fused ? at<float>(ws, L.y_s) : nullptr;
+  // fused combine: the tokens' fp32 accumulators (the output itself when fp32)
+  float* acc = !fused ? nullptr : c.out_fp32 ? static_cast<float*>(out) : at<float>(ws, L.acc);
+  ScatterAdd sc{};
+  if (fused) {
+    sc.acc = acc;
+    sc.s2e = s2e;
+    sc.w = w;
+    sc.k = c.top_k;
+  }
   const moe_status rs = run_route(ln, c, T, L, ws, x, w_router, bias, ids, w);
   if (rs != MOE_OK) {
     finish();
@@ -755,19 +812,22 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
   const WlPlan plan = wl_plan(c, !w8 && c.shared_inter > 0);
   const bool wl_built =
       run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale,
-                  ffn ? &plan : nullptr);
+                  ffn ? &plan : nullptr, w, acc);
   if (w8 && c.n_routed > 0)
     launch_quant_gather(ln, c, T, x, ids, e2s, offsets, plan.gemv_max, at<uint16_t>(ws, L.x16),
                         gemv_possible(plan.gemv_max) ? at<int8_t>(ws, L.x8) : nullptr, x_scale,
-                        at<int32_t>(ws, L.xn2));
+                        at<int32_t>(ws, L.xn2), w, acc);
   moe_status fs = MOE_OK;
   if (w8 && c.n_routed > 0)
     fs = run_ffn_w8a8(ln, c, T, L, ws, offsets, x_perm, x_scale, w_gate, w_up, w_down, s_gate,
-                      s_up, s_down, y, wl_built);
+                      s_up, s_down, y, wl_built, sc);
   else if (!w8 && (c.n_routed > 0 || c.shared_inter > 0))
     fs = run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y, x, ws_gate, ws_up,
-                 ws_down, y_s, wl_built);
-  launch_combine(ln, c, T, y, e2s, ids, w, x, y_s, out);
+                 ws_down, y_s, wl_built, sc);
+  if (!fused)
+    launch_combine(ln, c, T, y, e2s, ids, w, x, y_s, out);
+  else if (!c.out_fp32)
+    launch_finalize(ln, T, c.hidden, acc, out);
   const moe_status f = finish();
   return fs != MOE_OK ? fs : f;
 }
@@ -846,6 +906,7 @@ moe_status moe_qgemm_s8(int32_t n_experts, int32_t K, int32_t N, int32_t R, cons
   wl.capacity = Q.cap;
   wl.redo_gu = nullptr;
   wl.redo_dn = at<int32_t>(ws, Q.redo);
+  wl.gu_done = nullptr;
   // Tasks: the experts' row ranges in <= 256-row chunks, N/256 two-SM tiles
   // each (the work-list kernel's W8A8 "down" tiling, hidden = N).
   moe_config c{};

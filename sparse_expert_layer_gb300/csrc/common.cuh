@@ -146,6 +146,7 @@ __device__ __forceinline__ bool warp_flag(const volatile int* f) {
 constexpr int kTileQueue = 4;
 struct QTile {
   int tile, row0, n, ct, e, shared;
+  int task, gu;  // single-launch FFN: the tile's task and pass (1: gate/up, 0: down)
 };
 __device__ __forceinline__ bool tq_push(QTile* q, uint64_t* full, uint64_t* empty, uint32_t n,
                                         const QTile& v) {
@@ -170,12 +171,43 @@ __device__ __forceinline__ bool tq_pop(const QTile* q, uint64_t* full, uint64_t*
     v->ct = p->ct;
     v->e = p->e;
     v->shared = p->shared;
+    v->task = p->task;
+    v->gu = p->gu;
   } else {
     v->tile = -1;
   }
   if (warp_level) __syncwarp();
   if (ok && (!warp_level || (threadIdx.x % 32) == 0)) mbar_arrive(smem_u32(&empty[s]));
   return ok;
+}
+
+// ------------------------------------------------ cross-CTA dependencies ----
+// A tile that reads rows another CTA writes with ordinary stores (the gate/up
+// epilogue's h rows, read by TMA in the down pass of the single-launch FFN):
+// the writer's lanes store, the warp synchronises, and one lane makes the
+// stores visible at GPU scope before counting them; the reader waits for the
+// count with acquire loads, then orders the async proxy (TMA) after them.
+__device__ __forceinline__ void signal_rows_done(int* counter) {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+  atomicAdd(counter, 1);
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Waits until *counter >= target, for at most kWaitCycles.  false = gave up.
+__device__ __forceinline__ bool wait_rows_done(const int* counter, int target) {
+  if (ld_acquire_gpu(counter) < target) {
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(counter) < target) {
+      if (clock64() - t0 > kWaitCycles) return false;
+      __nanosleep(64);
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
 }
 
 // ------------------------------------------------------------ bulk copies ---

@@ -40,13 +40,18 @@ constexpr int kBTileBytes = kTcMaxN * kBK * 2;   // 16 KB
 constexpr int kBoxRows = 64;
 constexpr int kBoxBytes = kBoxRows * kBK * 2;    // 8 KB
 
-template <bool GU>
+// Pass of a launch: the down projection, the gate/up projection with SwiGLU,
+// or both in one launch (every gate/up tile, then every down tile; a down tile
+// starts once its task's gate/up tiles have stored their h rows).
+enum { kTcDown = 0, kTcGateUp = 1, kTcFfn = 2 };
+
+template <int MODE>
 struct Geom {
-  static constexpr int kNA = GU ? 2 : 1;
+  static constexpr int kNA = MODE == kTcDown ? 1 : 2;  // weight tiles a stage can hold
   static constexpr int kStageBytes = kNA * kATileBytes + kBTileBytes;
-  static constexpr int kStages = GU ? 4 : 6;
-  static constexpr int kTmemCols = GU ? 512 : 256;
-  static constexpr int kAccStride = GU ? 256 : 128;  // TMEM columns per accumulator buffer
+  static constexpr int kStages = MODE == kTcDown ? 6 : 4;
+  static constexpr int kTmemCols = MODE == kTcDown ? 256 : 512;
+  static constexpr int kAccStride = MODE == kTcDown ? 128 : 256;  // columns per accumulator buffer
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
 };
@@ -58,6 +63,11 @@ struct TcMaps {
   CUtensorMap sa1;
   CUtensorMap b;    // routed activation rows
   CUtensorMap sb;   // shared expert activation rows
+  // single-launch FFN only: the down pass's weights and activation (h) rows
+  CUtensorMap d0;
+  CUtensorMap sd0;
+  CUtensorMap h;
+  CUtensorMap sh;
 };
 
 struct TcArgs {
@@ -69,34 +79,46 @@ struct TcArgs {
   float* out_y;
   uint16_t* sout_h;
   float* sout_y;
-  int K, Ks, N, Ns;
+  int K, Ks, N, Ns;  // of the pass (single-launch FFN: of its gate/up pass)
   int b_kmod;  // > 0: routed activation K coordinate modulo b_kmod (router tiles)
   int* sched;  // dynamic tile counter, zero at launch
   DevStatus* status;
+  ScatterAdd sc;  // down pass: add w * y into the tokens' accumulators
+  // single-launch FFN: the down tiles (numbered after the gate/up tiles), and
+  // the per-task count of gate/up epilogue warps done (4 per channel tile)
+  const int32_t* tile_start_dn;
+  int tile_slot_dn;
+  int* gu_done;
+  int gu_tiles, gu_tiles_shared;  // gate/up channel tiles of a routed / shared task
 };
 
-__device__ __forceinline__ QTile decode_tile(const TcArgs& a, int tile, int ntasks) {
+__device__ __forceinline__ QTile decode_tile(const TcArgs& a, int tile, int ntasks, int gu,
+                                             const int32_t* start) {
   QTile t;
   int task;
-  tc_tile_of(a.tasks, a.tile_start, ntasks, tile, &task, &t.ct);
+  tc_tile_of(a.tasks, start, ntasks, tile, &task, &t.ct);
   const FfnTask tk = a.tasks[task];
   t.tile = tile;
   t.row0 = tk.row0;
   t.n = tk.nrows;
   t.shared = tk.expert < 0;
   t.e = t.shared ? 0 : tk.expert;
+  t.task = task;
+  t.gu = gu;
   return t;
 }
 
-template <bool GU>
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   pdl_wait();
-  using G = Geom<GU>;
+  using G = Geom<MODE>;
+  constexpr bool FFN = MODE == kTcFfn;
   extern __shared__ uint8_t smem_raw[];
-  const int kind = GU ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
+  const int kind = MODE == kTcDown ? MOE_K_TC_DOWN : MOE_K_TC_GATE_UP;
   const int ntasks = a.counts[a.task_slot];
-  const int ntiles = a.counts[a.tile_slot];
+  const int ntiles_first = a.counts[a.tile_slot];
+  const int ntiles = ntiles_first + (FFN ? a.counts[a.tile_slot_dn] : 0);
   if (ntiles <= 0 || (int)blockIdx.x >= ntiles) return;  // uniform across the CTA
 
   // 1024-byte aligned ring (128-byte swizzle atoms), barriers after it
@@ -134,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&maps.a0);
     prefetch_tensormap(&maps.b);
-    if (GU) prefetch_tensormap(&maps.a1);
+    if (MODE != kTcDown) prefetch_tensormap(&maps.a1);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), G::kTmemCols);
   tc_fence_before();
@@ -151,7 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       t.tile = -1;
       if (!*abort_flag) {
         const int tile = atomicAdd(a.sched, 1);
-        if (tile < ntiles) t = decode_tile(a, tile, ntasks);
+        if (tile < ntiles_first)
+          t = decode_tile(a, tile, ntasks, MODE != kTcDown, a.tile_start);
+        else if (tile < ntiles)
+          t = decode_tile(a, tile - ntiles_first, ntasks, 0, a.tile_start_dn);
       }
       if (!tq_push(tq, tq_full, tq_empty, n, t)) {
         raise_status(a.status, kStTimeout, kind);
@@ -176,12 +201,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (t.tile < 0) break;
-      const CUtensorMap* A0 = t.shared ? &maps.sa0 : &maps.a0;
+      const bool gu = t.gu != 0;
+      const CUtensorMap* A0;
       const CUtensorMap* A1 = t.shared ? &maps.sa1 : &maps.a1;
-      const CUtensorMap* B = t.shared ? &maps.sb : &maps.b;
+      const CUtensorMap* B;
+      int K;
+      if (FFN && !gu) {
+        // the task's h rows are complete once all its gate/up tiles are stored
+        const int target = 4 * (t.shared ? a.gu_tiles_shared : a.gu_tiles);
+        if (!wait_rows_done(a.gu_done + t.task, target)) {
+          raise_status(a.status, kStTimeout, kind);
+          *abort_flag = 1;
+          break;
+        }
+        A0 = t.shared ? &maps.sd0 : &maps.d0;
+        B = t.shared ? &maps.sh : &maps.h;
+        K = t.shared ? a.Ns : a.N;  // the down pass reduces over the intermediate size
+      } else {
+        A0 = t.shared ? &maps.sa0 : &maps.a0;
+        B = t.shared ? &maps.sb : &maps.b;
+        K = t.shared ? a.Ks : a.K;
+      }
       const int nb = (t.n + kBoxRows - 1) / kBoxRows;
-      const uint32_t bytes = (uint32_t)(G::kNA * kATileBytes + nb * kBoxBytes);
-      const int nks = ((t.shared ? a.Ks : a.K) + kBK - 1) / kBK;
+      const uint32_t bytes = (uint32_t)((gu ? 2 : 1) * kATileBytes + nb * kBoxBytes);
+      const int nks = (K + kBK - 1) / kBK;
       for (int ks = 0; ks < nks; ++ks) {
         if (*abort_flag) {
           ok = false;
@@ -199,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(bar, bytes);
         uint8_t* st = smem + (size_t)stage * G::kStageBytes;
         tma_load_3d(smem_u32(st), A0, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
-        if (GU) tma_load_3d(smem_u32(st + kATileBytes), A1, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
+        if (gu) tma_load_3d(smem_u32(st + kATileBytes), A1, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
         uint8_t* sb = st + G::kNA * kATileBytes;
         const int bk = (!t.shared && a.b_kmod > 0) ? (ks * kBK) % a.b_kmod : ks * kBK;
         for (int j = 0; j < nb; ++j)
@@ -222,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (t.tile < 0) break;
+      const bool gu = t.gu != 0;
       const uint32_t buf = local & 1u, use = local >> 1;
       if (!mbar_wait(smem_u32(&acc_empty[buf]), (use & 1u) ^ 1u)) {
         raise_status(a.status, kStTimeout, kind);
@@ -233,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16_f32(kTcM, nmma);
       const uint32_t d0 = tmem + buf * G::kAccStride;
       const uint32_t d1 = d0 + kTcMaxN;
-      const int nks = ((t.shared ? a.Ks : a.K) + kBK - 1) / kBK;
+      const int K = (FFN && !gu) ? (t.shared ? a.Ns : a.N) : (t.shared ? a.Ks : a.K);
+      const int nks = (K + kBK - 1) / kBK;
       for (int ks = 0; ks < nks; ++ks) {
         if (*abort_flag) {
           ok = false;
@@ -255,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = sdesc_sw128(sb + k * 32);
           const uint32_t acc = (ks > 0 || k > 0) ? 1u : 0u;
           tc_mma_bf16(d0, sdesc_sw128(sa + k * 32), bdesc, idesc, acc);
-          if (GU) tc_mma_bf16(d1, sdesc_sw128(sa + kATileBytes + k * 32), bdesc, idesc, acc);
+          if (gu) tc_mma_bf16(d1, sdesc_sw128(sa + kATileBytes + k * 32), bdesc, idesc, acc);
         }
         tc_commit(smem_u32(&empty[stage]));
         ++iter;
@@ -279,7 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (t.tile < 0 || warp_flag(abort_flag)) break;
-      const int tN = t.shared ? a.Ns : a.N;
+      const bool gu = t.gu != 0;
+      // output channels of this tile's pass: gate/up -> N (I or I_s); down -> H
+      const int tN = (FFN && !gu) ? a.K : (t.shared ? a.Ns : a.N);
       const uint32_t buf = local & 1u, use = local >> 1;
       if (!warp_wait(smem_u32(&acc_full[buf]), use & 1u)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
@@ -289,19 +336,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int ch = t.ct * kTcM + q * 32 + lane;
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * G::kAccStride;
+      const bool fused = !gu && a.sc.acc != nullptr;
       for (int j0 = 0; j0 < t.n; j0 += 16) {
+        // fused combine: lane i < 16 looks up token j0 + i's target row and
+        // routing weight while the accumulators are loaded
+        int tk_l = 0;
+        float wt_l = 0.f;
+        if (fused && lane < 16 && j0 + lane < t.n)
+          scatter_target(a.sc, t.row0 + j0 + lane, t.shared, &tk_l, &wt_l);
         uint32_t g[16], u[16];
         tmem_ld16(trow + j0, g);
-        if (GU) tmem_ld16(trow + kTcMaxN + j0, u);
+        if (gu) tmem_ld16(trow + kTcMaxN + j0, u);
         tmem_ld_wait();
-        if (ch < tN) {
+        if (fused) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int tk = __shfl_sync(0xffffffffu, tk_l, i);
+            const float wt = __shfl_sync(0xffffffffu, wt_l, i);
+            if (ch < tN && j0 + i < t.n)
+              atomicAdd(a.sc.acc + (size_t)tk * tN + ch, wt * __uint_as_float(g[i]));
+          }
+        } else if (ch < tN) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int tok = j0 + i;
             if (tok < t.n) {
               const size_t o = (size_t)(t.row0 + tok) * tN + ch;
               const float gv = __uint_as_float(g[i]);
-              if (GU) {
+              if (gu) {
                 const float h = gv * __frcp_rn(1.f + __expf(-gv)) * __uint_as_float(u[i]);
                 (t.shared ? a.sout_h : a.out_h)[o] = f_to_bf16(h);
               } else {
@@ -313,7 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[buf]));
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&acc_empty[buf]));
+        // single-launch FFN: this warp's h rows of the tile are stored
+        if (FFN && gu) signal_rows_done(a.gu_done + t.task);
+      }
     }
   }
 
@@ -376,23 +442,8 @@ __global__ void router_tasks_kernel(FfnTask* tasks, int32_t* start, int32_t* cou
   }
 }
 
-template <bool GU>
-bool launch_tc(const Launch& L, const TcPass& p, int kind) {
-  using G = Geom<GU>;
-  TcMaps maps;
-  memset(&maps, 0, sizeof maps);
-  const uint64_t Kr = p.K, Nr = p.N;
-  const uint64_t Kb = p.b_kmod > 0 ? (uint64_t)p.b_kmod : Kr;  // activation row length
-  bool ok = make_map(&maps.a0, p.w0, Kr, Nr, p.n_experts, kTcM) &&
-            make_map(&maps.b, p.act, Kb, p.act_rows, 1, kBoxRows);
-  if (GU) ok = ok && make_map(&maps.a1, p.w1, Kr, Nr, p.n_experts, kTcM);
-  if (p.sw0) {
-    ok = ok && make_map(&maps.sa0, p.sw0, p.Ks, p.Ns, 1, kTcM) &&
-         make_map(&maps.sb, p.sact, p.Ks, p.sact_rows, 1, kBoxRows);
-    if (GU) ok = ok && make_map(&maps.sa1, p.sw1, p.Ks, p.Ns, 1, kTcM);
-  }
-  if (!ok) return false;
-  TcArgs a;
+TcArgs make_args(const Launch& L, const TcPass& p) {
+  TcArgs a{};
   a.tasks = p.tasks;
   a.tile_start = p.tile_start;
   a.counts = p.counts;
@@ -409,10 +460,39 @@ bool launch_tc(const Launch& L, const TcPass& p, int kind) {
   a.b_kmod = p.b_kmod;
   a.sched = const_cast<int32_t*>(p.counts) + p.sched_slot;
   a.status = L.status;
-  set_smem_attr_once(reinterpret_cast<const void*>(tc_kernel<GU>), G::kSmemBytes,
-                     GU ? kAttrTcGU : kAttrTcDN);
+  a.sc = p.sc;
+  return a;
+}
+
+// Tensor maps of one pass's weights and activation rows (routed, then shared).
+bool pass_maps(const TcPass& p, bool gu, CUtensorMap* w0, CUtensorMap* w1, CUtensorMap* act,
+               CUtensorMap* sw0, CUtensorMap* sw1, CUtensorMap* sact) {
+  const uint64_t Kr = p.K, Nr = p.N;
+  const uint64_t Kb = p.b_kmod > 0 ? (uint64_t)p.b_kmod : Kr;  // activation row length
+  bool ok = make_map(w0, p.w0, Kr, Nr, p.n_experts, kTcM) &&
+            make_map(act, p.act, Kb, p.act_rows, 1, kBoxRows);
+  if (gu) ok = ok && make_map(w1, p.w1, Kr, Nr, p.n_experts, kTcM);
+  if (p.sw0) {
+    ok = ok && make_map(sw0, p.sw0, p.Ks, p.Ns, 1, kTcM) &&
+         make_map(sact, p.sact, p.Ks, p.sact_rows, 1, kBoxRows);
+    if (gu) ok = ok && make_map(sw1, p.sw1, p.Ks, p.Ns, 1, kTcM);
+  }
+  return ok;
+}
+
+template <int MODE>
+bool launch_tc(const Launch& L, const TcPass& p, int kind) {
+  using G = Geom<MODE>;
+  TcMaps maps;
+  memset(&maps, 0, sizeof maps);
+  if (!pass_maps(p, MODE == kTcGateUp, &maps.a0, &maps.a1, &maps.b, &maps.sa0, &maps.sa1,
+                 &maps.sb))
+    return false;
+  const TcArgs a = make_args(L, p);
+  set_smem_attr_once(reinterpret_cast<const void*>(tc_kernel<MODE>), G::kSmemBytes,
+                     MODE == kTcGateUp ? kAttrTcGU : kAttrTcDN);
   launch_begin(L, kind);
-  launch_kernel(tc_kernel<GU>, L.num_sms, kThreads, G::kSmemBytes, L.stream, maps, a);
+  launch_kernel(tc_kernel<MODE>, L.num_sms, kThreads, G::kSmemBytes, L.stream, maps, a);
   launch_end(L, kind);
   return true;
 }
@@ -420,10 +500,34 @@ bool launch_tc(const Launch& L, const TcPass& p, int kind) {
 }  // namespace
 
 bool launch_tc_gate_up(const Launch& L, const TcPass& p) {
-  return launch_tc<true>(L, p, MOE_K_TC_GATE_UP);
+  return launch_tc<kTcGateUp>(L, p, MOE_K_TC_GATE_UP);
 }
 bool launch_tc_down(const Launch& L, const TcPass& p) {
-  return launch_tc<false>(L, p, MOE_K_TC_DOWN);
+  return launch_tc<kTcDown>(L, p, MOE_K_TC_DOWN);
+}
+
+bool launch_tc_ffn(const Launch& L, const TcPass& gu, const TcPass& dn, int32_t* gu_done) {
+  using G = Geom<kTcFfn>;
+  TcMaps maps;
+  memset(&maps, 0, sizeof maps);
+  CUtensorMap unused;
+  if (!pass_maps(gu, true, &maps.a0, &maps.a1, &maps.b, &maps.sa0, &maps.sa1, &maps.sb) ||
+      !pass_maps(dn, false, &maps.d0, &unused, &maps.h, &maps.sd0, &unused, &maps.sh))
+    return false;
+  TcArgs a = make_args(L, gu);
+  a.out_y = dn.out_y;
+  a.sout_y = dn.sout_y;
+  a.sc = dn.sc;
+  a.tile_start_dn = dn.tile_start;
+  a.tile_slot_dn = dn.tile_slot;
+  a.gu_done = gu_done;
+  a.gu_tiles = (gu.N + kTcM - 1) / kTcM;
+  a.gu_tiles_shared = (gu.Ns + kTcM - 1) / kTcM;
+  set_smem_attr_once(reinterpret_cast<const void*>(tc_kernel<kTcFfn>), G::kSmemBytes, kAttrTcFfn);
+  launch_begin(L, MOE_K_TC_GATE_UP);
+  launch_kernel(tc_kernel<kTcFfn>, L.num_sms, kThreads, G::kSmemBytes, L.stream, maps, a);
+  launch_end(L, MOE_K_TC_GATE_UP);
+  return true;
 }
 
 bool launch_tc_router(const Launch& L, const moe_config& c, int T, const void* x,
@@ -451,7 +555,7 @@ bool launch_tc_router(const Launch& L, const moe_config& c, int T, const void* x
   p.K = 3 * c.hidden;
   p.N = E;
   p.b_kmod = c.hidden;
-  return launch_tc<false>(L, p, MOE_K_ROUTER);
+  return launch_tc<kTcDown>(L, p, MOE_K_ROUTER);
 }
 
 }  // namespace moe

@@ -65,6 +65,7 @@ struct Item {
   uint16_t* out_h;
   float* out_y;
   int n, row0, N, c0, K;
+  bool shared;
 };
 
 template <bool GU>
@@ -83,6 +84,7 @@ __device__ __forceinline__ void decode_item(const GemvPass& p, const int32_t* st
   const bool shared = tk.expert < 0;
   it.n = tk.nrows;
   it.row0 = tk.row0;
+  it.shared = shared;
   it.N = shared ? p.Ns : p.N;
   it.K = shared ? p.Ks : p.K;
   it.c0 = block * (GU ? kGemvChGU : kGemvChDN);
@@ -168,6 +170,14 @@ __device__ bool consume_item(const GemvPass& p, const Item& it, uint8_t* smem, u
         if (GU) {
           const int c = it.c0 + cw;
           if (c < it.N) it.out_h[row + c] = f_to_bf16(g / (1.f + expf(-g)) * u);
+        } else if (p.sc.acc) {  // fused combine: add w * y into the token's row
+          int tk;
+          float wt;
+          scatter_target(p.sc, it.row0 + r, it.shared, &tk, &wt);
+          float* dst = p.sc.acc + (size_t)tk * it.N;
+          const int c = it.c0 + 2 * cw;
+          if (c < it.N) atomicAdd(dst + c, wt * g);
+          if (c + 1 < it.N) atomicAdd(dst + c + 1, wt * u);
         } else {
           const int c = it.c0 + 2 * cw;
           if (c < it.N) it.out_y[row + c] = g;

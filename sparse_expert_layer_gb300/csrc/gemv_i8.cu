@@ -107,6 +107,10 @@ __device__ bool consume_item(const GemvI8Pass& p, const Item& it, uint8_t* smem,
   // lane a < n holds row a's activation scale
   const int ch[2] = {it.c0 + r0, it.c0 + r0 + 8};
   const float sr_l = lane < n ? p.row_scale[it.row0 + lane] : 0.f;
+  // fused combine (down pass): lane a < n also holds row a's token and weight
+  int tk_l = 0;
+  float wt_l = 0.f;
+  if (!GU && p.sc.acc && lane < n) scatter_target(p.sc, it.row0 + lane, false, &tk_l, &wt_l);
   float sc[NA][2];
 #pragma unroll
   for (int m = 0; m < NA; ++m)
@@ -170,6 +174,8 @@ __device__ bool consume_item(const GemvI8Pass& p, const Item& it, uint8_t* smem,
 #pragma unroll
   for (int a = 0; a < NR; ++a) {
     const float sr = __shfl_sync(0xffffffffu, sr_l, a);
+    const int tk = __shfl_sync(0xffffffffu, tk_l, a);
+    const float wt = __shfl_sync(0xffffffffu, wt_l, a);
     if (a < n && part == 0) {
       const size_t o = (size_t)(it.row0 + a) * p.N;
 #pragma unroll
@@ -179,6 +185,8 @@ __device__ bool consume_item(const GemvI8Pass& p, const Item& it, uint8_t* smem,
         if (GU) {
           const float u = (float)acc[NA - 1][i][a] * sr * sc[NA - 1][i];
           p.out_f32[o + ch[i]] = __fdividef(g, 1.f + __expf(-g)) * u;
+        } else if (p.sc.acc) {
+          atomicAdd(p.sc.acc + (size_t)tk * p.N + ch[i], wt * g);
         } else {
           p.out_f32[o + ch[i]] = g;
         }

@@ -43,6 +43,29 @@ __device__ __forceinline__ void tc_tile_of(const FfnTask* tasks, const int32_t* 
   *ct = u / nt;
 }
 
+// The down projection's outputs added straight into the tokens' fp32
+// accumulators (the combine fused into the down epilogue; acc == nullptr:
+// store the y rows instead, for the ordered combine).  Sorted row p adds
+// w[r] * y to acc[r / k], r = s2e[p]; a row of the shared expert is the token
+// itself and adds y at weight 1.
+struct ScatterAdd {
+  float* acc;          // [T, H] fp32
+  const int32_t* s2e;  // sorted position -> expanded index t * k + j
+  const float* w;      // [T * k] routing weights
+  int k;
+};
+__device__ __forceinline__ void scatter_target(const ScatterAdd& s, int row, bool shared,
+                                               int* tok, float* wt) {
+  if (shared) {
+    *tok = row;
+    *wt = 1.f;
+  } else {
+    const int r = s.s2e[row];
+    *tok = r / s.k;
+    *wt = s.w[r];
+  }
+}
+
 // Slots of the device work-list counter array.
 enum {
   kWlGemvTasks = 0,
@@ -67,6 +90,7 @@ struct WorkList {
   int32_t capacity; // max tasks of each kind
   int32_t* redo_gu; // W8A8 guard-failure lists (count word zeroed here), or nullptr
   int32_t* redo_dn;
+  int32_t* gu_done; // single-launch FFN: per tensor-core task counter, zeroed here
 };
 
 // Geometry of the streaming (GEMV) path.
@@ -101,6 +125,15 @@ struct Launch {
 constexpr int kRouterCounterBytes = 3840;  // counters kept right after the status word
 int router_tiles(const moe_config& c, int T);
 int router_splits(const moe_config& c, int T, int num_sms);
+// The CUDA-core router's split-K count as every entry point sizes its scratch
+// (the split aims at about two CTAs on each of 152 SMs).
+int router_splits_default(const moe_config& c, int T);
+// Whether launch_router runs the decode router on tensor cores for (c, T): H a
+// multiple of 64, enough parallel work, and MOE_ROUTER_TC not set to 0.  That
+// router needs neither the split-K partials nor the tile counters.  (If its
+// tensor maps cannot be encoded, launch_router falls back to the CUDA-core
+// router with the split count it was given.)
+bool router_tc_decode_chosen(const moe_config& c, int T);
 void launch_router(const Launch& L, const moe_config& c, int T, const void* x, const float* w_r,
                    float* partial, int splits, float* logits, int* counters);
 void launch_topk(const Launch& L, const moe_config& c, int T, const float* logits,
@@ -118,7 +151,8 @@ void launch_perm_scan(const Launch& L, int T, int E, int32_t* bc, int32_t* count
 void launch_perm_scatter(const Launch& L, int T, int k, int E, const int32_t* ids,
                          const int32_t* bc, int32_t* s2e, int32_t* e2s);
 void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32_t* ids,
-                        const int32_t* e2s, const void* x, void* x_perm, float* x_perm_scale);
+                        const int32_t* e2s, const void* x, void* x_perm, float* x_perm_scale,
+                        const float* w = nullptr, float* acc = nullptr);
 void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
                      const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk);
 // Small batches (one CTA holds the [expert][token] pick bitmap): count, scan and
@@ -150,6 +184,7 @@ struct GemvPass {
   int K, Ks;              // reduction length, routed / shared
   int N, Ns;              // output channels, routed / shared
   int max_rows;           // rows per task (1, 2, 4 or 8); the work list chunks by it
+  ScatterAdd sc;          // down pass: acc != nullptr adds into the tokens' rows
 };
 void launch_gemv_gate_up(const Launch& L, const GemvPass& p);
 void launch_gemv_down(const Launch& L, const GemvPass& p);
@@ -172,6 +207,7 @@ struct GemvI8Pass {
   const float* row_scale;   // [rows]
   float* out_f32;           // gate/up: h [rows, N]; down: y [rows, N]
   int K, N;
+  ScatterAdd sc;            // down pass: acc != nullptr adds into the tokens' rows
 };
 bool launch_gemv_i8_gate_up(const Launch& L, const GemvI8Pass& p);
 bool launch_gemv_i8_down(const Launch& L, const GemvI8Pass& p);
@@ -198,9 +234,16 @@ struct TcPass {
   float* sout_y;
   int K, Ks, N, Ns;
   int b_kmod;              // > 0: activation K coordinate taken modulo b_kmod
+  ScatterAdd sc;           // down pass: acc != nullptr adds into the tokens' rows
 };
 bool launch_tc_gate_up(const Launch& L, const TcPass& p);
 bool launch_tc_down(const Launch& L, const TcPass& p);
+// Both passes in one persistent launch: every gate/up tile, then every down
+// tile; a down tile waits (bounded) until its task's gate/up tiles have stored
+// their h rows, counted in gu_done [tasks] (zeroed by the work-list kernel).
+// gu.tile_slot / dn.tile_slot count the tiles of each pass, gu.sched_slot is
+// the one claim counter.  Timed and counted as MOE_K_TC_GATE_UP.
+bool launch_tc_ffn(const Launch& L, const TcPass& gu, const TcPass& dn, int32_t* gu_done);
 // logits[T, E] = x[T, H] . [W3 | W2 | W1]^T on tensor cores (K = 3H, the token
 // rows read three times); tasks/start/counts are its own small work list.
 bool launch_tc_router(const Launch& L, const moe_config& c, int T, const void* x,
@@ -231,6 +274,7 @@ struct W8Pass {
   int32_t* redo;            // [0] count (zeroed by the work-list kernel), [1..cap]
   int redo_cap;
   int K, N;
+  ScatterAdd sc;            // down mode: acc != nullptr adds into the tokens' rows
 };
 bool launch_w8a8(const Launch& L, const W8Pass& p);
 void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, int32_t* norm2,
@@ -241,7 +285,8 @@ void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, in
 // row integer-valued fp16 codes in x16; x8 nullptr sends every row to x16.
 void launch_quant_gather(const Launch& L, const moe_config& c, int T, const void* x,
                          const int32_t* ids, const int32_t* e2s, const int32_t* offsets,
-                         int gemv_max, uint16_t* x16, int8_t* x8, float* scale, int32_t* norm2);
+                         int gemv_max, uint16_t* x16, int8_t* x8, float* scale, int32_t* norm2,
+                         const float* w = nullptr, float* acc = nullptr);
 // The first offsets[n_experts] of R fp32 rows -> codes, by the same rule: int8
 // into dst8 for rows of experts of at most gemv_max rows, else fp16 into dst;
 // dst8 nullptr sends every row to dst.
@@ -253,6 +298,37 @@ void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, int8_t*
 void launch_combine(const Launch& L, const moe_config& c, int T, const float* y_perm,
                     const int32_t* e2s, const int32_t* ids, const float* w, const void* x,
                     const float* shared_out, void* out);
+
+// Fused combine (combine.cu): the tokens' fp32 accumulators [T, H] rounded to
+// the bf16 output.  (Their zero-computation picks are added by the gather
+// kernels, which write every accumulator row first; the down passes add the
+// expert outputs.)
+void launch_finalize(const Launch& L, int T, int H, const float* acc, void* out);
+// Zero-computation picks of token t: acc[t] = sum over such slots j, in slot
+// order, of w[t, j] * x[t] (zero when there are none); elements 8i .. 8i + 7
+// of the row for i = first, first + stride, ... below H / 8.
+__device__ __forceinline__ void zero_pick_init(const int32_t* ids, const float* w, int t, int k,
+                                               int E_r, int E, const uint16_t* xrow, float* arow,
+                                               int H, int first, int stride) {
+  for (int i = first; i < H / 8; i += stride) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[(size_t)t * k + j];
+      if (e < E_r || e >= E) continue;
+      const float wj = w[(size_t)t * k + j];
+      const uint4 v = reinterpret_cast<const uint4*>(xrow)[i];
+      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc[2 * u] += wj * __uint_as_float(q[u] << 16);
+        acc[2 * u + 1] += wj * __uint_as_float(q[u] & 0xffff0000u);
+      }
+    }
+    float4* o = reinterpret_cast<float4*>(arow) + 2 * i;
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
 
 // Failure-path self-test (combine.cu): a bounded wait that is never satisfied.
 void launch_wait_timeout_selftest(const Launch& L, long long limit_cycles);
@@ -269,6 +345,7 @@ enum {
   kAttrRouter = kAttrGemvI8Base + 8,
   kAttrRouterTc,
   kAttrSortSmall,
+  kAttrTcFfn,
   kAttrSlots
 };
 void set_smem_attr_once(const void* func, int bytes, int slot);

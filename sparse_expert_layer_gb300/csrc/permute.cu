@@ -136,12 +136,26 @@ struct GatherArgs {
   const uint16_t* x;
   void* x_perm;
   float* scale;
-  int R, k, H, E_r, w8a8;
+  const float* w;  // fused combine: routing weights and the tokens' accumulators
+  float* acc;      // (nullptr: no accumulator rows to start)
+  int R, k, H, E_r, E, w8a8, gather_blocks;
 };
 
 __global__ void __launch_bounds__(256) perm_gather_kernel(GatherArgs a) {
   pdl_enter();
   const int lane = threadIdx.x % 32;
+  if ((int)blockIdx.x >= a.gather_blocks) {
+    // fused combine: the tokens' accumulator rows start with their
+    // zero-computation picks' w * x (the down pass adds the expert outputs);
+    // one thread per 8 elements
+    const int per_row = a.H / 8;
+    const long long idx = (long long)(blockIdx.x - a.gather_blocks) * blockDim.x + threadIdx.x;
+    const int t = (int)(idx / per_row);
+    if (t < a.R / a.k)
+      zero_pick_init(a.ids, a.w, t, a.k, a.E_r, a.E, a.x + (size_t)t * a.H,
+                     a.acc + (size_t)t * a.H, a.H, (int)(idx % per_row), per_row);
+    return;
+  }
   const int r = blockIdx.x * 8 + threadIdx.x / 32;
   if (r >= a.R) return;
   const int e = a.ids[r];
@@ -281,6 +295,7 @@ __device__ void build_worklist(const WlArgs& a, const int32_t* offsets, int* sh)
       a.wl.tc_tasks[ti] = tk;
       a.wl.tc_start_gu[ti] = pos[4] + j * ti_gu;
       a.wl.tc_start_dn[ti] = pos[5] + j * a.tiles_dn;
+      if (a.wl.gu_done) a.wl.gu_done[ti] = 0;
     }
   }
   if (threadIdx.x == 0) {
@@ -448,7 +463,8 @@ void launch_perm_scatter(const Launch& L, int T, int k, int E, const int32_t* id
 }
 
 void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32_t* ids,
-                        const int32_t* e2s, const void* x, void* x_perm, float* x_perm_scale) {
+                        const int32_t* e2s, const void* x, void* x_perm, float* x_perm_scale,
+                        const float* w, float* acc) {
   GatherArgs a;
   a.ids = ids;
   a.e2s = e2s;
@@ -459,9 +475,14 @@ void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32
   a.k = c.top_k;
   a.H = c.hidden;
   a.E_r = c.n_routed;
+  a.E = c.n_routed + c.n_zero;
   a.w8a8 = c.wdtype == MOE_W8A8;
+  a.w = w;
+  a.acc = acc;
+  a.gather_blocks = (a.R + 7) / 8;
+  const int init_blocks = acc ? (int)(((long long)T * (c.hidden / 8) + 255) / 256) : 0;
   launch_begin(L, MOE_K_PERM_GATHER);
-  launch_kernel(perm_gather_kernel, (a.R + 7) / 8, 256, 0, L.stream, a);
+  launch_kernel(perm_gather_kernel, a.gather_blocks + init_blocks, 256, 0, L.stream, a);
   launch_end(L, MOE_K_PERM_GATHER);
 }
 

@@ -489,7 +489,8 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
   uint64_t* x_full = reinterpret_cast<uint64_t*>(smem + kRcBarOff);  // [2]
   uint64_t* w_full = x_full + 2;                                      // [kRcWStages]
   uint64_t* mma_done = w_full + kRcWStages;                           // [2], per plane buffer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2);
+  uint64_t* drain = mma_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int e0 = blockIdx.x * kRcM, t0 = blockIdx.y * kRcN;
   const int rank = (int)cluster_rank();  // this CTA's H slice
@@ -505,6 +506,7 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
       mbar_init(smem_u32(&mma_done[b]), 1);
     }
     for (int s = 0; s < kRcWStages; ++s) mbar_init(smem_u32(&w_full[s]), 1);
+    mbar_init(smem_u32(drain), 1);
     fence_barrier_init();
     prefetch_tensormap(&xmap);
     prefetch_tensormap(&wmap);
@@ -516,38 +518,45 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
   const uint32_t tmem = *tmem_slot;
 
   const uint64_t pol_x = policy_evict_last(), pol_w = policy_evict_first();
+  int nw = 0, nx = 0;  // copies issued (thread 0)
   // chunk i of this CTA's slice (issued by thread 0); rows past E or T read as zero
   auto w_copy = [&](int i) {
     const uint32_t bar = smem_u32(&w_full[i % kRcWStages]);
     mbar_arrive_expect_tx(bar, (uint32_t)kRcWStage);
     tma_load_2d(smem_u32(smem + kRcWOff + (i % kRcWStages) * kRcWStage), &wmap, (c0 + i) * kRcK,
                 e0, bar, pol_w);
+    nw = i + 1;
   };
   auto x_copy = [&](int i) {
     const uint32_t bar = smem_u32(&x_full[i & 1]);
     mbar_arrive_expect_tx(bar, (uint32_t)kRcX);
     tma_load_3d(smem_u32(smem + kRcXOff + (i & 1) * kRcX), &xmap, (c0 + i) * kRcK, t0, 0, bar,
                 pol_x);
+    nx = i + 1;
   };
   if (tid == 0)
     for (int i = 0; i < kRcWStages - 1 && i < nch; ++i) w_copy(i);
   const uint32_t idesc = idesc_bf16_f32(kRcM, N);
+  // A wait that runs out makes its thread report the timeout; the block learns
+  // of it at the next barrier (uniformly, through __syncthreads_or) and stops:
+  // no further copies or MMAs are issued, the ones in flight are waited for,
+  // the logits are not written, and the cluster barriers and the TMEM release
+  // are still reached.  Thread 0 skips the MMAs of a chunk whose x it did not
+  // see arrive but still commits, so the others' waits on mma_done end.
+  bool fail = false, aborted = false;
+  int done = 0;  // chunks whose W and x were consumed (their copies landed)
   for (int i = 0; i < nch; ++i) {
     const int pbuf = i & 1;
-    // (a wait that runs out is reported; the pipeline keeps its order so that
-    // every thread reaches the same barriers)
     // plane buffer pbuf and x stage pbuf are free once chunk i - 2's MMAs are done
-    if (i >= 2 && !mbar_wait(smem_u32(&mma_done[pbuf]), (uint32_t)((i - 2) >> 1) & 1u) &&
-        lane == 0)
-      raise_status(st, kStTimeout, MOE_K_ROUTER);
-    if (tid == 0) {
+    if (i >= 2 && !mbar_wait(smem_u32(&mma_done[pbuf]), (uint32_t)((i - 2) >> 1) & 1u))
+      fail = true;
+    if (tid == 0 && !fail) {
       x_copy(i);
       // the W stage of chunk i - 1 was read before the last block barrier
       if (i + kRcWStages - 1 < nch) w_copy(i + kRcWStages - 1);
     }
-    if (!mbar_wait(smem_u32(&w_full[i % kRcWStages]), (uint32_t)(i / kRcWStages) & 1u) &&
-        lane == 0)
-      raise_status(st, kStTimeout, MOE_K_ROUTER);
+    if (!fail && !mbar_wait(smem_u32(&w_full[i % kRcWStages]), (uint32_t)(i / kRcWStages) & 1u))
+      fail = true;
     // split: a quarter warp takes one W row, eight 16-byte plane chunks of it
     const uint8_t* wst = smem + kRcWOff + (i % kRcWStages) * kRcWStage;
     uint8_t* planes = smem + pbuf * kRcPlanes;
@@ -568,28 +577,47 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
       *reinterpret_cast<uint4*>(planes + 2 * kRcPlane + off) = q1;
     }
     fence_proxy_async_smem();
-    __syncthreads();
+    if (__syncthreads_or(fail ? 1 : 0)) {
+      aborted = true;
+      break;
+    }
     if (tid == 0) {
-      if (!mbar_wait(smem_u32(&x_full[pbuf]), (uint32_t)(i >> 1) & 1u))
-        raise_status(st, kStTimeout, MOE_K_ROUTER);
-      tc_fence_after();
-      const uint32_t xb = smem_u32(smem + kRcXOff + pbuf * kRcX);
-      const uint32_t pb = smem_u32(planes);
+      if (mbar_wait(smem_u32(&x_full[pbuf]), (uint32_t)(i >> 1) & 1u)) {
+        tc_fence_after();
+        const uint32_t xb = smem_u32(smem + kRcXOff + pbuf * kRcX);
+        const uint32_t pb = smem_u32(planes);
 #pragma unroll
-      for (int kk = 0; kk < kRcK / 16; ++kk) {
-        const uint64_t bd = sdesc_sw128(xb + kk * 32);
-        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-        tc_mma_bf16(tmem, sdesc_sw128(pb + 0 * kRcPlane + kk * 32), bd, idesc, acc);  // W3
-        tc_mma_bf16(tmem, sdesc_sw128(pb + 1 * kRcPlane + kk * 32), bd, idesc, 1u);   // W2
-        tc_mma_bf16(tmem + kRcN, sdesc_sw128(pb + 2 * kRcPlane + kk * 32), bd, idesc, acc);  // W1
+        for (int kk = 0; kk < kRcK / 16; ++kk) {
+          const uint64_t bd = sdesc_sw128(xb + kk * 32);
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_bf16(tmem, sdesc_sw128(pb + 0 * kRcPlane + kk * 32), bd, idesc, acc);  // W3
+          tc_mma_bf16(tmem, sdesc_sw128(pb + 1 * kRcPlane + kk * 32), bd, idesc, 1u);   // W2
+          tc_mma_bf16(tmem + kRcN, sdesc_sw128(pb + 2 * kRcPlane + kk * 32), bd, idesc,
+                      acc);  // W1
+        }
+      } else {
+        fail = true;  // reported; the next barrier stops the block
       }
       tc_commit(smem_u32(&mma_done[pbuf]));
     }
+    done = i + 1;
   }
   // the last commit covers every MMA of the CTA
-  if (nch > 0 && !mbar_wait(smem_u32(&mma_done[(nch - 1) & 1]), (uint32_t)((nch - 1) >> 1) & 1u) &&
-      lane == 0)
+  if (!aborted && nch > 0 &&
+      !mbar_wait(smem_u32(&mma_done[(nch - 1) & 1]), (uint32_t)((nch - 1) >> 1) & 1u))
+    fail = true;
+  if (__syncthreads_or(fail ? 1 : 0)) aborted = true;
+  if (aborted && tid == 0) {
     raise_status(st, kStTimeout, MOE_K_ROUTER);
+    // every MMA issued so far completes before TMEM is read or released, and
+    // every copy issued so far lands before the CTA can leave
+    tc_commit(smem_u32(drain));
+    mbar_wait(smem_u32(drain), 0u);
+    for (int j = done; j < nw; ++j)
+      mbar_wait(smem_u32(&w_full[j % kRcWStages]), (uint32_t)(j / kRcWStages) & 1u);
+    for (int j = max(0, nx - 2); j < nx; ++j)
+      mbar_wait(smem_u32(&x_full[j & 1]), (uint32_t)(j >> 1) & 1u);
+  }
   tc_fence_after();
   __syncthreads();  // the W ring is free for the slice
 
@@ -602,7 +630,7 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
     for (int cc = 0; cc < 2; ++cc) {
       const int tc = half * 64 + cc * 32;
       uint32_t sm[32], bg[32];
-      if (nch > 0 && tc < (int)N) {
+      if (!aborted && nch > 0 && tc < (int)N) {
         const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + tc;
         tmem_ld32(ta, sm);
         tmem_ld32(ta + kRcN, bg);
@@ -633,7 +661,7 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
         float sum = 0.f;
 #pragma unroll
         for (int q = 0; q < kRcSplits; ++q) sum += v[q];
-        if (e0 + el < E) logits[(size_t)(t0 + t) * E + e0 + el] = sum;
+        if (e0 + el < E && !aborted) logits[(size_t)(t0 + t) * E + e0 + el] = sum;
       }
     }
   }
@@ -713,6 +741,19 @@ int router_tiles(const moe_config& c, int T) {
   return ((E + kRtExp - 1) / kRtExp) * ((T + kRtTok - 1) / kRtTok);
 }
 
+int router_splits_default(const moe_config& c, int T) { return router_splits(c, T, 152); }
+
+bool router_tc_decode_chosen(const moe_config& c, int T) {
+  // The tensor-core router runs where it has enough parallel work: at least 32
+  // CTAs, or at most four K chunks per CTA (a few-tile layer with a long H, such
+  // as 256 experts x 128 tokens x 7168, keeps the CUDA-core router's wider grid).
+  const int E = c.n_routed + c.n_zero;
+  const int rc_tiles = ((E + kRcM - 1) / kRcM) * ((T + kRcN - 1) / kRcN);
+  const int rc_chunks = (c.hidden / kRcK + kRcSplits - 1) / kRcSplits;
+  const bool rc_fits = rc_tiles * kRcSplits >= 32 || rc_chunks <= 4;
+  return router_tc_decode_enabled() && c.hidden % kRcK == 0 && rc_fits;
+}
+
 int router_splits(const moe_config& c, int T, int num_sms) {
   const long tiles = router_tiles(c, T);
   // at least 512 K per split; down to 256 while the partials stay under 2 MiB
@@ -743,14 +784,8 @@ void launch_router(const Launch& L, const moe_config& c, int T, const void* x, c
   CUtensorMap xmap, wmap;
   memset(&xmap, 0, sizeof xmap);
   memset(&wmap, 0, sizeof wmap);
-  // The tensor-core router runs where it has enough parallel work: at least 32
-  // CTAs, or at most four K chunks per CTA (a few-tile layer with a long H, such
-  // as 256 experts x 128 tokens x 7168, keeps the CUDA-core router's wider grid).
-  const int rc_tiles = ((E + kRcM - 1) / kRcM) * ((T + kRcN - 1) / kRcN);
-  const int rc_chunks = (c.hidden / kRcK + kRcSplits - 1) / kRcSplits;
-  const bool rc_fits = rc_tiles * kRcSplits >= 32 || rc_chunks <= 4;
-  if (router_tc_decode_enabled() && c.hidden % kRcK == 0 && rc_fits &&
-      rc_x_map(&xmap, x, T, c.hidden) && rc_w_map(&wmap, w_r, E, c.hidden)) {
+  if (router_tc_decode_chosen(c, T) && rc_x_map(&xmap, x, T, c.hidden) &&
+      rc_w_map(&wmap, w_r, E, c.hidden)) {
     // decode router on tensor cores: clusters of kRcSplits CTAs, one per H slice
     const dim3 g((E + kRcM - 1) / kRcM, (T + kRcN - 1) / kRcN, kRcSplits);
     set_smem_attr_once(reinterpret_cast<const void*>(router_tc_kernel), kRcSmem, kAttrRouterTc);

@@ -9,6 +9,14 @@
 // compiled into the library instead, so the caller passes x, the router
 // weights, the bias and the two outputs, and nothing is allocated.
 //
+// It always runs the small-batch routers (the decode router on tensor cores,
+// or the CUDA-core router), also for batches where moe_route switches to its
+// large-batch router (at least 1024 tokens, H a multiple of 64, 64 or more
+// 128 x 128 tiles), which needs a split copy of the router weights.  There the
+// two entry points sum the same products in different orders: routing ids are
+// the same unless two keys are closer than the logits' rounding, and weights
+// agree to about 1e-5 relative.
+//
 // The array (4 MiB of logits and split-K partials after a 4 KB head: status
 // word and router tile counters) exists on every GPU that loads the library and
 // stays there until the process exits.  All calls on a device share it: two
@@ -29,7 +37,6 @@ constexpr size_t kNoAllocStatusBytes = 256;
 constexpr size_t kNoAllocHeadBytes = kNoAllocStatusBytes + kRouterCounterBytes;
 constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;  // 4 MiB of fp32 logits + partials
 constexpr int kNoAllocMaxDevices = 64;
-constexpr int kRouterCtasPerSm = 152;  // same split-K choice as moe_route
 
 // Status word, router tile counters (zero at load time; the router leaves them
 // zero after every call), then final and split-K partial logits.
@@ -76,7 +83,10 @@ extern "C" moe_status moe_route_noalloc(const moe_config* cfg, int32_t T, const 
                         reinterpret_cast<uintptr_t>(topk_w);
   if (mis & 15u) return MOE_ERR_ALIGNMENT;
   const int E = cfg->n_routed + cfg->n_zero;
-  const int splits = router_splits(*cfg, T, kRouterCtasPerSm);
+  // The decode router on tensor cores needs no split-K partials; the CUDA-core
+  // router splits K as moe_route does.  (Should the tensor-core router's maps
+  // fail to encode, the fallback runs unsplit, so it needs no partials either.)
+  const int splits = router_tc_decode_chosen(*cfg, T) ? 1 : router_splits_default(*cfg, T);
   const size_t logit_bytes = (size_t)T * E * sizeof(float);
   const size_t partial_bytes = splits > 1 ? (size_t)splits * logit_bytes : 0;
   if (logit_bytes + partial_bytes > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;

@@ -82,6 +82,7 @@ struct Args {
   int* sched;                // dynamic tile counter, zero at launch
   int K, N;
   DevStatus* status;
+  ScatterAdd sc;             // down mode: add w * y into the tokens' accumulators
 };
 
 // Tile id -> rows, channel tile, expert.
@@ -112,6 +113,11 @@ __device__ __forceinline__ void emit(const Args& a, int row, int ch, int acc0, i
   if (MODE == kW8GateUp) {
     const float v1 = (float)acc1 * sr * sw1;
     a.out_f32[o] = __fdividef(v0, 1.f + __expf(-v0)) * v1;
+  } else if (a.sc.acc) {  // fused combine: add into the token's row
+    int tk;
+    float wt;
+    scatter_target(a.sc, row, false, &tk, &wt);
+    atomicAdd(a.sc.acc + (size_t)tk * a.N + ch, wt * v0);
   } else {
     a.out_f32[o] = v0;
   }
@@ -172,7 +178,7 @@ struct PGeom {
   static constexpr int kActOff = kSConv * kConvBytes;
   static constexpr int kRawOff = kActOff + kSAct * kActBytes;
   static constexpr int kBarOff = kRawOff + kSRaw * kRawBytes;
-  static constexpr int kBarCount = 2 * kSRaw + 2 * kSAct + 2 * kSConv + 8 + 1 + 2 * kTileQueue;
+  static constexpr int kBarCount = 2 * kSRaw + 2 * kSAct + 2 * kSConv + 10 + 1 + 2 * kTileQueue;
   static constexpr int kBarBytes = 1024;
   static constexpr int kNormOff = kBarOff + kBarBytes;
   static constexpr int kNormBytes = 2 * 2 * kTcM * 4;
@@ -180,9 +186,9 @@ struct PGeom {
 };
 static_assert(PGeom<kW8GateUp>::kSmemBytes <= 227 * 1024, "pair gate/up shared memory");
 static_assert(PGeom<kW8Down>::kSmemBytes <= 227 * 1024, "pair down shared memory");
-static_assert(PGeom<kW8GateUp>::kBarCount * 8 + kTileQueue * (int)sizeof(QTile) + 32 <=
+static_assert(PGeom<kW8GateUp>::kBarCount * 8 + kTileQueue * (int)sizeof(QTile) + 48 <=
                   PGeom<kW8GateUp>::kBarBytes, "pair gate/up barriers");
-static_assert(PGeom<kW8Down>::kBarCount * 8 + kTileQueue * (int)sizeof(QTile) + 32 <=
+static_assert(PGeom<kW8Down>::kBarCount * 8 + kTileQueue * (int)sizeof(QTile) + 48 <=
                   PGeom<kW8Down>::kBarBytes, "pair down barriers");
 static_assert(PGeom<kW8GateUp>::kNA * kAccCols * PGeom<kW8GateUp>::kAccBufs <= 512,
               "pair gate/up accumulators");
@@ -222,7 +228,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* norm_full = acc_empty + 2;
   uint64_t* norm_empty = norm_full + 2;
-  uint64_t* drain = norm_empty + 2;
+  uint64_t* guard = norm_empty + 2;  // [2] fused down mode: the epilogue warps' guard vote
+  uint64_t* drain = guard + 2;
   uint64_t* tq_full = drain + 1;
   uint64_t* tq_empty = tq_full + kTileQueue;
   QTile* tq = reinterpret_cast<QTile*>(tq_empty + kTileQueue);
@@ -230,6 +237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* tile_bad = abort_flag + 1;   // [2], per accumulator buffer
   volatile int* tile_done = abort_flag + 3;  // [2], epilogue warps finished
+  volatile int* bad_seq = abort_flag + 5;    // [2] fused down mode: 1 + tile count if bad
   int32_t* wnorm = reinterpret_cast<int32_t*>(smem + G::kNormOff);
 
   const uint32_t rank = cluster_rank();
@@ -253,8 +261,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&acc_empty[b]), 2 * kEpiWarps);  // first CTA: both epilogues
       mbar_init(smem_u32(&norm_full[b]), 4);
       mbar_init(smem_u32(&norm_empty[b]), kEpiWarps);
+      mbar_init(smem_u32(&guard[b]), kEpiWarps);
       tile_bad[b] = 0;
       tile_done[b] = 0;
+      bad_seq[b] = 0;
     }
     mbar_init(smem_u32(drain), 1);
     for (int s = 0; s < kTileQueue; ++s) {
@@ -606,16 +616,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (NA == 2) sw1 = a.s1[(size_t)t.e * a.N + ch];
       }
       const int cbeg = half * (TN / 2), cend = min(t.n, (half + 1) * (TN / 2));
+      // fused combine (down mode): the rows' tokens and routing weights too
+      const bool fused = MODE == kW8Down && a.sc.acc != nullptr;
       int xn[kChunks];
       float sr_l[kChunks];
+      int tk_l[kChunks];
+      float wt_l[kChunks];
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
         const int tl = cbeg + 32 * c + lane;
         xn[c] = 0;
         sr_l[c] = 0.f;
+        tk_l[c] = 0;
+        wt_l[c] = 0.f;
         if (tl < cend) {
           xn[c] = a.row_norm2[t.row0 + tl];
           if (MODE != kW8Raw) sr_l[c] = a.row_scale[t.row0 + tl];
+          if (fused) scatter_target(a.sc, t.row0 + tl, false, &tk_l[c], &wt_l[c]);
         }
       }
       if (!warp_wait_cluster(smem_u32(&acc_full[buf]), use & 1u) ||
@@ -631,6 +648,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const long long wn1 = NA == 2 ? wnorm[(nb * 2 + 1) * kTcM + r] : 0;
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
       bool bad = false;
+      if (fused) {
+        // Adds cannot be undone, so the CTA's half of the tile is judged as a
+        // whole before any is made: every epilogue warp checks the guard on its
+        // rows, the eight vote through a barrier, and a half that fails adds
+        // nothing here (the exact kernel adds it).
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+          int xmax = xn[c];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+            xmax = max(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
+          bad |= (long long)xmax * wn0 >= kGuard;
+        }
+        const bool any = __any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+          if (any) bad_seq[buf] = (int)local + 1;
+          mbar_arrive(smem_u32(&guard[buf]));
+        }
+        if (!warp_wait(smem_u32(&guard[buf]), use & 1u)) {
+          if (lane == 0) {
+            raise_status(a.status, kStTimeout, kind);
+            fail();
+          }
+          break;
+        }
+        const bool half_bad = bad_seq[buf] == (int)local + 1;
+        if (half_bad && warp == 2 && lane == 0) {
+          const int slot = atomicAdd(&a.redo[0], 1);
+          if (slot < a.redo_cap)
+            a.redo[1 + slot] = t.tile * 2 + (int)rank;
+          else
+            raise_status(a.status, kStInternal, kind);
+        }
+        if (!half_bad) {
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            const int c0 = cbeg + 32 * c;
+            if (c0 >= cend) break;
+            const int cn = min(32, cend - c0);
+            uint32_t g[32];
+            tmem_ld32(trow + c0, g);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float sr = __shfl_sync(0xffffffffu, sr_l[c], i);
+              const int tk = __shfl_sync(0xffffffffu, tk_l[c], i);
+              const float wt = __shfl_sync(0xffffffffu, wt_l[c], i);
+              if (i < cn && live)
+                atomicAdd(a.sc.acc + (size_t)tk * a.N + ch, wt * (__uint_as_float(g[i]) * sr * sw0));
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&norm_empty[nb]));
+          mbar_arrive_remote(lead_acc_empty + 8u * buf);
+        }
+        continue;
+      }
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
         const int c0 = cbeg + 32 * c;
@@ -777,8 +854,14 @@ constexpr int kMaxTopKQuant = 32;  // the largest top_k the layer accepts
 __global__ void __launch_bounds__(kQgThreads)
     quant_gather_kernel(const uint16_t* x, const int32_t* ids, const int32_t* e2s,
                         const int32_t* offsets, int gemv_max, uint16_t* x16, int8_t* x8,
-                        float* scale, int32_t* norm2, int H, int k, int E_r) {
+                        float* scale, int32_t* norm2, int H, int k, int E_r, int E,
+                        const float* w, float* acc) {
   pdl_enter();
+  // fused combine: the token's accumulator row starts as its zero-computation
+  // picks' w * x (the down pass adds the expert outputs)
+  if (acc)
+    zero_pick_init(ids, w, blockIdx.x, k, E_r, E, x + (size_t)blockIdx.x * H,
+                   acc + (size_t)blockIdx.x * H, H, threadIdx.x, kQgThreads);
   __shared__ float red_f[kQgThreads / 32];
   __shared__ int red_i[kQgThreads / 32];
   __shared__ int rows[kMaxTopKQuant];   // all FFN rows: the fp16 ones, then the int8 ones
@@ -1036,6 +1119,7 @@ Args make_args(const Launch& L, const W8Pass& p) {
   a.K = p.K;
   a.N = p.N;
   a.status = L.status;
+  a.sc = p.sc;
   return a;
 }
 
@@ -1085,11 +1169,12 @@ void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, in
 
 void launch_quant_gather(const Launch& L, const moe_config& c, int T, const void* x,
                          const int32_t* ids, const int32_t* e2s, const int32_t* offsets,
-                         int gemv_max, uint16_t* x16, int8_t* x8, float* scale, int32_t* norm2) {
+                         int gemv_max, uint16_t* x16, int8_t* x8, float* scale, int32_t* norm2,
+                         const float* w, float* acc) {
   launch_begin(L, MOE_K_PERM_GATHER);
   launch_kernel(quant_gather_kernel, T, kQgThreads, 0, L.stream, static_cast<const uint16_t*>(x),
                 ids, e2s, offsets, gemv_max, x16, x8, scale, norm2, c.hidden, c.top_k,
-                c.n_routed);
+                c.n_routed, c.n_routed + c.n_zero, w, acc);
   launch_end(L, MOE_K_PERM_GATHER);
 }
 

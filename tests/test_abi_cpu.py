@@ -53,8 +53,8 @@ def test_binding_names_match_header(moe):
 
 
 def test_config_struct_layout_matches_header(moe):
-    # 15 int32 + 1 float, no padding
-    assert ctypes.sizeof(moe.MoeConfig) == 16 * 4
+    # 16 int32 + 1 float, no padding
+    assert ctypes.sizeof(moe.MoeConfig) == 17 * 4
 
 
 def _ws(moe, cfg, T):
@@ -75,7 +75,7 @@ def test_workspace_size_for_the_headline_layers(moe):
 @pytest.mark.parametrize("field,value,status", [
     ("hidden", 7, 1), ("hidden", 0, 1), ("top_k", 0, 1), ("top_k", 9, 1), ("n_group", 3, 1),
     ("score", 5, 1), ("bias_mode", 3, 1), ("shared_inter", 12, 1), ("inter", 4, 1),
-    ("renormalize", 2, 1), ("n_routed", -1, 1),
+    ("renormalize", 2, 1), ("n_routed", -1, 1), ("combine", 3, 1), ("combine", -1, 1),
 ])
 def test_invalid_configs_are_rejected(moe, field, value, status):
     import synth

@@ -45,9 +45,10 @@ def test_back_to_back_calls_on_one_workspace(m, name):
     d = gs.inputs(spec)
     xa = d["x_d"]
     xb = torch.flip(xa, dims=[0]).contiguous()
-    ref_a = gs.run_layer(m, spec, d, out_fp32=True, x=xa)
-    ref_b = gs.run_layer(m, spec, d, out_fp32=True, x=xb)
-    cfg = m.config_from_spec(spec, out_fp32=True)
+    ordered = m.COMBINE_ORDERED  # bit-exact comparisons need the deterministic combine
+    ref_a = gs.run_layer(m, spec, d, out_fp32=True, x=xa, combine=ordered)
+    ref_b = gs.run_layer(m, spec, d, out_fp32=True, x=xb, combine=ordered)
+    cfg = m.config_from_spec(spec, out_fp32=True, combine=ordered)
     T = xa.shape[0]
     ws = m.workspace(cfg, T, xa.device)
     outs = [torch.empty((T, spec["hidden"]), dtype=torch.float32, device=xa.device)
@@ -68,7 +69,7 @@ from tests import gpu_support as gs
 m = gs.lib()
 spec = synth.spec(sys.argv[2])
 d = gs.inputs(spec)
-out = gs.run_layer(m, spec, d, out_fp32=True)
+out = gs.run_layer(m, spec, d, out_fp32=True, combine=m.COMBINE_ORDERED)
 np.save(sys.argv[3], out.cpu().numpy())
 """
 
@@ -79,7 +80,7 @@ def test_plain_launches_give_the_same_bits(m, name, tmp_path):
     # order; the outputs must be identical.
     spec = synth.spec(name)
     d = gs.inputs(spec)
-    got = gs.run_layer(m, spec, d, out_fp32=True).cpu().numpy()
+    got = gs.run_layer(m, spec, d, out_fp32=True, combine=m.COMBINE_ORDERED).cpu().numpy()
     path = str(tmp_path / "plain.npy")
     env = dict(os.environ, MOE_PDL="0", PYTHONPATH=ROOT)
     r = subprocess.run([sys.executable, "-c", _PLAIN, ROOT, name, path], env=env, cwd=ROOT,
@@ -87,3 +88,38 @@ def test_plain_launches_give_the_same_bits(m, name, tmp_path):
     assert r.returncode == 0, r.stderr[-2000:]
     plain = np.load(path)
     assert np.array_equal(got, plain)
+
+
+_ROUTE_CC = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import oracle, synth
+from tests import gpu_support as gs, support
+m = gs.lib()
+for name in sys.argv[2:]:
+    spec = synth.spec(name)
+    x, w_r, bias, _ = support.make_inputs(spec)
+    cfg = m.config_from_spec(spec)
+    T, k = spec["T"], spec["top_k"]
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = m.workspace(cfg, T)
+    m.moe_route(cfg, T, x.cuda(), w_r.cuda(), None if bias is None else bias.cuda(), ids, w, ws)
+    torch.cuda.synchronize()
+    assert m.moe_check_device_status(ws) == m.MOE_OK
+    ids_o, w_o, _, _ = oracle.route(spec, synth.bf16_bits(x), w_r.numpy(), support.np_bias(bias))
+    assert np.array_equal(ids.cpu().numpy(), ids_o), name
+    assert np.allclose(w.cpu().numpy(), w_o, rtol=1e-5, atol=1e-7), name
+    print("ok", name)
+"""
+
+
+def test_route_with_tensor_core_router_off():
+    # MOE_ROUTER_TC=0 (read once per process) keeps small-batch routing on the
+    # CUDA-core router; the layers whose shapes pick the tensor-core router by
+    # default must still route exactly as the oracle does.
+    env = dict(os.environ, MOE_ROUTER_TC="0", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-c", _ROUTE_CC, ROOT, "dsv3_s", "longcat_s", "tiny"],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.count("ok ") == 3

@@ -35,6 +35,34 @@ def test_layer_matches_oracle(m, name, out_fp32, gemv_max_rows):
     gs.check_out(got, ref, bf16_out=not out_fp32, what=f"{name} gemv<={gemv_max_rows}")
 
 
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("out_fp32", [True, False])
+def test_layer_with_ordered_combine_matches_oracle(m, name, out_fp32):
+    # the per-pick rows and the deterministic combine kernel instead of the
+    # down epilogue's scatter-add
+    spec = synth.spec(name)
+    d = gs.inputs(spec)
+    ref = oracle_out(spec, d)
+    got = gs.run_layer(m, spec, d, out_fp32=out_fp32, combine=m.COMBINE_ORDERED)
+    gs.check_out(got, ref, bf16_out=not out_fp32, what=f"{name} ordered")
+
+
+@pytest.mark.parametrize("name", ["dsv3_s", "pangu_s", "ragged_s"])
+@pytest.mark.parametrize("gemv_max_rows", [0, 8])
+def test_fused_and_ordered_combine_agree(m, name, gemv_max_rows):
+    # The two combines add the same fp32 products, in a different order: they
+    # agree to fp32 rounding (and repeated fused calls agree with each other
+    # the same way; their atomic adds may land in any order).
+    spec = synth.spec(name)
+    d = gs.inputs(spec)
+    o = gs.run_layer(m, spec, d, gemv_max_rows=gemv_max_rows, combine=m.COMBINE_ORDERED)
+    f1 = gs.run_layer(m, spec, d, gemv_max_rows=gemv_max_rows, combine=m.COMBINE_FUSED)
+    f2 = gs.run_layer(m, spec, d, gemv_max_rows=gemv_max_rows, combine=m.COMBINE_FUSED)
+    scale = o.abs().max().item()
+    assert (f1 - o).abs().max().item() <= 1e-5 * scale
+    assert (f2 - f1).abs().max().item() <= 1e-5 * scale
+
+
 @pytest.mark.parametrize("gemv_max_rows", [1, 3, 1000])
 def test_layer_path_choice_does_not_change_result(m, gemv_max_rows):
     spec = synth.spec("pangu_s")
@@ -44,21 +72,23 @@ def test_layer_path_choice_does_not_change_result(m, gemv_max_rows):
     gs.check_out(got, ref, bf16_out=False, what=f"gemv_max_rows={gemv_max_rows}")
 
 
-def test_layer_is_deterministic(m):
+def test_layer_is_deterministic_with_ordered_combine(m):
     spec = synth.spec("dsv3_s")
     d = gs.inputs(spec)
-    a = gs.run_layer(m, spec, d, out_fp32=True)
-    b = gs.run_layer(m, spec, d, out_fp32=True)
+    a = gs.run_layer(m, spec, d, out_fp32=True, combine=m.COMBINE_ORDERED)
+    b = gs.run_layer(m, spec, d, out_fp32=True, combine=m.COMBINE_ORDERED)
     assert torch.equal(a, b)
 
 
 @pytest.mark.parametrize("name", ["dsv3_s", "w8a8_s"])
-def test_layer_replays_from_a_cuda_graph(m, name):
+@pytest.mark.parametrize("combine", [1, 2])  # ordered, fused
+def test_layer_replays_from_a_cuda_graph(m, name, combine):
     # The layer is stream-ordered with no host synchronisation, so one capture
-    # replays it: the replay on new inputs matches a direct call bit for bit.
+    # replays it: the replay on new inputs matches a direct call, bit for bit
+    # with the ordered combine, to fp32 rounding with the fused one.
     spec = synth.spec(name)
     d = gs.inputs(spec)
-    cfg = m.config_from_spec(spec, out_fp32=True)
+    cfg = m.config_from_spec(spec, out_fp32=True, combine=combine)
     T, H = spec["T"], spec["hidden"]
     w = d["wts_d"]
     x = d["x_d"].clone()
@@ -84,8 +114,11 @@ def test_layer_replays_from_a_cuda_graph(m, name):
     torch.cuda.synchronize()
     assert m.moe_check_device_status(ws) == m.MOE_OK
     replayed = out.clone()
-    direct = gs.run_layer(m, spec, d, out_fp32=True, x=x.clone())
-    assert torch.equal(replayed, direct)
+    direct = gs.run_layer(m, spec, d, out_fp32=True, x=x.clone(), combine=combine)
+    if combine == m.COMBINE_ORDERED:
+        assert torch.equal(replayed, direct)
+    else:
+        assert (replayed - direct).abs().max().item() <= 1e-5 * direct.abs().max().item()
 
 
 def test_single_token_and_empty_batch(m):

@@ -56,6 +56,25 @@ def test_route_on_tensor_cores_matches_oracle(m):
     assert np.allclose(w, w_o, rtol=1e-5, atol=1e-7), f"max rel {rel.max():.3e}"
 
 
+def _route_inputs(spec):
+    x, w_r, bias, _ = support.make_inputs(spec)
+    return dict(x=x, w_r=w_r, bias=bias, x_d=x.cuda(), w_r_d=w_r.cuda(),
+                bias_d=None if bias is None else bias.cuda())
+
+
+def test_route_on_cuda_cores_by_default_matches_oracle(m):
+    # 128 tokens x 256 experts x H = 4096: two 128 x 128 tiles with eight K
+    # chunks per CTA, the shape class (few tiles, long H) that keeps the
+    # CUDA-core router and its split-K reduction
+    spec = synth.spec("dsv3_s", hidden=4096, n_routed=256, name="router_cc")
+    d = _route_inputs(spec)
+    ids, w = route_gpu(m, spec, d)
+    ids_o, w_o, _, _ = oracle.route(spec, synth.bf16_bits(d["x"]), d["w_r"].numpy(),
+                                    support.np_bias(d["bias"]))
+    assert np.array_equal(ids, ids_o)
+    assert np.allclose(w, w_o, rtol=1e-5, atol=1e-7)
+
+
 @pytest.mark.parametrize("score", ["softmax", "sigmoid"])
 def test_route_select_bias_and_groups(m, score):
     spec = synth.spec("dsv3_s", score=score, bias_mode="select", bias_kind="iid",

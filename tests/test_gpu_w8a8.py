@@ -190,7 +190,9 @@ def test_w8a8_streaming_path_matches_oracle_and_tensor_cores(m, T, gemv, H, I):
                                         L["su"], L["qd"], L["sd"])
     got = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=gemv)
     gs.check_out(got, ref, bf16_out=False, what=f"w8a8 T={T} gemv<={gemv}")
-    tc = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=-1)
+    ordered = m.COMBINE_ORDERED
+    got = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=gemv, combine=ordered)
+    tc = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=-1, combine=ordered)
     assert torch.equal(got, tc)
 
 
@@ -248,5 +250,38 @@ def test_w8a8_layer_exact_fallback_on_guard_failures(m):
                                         L["su"], L["qd"], L["sd"])
     tc = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=-1)
     gs.check_out(tc, ref, bf16_out=False, what="w8a8 guard fallback")
-    stream = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=100000)
+    ordered = m.COMBINE_ORDERED
+    tc = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=-1, combine=ordered)
+    stream = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=100000, combine=ordered)
     assert torch.equal(tc, stream)
+
+
+@pytest.mark.parametrize("combine", [1, 2])  # ordered, fused
+def test_w8a8_down_pass_exact_fallback(m, combine):
+    # Every token is the same row of ones and every gate/up weight code is +127,
+    # so h is the same positive value in every channel and quantises to +127
+    # everywhere: with I = 2048 each down-pass pair has 127^4 I^2 > 2^48 and
+    # fails the tensor-core guard, as does each gate/up pair (H = 2048).  Both
+    # passes then run on the exact integer kernel; with the fused combine, the
+    # down tiles' halves that fail add nothing in the tensor-core epilogue and
+    # the exact kernel adds them.
+    H, I, E = 2048, 2048, 8
+    assert (127 ** 4) * I * I >= 2 ** 48
+    spec = synth.spec("w8a8_s", T=64, hidden=H, inter=I, n_routed=E, top_k=2,
+                      name="w8_guard_down")
+    base = gs.inputs(spec)
+    rng = np.random.default_rng(37)
+    x = torch.ones((spec["T"], H), dtype=torch.bfloat16)
+    wts = {"w_gate": torch.full((E, I, H), 127, dtype=torch.int8),
+           "w_up": torch.full((E, I, H), 127, dtype=torch.int8),
+           "w_down": torch.as_tensor(127 * rng.choice([-1, 1], size=(E, H, I)), dtype=torch.int8),
+           "s_gate": torch.full((E, I), 1e-5), "s_up": torch.full((E, I), 1e-5),
+           "s_down": torch.as_tensor(rng.uniform(0.5e-3, 1.5e-3, size=(E, H)),
+                                     dtype=torch.float32)}
+    d = dict(base, x=x, x_d=x.cuda(), wts=wts, wts_d={k: v.cuda() for k, v in wts.items()})
+    L = w8_lists(wts)
+    ref, _, _, _, _ = oracle.layer_w8a8(spec, synth.bf16_bits(x), d["w_r"].numpy(),
+                                        support.np_bias(d["bias"]), L["qg"], L["sg"], L["qu"],
+                                        L["su"], L["qd"], L["sd"])
+    got = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=-1, combine=combine)
+    gs.check_out(got, ref, bf16_out=False, what="w8a8 down-pass guard fallback")

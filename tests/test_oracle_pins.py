@@ -353,3 +353,17 @@ def test_margin_rule_holds_after_redraws():
     s = synth.spec("dsv3_s")
     x, w_r, bias, redraws = support.make_inputs(s)
     assert support.margin_rows(s, x, w_r, bias).all()
+
+
+def test_longcat_zero_expert_share_is_about_a_third():
+    # The LongCat-shaped layer's router is drawn so that about a third of the
+    # picks land on its 256 zero-computation experts (an i.i.d. per-expert bias
+    # keeps the 768 experts exchangeable).  Check the realised share on the
+    # seeded inputs, routed by the oracle: within [0.30, 0.37] on the full layer
+    # and on its scaled-down relative.
+    for name in ("longcat", "longcat_s"):
+        s = synth.spec(name)
+        x, w_r, bias, _ = support.make_inputs(s)
+        ids, _, _, _ = oracle.route(s, synth.bf16_bits(x), w_r.numpy(), support.np_bias(bias))
+        share = float(np.mean(ids >= s["n_routed"]))
+        assert 0.30 <= share <= 0.37, (name, share)
