@@ -85,7 +85,8 @@ def _load():
             lib.orc_quantize_rows.restype = None
             lib.orc_int8_matmul.argtypes = [I, I, I, P, P, P]
             lib.orc_int8_matmul.restype = None
-            lib.orc_layer_w8a8.argtypes = [C, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P]
+            lib.orc_layer_w8a8.argtypes = [C, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                           P, P, P, P, P]
             for f in ("orc_router_logits", "orc_select", "orc_permute", "orc_layer",
                       "orc_layer_w8a8"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -216,8 +217,9 @@ def int8_matmul(a, w):
     return acc
 
 
-def layer_w8a8(spec, x_bits, w_router, bias, qg, sg, qu, su, qd, sd):
-    """Whole W8A8 layer -> out [T,H] f64, ids, weights, q_x [T,H] int8, s_x [T] f32."""
+def layer_w8a8(spec, x_bits, w_router, bias, qg, sg, qu, su, qd, sd, shared=None):
+    """Whole W8A8 layer -> out [T,H] f64, ids, weights, q_x [T,H] int8, s_x [T] f32.
+    shared: (qsg, ssg, qsu, ssu, qsd, ssd) int8 matrices and fp32 scales, or None."""
     lib, cfg = _load(), make_cfg(spec)
     x_bits, w_router = _c(x_bits, np.uint16), _c(w_router, np.float32)
     bias = _c(bias, np.float32)
@@ -229,8 +231,12 @@ def layer_w8a8(spec, x_bits, w_router, bias, qg, sg, qu, su, qd, sd):
     w = np.empty((T, cfg.top_k), np.float64)
     qx = np.empty((T, cfg.hidden), np.int8)
     sx = np.empty(T, np.float32)
+    sh = [None] * 6
+    if shared is not None:
+        sh = [_c(a, np.int8 if i % 2 == 0 else np.float32) for i, a in enumerate(shared)]
     _check(lib.orc_layer_w8a8(ctypes.byref(cfg), T, _p(x_bits), _p(w_router), _p(bias),
-                              *[a[0] for a in arrays], _p(out), _p(ids), _p(w), _p(qx), _p(sx)),
+                              *[a[0] for a in arrays], *[_p(a) for a in sh], _p(out), _p(ids),
+                              _p(w), _p(qx), _p(sx)),
            "layer_w8a8")
-    del arrays
+    del arrays, sh
     return out, ids, w, qx, sx

@@ -346,14 +346,50 @@ void orc_int8_matmul(int R, int N, int K, const int8_t* a, const int8_t* w, int6
     }
 }
 
+/* One W8A8 SwiGLU expert on one token's codes q (scale sx): integer gate and up
+ * matmuls, dequantised acc * sx * s_channel in fp64, h = silu(g) * u rounded to
+ * fp32 and quantised per row like the token, integer down matmul, dequantised
+ * acc * s_h * s_channel.  y fp64 [H]; hf, qh scratch of I entries. */
+static void w8a8_expert(int H, int I, const int8_t* q, float sx, const int8_t* qg,
+                        const float* sg, const int8_t* qu, const float* su, const int8_t* qd,
+                        const float* sd, double* y, float* hf, int8_t* qh) {
+  for (int i = 0; i < I; ++i) {
+    int64_t ag = 0, au = 0;
+    for (int h = 0; h < H; ++h) {
+      ag += (int64_t)q[h] * qg[(size_t)i * H + h];
+      au += (int64_t)q[h] * qu[(size_t)i * H + h];
+    }
+    double g = (double)ag * (double)sx * (double)sg[i];
+    double u = (double)au * (double)sx * (double)su[i];
+    hf[i] = (float)(silu(g) * u);
+  }
+  float sh;
+  orc_quantize_rows(1, I, hf, qh, &sh);
+  for (int ch = 0; ch < H; ++ch) {
+    int64_t ad = 0;
+    for (int i = 0; i < I; ++i) ad += (int64_t)qh[i] * qd[(size_t)ch * I + i];
+    y[ch] = (double)ad * (double)sh * (double)sd[ch];
+  }
+}
+
+/* The shared expert of a W8A8 layer takes the same quantised token codes as the
+ * routed experts: [DS-ASC] section "2. 模型侧并发优化" moves the quantisation
+ * ahead of the token AllGather, so the MoE layer (shared expert included)
+ * receives int8 activations with their scales.  Reading taken: the shared
+ * expert is an int8 SwiGLU expert with per-output-channel scales like the
+ * routed ones, added at weight 1. */
 int orc_layer_w8a8(const orc_cfg* c, int T, const uint16_t* x, const float* w_router,
                    const float* bias, const int8_t* const* qg, const float* const* sg,
                    const int8_t* const* qu, const float* const* su, const int8_t* const* qd,
-                   const float* const* sd, double* out, int32_t* ids_out, double* weights_out,
-                   int8_t* q_x_out, float* s_x_out) {
-  if (!cfg_ok(c) || T < 0 || !out || c->shared_inter != 0) return -1;
+                   const float* const* sd, const int8_t* qsg, const float* ssg,
+                   const int8_t* qsu, const float* ssu, const int8_t* qsd, const float* ssd,
+                   double* out, int32_t* ids_out, double* weights_out, int8_t* q_x_out,
+                   float* s_x_out) {
+  if (!cfg_ok(c) || T < 0 || !out) return -1;
+  if (c->shared_inter > 0 && (!qsg || !ssg || !qsu || !ssu || !qsd || !ssd)) return -1;
   if (T == 0) return 0;
   const int H = c->hidden, I = c->inter, E = c->n_routed + c->n_zero, k = c->top_k;
+  const int Is = c->shared_inter;
   double* logits = (double*)malloc(sizeof(double) * (size_t)T * E);
   int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
   double* w = (double*)malloc(sizeof(double) * (size_t)T * k);
@@ -371,10 +407,12 @@ int orc_layer_w8a8(const orc_cfg* c, int T, const uint16_t* x, const float* w_ro
   if (rc == 0) {
 #pragma omp parallel
     {
+      const int Imax = I > Is ? I : Is;
       float* xf = (float*)malloc(sizeof(float) * H);
-      float* hf = (float*)malloc(sizeof(float) * I);
-      int8_t* qh = (int8_t*)malloc(I);
+      float* hf = (float*)malloc(sizeof(float) * (Imax > 0 ? Imax : 1));
+      int8_t* qh = (int8_t*)malloc(Imax > 0 ? Imax : 1);
       double* xt = (double*)malloc(sizeof(double) * H);
+      double* y = (double*)malloc(sizeof(double) * H);
 #pragma omp for schedule(dynamic, 1)
       for (int t = 0; t < T; ++t) {
         for (int i = 0; i < H; ++i) {
@@ -392,29 +430,19 @@ int orc_layer_w8a8(const orc_cfg* c, int T, const uint16_t* x, const float* w_ro
             for (int i = 0; i < H; ++i) o[i] += wj * xt[i];
             continue;
           }
-          for (int i = 0; i < I; ++i) {
-            int64_t ag = 0, au = 0;
-            for (int h = 0; h < H; ++h) {
-              ag += (int64_t)q[h] * qg[e][(size_t)i * H + h];
-              au += (int64_t)q[h] * qu[e][(size_t)i * H + h];
-            }
-            double g = (double)ag * (double)sx[t] * (double)sg[e][i];
-            double u = (double)au * (double)sx[t] * (double)su[e][i];
-            hf[i] = (float)(silu(g) * u);
-          }
-          float sh;
-          orc_quantize_rows(1, I, hf, qh, &sh);
-          for (int ch = 0; ch < H; ++ch) {
-            int64_t ad = 0;
-            for (int i = 0; i < I; ++i) ad += (int64_t)qh[i] * qd[e][(size_t)ch * I + i];
-            o[ch] += wj * ((double)ad * (double)sh * (double)sd[e][ch]);
-          }
+          w8a8_expert(H, I, q, sx[t], qg[e], sg[e], qu[e], su[e], qd[e], sd[e], y, hf, qh);
+          for (int ch = 0; ch < H; ++ch) o[ch] += wj * y[ch];
+        }
+        if (Is > 0) {
+          w8a8_expert(H, Is, q, sx[t], qsg, ssg, qsu, ssu, qsd, ssd, y, hf, qh);
+          for (int ch = 0; ch < H; ++ch) o[ch] += y[ch];
         }
       }
       free(xf);
       free(hf);
       free(qh);
       free(xt);
+      free(y);
     }
   }
   if (rc == 0 && ids_out) memcpy(ids_out, ids, sizeof(int32_t) * (size_t)T * k);

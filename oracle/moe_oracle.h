@@ -105,14 +105,17 @@ void orc_quantize_rows(int R, int K, const float* v, int8_t* q, float* scale);
  * a int8 [R,K], w int8 [N,K], acc int64 [R,N]. */
 void orc_int8_matmul(int R, int N, int K, const int8_t* a, const int8_t* w, int64_t* acc);
 
-/* Whole W8A8 layer (no shared expert).  qg/qu [I,H] int8 with scales sg/su [I];
- * qd [H,I] int8 with scale sd [H]; pointer arrays as in orc_layer.
- * Optional outputs (NULL to skip): q_x [T,H] int8, s_x [T]. */
+/* Whole W8A8 layer.  qg/qu [I,H] int8 with scales sg/su [I]; qd [H,I] int8
+ * with scale sd [H]; pointer arrays as in orc_layer.  Shared expert (when
+ * shared_inter > 0, else NULL): qsg/qsu [I_s,H] with ssg/ssu [I_s], qsd [H,I_s]
+ * with ssd [H]; it takes the token's int8 codes like the routed experts and adds
+ * at weight 1.  Optional outputs (NULL to skip): q_x [T,H] int8, s_x [T]. */
 int orc_layer_w8a8(const orc_cfg* c, int T, const uint16_t* x, const float* w_router,
                    const float* bias, const int8_t* const* qg, const float* const* sg,
                    const int8_t* const* qu, const float* const* su, const int8_t* const* qd,
-                   const float* const* sd, double* out, int32_t* ids, double* weights,
-                   int8_t* q_x, float* s_x);
+                   const float* const* sd, const int8_t* qsg, const float* ssg,
+                   const int8_t* qsu, const float* ssu, const int8_t* qsd, const float* ssd,
+                   double* out, int32_t* ids, double* weights, int8_t* q_x, float* s_x);
 
 #ifdef __cplusplus
 }

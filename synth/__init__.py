@@ -79,6 +79,15 @@ CONFIGS = {
     # Profiling-sized relative of the W8A8 decode layer (2.4 GB of int8 weights).
     "longcat_w8_prof": dict(_BASE, T=16, hidden=6144, inter=2048, n_routed=64, n_zero=32,
                             top_k=12, bias_mode="logit", bias_kind="iid", wdtype="w8a8"),
+    # DeepSeek-V3-shaped decode layer with W8A8 weights, shared expert included
+    # (int8 like the routed experts, fed the same quantised token codes), and its
+    # scaled-down relative.
+    "dsv3_w8": dict(_BASE, T=128, hidden=7168, inter=2048, n_routed=256, top_k=8, n_group=8,
+                    topk_group=4, score="sigmoid", renormalize=True, routed_scale=2.5,
+                    shared_inter=2048, wdtype="w8a8"),
+    "dsv3_w8_s": dict(_BASE, T=128, hidden=1024, inter=320, n_routed=64, top_k=8, n_group=8,
+                      topk_group=4, score="sigmoid", renormalize=True, routed_scale=2.5,
+                      shared_inter=384, wdtype="w8a8"),
     # Profiling-sized W8A8 prefill relative: full H and I, 64 experts, Zipf load,
     # 2.8 GB of int8 weights and 235 MB of activation codes.
     "w8a8_prof": dict(_BASE, T=2048, hidden=7168, inter=2048, n_routed=64, top_k=8,
@@ -168,9 +177,12 @@ def draw_expert_bf16(s: dict, which: str, e: int, device="cpu", seed: int = 0) -
 
 
 def draw_expert_int8(s: dict, which: str, e: int, device="cpu", seed: int = 0):
-    """One int8 expert matrix with per-output-channel fp32 scales: (q, scale)."""
-    H, I = s["hidden"], s["inter"]
-    shape = (H, I) if which == "down" else (I, H)
+    """One int8 expert matrix with per-output-channel fp32 scales: (q, scale).
+    which: 'gate'/'up' [I, H], 'down' [H, I], or the shared expert's
+    'shared_gate'/'shared_up' [I_s, H], 'shared_down' [H, I_s]."""
+    H = s["hidden"]
+    I = s["shared_inter"] if which.startswith("shared") else s["inter"]
+    shape = (H, I) if which.endswith("down") else (I, H)
     q = _normal(shape, 31.75, device, seed, s["name"], which + "-q", e).round_().clamp_(-127, 127)
     u = torch.rand((shape[0],), generator=_gen(device, seed, s["name"], which + "-s", e),
                    device=device, dtype=torch.float32)
@@ -183,7 +195,9 @@ def draw_weights(s: dict, device="cpu", seed: int = 0, experts=None) -> dict:
 
     bf16: {'w_gate': [E_r, I, H], 'w_up': [E_r, I, H], 'w_down': [E_r, H, I]} bf16, plus
     'shared_gate'/'shared_up' [I_s, H] and 'shared_down' [H, I_s] when shared_inter > 0.
-    w8a8: int8 'w_gate'/'w_up'/'w_down' with fp32 's_gate'/'s_up' [E_r, I], 's_down' [E_r, H].
+    w8a8: int8 'w_gate'/'w_up'/'w_down' with fp32 's_gate'/'s_up' [E_r, I], 's_down' [E_r, H],
+    plus int8 'shared_gate'/'shared_up' [I_s, H], 'shared_down' [H, I_s] with fp32
+    's_shared_gate'/'s_shared_up' [I_s], 's_shared_down' [H] when shared_inter > 0.
     `experts`: optional iterable of expert indices to draw; the others stay zero.
     """
     E, H, I = s["n_routed"], s["hidden"], s["inter"]
@@ -212,6 +226,11 @@ def draw_weights(s: dict, device="cpu", seed: int = 0, experts=None) -> dict:
                 q, sc = draw_expert_int8(s, which, e, device, seed)
                 out["w_" + which][e] = q
                 out["s_" + which][e] = sc
+        if s["shared_inter"] > 0:
+            for which in ("shared_gate", "shared_up", "shared_down"):
+                q, sc = draw_expert_int8(s, which, 0, device, seed)
+                out[which] = q
+                out["s_" + which] = sc
     return out
 
 

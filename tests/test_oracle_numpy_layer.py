@@ -126,8 +126,18 @@ def np_quantise(v32):
     return z.astype(np.int64), s
 
 
+def _np_w8_expert(q, rs, qg, sg, qu, su, qd, sd):
+    """W8A8 SwiGLU expert on code rows q [n,H] with row scales rs [n,1]."""
+    g = (q @ qg.T).astype(np.float64) * rs * sg[None, :]
+    u = (q @ qu.T).astype(np.float64) * rs * su[None, :]
+    h32 = (_silu(g) * u).astype(np.float32)
+    qh, sh = np_quantise(h32)
+    return (qh @ qd.T).astype(np.float64) * sh.astype(np.float64)[:, None] * sd[None, :]
+
+
 def np_layer_w8a8(spec, xbits, w_r, bias, wts):
-    """out [T,H] float64 of the W8A8 layer (no shared expert)."""
+    """out [T,H] float64 of the W8A8 layer (the shared expert, when present, is
+    int8 too and takes the same token codes)."""
     x32 = support.bf16_to_f64(xbits).astype(np.float32)
     x = x32.astype(np.float64)
     T, H = x.shape
@@ -145,12 +155,14 @@ def np_layer_w8a8(spec, xbits, w_r, bias, wts):
             y = x[tok]
         else:
             rs = sx[tok].astype(np.float64)[:, None]
-            g = (qx[tok] @ qg[e].T).astype(np.float64) * rs * sg[e][None, :]
-            u = (qx[tok] @ qu[e].T).astype(np.float64) * rs * su[e][None, :]
-            h32 = (_silu(g) * u).astype(np.float32)
-            qh, sh = np_quantise(h32)
-            y = (qh @ qd[e].T).astype(np.float64) * sh.astype(np.float64)[:, None] * sd[e][None, :]
+            y = _np_w8_expert(qx[tok], rs, qg[e], sg[e], qu[e], su[e], qd[e], sd[e])
         np.add.at(out, tok, w[tok, slot][:, None] * y)
+    if spec["shared_inter"] > 0:
+        m = lambda n: wts[n].numpy().astype(np.int64)
+        f = lambda n: wts[n].numpy().astype(np.float64)
+        out += _np_w8_expert(qx, sx.astype(np.float64)[:, None], m("shared_gate"),
+                             f("s_shared_gate"), m("shared_up"), f("s_shared_up"),
+                             m("shared_down"), f("s_shared_down"))
     return out, ids, w, qx, sx
 
 
@@ -199,9 +211,13 @@ def _w8_case():
 def _oracle_w8(s, x, w_r, bias, wts):
     E = s["n_routed"]
     lst = lambda n: [wts[n][e].numpy() for e in range(E)]
+    shared = None
+    if s["shared_inter"] > 0:
+        shared = tuple(wts[n].numpy() for n in ("shared_gate", "s_shared_gate", "shared_up",
+                                                "s_shared_up", "shared_down", "s_shared_down"))
     return oracle.layer_w8a8(s, synth.bf16_bits(x), w_r.numpy(), support.np_bias(bias),
                              lst("w_gate"), lst("s_gate"), lst("w_up"), lst("s_up"),
-                             lst("w_down"), lst("s_down"))
+                             lst("w_down"), lst("s_down"), shared)
 
 
 def test_w8a8_inputs_exercise_every_scale():
@@ -233,3 +249,27 @@ def test_w8a8_layer_matches_numpy_restatement():
     # rounding-boundary straddle between two fp64 evaluations of silu would move
     # one code by one step, far below this bound but far above fp64 noise.
     _close(out, ref, 1e-9)
+
+
+W8_SHARED_PIN = dict(W8_PIN, name="w8_numpy_shared_pin", n_group=2, topk_group=1, n_zero=0,
+                     bias_mode="none", bias_kind="none", score="sigmoid", renormalize=True,
+                     routed_scale=2.5, shared_inter=72)
+
+
+def test_w8a8_layer_with_shared_expert_matches_numpy_restatement():
+    # DSv3-like routing (sigmoid, groups, renormalised x 2.5) plus an int8 shared
+    # expert fed the same token codes; the shared expert's scales vary by channel
+    s = dict(W8_SHARED_PIN)
+    x, w_r, bias, _ = support.make_inputs(s)
+    wts = synth.draw_weights(s)
+    v = wts["s_shared_down"].numpy()
+    assert v.max() / v.min() > 1.1
+    out, ids, w, qx, sx = _oracle_w8(s, x, w_r, bias, wts)
+    ref, ids_ref, w_ref, _, _ = np_layer_w8a8(s, synth.bf16_bits(x), w_r.numpy(),
+                                              support.np_bias(bias), wts)
+    assert np.array_equal(ids, ids_ref)
+    assert np.allclose(w, w_ref, rtol=1e-12, atol=0)
+    _close(out, ref, 1e-9)
+    # the shared expert's part is not negligible
+    no_shared = _oracle_w8(dict(s, shared_inter=0), x, w_r, bias, wts)[0]
+    assert np.abs(out - no_shared).max() > 0.05 * np.abs(out).max()
