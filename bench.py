@@ -252,9 +252,11 @@ def algorithmic_bytes(spec, counts):
     U = int((counts[:spec["n_routed"]] > 0).sum())
     if spec["wdtype"] == "w8a8":
         per = 3 * H * I + 4 * (2 * I + H)  # int8 gate + up + down and their scales
+        shared = 3 * H * Is + 4 * (2 * Is + H) if Is else 0
     else:
         per = 6 * H * I  # gate + up + down, bf16
-    b = U * per + 6 * H * Is + 4 * E * H + 2 * 2 * spec["T"] * H
+        shared = 6 * H * Is
+    b = U * per + shared + 4 * E * H + 2 * 2 * spec["T"] * H
     if spec["bias_mode"] != "none":
         b += 4 * E
     return b, U
@@ -272,8 +274,13 @@ def oracle_runner(spec, wts, need, w_r, b):
         for e in need:
             for k in L:
                 L[k][e] = wts[k][e].cpu().numpy()
+        sh = None
+        if spec["shared_inter"]:
+            sh = tuple(wts[k].cpu().numpy() for k in ("shared_gate", "s_shared_gate", "shared_up",
+                                                      "s_shared_up", "shared_down",
+                                                      "s_shared_down"))
         return lambda xb: oracle.layer_w8a8(spec, xb, w_r.numpy(), b, L["w_gate"], L["s_gate"],
-                                            L["w_up"], L["s_up"], L["w_down"], L["s_down"])
+                                            L["w_up"], L["s_up"], L["w_down"], L["s_down"], sh)
     g, u, dn = [None] * E, [None] * E, [None] * E
     for e in need:
         g[e] = synth.bf16_bits(wts["w_gate"][e])

@@ -94,6 +94,14 @@ typedef enum {
                               from call to call) */
 } moe_combine_mode;
 
+/* How the bf16 grouped FFN launches its tensor-core passes. */
+typedef enum {
+  MOE_FFN_LAUNCH_DEFAULT = 0, /* the library's tile-parameter table decides */
+  MOE_FFN_LAUNCH_TWO = 1,     /* gate/up, then down: two persistent launches */
+  MOE_FFN_LAUNCH_ONE = 2      /* one persistent launch: a down tile starts as soon as
+                                 its expert's gate/up tiles have stored h */
+} moe_ffn_launch;
+
 typedef enum {
   MOE_W_BF16 = 0, /* bf16 weights and activations, fp32 accumulation */
   MOE_W8A8 = 1    /* int8 weights + per-output-channel fp32 scales; per-row int8 activations */
@@ -125,11 +133,12 @@ typedef struct {
   int32_t out_fp32;      /* moe_layer_forward `out`: 1 = fp32, 0 = bf16 */
   int32_t gemv_max_rows; /* experts with <= this many rows take the streaming GEMV
                             path (bf16 FMA, or int8 dp4a for MOE_W8A8), the rest
-                            tensor-core tiles.  0 = library default (bf16: 0, all
-                            tensor cores; MOE_W8A8: 8), < 0 = never GEMV.  Fixed
-                            with the workspace size: W8A8 streaming needs int8 copies
+                            tensor-core tiles.  0 = the library's tile-parameter
+                            table (moe_tile_choice), < 0 = never GEMV.  Fixed with
+                            the workspace size: W8A8 streaming needs int8 copies
                             of the sorted activations. */
   int32_t combine;       /* moe_combine_mode; fixed with the workspace size */
+  int32_t ffn_launch;    /* moe_ffn_launch (bf16 layers) */
 } moe_config;
 
 /* Human-readable name of a status. Never NULL. */
@@ -201,8 +210,13 @@ moe_status moe_combine(const moe_config* cfg, int32_t T, const float* y_perm,
 
 /* The whole layer: route -> permute -> grouped FFN (+ shared expert) -> combine.
  *  x, w_router, bias, w_gate/w_up/w_down, s_* as above
- *  ws_gate, ws_up [I_s, H], ws_down [H, I_s]: shared expert (bf16), NULL when
- *  cfg->shared_inter == 0 ([DS-ASC] deployment paragraph: 1 shared expert)
+ *  ws_gate, ws_up [I_s, H], ws_down [H, I_s]: shared expert, NULL when
+ *  cfg->shared_inter == 0 ([DS-ASC] deployment paragraph: 1 shared expert).
+ *  bf16, or int8 for MOE_W8A8: the shared expert then takes the same per-token
+ *  int8 codes as the routed experts ([DS-ASC] "2. 模型侧并发优化": activations
+ *  are quantised before they are gathered for the MoE layer), and its
+ *  per-output-channel scales follow the routed experts' in s_gate / s_up
+ *  ([E_r * I + I_s] each) and s_down ([E_r * H + H]).
  *  out       bf16 or fp32 [T, H] per cfg->out_fp32 */
 moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
                              const float* w_router, const float* bias, const void* w_gate,
@@ -236,6 +250,15 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
 moe_status moe_route_noalloc(const moe_config* cfg, int32_t T, const void* x,
                              const float* w_router, const float* bias, int32_t* topk_ids,
                              float* topk_w, moe_stream_t stream);
+
+/* The grouped FFN's tiling choices for (cfg, T): the GEMV / tensor-core switch
+ * point and whether a bf16 FFN runs as one persistent launch (1) or two (0).
+ * They come from cfg where it sets them, else from the tile-parameter table the
+ * library was built with ([PANGU] SwiftGMM: tiling chosen from measured
+ * history, by expert load): the entry of the same weight type nearest in load
+ * bucket (expected picks per expert, T * k / (E_r + E_z)), then in H * I. */
+moe_status moe_tile_choice(const moe_config* cfg, int32_t T, int32_t* gemv_max_rows,
+                           int32_t* ffn_one_launch);
 
 /* Synchronises `stream`, reads and clears the device status word in `ws`.
  * MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_DEVICE_TIMEOUT (or MOE_ERR_CUDA). */

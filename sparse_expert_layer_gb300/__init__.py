@@ -39,6 +39,7 @@ SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 BIAS_NONE, BIAS_LOGIT, BIAS_SELECT = 0, 1, 2
 W_BF16, W8A8 = 0, 1
 COMBINE_DEFAULT, COMBINE_ORDERED, COMBINE_FUSED = 0, 1, 2
+FFN_LAUNCH_DEFAULT, FFN_LAUNCH_TWO, FFN_LAUNCH_ONE = 0, 1, 2
 
 KERNELS = ["router", "topk", "perm_count", "perm_scan", "perm_scatter", "perm_gather",
            "worklist", "gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down", "quant_h", "combine",
@@ -52,7 +53,8 @@ class MoeConfig(ctypes.Structure):
         "hidden", "inter", "n_routed", "n_zero", "top_k", "n_group", "topk_group", "per_group_k",
         "score", "renormalize")] + [("routed_scale", ctypes.c_float)] + [
         (n, ctypes.c_int32) for n in (
-            "bias_mode", "shared_inter", "wdtype", "out_fp32", "gemv_max_rows", "combine")]
+            "bias_mode", "shared_inter", "wdtype", "out_fp32", "gemv_max_rows", "combine",
+            "ffn_launch")]
 
 
 class MoeError(RuntimeError):
@@ -80,6 +82,7 @@ _SIGS = {
                           _P],
     "moe_check_device_status": [_P, _P],
     "moe_route_noalloc": [_C, _I, _P, _P, _P, _P, _P, _P],
+    "moe_tile_choice": [_C, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)],
     "moe_qgemm_s8_workspace_size": [_I, _I, _I, _I, ctypes.POINTER(_SZ)],
     "moe_qgemm_s8": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P],
     "moe_selftest_wait_timeout": [_P, ctypes.c_int64, _P],
@@ -118,7 +121,8 @@ def _check(status, what):
 
 
 def config_from_spec(spec: dict, out_fp32: bool = False, gemv_max_rows: int = 0,
-                     combine: int = COMBINE_DEFAULT) -> MoeConfig:
+                     combine: int = COMBINE_DEFAULT,
+                     ffn_launch: int = FFN_LAUNCH_DEFAULT) -> MoeConfig:
     """MoeConfig from a layer description dict (the keys used by the input generator)."""
     return MoeConfig(
         hidden=spec["hidden"], inter=spec["inter"], n_routed=spec["n_routed"],
@@ -131,7 +135,16 @@ def config_from_spec(spec: dict, out_fp32: bool = False, gemv_max_rows: int = 0,
             spec.get("bias_mode", "none")],
         shared_inter=spec.get("shared_inter", 0),
         wdtype=W8A8 if spec.get("wdtype", "bf16") == "w8a8" else W_BF16,
-        out_fp32=int(bool(out_fp32)), gemv_max_rows=int(gemv_max_rows), combine=int(combine))
+        out_fp32=int(bool(out_fp32)), gemv_max_rows=int(gemv_max_rows), combine=int(combine),
+        ffn_launch=int(ffn_launch))
+
+
+def moe_tile_choice(cfg: MoeConfig, T: int):
+    """(GEMV switch point, one-launch FFN) the library picks for (cfg, T)."""
+    g, o = _I(0), _I(0)
+    _check(lib.moe_tile_choice(ctypes.byref(cfg), T, ctypes.byref(g), ctypes.byref(o)),
+           "moe_tile_choice")
+    return g.value, bool(o.value)
 
 
 def moe_workspace_size(cfg: MoeConfig, T: int) -> int:
@@ -242,6 +255,21 @@ def _ws_bytes(ws):
     return ws.numel() * ws.element_size()
 
 
+def layer_scales(weights: dict):
+    """(s_gate, s_up, s_down) as moe_layer_forward takes them: the routed
+    experts' per-channel scales, followed (W8A8 with a shared expert) by the
+    shared expert's ('s_shared_gate' / '_up' / '_down')."""
+    out = []
+    for n in ("gate", "up", "down"):
+        s = weights.get("s_" + n)
+        sh = weights.get("s_shared_" + n)
+        if s is not None and sh is not None:
+            import torch
+            s = torch.cat([s.reshape(-1), sh.reshape(-1)])
+        out.append(s)
+    return tuple(out)
+
+
 class MoeLayer:
     """Convenience holder: config + device weights + workspace for a fixed T."""
 
@@ -249,13 +277,13 @@ class MoeLayer:
                  device="cuda"):
         self.cfg, self.T = cfg, T
         self.w = weights
+        self.scales = layer_scales(weights)
         self.w_router, self.bias = w_router, bias
         self.ws = workspace(cfg, T, device)
 
     def forward(self, x, out, stream=None):
         w = self.w
         moe_layer_forward(self.cfg, x.shape[0], x, self.w_router, self.bias, w.get("w_gate"),
-                          w.get("w_up"), w.get("w_down"), w.get("s_gate"), w.get("s_up"),
-                          w.get("s_down"), w.get("shared_gate"), w.get("shared_up"),
-                          w.get("shared_down"), out, self.ws, stream)
+                          w.get("w_up"), w.get("w_down"), *self.scales, w.get("shared_gate"),
+                          w.get("shared_up"), w.get("shared_down"), out, self.ws, stream)
         return out

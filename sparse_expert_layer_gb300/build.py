@@ -21,7 +21,7 @@ SOURCES = ["abi.cu", "route.cu", "permute.cu", "gemv.cu", "gemm_tc.cu", "w8a8.cu
            "route_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
-         "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
+         "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC, "-I", BUILD]
 
 
 def _nvcc() -> str:
@@ -31,11 +31,34 @@ def _nvcc() -> str:
     return cand
 
 
+TABLE_JSON = os.path.join(HERE, "tuning", "tile_table.json")
+TABLE_INC = os.path.join(BUILD, "tile_table.inc")
+
+
 def _deps():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     files.append(os.path.join(INCLUDE, "moe.h"))
     files.append(os.path.abspath(__file__))
+    files.append(TABLE_JSON)
     return files
+
+
+def write_table_inc(path: str = TABLE_INC) -> None:
+    """tuning/tile_table.json -> a C table compiled into the library."""
+    import json
+
+    t = json.load(open(TABLE_JSON))
+    wd = {"bf16": 0, "w8a8": 1}
+    rows = [f"    {{{wd[e['wdtype']]}, {int(e['hidden'])}, {int(e['inter'])}, {int(e['bucket'])}, "
+            f"{int(e['gemv_max'])}, {int(e['one_launch'])}}}," for e in t["entries"]]
+    b = ", ".join(str(int(v)) for v in t["buckets"])
+    text = ("// Generated from tuning/tile_table.json by build.py; do not edit.\n"
+            f"static const int kTileBuckets[] = {{{b}}};\n"
+            "static const TileEntry kTileTable[] = {\n" + "\n".join(rows) + "\n};\n")
+    tmp = path + f".tmp{os.getpid()}"
+    with open(tmp, "w") as f:
+        f.write(text)
+    os.replace(tmp, path)
 
 
 def _newest(paths):
@@ -49,6 +72,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         return LIB
     nvcc = _nvcc()
     objs = []
+    write_table_inc()
 
     def compile_one(src):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))

@@ -104,21 +104,65 @@ moe_status check_cfg(const moe_config* c, int32_t T) {
     // fit int32 (K <= 131071); no shared expert in this mode.
     if (c->hidden % 16 || (c->n_routed > 0 && c->inter % 16)) return MOE_ERR_INVALID_ARG;
     if (c->hidden > 131071 || c->inter > 131071) return MOE_ERR_UNSUPPORTED;
-    if (c->shared_inter > 0) return MOE_ERR_UNSUPPORTED;
+    // the shared expert is int8 like the routed ones: its K (I_s) in 16-byte rows
+    if (c->shared_inter % 16 || c->shared_inter > 131071) return MOE_ERR_INVALID_ARG;
+    if (c->shared_inter > 0 && c->n_routed == 0) return MOE_ERR_UNSUPPORTED;
   }
   if (c->out_fp32 != 0 && c->out_fp32 != 1) return MOE_ERR_INVALID_ARG;
   if (c->combine < MOE_COMBINE_DEFAULT || c->combine > MOE_COMBINE_FUSED)
+    return MOE_ERR_INVALID_ARG;
+  if (c->ffn_launch < MOE_FFN_LAUNCH_DEFAULT || c->ffn_launch > MOE_FFN_LAUNCH_ONE)
     return MOE_ERR_INVALID_ARG;
   // work-list chunk indices are 16-bit: at most 65535 chunks of 128 rows per unit
   if ((long long)T * c->top_k > (1LL << 30) || T > 65535 * kTcMaxN) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
+// ------------------------------------------------------ tile parameters --
+// The grouped FFN's tiling choices come from a table measured offline on GB300
+// (tuning/tile_table.json, compiled in): the history-based tiling choice of the
+// Pangu Pro MoE disclosure, section SwiftGMM.  It is keyed by weight type, H, I
+// and the load bucket of the expected picks per expert, T * k / (E_r + E_z);
+// the entry of the same weight type nearest in bucket, then in H * I, applies.
+struct TileEntry {
+  int wdtype, hidden, inter, bucket, gemv_max, one_launch;
+};
+#include "tile_table.inc"
+
+int load_bucket(const moe_config& c, int T) {
+  const double m = (double)T * c.top_k / (double)(c.n_routed + c.n_zero);
+  int b = 0;
+  for (int v : kTileBuckets) {
+    if (m < v) return b;
+    ++b;
+  }
+  return b;
+}
+
+const TileEntry* tile_entry(const moe_config& c, int T) {
+  const int b = load_bucket(c, T);
+  const double hi = (double)c.hidden * (c.inter > 0 ? c.inter : 1);
+  const TileEntry* best = nullptr;
+  double best_d = 0.0;
+  for (const TileEntry& e : kTileTable) {
+    if (e.wdtype != c.wdtype) continue;
+    const double d = 1000.0 * abs(e.bucket - b) + fabs(log2(hi / ((double)e.hidden * e.inter)));
+    if (!best || d < best_d) {
+      best = &e;
+      best_d = d;
+    }
+  }
+  return best;
+}
+
 // Experts (and the shared expert) with at most this many rows stream through
-// the GEMV path; the others run on tensor-core tiles.
-int effective_gemv_max(const moe_config& c) {
+// the GEMV path; the others run on tensor-core tiles.  gemv_max_rows > 0 sets
+// the switch point, < 0 turns the GEMV path off, 0 takes the table's.
+int effective_gemv_max(const moe_config& c, int T) {
   if (c.gemv_max_rows > 0) return c.gemv_max_rows;
   if (c.gemv_max_rows < 0) return 0;
+  const TileEntry* e = tile_entry(c, T);
+  if (e) return e->gemv_max;
   return c.wdtype == MOE_W8A8 ? kDefaultGemvMaxRowsW8 : kDefaultGemvMaxRows;
 }
 // Whether moe_layer_forward adds the expert outputs into the tokens' fp32
@@ -134,19 +178,14 @@ bool fused_combine(const moe_config& c) {
 
 // Whether the bf16 grouped FFN runs its tensor-core gate/up and down passes as
 // one persistent launch (down tiles wait for their task's gate/up tiles, which
-// fills the gate/up pass's last partial wave) instead of two.  MOE_FFN_ONE_LAUNCH
-// =0 or =1 in the environment (read once) overrides the choice.
+// fills the gate/up pass's last partial wave) instead of two: cfg.ffn_launch,
+// or the table's choice when it is MOE_FFN_LAUNCH_DEFAULT.
 bool ffn_one_launch(const moe_config& c, int T) {
-  static const int env = [] {
-    const char* v = getenv("MOE_FFN_ONE_LAUNCH");
-    if (v && v[0] == '0' && v[1] == 0) return 0;
-    if (v && v[0] == '1' && v[1] == 0) return 1;
-    return -1;
-  }();
-  (void)T;
-  (void)c;
-  if (env >= 0) return env == 1;
-  return false;
+  if (c.wdtype != MOE_W_BF16) return false;
+  if (c.ffn_launch == MOE_FFN_LAUNCH_TWO) return false;
+  if (c.ffn_launch == MOE_FFN_LAUNCH_ONE) return true;
+  const TileEntry* e = tile_entry(c, T);
+  return e ? e->one_launch != 0 : true;
 }
 
 // The GEMV launches are skipped when no unit can take that path.
@@ -174,6 +213,11 @@ struct Layout {
   // its codes/scales, and the guard-failure lists of the two passes
   size_t x16, xn2, h32, hq16, hsc, hn2, redo_gu, redo_dn;
   size_t x8, h8;  // int8 codes for the W8A8 streaming path (only when it may run)
+  // W8A8 shared expert: the tokens' codes (one row per token), its fp32 h and
+  // codes, and a work list and guard-failure lists of its own
+  size_t xs16, xsn2, xss, hs32, hsq16, hssc, hsn2;
+  size_t swl_tasks, swl_gu, swl_dn, swl_counts, sredo_gu, sredo_dn;
+  int swl_cap, sredo_cap;
   int redo_cap;
   size_t total;
   int splits, nblk, wl_cap;
@@ -248,9 +292,26 @@ Layout make_layout(const moe_config& c, int T) {
     L.hn2 = take(R * 4);
     L.redo_gu = take((size_t)(1 + L.redo_cap) * 4);
     L.redo_dn = take((size_t)(1 + L.redo_cap) * 4);
-    const bool gemv = gemv_possible(effective_gemv_max(c));
+    const bool gemv = gemv_possible(effective_gemv_max(c, T));
     L.x8 = take(gemv ? R * H : 0);
     L.h8 = take(gemv ? R * I : 0);
+    if (Is > 0) {
+      L.swl_cap = (int)(4 + ((size_t)T + kW8MaxN - 1) / kW8MaxN);
+      L.sredo_cap = L.swl_cap * 2 * (int)((std::max(Is, H) + 2 * kTcM - 1) / (2 * kTcM));
+      L.xs16 = take((size_t)T * H * 2);
+      L.xsn2 = take((size_t)T * 4);
+      L.xss = take((size_t)T * 4);
+      L.hs32 = take((size_t)T * Is * 4);
+      L.hsq16 = take((size_t)T * Is * 2);
+      L.hssc = take((size_t)T * 4);
+      L.hsn2 = take((size_t)T * 4);
+      L.swl_tasks = take((size_t)L.swl_cap * sizeof(FfnTask));
+      L.swl_gu = take((size_t)L.swl_cap * 4);
+      L.swl_dn = take((size_t)L.swl_cap * 4);
+      L.swl_counts = take(kWlCount * 4);
+      L.sredo_gu = take((size_t)(1 + L.sredo_cap) * 4);
+      L.sredo_dn = take((size_t)(1 + L.sredo_cap) * 4);
+    }
   }
   L.total = off;
   return L;
@@ -310,12 +371,12 @@ moe_status run_route(const Launch& ln, const moe_config& c, int T, const Layout&
     if (!launch_tc_router(ln, c, T, x, split, at<FfnTask>(ws, L.rtasks), at<int32_t>(ws, L.rstart),
                           at<int32_t>(ws, L.rcounts), logits))
       return MOE_ERR_CUDA;
+    launch_topk_only(ln, c, T, logits, bias, ids, w);
   } else {
     float* partial = at<float>(ws, L.partial);
     int* counters = at<int>(ws, L.status + 256);
-    launch_router(ln, c, T, x, w_router, partial, L.splits, logits, counters);
+    launch_route(ln, c, T, x, w_router, bias, partial, L.splits, logits, counters, ids, w);
   }
-  launch_topk(ln, c, T, logits, bias, ids, w);
   return MOE_OK;
 }
 
@@ -326,11 +387,11 @@ struct WlPlan {
   moe_config cw;
   int gemv_max, chunk, tc_chunk;
 };
-WlPlan wl_plan(const moe_config& c, bool shared_weights) {
+WlPlan wl_plan(const moe_config& c, int T, bool shared_weights) {
   WlPlan p;
   p.cw = c;
   if (!shared_weights || c.wdtype == MOE_W8A8) p.cw.shared_inter = 0;
-  p.gemv_max = effective_gemv_max(c);
+  p.gemv_max = effective_gemv_max(c, T);
   p.chunk = gemv_chunk(p.gemv_max);
   p.tc_chunk = c.wdtype == MOE_W8A8 ? kW8MaxN : kTcMaxN;
   return p;
@@ -346,10 +407,24 @@ bool run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, 
   bool built = false;
   if (sort_small_fits(T, E)) {
     const WorkList wl = worklist_view(ws, L);
+    // small bf16 layers: the sort CTA also gathers the rows
+    const size_t gather_bytes = (size_t)T * c.top_k * c.hidden * 2 + (size_t)T * c.hidden * 4;
+    SmallGather g{};
+    const bool small = x_perm && c.wdtype == MOE_W_BF16 && gather_bytes <= kSmallGatherBytes &&
+                       folds_enabled();
+    if (small) {
+      g.x = static_cast<const uint16_t*>(x);
+      g.x_perm = static_cast<uint16_t*>(x_perm);
+      g.w = w;
+      g.acc = acc;
+      g.H = c.hidden;
+      g.E_r = c.n_routed;
+    }
     launch_sort_small(ln, plan ? plan->cw : c, T, ids, counts, offsets, s2e, e2s,
                       plan ? &wl : nullptr, plan ? plan->gemv_max : 0, plan ? plan->chunk : 1,
-                      plan ? plan->tc_chunk : kTcMaxN);
+                      plan ? plan->tc_chunk : kTcMaxN, small ? &g : nullptr);
     built = plan != nullptr;
+    if (small) return built;
   } else {
     int32_t* bc = at<int32_t>(ws, L.bc);
     launch_perm_count(ln, T, c.top_k, E, ids, bc);
@@ -365,10 +440,11 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
                    const int32_t* offsets, const void* x_perm, const void* w_gate,
                    const void* w_up, const void* w_down, float* y_perm, const void* x,
                    const void* sg, const void* su, const void* sd, float* y_shared,
-                   bool wl_built, const ScatterAdd& sc = ScatterAdd{}) {
+                   bool wl_built, const ScatterAdd& sc = ScatterAdd{},
+                   const SmallFinalize& fin = SmallFinalize{}) {
   const WorkList wl = worklist_view(ws, L);
   const bool shared = c.shared_inter > 0 && sg != nullptr;
-  const WlPlan plan = wl_plan(c, shared);
+  const WlPlan plan = wl_plan(c, T, shared);
   const int gemv_max = plan.gemv_max;
   const int chunk = plan.chunk;
   if (!wl_built) launch_worklist(ln, plan.cw, T, offsets, wl, gemv_max, chunk, plan.tc_chunk);
@@ -459,6 +535,7 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   td.Ks = c.shared_inter;
   td.N = td.Ns = c.hidden;
   td.sc = sc;
+  td.fin = fin;
   if (c.n_routed > 0) {
     const bool ok = one_launch ? launch_tc_ffn(ln, tg, td, wl.gu_done) : launch_tc_down(ln, td);
     if (!ok) return MOE_ERR_CUDA;
@@ -477,7 +554,7 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
                         const float* s_gate, const float* s_up, const float* s_down,
                         float* y_perm, bool wl_built, const ScatterAdd& sc = ScatterAdd{}) {
   const WorkList wl = worklist_view(ws, L);
-  const WlPlan plan = wl_plan(c, false);
+  const WlPlan plan = wl_plan(c, T, false);
   const int gemv_max = plan.gemv_max;
   const bool gemv = gemv_possible(gemv_max);
   if (!wl_built)
@@ -577,6 +654,82 @@ moe_status run_ffn_w8a8(const Launch& ln, const moe_config& c, int T, const Layo
   return MOE_OK;
 }
 
+// The W8A8 shared expert: a one-expert grouped FFN over every token, on the
+// tokens' own codes (written by the quantising gather), with its weights after
+// the routed experts' scales in s_gate / s_up / s_down.  Its outputs add into
+// the tokens' accumulators at weight 1 (fused combine) or fill y_shared.
+moe_status run_shared_w8a8(const Launch& ln, const moe_config& c, int T, const Layout& L,
+                           void* ws, const void* sg, const void* su, const void* sd,
+                           const float* s_gate, const float* s_up, const float* s_down,
+                           float* y_shared, const ScatterAdd& sc) {
+  const int Is = c.shared_inter;
+  WorkList wl{};
+  wl.gemv_tasks = at<FfnTask>(ws, L.swl_tasks);  // no streaming tasks: shares the array
+  wl.gemv_start_gu = at<int32_t>(ws, L.swl_gu);
+  wl.gemv_start_dn = at<int32_t>(ws, L.swl_dn);
+  wl.tc_tasks = at<FfnTask>(ws, L.swl_tasks);
+  wl.tc_start_gu = at<int32_t>(ws, L.swl_gu);
+  wl.tc_start_dn = at<int32_t>(ws, L.swl_dn);
+  wl.counts = at<int32_t>(ws, L.swl_counts);
+  wl.capacity = L.swl_cap;
+  wl.redo_gu = at<int32_t>(ws, L.sredo_gu);
+  wl.redo_dn = at<int32_t>(ws, L.sredo_dn);
+  wl.gu_done = nullptr;
+  // one unit: the shared expert over all T tokens, in 256-row two-SM tiles
+  moe_config cs = c;
+  cs.n_routed = 0;
+  cs.n_zero = 1;
+  launch_worklist(ln, cs, T, nullptr, wl, 0, 1, kW8MaxN);
+
+  W8Pass g{};
+  g.mode = kW8GateUp;
+  g.tasks = wl.tc_tasks;
+  g.tile_start = wl.tc_start_gu;
+  g.counts = wl.counts;
+  g.task_slot = kWlTcTasks;
+  g.tile_slot = kWlTcTilesGU;
+  g.sched_slot = kWlSchedGU;
+  g.w0 = sg;
+  g.w1 = su;
+  g.n_experts = 1;
+  g.s0 = s_gate + (size_t)c.n_routed * c.inter;
+  g.s1 = s_up + (size_t)c.n_routed * c.inter;
+  g.act = at<uint16_t>(ws, L.xs16);
+  g.act_rows = T;
+  g.row_norm2 = at<int32_t>(ws, L.xsn2);
+  g.row_scale = at<float>(ws, L.xss);
+  g.out_f32 = at<float>(ws, L.hs32);
+  g.redo = wl.redo_gu;
+  g.redo_cap = L.sredo_cap;
+  g.K = c.hidden;
+  g.N = Is;
+  if (!launch_w8a8(ln, g)) return MOE_ERR_CUDA;
+
+  launch_quant_rows(ln, at<float>(ws, L.hs32), at<uint16_t>(ws, L.hsq16), nullptr,
+                    at<float>(ws, L.hssc), at<int32_t>(ws, L.hsn2), T, Is, nullptr, 0, 0);
+
+  W8Pass d = g;
+  d.mode = kW8Down;
+  d.tile_start = wl.tc_start_dn;
+  d.tile_slot = kWlTcTilesDN;
+  d.sched_slot = kWlSchedDN;
+  d.w0 = sd;
+  d.w1 = nullptr;
+  d.s0 = s_down + (size_t)c.n_routed * c.hidden;
+  d.s1 = nullptr;
+  d.act = at<uint16_t>(ws, L.hsq16);
+  d.row_norm2 = at<int32_t>(ws, L.hsn2);
+  d.row_scale = at<float>(ws, L.hssc);
+  d.out_f32 = y_shared;
+  d.redo = wl.redo_dn;
+  d.K = Is;
+  d.N = c.hidden;
+  d.sc = sc;
+  d.sc.s2e = nullptr;  // the shared expert's rows are the tokens, at weight 1
+  if (!launch_w8a8(ln, d)) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 }  // namespace
 
 void set_smem_attr_once(const void* func, int bytes, int slot) {
@@ -595,6 +748,14 @@ moe_status launch_status_take() { return finish(); }
 
 void launch_note(cudaError_t e) {
   if (e != cudaSuccess && t_launch_error == cudaSuccess) t_launch_error = e;
+}
+
+bool folds_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_FOLDS");
+    return !(v && v[0] == '0' && v[1] == 0);
+  }();
+  return on;
 }
 
 bool pdl_enabled() {
@@ -809,24 +970,47 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
   }
   // the FFN's work list is built with the re-sort when that runs as one CTA
   const bool ffn = w8 ? c.n_routed > 0 : (c.n_routed > 0 || c.shared_inter > 0);
-  const WlPlan plan = wl_plan(c, !w8 && c.shared_inter > 0);
+  const WlPlan plan = wl_plan(c, T, !w8 && c.shared_inter > 0);
   const bool wl_built =
       run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale,
                   ffn ? &plan : nullptr, w, acc);
-  if (w8 && c.n_routed > 0)
-    launch_quant_gather(ln, c, T, x, ids, e2s, offsets, plan.gemv_max, at<uint16_t>(ws, L.x16),
-                        gemv_possible(plan.gemv_max) ? at<int8_t>(ws, L.x8) : nullptr, x_scale,
-                        at<int32_t>(ws, L.xn2), w, acc);
+  const bool w8_shared = w8 && c.shared_inter > 0;
+  if (w8 && c.n_routed > 0) {
+    QuantGatherOut qo{};
+    qo.x16 = at<uint16_t>(ws, L.x16);
+    qo.x8 = gemv_possible(plan.gemv_max) ? at<int8_t>(ws, L.x8) : nullptr;
+    qo.scale = x_scale;
+    qo.norm2 = at<int32_t>(ws, L.xn2);
+    if (w8_shared) {
+      qo.tok16 = at<uint16_t>(ws, L.xs16);
+      qo.tok_scale = at<float>(ws, L.xss);
+      qo.tok_norm2 = at<int32_t>(ws, L.xsn2);
+    }
+    launch_quant_gather(ln, c, T, x, ids, e2s, offsets, plan.gemv_max, qo, w, acc);
+  }
+  // small bf16 layers: the down pass's last CTA rounds the output itself
+  SmallFinalize fin{};
+  if (fused && !c.out_fp32 && !w8 && c.n_routed > 0 &&
+      (long long)T * c.hidden <= kSmallFinalizeElems && folds_enabled()) {
+    fin.ctr = reinterpret_cast<int*>(static_cast<char*>(ws) + L.status + kFinalizeCtrOffset);
+    fin.acc = acc;
+    fin.out = static_cast<uint16_t*>(out);
+    fin.n8 = T * c.hidden / 8;
+  }
   moe_status fs = MOE_OK;
-  if (w8 && c.n_routed > 0)
+  if (w8 && c.n_routed > 0) {
     fs = run_ffn_w8a8(ln, c, T, L, ws, offsets, x_perm, x_scale, w_gate, w_up, w_down, s_gate,
                       s_up, s_down, y, wl_built, sc);
-  else if (!w8 && (c.n_routed > 0 || c.shared_inter > 0))
+    if (fs == MOE_OK && w8_shared)
+      fs = run_shared_w8a8(ln, c, T, L, ws, ws_gate, ws_up, ws_down, s_gate, s_up, s_down, y_s,
+                           sc);
+  } else if (!w8 && (c.n_routed > 0 || c.shared_inter > 0)) {
     fs = run_ffn(ln, c, T, L, ws, offsets, x_perm, w_gate, w_up, w_down, y, x, ws_gate, ws_up,
-                 ws_down, y_s, wl_built, sc);
+                 ws_down, y_s, wl_built, sc, fin);
+  }
   if (!fused)
     launch_combine(ln, c, T, y, e2s, ids, w, x, y_s, out);
-  else if (!c.out_fp32)
+  else if (!c.out_fp32 && !fin.ctr)
     launch_finalize(ln, T, c.hidden, acc, out);
   const moe_status f = finish();
   return fs != MOE_OK ? fs : f;
@@ -941,6 +1125,16 @@ moe_status moe_qgemm_s8(int32_t n_experts, int32_t K, int32_t N, int32_t R, cons
   const bool ok = launch_w8a8(ln, p);
   const moe_status f = finish();
   return ok ? f : MOE_ERR_CUDA;
+}
+
+moe_status moe_tile_choice(const moe_config* cfg, int32_t T, int32_t* gemv_max_rows,
+                           int32_t* one_launch) {
+  const moe_status s = check_cfg(cfg, T);
+  if (s != MOE_OK) return s;
+  if (!gemv_max_rows || !one_launch) return MOE_ERR_INVALID_ARG;
+  *gemv_max_rows = effective_gemv_max(*cfg, T);
+  *one_launch = ffn_one_launch(*cfg, T) ? 1 : 0;
+  return MOE_OK;
 }
 
 moe_status moe_check_device_status(void* ws, moe_stream_t stream) {

@@ -90,7 +90,41 @@ struct TcArgs {
   int tile_slot_dn;
   int* gu_done;
   int gu_tiles, gu_tiles_shared;  // gate/up channel tiles of a routed / shared task
+  SmallFinalize fin;
 };
+
+// Small layers: the last CTA of the down pass to finish rounds the tokens'
+// accumulators to bf16.  Every thread fences its own adds before the CTA
+// counts itself done, so the last CTA sees all of them.
+__device__ __forceinline__ void finalize_if_last(const SmallFinalize& f) {
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(f.ctr, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < f.n8; i += blockDim.x) {
+    const float4 a0 = __ldcg(reinterpret_cast<const float4*>(f.acc) + 2 * i);
+    const float4 a1 = __ldcg(reinterpret_cast<const float4*>(f.acc) + 2 * i + 1);
+    const float v[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    uint32_t q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      q[j] = (uint32_t)f_to_bf16(v[2 * j]) | ((uint32_t)f_to_bf16(v[2 * j + 1]) << 16);
+    reinterpret_cast<uint4*>(f.out)[i] = make_uint4(q[0], q[1], q[2], q[3]);
+  }
+  if (threadIdx.x == 0) *f.ctr = 0;  // ready for the next call
+}
+
+// Single-launch FFN: a down tile of at most one 64-row activation box carries
+// two K steps per stage, each [16 KB weight tile | 8 KB activation box].
+constexpr int kPackedStep = kATileBytes + kBoxBytes;
+template <int MODE>
+__device__ __forceinline__ bool packed_down(bool gu, int n) {
+  return MODE == kTcFfn && !gu && n <= kBoxRows;
+}
+static_assert(2 * kPackedStep <= Geom<kTcFfn>::kStageBytes, "two packed K steps fill a stage");
 
 __device__ __forceinline__ QTile decode_tile(const TcArgs& a, int tile, int ntasks, int gu,
                                              const int32_t* start) {
@@ -119,7 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntasks = a.counts[a.task_slot];
   const int ntiles_first = a.counts[a.tile_slot];
   const int ntiles = ntiles_first + (FFN ? a.counts[a.tile_slot_dn] : 0);
-  if (ntiles <= 0 || (int)blockIdx.x >= ntiles) return;  // uniform across the CTA
+  if (ntiles <= 0 || (int)blockIdx.x >= ntiles) {  // uniform across the CTA
+    if (MODE != kTcGateUp && a.fin.ctr) finalize_if_last(a.fin);
+    return;
+  }
 
   // 1024-byte aligned ring (128-byte swizzle atoms), barriers after it
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -201,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (t.tile < 0) break;
-      const bool gu = t.gu != 0;
+      const bool gu = MODE == kTcGateUp || (FFN && t.gu != 0);
       const CUtensorMap* A0;
       const CUtensorMap* A1 = t.shared ? &maps.sa1 : &maps.a1;
       const CUtensorMap* B;
@@ -223,9 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         K = t.shared ? a.Ks : a.K;
       }
       const int nb = (t.n + kBoxRows - 1) / kBoxRows;
-      const uint32_t bytes = (uint32_t)((gu ? 2 : 1) * kATileBytes + nb * kBoxBytes);
       const int nks = (K + kBK - 1) / kBK;
-      for (int ks = 0; ks < nks; ++ks) {
+      // single-launch FFN, down tile of <= 64 rows: two K steps per stage (each a
+      // 16 KB weight tile and an 8 KB activation box), so the down tiles keep as
+      // many weight bytes in flight as the gate/up tiles
+      const int sub = packed_down<MODE>(gu, t.n) ? 2 : 1;
+      for (int ks = 0; ks < nks; ks += sub) {
         if (*abort_flag) {
           ok = false;
           break;
@@ -239,8 +279,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t bar = smem_u32(&full[stage]);
-        mbar_arrive_expect_tx(bar, bytes);
         uint8_t* st = smem + (size_t)stage * G::kStageBytes;
+        if (sub == 2) {
+          const int nsub = min(2, nks - ks);
+          mbar_arrive_expect_tx(bar, (uint32_t)(nsub * (kATileBytes + kBoxBytes)));
+          for (int u = 0; u < nsub; ++u) {
+            uint8_t* su = st + u * kPackedStep;
+            tma_load_3d(smem_u32(su), A0, (ks + u) * kBK, t.ct * kTcM, t.e, bar, pol_w);
+            tma_load_3d(smem_u32(su + kATileBytes), B, (ks + u) * kBK, t.row0, 0, bar, pol_x);
+          }
+          ++iter;
+          continue;
+        }
+        mbar_arrive_expect_tx(bar, (uint32_t)((gu ? 2 : 1) * kATileBytes + nb * kBoxBytes));
         tma_load_3d(smem_u32(st), A0, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
         if (gu) tma_load_3d(smem_u32(st + kATileBytes), A1, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
         uint8_t* sb = st + G::kNA * kATileBytes;
@@ -265,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (t.tile < 0) break;
-      const bool gu = t.gu != 0;
+      const bool gu = MODE == kTcGateUp || (FFN && t.gu != 0);
       const uint32_t buf = local & 1u, use = local >> 1;
       if (!mbar_wait(smem_u32(&acc_empty[buf]), (use & 1u) ^ 1u)) {
         raise_status(a.status, kStTimeout, kind);
@@ -279,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t d1 = d0 + kTcMaxN;
       const int K = (FFN && !gu) ? (t.shared ? a.Ns : a.N) : (t.shared ? a.Ks : a.K);
       const int nks = (K + kBK - 1) / kBK;
-      for (int ks = 0; ks < nks; ++ks) {
+      const int sub = packed_down<MODE>(gu, t.n) ? 2 : 1;
+      for (int ks = 0; ks < nks; ks += sub) {
         if (*abort_flag) {
           ok = false;
           break;
@@ -294,6 +346,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + (size_t)stage * G::kStageBytes);
+        if (sub == 2) {
+          const int nsub = min(2, nks - ks);
+          for (int u = 0; u < nsub; ++u) {
+            const uint32_t su = sa + u * kPackedStep;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint32_t acc = (ks + u > 0 || k > 0) ? 1u : 0u;
+              tc_mma_bf16(d0, sdesc_sw128(su + k * 32), sdesc_sw128(su + kATileBytes + k * 32),
+                          idesc, acc);
+            }
+          }
+          tc_commit(smem_u32(&empty[stage]));
+          ++iter;
+          continue;
+        }
         const uint32_t sb = sa + G::kNA * kATileBytes;
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k) {
@@ -324,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (t.tile < 0 || warp_flag(abort_flag)) break;
-      const bool gu = t.gu != 0;
+      const bool gu = MODE == kTcGateUp || (FFN && t.gu != 0);
       // output channels of this tile's pass: gate/up -> N (I or I_s); down -> H
       const int tN = (FFN && !gu) ? a.K : (t.shared ? a.Ns : a.N);
       const uint32_t buf = local & 1u, use = local >> 1;
@@ -388,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, G::kTmemCols);
   }
+  if (MODE != kTcGateUp && a.fin.ctr) finalize_if_last(a.fin);
 }
 
 // ------------------------------------------------------------ host side --
@@ -461,6 +529,7 @@ TcArgs make_args(const Launch& L, const TcPass& p) {
   a.sched = const_cast<int32_t*>(p.counts) + p.sched_slot;
   a.status = L.status;
   a.sc = p.sc;
+  a.fin = p.fin;
   return a;
 }
 
@@ -518,6 +587,7 @@ bool launch_tc_ffn(const Launch& L, const TcPass& gu, const TcPass& dn, int32_t*
   a.out_y = dn.out_y;
   a.sout_y = dn.sout_y;
   a.sc = dn.sc;
+  a.fin = dn.fin;
   a.tile_start_dn = dn.tile_start;
   a.tile_slot_dn = dn.tile_slot;
   a.gu_done = gu_done;

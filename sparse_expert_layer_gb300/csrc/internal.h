@@ -50,13 +50,14 @@ __device__ __forceinline__ void tc_tile_of(const FfnTask* tasks, const int32_t* 
 // itself and adds y at weight 1.
 struct ScatterAdd {
   float* acc;          // [T, H] fp32
-  const int32_t* s2e;  // sorted position -> expanded index t * k + j
+  const int32_t* s2e;  // sorted position -> expanded index t * k + j (nullptr: the
+                       // rows are the tokens themselves, at weight 1)
   const float* w;      // [T * k] routing weights
   int k;
 };
 __device__ __forceinline__ void scatter_target(const ScatterAdd& s, int row, bool shared,
                                                int* tok, float* wt) {
-  if (shared) {
+  if (shared || s.s2e == nullptr) {
     *tok = row;
     *wt = 1.f;
   } else {
@@ -128,16 +129,21 @@ int router_splits(const moe_config& c, int T, int num_sms);
 // The CUDA-core router's split-K count as every entry point sizes its scratch
 // (the split aims at about two CTAs on each of 152 SMs).
 int router_splits_default(const moe_config& c, int T);
-// Whether launch_router runs the decode router on tensor cores for (c, T): H a
+// Whether launch_route runs the decode router on tensor cores for (c, T): H a
 // multiple of 64, enough parallel work, and MOE_ROUTER_TC not set to 0.  That
 // router needs neither the split-K partials nor the tile counters.  (If its
-// tensor maps cannot be encoded, launch_router falls back to the CUDA-core
+// tensor maps cannot be encoded, launch_route falls back to the CUDA-core
 // router with the split count it was given.)
 bool router_tc_decode_chosen(const moe_config& c, int T);
-void launch_router(const Launch& L, const moe_config& c, int T, const void* x, const float* w_r,
-                   float* partial, int splits, float* logits, int* counters);
-void launch_topk(const Launch& L, const moe_config& c, int T, const float* logits,
-                 const float* bias, int32_t* ids, float* w);
+// Router matmul then top-k gating (one launch when the decode router on tensor
+// cores holds all experts in one tile and picks the top-k itself; logits are
+// then not written).
+void launch_route(const Launch& L, const moe_config& c, int T, const void* x, const float* w_r,
+                  const float* bias, float* partial, int splits, float* logits, int* counters,
+                  int32_t* ids, float* w);
+// Top-k gating of given logits.
+void launch_topk_only(const Launch& L, const moe_config& c, int T, const float* logits,
+                      const float* bias, int32_t* ids, float* w);
 // Large batches: the router as a tensor-core GEMM over the exact three-term
 // bf16 split of W_r ([E, 3H], written by launch_router_split).
 bool router_on_tensor_cores(const moe_config& c, int T);
@@ -161,9 +167,21 @@ void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t*
 constexpr int kSortSmallMaxT = 1024;
 constexpr int kSortSmallSmem = 96 * 1024;
 bool sort_small_fits(int T, int E);
+// The bf16 row gather (and the fused combine's accumulator start) done by the
+// one-CTA sort itself, for layers whose gathered rows and accumulators are
+// small (kSmallGatherBytes at most): one launch fewer.
+constexpr size_t kSmallGatherBytes = 256 * 1024;
+struct SmallGather {
+  const uint16_t* x;  // bf16 [T, H]
+  uint16_t* x_perm;   // bf16 [T * k, H] (nullptr: no gather)
+  const float* w;     // routing weights (fused combine), or nullptr
+  float* acc;         // the tokens' accumulators (fused combine), or nullptr
+  int H, E_r;
+};
 void launch_sort_small(const Launch& L, const moe_config& c, int T, const int32_t* ids,
                        int32_t* counts, int32_t* offsets, int32_t* s2e, int32_t* e2s,
-                       const WorkList* wl, int gemv_max_rows, int gemv_chunk, int tc_chunk);
+                       const WorkList* wl, int gemv_max_rows, int gemv_chunk, int tc_chunk,
+                       const SmallGather* gather = nullptr);
 
 // Grouped FFN, streaming path (gemv.cu)
 struct GemvPass {
@@ -212,6 +230,19 @@ struct GemvI8Pass {
 bool launch_gemv_i8_gate_up(const Launch& L, const GemvI8Pass& p);
 bool launch_gemv_i8_down(const Launch& L, const GemvI8Pass& p);
 
+// Small layers with the fused combine: the down pass's last CTA to finish
+// rounds the tokens' fp32 accumulators to the bf16 output (ctr != nullptr), in
+// place of the finalize launch.  ctr is a zero word of the workspace head; the
+// last CTA leaves it zero.
+constexpr int kSmallFinalizeElems = 64 * 1024;
+struct SmallFinalize {
+  int* ctr;
+  const float* acc;
+  uint16_t* out;
+  int n8;  // T * H / 8
+};
+constexpr size_t kFinalizeCtrOffset = 64;  // in the workspace's 256-byte status block
+
 // Grouped FFN, tensor-core path (gemm_tc.cu).  Returns false if a tensor map
 // could not be encoded (nothing launched).
 struct TcPass {
@@ -235,6 +266,7 @@ struct TcPass {
   int K, Ks, N, Ns;
   int b_kmod;              // > 0: activation K coordinate taken modulo b_kmod
   ScatterAdd sc;           // down pass: acc != nullptr adds into the tokens' rows
+  SmallFinalize fin;       // down pass of a small layer: the last CTA rounds the output
 };
 bool launch_tc_gate_up(const Launch& L, const TcPass& p);
 bool launch_tc_down(const Launch& L, const TcPass& p);
@@ -283,13 +315,22 @@ void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, in
 // squares to the sorted rows of its FFN-expert picks.  A row of an expert of at
 // most gemv_max rows (offsets give the loads) gets int8 codes in x8, any other
 // row integer-valued fp16 codes in x16; x8 nullptr sends every row to x16.
+struct QuantGatherOut {
+  uint16_t* x16;       // sorted rows, integer-valued fp16 codes
+  int8_t* x8;          // sorted rows of streamed experts, int8 codes (or nullptr)
+  float* scale;        // [R] per sorted row
+  int32_t* norm2;      // [R]
+  uint16_t* tok16;     // W8A8 shared expert: one fp16 code row per token (or nullptr)
+  float* tok_scale;    // [T]
+  int32_t* tok_norm2;  // [T]
+};
 void launch_quant_gather(const Launch& L, const moe_config& c, int T, const void* x,
                          const int32_t* ids, const int32_t* e2s, const int32_t* offsets,
-                         int gemv_max, uint16_t* x16, int8_t* x8, float* scale, int32_t* norm2,
-                         const float* w = nullptr, float* acc = nullptr);
-// The first offsets[n_experts] of R fp32 rows -> codes, by the same rule: int8
-// into dst8 for rows of experts of at most gemv_max rows, else fp16 into dst;
-// dst8 nullptr sends every row to dst.
+                         int gemv_max, const QuantGatherOut& o, const float* w = nullptr,
+                         float* acc = nullptr);
+// The first offsets[n_experts] of R fp32 rows (all R when offsets is nullptr)
+// -> codes, by the same rule: int8 into dst8 for rows of experts of at most
+// gemv_max rows, else fp16 into dst; dst8 nullptr sends every row to dst.
 void launch_quant_rows(const Launch& L, const float* src, uint16_t* dst, int8_t* dst8,
                        float* scale, int32_t* norm2, int R, int K, const int32_t* offsets,
                        int n_experts, int gemv_max);
@@ -346,7 +387,8 @@ enum {
   kAttrRouterTc,
   kAttrSortSmall,
   kAttrTcFfn,
-  kAttrSlots
+  kAttrW8DirectBase,                 // 3 slots: W8A8 modes, direct weight loads
+  kAttrSlots = kAttrW8DirectBase + 3
 };
 void set_smem_attr_once(const void* func, int bytes, int slot);
 
@@ -358,6 +400,11 @@ void launch_note(cudaError_t e);
 // Programmatic dependent launch of the library's kernels: on unless the
 // environment sets MOE_PDL=0 (read once).
 bool pdl_enabled();
+
+// Small-layer folds (router + top-k in one launch, re-sort + gather in one CTA,
+// the output rounded by the down pass's last CTA): on unless the environment
+// sets MOE_FOLDS=0 (read once).
+bool folds_enabled();
 
 // Launches a library kernel so that it may start while the previous kernel of
 // the stream is still running (the kernel waits, pdl_wait, before it touches

@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
 __global__ void __launch_bounds__(1024)
     sort_small_kernel(const int32_t* ids, int32_t* counts, int32_t* offsets, int32_t* s2e,
                       int32_t* e2s, int T, int k, int E, WlArgs wla, int build_wl,
-                      DevStatus* st) {
+                      DevStatus* st, SmallGather g) {
   pdl_enter();
   extern __shared__ uint32_t sm[];  // bitmap [E][W], then offsets [E + 1]
   __shared__ int sh[32];
@@ -381,6 +381,26 @@ __global__ void __launch_bounds__(1024)
     __syncthreads();
     build_worklist(wla, off, sh);
   }
+  if (g.x_perm) {
+    // small layers: the row gather (and the fused combine's accumulator rows)
+    // in the same CTA, in place of the gather launch
+    __syncthreads();
+    const int per_row = g.H / 8;
+    for (int idx = tid; idx < R * per_row; idx += blockDim.x) {
+      const int r = idx / per_row, i = idx % per_row;
+      const int e = ids[r];
+      const int p = e2s[r];
+      if ((unsigned)e >= (unsigned)g.E_r || p < 0) continue;
+      reinterpret_cast<uint4*>(g.x_perm + (size_t)p * g.H)[i] =
+          reinterpret_cast<const uint4*>(g.x + (size_t)(r / k) * g.H)[i];
+    }
+    if (g.acc)
+      for (int idx = tid; idx < T * per_row; idx += blockDim.x) {
+        const int t = idx / per_row;
+        zero_pick_init(ids, g.w, t, k, g.E_r, E, g.x + (size_t)t * g.H, g.acc + (size_t)t * g.H,
+                       g.H, idx % per_row, per_row);
+      }
+  }
 }
 
 WlArgs make_wl_args(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
@@ -404,7 +424,7 @@ WlArgs make_wl_args(const Launch& L, const moe_config& c, int T, const int32_t* 
   // W8A8 tensor-core tiles span 256 channels (two-SM tiles), bf16 ones 128
   const int tch = c.wdtype == MOE_W8A8 ? 2 * kTcM : kTcM;
   a.tiles_gu = (c.inter + tch - 1) / tch;
-  a.tiles_gu_shared = (c.shared_inter + kTcM - 1) / kTcM;
+  a.tiles_gu_shared = (c.shared_inter + tch - 1) / tch;
   a.tiles_dn = (c.hidden + tch - 1) / tch;
   a.status = L.status;
   return a;
@@ -422,15 +442,18 @@ bool sort_small_fits(int T, int E) {
 
 void launch_sort_small(const Launch& L, const moe_config& c, int T, const int32_t* ids,
                        int32_t* counts, int32_t* offsets, int32_t* s2e, int32_t* e2s,
-                       const WorkList* wl, int gemv_max_rows, int gemv_chunk, int tc_chunk) {
+                       const WorkList* wl, int gemv_max_rows, int gemv_chunk, int tc_chunk,
+                       const SmallGather* gather) {
   const int E = c.n_routed + c.n_zero;
   WlArgs a{};
   if (wl) a = make_wl_args(L, c, T, offsets, *wl, gemv_max_rows, gemv_chunk, tc_chunk);
   set_smem_attr_once(reinterpret_cast<const void*>(sort_small_kernel), kSortSmallSmem,
                      kAttrSortSmall);
   launch_begin(L, MOE_K_SORT);
+  SmallGather g{};
+  if (gather) g = *gather;
   launch_kernel(sort_small_kernel, 1, 1024, sort_small_smem(T, E), L.stream, ids, counts, offsets,
-                s2e, e2s, T, c.top_k, E, a, wl ? 1 : 0, L.status);
+                s2e, e2s, T, c.top_k, E, a, wl ? 1 : 0, L.status, g);
   launch_end(L, MOE_K_SORT);
 }
 

@@ -260,16 +260,12 @@ struct TopkArgs {
 
 constexpr int kTkBatch = 8;  // experts per lane whose logits are loaded together
 
-__global__ void topk_kernel(TopkArgs a) {
-  pdl_enter();
-  extern __shared__ float sm[];
-  const int warps = blockDim.x / 32;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int t = blockIdx.x * warps + warp;
-  if (t >= a.T) return;
+// Scores, group stage and top-k of token t, by one warp: row holds the token's
+// E logits (global or shared memory), sc a 3 * E float scratch of the warp.
+__device__ void topk_token(const TopkArgs& a, int t, const float* row, float* sc) {
+  const int lane = threadIdx.x % 32;
   const int E = a.E;
-  float* sc = sm + (size_t)warp * 3 * E;  // scores
-  float* sel = sc + E;                    // selection keys, -inf = not eligible
+  float* sel = sc + E;  // selection keys, -inf = not eligible
   float* tmp = sel + E;
 
   // logits and scores.  The global loads of kTkBatch experts per lane are
@@ -282,7 +278,7 @@ __global__ void topk_kernel(TopkArgs a) {
 #pragma unroll
     for (int b = 0; b < kTkBatch; ++b) {
       const int e = e0 + 32 * b;
-      l[b] = e < E ? a.logits[(size_t)t * E + e] : 0.f;
+      l[b] = e < E ? row[e] : 0.f;
       bv[b] = e < E && a.bias_mode != MOE_BIAS_NONE ? a.bias[e] : 0.f;
     }
 #pragma unroll
@@ -403,6 +399,16 @@ __global__ void topk_kernel(TopkArgs a) {
   }
 }
 
+__global__ void topk_kernel(TopkArgs a) {
+  pdl_enter();
+  extern __shared__ float sm[];
+  const int warps = blockDim.x / 32;
+  const int warp = threadIdx.x / 32;
+  const int t = blockIdx.x * warps + warp;
+  if (t >= a.T) return;
+  topk_token(a, t, a.logits + (size_t)t * a.E, sm + (size_t)warp * 3 * a.E);
+}
+
 // Exact three-term bf16 split of the fp32 router weights for the tensor-core
 // router: W1 = bf16(W), W2 = bf16(W - W1), W3 = bf16(W - W1 - W2).  Each
 // remainder is exact in fp32 and W1 + W2 + W3 == W, and bf16 x bf16 products
@@ -478,10 +484,13 @@ __device__ __forceinline__ void split3x2(float a, float b, uint32_t& p1, uint32_
   p3 = bf162_as_u32(__floats2bfloat162_rn(sa, sb));
 }
 
+// With fuse_topk (all experts in one 128-expert tile) each CTA also scores and
+// picks the top-k of the tokens it reduced, from shared memory, so no logits
+// go to global memory and no top-k launch follows.
 __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                      const __grid_constant__ CUtensorMap wmap, float* logits, int T, int E, int H,
-                     DevStatus* st) {
+                     DevStatus* st, const TopkArgs tk, int fuse_topk) {
   pdl_enter();
   extern __shared__ uint8_t rc_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -645,14 +654,21 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
     }
   }
   cluster_sync_all();  // every CTA's slice is in place
+  // fused top-k: the final logits of this CTA's 16 tokens, [token][expert], and
+  // a 3 * E float scratch per warp, in the (now idle) plane buffers
+  constexpr int kRcTokPerCta = kRcN / kRcSplits;
+  float* fin = reinterpret_cast<float*>(smem);
+  float* tk_scratch = fin + kRcTokPerCta * kRcM;
   {
-    // this CTA adds the eight slices, in rank order, for 16 of the tile's tokens
+    // this CTA adds the eight slices, in rank order, for 16 of the tile's tokens:
+    // tokens rank, rank + 8, rank + 16, ... (interleaved, so that a batch of at
+    // most 64 tokens spreads one token per warp over the cluster)
     const int el = tid % kRcM;
-    const int tb = rank * (kRcN / kRcSplits) + (tid / kRcM) * (kRcN / kRcSplits / 2);
+    const int tl0 = (tid / kRcM) * (kRcTokPerCta / 2);
     const uint32_t base = smem_u32(slice);
 #pragma unroll 1
-    for (int u = 0; u < kRcN / kRcSplits / 2; ++u) {
-      const int t = tb + u;
+    for (int u = 0; u < kRcTokPerCta / 2; ++u) {
+      const int t = (tl0 + u) * kRcSplits + rank;
       if (t < rows) {
         const uint32_t a = base + (uint32_t)((t * kRcM + el) * 4);
         float v[kRcSplits];
@@ -661,9 +677,20 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
         float sum = 0.f;
 #pragma unroll
         for (int q = 0; q < kRcSplits; ++q) sum += v[q];
-        if (e0 + el < E && !aborted) logits[(size_t)(t0 + t) * E + e0 + el] = sum;
+        if (fuse_topk)
+          fin[(tl0 + u) * kRcM + el] = sum;
+        else if (e0 + el < E && !aborted)
+          logits[(size_t)(t0 + t) * E + e0 + el] = sum;
       }
     }
+  }
+  if (fuse_topk) {
+    __syncthreads();
+    if (!aborted)
+      for (int u = warp; u < kRcTokPerCta; u += kRcThreads / 32) {
+        const int t = u * kRcSplits + rank;
+        if (t < rows) topk_token(tk, t0 + t, fin + u * kRcM, tk_scratch + warp * 3 * E);
+      }
   }
   cluster_sync_all();  // no CTA leaves while another reads its slice
   tc_fence_before();
@@ -767,43 +794,9 @@ int router_splits(const moe_config& c, int T, int num_sms) {
   return (int)s;
 }
 
-void launch_router(const Launch& L, const moe_config& c, int T, const void* x, const float* w_r,
-                   float* partial, int splits, float* logits, int* counters) {
-  RouterArgs a;
-  a.x = static_cast<const uint16_t*>(x);
-  a.w = w_r;
-  a.partial = partial;
-  a.logits = logits;
-  a.counters = counters;
-  a.T = T;
-  a.E = c.n_routed + c.n_zero;
-  a.H = c.hidden;
-  a.splits = splits;
-  a.kper = ((c.hidden + splits - 1) / splits + kRtK - 1) / kRtK * kRtK;
-  const int E = c.n_routed + c.n_zero;
-  CUtensorMap xmap, wmap;
-  memset(&xmap, 0, sizeof xmap);
-  memset(&wmap, 0, sizeof wmap);
-  if (router_tc_decode_chosen(c, T) && rc_x_map(&xmap, x, T, c.hidden) &&
-      rc_w_map(&wmap, w_r, E, c.hidden)) {
-    // decode router on tensor cores: clusters of kRcSplits CTAs, one per H slice
-    const dim3 g((E + kRcM - 1) / kRcM, (T + kRcN - 1) / kRcN, kRcSplits);
-    set_smem_attr_once(reinterpret_cast<const void*>(router_tc_kernel), kRcSmem, kAttrRouterTc);
-    launch_begin(L, MOE_K_ROUTER);
-    launch_kernel(router_tc_kernel, g, kRcThreads, kRcSmem, L.stream, xmap, wmap, logits, T, E,
-                  c.hidden, L.status);
-    launch_end(L, MOE_K_ROUTER);
-    return;
-  }
-  dim3 grid((a.E + kRtExp - 1) / kRtExp, (T + kRtTok - 1) / kRtTok, splits);
-  set_smem_attr_once(reinterpret_cast<const void*>(router_kernel), kRtSmemBytes, kAttrRouter);
-  launch_begin(L, MOE_K_ROUTER);
-  launch_kernel(router_kernel, grid, kRtThreads, kRtSmemBytes, L.stream, a);
-  launch_end(L, MOE_K_ROUTER);
-}
-
-void launch_topk(const Launch& L, const moe_config& c, int T, const float* logits,
-                 const float* bias, int32_t* ids, float* w) {
+namespace {
+TopkArgs topk_args(const Launch& L, const moe_config& c, int T, const float* logits,
+                   const float* bias, int32_t* ids, float* w) {
   TopkArgs a;
   a.logits = logits;
   a.bias = bias;
@@ -820,6 +813,10 @@ void launch_topk(const Launch& L, const moe_config& c, int T, const float* logit
   a.renorm = c.renormalize;
   a.bias_mode = c.bias_mode;
   a.scale = c.routed_scale == 0.f ? 1.f : c.routed_scale;
+  return a;
+}
+
+void launch_topk(const Launch& L, const TopkArgs& a, int T) {
   const size_t per_warp = (size_t)3 * a.E * sizeof(float);
   // few warps per CTA: tokens spread over more SMs
   int warps = (int)((96 * 1024) / per_warp);
@@ -829,6 +826,54 @@ void launch_topk(const Launch& L, const moe_config& c, int T, const float* logit
   launch_begin(L, MOE_K_TOPK);
   launch_kernel(topk_kernel, (T + warps - 1) / warps, warps * 32, smem, L.stream, a);
   launch_end(L, MOE_K_TOPK);
+}
+}  // namespace
+
+void launch_route(const Launch& L, const moe_config& c, int T, const void* x, const float* w_r,
+                  const float* bias, float* partial, int splits, float* logits, int* counters,
+                  int32_t* ids, float* w) {
+  const TopkArgs tk = topk_args(L, c, T, logits, bias, ids, w);
+  const int E = c.n_routed + c.n_zero;
+  CUtensorMap xmap, wmap;
+  memset(&xmap, 0, sizeof xmap);
+  memset(&wmap, 0, sizeof wmap);
+  if (router_tc_decode_chosen(c, T) && rc_x_map(&xmap, x, T, c.hidden) &&
+      rc_w_map(&wmap, w_r, E, c.hidden)) {
+    // decode router on tensor cores: clusters of kRcSplits CTAs, one per H
+    // slice; with all experts in one tile and at most one token per warp of
+    // the cluster it also picks the top-k
+    const int fuse = (E <= kRcM && T <= kRcSplits * (kRcThreads / 32) && folds_enabled()) ? 1 : 0;
+    const dim3 g((E + kRcM - 1) / kRcM, (T + kRcN - 1) / kRcN, kRcSplits);
+    set_smem_attr_once(reinterpret_cast<const void*>(router_tc_kernel), kRcSmem, kAttrRouterTc);
+    launch_begin(L, MOE_K_ROUTER);
+    launch_kernel(router_tc_kernel, g, kRcThreads, kRcSmem, L.stream, xmap, wmap, logits, T, E,
+                  c.hidden, L.status, tk, fuse);
+    launch_end(L, MOE_K_ROUTER);
+    if (!fuse) launch_topk(L, tk, T);
+    return;
+  }
+  RouterArgs a;
+  a.x = static_cast<const uint16_t*>(x);
+  a.w = w_r;
+  a.partial = partial;
+  a.logits = logits;
+  a.counters = counters;
+  a.T = T;
+  a.E = E;
+  a.H = c.hidden;
+  a.splits = splits;
+  a.kper = ((c.hidden + splits - 1) / splits + kRtK - 1) / kRtK * kRtK;
+  dim3 grid((a.E + kRtExp - 1) / kRtExp, (T + kRtTok - 1) / kRtTok, splits);
+  set_smem_attr_once(reinterpret_cast<const void*>(router_kernel), kRtSmemBytes, kAttrRouter);
+  launch_begin(L, MOE_K_ROUTER);
+  launch_kernel(router_kernel, grid, kRtThreads, kRtSmemBytes, L.stream, a);
+  launch_end(L, MOE_K_ROUTER);
+  launch_topk(L, tk, T);
+}
+
+void launch_topk_only(const Launch& L, const moe_config& c, int T, const float* logits,
+                      const float* bias, int32_t* ids, float* w) {
+  launch_topk(L, topk_args(L, c, T, logits, bias, ids, w), T);
 }
 
 }  // namespace moe

@@ -106,7 +106,6 @@ extern "C" moe_status moe_route_noalloc(const moe_config* cfg, int32_t T, const 
   float* logits = reinterpret_cast<float*>(b + kNoAllocHeadBytes);
   float* partial = reinterpret_cast<float*>(b + kNoAllocHeadBytes + logit_bytes);
   if (cudaMemsetAsync(base, 0, kNoAllocStatusBytes, L.stream) != cudaSuccess) return MOE_ERR_CUDA;
-  launch_router(L, *cfg, T, x, w_router, partial, splits, logits, counters);
-  launch_topk(L, *cfg, T, logits, bias, topk_ids, topk_w);
+  launch_route(L, *cfg, T, x, w_router, bias, partial, splits, logits, counters, topk_ids, topk_w);
   return launch_status_take();
 }

@@ -39,6 +39,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <algorithm>
 #include <mutex>
@@ -60,6 +61,7 @@ constexpr int kBoxRows = 64;                     // activation rows per TMA box
 constexpr int kBoxBytes = kBoxRows * kBK * 2;    // 8 KB
 constexpr long long kGuard = 1LL << 48;          // (2^24)^2
 constexpr int kAccCols = 256;                    // TMEM columns of one accumulator buffer
+constexpr int kPrefetch = 4;                     // direct loads: L2 prefetch distance (stages)
 
 struct Maps {
   CUtensorMap a0, a1;  // int8 weights [E][N][K]
@@ -83,6 +85,8 @@ struct Args {
   int K, N;
   DevStatus* status;
   ScatterAdd sc;             // down mode: add w * y into the tokens' accumulators
+  const int8_t* w0;          // int8 weights [E, N, K] (gate or down), for direct loads
+  const int8_t* w1;          // (up)
 };
 
 // Tile id -> rows, channel tile, expert.
@@ -94,7 +98,7 @@ __device__ __forceinline__ QTile decode(const Args& a, int tile, int ntasks) {
   t.tile = tile;
   t.row0 = tk.row0;
   t.n = tk.nrows;
-  t.e = tk.expert;
+  t.e = tk.expert < 0 ? 0 : tk.expert;  // the shared expert is a one-expert stack
   t.shared = 0;
   return t;
 }
@@ -203,7 +207,10 @@ static_assert(PGeom<kW8Raw>::kSmemBytes == PGeom<kW8Down>::kSmemBytes &&
 // the MMA thread.
 constexpr int kPairQueueReaders = (2 + 4 + kEpiWarps) + (1 + 4 + kEpiWarps);
 
-template <int MODE>
+// DIRECT: the converter warps load the int8 weights from global memory (L2,
+// warmed by the producer's tensor prefetches) straight into registers, so the
+// weight tiles never pass through shared memory as int8.
+template <int MODE, bool DIRECT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     w8a8_pair_kernel(const __grid_constant__ Maps maps, const Args a) {
   pdl_wait();
@@ -366,30 +373,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int nb = (hrows + kBoxRows - 1) / kBoxRows;
       const int arow = t.row0 + (int)rank * hrows;
       const int wrow = (t.ct * 2 + (int)rank) * kTcM;
+      // direct loads: the weight boxes of the first steps into L2 now, then each
+      // step's box kPrefetch steps ahead
+      auto prefetch = [&](int ks) {
+#pragma unroll
+        for (int u = 0; u < G::kSub; ++u) {
+          const int kx = (ks * G::kSub + u) * kBK;
+          tma_prefetch_l2_3d(&maps.a0, kx, wrow, t.e);
+          if (NA == 2) tma_prefetch_l2_3d(&maps.a1, kx, wrow, t.e);
+        }
+      };
+      if (DIRECT)
+        for (int ks = 0; ks < kPrefetch && ks < nks; ++ks) prefetch(ks);
       for (int ks = 0; ks < nks; ++ks) {
         if (*abort_flag) {
           ok = false;
           break;
         }
-        const int sr = n_raw % G::kSRaw;
-        if (!mbar_wait(smem_u32(&raw_empty[sr]), ((n_raw / G::kSRaw) & 1u) ^ 1u)) {
-          raise_status(a.status, kStTimeout, kind);
-          fail();
-          ok = false;
-          break;
-        }
-        // a sub-step past K is a box outside the matrix: TMA fills it with zeros
-        uint32_t bar = smem_u32(&raw_full[sr]);
-        mbar_arrive_expect_tx(bar, G::kRawBytes);
-        const uint32_t raw = smem_u32(smem + G::kRawOff + sr * G::kRawBytes);
+        if (DIRECT) {
+          if (ks + kPrefetch < nks) prefetch(ks + kPrefetch);
+        } else {
+          const int sr = n_raw % G::kSRaw;
+          if (!mbar_wait(smem_u32(&raw_empty[sr]), ((n_raw / G::kSRaw) & 1u) ^ 1u)) {
+            raise_status(a.status, kStTimeout, kind);
+            fail();
+            ok = false;
+            break;
+          }
+          // a sub-step past K is a box outside the matrix: TMA fills it with zeros
+          uint32_t bar = smem_u32(&raw_full[sr]);
+          mbar_arrive_expect_tx(bar, G::kRawBytes);
+          const uint32_t raw = smem_u32(smem + G::kRawOff + sr * G::kRawBytes);
 #pragma unroll
-        for (int u = 0; u < G::kSub; ++u) {
-          const int kx = (ks * G::kSub + u) * kBK;
-          tma_load_3d(raw + (u * NA) * kRawTileBytes, &maps.a0, kx, wrow, t.e, bar, pol_w);
-          if (NA == 2)
-            tma_load_3d(raw + (u * NA + 1) * kRawTileBytes, &maps.a1, kx, wrow, t.e, bar, pol_w);
+          for (int u = 0; u < G::kSub; ++u) {
+            const int kx = (ks * G::kSub + u) * kBK;
+            tma_load_3d(raw + (u * NA) * kRawTileBytes, &maps.a0, kx, wrow, t.e, bar, pol_w);
+            if (NA == 2)
+              tma_load_3d(raw + (u * NA + 1) * kRawTileBytes, &maps.a1, kx, wrow, t.e, bar,
+                          pol_w);
+          }
+          ++n_raw;
         }
-        ++n_raw;
         const int sa = n_act % G::kSAct;
         if (!mbar_wait_cluster(smem_u32(&act_empty[sa]), ((n_act / G::kSAct) & 1u) ^ 1u)) {
           raise_status(a.status, kStTimeout, kind);
@@ -412,8 +436,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     // every issued copy lands before the CTA can exit (the first CTA's
     // activation barriers also count the second CTA's copies)
-    for (uint32_t j = n_raw > (uint32_t)G::kSRaw ? n_raw - G::kSRaw : 0u; j < n_raw; ++j)
-      mbar_wait(smem_u32(&raw_full[j % G::kSRaw]), (j / G::kSRaw) & 1u);
+    if (!DIRECT)
+      for (uint32_t j = n_raw > (uint32_t)G::kSRaw ? n_raw - G::kSRaw : 0u; j < n_raw; ++j)
+        mbar_wait(smem_u32(&raw_full[j % G::kSRaw]), (j / G::kSRaw) & 1u);
     if (lead)
       for (uint32_t j = n_act > (uint32_t)G::kSAct ? n_act - G::kSAct : 0u; j < n_act; ++j)
         mbar_wait_cluster(smem_u32(&act_full[j % G::kSAct]), (j / G::kSAct) & 1u);
@@ -495,32 +520,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) nrm[m][i] = 0;
       bool ok = true;
-      for (int ks = 0; ks < nks; ++ks, ++it) {
-        const int sr = it % G::kSRaw, sc = it % G::kSConv;
-        if (!warp_wait(smem_u32(&raw_full[sr]), (it / G::kSRaw) & 1u) ||
-            !warp_wait_cluster(smem_u32(&conv_empty[sc]), ((it / G::kSConv) & 1u) ^ 1u)) {
-          if (lane == 0) {
-            raise_status(a.status, kStTimeout, kind);
-            fail();
-          }
-          ok = false;
-          break;
-        }
-        const uint8_t* rawt = smem + G::kRawOff + sr * G::kRawBytes;
+      // One pipeline step: v holds this thread's int8 chunks of step ks (from
+      // the raw ring, or loaded straight from global memory).  Converts them into
+      // the conv ring (128-byte swizzled fp16 rows), sums squares for the guard,
+      // and hands the stage to the MMA thread.
+      // (int8 chunks [sub-step][matrix][4]: chunk c = ti + 128 i of a tile is
+      // row c / 4, 16-byte column c % 4)
+      auto step = [&](uint4 (&v)[G::kSub * NA][4], int sr) -> bool {
+        const int sc = it % G::kSConv;
+        if (!warp_wait_cluster(smem_u32(&conv_empty[sc]), ((it / G::kSConv) & 1u) ^ 1u))
+          return false;
         uint8_t* conv = smem + sc * G::kConvBytes;
-        // all of this thread's 16-byte chunks are loaded before any store, so
-        // their latencies overlap (a store could alias a later load otherwise)
-        // (int8 tiles [sub-step][matrix], 64 bytes a row; fp16 tiles in the same
-        // order, 128-byte rows, 128-byte swizzle)
-        uint4 v[G::kSub * NA][4];
-#pragma unroll
-        for (int b = 0; b < G::kSub * NA; ++b)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = ti + 128 * i;  // 16-byte chunk of the int8 tile
-            v[b][i] = *reinterpret_cast<const uint4*>(rawt + b * kRawTileBytes + (c >> 2) * kBK +
-                                                      (c & 3) * 16);
-          }
 #pragma unroll
         for (int b = 0; b < G::kSub * NA; ++b) {
           const int m = b % NA;
@@ -549,21 +559,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // (their barrier counts both CTAs' copies), so conv_full alone tells the
         // MMA thread that the whole stage is in place: one wait fewer on its path.
         const int sa = it % G::kSAct;
-        if (lead && !warp_wait_cluster(smem_u32(&act_full[sa]), (it / G::kSAct) & 1u)) {
-          if (lane == 0) {
-            raise_status(a.status, kStTimeout, kind);
-            fail();
-          }
-          ok = false;
-          break;
-        }
+        if (lead && !warp_wait_cluster(smem_u32(&act_full[sa]), (it / G::kSAct) & 1u))
+          return false;
         __syncwarp();
         if (lane == 0) {
           // the first CTA's MMA thread waits on this; the converted tile is
           // read by this CTA's own tensor core
           mbar_arrive_remote(lead_conv_full + 8u * sc);
-          mbar_arrive(smem_u32(&raw_empty[sr]));
+          if (!DIRECT) mbar_arrive(smem_u32(&raw_empty[sr]));
         }
+        ++it;
+        return true;
+      };
+      if (!DIRECT) {
+        for (int ks = 0; ks < nks; ++ks) {
+          const int sr = it % G::kSRaw;
+          if (!warp_wait(smem_u32(&raw_full[sr]), (it / G::kSRaw) & 1u)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* rawt = smem + G::kRawOff + sr * G::kRawBytes;
+          // all of this thread's 16-byte chunks are loaded before any store, so
+          // their latencies overlap (a store could alias a later load otherwise)
+          uint4 v[G::kSub * NA][4];
+#pragma unroll
+          for (int b = 0; b < G::kSub * NA; ++b)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int c = ti + 128 * i;
+              v[b][i] = *reinterpret_cast<const uint4*>(rawt + b * kRawTileBytes + (c >> 2) * kBK +
+                                                        (c & 3) * 16);
+            }
+          if (!step(v, sr)) {
+            ok = false;
+            break;
+          }
+        }
+      } else {
+        // direct: step ks + 1's chunks are in flight while step ks is converted
+        const size_t mat = (size_t)a.N * a.K;
+        const int8_t* W0 = a.w0 + (size_t)t.e * mat;
+        const int8_t* W1 = NA == 2 ? a.w1 + (size_t)t.e * mat : nullptr;
+        const int wrow = (t.ct * 2 + (int)rank) * kTcM;
+        auto load = [&](uint4 (&v)[G::kSub * NA][4], int ks) {
+#pragma unroll
+          for (int b = 0; b < G::kSub * NA; ++b) {
+            const int u = b / NA, m = b % NA;
+            const int8_t* W = m == 0 ? W0 : W1;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int c = ti + 128 * i;
+              const int ch = wrow + (c >> 2);
+              const int kx = (ks * G::kSub + u) * kBK + (c & 3) * 16;
+              v[b][i] = (ch < a.N && kx < a.K) ? ld_nc_na_v4(W + (size_t)ch * a.K + kx)
+                                               : make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+        };
+        uint4 va[G::kSub * NA][4], vb[G::kSub * NA][4];
+        load(va, 0);
+        for (int ks = 0; ks < nks; ks += 2) {
+          if (ks + 1 < nks) load(vb, ks + 1);
+          if (!step(va, 0)) {
+            ok = false;
+            break;
+          }
+          if (ks + 1 >= nks) break;
+          if (ks + 2 < nks) load(va, ks + 2);
+          if (!step(vb, 0)) {
+            ok = false;
+            break;
+          }
+        }
+      }
+      if (!ok && lane == 0) {
+        raise_status(a.status, kStTimeout, kind);
+        fail();
       }
       if (!ok) break;
       // weight-row norms of this tile for the epilogue's guard
@@ -853,9 +924,10 @@ constexpr int kQgThreads = 256;
 constexpr int kMaxTopKQuant = 32;  // the largest top_k the layer accepts
 __global__ void __launch_bounds__(kQgThreads)
     quant_gather_kernel(const uint16_t* x, const int32_t* ids, const int32_t* e2s,
-                        const int32_t* offsets, int gemv_max, uint16_t* x16, int8_t* x8,
-                        float* scale, int32_t* norm2, int H, int k, int E_r, int E,
-                        const float* w, float* acc) {
+                        const int32_t* offsets, int gemv_max, QuantGatherOut qo, int H, int k,
+                        int E_r, int E, const float* w, float* acc) {
+  uint16_t* x16 = qo.x16;
+  int8_t* x8 = qo.x8;
   pdl_enter();
   // fused combine: the token's accumulator row starts as its zero-computation
   // picks' w * x (the down pass adds the expert outputs)
@@ -899,7 +971,8 @@ __global__ void __launch_bounds__(kQgThreads)
   amax = red_f[0];
   for (int w = 1; w < kQgThreads / 32; ++w) amax = fmaxf(amax, red_f[w]);
   const int n = nrows, na = n16;
-  if (n == 0) return;
+  const bool tok_row = qo.tok16 != nullptr;  // the shared expert reads every token
+  if (n == 0 && !tok_row) return;
   const float s = amax / 127.0f;
   int n2 = 0;
   for (int i = tid; i < nv; i += kQgThreads) {
@@ -916,6 +989,7 @@ __global__ void __launch_bounds__(kQgThreads)
       b[j / 4] |= (uint32_t)(qi & 0xff) << (8 * (j % 4));
     }
     const uint4 o = make_uint4(h[0], h[1], h[2], h[3]);
+    if (tok_row) reinterpret_cast<uint4*>(qo.tok16 + (size_t)t * H)[i] = o;
     for (int r = 0; r < na; ++r) reinterpret_cast<uint4*>(x16 + (size_t)rows[r] * H)[i] = o;
     for (int r = na; r < n; ++r)
       reinterpret_cast<uint2*>(x8 + (size_t)rows[r] * H)[i] = make_uint2(b[0], b[1]);
@@ -923,11 +997,16 @@ __global__ void __launch_bounds__(kQgThreads)
   for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
   if (lane == 0) red_i[warp] = n2;
   __syncthreads();
-  if (tid < n) {
+  if (tid < n || (tok_row && tid == n)) {
     int tot = 0;
     for (int w = 0; w < kQgThreads / 32; ++w) tot += red_i[w];
-    norm2[rows[tid]] = tot;
-    scale[rows[tid]] = s;
+    if (tid < n) {
+      qo.norm2[rows[tid]] = tot;
+      qo.scale[rows[tid]] = s;
+    } else {
+      qo.tok_norm2[t] = tot;
+      qo.tok_scale[t] = s;
+    }
   }
 }
 
@@ -995,7 +1074,7 @@ __global__ void __launch_bounds__(256)
   pdl_enter();
   const int lane = threadIdx.x % 32;
   const int r = blockIdx.x * 8 + threadIdx.x / 32;
-  const int rows = min(R, offsets[n_experts]);
+  const int rows = offsets ? min(R, offsets[n_experts]) : R;
   if (r >= rows) return;
   bool streamed = false;
   if (dst8) {
@@ -1120,7 +1199,19 @@ Args make_args(const Launch& L, const W8Pass& p) {
   a.N = p.N;
   a.status = L.status;
   a.sc = p.sc;
+  a.w0 = static_cast<const int8_t*>(p.w0);
+  a.w1 = static_cast<const int8_t*>(p.w1);
   return a;
+}
+
+// The converters load the int8 weights from global memory (DIRECT) when the
+// environment sets MOE_W8_DIRECT=1 (read once).
+bool w8_direct() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_W8_DIRECT");
+    return v && v[0] == '1' && v[1] == 0;
+  }();
+  return on;
 }
 
 // Two-SM tiles (clusters of two CTAs), then the exact fallback for entries
@@ -1135,11 +1226,13 @@ bool launch_pair(const Launch& L, const W8Pass& p) {
   if (!ok) return false;
   const Args a = make_args(L, p);
   const int kind = MODE == kW8GateUp ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
-  set_smem_attr_once(reinterpret_cast<const void*>(w8a8_pair_kernel<MODE>), G::kSmemBytes,
-                     kAttrW8Base + MODE);
+  const bool direct = w8_direct();
+  const auto kernel = direct ? w8a8_pair_kernel<MODE, true> : w8a8_pair_kernel<MODE, false>;
+  set_smem_attr_once(reinterpret_cast<const void*>(kernel), G::kSmemBytes,
+                     (direct ? kAttrW8DirectBase : kAttrW8Base) + MODE);
   const int grid = std::max(2, L.num_sms & ~1);  // whole clusters of two
   launch_begin(L, kind);
-  launch_kernel(w8a8_pair_kernel<MODE>, grid, kThreads, G::kSmemBytes, L.stream, maps, a);
+  launch_kernel(kernel, grid, kThreads, G::kSmemBytes, L.stream, maps, a);
   launch_end(L, kind);
   launch_begin(L, MOE_K_W8_EXACT);
   launch_kernel(w8a8_exact_kernel<MODE>, L.num_sms, 256, 0, L.stream,
@@ -1169,12 +1262,11 @@ void launch_i8_rows_to_f16(const Launch& L, const int8_t* src, uint16_t* dst, in
 
 void launch_quant_gather(const Launch& L, const moe_config& c, int T, const void* x,
                          const int32_t* ids, const int32_t* e2s, const int32_t* offsets,
-                         int gemv_max, uint16_t* x16, int8_t* x8, float* scale, int32_t* norm2,
-                         const float* w, float* acc) {
+                         int gemv_max, const QuantGatherOut& o, const float* w, float* acc) {
   launch_begin(L, MOE_K_PERM_GATHER);
   launch_kernel(quant_gather_kernel, T, kQgThreads, 0, L.stream, static_cast<const uint16_t*>(x),
-                ids, e2s, offsets, gemv_max, x16, x8, scale, norm2, c.hidden, c.top_k,
-                c.n_routed, c.n_routed + c.n_zero, w, acc);
+                ids, e2s, offsets, gemv_max, o, c.hidden, c.top_k, c.n_routed,
+                c.n_routed + c.n_zero, w, acc);
   launch_end(L, MOE_K_PERM_GATHER);
 }
 

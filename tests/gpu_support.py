@@ -57,8 +57,8 @@ def run_layer(m, spec, d, out_fp32=True, gemv_max_rows=0, x=None, combine=0):
     ws = m.workspace(cfg, T, x.device)
     w = d["wts_d"]
     m.moe_layer_forward(cfg, T, x, d["w_r_d"], d["bias_d"], w.get("w_gate"), w.get("w_up"),
-                        w.get("w_down"), w.get("s_gate"), w.get("s_up"), w.get("s_down"),
-                        w.get("shared_gate"), w.get("shared_up"), w.get("shared_down"), out, ws)
+                        w.get("w_down"), *m.layer_scales(w), w.get("shared_gate"),
+                        w.get("shared_up"), w.get("shared_down"), out, ws)
     torch.cuda.synchronize()
     st = m.moe_check_device_status(ws)
     assert st == m.MOE_OK, f"device status {st}"

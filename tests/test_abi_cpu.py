@@ -53,8 +53,8 @@ def test_binding_names_match_header(moe):
 
 
 def test_config_struct_layout_matches_header(moe):
-    # 16 int32 + 1 float, no padding
-    assert ctypes.sizeof(moe.MoeConfig) == 17 * 4
+    # 17 int32 + 1 float, no padding
+    assert ctypes.sizeof(moe.MoeConfig) == 18 * 4
 
 
 def _ws(moe, cfg, T):
@@ -76,6 +76,7 @@ def test_workspace_size_for_the_headline_layers(moe):
     ("hidden", 7, 1), ("hidden", 0, 1), ("top_k", 0, 1), ("top_k", 9, 1), ("n_group", 3, 1),
     ("score", 5, 1), ("bias_mode", 3, 1), ("shared_inter", 12, 1), ("inter", 4, 1),
     ("renormalize", 2, 1), ("n_routed", -1, 1), ("combine", 3, 1), ("combine", -1, 1),
+    ("ffn_launch", 3, 1), ("ffn_launch", -1, 1),
 ])
 def test_invalid_configs_are_rejected(moe, field, value, status):
     import synth
@@ -119,7 +120,13 @@ def test_w8a8_rules(moe):
     assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 512, ctypes.byref(n)) == 0
     cfg.hidden = 1000  # int8 rows must be whole 16-byte vectors
     assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 512, ctypes.byref(n)) == 1
+    # the shared expert is int8 too: its intermediate size in whole 16-byte rows
     cfg = moe.config_from_spec(synth.spec("w8a8_s", shared_inter=64))
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 512, ctypes.byref(n)) == 0
+    cfg = moe.config_from_spec(synth.spec("w8a8_s", shared_inter=72))
+    assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 512, ctypes.byref(n)) == 1
+    # a shared expert with no routed FFN experts is not supported in this mode
+    cfg = moe.config_from_spec(synth.spec("w8a8_s", shared_inter=64, n_routed=0, n_zero=8))
     assert moe.lib.moe_workspace_size(ctypes.byref(cfg), 512, ctypes.byref(n)) == 2
     assert moe.lib.moe_qgemm_s8_workspace_size(4, 1024, 256, 100, ctypes.byref(n)) == 0
     assert moe.lib.moe_qgemm_s8_workspace_size(4, 1000, 256, 100, ctypes.byref(n)) == 1
@@ -177,3 +184,51 @@ def test_selftest_arguments_are_checked_on_the_host(moe):
     assert moe.lib.moe_selftest_wait_timeout(fake, 0, None) == moe.MOE_ERR_INVALID_ARG
     assert moe.lib.moe_selftest_wait_timeout(fake, 3_000_000_000, None) == moe.MOE_ERR_INVALID_ARG
     assert moe.lib.moe_selftest_wait_timeout(fake + 16, 1000, None) == moe.MOE_ERR_ALIGNMENT
+
+
+def _table_choice(table, wdtype, H, I, T, k, E):
+    """Independent restatement of the tile-table rule: entries of the same weight
+    type, nearest in load bucket, then in log2(H * I); first in table order on ties."""
+    import math
+
+    m = T * k / E
+    b = next((i for i, v in enumerate(table["buckets"]) if m < v), len(table["buckets"]))
+    best, best_d = None, None
+    for e in table["entries"]:
+        if e["wdtype"] != wdtype:
+            continue
+        d = 1000.0 * abs(e["bucket"] - b) + abs(math.log2(H * max(I, 1) / (e["hidden"] * e["inter"])))
+        if best is None or d < best_d:
+            best, best_d = e, d
+    return best
+
+
+def test_tile_choice_follows_the_table(moe):
+    import json
+    import os
+
+    import numpy as np
+    import synth
+
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "sparse_expert_layer_gb300", "tuning", "tile_table.json")
+    table = json.load(open(path))
+    rng = np.random.default_rng(13)
+    for wdtype in ("bf16", "w8a8"):
+        for _ in range(60):
+            H = int(rng.choice([256, 1024, 4096, 5120, 6144, 7168, 8192]))
+            I = int(rng.choice([128, 512, 1536, 2048, 4096]))
+            E = int(rng.choice([8, 64, 256, 768]))
+            k = int(rng.choice([1, 2, 8]))
+            T = int(rng.choice([1, 16, 64, 128, 456, 2048, 8192]))
+            s = synth.spec("tiny", hidden=H, inter=I, n_routed=E, top_k=k, wdtype=wdtype)
+            g, one = moe.moe_tile_choice(moe.config_from_spec(s), T)
+            want = _table_choice(table, wdtype, H, I, T, k, E)
+            assert g == want["gemv_max"], (wdtype, H, I, E, k, T)
+            assert one == (wdtype == "bf16" and bool(want["one_launch"])), (wdtype, H, I, E, k, T)
+    # explicit settings win over the table
+    s = synth.spec("longcat")
+    assert moe.moe_tile_choice(moe.config_from_spec(s, gemv_max_rows=5), 64)[0] == 5
+    assert moe.moe_tile_choice(moe.config_from_spec(s, gemv_max_rows=-1), 64)[0] == 0
+    assert moe.moe_tile_choice(moe.config_from_spec(s, ffn_launch=moe.FFN_LAUNCH_TWO), 64)[1] is False
+    assert moe.moe_tile_choice(moe.config_from_spec(s, ffn_launch=moe.FFN_LAUNCH_ONE), 64)[1] is True

@@ -160,6 +160,28 @@ def w8_lists(wts, experts=None):
     return out
 
 
+def w8_shared(wts):
+    if "shared_gate" not in wts:
+        return None
+    return tuple(wts[n].cpu().numpy() for n in ("shared_gate", "s_shared_gate", "shared_up",
+                                                "s_shared_up", "shared_down", "s_shared_down"))
+
+
+@pytest.mark.parametrize("out_fp32", [True, False])
+@pytest.mark.parametrize("combine", [1, 2])  # ordered, fused
+def test_w8a8_layer_with_shared_expert_matches_oracle(m, out_fp32, combine):
+    # DSv3-shaped routing (sigmoid, groups, x 2.5) with an int8 shared expert fed
+    # the same per-token codes; its scales ride after the routed experts'
+    spec = synth.spec("dsv3_w8_s")
+    d = gs.inputs(spec)
+    L = w8_lists(d["wts"])
+    ref, _, _, _, _ = oracle.layer_w8a8(spec, synth.bf16_bits(d["x"]), d["w_r"].numpy(),
+                                        support.np_bias(d["bias"]), L["qg"], L["sg"], L["qu"],
+                                        L["su"], L["qd"], L["sd"], w8_shared(d["wts"]))
+    got = gs.run_layer(m, spec, d, out_fp32=out_fp32, combine=combine)
+    gs.check_out(got, ref, bf16_out=not out_fp32, what=f"dsv3_w8_s combine={combine}")
+
+
 @pytest.mark.parametrize("out_fp32", [True, False])
 def test_w8a8_layer_matches_oracle(m, out_fp32):
     spec = synth.spec("w8a8_s")
@@ -285,3 +307,37 @@ def test_w8a8_down_pass_exact_fallback(m, combine):
                                         L["su"], L["qd"], L["sd"])
     got = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=-1, combine=combine)
     gs.check_out(got, ref, bf16_out=False, what="w8a8 down-pass guard fallback")
+
+
+@pytest.mark.parametrize("name", ["longcat_w8", "dsv3_w8"])
+def test_w8a8_full_size_decode_layers(m, name):
+    # The W8A8 decode layers at full size (LongCat-shaped: 512 int8 experts and
+    # 256 zero-computation ones; DSv3-shaped: 256 int8 experts in 8 groups plus
+    # the int8 shared expert), bf16 out, the default streaming / tensor-core
+    # split: every token's routing exactly, sampled tokens' outputs against the
+    # oracle run with only the experts they pick.
+    spec = synth.spec(name)
+    x, w_r, bias, _ = support.make_inputs(spec)
+    wts_d = synth.draw_weights(spec, device="cuda")
+    d = dict(x=x, w_r=w_r, bias=bias, x_d=x.cuda(), w_r_d=w_r.cuda(),
+             bias_d=None if bias is None else bias.cuda(), wts_d=wts_d)
+    T, k = spec["T"], spec["top_k"]
+    cfg = m.config_from_spec(spec)
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wgt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = m.workspace(cfg, T)
+    m.moe_route(cfg, T, d["x_d"], d["w_r_d"], d["bias_d"], ids, wgt, ws)
+    torch.cuda.synchronize()
+    ids_o, w_o, _, _ = oracle.route(spec, synth.bf16_bits(x), w_r.numpy(), support.np_bias(bias))
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    out = gs.run_layer(m, spec, d, out_fp32=False)
+    rng = np.random.default_rng(5)
+    sample = np.sort(rng.choice(T, 3, replace=False))
+    L = w8_lists(wts_d, set(int(e) for e in ids_o[sample].reshape(-1) if e < spec["n_routed"]))
+    ref, ids_s, _, _, _ = oracle.layer_w8a8(spec, synth.bf16_bits(x[sample]), w_r.numpy(),
+                                            support.np_bias(bias), L["qg"], L["sg"], L["qu"],
+                                            L["su"], L["qd"], L["sd"], w8_shared(wts_d))
+    assert np.array_equal(ids_s, ids_o[sample])
+    gs.check_out(out[torch.as_tensor(sample, device="cuda")], ref, bf16_out=True, what=name)
+    del wts_d, d
+    torch.cuda.empty_cache()
