@@ -190,30 +190,27 @@ def tensor_peak():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-# the library's default switch points: bf16 units all on tensor cores, W8A8 units
-# of <= 8 rows on the int8 GEMV
-DEFAULT_GEMV_MAX_ROWS = {"bf16": 0, "w8a8": 8}
-
-
-def kernel_work(spec, counts, gemv_max_rows):
+def kernel_work(spec, counts, gemv_max, one_launch):
     """{kernel: (algorithmic bytes, flops)} per launch, from the realised loads.
     A unit (routed expert, or the shared expert over all T rows) with n rows goes
-    to the GEMV kernels when n <= the switch point, else to the tensor-core ones;
-    bytes = its weights once + its activation rows in and results out."""
+    to the GEMV kernels when n <= the switch point (the library's choice, from
+    moe_tile_choice), else to the tensor-core ones; bytes = its weights once + its
+    activation rows in and results out.  A W8A8 shared expert always runs on the
+    tensor-core kernels; a one-launch bf16 FFN is timed as tc_gate_up (both passes)."""
     H, I, Is, T = spec["hidden"], spec["inter"], spec["shared_inter"], spec["T"]
-    gm = (gemv_max_rows if gemv_max_rows > 0 else
-          (0 if gemv_max_rows < 0 else DEFAULT_GEMV_MAX_ROWS[spec["wdtype"]]))
-    wb = 1 if spec["wdtype"] == "w8a8" else 2
-    units = [(int(n), I) for n in counts[:spec["n_routed"]] if n > 0]
+    w8 = spec["wdtype"] == "w8a8"
+    wb = 1 if w8 else 2
+    units = [(int(n), I, False) for n in counts[:spec["n_routed"]] if n > 0]
     if Is:
-        units.append((T, Is))
+        units.append((T, Is, w8))
     out = {k: [0, 0] for k in ("gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down")}
-    for n, inter in units:
-        p = "gemv_" if n <= gm else "tc_"
+    for n, inter, force_tc in units:
+        p = "gemv_" if n <= gemv_max and not force_tc else "tc_"
+        d = "gate_up" if (p == "tc_" and one_launch) else "down"
         out[p + "gate_up"][0] += 2 * inter * H * wb + 2 * n * H + 2 * n * inter
         out[p + "gate_up"][1] += 4 * n * inter * H
-        out[p + "down"][0] += inter * H * wb + 2 * n * inter + 4 * n * H
-        out[p + "down"][1] += 2 * n * inter * H
+        out[p + d][0] += inter * H * wb + 2 * n * inter + 4 * n * H
+        out[p + d][1] += 2 * n * inter * H
     return {k: tuple(v) for k, v in out.items() if v[0]}
 
 
@@ -421,7 +418,7 @@ def measure(args, spec, dev, world, full):
     counts_h = counts.cpu().numpy()
     alg_bytes, U = algorithmic_bytes(spec, counts_h)
     del x_perm
-    if spec["n_zero"] > 0 and spec["bias_kind"] == "iid":
+    if spec["name"] in ("longcat", "longcat_w8"):
         # the LongCat-shaped router is drawn so that about a third of the picks
         # land on zero-computation experts
         share = zero_pick_share(spec, counts_h)
@@ -479,7 +476,9 @@ def measure(args, spec, dev, world, full):
     per_kernel = moe.timing_collect()
     moe.timing_enable(False)
 
-    res = {"spec": spec, "combine": args.combine, "value": value, "ms_step": ms_step,
+    gemv_max, one_launch = moe.moe_tile_choice(cfg, T)
+    res = {"spec": spec, "combine": args.combine, "gemv_max": gemv_max,
+           "one_launch": one_launch, "value": value, "ms_step": ms_step,
            "p50": p50, "p90": p90,
            "gpu_launches": gpu_launches, "clocks": clk.summary(), "per_kernel": per_kernel,
            "counts": counts_h, "alg_bytes": alg_bytes, "U": U}
@@ -565,7 +564,7 @@ def roofline_of(args, res):
     tpeak, tpeak_kind = tensor_peak()
     dom = max(per_kernel, key=lambda kname: per_kernel[kname][0])
     dom_ms, dom_n = per_kernel[dom]
-    work = kernel_work(spec, counts_h, args.gemv_max_rows)
+    work = kernel_work(spec, counts_h, res["gemv_max"], res["one_launch"])
     roof = None
     if dom in work and dom_n:
         kb, kf = work[dom]
@@ -602,6 +601,7 @@ def config_block(spec, res):
           if gb > 0.5 else f"L2-resident: {gb * 1e3:.1f} MB per step, not flushed "
           "(latency-bound layer)")
     return {"workload": describe(spec), "tokens": spec["T"], "unique_experts": res["U"],
+            "gemv_max_rows": res["gemv_max"], "ffn_one_launch": res["one_launch"],
             "real_picks": int(counts_h[:spec["n_routed"]].sum()),
             "zero_pick_share": zero_pick_share(spec, counts_h) if spec["n_zero"] else 0.0,
             "l2": l2, "combine": res["combine"]}

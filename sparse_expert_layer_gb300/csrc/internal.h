@@ -387,8 +387,7 @@ enum {
   kAttrRouterTc,
   kAttrSortSmall,
   kAttrTcFfn,
-  kAttrW8DirectBase,                 // 3 slots: W8A8 modes, direct weight loads
-  kAttrSlots = kAttrW8DirectBase + 3
+  kAttrSlots
 };
 void set_smem_attr_once(const void* func, int bytes, int slot);
 

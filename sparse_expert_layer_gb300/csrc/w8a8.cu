@@ -39,7 +39,6 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
-#include <cstdlib>
 #include <cstring>
 #include <algorithm>
 #include <mutex>
@@ -60,8 +59,6 @@ constexpr int kF16TileBytes = kTcM * kBK * 2;    // 16 KB of fp16
 constexpr int kBoxRows = 64;                     // activation rows per TMA box
 constexpr int kBoxBytes = kBoxRows * kBK * 2;    // 8 KB
 constexpr long long kGuard = 1LL << 48;          // (2^24)^2
-constexpr int kAccCols = 256;                    // TMEM columns of one accumulator buffer
-constexpr int kPrefetch = 4;                     // direct loads: L2 prefetch distance (stages)
 
 struct Maps {
   CUtensorMap a0, a1;  // int8 weights [E][N][K]
@@ -85,8 +82,6 @@ struct Args {
   int K, N;
   DevStatus* status;
   ScatterAdd sc;             // down mode: add w * y into the tokens' accumulators
-  const int8_t* w0;          // int8 weights [E, N, K] (gate or down), for direct loads
-  const int8_t* w1;          // (up)
 };
 
 // Tile id -> rows, channel tile, expert.
@@ -168,6 +163,7 @@ struct PGeom {
   static constexpr int kTN = kW8MaxN;                        // token rows per tile
   static constexpr int kHalfRows = kTN / 2;                  // activation rows per CTA
   static constexpr int kAccBufs = MODE == kW8GateUp ? 1 : 2;
+  static constexpr int kAccCols = kTN;                       // TMEM columns of one accumulator
   // 64-wide K sub-steps per ring stage: a down or raw stage carries two, so
   // each handshake of the pipeline feeds as many MMAs as a gate/up stage
   static constexpr int kSub = MODE == kW8GateUp ? 1 : 2;
@@ -194,9 +190,9 @@ static_assert(PGeom<kW8GateUp>::kBarCount * 8 + kTileQueue * (int)sizeof(QTile) 
                   PGeom<kW8GateUp>::kBarBytes, "pair gate/up barriers");
 static_assert(PGeom<kW8Down>::kBarCount * 8 + kTileQueue * (int)sizeof(QTile) + 48 <=
                   PGeom<kW8Down>::kBarBytes, "pair down barriers");
-static_assert(PGeom<kW8GateUp>::kNA * kAccCols * PGeom<kW8GateUp>::kAccBufs <= 512,
-              "pair gate/up accumulators");
-static_assert(PGeom<kW8Down>::kNA * kAccCols * PGeom<kW8Down>::kAccBufs <= 512,
+static_assert(PGeom<kW8GateUp>::kNA * PGeom<kW8GateUp>::kAccCols *
+                  PGeom<kW8GateUp>::kAccBufs <= 512, "pair gate/up accumulators");
+static_assert(PGeom<kW8Down>::kNA * PGeom<kW8Down>::kAccCols * PGeom<kW8Down>::kAccBufs <= 512,
               "pair down accumulators");
 static_assert(PGeom<kW8Raw>::kSmemBytes == PGeom<kW8Down>::kSmemBytes &&
                   PGeom<kW8Raw>::kBarCount == PGeom<kW8Down>::kBarCount,
@@ -207,10 +203,7 @@ static_assert(PGeom<kW8Raw>::kSmemBytes == PGeom<kW8Down>::kSmemBytes &&
 // the MMA thread.
 constexpr int kPairQueueReaders = (2 + 4 + kEpiWarps) + (1 + 4 + kEpiWarps);
 
-// DIRECT: the converter warps load the int8 weights from global memory (L2,
-// warmed by the producer's tensor prefetches) straight into registers, so the
-// weight tiles never pass through shared memory as int8.
-template <int MODE, bool DIRECT>
+template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     w8a8_pair_kernel(const __grid_constant__ Maps maps, const Args a) {
   pdl_wait();
@@ -373,47 +366,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int nb = (hrows + kBoxRows - 1) / kBoxRows;
       const int arow = t.row0 + (int)rank * hrows;
       const int wrow = (t.ct * 2 + (int)rank) * kTcM;
-      // direct loads: the weight boxes of the first steps into L2 now, then each
-      // step's box kPrefetch steps ahead
-      auto prefetch = [&](int ks) {
-#pragma unroll
-        for (int u = 0; u < G::kSub; ++u) {
-          const int kx = (ks * G::kSub + u) * kBK;
-          tma_prefetch_l2_3d(&maps.a0, kx, wrow, t.e);
-          if (NA == 2) tma_prefetch_l2_3d(&maps.a1, kx, wrow, t.e);
-        }
-      };
-      if (DIRECT)
-        for (int ks = 0; ks < kPrefetch && ks < nks; ++ks) prefetch(ks);
       for (int ks = 0; ks < nks; ++ks) {
         if (*abort_flag) {
           ok = false;
           break;
         }
-        if (DIRECT) {
-          if (ks + kPrefetch < nks) prefetch(ks + kPrefetch);
-        } else {
-          const int sr = n_raw % G::kSRaw;
-          if (!mbar_wait(smem_u32(&raw_empty[sr]), ((n_raw / G::kSRaw) & 1u) ^ 1u)) {
-            raise_status(a.status, kStTimeout, kind);
-            fail();
-            ok = false;
-            break;
-          }
-          // a sub-step past K is a box outside the matrix: TMA fills it with zeros
-          uint32_t bar = smem_u32(&raw_full[sr]);
-          mbar_arrive_expect_tx(bar, G::kRawBytes);
-          const uint32_t raw = smem_u32(smem + G::kRawOff + sr * G::kRawBytes);
-#pragma unroll
-          for (int u = 0; u < G::kSub; ++u) {
-            const int kx = (ks * G::kSub + u) * kBK;
-            tma_load_3d(raw + (u * NA) * kRawTileBytes, &maps.a0, kx, wrow, t.e, bar, pol_w);
-            if (NA == 2)
-              tma_load_3d(raw + (u * NA + 1) * kRawTileBytes, &maps.a1, kx, wrow, t.e, bar,
-                          pol_w);
-          }
-          ++n_raw;
+        const int sr = n_raw % G::kSRaw;
+        if (!mbar_wait(smem_u32(&raw_empty[sr]), ((n_raw / G::kSRaw) & 1u) ^ 1u)) {
+          raise_status(a.status, kStTimeout, kind);
+          fail();
+          ok = false;
+          break;
         }
+        // a sub-step past K is a box outside the matrix: TMA fills it with zeros
+        uint32_t bar = smem_u32(&raw_full[sr]);
+        mbar_arrive_expect_tx(bar, G::kRawBytes);
+        const uint32_t raw = smem_u32(smem + G::kRawOff + sr * G::kRawBytes);
+#pragma unroll
+        for (int u = 0; u < G::kSub; ++u) {
+          const int kx = (ks * G::kSub + u) * kBK;
+          tma_load_3d(raw + (u * NA) * kRawTileBytes, &maps.a0, kx, wrow, t.e, bar, pol_w);
+          if (NA == 2)
+            tma_load_3d(raw + (u * NA + 1) * kRawTileBytes, &maps.a1, kx, wrow, t.e, bar, pol_w);
+        }
+        ++n_raw;
         const int sa = n_act % G::kSAct;
         if (!mbar_wait_cluster(smem_u32(&act_empty[sa]), ((n_act / G::kSAct) & 1u) ^ 1u)) {
           raise_status(a.status, kStTimeout, kind);
@@ -436,9 +412,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     // every issued copy lands before the CTA can exit (the first CTA's
     // activation barriers also count the second CTA's copies)
-    if (!DIRECT)
-      for (uint32_t j = n_raw > (uint32_t)G::kSRaw ? n_raw - G::kSRaw : 0u; j < n_raw; ++j)
-        mbar_wait(smem_u32(&raw_full[j % G::kSRaw]), (j / G::kSRaw) & 1u);
+    for (uint32_t j = n_raw > (uint32_t)G::kSRaw ? n_raw - G::kSRaw : 0u; j < n_raw; ++j)
+      mbar_wait(smem_u32(&raw_full[j % G::kSRaw]), (j / G::kSRaw) & 1u);
     if (lead)
       for (uint32_t j = n_act > (uint32_t)G::kSAct ? n_act - G::kSAct : 0u; j < n_act; ++j)
         mbar_wait_cluster(smem_u32(&act_full[j % G::kSAct]), (j / G::kSAct) & 1u);
@@ -462,7 +437,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t idesc = idesc_f16_f32(2 * kTcM, (uint32_t)((t.n + 15) / 16 * 16));
-      const uint32_t d0 = tmem + buf * kAccCols;
+      const uint32_t d0 = tmem + buf * G::kAccCols;
       for (int ks = 0; ks < nks; ++ks, ++it) {
         if (*abort_flag) {
           ok = false;
@@ -520,10 +495,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) nrm[m][i] = 0;
       bool ok = true;
-      // One pipeline step: v holds this thread's int8 chunks of step ks (from
-      // the raw ring, or loaded straight from global memory).  Converts them into
-      // the conv ring (128-byte swizzled fp16 rows), sums squares for the guard,
-      // and hands the stage to the MMA thread.
+      // One pipeline step: v holds this thread's int8 chunks of the step, read
+      // from raw ring stage sr.  Converts them into the conv ring (128-byte
+      // swizzled fp16 rows), sums squares for the guard, and hands the stage to
+      // the MMA thread.
       // (int8 chunks [sub-step][matrix][4]: chunk c = ti + 128 i of a tile is
       // row c / 4, 16-byte column c % 4)
       auto step = [&](uint4 (&v)[G::kSub * NA][4], int sr) -> bool {
@@ -566,70 +541,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // the first CTA's MMA thread waits on this; the converted tile is
           // read by this CTA's own tensor core
           mbar_arrive_remote(lead_conv_full + 8u * sc);
-          if (!DIRECT) mbar_arrive(smem_u32(&raw_empty[sr]));
+          mbar_arrive(smem_u32(&raw_empty[sr]));
         }
         ++it;
         return true;
       };
-      if (!DIRECT) {
-        for (int ks = 0; ks < nks; ++ks) {
-          const int sr = it % G::kSRaw;
-          if (!warp_wait(smem_u32(&raw_full[sr]), (it / G::kSRaw) & 1u)) {
-            ok = false;
-            break;
-          }
-          const uint8_t* rawt = smem + G::kRawOff + sr * G::kRawBytes;
-          // all of this thread's 16-byte chunks are loaded before any store, so
-          // their latencies overlap (a store could alias a later load otherwise)
-          uint4 v[G::kSub * NA][4];
-#pragma unroll
-          for (int b = 0; b < G::kSub * NA; ++b)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int c = ti + 128 * i;
-              v[b][i] = *reinterpret_cast<const uint4*>(rawt + b * kRawTileBytes + (c >> 2) * kBK +
-                                                        (c & 3) * 16);
-            }
-          if (!step(v, sr)) {
-            ok = false;
-            break;
-          }
+      for (int ks = 0; ks < nks; ++ks) {
+        const int sr = it % G::kSRaw;
+        if (!warp_wait(smem_u32(&raw_full[sr]), (it / G::kSRaw) & 1u)) {
+          ok = false;
+          break;
         }
-      } else {
-        // direct: step ks + 1's chunks are in flight while step ks is converted
-        const size_t mat = (size_t)a.N * a.K;
-        const int8_t* W0 = a.w0 + (size_t)t.e * mat;
-        const int8_t* W1 = NA == 2 ? a.w1 + (size_t)t.e * mat : nullptr;
-        const int wrow = (t.ct * 2 + (int)rank) * kTcM;
-        auto load = [&](uint4 (&v)[G::kSub * NA][4], int ks) {
+        const uint8_t* rawt = smem + G::kRawOff + sr * G::kRawBytes;
+        // all of this thread's 16-byte chunks are loaded before any store, so
+        // their latencies overlap (a store could alias a later load otherwise)
+        uint4 v[G::kSub * NA][4];
 #pragma unroll
-          for (int b = 0; b < G::kSub * NA; ++b) {
-            const int u = b / NA, m = b % NA;
-            const int8_t* W = m == 0 ? W0 : W1;
+        for (int b = 0; b < G::kSub * NA; ++b)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int c = ti + 128 * i;
-              const int ch = wrow + (c >> 2);
-              const int kx = (ks * G::kSub + u) * kBK + (c & 3) * 16;
-              v[b][i] = (ch < a.N && kx < a.K) ? ld_nc_na_v4(W + (size_t)ch * a.K + kx)
-                                               : make_uint4(0u, 0u, 0u, 0u);
-            }
+          for (int i = 0; i < 4; ++i) {
+            const int c = ti + 128 * i;
+            v[b][i] = *reinterpret_cast<const uint4*>(rawt + b * kRawTileBytes + (c >> 2) * kBK +
+                                                      (c & 3) * 16);
           }
-        };
-        uint4 va[G::kSub * NA][4], vb[G::kSub * NA][4];
-        load(va, 0);
-        for (int ks = 0; ks < nks; ks += 2) {
-          if (ks + 1 < nks) load(vb, ks + 1);
-          if (!step(va, 0)) {
-            ok = false;
-            break;
-          }
-          if (ks + 1 >= nks) break;
-          if (ks + 2 < nks) load(va, ks + 2);
-          if (!step(vb, 0)) {
-            ok = false;
-            break;
-          }
+        if (!step(v, sr)) {
+          ok = false;
+          break;
         }
       }
       if (!ok && lane == 0) {
@@ -717,7 +654,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const long long wn0 = wnorm[(nb * 2 + 0) * kTcM + r];
       const long long wn1 = NA == 2 ? wnorm[(nb * 2 + 1) * kTcM + r] : 0;
-      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * G::kAccCols;
       bool bad = false;
       if (fused) {
         // Adds cannot be undone, so the CTA's half of the tile is judged as a
@@ -1155,6 +1092,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// int8 weights [outer][rows][K] in 64-byte x 128-row boxes.
 bool map_i8(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint64_t outer) {
   auto fn = encode_fn();
   if (!fn || !base) return false;
@@ -1199,19 +1137,7 @@ Args make_args(const Launch& L, const W8Pass& p) {
   a.N = p.N;
   a.status = L.status;
   a.sc = p.sc;
-  a.w0 = static_cast<const int8_t*>(p.w0);
-  a.w1 = static_cast<const int8_t*>(p.w1);
   return a;
-}
-
-// The converters load the int8 weights from global memory (DIRECT) when the
-// environment sets MOE_W8_DIRECT=1 (read once).
-bool w8_direct() {
-  static const bool on = [] {
-    const char* v = getenv("MOE_W8_DIRECT");
-    return v && v[0] == '1' && v[1] == 0;
-  }();
-  return on;
 }
 
 // Two-SM tiles (clusters of two CTAs), then the exact fallback for entries
@@ -1226,13 +1152,11 @@ bool launch_pair(const Launch& L, const W8Pass& p) {
   if (!ok) return false;
   const Args a = make_args(L, p);
   const int kind = MODE == kW8GateUp ? MOE_K_TC_GATE_UP : MOE_K_TC_DOWN;
-  const bool direct = w8_direct();
-  const auto kernel = direct ? w8a8_pair_kernel<MODE, true> : w8a8_pair_kernel<MODE, false>;
-  set_smem_attr_once(reinterpret_cast<const void*>(kernel), G::kSmemBytes,
-                     (direct ? kAttrW8DirectBase : kAttrW8Base) + MODE);
+  set_smem_attr_once(reinterpret_cast<const void*>(w8a8_pair_kernel<MODE>), G::kSmemBytes,
+                     kAttrW8Base + MODE);
   const int grid = std::max(2, L.num_sms & ~1);  // whole clusters of two
   launch_begin(L, kind);
-  launch_kernel(kernel, grid, kThreads, G::kSmemBytes, L.stream, maps, a);
+  launch_kernel(w8a8_pair_kernel<MODE>, grid, kThreads, G::kSmemBytes, L.stream, maps, a);
   launch_end(L, kind);
   launch_begin(L, MOE_K_W8_EXACT);
   launch_kernel(w8a8_exact_kernel<MODE>, L.num_sms, 256, 0, L.stream,
