@@ -221,15 +221,17 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel, algorithmic_bytes, wdtype):
+def traffic_for(kernel, algorithmic_bytes, wdtype, layer):
     """DRAM bytes of one launch: the committed ncu capture's ratio of DRAM bytes to
-    algorithmic bytes (taken on a smaller case of the same kernel; traffic grows
-    with the weight bytes streamed) times this launch's algorithmic bytes.  None
-    when there is no capture or the kernel source changed since it was taken."""
+    algorithmic bytes times this launch's algorithmic bytes.  A capture of this
+    layer itself is preferred; else one of a smaller case of the same kernel
+    (traffic grows with the weight bytes streamed).  None when there is no capture
+    or the kernel source changed since it was taken."""
     try:
-        rec = json.load(open(PROFILE_TABLE)).get(f"{kernel}/{wdtype}")
+        table = json.load(open(PROFILE_TABLE))
     except (OSError, ValueError):
         return None
+    rec = table.get(f"{kernel}/{wdtype}@{layer}") or table.get(f"{kernel}/{wdtype}")
     if not rec or rec.get("source_hash") != kernel_source_hash(rec["source_files"]):
         return None
     return rec["dram_bytes"] / rec["algorithmic_bytes"] * algorithmic_bytes
@@ -575,13 +577,13 @@ def roofline_of(args, res):
             achieved = kf / sec / 1e12
             roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tpeak,
                     "unit": "TFLOP/s", "frac": achieved / tpeak, "peak_source": tpeak_kind,
-                    "traffic": traffic_for(dom, kb, spec["wdtype"]),
+                    "traffic": traffic_for(dom, kb, spec["wdtype"], spec["name"]),
                     "algorithmic_flops_per_launch": kf, "avg_launch_ms": dom_ms / dom_n}
         else:
             achieved = kb / sec / 1e9
             roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
-                    "traffic": traffic_for(dom, kb, spec["wdtype"]),
+                    "traffic": traffic_for(dom, kb, spec["wdtype"], spec["name"]),
                     "algorithmic_bytes_per_launch": kb, "avg_launch_ms": dom_ms / dom_n}
     ms_step = res["ms_step"]
     layer_gbs = res["alg_bytes"] / (ms_step / 1e3) / 1e9

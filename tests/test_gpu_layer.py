@@ -203,3 +203,27 @@ def full_size_case(m, name, n_sample=4):
 @pytest.mark.parametrize("name", ["longcat", "dsv3", "pangu"])
 def test_full_size_decode_layers(m, name):
     full_size_case(m, name)
+
+
+def _bucket(spec, T):
+    m = T * spec["top_k"] / synth.n_experts(spec)
+    return next((i for i, v in enumerate([2, 8, 32, 128]) if m < v), 4)
+
+
+@pytest.mark.parametrize("name,T", [("longcat_s", 16), ("longcat_s", 48), ("dsv3_s", 128),
+                                    ("pangu_s", 456), ("dsv3_s", 1024)])
+def test_layer_in_every_load_bucket(m, name, T):
+    # One layer per load bucket of the tile-parameter table (expected picks per
+    # expert < 2, < 8, < 32, < 128, >= 128), with the tiling the table picks
+    # (moe_tile_choice), against the oracle.
+    spec = synth.spec(name, T=T, name=f"{name}_T{T}")
+    d = gs.inputs(spec)
+    ref = oracle_out(spec, d)
+    got = gs.run_layer(m, spec, d, out_fp32=True)
+    gs.check_out(got, ref, bf16_out=False, what=f"{name} T={T} bucket {_bucket(spec, T)}")
+
+
+def test_load_buckets_are_all_covered():
+    cases = [("longcat_s", 16), ("longcat_s", 48), ("dsv3_s", 128), ("pangu_s", 456),
+             ("dsv3_s", 1024)]
+    assert sorted(_bucket(synth.spec(n), T) for n, T in cases) == [0, 1, 2, 3, 4]
