@@ -145,19 +145,11 @@ __device__ __forceinline__ QTile decode_tile(const TcArgs& a, int tile, int ntas
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
-  pdl_wait();
   using G = Geom<MODE>;
   constexpr bool FFN = MODE == kTcFfn;
   extern __shared__ uint8_t smem_raw[];
   const int kind = MODE == kTcDown ? MOE_K_TC_DOWN : MOE_K_TC_GATE_UP;
-  const int ntasks = a.counts[a.task_slot];
-  const int ntiles_first = a.counts[a.tile_slot];
-  const int ntiles = ntiles_first + (FFN ? a.counts[a.tile_slot_dn] : 0);
-  if (ntiles <= 0 || (int)blockIdx.x >= ntiles) {  // uniform across the CTA
-    if (MODE != kTcGateUp && a.fin.ctr) finalize_if_last(a.fin);
-    return;
-  }
-
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // 1024-byte aligned ring (128-byte swizzle atoms), barriers after it
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -172,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq + kTileQueue);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // barriers and tensor maps first: they touch no global memory, so they run
+  // before the wait for the previous kernel of the stream
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
@@ -194,6 +187,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&maps.a0);
     prefetch_tensormap(&maps.b);
     if (MODE != kTcDown) prefetch_tensormap(&maps.a1);
+  }
+  pdl_wait();
+  const int ntasks = a.counts[a.task_slot];
+  const int ntiles_first = a.counts[a.tile_slot];
+  const int ntiles = ntiles_first + (FFN ? a.counts[a.tile_slot_dn] : 0);
+  if (ntiles <= 0 || (int)blockIdx.x >= ntiles) {  // uniform across the CTA
+    if (MODE != kTcGateUp && a.fin.ctr) finalize_if_last(a.fin);
+    return;
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), G::kTmemCols);
   tc_fence_before();

@@ -423,6 +423,27 @@ void launch_kernel(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cud
   cfg.numAttrs = pdl_enabled() ? 1 : 0;
   launch_note(cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...));
 }
+// The same with a cluster shape given at launch (for kernels whose cluster size
+// is chosen at run time).
+template <typename... P, typename... A>
+void launch_kernel_cluster(void (*kernel)(P...), dim3 grid, dim3 cluster, dim3 block, size_t smem,
+                           cudaStream_t stream, A&&... args) {
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster.x;
+  attr[0].val.clusterDim.y = cluster.y;
+  attr[0].val.clusterDim.z = cluster.z;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  launch_note(cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...));
+}
 // Status of the launches since the last call (MOE_OK or MOE_ERR_CUDA); resets it.
 moe_status launch_status_take();
 

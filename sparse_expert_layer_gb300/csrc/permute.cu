@@ -327,14 +327,14 @@ __global__ void __launch_bounds__(1024)
     sort_small_kernel(const int32_t* ids, int32_t* counts, int32_t* offsets, int32_t* s2e,
                       int32_t* e2s, int T, int k, int E, WlArgs wla, int build_wl,
                       DevStatus* st, SmallGather g) {
-  pdl_enter();
   extern __shared__ uint32_t sm[];  // bitmap [E][W], then offsets [E + 1]
   __shared__ int sh[32];
   const int tid = threadIdx.x;
   const int W = (T + 31) / 32, R = T * k;
   uint32_t* bm = sm;
   int32_t* off = reinterpret_cast<int32_t*>(sm + (size_t)E * W);
-  for (int i = tid; i < E * W; i += blockDim.x) bm[i] = 0u;
+  for (int i = tid; i < E * W; i += blockDim.x) bm[i] = 0u;  // shared only: before the wait
+  pdl_enter();
   __syncthreads();
   for (int r = tid; r < R; r += blockDim.x) {
     const int e = ids[r];

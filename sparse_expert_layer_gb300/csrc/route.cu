@@ -19,6 +19,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -439,34 +440,45 @@ __global__ void router_split_kernel(const float* w, uint16_t* out, int E, int H)
 // The same logits, x . W_r^T, with W_r split inside the kernel into three bf16
 // terms as above (W1 + W2 + W3 == W, every product exact in fp32), multiplied
 // by tcgen05 MMAs (kind::f16, fp32 accumulate).  A CTA owns 128 experts (the
-// MMA's M side) x 128 tokens (N) x one eighth of H:
+// MMA's M side) x up to 128 tokens (N) x one of SPLITS slices of H:
 //   - W_r arrives by TMA, one 128 x 64 fp32 box per K chunk, into a three-stage
-//     ring; x by TMA, 128 x 64 bf16 boxes, two stages;
+//     ring; x by TMA, boxes of 64 columns and as many rows as the batch needs
+//     (at most 128), two to four stages in 32 KB; both run two chunks ahead;
 //   - all threads split a chunk's weights into three bf16 planes (128-byte
 //     swizzle, the MMA's K-major layout; the planes are double-buffered, so the
 //     split of one chunk overlaps the MMAs of the one before), then the first
 //     thread issues the chunk's MMAs: the W3 and W2 products accumulate in one
 //     TMEM accumulator, the W1 products in another, so the small terms are never
 //     rounded against the large ones; the CTA's slice of the logits is the sum.
-// The eight CTAs of an (expert, token) tile form a cluster and add their slices
-// in rank order through distributed shared memory: the result does not depend
-// on scheduling, and no scratch memory is needed.
+// The SPLITS CTAs of an (expert, token) tile form a cluster (8, or 16 where H
+// has at least 32 chunks: half the chunks per CTA) and add their slices in rank
+// order through distributed shared memory: the result does not depend on
+// scheduling, and no scratch memory is needed.
 constexpr int kRcM = 128;                     // experts per tile (MMA M)
 constexpr int kRcN = 128;                     // tokens per tile (MMA N, rounded up to 16)
 constexpr int kRcK = 64;                      // K chunk: one 128-byte bf16 row
-constexpr int kRcSplits = 8;                  // CTAs per cluster, one H slice each
 constexpr int kRcThreads = 256;
 constexpr int kRcWStages = 3;
 constexpr int kRcWStage = kRcM * kRcK * 4;    // one fp32 W chunk (TMA box, 256-byte rows)
 constexpr int kRcPlane = kRcM * kRcK * 2;     // one bf16 term of a W chunk
 constexpr int kRcPlanes = 3 * kRcPlane;       // W3, W2, W1 of a chunk
-constexpr int kRcX = kRcN * kRcK * 2;         // one x chunk
+constexpr int kRcXBytes = 2 * kRcN * kRcK * 2;  // x stages: 2 x 128 rows, or more of fewer rows
+constexpr int kRcXMaxStages = 4;
 constexpr int kRcXOff = 2 * kRcPlanes;        // two plane buffers first
-constexpr int kRcWOff = kRcXOff + 2 * kRcX;
+constexpr int kRcWOff = kRcXOff + kRcXBytes;
 constexpr int kRcBarOff = kRcWOff + kRcWStages * kRcWStage;
 constexpr int kRcSmem = 1024 + kRcBarOff + 128;
 static_assert(kRcSmem <= 227 * 1024, "decode router shared memory");
 static_assert(kRcWStages * kRcWStage >= kRcN * kRcM * 4, "a logits slice fits in the W ring");
+
+// Rows of the decode router's x boxes for a batch of T tokens: the batch
+// rounded up to 16 (the MMA's N step), at most one 128-token tile.
+int rc_x_rows(int T) { return T >= kRcN ? kRcN : (T + 15) / 16 * 16; }
+// x stages in the 32 KB x region for boxes of `rows` rows.
+__host__ __device__ constexpr int rc_x_stages(int rows) {
+  return kRcXBytes / (rows * kRcK * 2) < kRcXMaxStages ? kRcXBytes / (rows * kRcK * 2)
+                                                        : kRcXMaxStages;
+}
 
 __device__ __forceinline__ uint32_t bf162_as_u32(__nv_bfloat162 v) {
   uint32_t u;
@@ -486,17 +498,18 @@ __device__ __forceinline__ void split3x2(float a, float b, uint32_t& p1, uint32_
 
 // With fuse_topk (all experts in one 128-expert tile) each CTA also scores and
 // picks the top-k of the tokens it reduced, from shared memory, so no logits
-// go to global memory and no top-k launch follows.
-__global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 1)
+// go to global memory and no top-k launch follows.  Launched with a cluster of
+// SPLITS CTAs along z; xrows = rc_x_rows(T), the x boxes' height.
+template <int SPLITS>
+__global__ void __launch_bounds__(kRcThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                      const __grid_constant__ CUtensorMap wmap, float* logits, int T, int E, int H,
-                     DevStatus* st, const TopkArgs tk, int fuse_topk) {
-  pdl_enter();
+                     int xrows, DevStatus* st, const TopkArgs tk, int fuse_topk) {
   extern __shared__ uint8_t rc_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(rc_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* x_full = reinterpret_cast<uint64_t*>(smem + kRcBarOff);  // [2]
-  uint64_t* w_full = x_full + 2;                                      // [kRcWStages]
+  uint64_t* x_full = reinterpret_cast<uint64_t*>(smem + kRcBarOff);  // [kRcXMaxStages]
+  uint64_t* w_full = x_full + kRcXMaxStages;                          // [kRcWStages]
   uint64_t* mma_done = w_full + kRcWStages;                           // [2], per plane buffer
   uint64_t* drain = mma_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -504,16 +517,18 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
   const int e0 = blockIdx.x * kRcM, t0 = blockIdx.y * kRcN;
   const int rank = (int)cluster_rank();  // this CTA's H slice
   const int nch_all = H / kRcK;
-  const int per = (nch_all + kRcSplits - 1) / kRcSplits;
+  const int per = (nch_all + SPLITS - 1) / SPLITS;
   const int c0 = min(nch_all, rank * per);
   const int nch = min(nch_all, c0 + per) - c0;
   const int rows = min(kRcN, T - t0);
   const uint32_t N = (uint32_t)((rows + 15) / 16 * 16);
+  const int nxs = rc_x_stages(xrows);
+  const uint32_t xstage = (uint32_t)xrows * kRcK * 2;
+  // set-up that touches no global memory runs before the wait for the
+  // previous kernel of the stream
   if (tid == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&x_full[b]), 1);
-      mbar_init(smem_u32(&mma_done[b]), 1);
-    }
+    for (int b = 0; b < kRcXMaxStages; ++b) mbar_init(smem_u32(&x_full[b]), 1);
+    for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&mma_done[b]), 1);
     for (int s = 0; s < kRcWStages; ++s) mbar_init(smem_u32(&w_full[s]), 1);
     mbar_init(smem_u32(drain), 1);
     fence_barrier_init();
@@ -525,6 +540,7 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_enter();
 
   const uint64_t pol_x = policy_evict_last(), pol_w = policy_evict_first();
   int nw = 0, nx = 0;  // copies issued (thread 0)
@@ -537,14 +553,16 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
     nw = i + 1;
   };
   auto x_copy = [&](int i) {
-    const uint32_t bar = smem_u32(&x_full[i & 1]);
-    mbar_arrive_expect_tx(bar, (uint32_t)kRcX);
-    tma_load_3d(smem_u32(smem + kRcXOff + (i & 1) * kRcX), &xmap, (c0 + i) * kRcK, t0, 0, bar,
+    const uint32_t bar = smem_u32(&x_full[i % nxs]);
+    mbar_arrive_expect_tx(bar, xstage);
+    tma_load_3d(smem_u32(smem + kRcXOff + (i % nxs) * xstage), &xmap, (c0 + i) * kRcK, t0, 0, bar,
                 pol_x);
     nx = i + 1;
   };
-  if (tid == 0)
+  if (tid == 0) {
     for (int i = 0; i < kRcWStages - 1 && i < nch; ++i) w_copy(i);
+    for (int i = 0; i < nxs && i < nch; ++i) x_copy(i);
+  }
   const uint32_t idesc = idesc_bf16_f32(kRcM, N);
   // A wait that runs out makes its thread report the timeout; the block learns
   // of it at the next barrier (uniformly, through __syncthreads_or) and stops:
@@ -553,14 +571,15 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
   // are still reached.  Thread 0 skips the MMAs of a chunk whose x it did not
   // see arrive but still commits, so the others' waits on mma_done end.
   bool fail = false, aborted = false;
-  int done = 0;  // chunks whose W and x were consumed (their copies landed)
+  int done = 0;  // chunks whose W was consumed (their copies landed)
   for (int i = 0; i < nch; ++i) {
     const int pbuf = i & 1;
-    // plane buffer pbuf and x stage pbuf are free once chunk i - 2's MMAs are done
+    // plane buffer pbuf, and the x stages of chunks up to i - 2, are free once
+    // chunk i - 2's MMAs are done (a commit covers every earlier MMA)
     if (i >= 2 && !mbar_wait(smem_u32(&mma_done[pbuf]), (uint32_t)((i - 2) >> 1) & 1u))
       fail = true;
     if (tid == 0 && !fail) {
-      x_copy(i);
+      while (nx < nch && nx <= i - 2 + nxs) x_copy(nx);
       // the W stage of chunk i - 1 was read before the last block barrier
       if (i + kRcWStages - 1 < nch) w_copy(i + kRcWStages - 1);
     }
@@ -591,9 +610,9 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
       break;
     }
     if (tid == 0) {
-      if (mbar_wait(smem_u32(&x_full[pbuf]), (uint32_t)(i >> 1) & 1u)) {
+      if (mbar_wait(smem_u32(&x_full[i % nxs]), (uint32_t)(i / nxs) & 1u)) {
         tc_fence_after();
-        const uint32_t xb = smem_u32(smem + kRcXOff + pbuf * kRcX);
+        const uint32_t xb = smem_u32(smem + kRcXOff + (i % nxs) * xstage);
         const uint32_t pb = smem_u32(planes);
 #pragma unroll
         for (int kk = 0; kk < kRcK / 16; ++kk) {
@@ -619,13 +638,14 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
   if (aborted && tid == 0) {
     raise_status(st, kStTimeout, MOE_K_ROUTER);
     // every MMA issued so far completes before TMEM is read or released, and
-    // every copy issued so far lands before the CTA can leave
+    // every copy issued so far lands before the CTA can leave (the newest copy
+    // of each stage; an older one of the same stage has been waited for)
     tc_commit(smem_u32(drain));
     mbar_wait(smem_u32(drain), 0u);
     for (int j = done; j < nw; ++j)
       mbar_wait(smem_u32(&w_full[j % kRcWStages]), (uint32_t)(j / kRcWStages) & 1u);
-    for (int j = max(0, nx - 2); j < nx; ++j)
-      mbar_wait(smem_u32(&x_full[j & 1]), (uint32_t)(j >> 1) & 1u);
+    for (int j = max(0, nx - nxs); j < nx; ++j)
+      mbar_wait(smem_u32(&x_full[j % nxs]), (uint32_t)(j / nxs) & 1u);
   }
   tc_fence_after();
   __syncthreads();  // the W ring is free for the slice
@@ -638,8 +658,9 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
       const int tc = half * 64 + cc * 32;
+      if (tc >= (int)N) continue;  // no token of this 32-column group in the tile
       uint32_t sm[32], bg[32];
-      if (!aborted && nch > 0 && tc < (int)N) {
+      if (!aborted && nch > 0) {
         const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + tc;
         tmem_ld32(ta, sm);
         tmem_ld32(ta + kRcN, bg);
@@ -654,41 +675,50 @@ __global__ void __cluster_dims__(1, 1, kRcSplits) __launch_bounds__(kRcThreads, 
     }
   }
   cluster_sync_all();  // every CTA's slice is in place
-  // fused top-k: the final logits of this CTA's 16 tokens, [token][expert], and
+  // fused top-k: the final logits of this CTA's tokens, [token][expert], and
   // a 3 * E float scratch per warp, in the (now idle) plane buffers
-  constexpr int kRcTokPerCta = kRcN / kRcSplits;
+  constexpr int kTokPerCta = kRcN / SPLITS;
   float* fin = reinterpret_cast<float*>(smem);
-  float* tk_scratch = fin + kRcTokPerCta * kRcM;
+  float* tk_scratch = fin + kTokPerCta * kRcM;
   {
-    // this CTA adds the eight slices, in rank order, for 16 of the tile's tokens:
-    // tokens rank, rank + 8, rank + 16, ... (interleaved, so that a batch of at
-    // most 64 tokens spreads one token per warp over the cluster)
-    const int el = tid % kRcM;
-    const int tl0 = (tid / kRcM) * (kRcTokPerCta / 2);
+    // this CTA adds the SPLITS slices, in rank order, for kTokPerCta of the
+    // tile's tokens: tokens rank, rank + SPLITS, rank + 2 SPLITS, ...
+    // (interleaved, so that a small batch spreads one token per warp over the
+    // cluster); a warp takes one token, a lane four adjacent experts (16-byte
+    // loads from each CTA's slice)
+    const int e4 = (tid % 32) * 4;
     const uint32_t base = smem_u32(slice);
 #pragma unroll 1
-    for (int u = 0; u < kRcTokPerCta / 2; ++u) {
-      const int t = (tl0 + u) * kRcSplits + rank;
+    for (int tl = tid / 32; tl < kTokPerCta; tl += kRcThreads / 32) {
+      const int t = tl * SPLITS + rank;
       if (t < rows) {
-        const uint32_t a = base + (uint32_t)((t * kRcM + el) * 4);
-        float v[kRcSplits];
+        const uint32_t a = base + (uint32_t)((t * kRcM + e4) * 4);
+        float4 v[SPLITS];
 #pragma unroll
-        for (int q = 0; q < kRcSplits; ++q) v[q] = ld_cluster_f32(mapa_shared(a, (uint32_t)q));
-        float sum = 0.f;
+        for (int q = 0; q < SPLITS; ++q) v[q] = ld_cluster_f32x4(mapa_shared(a, (uint32_t)q));
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int q = 0; q < kRcSplits; ++q) sum += v[q];
-        if (fuse_topk)
-          fin[(tl0 + u) * kRcM + el] = sum;
-        else if (e0 + el < E && !aborted)
-          logits[(size_t)(t0 + t) * E + e0 + el] = sum;
+        for (int q = 0; q < SPLITS; ++q) {
+          s4[0] += v[q].x;
+          s4[1] += v[q].y;
+          s4[2] += v[q].z;
+          s4[3] += v[q].w;
+        }
+        if (fuse_topk) {
+          *reinterpret_cast<float4*>(fin + tl * kRcM + e4) = make_float4(s4[0], s4[1], s4[2], s4[3]);
+        } else if (!aborted) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (e0 + e4 + j < E) logits[(size_t)(t0 + t) * E + e0 + e4 + j] = s4[j];
+        }
       }
     }
   }
   if (fuse_topk) {
     __syncthreads();
     if (!aborted)
-      for (int u = warp; u < kRcTokPerCta; u += kRcThreads / 32) {
-        const int t = u * kRcSplits + rank;
+      for (int u = warp; u < kTokPerCta; u += kRcThreads / 32) {
+        const int t = u * SPLITS + rank;
         if (t < rows) topk_token(tk, t0 + t, fin + u * kRcM, tk_scratch + warp * 3 * E);
       }
   }
@@ -725,14 +755,14 @@ bool rc_w_map(CUtensorMap* m, const float* w, int E, int H) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// x [T][H] bf16 as 128-token x 64-column boxes, 128-byte swizzle, rows past T
-// read as zero.
+// x [T][H] bf16 as rc_x_rows(T)-token x 64-column boxes, 128-byte swizzle, rows
+// past T read as zero.
 bool rc_x_map(CUtensorMap* m, const void* x, int T, int H) {
   auto fn = rc_encode_fn();
   if (!fn || !x) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)T, 1};
   const cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)T * H * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)kRcK, (cuuint32_t)kRcN, 1};
+  const cuuint32_t box[3] = {(cuuint32_t)kRcK, (cuuint32_t)rc_x_rows(T), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -770,14 +800,56 @@ int router_tiles(const moe_config& c, int T) {
 
 int router_splits_default(const moe_config& c, int T) { return router_splits(c, T, 152); }
 
+namespace {
+// H slices (CTAs per cluster) of the decode router for hidden size H: 16 where
+// H has at least 32 chunks, else 8.
+int rc_splits(int H) { return H / kRcK >= 32 ? 16 : 8; }
+
+// Whether clusters of 16 router CTAs (beyond the portable 8) can be placed on
+// this device; checked once per device.  Where they cannot, the router runs in
+// clusters of 8.
+bool rc_wide_clusters_ok() {
+  constexpr int kDev = 64;
+  static std::atomic<int> state[kDev];  // 0 unknown, 1 yes, 2 no
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kDev) return false;
+  const int v = state[d].load(std::memory_order_acquire);
+  if (v != 0) return v == 1;
+  const void* f = reinterpret_cast<const void*>(router_tc_kernel<16>);
+  bool ok = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                cudaSuccess &&
+            cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kRcSmem) ==
+                cudaSuccess;
+  if (ok) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 16;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 16);
+    cfg.blockDim = dim3(kRcThreads);
+    cfg.dynamicSmemBytes = kRcSmem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    ok = cudaOccupancyMaxActiveClusters(&n, router_tc_kernel<16>, &cfg) == cudaSuccess && n >= 1;
+  }
+  if (!ok) cudaGetLastError();  // a refused query leaves no error behind
+  state[d].store(ok ? 1 : 2, std::memory_order_release);
+  return ok;
+}
+}  // namespace
+
 bool router_tc_decode_chosen(const moe_config& c, int T) {
   // The tensor-core router runs where it has enough parallel work: at least 32
-  // CTAs, or at most four K chunks per CTA (a few-tile layer with a long H, such
-  // as 256 experts x 128 tokens x 7168, keeps the CUDA-core router's wider grid).
+  // CTAs, or at most four K chunks per CTA (a few-tile layer with a long H and
+  // clusters of 8 keeps the CUDA-core router's wider grid).
   const int E = c.n_routed + c.n_zero;
+  const int splits = rc_splits(c.hidden);
   const int rc_tiles = ((E + kRcM - 1) / kRcM) * ((T + kRcN - 1) / kRcN);
-  const int rc_chunks = (c.hidden / kRcK + kRcSplits - 1) / kRcSplits;
-  const bool rc_fits = rc_tiles * kRcSplits >= 32 || rc_chunks <= 4;
+  const int rc_chunks = (c.hidden / kRcK + splits - 1) / splits;
+  const bool rc_fits = rc_tiles * splits >= 32 || rc_chunks <= 4;
   return router_tc_decode_enabled() && c.hidden % kRcK == 0 && rc_fits;
 }
 
@@ -839,15 +911,26 @@ void launch_route(const Launch& L, const moe_config& c, int T, const void* x, co
   memset(&wmap, 0, sizeof wmap);
   if (router_tc_decode_chosen(c, T) && rc_x_map(&xmap, x, T, c.hidden) &&
       rc_w_map(&wmap, w_r, E, c.hidden)) {
-    // decode router on tensor cores: clusters of kRcSplits CTAs, one per H
+    // decode router on tensor cores: clusters of 8 or 16 CTAs, one per H
     // slice; with all experts in one tile and at most one token per warp of
-    // the cluster it also picks the top-k
-    const int fuse = (E <= kRcM && T <= kRcSplits * (kRcThreads / 32) && folds_enabled()) ? 1 : 0;
-    const dim3 g((E + kRcM - 1) / kRcM, (T + kRcN - 1) / kRcN, kRcSplits);
-    set_smem_attr_once(reinterpret_cast<const void*>(router_tc_kernel), kRcSmem, kAttrRouterTc);
+    // each CTA (clusters of 16: 8 of a tile's 128 tokens per CTA, whatever the
+    // batch; clusters of 8: batches of at most 64) it also picks the top-k
+    const int splits = rc_splits(c.hidden) == 16 && rc_wide_clusters_ok() ? 16 : 8;
+    constexpr int kWarps = kRcThreads / 32;
+    const bool one_per_warp = kRcN / splits <= kWarps || T <= splits * kWarps;
+    const int fuse = (E <= kRcM && one_per_warp && folds_enabled()) ? 1 : 0;
+    const dim3 g((E + kRcM - 1) / kRcM, (T + kRcN - 1) / kRcN, splits);
     launch_begin(L, MOE_K_ROUTER);
-    launch_kernel(router_tc_kernel, g, kRcThreads, kRcSmem, L.stream, xmap, wmap, logits, T, E,
-                  c.hidden, L.status, tk, fuse);
+    if (splits == 16) {
+      launch_kernel_cluster(router_tc_kernel<16>, g, dim3(1, 1, 16), kRcThreads, kRcSmem,
+                            L.stream, xmap, wmap, logits, T, E, c.hidden, rc_x_rows(T), L.status,
+                            tk, fuse);
+    } else {
+      set_smem_attr_once(reinterpret_cast<const void*>(router_tc_kernel<8>), kRcSmem,
+                         kAttrRouterTc);
+      launch_kernel_cluster(router_tc_kernel<8>, g, dim3(1, 1, 8), kRcThreads, kRcSmem, L.stream,
+                            xmap, wmap, logits, T, E, c.hidden, rc_x_rows(T), L.status, tk, fuse);
+    }
     launch_end(L, MOE_K_ROUTER);
     if (!fuse) launch_topk(L, tk, T);
     return;

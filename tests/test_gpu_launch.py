@@ -90,6 +90,22 @@ def test_plain_launches_give_the_same_bits(m, name, tmp_path):
     assert np.array_equal(got, plain)
 
 
+@pytest.mark.parametrize("name", ["tiny", "pangu_s", "longcat_s", "ragged_s"])
+def test_unfolded_launches_give_the_same_bits(m, name, tmp_path):
+    # MOE_FOLDS=0 (read once per process) runs the top-k, the re-sort, the
+    # gather and the finalize as launches of their own instead of in the last
+    # CTA of the kernel before; the outputs must be identical.
+    spec = synth.spec(name)
+    d = gs.inputs(spec)
+    got = gs.run_layer(m, spec, d, out_fp32=True, combine=m.COMBINE_ORDERED).cpu().numpy()
+    path = str(tmp_path / "unfolded.npy")
+    env = dict(os.environ, MOE_FOLDS="0", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-c", _PLAIN, ROOT, name, path], env=env, cwd=ROOT,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert np.array_equal(got, np.load(path))
+
+
 _ROUTE_CC = r"""
 import sys, numpy as np, torch
 sys.path.insert(0, sys.argv[1])
