@@ -444,12 +444,13 @@ __global__ void router_split_kernel(const float* w, uint16_t* out, int E, int H)
 //   - W_r arrives by TMA, one 128 x 64 fp32 box per K chunk, into a three-stage
 //     ring; x by TMA, boxes of 64 columns and as many rows as the batch needs
 //     (at most 128), two to four stages in 32 KB; both run two chunks ahead;
-//   - all threads split a chunk's weights into three bf16 planes (128-byte
-//     swizzle, the MMA's K-major layout; the planes are double-buffered, so the
-//     split of one chunk overlaps the MMAs of the one before), then the first
-//     thread issues the chunk's MMAs: the W3 and W2 products accumulate in one
-//     TMEM accumulator, the W1 products in another, so the small terms are never
-//     rounded against the large ones; the CTA's slice of the logits is the sum.
+//   - eight warps split a chunk's weights into three bf16 planes (128-byte
+//     swizzle, the MMA's K-major layout; the planes are double-buffered), and a
+//     ninth warp issues the chunk's MMAs while they split the next one: the W3
+//     and W2 products accumulate in one TMEM accumulator, the W1 products in
+//     another, so the small terms are never rounded against the large ones; the
+//     CTA's slice of the logits is the sum.  Warps hand stages to each other by
+//     mbarriers (W stage read, planes written, MMAs done), not block barriers.
 // The SPLITS CTAs of an (expert, token) tile form a cluster (8, or 16 where H
 // has at least 32 chunks: half the chunks per CTA) and add their slices in rank
 // order through distributed shared memory: the result does not depend on
@@ -457,7 +458,9 @@ __global__ void router_split_kernel(const float* w, uint16_t* out, int E, int H)
 constexpr int kRcM = 128;                     // experts per tile (MMA M)
 constexpr int kRcN = 128;                     // tokens per tile (MMA N, rounded up to 16)
 constexpr int kRcK = 64;                      // K chunk: one 128-byte bf16 row
-constexpr int kRcThreads = 256;
+constexpr int kRcSplitThreads = 256;       // warps 0-7: TMA (thread 0), split, epilogue
+constexpr int kRcSplitWarps = kRcSplitThreads / 32;
+constexpr int kRcThreads = kRcSplitThreads + 32;  // warp 8: MMA issue
 constexpr int kRcWStages = 3;
 constexpr int kRcWStage = kRcM * kRcK * 4;    // one fp32 W chunk (TMA box, 256-byte rows)
 constexpr int kRcPlane = kRcM * kRcK * 2;     // one bf16 term of a W chunk
@@ -467,7 +470,7 @@ constexpr int kRcXMaxStages = 4;
 constexpr int kRcXOff = 2 * kRcPlanes;        // two plane buffers first
 constexpr int kRcWOff = kRcXOff + kRcXBytes;
 constexpr int kRcBarOff = kRcWOff + kRcWStages * kRcWStage;
-constexpr int kRcSmem = 1024 + kRcBarOff + 128;
+constexpr int kRcSmem = 1024 + kRcBarOff + 192;
 static_assert(kRcSmem <= 227 * 1024, "decode router shared memory");
 static_assert(kRcWStages * kRcWStage >= kRcN * kRcM * 4, "a logits slice fits in the W ring");
 
@@ -510,9 +513,12 @@ __global__ void __launch_bounds__(kRcThreads, 1)
       (reinterpret_cast<uintptr_t>(rc_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* x_full = reinterpret_cast<uint64_t*>(smem + kRcBarOff);  // [kRcXMaxStages]
   uint64_t* w_full = x_full + kRcXMaxStages;                          // [kRcWStages]
-  uint64_t* mma_done = w_full + kRcWStages;                           // [2], per plane buffer
+  uint64_t* w_empty = w_full + kRcWStages;                            // [kRcWStages]
+  uint64_t* planes_full = w_empty + kRcWStages;                       // [2], per plane buffer
+  uint64_t* mma_done = planes_full + 2;                               // [2], per plane buffer
   uint64_t* drain = mma_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int e0 = blockIdx.x * kRcM, t0 = blockIdx.y * kRcN;
   const int rank = (int)cluster_rank();  // this CTA's H slice
@@ -528,9 +534,16 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   // previous kernel of the stream
   if (tid == 0) {
     for (int b = 0; b < kRcXMaxStages; ++b) mbar_init(smem_u32(&x_full[b]), 1);
-    for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&mma_done[b]), 1);
-    for (int s = 0; s < kRcWStages; ++s) mbar_init(smem_u32(&w_full[s]), 1);
+    for (int s = 0; s < kRcWStages; ++s) {
+      mbar_init(smem_u32(&w_full[s]), 1);
+      mbar_init(smem_u32(&w_empty[s]), kRcSplitWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&planes_full[b]), kRcSplitWarps);
+      mbar_init(smem_u32(&mma_done[b]), 1);
+    }
     mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&xmap);
     prefetch_tensormap(&wmap);
@@ -559,100 +572,126 @@ __global__ void __launch_bounds__(kRcThreads, 1)
                 pol_x);
     nx = i + 1;
   };
-  if (tid == 0) {
-    for (int i = 0; i < kRcWStages - 1 && i < nch; ++i) w_copy(i);
-    for (int i = 0; i < nxs && i < nch; ++i) x_copy(i);
-  }
-  const uint32_t idesc = idesc_bf16_f32(kRcM, N);
-  // A wait that runs out makes its thread report the timeout; the block learns
-  // of it at the next barrier (uniformly, through __syncthreads_or) and stops:
-  // no further copies or MMAs are issued, the ones in flight are waited for,
+  // A wait that runs out makes its thread report the timeout and set the abort
+  // flag; every role checks it before its next chunk and stops.  After the
+  // loops, the MMAs issued so far and the copies issued so far are waited for,
   // the logits are not written, and the cluster barriers and the TMEM release
-  // are still reached.  Thread 0 skips the MMAs of a chunk whose x it did not
-  // see arrive but still commits, so the others' waits on mma_done end.
-  bool fail = false, aborted = false;
-  int done = 0;  // chunks whose W was consumed (their copies landed)
-  for (int i = 0; i < nch; ++i) {
-    const int pbuf = i & 1;
-    // plane buffer pbuf, and the x stages of chunks up to i - 2, are free once
-    // chunk i - 2's MMAs are done (a commit covers every earlier MMA)
-    if (i >= 2 && !mbar_wait(smem_u32(&mma_done[pbuf]), (uint32_t)((i - 2) >> 1) & 1u))
-      fail = true;
-    if (tid == 0 && !fail) {
-      while (nx < nch && nx <= i - 2 + nxs) x_copy(nx);
-      // the W stage of chunk i - 1 was read before the last block barrier
-      if (i + kRcWStages - 1 < nch) w_copy(i + kRcWStages - 1);
-    }
-    if (!fail && !mbar_wait(smem_u32(&w_full[i % kRcWStages]), (uint32_t)(i / kRcWStages) & 1u))
-      fail = true;
-    // split: a quarter warp takes one W row, eight 16-byte plane chunks of it
-    const uint8_t* wst = smem + kRcWOff + (i % kRcWStages) * kRcWStage;
-    uint8_t* planes = smem + pbuf * kRcPlanes;
-#pragma unroll
-    for (int m = 0; m < kRcM * 8 / kRcThreads; ++m) {
-      const int u = tid + m * kRcThreads;
-      const int r = u >> 3, j = u & 7;
-      const float4 va = *reinterpret_cast<const float4*>(wst + r * kRcK * 4 + j * 32);
-      const float4 vb = *reinterpret_cast<const float4*>(wst + r * kRcK * 4 + j * 32 + 16);
-      uint4 q1, q2, q3;
-      split3x2(va.x, va.y, q1.x, q2.x, q3.x);
-      split3x2(va.z, va.w, q1.y, q2.y, q3.y);
-      split3x2(vb.x, vb.y, q1.z, q2.z, q3.z);
-      split3x2(vb.z, vb.w, q1.w, q2.w, q3.w);
-      const int off = r * 128 + ((j ^ (r & 7)) * 16);
-      *reinterpret_cast<uint4*>(planes + 0 * kRcPlane + off) = q3;
-      *reinterpret_cast<uint4*>(planes + 1 * kRcPlane + off) = q2;
-      *reinterpret_cast<uint4*>(planes + 2 * kRcPlane + off) = q1;
-    }
-    fence_proxy_async_smem();
-    if (__syncthreads_or(fail ? 1 : 0)) {
-      aborted = true;
-      break;
-    }
+  // are still reached.
+  auto fail_now = [&]() {
+    raise_status(st, kStTimeout, MOE_K_ROUTER);
+    *abort_flag = 1;
+  };
+  if (warp < kRcSplitWarps) {
+    // ------------------------------------------------- copies and split --
     if (tid == 0) {
-      if (mbar_wait(smem_u32(&x_full[i % nxs]), (uint32_t)(i / nxs) & 1u)) {
-        tc_fence_after();
-        const uint32_t xb = smem_u32(smem + kRcXOff + (i % nxs) * xstage);
-        const uint32_t pb = smem_u32(planes);
-#pragma unroll
-        for (int kk = 0; kk < kRcK / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(xb + kk * 32);
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_bf16(tmem, sdesc_sw128(pb + 0 * kRcPlane + kk * 32), bd, idesc, acc);  // W3
-          tc_mma_bf16(tmem, sdesc_sw128(pb + 1 * kRcPlane + kk * 32), bd, idesc, 1u);   // W2
-          tc_mma_bf16(tmem + kRcN, sdesc_sw128(pb + 2 * kRcPlane + kk * 32), bd, idesc,
-                      acc);  // W1
+      for (int i = 0; i < kRcWStages - 1 && i < nch; ++i) w_copy(i);
+      for (int i = 0; i < nxs && i < nch; ++i) x_copy(i);
+    }
+    for (int i = 0; i < nch; ++i) {
+      if (warp_flag(abort_flag)) break;
+      const int pbuf = i & 1;
+      // plane buffer pbuf, and the x stages of chunks up to i - 2, are free
+      // once chunk i - 2's MMAs are done (a commit covers every earlier MMA)
+      bool ok = i < 2 || warp_wait(smem_u32(&mma_done[pbuf]), (uint32_t)((i - 2) >> 1) & 1u);
+      if (ok && tid == 0) {
+        while (nx < nch && nx <= i - 2 + nxs) x_copy(nx);
+        // chunk i + 2 goes to the stage of chunk i - 1, free once every split
+        // warp has read it
+        if (i + kRcWStages - 1 < nch) {
+          if (i >= 1 && !mbar_wait(smem_u32(&w_empty[(i - 1) % kRcWStages]),
+                                   (uint32_t)((i - 1) / kRcWStages) & 1u))
+            fail_now();
+          else
+            w_copy(i + kRcWStages - 1);
         }
-      } else {
-        fail = true;  // reported; the next barrier stops the block
+      }
+      ok = ok && warp_wait(smem_u32(&w_full[i % kRcWStages]), (uint32_t)(i / kRcWStages) & 1u);
+      if (!ok) {
+        if (lane == 0) fail_now();
+        break;
+      }
+      // split: a quarter warp takes one W row, eight 16-byte plane chunks of it
+      const uint8_t* wst = smem + kRcWOff + (i % kRcWStages) * kRcWStage;
+      uint8_t* planes = smem + pbuf * kRcPlanes;
+#pragma unroll
+      for (int m = 0; m < kRcM * 8 / kRcSplitThreads; ++m) {
+        const int u = tid + m * kRcSplitThreads;
+        const int r = u >> 3, j = u & 7;
+        const float4 va = *reinterpret_cast<const float4*>(wst + r * kRcK * 4 + j * 32);
+        const float4 vb = *reinterpret_cast<const float4*>(wst + r * kRcK * 4 + j * 32 + 16);
+        uint4 q1, q2, q3;
+        split3x2(va.x, va.y, q1.x, q2.x, q3.x);
+        split3x2(va.z, va.w, q1.y, q2.y, q3.y);
+        split3x2(vb.x, vb.y, q1.z, q2.z, q3.z);
+        split3x2(vb.z, vb.w, q1.w, q2.w, q3.w);
+        const int off = r * 128 + ((j ^ (r & 7)) * 16);
+        *reinterpret_cast<uint4*>(planes + 0 * kRcPlane + off) = q3;
+        *reinterpret_cast<uint4*>(planes + 1 * kRcPlane + off) = q2;
+        *reinterpret_cast<uint4*>(planes + 2 * kRcPlane + off) = q1;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&w_empty[i % kRcWStages]));
+        mbar_arrive(smem_u32(&planes_full[pbuf]));
+      }
+    }
+  } else if (lane == 0) {
+    // ---------------------------------------------------------- MMA issue --
+    const uint32_t idesc = idesc_bf16_f32(kRcM, N);
+    for (int i = 0; i < nch; ++i) {
+      if (*abort_flag) break;
+      const int pbuf = i & 1;
+      if (!mbar_wait(smem_u32(&planes_full[pbuf]), (uint32_t)(i >> 1) & 1u) ||
+          !mbar_wait(smem_u32(&x_full[i % nxs]), (uint32_t)(i / nxs) & 1u)) {
+        fail_now();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t xb = smem_u32(smem + kRcXOff + (i % nxs) * xstage);
+      const uint32_t pb = smem_u32(smem + pbuf * kRcPlanes);
+#pragma unroll
+      for (int kk = 0; kk < kRcK / 16; ++kk) {
+        const uint64_t bd = sdesc_sw128(xb + kk * 32);
+        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+        tc_mma_bf16(tmem, sdesc_sw128(pb + 0 * kRcPlane + kk * 32), bd, idesc, acc);  // W3
+        tc_mma_bf16(tmem, sdesc_sw128(pb + 1 * kRcPlane + kk * 32), bd, idesc, 1u);   // W2
+        tc_mma_bf16(tmem + kRcN, sdesc_sw128(pb + 2 * kRcPlane + kk * 32), bd, idesc,
+                    acc);  // W1
       }
       tc_commit(smem_u32(&mma_done[pbuf]));
     }
-    done = i + 1;
   }
+  __syncthreads();
   // the last commit covers every MMA of the CTA
-  if (!aborted && nch > 0 &&
+  bool fail = false;
+  if (!*abort_flag && nch > 0 &&
       !mbar_wait(smem_u32(&mma_done[(nch - 1) & 1]), (uint32_t)((nch - 1) >> 1) & 1u))
     fail = true;
-  if (__syncthreads_or(fail ? 1 : 0)) aborted = true;
-  if (aborted && tid == 0) {
-    raise_status(st, kStTimeout, MOE_K_ROUTER);
-    // every MMA issued so far completes before TMEM is read or released, and
-    // every copy issued so far lands before the CTA can leave (the newest copy
-    // of each stage; an older one of the same stage has been waited for)
-    tc_commit(smem_u32(drain));
-    mbar_wait(smem_u32(drain), 0u);
-    for (int j = done; j < nw; ++j)
-      mbar_wait(smem_u32(&w_full[j % kRcWStages]), (uint32_t)(j / kRcWStages) & 1u);
-    for (int j = max(0, nx - nxs); j < nx; ++j)
-      mbar_wait(smem_u32(&x_full[j % nxs]), (uint32_t)(j / nxs) & 1u);
+  const bool aborted = __syncthreads_or(fail || *abort_flag ? 1 : 0) != 0;
+  if (aborted) {
+    if (fail) raise_status(st, kStTimeout, MOE_K_ROUTER);
+    // every MMA issued so far completes before TMEM is read or released (the
+    // issuing thread's commit covers them), and every copy issued so far lands
+    // before the CTA can leave (the newest copy of each stage; an older one of
+    // the same stage has been waited for)
+    if (warp == kRcSplitWarps && lane == 0) {
+      tc_commit(smem_u32(drain));
+      mbar_wait(smem_u32(drain), 0u);
+    }
+    if (tid == 0) {
+      for (int j = max(0, nw - kRcWStages); j < nw; ++j)
+        mbar_wait(smem_u32(&w_full[j % kRcWStages]), (uint32_t)(j / kRcWStages) & 1u);
+      for (int j = max(0, nx - nxs); j < nx; ++j)
+        mbar_wait(smem_u32(&x_full[j % nxs]), (uint32_t)(j / nxs) & 1u);
+    }
   }
   tc_fence_after();
   __syncthreads();  // the W ring is free for the slice
 
   // this CTA's slice, [token][expert]: small-term sum + W1 sum
   float* slice = reinterpret_cast<float*>(smem + kRcWOff);
-  {
+  if (warp < kRcSplitWarps) {
     const int quad = warp % 4, half = warp / 4;  // TMEM lane quadrant, token half
     const int el = quad * 32 + lane;
 #pragma unroll
@@ -680,7 +719,7 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   constexpr int kTokPerCta = kRcN / SPLITS;
   float* fin = reinterpret_cast<float*>(smem);
   float* tk_scratch = fin + kTokPerCta * kRcM;
-  {
+  if (warp < kRcSplitWarps) {
     // this CTA adds the SPLITS slices, in rank order, for kTokPerCta of the
     // tile's tokens: tokens rank, rank + SPLITS, rank + 2 SPLITS, ...
     // (interleaved, so that a small batch spreads one token per warp over the
@@ -689,7 +728,7 @@ __global__ void __launch_bounds__(kRcThreads, 1)
     const int e4 = (tid % 32) * 4;
     const uint32_t base = smem_u32(slice);
 #pragma unroll 1
-    for (int tl = tid / 32; tl < kTokPerCta; tl += kRcThreads / 32) {
+    for (int tl = warp; tl < kTokPerCta; tl += kRcSplitWarps) {
       const int t = tl * SPLITS + rank;
       if (t < rows) {
         const uint32_t a = base + (uint32_t)((t * kRcM + e4) * 4);
@@ -716,8 +755,8 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   }
   if (fuse_topk) {
     __syncthreads();
-    if (!aborted)
-      for (int u = warp; u < kTokPerCta; u += kRcThreads / 32) {
+    if (!aborted && warp < kRcSplitWarps)
+      for (int u = warp; u < kTokPerCta; u += kRcSplitWarps) {
         const int t = u * SPLITS + rank;
         if (t < rows) topk_token(tk, t0 + t, fin + u * kRcM, tk_scratch + warp * 3 * E);
       }
@@ -916,7 +955,7 @@ void launch_route(const Launch& L, const moe_config& c, int T, const void* x, co
     // each CTA (clusters of 16: 8 of a tile's 128 tokens per CTA, whatever the
     // batch; clusters of 8: batches of at most 64) it also picks the top-k
     const int splits = rc_splits(c.hidden) == 16 && rc_wide_clusters_ok() ? 16 : 8;
-    constexpr int kWarps = kRcThreads / 32;
+    constexpr int kWarps = kRcSplitWarps;
     const bool one_per_warp = kRcN / splits <= kWarps || T <= splits * kWarps;
     const int fuse = (E <= kRcM && one_per_warp && folds_enabled()) ? 1 : 0;
     const dim3 g((E + kRcM - 1) / kRcM, (T + kRcN - 1) / kRcN, splits);
