@@ -39,6 +39,7 @@ constexpr int kATileBytes = kTcM * kBK * 2;      // 16 KB
 constexpr int kBTileBytes = kTcMaxN * kBK * 2;   // 16 KB
 constexpr int kBoxRows = 64;
 constexpr int kBoxBytes = kBoxRows * kBK * 2;    // 8 KB
+constexpr int kTaskCache = 1024;                 // work-list tasks kept in shared memory
 
 // Pass of a launch: the down projection, the gate/up projection with SwiGLU,
 // or both in one launch (every gate/up tile, then every down tile; a down tile
@@ -53,7 +54,10 @@ struct Geom {
   static constexpr int kTmemCols = MODE == kTcDown ? 256 : 512;
   static constexpr int kAccStride = MODE == kTcDown ? 128 : 256;  // columns per accumulator buffer
   static constexpr int kBarBytes = 512;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  // the work list's tile starts and tasks, when it has at most kTaskCache tasks
+  static constexpr int kCacheOff = kStages * kStageBytes + kBarBytes;
+  static constexpr int kCacheBytes = kTaskCache * (2 * 4 + (int)sizeof(FfnTask));
+  static constexpr int kSmemBytes = 1024 + kCacheOff + kCacheBytes;
 };
 
 struct TcMaps {
@@ -126,12 +130,14 @@ __device__ __forceinline__ bool packed_down(bool gu, int n) {
 }
 static_assert(2 * kPackedStep <= Geom<kTcFfn>::kStageBytes, "two packed K steps fill a stage");
 
-__device__ __forceinline__ QTile decode_tile(const TcArgs& a, int tile, int ntasks, int gu,
+// tasks and start: the work list in shared memory when it fits, else in global
+// memory (a binary search of dependent loads).
+__device__ __forceinline__ QTile decode_tile(const FfnTask* tasks, int tile, int ntasks, int gu,
                                              const int32_t* start) {
   QTile t;
   int task;
-  tc_tile_of(a.tasks, start, ntasks, tile, &task, &t.ct);
-  const FfnTask tk = a.tasks[task];
+  tc_tile_of(tasks, start, ntasks, tile, &task, &t.ct);
+  const FfnTask tk = tasks[task];
   t.tile = tile;
   t.row0 = tk.row0;
   t.n = tk.nrows;
@@ -196,11 +202,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (MODE != kTcGateUp && a.fin.ctr) finalize_if_last(a.fin);
     return;
   }
+  // the work list's starts and tasks, in one round of parallel loads, so the
+  // scheduler's decodes read shared memory
+  int32_t* s_start = reinterpret_cast<int32_t*>(smem + G::kCacheOff);
+  int32_t* s_start_dn = s_start + kTaskCache;
+  FfnTask* s_tasks = reinterpret_cast<FfnTask*>(s_start_dn + kTaskCache);
+  const bool cached = ntasks <= kTaskCache;
+  if (cached)
+    for (int i = threadIdx.x; i < ntasks; i += blockDim.x) {
+      s_start[i] = a.tile_start[i];
+      if (FFN) s_start_dn[i] = a.tile_start_dn[i];
+      s_tasks[i] = a.tasks[i];
+    }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), G::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const FfnTask* d_tasks = cached ? s_tasks : a.tasks;
+  const int32_t* d_start = cached ? s_start : a.tile_start;
+  const int32_t* d_start_dn = cached ? s_start_dn : a.tile_start_dn;
 
   if (warp == kSchedWarp && lane == 0) {
     // ---------------------------------------------------------- scheduler --
@@ -212,9 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!*abort_flag) {
         const int tile = atomicAdd(a.sched, 1);
         if (tile < ntiles_first)
-          t = decode_tile(a, tile, ntasks, MODE != kTcDown, a.tile_start);
+          t = decode_tile(d_tasks, tile, ntasks, MODE != kTcDown, d_start);
         else if (tile < ntiles)
-          t = decode_tile(a, tile - ntiles_first, ntasks, 0, a.tile_start_dn);
+          t = decode_tile(d_tasks, tile - ntiles_first, ntasks, 0, d_start_dn);
       }
       if (!tq_push(tq, tq_full, tq_empty, n, t)) {
         raise_status(a.status, kStTimeout, kind);

@@ -236,8 +236,49 @@ __device__ int block_exclusive_scan(int v, int* tot, int* sh) {
   return excl;
 }
 
+// Exclusive scans of N values per thread across the block at once (three block
+// barriers for all N); sh holds 32 * N ints.
+template <int N>
+__device__ void block_exclusive_scan_n(const int (&v)[N], int (&excl)[N], int (&tot)[N], int* sh) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32, nw = blockDim.x / 32;
+  int incl[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) incl[i] = v[i];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int n = __shfl_up_sync(0xffffffffu, incl[i], o);
+      if (lane >= o) incl[i] += n;
+    }
+  if (lane == 31)
+#pragma unroll
+    for (int i = 0; i < N; ++i) sh[i * 32 + warp] = incl[i];
+  __syncthreads();
+  if (warp == 0)
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      int w = lane < nw ? sh[i * 32 + lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += n;
+      }
+      sh[i * 32 + lane] = w;
+    }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    excl[i] = (warp > 0 ? sh[i * 32 + warp - 1] : 0) + incl[i] - v[i];
+    tot[i] = sh[i * 32 + nw - 1];
+  }
+  __syncthreads();
+}
+
+constexpr int kWlScanInts = 32 * 6;  // shared scratch of build_worklist
+
 // Builds the work list from the experts' offsets; called by all threads of a
-// 1024-thread CTA (block-wide scans inside).
+// 1024-thread CTA (block-wide scans inside; sh holds kWlScanInts ints).
 __device__ void build_worklist(const WlArgs& a, const int32_t* offsets, int* sh) {
   int carry[6] = {0, 0, 0, 0, 0, 0};
   const int units = a.E_r + (a.has_shared ? 1 : 0);
@@ -259,12 +300,14 @@ __device__ void build_worklist(const WlArgs& a, const int32_t* offsets, int* sh)
     const int n_tc = (!gemv && n > 0) ? (n + a.tc_chunk - 1) / a.tc_chunk : 0;
     const int gi_gu = shared ? a.items_gu_shared : a.items_gu;
     const int ti_gu = shared ? a.tiles_gu_shared : a.tiles_gu;
-    int v[6] = {n_gemv, n_gemv * gi_gu, n_gemv * a.items_dn, n_tc, n_tc * ti_gu, n_tc * a.tiles_dn};
-    int pos[6];
+    const int v[6] = {n_gemv, n_gemv * gi_gu, n_gemv * a.items_dn, n_tc, n_tc * ti_gu,
+                      n_tc * a.tiles_dn};
+    int pos[6], tot[6];
+    block_exclusive_scan_n<6>(v, pos, tot, sh);
+#pragma unroll
     for (int i = 0; i < 6; ++i) {
-      int tot;
-      pos[i] = carry[i] + block_exclusive_scan(v[i], &tot, sh);
-      carry[i] += tot;
+      pos[i] += carry[i];
+      carry[i] += tot[i];
     }
     for (int j = 0; j < n_gemv; ++j) {
       const int ti = pos[0] + j;
@@ -314,7 +357,7 @@ __device__ void build_worklist(const WlArgs& a, const int32_t* offsets, int* sh)
 
 __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
   pdl_enter();
-  __shared__ int sh[32];
+  __shared__ int sh[kWlScanInts];
   build_worklist(a, a.offsets, sh);
 }
 
@@ -328,7 +371,7 @@ __global__ void __launch_bounds__(1024)
                       int32_t* e2s, int T, int k, int E, WlArgs wla, int build_wl,
                       DevStatus* st, SmallGather g) {
   extern __shared__ uint32_t sm[];  // bitmap [E][W], then offsets [E + 1]
-  __shared__ int sh[32];
+  __shared__ int sh[kWlScanInts];
   const int tid = threadIdx.x;
   const int W = (T + 31) / 32, R = T * k;
   uint32_t* bm = sm;
