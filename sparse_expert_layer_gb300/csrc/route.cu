@@ -882,8 +882,9 @@ bool rc_wide_clusters_ok() {
 
 bool router_tc_decode_chosen(const moe_config& c, int T) {
   // The tensor-core router runs where it has enough parallel work: at least 32
-  // CTAs, or at most four K chunks per CTA (a few-tile layer with a long H and
-  // clusters of 8 keeps the CUDA-core router's wider grid).
+  // CTAs, or at most four K chunks per CTA (a single-tile layer with a long H,
+  // 16 CTAs with more than four chunks each, keeps the CUDA-core router's wider
+  // grid).
   const int E = c.n_routed + c.n_zero;
   const int splits = rc_splits(c.hidden);
   const int rc_tiles = ((E + kRcM - 1) / kRcM) * ((T + kRcN - 1) / kRcN);

@@ -56,6 +56,29 @@ def test_route_on_tensor_cores_matches_oracle(m):
     assert np.allclose(w, w_o, rtol=1e-5, atol=1e-7), f"max rel {rel.max():.3e}"
 
 
+@pytest.mark.parametrize("name,over", [
+    # H = 2112: 33 chunks of 64 over clusters of 16 CTAs (three chunks each, the last
+    # five CTAs none); 200 tokens (a full and a ragged 72-token tile) x 200 experts
+    # (a full and a ragged 72-expert tile); the top-k kernel afterwards
+    ("wide_ragged", dict(T=200, hidden=2112, n_routed=150, n_zero=50, top_k=6)),
+    # all 96 experts in one tile, 300 tokens in three token tiles (the last one 44
+    # rows): the router CTAs pick the top-k themselves, one token per warp
+    ("wide_fused", dict(T=300, hidden=2048, n_routed=64, n_zero=32, top_k=4,
+                        renormalize=True)),
+    # the same with per-group (MoGE) selection over 8 groups
+    ("wide_fused_groups", dict(T=300, hidden=2048, n_routed=64, n_zero=0, top_k=8, n_group=8,
+                               per_group_k=1, bias_mode="none", bias_kind="none")),
+])
+def test_route_in_clusters_of_16_matches_oracle(m, name, over):
+    spec = synth.spec("longcat_s", name=name, **over)
+    d = _route_inputs(spec)
+    ids, w = route_gpu(m, spec, d)
+    ids_o, w_o, _, _ = oracle.route(spec, synth.bf16_bits(d["x"]), d["w_r"].numpy(),
+                                    support.np_bias(d["bias"]))
+    assert np.array_equal(ids, ids_o)
+    assert np.allclose(w, w_o, rtol=1e-5, atol=1e-7)
+
+
 def _route_inputs(spec):
     x, w_r, bias, _ = support.make_inputs(spec)
     return dict(x=x, w_r=w_r, bias=bias, x_d=x.cuda(), w_r_d=w_r.cuda(),
@@ -63,10 +86,10 @@ def _route_inputs(spec):
 
 
 def test_route_on_cuda_cores_by_default_matches_oracle(m):
-    # 128 tokens x 256 experts x H = 4096: two 128 x 128 tiles with eight K
-    # chunks per CTA, the shape class (few tiles, long H) that keeps the
-    # CUDA-core router and its split-K reduction
-    spec = synth.spec("dsv3_s", hidden=4096, n_routed=256, name="router_cc")
+    # 128 tokens x 128 experts x H = 6144: one 128 x 128 tile, so 16 CTAs with six
+    # K chunks each on tensor cores; the shape class (a single tile, long H) that
+    # keeps the CUDA-core router and its split-K reduction
+    spec = synth.spec("dsv3_s", hidden=6144, n_routed=128, name="router_cc")
     d = _route_inputs(spec)
     ids, w = route_gpu(m, spec, d)
     ids_o, w_o, _, _ = oracle.route(spec, synth.bf16_bits(d["x"]), d["w_r"].numpy(),
