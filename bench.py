@@ -9,6 +9,7 @@ experts, softmax top-12), weights bf16 ~N(0, 0.02).
 Prints one JSON line (rank 0).  Its headline is the main workload; its
 "configs" object holds the same measurements (ms per step with p50/p90,
 tokens/s, the layer's fraction of its roofline, the dominant kernel's roofline,
+the step replayed from a CUDA graph,
 the oracle timed on a sample) for the other headline layers: the tiny layer, the
 DSv3- and Pangu-shaped decode layers and the skewed W8A8 prefill layer, each
 generated, measured and freed in turn.  --impl reference times the fp64 CPU
@@ -484,8 +485,8 @@ def measure(args, spec, dev, world, full):
            "p50": p50, "p90": p90,
            "gpu_launches": gpu_launches, "clocks": clk.summary(), "per_kernel": per_kernel,
            "counts": counts_h, "alg_bytes": alg_bytes, "U": U}
+    res["graph"] = graph_replay(args, layer, x_d, out, dev, world, T)
     if full:
-        res["graph"] = graph_replay(args, layer, x_d, out, dev, world, T)
         res["e2e"] = end_to_end(args, layer, x, x_d, out, dev, world, T, H)
     res["cpu"] = None
     if world == 1 and not args.no_cpu_baseline:
@@ -626,6 +627,7 @@ def summary_of(args, res):
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in res["per_kernel"].items()
                                 if v[1]},
         "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
+        "cuda_graph": res["graph"],
         "cpu_baseline": res["cpu"],
     }
 

@@ -130,6 +130,22 @@ __device__ __forceinline__ bool packed_down(bool gu, int n) {
 }
 static_assert(2 * kPackedStep <= Geom<kTcFfn>::kStageBytes, "two packed K steps fill a stage");
 
+// Order in which the gate/up tiles are handed out: the shared expert's S tiles
+// (tiles 0 .. S-1, in groups of g: the g row chunks of one channel tile, which
+// read the same weights, once from HBM and otherwise from L2) are spread over
+// the first `span` of the R routed tiles, one group after every span / (S / g)
+// routed tiles, instead of all coming first.  A bijection of 0 .. S+R-1 that
+// keeps the routed tiles in order.
+__device__ __forceinline__ int interleave_tile(int c, int S, int g, int R, int span) {
+  if (S <= 0 || g <= 0 || R <= 0) return c;
+  const int G = S / g;
+  const int q = span / G;
+  if (q <= 0) return c;
+  const int b = c / (g + q), pos = c % (g + q);
+  if (b < G) return pos < g ? b * g + pos : S + b * q + (pos - g);
+  return S + G * q + (c - G * (g + q));
+}
+
 // tasks and start: the work list in shared memory when it fits, else in global
 // memory (a binary search of dependent loads).
 __device__ __forceinline__ QTile decode_tile(const FfnTask* tasks, int tile, int ntasks, int gu,
@@ -222,6 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const FfnTask* d_tasks = cached ? s_tasks : a.tasks;
   const int32_t* d_start = cached ? s_start : a.tile_start;
   const int32_t* d_start_dn = cached ? s_start_dn : a.tile_start_dn;
+  // the shared expert's tasks come first in the work list: its row chunks and
+  // its gate/up tiles (single-launch FFN)
+  int sh_chunks = 0, sh_gu = 0;
+  if (FFN && ntasks > 0 && d_tasks[0].expert < 0) {
+    sh_chunks = d_tasks[0].chunk & 0xffff;
+    sh_gu = sh_chunks * a.gu_tiles_shared;
+  }
 
   if (warp == kSchedWarp && lane == 0) {
     // ---------------------------------------------------------- scheduler --
@@ -233,7 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!*abort_flag) {
         const int tile = atomicAdd(a.sched, 1);
         if (tile < ntiles_first)
-          t = decode_tile(d_tasks, tile, ntasks, MODE != kTcDown, d_start);
+          t = decode_tile(d_tasks,
+                          interleave_tile(tile, sh_gu, sh_chunks, ntiles_first - sh_gu,
+                                          (ntiles_first - sh_gu) / 2),
+                          ntasks, MODE != kTcDown, d_start);
         else if (tile < ntiles)
           t = decode_tile(d_tasks, tile - ntiles_first, ntasks, 0, d_start_dn);
       }
