@@ -205,6 +205,20 @@ def test_full_size_decode_layers(m, name):
     full_size_case(m, name)
 
 
+def test_layer_with_more_tasks_than_the_kernel_caches(m):
+    # 1536 experts x 2048 tokens x top-2, all on tensor cores: ~1430 tasks, more than
+    # the one-launch FFN keeps in shared memory (1024), so its tile decodes read the
+    # work list from global memory; the batch also takes the large-batch router, the
+    # multi-CTA re-sort and the work-list kernel
+    spec = synth.spec("tiny", T=2048, n_routed=1536, top_k=2, name="many_tasks")
+    d = gs.inputs(spec)
+    ref = oracle_out(spec, d)
+    got = gs.run_layer(m, spec, d, out_fp32=True, gemv_max_rows=-1)
+    gs.check_out(got, ref, bf16_out=False, what="1536 experts x 2048 tokens")
+    cfg = m.config_from_spec(spec, gemv_max_rows=-1)
+    assert m.moe_tile_choice(cfg, 2048)[1]  # the one-launch FFN runs this layer
+
+
 def _bucket(spec, T):
     m = T * spec["top_k"] / synth.n_experts(spec)
     return next((i for i, v in enumerate([2, 8, 32, 128]) if m < v), 4)
