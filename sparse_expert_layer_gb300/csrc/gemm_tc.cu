@@ -44,13 +44,20 @@ constexpr int kTaskCache = 1024;                 // work-list tasks kept in shar
 // Pass of a launch: the down projection, the gate/up projection with SwiGLU,
 // or both in one launch (every gate/up tile, then every down tile; a down tile
 // starts once its task's gate/up tiles have stored their h rows).
-enum { kTcDown = 0, kTcGateUp = 1, kTcFfn = 2 };
+// kTcRouter: the large-batch router's logits, x . (W3 + W2 + W1)^T over the
+// exact three-term bf16 split of W_r (rows [W3 | W2 | W1], written by
+// router_split_kernel): a stage holds one x box and the three terms' weight
+// tiles of the same 64 columns, the W3 and W2 products accumulate in one TMEM
+// accumulator, the W1 products in another, and the logit is their sum (the
+// small terms are never rounded against the large ones, as in the decode
+// router).  x is read once per K step instead of once per term.
+enum { kTcDown = 0, kTcGateUp = 1, kTcFfn = 2, kTcRouter = 3 };
 
 template <int MODE>
 struct Geom {
-  static constexpr int kNA = MODE == kTcDown ? 1 : 2;  // weight tiles a stage can hold
+  static constexpr int kNA = MODE == kTcDown ? 1 : MODE == kTcRouter ? 3 : 2;  // weight tiles a stage holds
   static constexpr int kStageBytes = kNA * kATileBytes + kBTileBytes;
-  static constexpr int kStages = MODE == kTcDown ? 6 : 4;
+  static constexpr int kStages = MODE == kTcDown ? 6 : MODE == kTcRouter ? 3 : 4;
   static constexpr int kTmemCols = MODE == kTcDown ? 256 : 512;
   static constexpr int kAccStride = MODE == kTcDown ? 128 : 256;  // columns per accumulator buffer
   static constexpr int kBarBytes = 512;
@@ -170,7 +177,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using G = Geom<MODE>;
   constexpr bool FFN = MODE == kTcFfn;
   extern __shared__ uint8_t smem_raw[];
-  const int kind = MODE == kTcDown ? MOE_K_TC_DOWN : MOE_K_TC_GATE_UP;
+  const int kind = MODE == kTcDown ? MOE_K_TC_DOWN
+                   : MODE == kTcRouter ? MOE_K_ROUTER
+                                       : MOE_K_TC_GATE_UP;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // 1024-byte aligned ring (128-byte swizzle atoms), barriers after it
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -208,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&maps.a0);
     prefetch_tensormap(&maps.b);
-    if (MODE != kTcDown) prefetch_tensormap(&maps.a1);
+    if (MODE == kTcGateUp || MODE == kTcFfn) prefetch_tensormap(&maps.a1);
   }
   pdl_wait();
   const int ntasks = a.counts[a.task_slot];
@@ -259,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           t = decode_tile(d_tasks,
                           interleave_tile(tile, sh_gu, sh_chunks, ntiles_first - sh_gu,
                                           (ntiles_first - sh_gu) / 2),
-                          ntasks, MODE != kTcDown, d_start);
+                          ntasks, MODE == kTcGateUp || MODE == kTcFfn, d_start);
         else if (tile < ntiles)
           t = decode_tile(d_tasks, tile - ntiles_first, ntasks, 0, d_start_dn);
       }
@@ -339,9 +348,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++iter;
           continue;
         }
-        mbar_arrive_expect_tx(bar, (uint32_t)((gu ? 2 : 1) * kATileBytes + nb * kBoxBytes));
-        tma_load_3d(smem_u32(st), A0, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
-        if (gu) tma_load_3d(smem_u32(st + kATileBytes), A1, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
+        if (MODE == kTcRouter) {
+          // the three split terms' tiles of these 64 columns: K offsets 0, H, 2H
+          mbar_arrive_expect_tx(bar, (uint32_t)(3 * kATileBytes + nb * kBoxBytes));
+          for (int j = 0; j < 3; ++j)
+            tma_load_3d(smem_u32(st + j * kATileBytes), A0, j * K + ks * kBK, t.ct * kTcM, t.e,
+                        bar, pol_w);
+        } else {
+          mbar_arrive_expect_tx(bar, (uint32_t)((gu ? 2 : 1) * kATileBytes + nb * kBoxBytes));
+          tma_load_3d(smem_u32(st), A0, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
+          if (gu)
+            tma_load_3d(smem_u32(st + kATileBytes), A1, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
+        }
         uint8_t* sb = st + G::kNA * kATileBytes;
         const int bk = (!t.shared && a.b_kmod > 0) ? (ks * kBK) % a.b_kmod : ks * kBK;
         for (int j = 0; j < nb; ++j)
@@ -414,8 +432,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < kBK / 16; ++k) {
           const uint64_t bdesc = sdesc_sw128(sb + k * 32);
           const uint32_t acc = (ks > 0 || k > 0) ? 1u : 0u;
-          tc_mma_bf16(d0, sdesc_sw128(sa + k * 32), bdesc, idesc, acc);
-          if (gu) tc_mma_bf16(d1, sdesc_sw128(sa + kATileBytes + k * 32), bdesc, idesc, acc);
+          if (MODE == kTcRouter) {
+            tc_mma_bf16(d0, sdesc_sw128(sa + k * 32), bdesc, idesc, acc);                    // W3
+            tc_mma_bf16(d0, sdesc_sw128(sa + kATileBytes + k * 32), bdesc, idesc, 1u);      // W2
+            tc_mma_bf16(d1, sdesc_sw128(sa + 2 * kATileBytes + k * 32), bdesc, idesc, acc);  // W1
+          } else {
+            tc_mma_bf16(d0, sdesc_sw128(sa + k * 32), bdesc, idesc, acc);
+            if (gu) tc_mma_bf16(d1, sdesc_sw128(sa + kATileBytes + k * 32), bdesc, idesc, acc);
+          }
         }
         tc_commit(smem_u32(&empty[stage]));
         ++iter;
@@ -461,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           scatter_target(a.sc, t.row0 + j0 + lane, t.shared, &tk_l, &wt_l);
         uint32_t g[16], u[16];
         tmem_ld16(trow + j0, g);
-        if (gu) tmem_ld16(trow + kTcMaxN + j0, u);
+        if (gu || MODE == kTcRouter) tmem_ld16(trow + kTcMaxN + j0, u);
         tmem_ld_wait();
         if (fused) {
 #pragma unroll
@@ -481,6 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (gu) {
                 const float h = gv * __frcp_rn(1.f + __expf(-gv)) * __uint_as_float(u[i]);
                 (t.shared ? a.sout_h : a.out_h)[o] = f_to_bf16(h);
+              } else if (MODE == kTcRouter) {
+                a.out_y[o] = gv + __uint_as_float(u[i]);  // small terms + W1 terms
               } else {
                 (t.shared ? a.sout_y : a.out_y)[o] = gv;
               }
@@ -670,10 +696,21 @@ bool launch_tc_router(const Launch& L, const moe_config& c, int T, const void* x
   p.act = x;
   p.act_rows = T;
   p.out_y = logits;
-  p.K = 3 * c.hidden;
+  p.K = c.hidden;  // K steps over H; each loads the three terms' tiles
   p.N = E;
-  p.b_kmod = c.hidden;
-  return launch_tc<kTcDown>(L, p, MOE_K_ROUTER);
+  using G = Geom<kTcRouter>;
+  TcMaps maps;
+  memset(&maps, 0, sizeof maps);
+  if (!make_map(&maps.a0, w_split, 3 * (uint64_t)c.hidden, E, 1, kTcM) ||
+      !make_map(&maps.b, x, c.hidden, T, 1, kBoxRows))
+    return false;
+  const TcArgs a = make_args(L, p);
+  set_smem_attr_once(reinterpret_cast<const void*>(tc_kernel<kTcRouter>), G::kSmemBytes,
+                     kAttrTcRouter);
+  launch_begin(L, MOE_K_ROUTER);
+  launch_kernel(tc_kernel<kTcRouter>, L.num_sms, kThreads, G::kSmemBytes, L.stream, maps, a);
+  launch_end(L, MOE_K_ROUTER);
+  return true;
 }
 
 }  // namespace moe

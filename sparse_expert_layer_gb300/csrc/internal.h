@@ -380,6 +380,7 @@ enum {
   kAttrPermScatter,
   kAttrTcGU,
   kAttrTcDN,
+  kAttrTcRouter,
   kAttrGemvBase,                 // 8 slots: (gate/up, down) x row cap 1, 2, 4, 8
   kAttrW8Base = kAttrGemvBase + 8,  // 3 slots: W8A8 modes
   kAttrGemvI8Base = kAttrW8Base + 3, // 8 slots: W8A8 GEMV (gate/up, down) x row cap
