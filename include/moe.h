@@ -40,8 +40,11 @@
  *    variable MOE_PDL=0, read once per process, turns this off.
  *  - Small-batch routing runs its matmul on tensor cores where the batch gives
  *    enough parallel work; MOE_ROUTER_TC=0 (read once) keeps it on CUDA cores.
- *    Both compute fp32-class logits (routing ids do not depend on the choice
- *    beyond ties closer than the logits' rounding).
+ *    The smallest layers (T x (E_r + E_z) x H at most 2^20 multiply-adds, x and
+ *    w_router within one CTA's shared memory) route in one CTA on CUDA cores,
+ *    inside moe_layer_forward's re-sort kernel unless MOE_FOLDS=0.  All paths
+ *    compute fp32-class logits (routing ids do not depend on the choice beyond
+ *    ties closer than the logits' rounding).
  *  - bf16 tensors are passed as `const void*` holding IEEE bfloat16 values.
  *  - Expert indices 0 .. n_routed-1 are FFN experts; n_routed .. n_routed+n_zero-1
  *    are zero-computation experts (no weights; their pick contributes w * x_t).

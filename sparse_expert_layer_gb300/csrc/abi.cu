@@ -402,7 +402,8 @@ WlPlan wl_plan(const moe_config& c, int T, bool shared_weights) {
 bool run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, void* ws,
                  const int32_t* ids, const void* x, int32_t* counts, int32_t* offsets,
                  int32_t* s2e, int32_t* e2s, void* x_perm, float* x_scale, const WlPlan* plan,
-                 const float* w = nullptr, float* acc = nullptr) {
+                 const float* w = nullptr, float* acc = nullptr,
+                 const SmallRoute* route = nullptr, const TopkArgs* tk = nullptr) {
   const int E = c.n_routed + c.n_zero;
   bool built = false;
   if (sort_small_fits(T, E)) {
@@ -422,7 +423,7 @@ bool run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, 
     }
     launch_sort_small(ln, plan ? plan->cw : c, T, ids, counts, offsets, s2e, e2s,
                       plan ? &wl : nullptr, plan ? plan->gemv_max : 0, plan ? plan->chunk : 1,
-                      plan ? plan->tc_chunk : kTcMaxN, small ? &g : nullptr);
+                      plan ? plan->tc_chunk : kTcMaxN, small ? &g : nullptr, route, tk);
     built = plan != nullptr;
     if (small) return built;
   } else {
@@ -963,17 +964,24 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
     sc.w = w;
     sc.k = c.top_k;
   }
-  const moe_status rs = run_route(ln, c, T, L, ws, x, w_router, bias, ids, w);
-  if (rs != MOE_OK) {
-    finish();
-    return rs;
+  // small layers: the one-CTA re-sort routes the tokens first (one launch fewer)
+  const bool route_in_sort = route_small_fits(c, T) && folds_enabled();
+  const SmallRoute sroute{static_cast<const uint16_t*>(x), w_router, c.hidden};
+  const TopkArgs stk = topk_args(ln, c, T, nullptr, bias, ids, w);
+  if (!route_in_sort) {
+    const moe_status rs = run_route(ln, c, T, L, ws, x, w_router, bias, ids, w);
+    if (rs != MOE_OK) {
+      finish();
+      return rs;
+    }
   }
   // the FFN's work list is built with the re-sort when that runs as one CTA
   const bool ffn = w8 ? c.n_routed > 0 : (c.n_routed > 0 || c.shared_inter > 0);
   const WlPlan plan = wl_plan(c, T, !w8 && c.shared_inter > 0);
   const bool wl_built =
       run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale,
-                  ffn ? &plan : nullptr, w, acc);
+                  ffn ? &plan : nullptr, w, acc, route_in_sort ? &sroute : nullptr,
+                  route_in_sort ? &stk : nullptr);
   const bool w8_shared = w8 && c.shared_inter > 0;
   if (w8 && c.n_routed > 0) {
     QuantGatherOut qo{};

@@ -144,6 +144,34 @@ void launch_route(const Launch& L, const moe_config& c, int T, const void* x, co
 // Top-k gating of given logits.
 void launch_topk_only(const Launch& L, const moe_config& c, int T, const float* logits,
                       const float* bias, int32_t* ids, float* w);
+// Top-k gating arguments (one warp per token; topk.cuh).
+struct TopkArgs {
+  const float* logits;
+  const float* bias;
+  int32_t* ids;
+  float* w;
+  DevStatus* status;
+  int T, E, k;
+  int n_group, topk_group, per_group_k;
+  int score, renorm, bias_mode;
+  float scale;
+};
+TopkArgs topk_args(const Launch& L, const moe_config& c, int T, const float* logits,
+                   const float* bias, int32_t* ids, float* w);
+// Small layers: the router's x and W_r fit one CTA's shared memory and the work
+// (T * E * H multiply-adds) is at most kSmallRouteWork, so one CTA of
+// kSmallRouteWarps warps computes the logits and the top-k.  The one-CTA
+// re-sort runs that code before its own work when folds are on; otherwise
+// launch_route runs it as a kernel of its own: the same bits either way.
+constexpr int kSmallRouteWarps = 32;
+constexpr long long kSmallRouteWork = 1LL << 20;
+struct SmallRoute {
+  const uint16_t* x;  // bf16 [T, H], 16-byte aligned
+  const float* w_r;   // fp32 [E, H], 16-byte aligned
+  int H;
+};
+bool route_small_fits(const moe_config& c, int T);
+size_t route_small_smem(const moe_config& c, int T);
 // Large batches: the router as a tensor-core GEMM over the exact three-term
 // bf16 split of W_r ([E, 3H], written by launch_router_split).
 bool router_on_tensor_cores(const moe_config& c, int T);
@@ -178,10 +206,13 @@ struct SmallGather {
   float* acc;         // the tokens' accumulators (fused combine), or nullptr
   int H, E_r;
 };
+// With route != nullptr (route_small_fits(c, T)) the CTA first routes the
+// tokens itself (tk: where the ids and weights go) and then sorts those ids.
 void launch_sort_small(const Launch& L, const moe_config& c, int T, const int32_t* ids,
                        int32_t* counts, int32_t* offsets, int32_t* s2e, int32_t* e2s,
                        const WorkList* wl, int gemv_max_rows, int gemv_chunk, int tc_chunk,
-                       const SmallGather* gather = nullptr);
+                       const SmallGather* gather = nullptr, const SmallRoute* route = nullptr,
+                       const TopkArgs* tk = nullptr);
 
 // Grouped FFN, streaming path (gemv.cu)
 struct GemvPass {
@@ -388,6 +419,7 @@ enum {
   kAttrRouterTc,
   kAttrSortSmall,
   kAttrTcFfn,
+  kAttrRouteSmall,
   kAttrSlots
 };
 void set_smem_attr_once(const void* func, int bytes, int slot);

@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -366,11 +367,13 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WlArgs a) {
 // [expert][token] bitmap of all T tokens sits in shared memory: popcounts give
 // each expert's count and each pick's rank among the earlier tokens of its
 // expert, so the order inside an expert is by token, as in the multi-CTA path.
+static_assert(kSmallRouteWarps * 32 == 1024, "the one-CTA re-sort routes with all its warps");
 __global__ void __launch_bounds__(1024)
     sort_small_kernel(const int32_t* ids, int32_t* counts, int32_t* offsets, int32_t* s2e,
                       int32_t* e2s, int T, int k, int E, WlArgs wla, int build_wl,
-                      DevStatus* st, SmallGather g) {
-  extern __shared__ uint32_t sm[];  // bitmap [E][W], then offsets [E + 1]
+                      DevStatus* st, SmallGather g, SmallRoute rt, TopkArgs tk) {
+  // bitmap [E][W], offsets [E + 1], then (rt.x set) the router's region
+  extern __shared__ __align__(16) uint32_t sm[];
   __shared__ int sh[kWlScanInts];
   const int tid = threadIdx.x;
   const int W = (T + 31) / 32, R = T * k;
@@ -378,6 +381,11 @@ __global__ void __launch_bounds__(1024)
   int32_t* off = reinterpret_cast<int32_t*>(sm + (size_t)E * W);
   for (int i = tid; i < E * W; i += blockDim.x) bm[i] = 0u;  // shared only: before the wait
   pdl_enter();
+  // small layers: route the tokens here (ids and weights written to global
+  // memory, visible to the block after the routine's closing barrier)
+  if (rt.x)
+    route_small_block(rt, tk, reinterpret_cast<unsigned char*>(sm) +
+                                  align16(((size_t)E * W + E + 1) * 4));
   __syncthreads();
   for (int r = tid; r < R; r += blockDim.x) {
     const int e = ids[r];
@@ -483,10 +491,24 @@ bool sort_small_fits(int T, int E) {
   return T <= kSortSmallMaxT && sort_small_smem(T, E) <= (size_t)kSortSmallSmem;
 }
 
+bool route_small_fits(const moe_config& c, int T) {
+  const int E = c.n_routed + c.n_zero, H = c.hidden;
+  if (T < 1 || E < 1 || H % 8 != 0 || c.top_k > 32 || (long long)T * E * H > kSmallRouteWork ||
+      !sort_small_fits(T, E))
+    return false;
+  // the re-sort's bitmap and the router's region fit one CTA together
+  return align16(sort_small_smem(T, E)) + small_route_plan(T, E, H).total <=
+         (size_t)kSortSmallSmem;
+}
+
+size_t route_small_smem(const moe_config& c, int T) {
+  return small_route_plan(T, c.n_routed + c.n_zero, c.hidden).total;
+}
+
 void launch_sort_small(const Launch& L, const moe_config& c, int T, const int32_t* ids,
                        int32_t* counts, int32_t* offsets, int32_t* s2e, int32_t* e2s,
                        const WorkList* wl, int gemv_max_rows, int gemv_chunk, int tc_chunk,
-                       const SmallGather* gather) {
+                       const SmallGather* gather, const SmallRoute* route, const TopkArgs* tk) {
   const int E = c.n_routed + c.n_zero;
   WlArgs a{};
   if (wl) a = make_wl_args(L, c, T, offsets, *wl, gemv_max_rows, gemv_chunk, tc_chunk);
@@ -495,8 +517,16 @@ void launch_sort_small(const Launch& L, const moe_config& c, int T, const int32_
   launch_begin(L, MOE_K_SORT);
   SmallGather g{};
   if (gather) g = *gather;
-  launch_kernel(sort_small_kernel, 1, 1024, sort_small_smem(T, E), L.stream, ids, counts, offsets,
-                s2e, e2s, T, c.top_k, E, a, wl ? 1 : 0, L.status, g);
+  SmallRoute rt{};
+  TopkArgs tka{};
+  size_t smem = sort_small_smem(T, E);
+  if (route && tk) {
+    rt = *route;
+    tka = *tk;
+    smem = align16(smem) + route_small_smem(c, T);
+  }
+  launch_kernel(sort_small_kernel, 1, 1024, smem, L.stream, ids, counts, offsets, s2e, e2s, T,
+                c.top_k, E, a, wl ? 1 : 0, L.status, g, rt, tka);
   launch_end(L, MOE_K_SORT);
 }
 

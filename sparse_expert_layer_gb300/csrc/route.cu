@@ -11,11 +11,8 @@
 // batch gives the tensor cores enough parallel work, the tensor-core router
 // below takes its place (it needs neither the partials nor the tile counters).
 //
-// Top-k: one warp per token.  Scores are a softmax over every expert (zero-
-// computation ones included, as in LongCat-Flash's 768-way choice) or a
-// sigmoid; the group stage follows the grouped-expert designs of the Pangu Pro
-// MoE disclosure (opening section and section H2P); picks are taken in
-// descending key order, ties to the lower expert index.
+// Top-k: one warp per token (topk.cuh).  Small layers route in one CTA
+// (topk.cuh), as a kernel of their own here or inside the one-CTA re-sort.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -26,6 +23,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -245,159 +243,6 @@ __global__ void __launch_bounds__(kRtThreads) router_kernel(RouterArgs a) {
     }
   }
   if (tid == 0) a.counters[tile] = 0;  // ready for the next call
-}
-
-struct TopkArgs {
-  const float* logits;
-  const float* bias;
-  int32_t* ids;
-  float* w;
-  DevStatus* status;
-  int T, E, k;
-  int n_group, topk_group, per_group_k;
-  int score, renorm, bias_mode;
-  float scale;
-};
-
-constexpr int kTkBatch = 8;  // experts per lane whose logits are loaded together
-
-// Scores, group stage and top-k of token t, by one warp: row holds the token's
-// E logits (global or shared memory), sc a 3 * E float scratch of the warp.
-__device__ void topk_token(const TopkArgs& a, int t, const float* row, float* sc) {
-  const int lane = threadIdx.x % 32;
-  const int E = a.E;
-  float* sel = sc + E;  // selection keys, -inf = not eligible
-  float* tmp = sel + E;
-
-  // logits and scores.  The global loads of kTkBatch experts per lane are
-  // issued together (the select bias is parked in sel until the scores exist).
-  float m = -INFINITY;
-  const bool logit_bias = a.bias_mode == MOE_BIAS_LOGIT;
-  const bool select_bias = a.bias_mode == MOE_BIAS_SELECT;
-  for (int e0 = lane; e0 < E; e0 += 32 * kTkBatch) {
-    float l[kTkBatch], bv[kTkBatch];
-#pragma unroll
-    for (int b = 0; b < kTkBatch; ++b) {
-      const int e = e0 + 32 * b;
-      l[b] = e < E ? row[e] : 0.f;
-      bv[b] = e < E && a.bias_mode != MOE_BIAS_NONE ? a.bias[e] : 0.f;
-    }
-#pragma unroll
-    for (int b = 0; b < kTkBatch; ++b) {
-      const int e = e0 + 32 * b;
-      if (e < E) {
-        float v = l[b];
-        if (logit_bias) v += bv[b];
-        sc[e] = v;
-        sel[e] = select_bias ? bv[b] : 0.f;
-        m = fmaxf(m, v);
-      }
-    }
-  }
-  if (a.score == MOE_SCORE_SOFTMAX) {
-    m = warp_max(m);
-    float z = 0.f;
-    for (int e = lane; e < E; e += 32) {
-      const float p = expf(sc[e] - m);
-      sc[e] = p;
-      z += p;
-    }
-    z = warp_sum(z);
-    for (int e = lane; e < E; e += 32) sc[e] = sc[e] / z;
-  } else {
-    for (int e = lane; e < E; e += 32) sc[e] = 1.f / (1.f + expf(-sc[e]));
-  }
-  for (int e = lane; e < E; e += 32) sel[e] = sc[e] + sel[e];
-  __syncwarp();
-
-  // group stage
-  if (a.n_group > 1) {
-    const int G = E / a.n_group;
-    if (a.per_group_k == 0) {
-      float gs[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int g = lane + 32 * i;
-        gs[i] = -INFINITY;
-        if (g < a.n_group) {
-          float b1 = -INFINITY, b2 = -INFINITY;
-          for (int e = g * G; e < (g + 1) * G; ++e) {
-            const float v = sel[e];
-            if (v > b1) {
-              b2 = b1;
-              b1 = v;
-            } else if (v > b2) {
-              b2 = v;
-            }
-          }
-          gs[i] = G >= 2 ? b1 + b2 : b1;
-        }
-      }
-      uint64_t keep = 0;
-      for (int r = 0; r < a.topk_group; ++r) {
-        float v = -INFINITY;
-        int gi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int g = lane + 32 * i;
-          if (g < a.n_group && !((keep >> g) & 1ull) && (gi == 0x7fffffff || gs[i] > v)) {
-            v = gs[i];
-            gi = g;
-          }
-        }
-        warp_argmax(v, gi);
-        if (gi < a.n_group) keep |= 1ull << gi;
-      }
-      for (int e = lane; e < E; e += 32)
-        if (!((keep >> (e / G)) & 1ull)) sel[e] = -INFINITY;
-    } else {
-      for (int e = lane; e < E; e += 32) tmp[e] = sel[e];
-      __syncwarp();
-      for (int g = lane; g < a.n_group; g += 32) {
-        for (int r = 0; r < a.per_group_k; ++r) {
-          int best = -1;
-          for (int e = g * G; e < (g + 1) * G; ++e)
-            if (tmp[e] != -INFINITY && (best < 0 || tmp[e] > tmp[best])) best = e;
-          if (best >= 0) tmp[best] = -INFINITY;  // taken: a winner
-        }
-        for (int e = g * G; e < (g + 1) * G; ++e)
-          if (tmp[e] != -INFINITY) sel[e] = -INFINITY;  // not a winner
-      }
-    }
-    __syncwarp();
-  }
-
-  // top-k in descending key order, ties to the lower index
-  int my_id = 0;
-  float my_w = 0.f;
-  for (int j = 0; j < a.k; ++j) {
-    float v = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int e = lane; e < E; e += 32)
-      if (sel[e] > v) {
-        v = sel[e];
-        bi = e;
-      }
-    warp_argmax(v, bi);
-    if (bi == 0x7fffffff) {  // fewer eligible experts than k (non-finite keys)
-      if (lane == 0) raise_status(a.status, kStInternal, MOE_K_TOPK);
-      bi = 0;
-    }
-    if (lane == j) {
-      my_id = bi;
-      my_w = sc[bi];
-    }
-    __syncwarp();
-    if (lane == 0) sel[bi] = -INFINITY;
-    __syncwarp();
-  }
-  float wsum = warp_sum(lane < a.k ? my_w : 0.f);
-  if (lane < a.k) {
-    float w = my_w;
-    if (a.renorm) w = w / wsum;
-    a.ids[(size_t)t * a.k + lane] = my_id;
-    a.w[(size_t)t * a.k + lane] = w * a.scale;
-  }
 }
 
 __global__ void topk_kernel(TopkArgs a) {
@@ -823,7 +668,7 @@ bool router_tc_decode_enabled() {
 bool router_on_tensor_cores(const moe_config& c, int T) {
   const int E = c.n_routed + c.n_zero;
   const long tiles = (long)((T + kTcMaxN - 1) / kTcMaxN) * ((E + kTcM - 1) / kTcM);
-  return c.hidden % 64 == 0 && T >= 1024 && tiles >= 64;
+  return c.hidden % 64 == 0 && T >= 1024 && tiles >= 64 && !route_small_fits(c, T);
 }
 
 void launch_router_split(const Launch& L, const float* w_r, int E, int H, uint16_t* out) {
@@ -906,7 +751,6 @@ int router_splits(const moe_config& c, int T, int num_sms) {
   return (int)s;
 }
 
-namespace {
 TopkArgs topk_args(const Launch& L, const moe_config& c, int T, const float* logits,
                    const float* bias, int32_t* ids, float* w) {
   TopkArgs a;
@@ -928,6 +772,15 @@ TopkArgs topk_args(const Launch& L, const moe_config& c, int T, const float* log
   return a;
 }
 
+namespace {
+// The small layers' router and top-k as a kernel of its own.
+__global__ void __launch_bounds__(kSmallRouteWarps * 32)
+    router_small_kernel(SmallRoute r, TopkArgs tk) {
+  extern __shared__ __align__(16) unsigned char sm_route[];
+  pdl_enter();
+  route_small_block(r, tk, sm_route);
+}
+
 void launch_topk(const Launch& L, const TopkArgs& a, int T) {
   const size_t per_warp = (size_t)3 * a.E * sizeof(float);
   // few warps per CTA: tokens spread over more SMs
@@ -946,6 +799,18 @@ void launch_route(const Launch& L, const moe_config& c, int T, const void* x, co
                   int32_t* ids, float* w) {
   const TopkArgs tk = topk_args(L, c, T, logits, bias, ids, w);
   const int E = c.n_routed + c.n_zero;
+  if (route_small_fits(c, T) && ((reinterpret_cast<uintptr_t>(x) |
+                                  reinterpret_cast<uintptr_t>(w_r)) & 15u) == 0) {
+    // one CTA: logits and top-k (logits are not written)
+    const SmallRoute r{static_cast<const uint16_t*>(x), w_r, c.hidden};
+    set_smem_attr_once(reinterpret_cast<const void*>(router_small_kernel), kSortSmallSmem,
+                       kAttrRouteSmall);
+    launch_begin(L, MOE_K_ROUTER);
+    launch_kernel(router_small_kernel, 1, kSmallRouteWarps * 32, route_small_smem(c, T),
+                  L.stream, r, tk);
+    launch_end(L, MOE_K_ROUTER);
+    return;
+  }
   CUtensorMap xmap, wmap;
   memset(&xmap, 0, sizeof xmap);
   memset(&wmap, 0, sizeof wmap);

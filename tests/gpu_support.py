@@ -19,6 +19,30 @@ from tests import support
 REL_L2 = 5e-3
 MAX_ABS = 2e-2
 
+# Layers small enough for the one-CTA router (T * E * H at most 2^20, x and W_r
+# within one CTA's shared memory next to the re-sort's bitmap), with the
+# routing rules of the larger layers: DSv3-style groups with a sigmoid, a
+# select-only bias and a scale; zero-computation experts and a logit bias at a
+# single token and an H that is not a multiple of 64; MoGE per-group picks with
+# a shared expert; more tokens than warps.
+ONE_CTA = {
+    "one_cta_groups": dict(T=5, hidden=136, inter=64, n_routed=32, top_k=4, n_group=4,
+                           topk_group=2, score="sigmoid", bias_mode="select", bias_kind="iid",
+                           routed_scale=2.5, renormalize=True),
+    "one_cta_zero": dict(T=1, hidden=200, inter=48, n_routed=32, n_zero=16, top_k=6,
+                         bias_mode="logit", bias_kind="iid", renormalize=False),
+    "one_cta_per_group": dict(T=33, hidden=512, inter=64, n_routed=16, top_k=4, n_group=4,
+                              per_group_k=1, shared_inter=96),
+    "one_cta_tokens": dict(T=64, hidden=256, inter=32, n_routed=24, top_k=3),
+}
+
+
+def layer_spec(name: str) -> dict:
+    """A named layer, or one of the one-CTA routing shapes (built on 'tiny')."""
+    if name in ONE_CTA:
+        return synth.spec("tiny", name=name, **ONE_CTA[name])
+    return synth.spec(name)
+
 _cache = {}
 
 

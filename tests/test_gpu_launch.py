@@ -67,7 +67,7 @@ sys.path.insert(0, sys.argv[1])
 import synth
 from tests import gpu_support as gs
 m = gs.lib()
-spec = synth.spec(sys.argv[2])
+spec = gs.layer_spec(sys.argv[2])
 d = gs.inputs(spec)
 out = gs.run_layer(m, spec, d, out_fp32=True, combine=m.COMBINE_ORDERED)
 np.save(sys.argv[3], out.cpu().numpy())
@@ -90,12 +90,13 @@ def test_plain_launches_give_the_same_bits(m, name, tmp_path):
     assert np.array_equal(got, plain)
 
 
-@pytest.mark.parametrize("name", ["tiny", "pangu_s", "longcat_s", "ragged_s"])
+@pytest.mark.parametrize("name", ["tiny", "pangu_s", "longcat_s", "ragged_s", "one_cta_groups",
+                                  "one_cta_per_group"])
 def test_unfolded_launches_give_the_same_bits(m, name, tmp_path):
-    # MOE_FOLDS=0 (read once per process) runs the top-k, the re-sort, the
-    # gather and the finalize as launches of their own instead of in the last
-    # CTA of the kernel before; the outputs must be identical.
-    spec = synth.spec(name)
+    # MOE_FOLDS=0 (read once per process) runs the small layers' router, the
+    # top-k, the re-sort, the gather and the finalize as launches of their own
+    # instead of inside another kernel; the outputs must be identical.
+    spec = gs.layer_spec(name)
     d = gs.inputs(spec)
     got = gs.run_layer(m, spec, d, out_fp32=True, combine=m.COMBINE_ORDERED).cpu().numpy()
     path = str(tmp_path / "unfolded.npy")

@@ -35,6 +35,19 @@ def test_layer_matches_oracle(m, name, out_fp32, gemv_max_rows):
     gs.check_out(got, ref, bf16_out=not out_fp32, what=f"{name} gemv<={gemv_max_rows}")
 
 
+@pytest.mark.parametrize("name", list(gs.ONE_CTA))
+@pytest.mark.parametrize("combine", ["default", "ordered"])
+def test_layer_routed_by_the_sort_matches_oracle(m, name, combine):
+    # small layers: the one-CTA re-sort routes the tokens itself, then sorts,
+    # gathers and starts the accumulators
+    spec = gs.layer_spec(name)
+    d = gs.inputs(spec)
+    ref = oracle_out(spec, d)
+    mode = m.COMBINE_ORDERED if combine == "ordered" else 0
+    got = gs.run_layer(m, spec, d, out_fp32=False, combine=mode)
+    gs.check_out(got, ref, bf16_out=True, what=f"{name} {combine}")
+
+
 @pytest.mark.parametrize("name", SMALL)
 @pytest.mark.parametrize("out_fp32", [True, False])
 def test_layer_with_ordered_combine_matches_oracle(m, name, out_fp32):

@@ -79,6 +79,19 @@ def test_route_in_clusters_of_16_matches_oracle(m, name, over):
     assert np.allclose(w, w_o, rtol=1e-5, atol=1e-7)
 
 
+@pytest.mark.parametrize("name", ["tiny", *gs.ONE_CTA])
+def test_route_in_one_cta_matches_oracle(m, name):
+    # the router's x and W_r sit in one CTA's shared memory; its 32 warps compute
+    # the logits and then the top-k (a token per warp, two for the 64-token case)
+    spec = gs.layer_spec(name)
+    d = _route_inputs(spec)
+    ids, w = route_gpu(m, spec, d)
+    ids_o, w_o, _, _ = oracle.route(spec, synth.bf16_bits(d["x"]), d["w_r"].numpy(),
+                                    support.np_bias(d["bias"]))
+    assert np.array_equal(ids, ids_o)
+    assert np.allclose(w, w_o, rtol=1e-5, atol=1e-7)
+
+
 def _route_inputs(spec):
     x, w_r, bias, _ = support.make_inputs(spec)
     return dict(x=x, w_r=w_r, bias=bias, x_d=x.cuda(), w_r_d=w_r.cuda(),
