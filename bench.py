@@ -479,9 +479,9 @@ def measure(args, spec, dev, world, full):
     per_kernel = moe.timing_collect()
     moe.timing_enable(False)
 
-    gemv_max, one_launch = moe.moe_tile_choice(cfg, T)
+    gemv_max, one_launch, dn_wide = moe.moe_tile_choice(cfg, T)
     res = {"spec": spec, "combine": args.combine, "gemv_max": gemv_max,
-           "one_launch": one_launch, "value": value, "ms_step": ms_step,
+           "one_launch": one_launch, "dn_wide": dn_wide, "value": value, "ms_step": ms_step,
            "p50": p50, "p90": p90,
            "gpu_launches": gpu_launches, "clocks": clk.summary(), "per_kernel": per_kernel,
            "counts": counts_h, "alg_bytes": alg_bytes, "U": U}
@@ -605,6 +605,7 @@ def config_block(spec, res):
           "(latency-bound layer)")
     return {"workload": describe(spec), "tokens": spec["T"], "unique_experts": res["U"],
             "gemv_max_rows": res["gemv_max"], "ffn_one_launch": res["one_launch"],
+            "ffn_wide_down_tiles": res["dn_wide"],
             "real_picks": int(counts_h[:spec["n_routed"]].sum()),
             "zero_pick_share": zero_pick_share(spec, counts_h) if spec["n_zero"] else 0.0,
             "l2": l2, "combine": res["combine"]}

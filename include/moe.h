@@ -101,8 +101,12 @@ typedef enum {
 typedef enum {
   MOE_FFN_LAUNCH_DEFAULT = 0, /* the library's tile-parameter table decides */
   MOE_FFN_LAUNCH_TWO = 1,     /* gate/up, then down: two persistent launches */
-  MOE_FFN_LAUNCH_ONE = 2      /* one persistent launch: a down tile starts as soon as
+  MOE_FFN_LAUNCH_ONE = 2,     /* one persistent launch: a down tile starts as soon as
                                  its expert's gate/up tiles have stored h */
+  MOE_FFN_LAUNCH_ONE_WIDE = 3 /* one persistent launch whose down tiles span 256 output
+                                 channels: two 128-channel weight boxes share each
+                                 activation box, so h rows are read half as often
+                                 (pays off with many rows per expert) */
 } moe_ffn_launch;
 
 typedef enum {
@@ -262,6 +266,8 @@ moe_status moe_route_noalloc(const moe_config* cfg, int32_t T, const void* x,
  * bucket (expected picks per expert, T * k / (E_r + E_z)), then in H * I. */
 moe_status moe_tile_choice(const moe_config* cfg, int32_t T, int32_t* gemv_max_rows,
                            int32_t* ffn_one_launch);
+/* *ffn_one_launch: 0 = two launches, 1 = one launch, 2 = one launch with
+ * 256-channel down tiles (MOE_FFN_LAUNCH_ONE_WIDE). */
 
 /* Synchronises `stream`, reads and clears the device status word in `ws`.
  * MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_DEVICE_TIMEOUT (or MOE_ERR_CUDA). */

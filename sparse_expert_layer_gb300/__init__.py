@@ -39,7 +39,7 @@ SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 BIAS_NONE, BIAS_LOGIT, BIAS_SELECT = 0, 1, 2
 W_BF16, W8A8 = 0, 1
 COMBINE_DEFAULT, COMBINE_ORDERED, COMBINE_FUSED = 0, 1, 2
-FFN_LAUNCH_DEFAULT, FFN_LAUNCH_TWO, FFN_LAUNCH_ONE = 0, 1, 2
+FFN_LAUNCH_DEFAULT, FFN_LAUNCH_TWO, FFN_LAUNCH_ONE, FFN_LAUNCH_ONE_WIDE = 0, 1, 2, 3
 
 KERNELS = ["router", "topk", "perm_count", "perm_scan", "perm_scatter", "perm_gather",
            "worklist", "gemv_gate_up", "gemv_down", "tc_gate_up", "tc_down", "quant_h", "combine",
@@ -140,11 +140,12 @@ def config_from_spec(spec: dict, out_fp32: bool = False, gemv_max_rows: int = 0,
 
 
 def moe_tile_choice(cfg: MoeConfig, T: int):
-    """(GEMV switch point, one-launch FFN) the library picks for (cfg, T)."""
+    """(GEMV switch point, one-launch FFN, 256-channel down tiles) the library
+    picks for (cfg, T)."""
     g, o = _I(0), _I(0)
     _check(lib.moe_tile_choice(ctypes.byref(cfg), T, ctypes.byref(g), ctypes.byref(o)),
            "moe_tile_choice")
-    return g.value, bool(o.value)
+    return g.value, o.value >= 1, o.value == 2
 
 
 def moe_workspace_size(cfg: MoeConfig, T: int) -> int:

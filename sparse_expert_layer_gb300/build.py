@@ -50,7 +50,8 @@ def write_table_inc(path: str = TABLE_INC) -> None:
     t = json.load(open(TABLE_JSON))
     wd = {"bf16": 0, "w8a8": 1}
     rows = [f"    {{{wd[e['wdtype']]}, {int(e['hidden'])}, {int(e['inter'])}, {int(e['bucket'])}, "
-            f"{int(e['gemv_max'])}, {int(e['one_launch'])}}}," for e in t["entries"]]
+            f"{int(e['gemv_max'])}, {int(e['one_launch'])}, {int(e.get('dn_wide', 0))}}},"
+            for e in t["entries"]]
     b = ", ".join(str(int(v)) for v in t["buckets"])
     text = ("// Generated from tuning/tile_table.json by build.py; do not edit.\n"
             f"static const int kTileBuckets[] = {{{b}}};\n"

@@ -111,7 +111,7 @@ moe_status check_cfg(const moe_config* c, int32_t T) {
   if (c->out_fp32 != 0 && c->out_fp32 != 1) return MOE_ERR_INVALID_ARG;
   if (c->combine < MOE_COMBINE_DEFAULT || c->combine > MOE_COMBINE_FUSED)
     return MOE_ERR_INVALID_ARG;
-  if (c->ffn_launch < MOE_FFN_LAUNCH_DEFAULT || c->ffn_launch > MOE_FFN_LAUNCH_ONE)
+  if (c->ffn_launch < MOE_FFN_LAUNCH_DEFAULT || c->ffn_launch > MOE_FFN_LAUNCH_ONE_WIDE)
     return MOE_ERR_INVALID_ARG;
   // work-list chunk indices are 16-bit: at most 65535 chunks of 128 rows per unit
   if ((long long)T * c->top_k > (1LL << 30) || T > 65535 * kTcMaxN) return MOE_ERR_UNSUPPORTED;
@@ -125,7 +125,7 @@ moe_status check_cfg(const moe_config* c, int32_t T) {
 // and the load bucket of the expected picks per expert, T * k / (E_r + E_z);
 // the entry of the same weight type nearest in bucket, then in H * I, applies.
 struct TileEntry {
-  int wdtype, hidden, inter, bucket, gemv_max, one_launch;
+  int wdtype, hidden, inter, bucket, gemv_max, one_launch, dn_wide;
 };
 #include "tile_table.inc"
 
@@ -183,9 +183,21 @@ bool fused_combine(const moe_config& c) {
 bool ffn_one_launch(const moe_config& c, int T) {
   if (c.wdtype != MOE_W_BF16) return false;
   if (c.ffn_launch == MOE_FFN_LAUNCH_TWO) return false;
-  if (c.ffn_launch == MOE_FFN_LAUNCH_ONE) return true;
+  if (c.ffn_launch == MOE_FFN_LAUNCH_ONE || c.ffn_launch == MOE_FFN_LAUNCH_ONE_WIDE) return true;
   const TileEntry* e = tile_entry(c, T);
   return e ? e->one_launch != 0 : true;
+}
+
+// Whether the one-launch FFN's down tiles span 2 x kTcM output channels: two
+// weight boxes and two accumulators per K step share one activation box, so a
+// task's h rows are read half as often (measured on GB300: a gain with tens of
+// rows per expert, a small loss with a few): cfg.ffn_launch, or the table's
+// choice when it is MOE_FFN_LAUNCH_DEFAULT.
+bool ffn_dn_wide(const moe_config& c, int T) {
+  if (!ffn_one_launch(c, T)) return false;
+  if (c.ffn_launch != MOE_FFN_LAUNCH_DEFAULT) return c.ffn_launch == MOE_FFN_LAUNCH_ONE_WIDE;
+  const TileEntry* e = tile_entry(c, T);
+  return e && e->dn_wide != 0;
 }
 
 // The GEMV launches are skipped when no unit can take that path.
@@ -385,7 +397,7 @@ moe_status run_route(const Launch& ln, const moe_config& c, int T, const Layout&
 // chunk, and the tensor-core chunk.
 struct WlPlan {
   moe_config cw;
-  int gemv_max, chunk, tc_chunk;
+  int gemv_max, chunk, tc_chunk, dn_ch;
 };
 WlPlan wl_plan(const moe_config& c, int T, bool shared_weights) {
   WlPlan p;
@@ -394,6 +406,7 @@ WlPlan wl_plan(const moe_config& c, int T, bool shared_weights) {
   p.gemv_max = effective_gemv_max(c, T);
   p.chunk = gemv_chunk(p.gemv_max);
   p.tc_chunk = c.wdtype == MOE_W8A8 ? kW8MaxN : kTcMaxN;
+  p.dn_ch = ffn_dn_wide(c, T) ? 2 * kTcM : 0;
   return p;
 }
 
@@ -423,7 +436,8 @@ bool run_permute(const Launch& ln, const moe_config& c, int T, const Layout& L, 
     }
     launch_sort_small(ln, plan ? plan->cw : c, T, ids, counts, offsets, s2e, e2s,
                       plan ? &wl : nullptr, plan ? plan->gemv_max : 0, plan ? plan->chunk : 1,
-                      plan ? plan->tc_chunk : kTcMaxN, small ? &g : nullptr, route, tk);
+                      plan ? plan->tc_chunk : kTcMaxN, small ? &g : nullptr, route, tk,
+                      plan ? plan->dn_ch : 0);
     built = plan != nullptr;
     if (small) return built;
   } else {
@@ -448,7 +462,8 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   const WlPlan plan = wl_plan(c, T, shared);
   const int gemv_max = plan.gemv_max;
   const int chunk = plan.chunk;
-  if (!wl_built) launch_worklist(ln, plan.cw, T, offsets, wl, gemv_max, chunk, plan.tc_chunk);
+  if (!wl_built)
+    launch_worklist(ln, plan.cw, T, offsets, wl, gemv_max, chunk, plan.tc_chunk, plan.dn_ch);
   uint16_t* h = at<uint16_t>(ws, L.h);
   uint16_t* h_s = at<uint16_t>(ws, L.h_s);
 
@@ -537,6 +552,7 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   td.N = td.Ns = c.hidden;
   td.sc = sc;
   td.fin = fin;
+  td.dn_wide = plan.dn_ch > 0;
   if (c.n_routed > 0) {
     const bool ok = one_launch ? launch_tc_ffn(ln, tg, td, wl.gu_done) : launch_tc_down(ln, td);
     if (!ok) return MOE_ERR_CUDA;
@@ -1141,7 +1157,8 @@ moe_status moe_tile_choice(const moe_config* cfg, int32_t T, int32_t* gemv_max_r
   if (s != MOE_OK) return s;
   if (!gemv_max_rows || !one_launch) return MOE_ERR_INVALID_ARG;
   *gemv_max_rows = effective_gemv_max(*cfg, T);
-  *one_launch = ffn_one_launch(*cfg, T) ? 1 : 0;
+  // 0 two launches, 1 one, 2 one with wide down tiles
+  *one_launch = ffn_dn_wide(*cfg, T) ? 2 : ffn_one_launch(*cfg, T) ? 1 : 0;
   return MOE_OK;
 }
 

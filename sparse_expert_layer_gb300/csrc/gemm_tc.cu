@@ -102,6 +102,8 @@ struct TcArgs {
   int* gu_done;
   int gu_tiles, gu_tiles_shared;  // gate/up channel tiles of a routed / shared task
   SmallFinalize fin;
+  int dn_wide;  // single-launch FFN: down tiles of 2 x kTcM channels (two weight boxes and
+                // two accumulators per K step, one activation box)
 };
 
 // Small layers: the last CTA of the down pass to finish rounds the tokens'
@@ -129,11 +131,18 @@ __device__ __forceinline__ void finalize_if_last(const SmallFinalize& f) {
 }
 
 // Single-launch FFN: a down tile of at most one 64-row activation box carries
-// two K steps per stage, each [16 KB weight tile | 8 KB activation box].
+// two K steps per stage, each [16 KB weight tile | 8 KB activation box] (narrow
+// down tiles; wide ones hold two weight tiles per K step, as gate/up tiles do).
 constexpr int kPackedStep = kATileBytes + kBoxBytes;
 template <int MODE>
-__device__ __forceinline__ bool packed_down(bool gu, int n) {
-  return MODE == kTcFfn && !gu && n <= kBoxRows;
+__device__ __forceinline__ bool packed_down(bool gu, int n, int wide) {
+  return MODE == kTcFfn && !gu && !wide && n <= kBoxRows;
+}
+// Whether a tile carries two weight tiles per K step: gate and up, or the two
+// channel halves of a wide down tile.
+template <int MODE>
+__device__ __forceinline__ bool two_weight_tiles(bool gu, int wide) {
+  return MODE == kTcGateUp || (MODE == kTcFfn && (gu || wide));
 }
 static_assert(2 * kPackedStep <= Geom<kTcFfn>::kStageBytes, "two packed K steps fill a stage");
 
@@ -296,10 +305,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (t.tile < 0) break;
       const bool gu = MODE == kTcGateUp || (FFN && t.gu != 0);
+      const bool two = two_weight_tiles<MODE>(gu, a.dn_wide);
       const CUtensorMap* A0;
       const CUtensorMap* A1 = t.shared ? &maps.sa1 : &maps.a1;
       const CUtensorMap* B;
       int K;
+      // weight rows of the tile's first box; the second box (up weights, or a
+      // wide down tile's second channel half) starts at a1_row of A1
+      int a0_row = t.ct * kTcM, a1_row = t.ct * kTcM;
       if (FFN && !gu) {
         // the task's h rows are complete once all its gate/up tiles are stored
         const int target = 4 * (t.shared ? a.gu_tiles_shared : a.gu_tiles);
@@ -311,6 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         A0 = t.shared ? &maps.sd0 : &maps.d0;
         B = t.shared ? &maps.sh : &maps.h;
         K = t.shared ? a.Ns : a.N;  // the down pass reduces over the intermediate size
+        if (a.dn_wide) {
+          A1 = A0;
+          a0_row = t.ct * 2 * kTcM;
+          a1_row = a0_row + kTcM;
+        }
       } else {
         A0 = t.shared ? &maps.sa0 : &maps.a0;
         B = t.shared ? &maps.sb : &maps.b;
@@ -321,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // single-launch FFN, down tile of <= 64 rows: two K steps per stage (each a
       // 16 KB weight tile and an 8 KB activation box), so the down tiles keep as
       // many weight bytes in flight as the gate/up tiles
-      const int sub = packed_down<MODE>(gu, t.n) ? 2 : 1;
+      const int sub = packed_down<MODE>(gu, t.n, a.dn_wide) ? 2 : 1;
       for (int ks = 0; ks < nks; ks += sub) {
         if (*abort_flag) {
           ok = false;
@@ -342,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar, (uint32_t)(nsub * (kATileBytes + kBoxBytes)));
           for (int u = 0; u < nsub; ++u) {
             uint8_t* su = st + u * kPackedStep;
-            tma_load_3d(smem_u32(su), A0, (ks + u) * kBK, t.ct * kTcM, t.e, bar, pol_w);
+            tma_load_3d(smem_u32(su), A0, (ks + u) * kBK, a0_row, t.e, bar, pol_w);
             tma_load_3d(smem_u32(su + kATileBytes), B, (ks + u) * kBK, t.row0, 0, bar, pol_x);
           }
           ++iter;
@@ -355,10 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smem_u32(st + j * kATileBytes), A0, j * K + ks * kBK, t.ct * kTcM, t.e,
                         bar, pol_w);
         } else {
-          mbar_arrive_expect_tx(bar, (uint32_t)((gu ? 2 : 1) * kATileBytes + nb * kBoxBytes));
-          tma_load_3d(smem_u32(st), A0, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
-          if (gu)
-            tma_load_3d(smem_u32(st + kATileBytes), A1, ks * kBK, t.ct * kTcM, t.e, bar, pol_w);
+          mbar_arrive_expect_tx(bar, (uint32_t)((two ? 2 : 1) * kATileBytes + nb * kBoxBytes));
+          tma_load_3d(smem_u32(st), A0, ks * kBK, a0_row, t.e, bar, pol_w);
+          if (two)
+            tma_load_3d(smem_u32(st + kATileBytes), A1, ks * kBK, a1_row, t.e, bar, pol_w);
         }
         uint8_t* sb = st + G::kNA * kATileBytes;
         const int bk = (!t.shared && a.b_kmod > 0) ? (ks * kBK) % a.b_kmod : ks * kBK;
@@ -394,9 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16_f32(kTcM, nmma);
       const uint32_t d0 = tmem + buf * G::kAccStride;
       const uint32_t d1 = d0 + kTcMaxN;
+      const bool two = two_weight_tiles<MODE>(gu, a.dn_wide);
       const int K = (FFN && !gu) ? (t.shared ? a.Ns : a.N) : (t.shared ? a.Ks : a.K);
       const int nks = (K + kBK - 1) / kBK;
-      const int sub = packed_down<MODE>(gu, t.n) ? 2 : 1;
+      const int sub = packed_down<MODE>(gu, t.n, a.dn_wide) ? 2 : 1;
       for (int ks = 0; ks < nks; ks += sub) {
         if (*abort_flag) {
           ok = false;
@@ -438,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_mma_bf16(d1, sdesc_sw128(sa + 2 * kATileBytes + k * 32), bdesc, idesc, acc);  // W1
           } else {
             tc_mma_bf16(d0, sdesc_sw128(sa + k * 32), bdesc, idesc, acc);
-            if (gu) tc_mma_bf16(d1, sdesc_sw128(sa + kATileBytes + k * 32), bdesc, idesc, acc);
+            if (two) tc_mma_bf16(d1, sdesc_sw128(sa + kATileBytes + k * 32), bdesc, idesc, acc);
           }
         }
         tc_commit(smem_u32(&empty[stage]));
@@ -466,6 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool gu = MODE == kTcGateUp || (FFN && t.gu != 0);
       // output channels of this tile's pass: gate/up -> N (I or I_s); down -> H
       const int tN = (FFN && !gu) ? a.K : (t.shared ? a.Ns : a.N);
+      // a wide down tile's second accumulator holds channels ch + kTcM
+      const bool wide = FFN && !gu && a.dn_wide;
       const uint32_t buf = local & 1u, use = local >> 1;
       if (!warp_wait(smem_u32(&acc_full[buf]), use & 1u)) {
         if (lane == 0) raise_status(a.status, kStTimeout, kind);
@@ -473,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int ch = t.ct * kTcM + q * 32 + lane;
+      const int ch = t.ct * (wide ? 2 * kTcM : kTcM) + q * 32 + lane;
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * G::kAccStride;
       const bool fused = !gu && a.sc.acc != nullptr;
       for (int j0 = 0; j0 < t.n; j0 += 16) {
@@ -485,15 +506,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           scatter_target(a.sc, t.row0 + j0 + lane, t.shared, &tk_l, &wt_l);
         uint32_t g[16], u[16];
         tmem_ld16(trow + j0, g);
-        if (gu || MODE == kTcRouter) tmem_ld16(trow + kTcMaxN + j0, u);
+        if (gu || MODE == kTcRouter || wide) tmem_ld16(trow + kTcMaxN + j0, u);
         tmem_ld_wait();
         if (fused) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int tk = __shfl_sync(0xffffffffu, tk_l, i);
             const float wt = __shfl_sync(0xffffffffu, wt_l, i);
-            if (ch < tN && j0 + i < t.n)
-              atomicAdd(a.sc.acc + (size_t)tk * tN + ch, wt * __uint_as_float(g[i]));
+            if (j0 + i < t.n) {
+              float* arow = a.sc.acc + (size_t)tk * tN;
+              if (ch < tN) atomicAdd(arow + ch, wt * __uint_as_float(g[i]));
+              if (wide && ch + kTcM < tN) atomicAdd(arow + ch + kTcM, wt * __uint_as_float(u[i]));
+            }
+          }
+        } else if (wide) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int tok = j0 + i;
+            if (tok < t.n) {
+              float* yrow = (t.shared ? a.sout_y : a.out_y) + (size_t)(t.row0 + tok) * tN;
+              if (ch < tN) yrow[ch] = __uint_as_float(g[i]);
+              if (ch + kTcM < tN) yrow[ch + kTcM] = __uint_as_float(u[i]);
+            }
           }
         } else if (ch < tN) {
 #pragma unroll
@@ -667,6 +701,7 @@ bool launch_tc_ffn(const Launch& L, const TcPass& gu, const TcPass& dn, int32_t*
   a.gu_done = gu_done;
   a.gu_tiles = (gu.N + kTcM - 1) / kTcM;
   a.gu_tiles_shared = (gu.Ns + kTcM - 1) / kTcM;
+  a.dn_wide = dn.dn_wide;
   set_smem_attr_once(reinterpret_cast<const void*>(tc_kernel<kTcFfn>), G::kSmemBytes, kAttrTcFfn);
   launch_begin(L, MOE_K_TC_GATE_UP);
   launch_kernel(tc_kernel<kTcFfn>, L.num_sms, kThreads, G::kSmemBytes, L.stream, maps, a);

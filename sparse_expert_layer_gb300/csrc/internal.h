@@ -187,8 +187,11 @@ void launch_perm_scatter(const Launch& L, int T, int k, int E, const int32_t* id
 void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32_t* ids,
                         const int32_t* e2s, const void* x, void* x_perm, float* x_perm_scale,
                         const float* w = nullptr, float* acc = nullptr);
+// dn_ch: output channels of a tensor-core down tile (0: the weight type's own,
+// kTcM for bf16, 2 * kTcM for W8A8).
 void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
-                     const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk);
+                     const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk,
+                     int dn_ch = 0);
 // Small batches (one CTA holds the [expert][token] pick bitmap): count, scan and
 // stable scatter in one launch, plus the work list when wl is not nullptr.
 // Outputs equal those of the count / scan / scatter / work-list launches.
@@ -212,7 +215,7 @@ void launch_sort_small(const Launch& L, const moe_config& c, int T, const int32_
                        int32_t* counts, int32_t* offsets, int32_t* s2e, int32_t* e2s,
                        const WorkList* wl, int gemv_max_rows, int gemv_chunk, int tc_chunk,
                        const SmallGather* gather = nullptr, const SmallRoute* route = nullptr,
-                       const TopkArgs* tk = nullptr);
+                       const TopkArgs* tk = nullptr, int dn_ch = 0);
 
 // Grouped FFN, streaming path (gemv.cu)
 struct GemvPass {
@@ -298,6 +301,7 @@ struct TcPass {
   int b_kmod;              // > 0: activation K coordinate taken modulo b_kmod
   ScatterAdd sc;           // down pass: acc != nullptr adds into the tokens' rows
   SmallFinalize fin;       // down pass of a small layer: the last CTA rounds the output
+  int dn_wide;             // one-launch FFN: a down tile spans 2 x kTcM channels
 };
 bool launch_tc_gate_up(const Launch& L, const TcPass& p);
 bool launch_tc_down(const Launch& L, const TcPass& p);

@@ -455,7 +455,8 @@ __global__ void __launch_bounds__(1024)
 }
 
 WlArgs make_wl_args(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
-                    const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk) {
+                    const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk,
+                    int dn_ch) {
   WlArgs a;
   a.offsets = offsets;
   a.wl = wl;
@@ -476,7 +477,8 @@ WlArgs make_wl_args(const Launch& L, const moe_config& c, int T, const int32_t* 
   const int tch = c.wdtype == MOE_W8A8 ? 2 * kTcM : kTcM;
   a.tiles_gu = (c.inter + tch - 1) / tch;
   a.tiles_gu_shared = (c.shared_inter + tch - 1) / tch;
-  a.tiles_dn = (c.hidden + tch - 1) / tch;
+  const int dch = dn_ch > 0 ? dn_ch : tch;
+  a.tiles_dn = (c.hidden + dch - 1) / dch;
   a.status = L.status;
   return a;
 }
@@ -508,10 +510,11 @@ size_t route_small_smem(const moe_config& c, int T) {
 void launch_sort_small(const Launch& L, const moe_config& c, int T, const int32_t* ids,
                        int32_t* counts, int32_t* offsets, int32_t* s2e, int32_t* e2s,
                        const WorkList* wl, int gemv_max_rows, int gemv_chunk, int tc_chunk,
-                       const SmallGather* gather, const SmallRoute* route, const TopkArgs* tk) {
+                       const SmallGather* gather, const SmallRoute* route, const TopkArgs* tk,
+                       int dn_ch) {
   const int E = c.n_routed + c.n_zero;
   WlArgs a{};
-  if (wl) a = make_wl_args(L, c, T, offsets, *wl, gemv_max_rows, gemv_chunk, tc_chunk);
+  if (wl) a = make_wl_args(L, c, T, offsets, *wl, gemv_max_rows, gemv_chunk, tc_chunk, dn_ch);
   set_smem_attr_once(reinterpret_cast<const void*>(sort_small_kernel), kSortSmallSmem,
                      kAttrSortSmall);
   launch_begin(L, MOE_K_SORT);
@@ -583,8 +586,10 @@ void launch_perm_gather(const Launch& L, const moe_config& c, int T, const int32
 }
 
 void launch_worklist(const Launch& L, const moe_config& c, int T, const int32_t* offsets,
-                     const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk) {
-  const WlArgs a = make_wl_args(L, c, T, offsets, wl, gemv_max_rows, gemv_chunk, tc_chunk);
+                     const WorkList& wl, int gemv_max_rows, int gemv_chunk, int tc_chunk,
+                     int dn_ch) {
+  const WlArgs a =
+      make_wl_args(L, c, T, offsets, wl, gemv_max_rows, gemv_chunk, tc_chunk, dn_ch);
   launch_begin(L, MOE_K_WORKLIST);
   launch_kernel(worklist_kernel, 1, 1024, 0, L.stream, a);
   launch_end(L, MOE_K_WORKLIST);

@@ -1,9 +1,9 @@
 """Offline sweep that writes the grouped FFN's tile-parameter table.
 
 For each layer shape it times moe_layer_forward on a GB300 over the candidate
-tilings (GEMV / tensor-core switch point; one or two persistent launches for
-bf16 layers) and records the fastest in tuning/tile_table.json, together with
-every candidate's time.  The library compiles that table in (build.py) and
+tilings (GEMV / tensor-core switch point; for bf16 layers two persistent
+launches, one, or one with 256-channel down tiles) and records the fastest in
+tuning/tile_table.json, together with every candidate's time.  The library compiles that table in (build.py) and
 looks it up per call (moe_tile_choice): the tiling choice made from measured
 history of the Pangu Pro MoE disclosure, section SwiftGMM.
 
@@ -80,12 +80,13 @@ def main():
         d = dict(x=x.to(dev), w_r=w_r.to(dev), bias=None if bias is None else bias.to(dev),
                  w=synth.draw_weights(spec, device=dev), dev=dev)
         w8 = spec["wdtype"] == "w8a8"
-        launches = [moe.FFN_LAUNCH_DEFAULT] if w8 else [moe.FFN_LAUNCH_TWO, moe.FFN_LAUNCH_ONE]
+        suffix = {moe.FFN_LAUNCH_TWO: "_two", moe.FFN_LAUNCH_ONE: "_one",
+                  moe.FFN_LAUNCH_ONE_WIDE: "_wide"}
+        launches = [moe.FFN_LAUNCH_DEFAULT] if w8 else list(suffix)
         ms = {}
         for gemv in (GEMV_W8 if w8 else GEMV_BF16):
             for launch in launches:
-                key = f"gemv{max(gemv, 0)}" + ("" if w8 else
-                                               ("_one" if launch == moe.FFN_LAUNCH_ONE else "_two"))
+                key = f"gemv{max(gemv, 0)}" + ("" if w8 else suffix[launch])
                 ms[key] = round(time_layer(moe, torch, spec, d, gemv, launch, args.steps,
                                            args.warmup), 5)
                 print(name, key, ms[key], flush=True)
@@ -93,8 +94,9 @@ def main():
         gemv_best = int(best.split("_")[0][4:])
         entries.append({"wdtype": spec["wdtype"], "hidden": spec["hidden"],
                         "inter": spec["inter"], "bucket": load_bucket(spec, buckets),
-                        "gemv_max": gemv_best, "one_launch": int(best.endswith("_one")),
-                        "layer": name, "ms": ms})
+                        "gemv_max": gemv_best,
+                        "one_launch": int(best.endswith("_one") or best.endswith("_wide")),
+                        "dn_wide": int(best.endswith("_wide")), "layer": name, "ms": ms})
         del d
         torch.cuda.empty_cache()
     table["entries"] = entries

@@ -71,9 +71,9 @@ def inputs(spec: dict, device="cuda", weights_on="cpu"):
     return d
 
 
-def run_layer(m, spec, d, out_fp32=True, gemv_max_rows=0, x=None, combine=0):
+def run_layer(m, spec, d, out_fp32=True, gemv_max_rows=0, x=None, combine=0, ffn_launch=0):
     cfg = m.config_from_spec(spec, out_fp32=out_fp32, gemv_max_rows=gemv_max_rows,
-                             combine=combine)
+                             combine=combine, ffn_launch=ffn_launch)
     x = d["x_d"] if x is None else x
     T = x.shape[0]
     out = torch.empty((T, spec["hidden"]), dtype=torch.float32 if out_fp32 else torch.bfloat16,

@@ -76,7 +76,7 @@ def test_workspace_size_for_the_headline_layers(moe):
     ("hidden", 7, 1), ("hidden", 0, 1), ("top_k", 0, 1), ("top_k", 9, 1), ("n_group", 3, 1),
     ("score", 5, 1), ("bias_mode", 3, 1), ("shared_inter", 12, 1), ("inter", 4, 1),
     ("renormalize", 2, 1), ("n_routed", -1, 1), ("combine", 3, 1), ("combine", -1, 1),
-    ("ffn_launch", 3, 1), ("ffn_launch", -1, 1),
+    ("ffn_launch", 4, 1), ("ffn_launch", -1, 1),
 ])
 def test_invalid_configs_are_rejected(moe, field, value, status):
     import synth
@@ -222,13 +222,24 @@ def test_tile_choice_follows_the_table(moe):
             k = int(rng.choice([1, 2, 8]))
             T = int(rng.choice([1, 16, 64, 128, 456, 2048, 8192]))
             s = synth.spec("tiny", hidden=H, inter=I, n_routed=E, top_k=k, wdtype=wdtype)
-            g, one = moe.moe_tile_choice(moe.config_from_spec(s), T)
+            g, one, wide = moe.moe_tile_choice(moe.config_from_spec(s), T)
             want = _table_choice(table, wdtype, H, I, T, k, E)
             assert g == want["gemv_max"], (wdtype, H, I, E, k, T)
             assert one == (wdtype == "bf16" and bool(want["one_launch"])), (wdtype, H, I, E, k, T)
+            assert wide == (one and bool(want.get("dn_wide", 0))), (wdtype, H, I, E, k, T)
     # explicit settings win over the table
     s = synth.spec("longcat")
     assert moe.moe_tile_choice(moe.config_from_spec(s, gemv_max_rows=5), 64)[0] == 5
     assert moe.moe_tile_choice(moe.config_from_spec(s, gemv_max_rows=-1), 64)[0] == 0
     assert moe.moe_tile_choice(moe.config_from_spec(s, ffn_launch=moe.FFN_LAUNCH_TWO), 64)[1] is False
-    assert moe.moe_tile_choice(moe.config_from_spec(s, ffn_launch=moe.FFN_LAUNCH_ONE), 64)[1] is True
+    assert moe.moe_tile_choice(moe.config_from_spec(s, ffn_launch=moe.FFN_LAUNCH_ONE), 64)[1:] \
+        == (True, False)
+    assert moe.moe_tile_choice(moe.config_from_spec(s, ffn_launch=moe.FFN_LAUNCH_ONE_WIDE),
+                               64)[1:] == (True, True)
+    # the table's wide down tiles need one launch; W8A8 layers have neither
+    sp = synth.spec("pangu")
+    assert moe.moe_tile_choice(moe.config_from_spec(sp, ffn_launch=moe.FFN_LAUNCH_TWO),
+                               456)[1:] == (False, False)
+    sw = synth.spec("pangu", wdtype="w8a8")
+    assert moe.moe_tile_choice(moe.config_from_spec(sw, ffn_launch=moe.FFN_LAUNCH_ONE_WIDE),
+                               456)[1:] == (False, False)

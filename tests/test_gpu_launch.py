@@ -107,6 +107,21 @@ def test_unfolded_launches_give_the_same_bits(m, name, tmp_path):
     assert np.array_equal(got, np.load(path))
 
 
+@pytest.mark.parametrize("name", ["tiny", "pangu_s", "dsv3_s", "ragged_s"])
+def test_wide_down_tiles_give_the_same_bits(m, name):
+    # The one-launch FFN's down pass in 256-channel tiles (two weight boxes per
+    # activation box) or in 128-channel ones: each output channel is the same
+    # sequence of MMAs either way, so with the ordered combine the outputs are
+    # identical.  H = 640 and 1000 leave a partial wide tile; pangu_s's shared
+    # expert has row chunks of more than 64 rows.
+    spec = gs.layer_spec(name)
+    d = gs.inputs(spec)
+    ordered = m.COMBINE_ORDERED
+    wide = gs.run_layer(m, spec, d, combine=ordered, ffn_launch=m.FFN_LAUNCH_ONE_WIDE)
+    narrow = gs.run_layer(m, spec, d, combine=ordered, ffn_launch=m.FFN_LAUNCH_ONE)
+    assert torch.equal(wide, narrow)
+
+
 _ROUTE_CC = r"""
 import sys, numpy as np, torch
 sys.path.insert(0, sys.argv[1])
