@@ -19,7 +19,10 @@
 //   warps 2-5 : epilogue -- tcgen05.ld of the accumulators (each warp owns one
 //               32-lane quadrant of TMEM), SwiGLU, coalesced stores.
 // Accumulators are double-buffered in TMEM so the epilogue of one tile overlaps
-// the MMAs of the next.  Every wait is bounded.
+// the MMAs of the next.  Every wait is bounded.  In the single-launch FFN a down
+// tile may span 2 x 128 channels (two weight boxes and two accumulators per K
+// step sharing one activation box, as gate and up do), so loaded experts' h
+// rows are read half as often.
 #include <cudaTypedefs.h>
 
 #include <cstring>
