@@ -279,10 +279,13 @@ __device__ void block_exclusive_scan_n(const int (&v)[N], int (&excl)[N], int (&
 constexpr int kWlScanInts = 32 * 6;  // shared scratch of build_worklist
 
 // Builds the work list from the experts' offsets; called by all threads of a
-// 1024-thread CTA (block-wide scans inside; sh holds kWlScanInts ints).
+// 1024-thread CTA (block-wide scans inside; sh holds kWlScanInts ints).  With
+// at most 32 units, warp 0 builds it alone with warp scans (no block barrier).
 __device__ void build_worklist(const WlArgs& a, const int32_t* offsets, int* sh) {
   int carry[6] = {0, 0, 0, 0, 0, 0};
   const int units = a.E_r + (a.has_shared ? 1 : 0);
+  const bool one_warp = units <= 32;
+  if (one_warp && threadIdx.x >= 32) return;
   for (int base = 0; base < units; base += blockDim.x) {
     const int u = base + threadIdx.x;
     const int e = a.has_shared ? u - 1 : u;  // routed expert of this unit; -1: shared
@@ -304,7 +307,22 @@ __device__ void build_worklist(const WlArgs& a, const int32_t* offsets, int* sh)
     const int v[6] = {n_gemv, n_gemv * gi_gu, n_gemv * a.items_dn, n_tc, n_tc * ti_gu,
                       n_tc * a.tiles_dn};
     int pos[6], tot[6];
-    block_exclusive_scan_n<6>(v, pos, tot, sh);
+    if (one_warp) {
+      const int lane = threadIdx.x;
+#pragma unroll
+      for (int i = 0; i < 6; ++i) {
+        int incl = v[i];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += nb;
+        }
+        pos[i] = incl - v[i];
+        tot[i] = __shfl_sync(0xffffffffu, incl, 31);
+      }
+    } else {
+      block_exclusive_scan_n<6>(v, pos, tot, sh);
+    }
 #pragma unroll
     for (int i = 0; i < 6; ++i) {
       pos[i] += carry[i];
