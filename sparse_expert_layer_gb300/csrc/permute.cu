@@ -415,21 +415,40 @@ __global__ void __launch_bounds__(1024)
     atomicOr(&bm[e * W + t / 32], 1u << (t % 32));
   }
   __syncthreads();
-  // counts, and their exclusive scan, 1024 experts per round
-  int carry = 0;
-  for (int base = 0; base < E; base += blockDim.x) {
-    const int e = base + tid;
-    int c = 0;
-    if (e < E) {
-      for (int w = 0; w < W; ++w) c += __popc(bm[e * W + w]);
-      counts[e] = c;
+  // counts, and their exclusive scan: by warp 0 alone for at most 32 experts,
+  // else 1024 experts per round
+  if (E <= 32) {
+    if (tid < 32) {
+      int c = 0;
+      if (tid < E) {
+        for (int w = 0; w < W; ++w) c += __popc(bm[tid * W + w]);
+        counts[tid] = c;
+      }
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += nb;
+      }
+      if (tid < E) off[tid] = incl - c;
+      if (tid == 31) off[E] = incl;
     }
-    int tot;
-    const int excl = block_exclusive_scan(c, &tot, sh);
-    if (e < E) off[e] = carry + excl;
-    carry += tot;
+  } else {
+    int carry = 0;
+    for (int base = 0; base < E; base += blockDim.x) {
+      const int e = base + tid;
+      int c = 0;
+      if (e < E) {
+        for (int w = 0; w < W; ++w) c += __popc(bm[e * W + w]);
+        counts[e] = c;
+      }
+      int tot;
+      const int excl = block_exclusive_scan(c, &tot, sh);
+      if (e < E) off[e] = carry + excl;
+      carry += tot;
+    }
+    if (tid == 0) off[E] = carry;
   }
-  if (tid == 0) off[E] = carry;
   __syncthreads();
   for (int e = tid; e <= E; e += blockDim.x) offsets[e] = off[e];
   for (int r = tid; r < R; r += blockDim.x) {

@@ -206,38 +206,51 @@ __device__ void topk_token(const TopkArgs& a, int t, const float* row, float* sc
   }
 }
 
-// Shared-memory plan of the one-CTA router: x [T][H] bf16, W_r [E][H] fp32,
-// logits [T][E] fp32, then kSmallRouteWarps top-k scratch rows of 3 * E floats.
+// Shared-memory plan of the one-CTA router: x [T][H] bf16 in rows of
+// small_route_xstride bytes (32 bytes of padding, so the lane groups of a warp,
+// which read neighbouring tokens' rows at the same column, hit different
+// banks), W_r [E][H] fp32, logits [T][E] fp32, then kSmallRouteWarps top-k
+// scratch rows of 3 * E floats.
 struct SmallRoutePlan {
   size_t x, w, logits, scratch, total;
 };
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
+__host__ __device__ inline int small_route_xstride(int H) { return H * 2 + 32; }
 __host__ __device__ inline SmallRoutePlan small_route_plan(int T, int E, int H) {
   SmallRoutePlan p;
   p.x = 0;
-  p.w = align16((size_t)T * H * 2);
+  p.w = align16((size_t)T * small_route_xstride(H));
   p.logits = p.w + align16((size_t)E * H * 4);
   p.scratch = p.logits + align16((size_t)T * E * 4);
   p.total = p.scratch + (size_t)kSmallRouteWarps * 3 * E * 4;
   return p;
 }
 
-// Fills n 16-byte chunks of shared memory at dst with the whole block, four
-// loads in flight per thread: chunk q < n0 from s0[q], the others from
-// s1[q - n0] (two sources, one round of loads).
-__device__ __forceinline__ void copy16_block(uint4* dst, const uint4* s0, int n0,
-                                             const uint4* s1, int n) {
+// Stages x (T rows of H bf16, into rows of small_route_xstride(H) bytes at
+// sm + p.x) and W_r (E rows of H fp32, contiguous at sm + p.w) with the whole
+// block: one round of 16-byte loads, four in flight per thread.
+__device__ __forceinline__ void stage_route_inputs(unsigned char* sm, const SmallRoutePlan& p,
+                                                   const SmallRoute& r, int T, int E) {
+  const int H = r.H, xc = H / 8;  // 16-byte chunks per x row
+  const int n0 = T * xc, n = n0 + E * H / 4;
+  const uint4* x = reinterpret_cast<const uint4*>(r.x);
+  const uint4* w = reinterpret_cast<const uint4*>(r.w_r);
+  const int xs = small_route_xstride(H);
   for (int i = threadIdx.x; i < n; i += 4 * blockDim.x) {
     uint4 v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int q = i + j * blockDim.x;
-      if (q < n) v[j] = __ldg(q < n0 ? s0 + q : s1 + (q - n0));
+      if (q < n) v[j] = __ldg(q < n0 ? x + q : w + (q - n0));
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int q = i + j * blockDim.x;
-      if (q < n) dst[q] = v[j];
+      if (q < n) {
+        unsigned char* d = q < n0 ? sm + p.x + (size_t)(q / xc) * xs + (size_t)(q % xc) * 16
+                                  : sm + p.w + (size_t)(q - n0) * 16;
+        *reinterpret_cast<uint4*>(d) = v[j];
+      }
     }
   }
 }
@@ -258,9 +271,7 @@ __device__ void route_small_block(const SmallRoute& r, const TopkArgs& tk, unsig
   const float* wsm = reinterpret_cast<const float*>(sm + p.w);
   float* lg = reinterpret_cast<float*>(sm + p.logits);
   float* sc = reinterpret_cast<float*>(sm + p.scratch);
-  // x and W_r are adjacent in shared memory (T * H * 2 is a multiple of 16)
-  copy16_block(reinterpret_cast<uint4*>(sm + p.x), reinterpret_cast<const uint4*>(r.x),
-               T * H / 8, reinterpret_cast<const uint4*>(r.w_r), T * H / 8 + E * H / 4);
+  stage_route_inputs(sm, p, r, T, E);
   __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // L lanes per (t, e) pair: the widest power of two (at most 32) that still
@@ -269,12 +280,14 @@ __device__ void route_small_block(const SmallRoute& r, const TopkArgs& tk, unsig
   int L = 32;
   while (L > 1 && (32 / L) * kSmallRouteWarps < P) L >>= 1;
   const int G = 32 / L, grp = lane / L, gl = lane % L;
+  const int xstride = small_route_xstride(H);
   for (int q0 = warp * G; q0 < P; q0 += kSmallRouteWarps * G) {
-    const int q = q0 + grp;
+    const int q = q0 + grp;  // pair (t, e) = (q % T, q / T): a warp's groups share e
     float acc = 0.f;
     if (q < P) {
-      const int t = q / E, e = q % E;
-      const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs + (size_t)t * H);
+      const int t = q % T, e = q / T;
+      const uint32_t* xr = reinterpret_cast<const uint32_t*>(
+          reinterpret_cast<const unsigned char*>(xs) + (size_t)t * xstride);
       const float2* wr = reinterpret_cast<const float2*>(wsm + (size_t)e * H);
       for (int i = gl; i < H / 2; i += L) {
         const uint32_t xv = xr[i];
@@ -284,7 +297,7 @@ __device__ void route_small_block(const SmallRoute& r, const TopkArgs& tk, unsig
       }
     }
     for (int o = L / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (q < P && gl == 0) lg[q] = acc;
+    if (q < P && gl == 0) lg[(size_t)(q % T) * E + q / T] = acc;
   }
   __syncthreads();
   for (int t = warp; t < T; t += kSmallRouteWarps)
