@@ -509,6 +509,7 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   tg.K = tg.Ks = c.hidden;
   tg.N = c.inter;
   tg.Ns = c.shared_inter;
+  tg.task_cap = wl.capacity;
   const bool one_launch = ffn_one_launch(c, T);
   if (c.n_routed > 0 && !one_launch && !launch_tc_gate_up(ln, tg)) return MOE_ERR_CUDA;
 
@@ -553,6 +554,7 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
   td.sc = sc;
   td.fin = fin;
   td.dn_wide = plan.dn_ch > 0;
+  td.task_cap = wl.capacity;
   if (c.n_routed > 0) {
     const bool ok = one_launch ? launch_tc_ffn(ln, tg, td, wl.gu_done) : launch_tc_down(ln, td);
     if (!ok) return MOE_ERR_CUDA;

@@ -107,6 +107,8 @@ struct TcArgs {
   SmallFinalize fin;
   int dn_wide;  // single-launch FFN: down tiles of 2 x kTcM channels (two weight boxes and
                 // two accumulators per K step, one activation box)
+  int task_prefetch;  // work-list entries (< the arrays' capacity, <= kThreads) loaded
+                      // together with the counts
 };
 
 // Small layers: the last CTA of the down pass to finish rounds the tokens'
@@ -163,6 +165,17 @@ __device__ __forceinline__ int interleave_tile(int c, int S, int g, int R, int s
   const int b = c / (g + q), pos = c % (g + q);
   if (b < G) return pos < g ? b * g + pos : S + b * q + (pos - g);
   return S + G * q + (c - G * (g + q));
+}
+
+// Single-launch FFN producer: waits (bounded) until a down tile's task has
+// target gate/up epilogue warps done; on a timeout it reports the status and
+// sets the CTA's abort flag.
+__device__ __forceinline__ bool wait_h_rows(const TcArgs& a, int task, int target, int kind,
+                                            volatile int* abort_flag) {
+  if (wait_rows_done(a.gu_done + task, target)) return true;
+  raise_status(a.status, kStTimeout, kind);
+  *abort_flag = 1;
+  return false;
 }
 
 // tasks and start: the work list in shared memory when it fits, else in global
@@ -231,11 +244,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&maps.b);
     if (MODE == kTcGateUp || MODE == kTcFfn) prefetch_tensormap(&maps.a1);
   }
+  // TMEM touches no global memory either (no kernel of this library that can
+  // share an SM with this one holds TMEM)
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), G::kTmemCols);
   pdl_wait();
+  // the work list's first entries load in the same round as its counts (any
+  // index below the arrays' capacity may be read; those past the count go unused)
+  const bool pf = (int)threadIdx.x < a.task_prefetch;
+  int32_t pf_start = 0, pf_start_dn = 0;
+  FfnTask pf_task{};
+  if (pf) {
+    pf_start = a.tile_start[threadIdx.x];
+    if (FFN) pf_start_dn = a.tile_start_dn[threadIdx.x];
+    pf_task = a.tasks[threadIdx.x];
+  }
   const int ntasks = a.counts[a.task_slot];
   const int ntiles_first = a.counts[a.tile_slot];
   const int ntiles = ntiles_first + (FFN ? a.counts[a.tile_slot_dn] : 0);
   if (ntiles <= 0 || (int)blockIdx.x >= ntiles) {  // uniform across the CTA
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(*tmem_slot, G::kTmemCols);
     if (MODE != kTcGateUp && a.fin.ctr) finalize_if_last(a.fin);
     return;
   }
@@ -247,11 +277,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool cached = ntasks <= kTaskCache;
   if (cached)
     for (int i = threadIdx.x; i < ntasks; i += blockDim.x) {
-      s_start[i] = a.tile_start[i];
-      if (FFN) s_start_dn[i] = a.tile_start_dn[i];
-      s_tasks[i] = a.tasks[i];
+      if (i < a.task_prefetch) {  // i == threadIdx.x: this thread's prefetched entry
+        s_start[i] = pf_start;
+        if (FFN) s_start_dn[i] = pf_start_dn;
+        s_tasks[i] = pf_task;
+      } else {
+        s_start[i] = a.tile_start[i];
+        if (FFN) s_start_dn[i] = a.tile_start_dn[i];
+        s_tasks[i] = a.tasks[i];
+      }
     }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), G::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -316,14 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // weight rows of the tile's first box; the second box (up weights, or a
       // wide down tile's second channel half) starts at a1_row of A1
       int a0_row = t.ct * kTcM, a1_row = t.ct * kTcM;
+      // a down tile's h rows are complete once all its task's gate/up tiles are
+      // stored; its first stage's weight boxes are issued before that wait
+      bool h_wait = false;
+      int h_target = 0;
       if (FFN && !gu) {
-        // the task's h rows are complete once all its gate/up tiles are stored
-        const int target = 4 * (t.shared ? a.gu_tiles_shared : a.gu_tiles);
-        if (!wait_rows_done(a.gu_done + t.task, target)) {
-          raise_status(a.status, kStTimeout, kind);
-          *abort_flag = 1;
-          break;
-        }
+        h_wait = true;
+        h_target = 4 * (t.shared ? a.gu_tiles_shared : a.gu_tiles);
         A0 = t.shared ? &maps.sd0 : &maps.d0;
         B = t.shared ? &maps.sh : &maps.h;
         K = t.shared ? a.Ns : a.N;  // the down pass reduces over the intermediate size
@@ -361,12 +395,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (sub == 2) {
           const int nsub = min(2, nks - ks);
           mbar_arrive_expect_tx(bar, (uint32_t)(nsub * (kATileBytes + kBoxBytes)));
-          for (int u = 0; u < nsub; ++u) {
-            uint8_t* su = st + u * kPackedStep;
-            tma_load_3d(smem_u32(su), A0, (ks + u) * kBK, a0_row, t.e, bar, pol_w);
-            tma_load_3d(smem_u32(su + kATileBytes), B, (ks + u) * kBK, t.row0, 0, bar, pol_x);
-          }
+          for (int u = 0; u < nsub; ++u)
+            tma_load_3d(smem_u32(st + u * kPackedStep), A0, (ks + u) * kBK, a0_row, t.e, bar,
+                        pol_w);
+          if (h_wait && !wait_h_rows(a, t.task, h_target, kind, abort_flag)) ok = false;
+          h_wait = false;
+          // (after a failed wait the boxes still load, so the stage completes)
+          for (int u = 0; u < nsub; ++u)
+            tma_load_3d(smem_u32(st + u * kPackedStep + kATileBytes), B, (ks + u) * kBK, t.row0,
+                        0, bar, pol_x);
           ++iter;
+          if (!ok) break;
           continue;
         }
         if (MODE == kTcRouter) {
@@ -381,11 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (two)
             tma_load_3d(smem_u32(st + kATileBytes), A1, ks * kBK, a1_row, t.e, bar, pol_w);
         }
+        if (h_wait && !wait_h_rows(a, t.task, h_target, kind, abort_flag)) ok = false;
+        h_wait = false;
         uint8_t* sb = st + G::kNA * kATileBytes;
         const int bk = (!t.shared && a.b_kmod > 0) ? (ks * kBK) % a.b_kmod : ks * kBK;
         for (int j = 0; j < nb; ++j)
           tma_load_3d(smem_u32(sb + j * kBoxBytes), B, bk, t.row0 + j * kBoxRows, 0, bar, pol_x);
         ++iter;
+        if (!ok) break;
       }
     }
     const uint32_t first = iter > (uint32_t)G::kStages ? iter - G::kStages : 0u;
@@ -641,6 +683,7 @@ TcArgs make_args(const Launch& L, const TcPass& p) {
   a.status = L.status;
   a.sc = p.sc;
   a.fin = p.fin;
+  a.task_prefetch = p.task_cap < kThreads ? p.task_cap : kThreads;
   return a;
 }
 

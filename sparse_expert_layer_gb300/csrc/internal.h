@@ -302,6 +302,7 @@ struct TcPass {
   ScatterAdd sc;           // down pass: acc != nullptr adds into the tokens' rows
   SmallFinalize fin;       // down pass of a small layer: the last CTA rounds the output
   int dn_wide;             // one-launch FFN: a down tile spans 2 x kTcM channels
+  int task_cap;            // entries the work-list arrays hold (0: unknown)
 };
 bool launch_tc_gate_up(const Launch& L, const TcPass& p);
 bool launch_tc_down(const Launch& L, const TcPass& p);
