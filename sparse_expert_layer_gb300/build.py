@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
 
 SOURCES = ["abi.cu", "route.cu", "permute.cu", "gemv.cu", "gemm_tc.cu", "w8a8.cu", "gemv_i8.cu", "combine.cu",
-           "route_noalloc.cu"]
+           "route_noalloc.cu", "small_ffn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC, "-I", BUILD]

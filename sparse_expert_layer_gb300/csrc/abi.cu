@@ -11,6 +11,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "small_ffn.h"
 
 namespace moe {
 
@@ -198,6 +199,13 @@ bool ffn_dn_wide(const moe_config& c, int T) {
   if (c.ffn_launch != MOE_FFN_LAUNCH_DEFAULT) return c.ffn_launch == MOE_FFN_LAUNCH_ONE_WIDE;
   const TileEntry* e = tile_entry(c, T);
   return e && e->dn_wide != 0;
+}
+
+// Whether the bf16 grouped FFN runs as the small-layer kernel (library defaults
+// only: an explicit GEMV switch point or launch form keeps the other paths).
+bool small_ffn_chosen(const moe_config& c, int T) {
+  return c.gemv_max_rows == 0 && c.ffn_launch == MOE_FFN_LAUNCH_DEFAULT && c.n_routed > 0 &&
+         small_ffn_fits(c, T);
 }
 
 // The GEMV launches are skipped when no unit can take that path.
@@ -459,6 +467,23 @@ moe_status run_ffn(const Launch& ln, const moe_config& c, int T, const Layout& L
                    const SmallFinalize& fin = SmallFinalize{}) {
   const WorkList wl = worklist_view(ws, L);
   const bool shared = c.shared_inter > 0 && sg != nullptr;
+  if (small_ffn_chosen(c, T) && !shared) {
+    // the smallest layers: one CTA per expert, both projections in one launch
+    SmallFfnArgs s{};
+    s.x_perm = static_cast<const uint16_t*>(x_perm);
+    s.offsets = offsets;
+    s.w_gate = static_cast<const uint16_t*>(w_gate);
+    s.w_up = static_cast<const uint16_t*>(w_up);
+    s.w_down = static_cast<const uint16_t*>(w_down);
+    s.sc = sc;
+    s.out_y = y_perm;
+    s.fin = fin;
+    s.H = c.hidden;
+    s.I = c.inter;
+    s.E_r = c.n_routed;
+    s.R = (int64_t)T * c.top_k;
+    return launch_small_ffn(ln, s) ? MOE_OK : MOE_ERR_CUDA;
+  }
   const WlPlan plan = wl_plan(c, T, shared);
   const int gemv_max = plan.gemv_max;
   const int chunk = plan.chunk;

@@ -37,10 +37,23 @@ ONE_CTA = {
 }
 
 
+# Layers small enough for the small-layer FFN kernel (at most 16 tokens, H and I
+# multiples of 64 up to 256, no shared expert, one expert's weights within one
+# CTA's shared memory): every token on every expert (16 rows per expert, both 8-row MMA tiles),
+# and a ragged one (3 tokens, most experts empty, zero-computation experts).
+SMALL_FFN = {
+    "small_ffn_full": dict(T=16, hidden=256, inter=128, n_routed=8, top_k=8, renormalize=True),
+    "small_ffn_ragged": dict(T=3, hidden=192, inter=64, n_routed=16, n_zero=4, top_k=2,
+                             bias_mode="logit", bias_kind="iid", renormalize=False),
+}
+
+
 def layer_spec(name: str) -> dict:
-    """A named layer, or one of the one-CTA routing shapes (built on 'tiny')."""
+    """A named layer, or one of the one-CTA routing or small-FFN shapes (built on 'tiny')."""
     if name in ONE_CTA:
         return synth.spec("tiny", name=name, **ONE_CTA[name])
+    if name in SMALL_FFN:
+        return synth.spec("tiny", name=name, **SMALL_FFN[name])
     return synth.spec(name)
 
 _cache = {}

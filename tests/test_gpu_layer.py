@@ -35,6 +35,24 @@ def test_layer_matches_oracle(m, name, out_fp32, gemv_max_rows):
     gs.check_out(got, ref, bf16_out=not out_fp32, what=f"{name} gemv<={gemv_max_rows}")
 
 
+@pytest.mark.parametrize("name", ["tiny", *gs.SMALL_FFN])
+@pytest.mark.parametrize("out_fp32", [True, False])
+@pytest.mark.parametrize("combine", ["default", "ordered"])
+def test_small_layer_ffn_matches_oracle(m, name, out_fp32, combine):
+    # at most 16 tokens: one CTA per expert runs gate/up and down as warp-level
+    # MMAs out of shared memory (the library default for such layers); an
+    # explicit launch form keeps the persistent tensor-core kernel, which must
+    # agree with the oracle too
+    spec = gs.layer_spec(name)
+    d = gs.inputs(spec)
+    ref = oracle_out(spec, d)
+    mode = m.COMBINE_ORDERED if combine == "ordered" else 0
+    got = gs.run_layer(m, spec, d, out_fp32=out_fp32, combine=mode)
+    gs.check_out(got, ref, bf16_out=not out_fp32, what=f"{name} {combine}")
+    tc = gs.run_layer(m, spec, d, out_fp32=out_fp32, combine=mode, ffn_launch=m.FFN_LAUNCH_ONE)
+    gs.check_out(tc, ref, bf16_out=not out_fp32, what=f"{name} {combine} tensor-core kernel")
+
+
 @pytest.mark.parametrize("name", list(gs.ONE_CTA))
 @pytest.mark.parametrize("combine", ["default", "ordered"])
 def test_layer_routed_by_the_sort_matches_oracle(m, name, combine):
