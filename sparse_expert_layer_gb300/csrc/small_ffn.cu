@@ -1,17 +1,19 @@
 // Grouped SwiGLU FFN of the smallest layers (a few tokens, experts of a few
 // hundred KB): latency, not bandwidth, sets their pace.  The persistent
 // tensor-core kernel spends most of such a layer in its claim / hand-off /
-// fence chain between a gate/up tile and the down tiles of other CTAs; here
-// one CTA takes a whole expert instead:
-//   - its rows and its three weight matrices land in shared memory as a few
-//     TMA boxes of 64 columns (128-byte rows, 128-byte swizzle, so the MMA
-//     fragment loads of eight rows hit different banks);
-//   - eight warps run gate/up as warp-level bf16 MMAs (m16n8k16, fp32
-//     accumulate), one 16-channel tile of both matrices per warp, SwiGLU in
-//     registers, h rounded to bf16 into shared memory (as the tensor-core path
-//     rounds it);
-//   - then the down projection the same way, and w * y added into the tokens'
-//     fp32 accumulators (or the y rows stored for the ordered combine).
+// fence chain between a gate/up tile and the down tiles of other CTAs; here a
+// cluster of kSfCluster CTAs takes a whole expert instead, CTA q a quarter:
+//   - its rows, a quarter of the gate and up rows and a quarter of the down
+//     rows land in shared memory as a few TMA boxes of 64 columns (128-byte
+//     rows, 128-byte swizzle, so the MMA fragment loads of eight rows hit
+//     different banks);
+//   - warps run gate/up as warp-level bf16 MMAs (m16n8k16, fp32 accumulate),
+//     a 16-channel tile of both matrices each, SwiGLU in registers, and write
+//     h, rounded to bf16 as on the tensor-core path, into the shared memory of
+//     every CTA of the cluster;
+//   - after one cluster barrier each CTA runs its quarter of the down
+//     projection over the whole h and adds w * y into the tokens' fp32
+//     accumulators (or stores the y rows for the ordered combine).
 // The products are the grouped FFN of the Pangu Pro MoE disclosure, section
 // SwiftGMM, for experts whose weights stay in L2.
 #include <cudaTypedefs.h>
@@ -31,26 +33,28 @@ namespace {
 constexpr int kSfThreads = 256;  // 8 warps
 constexpr int kSfWarps = kSfThreads / 32;
 constexpr int kSfBoxK = 64;      // columns of a TMA box: one 128-byte row
+constexpr int kSfCluster = 4;    // CTAs per expert (a cluster)
 constexpr int kSfSmemMax = 220 * 1024;
 
 struct SfMaps {
-  CUtensorMap wg, wu;  // [E_r * I rows][H], boxes of 64 columns x I rows
-  CUtensorMap wd;      // [E_r * H rows][I], boxes of 64 columns x H rows
+  CUtensorMap wg, wu;  // [E_r * I rows][H], boxes of 64 columns x I / 4 rows
+  CUtensorMap wd;      // [E_r * H rows][I], boxes of 64 columns x H / 4 rows
   CUtensorMap x;       // [R rows][H], boxes of 64 columns x 16 rows
 };
 
-// Shared-memory plan: gate, up (H / 64 boxes of I rows each), down (I / 64
-// boxes of H rows), x and h (16 rows), every box 1024-byte aligned, then the
-// copy barrier.
+// Shared-memory plan of one CTA: its gate and up rows (H / 64 boxes of I / 4
+// rows each), its down rows (I / 64 boxes of H / 4 rows), x and the whole h
+// (16 rows), every box 1024-byte aligned, then the copy barrier.
 struct SfPlan {
   uint32_t wg, wu, wd, x, h, bar, total;
 };
 __host__ __device__ inline SfPlan sf_plan(int H, int I) {
   SfPlan p;
+  const uint32_t Is = (uint32_t)I / kSfCluster, Hs = (uint32_t)H / kSfCluster;
   p.wg = 0;
-  p.wu = p.wg + (uint32_t)I * H * 2;
-  p.wd = p.wu + (uint32_t)I * H * 2;
-  p.x = p.wd + (uint32_t)H * I * 2;
+  p.wu = p.wg + Is * H * 2;
+  p.wd = p.wu + Is * H * 2;
+  p.x = p.wd + Hs * I * 2;
   p.h = p.x + (uint32_t)kSmallFfnMaxRows * H * 2;
   p.bar = p.h + (uint32_t)kSmallFfnMaxRows * I * 2;
   p.total = p.bar + 16;
@@ -68,6 +72,9 @@ __device__ __forceinline__ uint32_t swz(uint32_t rows, int r, int k) {
 
 __device__ __forceinline__ uint32_t ld_s32(const uint8_t* p) {
   return *reinterpret_cast<const uint32_t*>(p);
+}
+__device__ __forceinline__ void st_cluster_u16(uint32_t cluster_addr, uint16_t v) {
+  asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(cluster_addr), "h"(v) : "memory");
 }
 
 // D (16 x 8, fp32) += A (16 x 16, bf16, row-major) * B (16 x 8, bf16, given as
@@ -105,7 +112,8 @@ __global__ void __launch_bounds__(kSfThreads, 1)
       (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ int last;
   const SfPlan p = sf_plan(a.H, a.I);
-  const int e = blockIdx.x, tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int e = blockIdx.x / kSfCluster, q = (int)cluster_rank();
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int g = lane / 4, t = lane % 4;
   const uint32_t bar = smem_u32(sm + p.bar);
   if (tid == 0) {
@@ -117,93 +125,104 @@ __global__ void __launch_bounds__(kSfThreads, 1)
     prefetch_tensormap(&maps.x);
   }
   __syncthreads();
+  cluster_sync_all();  // every CTA of the cluster runs before any writes into another
   pdl_enter();
-  const int H = a.H, I = a.I;
+  const int H = a.H, I = a.I, Is = I / kSfCluster, Hs = H / kSfCluster;
   const int r0 = a.offsets[e];
-  int n = a.offsets[e + 1] - r0;
-  if (n > kSmallFfnMaxRows) {  // more rows than tokens: bad offsets
+  int n = a.offsets[e + 1] - r0;  // the same in every CTA of the cluster
+  if (n > kSmallFfnMaxRows) {     // more rows than tokens: bad offsets
     if (tid == 0) raise_status(st, kStInternal, MOE_K_TC_GATE_UP);
     n = 0;
   }
-  bool ok = true;
   if (n > 0) {
     if (tid == 0) {
-      // the expert's three matrices and its rows (16 from r0; rows of other
-      // experts or past the end only feed output columns that are not kept)
-      mbar_arrive_expect_tx(bar, (uint32_t)(6 * I * H + 2 * kSmallFfnMaxRows * H));
+      // this CTA's gate, up and down rows and the expert's rows (16 from r0;
+      // rows of other experts or past the end only feed output columns that
+      // are not kept)
+      mbar_arrive_expect_tx(bar, (uint32_t)(4 * Is * H + 2 * Hs * I + 2 * kSmallFfnMaxRows * H));
       const uint64_t pol = policy_evict_last();
       for (int b = 0; b < H / kSfBoxK; ++b) {
-        tma_load_2d(smem_u32(sm + p.wg + b * I * 128), &maps.wg, b * kSfBoxK, e * I, bar, pol);
-        tma_load_2d(smem_u32(sm + p.wu + b * I * 128), &maps.wu, b * kSfBoxK, e * I, bar, pol);
+        tma_load_2d(smem_u32(sm + p.wg + b * Is * 128), &maps.wg, b * kSfBoxK, e * I + q * Is,
+                    bar, pol);
+        tma_load_2d(smem_u32(sm + p.wu + b * Is * 128), &maps.wu, b * kSfBoxK, e * I + q * Is,
+                    bar, pol);
         tma_load_2d(smem_u32(sm + p.x + b * kSmallFfnMaxRows * 128), &maps.x, b * kSfBoxK, r0,
                     bar, pol);
       }
       for (int b = 0; b < I / kSfBoxK; ++b)
-        tma_load_2d(smem_u32(sm + p.wd + b * H * 128), &maps.wd, b * kSfBoxK, e * H, bar, pol);
+        tma_load_2d(smem_u32(sm + p.wd + b * Hs * 128), &maps.wd, b * kSfBoxK, e * H + q * Hs,
+                    bar, pol);
     }
-    ok = __syncthreads_and(mbar_wait(bar, 0));
+    const bool ok = __syncthreads_and(mbar_wait(bar, 0));
     if (!ok) {
-      // report, and give the copies in flight one more bounded wait before
-      // the CTA moves on
+      // report, and give the copies in flight one more bounded wait
       if (tid == 0) raise_status(st, kStTimeout, MOE_K_TC_GATE_UP);
       mbar_wait(bar, 0);
     }
-  }
-  if (n > 0 && ok) {
     const int ntn = n > 8 ? 2 : 1;  // 8-row MMA column tiles with rows
-    // gate/up: warp w takes channel tiles w, w + 8, ...
-    for (int m = warp; m < I / 16; m += kSfWarps) {
-      float cg[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float cu[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      for (int k0 = 0; k0 < H; k0 += 16) {
-        uint32_t ag[4], au[4];
-        load_a(sm + p.wg, I, m * 16, k0, g, t, ag);
-        load_a(sm + p.wu, I, m * 16, k0, g, t, au);
-        for (int nt = 0; nt < ntn; ++nt) {
-          uint32_t b[2];
-          load_b(sm + p.x, kSmallFfnMaxRows, nt * 8, k0, g, t, b);
-          mma_bf16_16816(cg[nt], ag, b);
-          mma_bf16_16816(cu[nt], au, b);
-        }
-      }
-      // element j of a tile: channel m * 16 + g (+ 8 for j >= 2), row 2t (+ 1 for odd j)
-      for (int nt = 0; nt < ntn; ++nt)
+    if (ok) {
+      // gate/up: warp w takes this CTA's channel tile w (of Is / 16), and
+      // writes h into the same place in every CTA of the cluster
+      uint32_t hbase[kSfCluster];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int ch = m * 16 + g + (j >= 2 ? 8 : 0), r = nt * 8 + 2 * t + (j & 1);
-          const float gv = cg[nt][j];
-          const float h = gv * __frcp_rn(1.f + __expf(-gv)) * cu[nt][j];
-          *reinterpret_cast<uint16_t*>(sm + p.h + swz(kSmallFfnMaxRows, r, ch)) = f_to_bf16(h);
-        }
-    }
-    __syncthreads();
-    // down: warp w takes output-channel tiles w, w + 8, ...
-    const bool fused = a.sc.acc != nullptr;
-    for (int m = warp; m < H / 16; m += kSfWarps) {
-      float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      for (int k0 = 0; k0 < I; k0 += 16) {
-        uint32_t ad[4];
-        load_a(sm + p.wd, H, m * 16, k0, g, t, ad);
-        for (int nt = 0; nt < ntn; ++nt) {
-          uint32_t b[2];
-          load_b(sm + p.h, kSmallFfnMaxRows, nt * 8, k0, g, t, b);
-          mma_bf16_16816(c[nt], ad, b);
-        }
-      }
-      for (int nt = 0; nt < ntn; ++nt)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int ch = m * 16 + g + (j >= 2 ? 8 : 0), r = nt * 8 + 2 * t + (j & 1);
-          if (r >= n) continue;
-          if (fused) {
-            int tk;
-            float wt;
-            scatter_target(a.sc, r0 + r, false, &tk, &wt);
-            atomicAdd(a.sc.acc + (size_t)tk * H + ch, wt * c[nt][j]);
-          } else {
-            a.out_y[(size_t)(r0 + r) * H + ch] = c[nt][j];
+      for (int j = 0; j < kSfCluster; ++j) hbase[j] = mapa_shared(smem_u32(sm + p.h), (uint32_t)j);
+      for (int m = warp; m < Is / 16; m += kSfWarps) {
+        float cg[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float cu[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int k0 = 0; k0 < H; k0 += 16) {
+          uint32_t ag[4], au[4];
+          load_a(sm + p.wg, Is, m * 16, k0, g, t, ag);
+          load_a(sm + p.wu, Is, m * 16, k0, g, t, au);
+          for (int nt = 0; nt < ntn; ++nt) {
+            uint32_t b[2];
+            load_b(sm + p.x, kSmallFfnMaxRows, nt * 8, k0, g, t, b);
+            mma_bf16_16816(cg[nt], ag, b);
+            mma_bf16_16816(cu[nt], au, b);
           }
         }
+        // element j of a tile: channel m * 16 + g (+ 8 for j >= 2), row 2t (+ 1 for odd j)
+        for (int nt = 0; nt < ntn; ++nt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int ch = q * Is + m * 16 + g + (j >= 2 ? 8 : 0), r = nt * 8 + 2 * t + (j & 1);
+            const float gv = cg[nt][j];
+            const uint16_t h = f_to_bf16(gv * __frcp_rn(1.f + __expf(-gv)) * cu[nt][j]);
+            const uint32_t off = swz(kSmallFfnMaxRows, r, ch);
+#pragma unroll
+            for (int c = 0; c < kSfCluster; ++c) st_cluster_u16(hbase[c] + off, h);
+          }
+      }
+    }
+    cluster_sync_all();  // h complete in every CTA (reached by every CTA of the cluster)
+    if (ok) {
+      // down: warp w takes this CTA's output-channel tile w (of Hs / 16)
+      const bool fused = a.sc.acc != nullptr;
+      for (int m = warp; m < Hs / 16; m += kSfWarps) {
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int k0 = 0; k0 < I; k0 += 16) {
+          uint32_t ad[4];
+          load_a(sm + p.wd, Hs, m * 16, k0, g, t, ad);
+          for (int nt = 0; nt < ntn; ++nt) {
+            uint32_t b[2];
+            load_b(sm + p.h, kSmallFfnMaxRows, nt * 8, k0, g, t, b);
+            mma_bf16_16816(c[nt], ad, b);
+          }
+        }
+        for (int nt = 0; nt < ntn; ++nt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int ch = q * Hs + m * 16 + g + (j >= 2 ? 8 : 0), r = nt * 8 + 2 * t + (j & 1);
+            if (r >= n) continue;
+            if (fused) {
+              int tk;
+              float wt;
+              scatter_target(a.sc, r0 + r, false, &tk, &wt);
+              atomicAdd(a.sc.acc + (size_t)tk * H + ch, wt * c[nt][j]);
+            } else {
+              a.out_y[(size_t)(r0 + r) * H + ch] = c[nt][j];
+            }
+          }
+      }
     }
   }
   if (!a.fin.ctr) return;
@@ -273,9 +292,9 @@ bool launch_small_ffn(const Launch& L, const SmallFfnArgs& a) {
   SfMaps maps;
   memset(&maps, 0, sizeof maps);
   const uint64_t er = (uint64_t)a.E_r;
-  if (!sf_map(&maps.wg, a.w_gate, a.H, er * a.I, a.I) ||
-      !sf_map(&maps.wu, a.w_up, a.H, er * a.I, a.I) ||
-      !sf_map(&maps.wd, a.w_down, a.I, er * a.H, a.H) ||
+  if (!sf_map(&maps.wg, a.w_gate, a.H, er * a.I, a.I / kSfCluster) ||
+      !sf_map(&maps.wu, a.w_up, a.H, er * a.I, a.I / kSfCluster) ||
+      !sf_map(&maps.wd, a.w_down, a.I, er * a.H, a.H / kSfCluster) ||
       !sf_map(&maps.x, a.x_perm, a.H, a.R, kSmallFfnMaxRows))
     return false;
   const uint32_t smem = sf_plan(a.H, a.I).total + 1024;
@@ -289,7 +308,8 @@ bool launch_small_ffn(const Launch& L, const SmallFfnArgs& a) {
       g_sf_attr[dev].store(1, std::memory_order_release);
   }
   launch_begin(L, MOE_K_TC_GATE_UP);
-  launch_kernel(small_ffn_kernel, a.E_r, kSfThreads, smem, L.stream, maps, a, L.status);
+  launch_kernel_cluster(small_ffn_kernel, dim3(a.E_r * kSfCluster), dim3(kSfCluster), kSfThreads,
+                        smem, L.stream, maps, a, L.status);
   launch_end(L, MOE_K_TC_GATE_UP);
   return true;
 }

@@ -12,12 +12,13 @@ namespace moe {
 constexpr int kSmallFfnMaxRows = 16;
 bool small_ffn_fits(const moe_config& c, int T);
 
-// One CTA per routed expert: its rows x_perm[offsets[e] .. offsets[e + 1]) and
-// its weights staged in shared memory by TMA, gate/up and down as
-// warp-level bf16 MMAs (h kept in shared memory, rounded to bf16 as on the
-// tensor-core path), then w * y added into the tokens' fp32 accumulators
-// (sc.acc set) or the y rows written to out_y [R, H].  With fin.ctr set the
-// last CTA rounds the accumulators to bf16.
+// A cluster of four CTAs per routed expert: its rows x_perm[offsets[e] ..
+// offsets[e + 1]) and a quarter of its weights in each CTA's shared memory by
+// TMA, gate/up and down as warp-level bf16 MMAs (h exchanged through the
+// cluster's shared memory, rounded to bf16 as on the tensor-core path), then
+// w * y added into the tokens' fp32 accumulators (sc.acc set) or the y rows
+// written to out_y [R, H].  With fin.ctr set the last CTA rounds the
+// accumulators to bf16.
 struct SmallFfnArgs {
   const uint16_t* x_perm;   // bf16 [R, H], rows sorted by expert
   const int32_t* offsets;   // [E + 1]
