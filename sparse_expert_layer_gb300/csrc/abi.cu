@@ -1019,7 +1019,10 @@ moe_status moe_layer_forward(const moe_config* cfg, int32_t T, const void* x,
     }
   }
   // the FFN's work list is built with the re-sort when that runs as one CTA
-  const bool ffn = w8 ? c.n_routed > 0 : (c.n_routed > 0 || c.shared_inter > 0);
+  // (the small-layer FFN reads only the offsets)
+  const bool ffn = w8 ? c.n_routed > 0
+                      : ((c.n_routed > 0 || c.shared_inter > 0) &&
+                         !(c.shared_inter == 0 && small_ffn_chosen(c, T)));
   const WlPlan plan = wl_plan(c, T, !w8 && c.shared_inter > 0);
   const bool wl_built =
       run_permute(ln, c, T, L, ws, ids, x, counts, offsets, s2e, e2s, x_perm, x_scale,
