@@ -45,6 +45,8 @@ SMALL_FFN = {
     "small_ffn_full": dict(T=16, hidden=256, inter=128, n_routed=8, top_k=8, renormalize=True),
     "small_ffn_ragged": dict(T=3, hidden=192, inter=64, n_routed=16, n_zero=4, top_k=2,
                              bias_mode="logit", bias_kind="iid", renormalize=False),
+    # the smallest dimensions (one 16-channel tile per CTA in both passes), one token
+    "small_ffn_min": dict(T=1, hidden=64, inter=64, n_routed=4, top_k=2, renormalize=True),
 }
 
 
