@@ -280,7 +280,10 @@ bool sf_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint
 }  // namespace
 
 bool small_ffn_fits(const moe_config& c, int T) {
-  if (c.wdtype != MOE_W_BF16 || c.shared_inter > 0 || c.n_routed < 1) return false;
+  // (a cluster per routed expert, empty or not: at most kSmallFfnMaxExperts)
+  if (c.wdtype != MOE_W_BF16 || c.shared_inter > 0 || c.n_routed < 1 ||
+      c.n_routed > kSmallFfnMaxExperts)
+    return false;
   if (T < 1 || T > kSmallFfnMaxRows) return false;
   // whole 64-column boxes, at most 256 rows a box
   if (c.hidden % kSfBoxK != 0 || c.inter % kSfBoxK != 0 || c.hidden > 256 || c.inter > 256)

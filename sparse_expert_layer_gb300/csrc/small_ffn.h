@@ -6,10 +6,12 @@
 namespace moe {
 
 // Whether (c, T) takes the small-layer FFN: bf16 weights, no shared expert, at
-// most kSmallFfnMaxRows tokens (so at most that many rows per expert), H and I
-// multiples of 64 and at most 256, and one expert's three weight matrices plus
-// its rows fit one CTA's shared memory.
+// most kSmallFfnMaxRows tokens (so at most that many rows per expert) and
+// kSmallFfnMaxExperts routed experts, H and I multiples of 64 and at most 256,
+// and a quarter of one expert's weights plus its rows fit one CTA's shared
+// memory.
 constexpr int kSmallFfnMaxRows = 16;
+constexpr int kSmallFfnMaxExperts = 64;
 bool small_ffn_fits(const moe_config& c, int T);
 
 // A cluster of four CTAs per routed expert: its rows x_perm[offsets[e] ..
