@@ -116,6 +116,46 @@ __device__ void topk_token(const TopkArgs& a, int t, const float* row, float* sc
   for (int e = lane; e < E; e += 32) sel[e] = sc[e] + sel[e];
   __syncwarp();
 
+  int my_id = 0;
+  float my_w = 0.f;
+  if (a.n_group > 1 && a.per_group_k == 1 && a.n_group <= 32) {
+    // one winner per group (MoGE, k = n_group): the picks are the group
+    // winners in key order.  Lane g finds group g's winner (the first of its
+    // largest keys, as the stage below), then a bitonic sort across the warp
+    // orders the winners by key, ties to the lower index: the picks of the
+    // rounds below, in 15 exchange steps instead of k arg-max rounds.
+    const int G = E / a.n_group;
+    float v = -INFINITY;
+    int bi = 0x7fffffff;
+    if (lane < a.n_group) {
+      int best = -1;
+      for (int e = lane * G; e < (lane + 1) * G; ++e)
+        if (sel[e] != -INFINITY && (best < 0 || sel[e] > sel[best])) best = e;
+      if (best >= 0 && sel[best] > -INFINITY) {  // (a NaN key is never picked below either)
+        v = sel[best];
+        bi = best;
+      }
+    }
+    for (int size = 2; size <= 32; size <<= 1)
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, stride);
+        const bool mine_better = v > ov || (v == ov && bi < oi);
+        const bool keep_better = ((lane & stride) == 0) == ((lane & size) == 0);
+        if (mine_better != keep_better) {
+          v = ov;
+          bi = oi;
+        }
+      }
+    if (lane < a.k) {  // lane j holds the j-th pick
+      if (bi == 0x7fffffff) {  // fewer eligible experts than k (non-finite keys)
+        raise_status(a.status, kStInternal, MOE_K_TOPK);
+        bi = 0;
+      }
+      my_id = bi;
+      my_w = sc[bi];
+    }
+  } else {
   // group stage
   if (a.n_group > 1) {
     const int G = E / a.n_group;
@@ -174,8 +214,6 @@ __device__ void topk_token(const TopkArgs& a, int t, const float* row, float* sc
   }
 
   // top-k in descending key order, ties to the lower index
-  int my_id = 0;
-  float my_w = 0.f;
   for (int j = 0; j < a.k; ++j) {
     float v = -INFINITY;
     int bi = 0x7fffffff;
@@ -196,6 +234,7 @@ __device__ void topk_token(const TopkArgs& a, int t, const float* row, float* sc
     __syncwarp();
     if (lane == 0) sel[bi] = -INFINITY;
     __syncwarp();
+  }
   }
   float wsum = warp_sum(lane < a.k ? my_w : 0.f);
   if (lane < a.k) {
